@@ -1,0 +1,282 @@
+"""Plain CPU fp64 oracle of the tensor-parallel MLP block and its sequence-parallel variant.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference arm of ``bench.py`` may import this module.  The
+CUDA library never calls it, shares no code with it, and the product path
+fails rather than fall back to it.
+
+Everything is float64 numpy; the matrix product is ``numpy.matmul`` and the
+error function is ``scipy.special.erf`` (library primitives); there is no
+blocking, fusion or reordering beyond what the definitions state.  Inputs are
+the exact bf16 (or fp32) values the GPU consumes, widened to float64; no
+intermediate is rounded.
+
+Sources (pages by title, then section):
+
+* [6D] "Megatron 架构与 6D 并行完整指南" (walkerchi.com), §3.1 "原理": the MLP
+  is ``Y = GeLU(X·A)·B`` with ``A ∈ R^{d×4d}``, ``B ∈ R^{4d×d}``; with TP=2
+  ``A0 = A[:, :2d]``, ``A1 = A[:, 2d:]``, ``B0 = B[:2d, :]``, ``B1 = B[2d:, :]``;
+  each shard computes ``Y_i = GeLU(X·A_i)·B_i`` and an AllReduce gives
+  ``Y = Y_0 + Y_1``; GeLU is elementwise so the column split commutes with it.
+* [DEEP] "Megatron-LM 심층 아키텍처: 3D 하이브리드 병렬화(TP·SP·PP)…"
+  (techknowgenie.com):
+  - section "열 병렬(Column Parallel)과 행 병렬(Row Parallel)의 결합":
+    ``Z = GeLU(X W1)``, ``Output = Z W2 = Σ_i Z_i W2_i = Σ_i Y_i``, W1 split
+    into N column blocks, W2 into N row blocks;
+  - section "All-Reduce 통신의 All-Gather 및 Reduce-Scatter 분해":
+    ``AllReduce(X) = AllGather(ReduceScatter(X))``; LayerNorm runs on the
+    S/N sequence slice, an All-Gather restores the full sequence before the
+    GEMMs and a Reduce-Scatter after them sums the partials and splits the
+    result by sequence;
+  - section "분산 제어 소스코드 구조 패턴" (listing of ColumnParallelLinear,
+    RowParallelLinear, SequenceParallelLayerNorm): the column layer adds a
+    bias of ``out_features // world`` entries, ``split = out // world`` sizes
+    the shards, the norm uses fp32 statistics and ``eps = 1e-5`` on a
+    ``[S/N, batch, hidden]`` slice.
+* [GLOSS] "Megatron-LM" glossary (jisaku.com), tensor-parallel table and the
+  sequence-parallel paragraph: FFN layer 1 column-parallel, GeLU per GPU,
+  layer 2 row-parallel with an AllReduce in forward; two AllReduces per
+  block in backward; SP splits LayerNorm/Dropout along the sequence and
+  replaces the AllReduce by ReduceScatter + AllGather.
+
+Readings where the pages are silent or disagree (each is listed with its
+reason in the design notes):
+
+* GeLU is the exact ``0.5·x·(1 + erf(x/√2))`` ("GeLU" is all the pages say).
+* ``bias`` is the column layer's bias, one entry per FFN column, split with
+  A's columns; the row layer's bias is not part of this block.
+* The sequence-parallel norm is a standard LayerNorm (the text says
+  LayerNorm; the listing computes an RMS norm): biased variance (divide by
+  d), ``eps`` inside the square root, scale ``gamma`` and shift ``beta``.
+* Chunk ``j`` of the sequence is the contiguous row range
+  ``[j·T/N, (j+1)·T/N)`` (tokens are sequence-major, ``[S/N, batch, hidden]``).
+* The backward pass is not written on the pages; it is the chain rule of
+  the forward definitions (``GeLU'(x) = Φ(x) + x·φ(x)``), with the backward
+  AllReduce of the MLP summing the shards' input gradients, and in the SP
+  block the mirror collectives: AllGather of dY, ReduceScatter of the input
+  gradient.  dgamma and dbeta sum over all chunks.
+* Non-divisible sizes (``F % N``, ``T % N``) are rejected, not truncated.
+
+Every function is pinned by tests in ``tests/test_oracle_pins.py`` (values
+printed on the pages, closed forms, invariants, brute force, library
+witnesses and finite differences); none is parity-unpinned.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import erf as _erf
+
+SQRT_HALF = 1.0 / math.sqrt(2.0)
+INV_SQRT_2PI = 1.0 / math.sqrt(2.0 * math.pi)
+
+
+# --------------------------------------------------------------------------- partition
+
+def shard_ranges(F: int, N: int) -> list[tuple[int, int]]:
+    """Column shard ``i`` of A (row shard ``i`` of B): ``[i·F/N, (i+1)·F/N)``.
+
+    [6D] §3.1 (TP=2: ``A[:, :2d]``, ``A[:, 2d:]``); [DEEP] listing
+    (``split_out_features = out_features // world``).  Rejects ``F % N != 0``.
+    """
+    if N <= 0 or F <= 0 or F % N:
+        raise ValueError(f"F={F} is not split evenly into N={N} shards")
+    w = F // N
+    return [(i * w, (i + 1) * w) for i in range(N)]
+
+
+def chunk_ranges(T: int, N: int) -> list[tuple[int, int]]:
+    """Sequence chunk ``j``: rows ``[j·T/N, (j+1)·T/N)`` ([DEEP] SP section: S/N per GPU)."""
+    if N <= 0 or T <= 0 or T % N:
+        raise ValueError(f"T={T} is not split evenly into N={N} chunks")
+    w = T // N
+    return [(j * w, (j + 1) * w) for j in range(N)]
+
+
+# --------------------------------------------------------------------------- elementwise
+
+def gelu(x):
+    """Exact GeLU: ``x·Φ(x) = 0.5·x·(1 + erf(x/√2))``."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + _erf(x * SQRT_HALF))
+
+
+def gelu_prime(x):
+    """Derivative of the exact GeLU: ``Φ(x) + x·φ(x)``."""
+    x = np.asarray(x, dtype=np.float64)
+    cdf = 0.5 * (1.0 + _erf(x * SQRT_HALF))
+    pdf = INV_SQRT_2PI * np.exp(-0.5 * x * x)
+    return cdf + x * pdf
+
+
+# --------------------------------------------------------------------------- collectives (on explicit per-shard buffers)
+
+def all_reduce(parts):
+    """Sum of the shards' partial outputs, shard 0 first ([DEEP] eq. ``Output = Σ_i Y_i``)."""
+    total = np.zeros_like(np.asarray(parts[0], dtype=np.float64))
+    for p in parts:
+        total = total + p
+    return total
+
+
+def reduce_scatter(parts, N: int):
+    """Sum the partials, then split the rows into N sequence chunks ([DEEP] SP section)."""
+    total = all_reduce(parts)
+    return [total[lo:hi] for lo, hi in chunk_ranges(total.shape[0], N)]
+
+
+def all_gather(chunks):
+    """Concatenate sequence chunks back into the full sequence ([DEEP] SP section)."""
+    return np.concatenate([np.asarray(c, dtype=np.float64) for c in chunks], axis=0)
+
+
+# --------------------------------------------------------------------------- forward
+
+def _bias_or_zero(b, F):
+    return np.zeros(F, dtype=np.float64) if b is None else np.asarray(b, dtype=np.float64)
+
+
+def mlp_reference(X, A, B, b=None):
+    """Unsharded block: ``Y = GeLU(X·A + b)·B`` ([6D] §3.1 ``Y = GeLU(X·A)·B``; bias of the column layer)."""
+    X = np.asarray(X, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    Z = gelu(X @ A + _bias_or_zero(b, A.shape[1]))
+    return Z @ B
+
+
+def column_parallel(X, A_i, b_i):
+    """Shard i of the first layer: ``Z_i = GeLU(X·A_i + b_i)`` (no communication)."""
+    return gelu(np.asarray(X, dtype=np.float64) @ np.asarray(A_i, dtype=np.float64) + b_i)
+
+
+def row_parallel_partial(Z_i, B_i):
+    """Shard i of the second layer: the partial ``Y_i = Z_i·B_i``."""
+    return Z_i @ np.asarray(B_i, dtype=np.float64)
+
+
+def mlp_partials(X, A, B, b, N: int):
+    """The N partial outputs ``Y_i = GeLU(X·A_i + b_i)·B_i``, one per shard."""
+    F = np.asarray(A).shape[1]
+    bias = _bias_or_zero(b, F)
+    parts = []
+    for lo, hi in shard_ranges(F, N):
+        Z_i = column_parallel(X, np.asarray(A)[:, lo:hi], bias[lo:hi])
+        parts.append(row_parallel_partial(Z_i, np.asarray(B)[lo:hi, :]))
+    return parts
+
+
+def mlp_tp(X, A, B, b, N: int):
+    """Tensor-parallel block: AllReduce of the shard partials."""
+    return all_reduce(mlp_partials(X, A, B, b, N))
+
+
+def layer_norm(x, gamma, beta, eps: float = 1e-5):
+    """LayerNorm of each row: ``(x - mean)/sqrt(var + eps)·gamma + beta``, biased variance."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * np.asarray(gamma, dtype=np.float64) + np.asarray(beta, dtype=np.float64)
+
+
+def sp_forward(X_chunks, gamma, beta, eps, A, B, b, N: int, return_intermediates: bool = False):
+    """Sequence-parallel block forward.
+
+    LayerNorm on each S/N chunk, AllGather, the N shard partials, then
+    ReduceScatter back to chunks ([DEEP] SP section).
+    """
+    if len(X_chunks) != N:
+        raise ValueError("one input chunk per shard")
+    normed = [layer_norm(c, gamma, beta, eps) for c in X_chunks]
+    Xg = all_gather(normed)
+    parts = mlp_partials(Xg, A, B, b, N)
+    Y_chunks = reduce_scatter(parts, N)
+    if return_intermediates:
+        return Y_chunks, {"Xg": Xg, "partials": parts}
+    return Y_chunks
+
+
+# --------------------------------------------------------------------------- backward (chain rule)
+
+def mlp_backward(X, A, B, b, dY):
+    """Gradients of ``Y = GeLU(X·A + b)·B`` (unsharded).
+
+    ``Hpre = X·A + b``, ``H = GeLU(Hpre)``, ``dH = dY·Bᵀ``,
+    ``dHpre = dH ⊙ GeLU'(Hpre)``, ``dB = Hᵀ·dY``, ``dA = Xᵀ·dHpre``,
+    ``db = Σ_rows dHpre``, ``dX = dHpre·Aᵀ``.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    Hpre = X @ A + _bias_or_zero(b, A.shape[1])
+    H = gelu(Hpre)
+    dH = dY @ B.T
+    dHpre = dH * gelu_prime(Hpre)
+    return {"dX": dHpre @ A.T, "dA": X.T @ dHpre, "dB": H.T @ dY, "db": dHpre.sum(axis=0),
+            "Hpre": Hpre, "H": H, "dHpre": dHpre}
+
+
+def mlp_backward_tp(X, A, B, b, dY, N: int):
+    """Per-shard gradients; the input gradient is the AllReduce of the shards' ``dX_i``.
+
+    Shard i owns ``A_i``, ``B_i``, ``b_i`` and so ``dA_i``, ``dB_i``, ``db_i``
+    (concatenated here); ``dX_i = dHpre_i·A_iᵀ`` is a partial that the
+    backward AllReduce sums ([GLOSS] tensor-parallel section: two AllReduces
+    per block in backward).
+    """
+    F = np.asarray(A).shape[1]
+    bias = _bias_or_zero(b, F)
+    dA = np.zeros(np.asarray(A).shape)
+    dB = np.zeros(np.asarray(B).shape)
+    db = np.zeros(F)
+    dX_parts = []
+    for lo, hi in shard_ranges(F, N):
+        g = mlp_backward(X, np.asarray(A)[:, lo:hi], np.asarray(B)[lo:hi, :], bias[lo:hi], dY)
+        dA[:, lo:hi] = g["dA"]
+        dB[lo:hi, :] = g["dB"]
+        db[lo:hi] = g["db"]
+        dX_parts.append(g["dX"])
+    return {"dX": all_reduce(dX_parts), "dX_parts": dX_parts, "dA": dA, "dB": dB, "db": db}
+
+
+def layer_norm_backward(x, gamma, eps, dy):
+    """Gradients of :func:`layer_norm` for one chunk of rows.
+
+    With ``x̂ = (x - mean)·rstd`` and ``g = dy·gamma``:
+    ``dx = rstd·(g - mean(g) - x̂·mean(g·x̂))``, ``dgamma = Σ_rows dy·x̂``,
+    ``dbeta = Σ_rows dy``.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    rstd = 1.0 / np.sqrt(var + eps)
+    xhat = (x - mu) * rstd
+    g = dy * np.asarray(gamma, dtype=np.float64)
+    dx = rstd * (g - g.mean(axis=-1, keepdims=True) - xhat * (g * xhat).mean(axis=-1, keepdims=True))
+    return dx, (dy * xhat).sum(axis=0), dy.sum(axis=0)
+
+
+def sp_backward(X_chunks, gamma, beta, eps, A, B, b, dY_chunks, N: int):
+    """Sequence-parallel block backward: the mirror of :func:`sp_forward`.
+
+    AllGather of the output-gradient chunks (mirror of the forward
+    ReduceScatter), per-shard MLP gradients, ReduceScatter of the shards'
+    input-gradient partials (mirror of the forward AllGather), then the
+    LayerNorm backward on each chunk.
+    """
+    normed = [layer_norm(c, gamma, beta, eps) for c in X_chunks]
+    Xg = all_gather(normed)
+    dYg = all_gather(dY_chunks)
+    g = mlp_backward_tp(Xg, A, B, b, dYg, N)
+    dXg_chunks = reduce_scatter(g["dX_parts"], N)
+    dX_chunks, dgamma, dbeta = [], 0.0, 0.0
+    for xc, dyc in zip(X_chunks, dXg_chunks):
+        dx, dga, dbe = layer_norm_backward(xc, gamma, eps, dyc)
+        dX_chunks.append(dx)
+        dgamma = dgamma + dga
+        dbeta = dbeta + dbe
+    return {"dX_chunks": dX_chunks, "dA": g["dA"], "dB": g["dB"], "db": g["db"],
+            "dgamma": dgamma, "dbeta": dbeta, "dXg_chunks": dXg_chunks}

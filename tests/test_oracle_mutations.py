@@ -1,0 +1,123 @@
+"""Planted mistakes: each plausible slip in the oracle must make at least one pin fail.
+
+Every case swaps one oracle function for a subtly wrong copy (on the CPU,
+for the duration of the test) and runs a pin from ``test_oracle_pins``;
+the pin has to raise.  This guards against pins that would pass whatever
+the oracle computes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+_orig = {name: getattr(oracle, name) for name in dir(oracle) if not name.startswith("__")}
+
+
+def _gelu_tanh(x):
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1 + np.tanh(np.sqrt(2 / np.pi) * (x + 0.044715 * x ** 3)))
+
+
+def _gelu_prime_no_pdf(x):
+    return 0.5 * (1.0 + oracle._erf(np.asarray(x, dtype=np.float64) * oracle.SQRT_HALF))
+
+
+def _mlp_reference_no_bias(X, A, B, b=None):
+    return _orig["mlp_reference"](X, A, B, None)
+
+
+def _shard_ranges_overlap(F, N):
+    r = _orig["shard_ranges"](F, N)
+    return [(max(lo - 1, 0), hi) for lo, hi in r]
+
+
+def _layer_norm_unbiased(x, gamma, beta, eps=1e-5):
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = x.var(axis=-1, ddof=1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * gamma + beta
+
+
+def _layer_norm_eps_outside(x, gamma, beta, eps=1e-5):
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / (np.sqrt(var) + eps) * gamma + beta
+
+
+def _reduce_scatter_reversed(parts, N):
+    return _orig["reduce_scatter"](parts, N)[::-1]
+
+
+def _mlp_partials_transposed_shard(X, A, B, b, N):
+    # uses the *last* shard's rows of B for every shard (a wrong index)
+    F = np.asarray(A).shape[1]
+    bias = oracle._bias_or_zero(b, F)
+    r = oracle.shard_ranges(F, N)
+    lo_last, hi_last = r[-1]
+    return [oracle.row_parallel_partial(oracle.column_parallel(X, np.asarray(A)[:, lo:hi], bias[lo:hi]),
+                                        np.asarray(B)[lo_last:hi_last, :]) for lo, hi in r]
+
+
+def _mlp_backward_dA_uses_dH(X, A, B, b, dY):
+    g = _orig["mlp_backward"](X, A, B, b, dY)
+    dH = np.asarray(dY, dtype=np.float64) @ np.asarray(B, dtype=np.float64).T
+    g["dA"] = np.asarray(X, dtype=np.float64).T @ dH          # dropped GeLU' factor
+    return g
+
+
+def _mlp_backward_sign(X, A, B, b, dY):
+    g = _orig["mlp_backward"](X, A, B, b, dY)
+    g["dX"] = -g["dX"]
+    return g
+
+
+def _ln_backward_no_mean_g(x, gamma, eps, dy):
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    rstd = 1.0 / np.sqrt(var + eps)
+    xhat = (x - mu) * rstd
+    g = dy * gamma
+    dx = rstd * (g - xhat * (g * xhat).mean(axis=-1, keepdims=True))
+    return dx, (dy * xhat).sum(axis=0), dy.sum(axis=0)
+
+
+def _sp_backward_last_chunk_dgamma(*args, **kw):
+    out = _orig["sp_backward"](*args, **kw)
+    out["dgamma"] = out["dgamma"] / len(out["dX_chunks"])
+    return out
+
+
+CASES = [
+    ("gelu", _gelu_tanh, lambda: pins.test_gelu_textbook_values()),
+    ("gelu", _gelu_tanh, lambda: pins.test_mlp_bruteforce_d8(3, 2)),
+    ("gelu_prime", _gelu_prime_no_pdf, lambda: pins.test_gelu_prime_finite_difference()),
+    ("gelu_prime", _gelu_prime_no_pdf, lambda: pins.test_backward_autograd_witness(2)),
+    ("mlp_reference", _mlp_reference_no_bias, lambda: pins.test_mlp_torch_witness()),
+    ("shard_ranges", _shard_ranges_overlap, lambda: pins.test_shard_ranges_partition_exactly(32)),
+    ("shard_ranges", _shard_ranges_overlap, lambda: pins.test_tp2_split_matches_pages()),
+    ("layer_norm", _layer_norm_unbiased, lambda: pins.test_layer_norm_identities()),
+    ("layer_norm", _layer_norm_eps_outside, lambda: pins.test_layer_norm_torch_witness()),
+    ("reduce_scatter", _reduce_scatter_reversed, lambda: pins.test_reduce_scatter_chunks_are_row_ranges()),
+    ("reduce_scatter", _reduce_scatter_reversed, lambda: pins.test_sp_forward_equals_layernorm_then_mlp(4)),
+    ("mlp_partials", _mlp_partials_transposed_shard, lambda: pins.test_shard_sum_equals_unsharded(4)),
+    ("mlp_backward", _mlp_backward_dA_uses_dH, lambda: pins.test_backward_finite_difference_d8()),
+    ("mlp_backward", _mlp_backward_sign, lambda: pins.test_backward_autograd_witness(1)),
+    ("layer_norm_backward", _ln_backward_no_mean_g, lambda: pins.test_layer_norm_backward_autograd_and_fd()),
+    ("sp_backward", _sp_backward_last_chunk_dgamma, lambda: pins.test_sp_backward_autograd_witness(4)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)), ids=[f"{c[0]}-{i}" for i, c in enumerate(CASES)])
+def test_planted_mistake_is_caught(case, monkeypatch):
+    name, bad, pin = CASES[case]
+    monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises((AssertionError, ValueError)):
+        pin()
+
+
+def test_unmutated_pins_pass():
+    for _, _, pin in CASES:
+        pin()

@@ -1,0 +1,342 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each test checks an oracle function against one of: values the pages print
+(golden files), closed forms and textbook constants, identities stated on the
+pages, brute force with pure-Python loops on tiny inputs, library witnesses
+(torch fp64 on the CPU: ``gelu(approximate='none')``, ``layer_norm``,
+autograd) and finite differences.  Sizes keep the whole module to seconds.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import read_golden
+from tensor_transformer_mlp_tp_gb300 import inputs
+
+RNG = np.random.default_rng(1234)
+
+
+def rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+# --------------------------------------------------------------------------- partition
+
+def test_tp2_split_matches_pages():
+    for d, F, shard, lo, hi in (map(int, r) for r in read_golden("tp2_split.txt")):
+        assert F == 4 * d
+        assert oracle.shard_ranges(F, 2)[shard] == (lo, hi)
+
+
+@pytest.mark.parametrize("F", [4, 8, 12, 32, 48, 64, 96, 256, 4096, 16384, 32768])
+def test_shard_ranges_partition_exactly(F):
+    for N in range(1, 17):
+        if F % N:
+            with pytest.raises(ValueError):
+                oracle.shard_ranges(F, N)
+            continue
+        r = oracle.shard_ranges(F, N)
+        assert len(r) == N
+        covered = np.zeros(F, dtype=np.int64)
+        for lo, hi in r:
+            assert hi - lo == F // N
+            covered[lo:hi] += 1
+        assert np.all(covered == 1)                      # disjoint and complete, bit-exact
+        assert r[0][0] == 0 and r[-1][1] == F
+        assert all(r[i][1] == r[i + 1][0] for i in range(N - 1))
+
+
+def test_chunk_ranges_partition_rows():
+    for T, N in [(8192, 8), (4096, 8), (24, 3), (7, 7)]:
+        r = oracle.chunk_ranges(T, N)
+        assert [hi - lo for lo, hi in r] == [T // N] * N
+        assert r[0][0] == 0 and r[-1][1] == T
+    with pytest.raises(ValueError):
+        oracle.chunk_ranges(10, 4)
+
+
+# --------------------------------------------------------------------------- GeLU
+
+def test_gelu_textbook_values():
+    for x, Phi, phi in (map(float, r) for r in read_golden("normal_cdf.txt")):
+        assert oracle.gelu(x) == pytest.approx(x * Phi, abs=2e-15)
+        assert oracle.gelu_prime(x) == pytest.approx(Phi + x * phi, abs=2e-15)
+
+
+def test_gelu_closed_forms():
+    x = np.linspace(-8, 8, 2001)
+    g = oracle.gelu(x)
+    assert oracle.gelu(0.0) == 0.0
+    np.testing.assert_allclose(g - oracle.gelu(-x), x, rtol=0, atol=1e-14)   # x·Φ(x) - (-x)·Φ(-x) = x
+    big = np.array([10.0, 20.0, 40.0])
+    np.testing.assert_allclose(oracle.gelu(big), big, rtol=1e-15)
+    np.testing.assert_allclose(oracle.gelu(-big), 0.0, atol=1e-20)
+    assert oracle.gelu_prime(0.0) == 0.5
+
+
+def test_gelu_matches_math_erf_bruteforce():
+    xs = RNG.normal(0, 3, 500)
+    ref = [0.5 * v * (1 + math.erf(v / math.sqrt(2))) for v in xs]
+    np.testing.assert_allclose(oracle.gelu(xs), ref, rtol=1e-15, atol=1e-15)
+
+
+def test_gelu_torch_witness():
+    xs = RNG.normal(0, 3, 4096)
+    ref = torch.nn.functional.gelu(torch.from_numpy(xs), approximate="none").numpy()
+    np.testing.assert_allclose(oracle.gelu(xs), ref, rtol=1e-14, atol=1e-15)  # 1+erf cancels in the left tail
+
+
+def test_gelu_prime_finite_difference():
+    xs = np.linspace(-6, 6, 241)
+    h = 1e-5
+    fd = (oracle.gelu(xs + h) - oracle.gelu(xs - h)) / (2 * h)
+    np.testing.assert_allclose(oracle.gelu_prime(xs), fd, rtol=0, atol=1e-9)
+
+
+# --------------------------------------------------------------------------- forward
+
+def _rand_block(T, d, F, bias=True):
+    X = RNG.normal(0, 1, (T, d))
+    A = RNG.normal(0, 0.3, (d, F))
+    B = RNG.normal(0, 0.3, (F, d))
+    b = RNG.normal(0, 0.3, F) if bias else None
+    return X, A, B, b
+
+
+def test_worked_example_d1():
+    g = {k: float(v) for k, v in read_golden("worked_mlp_d1.txt")}
+    X = np.array([[1.0]])
+    A = np.array([[1.0, -1.0, 2.0, 0.0]])
+    B = np.ones((4, 1))
+    parts = oracle.mlp_partials(X, A, B, None, 2)
+    assert parts[0][0, 0] == pytest.approx(g["Y0"], abs=2e-15)
+    assert parts[1][0, 0] == pytest.approx(g["Y1"], abs=2e-15)
+    assert oracle.mlp_tp(X, A, B, None, 2)[0, 0] == pytest.approx(g["Y"], abs=4e-15)
+    assert oracle.mlp_reference(X, A, B)[0, 0] == pytest.approx(g["Y"], abs=4e-15)
+
+
+def _bruteforce_mlp(X, A, B, b):
+    T, d = len(X), len(X[0])
+    F = len(A[0])
+    Y = [[0.0] * d for _ in range(T)]
+    for t in range(T):
+        z = []
+        for f in range(F):
+            s = 0.0 if b is None else b[f]
+            for k in range(d):
+                s += X[t][k] * A[k][f]
+            z.append(0.5 * s * (1.0 + math.erf(s / math.sqrt(2.0))))
+        for j in range(d):
+            acc = 0.0
+            for f in range(F):
+                acc += z[f] * B[f][j]
+            Y[t][j] = acc
+    return np.array(Y)
+
+
+@pytest.mark.parametrize("T", [1, 3, 16])
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_mlp_bruteforce_d8(T, N):
+    X, A, B, b = _rand_block(T, 8, 32)
+    ref = _bruteforce_mlp(X.tolist(), A.tolist(), B.tolist(), b.tolist())
+    assert rel(oracle.mlp_tp(X, A, B, b, N), ref) < 1e-13
+    assert rel(oracle.mlp_reference(X, A, B, b), ref) < 1e-13
+
+
+def test_mlp_torch_witness():
+    X, A, B, b = _rand_block(37, 24, 96)
+    t = lambda a: torch.from_numpy(a)
+    ref = torch.nn.functional.linear(
+        torch.nn.functional.gelu(torch.nn.functional.linear(t(X), t(A).T, t(b)), approximate="none"),
+        t(B).T).numpy()
+    assert rel(oracle.mlp_reference(X, A, B, b), ref) < 1e-13
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 6, 8, 12, 16, 24, 48])
+def test_shard_sum_equals_unsharded(N):
+    """Output = Z·W2 = Σ_i Z_i·W2_i (column-parallel / row-parallel section of the deep-dive page)."""
+    X, A, B, b = _rand_block(19, 16, 48)
+    assert rel(oracle.mlp_tp(X, A, B, b, N), oracle.mlp_reference(X, A, B, b)) < 1e-12
+
+
+def test_n1_is_textbook_mlp():
+    X, A, B, b = _rand_block(5, 8, 32)
+    parts = oracle.mlp_partials(X, A, B, b, 1)
+    assert len(parts) == 1
+    assert rel(parts[0], oracle.mlp_reference(X, A, B, b)) < 1e-15
+
+
+def test_partials_are_the_column_row_blocks():
+    """Shard i of the partials uses exactly A[:, s_i], b[s_i] and B[s_i, :]."""
+    X, A, B, b = _rand_block(4, 8, 32)
+    parts = oracle.mlp_partials(X, A, B, b, 4)
+    for i, (lo, hi) in enumerate(oracle.shard_ranges(32, 4)):
+        ref = _bruteforce_mlp(X.tolist(), A[:, lo:hi].tolist(), B[lo:hi].tolist(), b[lo:hi].tolist())
+        assert rel(parts[i], ref) < 1e-13
+
+
+# --------------------------------------------------------------------------- collectives
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_allreduce_is_allgather_of_reducescatter_integers(N):
+    """AllReduce(X) = AllGather(ReduceScatter(X)), bit-exact on integer-valued partials."""
+    T, d = 16 * N, 24
+    parts = [RNG.integers(-3, 4, (T, d)).astype(np.float64) for _ in range(N)]
+    ar = oracle.all_reduce(parts)
+    ag = oracle.all_gather(oracle.reduce_scatter(parts, N))
+    assert np.array_equal(ar, ag)
+    assert np.array_equal(ar, np.sum(np.stack(parts), axis=0))   # integers: order-free
+
+
+def test_reduce_scatter_chunks_are_row_ranges():
+    N, T, d = 4, 12, 5
+    parts = [RNG.normal(size=(T, d)) for _ in range(N)]
+    chunks = oracle.reduce_scatter(parts, N)
+    total = sum(parts[i] for i in range(N))
+    for j, (lo, hi) in enumerate(oracle.chunk_ranges(T, N)):
+        np.testing.assert_allclose(chunks[j], total[lo:hi], rtol=1e-15, atol=0)
+
+
+# --------------------------------------------------------------------------- LayerNorm
+
+def test_layer_norm_identities():
+    x = RNG.normal(2.0, 3.0, (64, 128))
+    y = oracle.layer_norm(x, np.ones(128), np.zeros(128), 1e-5)
+    np.testing.assert_allclose(y.mean(axis=1), 0.0, atol=1e-13)
+    var = x.var(axis=1)                                       # numpy var is the biased (1/d) variance
+    np.testing.assert_allclose(y.var(axis=1), var / (var + 1e-5), rtol=1e-12)
+    # affine invariance: LN(a·x + c) = LN(x) for a > 0, up to the eps term
+    y2 = oracle.layer_norm(7.0 * x - 3.0, np.ones(128), np.zeros(128), 0.0)
+    y3 = oracle.layer_norm(x, np.ones(128), np.zeros(128), 0.0)
+    np.testing.assert_allclose(y2, y3, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_norm_torch_witness():
+    x = RNG.normal(0, 1, (33, 96))
+    g = 1 + 0.1 * RNG.normal(size=96)
+    bt = 0.1 * RNG.normal(size=96)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (96,), torch.from_numpy(g),
+                                         torch.from_numpy(bt), eps=1e-5).numpy()
+    np.testing.assert_allclose(oracle.layer_norm(x, g, bt, 1e-5), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_layer_norm_single_row_bruteforce():
+    x = [3.0, -1.0, 0.5, 2.5]
+    mu = sum(x) / 4
+    var = sum((v - mu) ** 2 for v in x) / 4
+    ref = [(v - mu) / math.sqrt(var + 1e-5) * 2.0 + 0.25 for v in x]
+    np.testing.assert_allclose(oracle.layer_norm(np.array([x]), 2.0 * np.ones(4), 0.25 * np.ones(4))[0], ref,
+                               rtol=1e-15)
+
+
+# --------------------------------------------------------------------------- SP forward
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_sp_forward_equals_layernorm_then_mlp(N):
+    T, d, F = 8 * N, 16, 64
+    X = RNG.normal(size=(T, d))
+    g = 1 + 0.1 * RNG.normal(size=d)
+    bt = 0.1 * RNG.normal(size=d)
+    _, A, B, b = _rand_block(1, d, F)
+    chunks = [X[lo:hi] for lo, hi in oracle.chunk_ranges(T, N)]
+    Yc = oracle.sp_forward(chunks, g, bt, 1e-5, A, B, b, N)
+    ref = oracle.mlp_reference(oracle.layer_norm(X, g, bt, 1e-5), A, B, b)
+    assert len(Yc) == N and all(c.shape == (T // N, d) for c in Yc)
+    assert rel(np.concatenate(Yc), ref) < 1e-12
+
+
+# --------------------------------------------------------------------------- backward
+
+def _torch_block_grads(X, A, B, b, dY):
+    t = [torch.tensor(v, dtype=torch.float64, requires_grad=True) for v in (X, A, B, b)]
+    Y = torch.nn.functional.gelu(t[0] @ t[1] + t[3], approximate="none") @ t[2]
+    Y.backward(torch.from_numpy(dY))
+    return [v.grad.numpy() for v in t]
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_backward_autograd_witness(N):
+    X, A, B, b = _rand_block(11, 12, 48)
+    dY = RNG.normal(size=(11, 12))
+    gX, gA, gB, gb = _torch_block_grads(X, A, B, b, dY)
+    g = oracle.mlp_backward_tp(X, A, B, b, dY, N)
+    for mine, ref in [(g["dX"], gX), (g["dA"], gA), (g["dB"], gB), (g["db"], gb)]:
+        assert rel(mine, ref) < 1e-12
+    g1 = oracle.mlp_backward(X, A, B, b, dY)
+    for k in ("dX", "dA", "dB", "db"):
+        assert rel(g1[k], g[k]) < 1e-12
+
+
+def test_backward_finite_difference_d8():
+    X, A, B, b = _rand_block(3, 8, 32)
+    dY = RNG.normal(size=(3, 8))
+    g = oracle.mlp_backward(X, A, B, b, dY)
+    loss = lambda X_, A_, B_, b_: float(np.sum(oracle.mlp_reference(X_, A_, B_, b_) * dY))
+    h = 1e-6
+    for name, arr, idx in [("dX", X, (1, 3)), ("dA", A, (2, 17)), ("dB", B, (30, 5)), ("db", b, (9,))]:
+        args = {"dX": [X, A, B, b], "dA": [X, A, B, b], "dB": [X, A, B, b], "db": [X, A, B, b]}[name]
+        pos = {"dX": 0, "dA": 1, "dB": 2, "db": 3}[name]
+        plus = [a.copy() for a in args]
+        minus = [a.copy() for a in args]
+        plus[pos][idx] += h
+        minus[pos][idx] -= h
+        fd = (loss(*plus) - loss(*minus)) / (2 * h)
+        assert g[name][idx] == pytest.approx(fd, rel=1e-7, abs=1e-9)
+
+
+def test_layer_norm_backward_autograd_and_fd():
+    x = RNG.normal(0.5, 2.0, (7, 24))
+    gam = 1 + 0.2 * RNG.normal(size=24)
+    bet = 0.2 * RNG.normal(size=24)
+    dy = RNG.normal(size=(7, 24))
+    tx = torch.tensor(x, requires_grad=True)
+    tg = torch.tensor(gam, requires_grad=True)
+    tb = torch.tensor(bet, requires_grad=True)
+    torch.nn.functional.layer_norm(tx, (24,), tg, tb, eps=1e-5).backward(torch.from_numpy(dy))
+    dx, dga, dbe = oracle.layer_norm_backward(x, gam, 1e-5, dy)
+    assert rel(dx, tx.grad.numpy()) < 1e-12
+    assert rel(dga, tg.grad.numpy()) < 1e-12
+    assert rel(dbe, tb.grad.numpy()) < 1e-12
+    h = 1e-6
+    xp, xm = x.copy(), x.copy()
+    xp[2, 5] += h
+    xm[2, 5] -= h
+    f = lambda v: float(np.sum(oracle.layer_norm(v, gam, bet, 1e-5) * dy))
+    assert dx[2, 5] == pytest.approx((f(xp) - f(xm)) / (2 * h), rel=1e-7, abs=1e-9)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_sp_backward_autograd_witness(N):
+    T, d, F = 4 * N, 8, 32
+    X = RNG.normal(size=(T, d))
+    gam = 1 + 0.1 * RNG.normal(size=d)
+    bet = 0.1 * RNG.normal(size=d)
+    _, A, B, b = _rand_block(1, d, F)
+    dY = RNG.normal(size=(T, d))
+    tt = [torch.tensor(v, requires_grad=True) for v in (X, gam, bet, A, B, b)]
+    xn = torch.nn.functional.layer_norm(tt[0], (d,), tt[1], tt[2], eps=1e-5)
+    Y = torch.nn.functional.gelu(xn @ tt[3] + tt[5], approximate="none") @ tt[4]
+    Y.backward(torch.from_numpy(dY))
+    cr = oracle.chunk_ranges(T, N)
+    g = oracle.sp_backward([X[lo:hi] for lo, hi in cr], gam, bet, 1e-5, A, B, b,
+                           [dY[lo:hi] for lo, hi in cr], N)
+    assert rel(np.concatenate(g["dX_chunks"]), tt[0].grad.numpy()) < 1e-12
+    assert rel(g["dgamma"], tt[1].grad.numpy()) < 1e-12
+    assert rel(g["dbeta"], tt[2].grad.numpy()) < 1e-12
+    assert rel(g["dA"], tt[3].grad.numpy()) < 1e-12
+    assert rel(g["dB"], tt[4].grad.numpy()) < 1e-12
+    assert rel(g["db"], tt[5].grad.numpy()) < 1e-12
+
+
+# --------------------------------------------------------------------------- inputs feed the oracle exactly
+
+def test_bf16_inputs_are_exact_in_fp64():
+    w = inputs.small_workload(64, 32, 4)
+    bits, vals = inputs.draw(w, "X")
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(vals, ref)
