@@ -1,0 +1,242 @@
+/*
+ * tpmlp.h -- C ABI of the GB300 tensor-parallel MLP block (libtpmlp.so).
+ *
+ * The block is the Megatron MLP  Y = GeLU(X A + b) B  with A in R^{d x 4d}
+ * split into N column shards and B in R^{4d x d} split into N row shards:
+ * shard i computes Y_i = GeLU(X A_i + b_i) B_i and an AllReduce sums the
+ * partials, Y = sum_i Y_i.  Sources: "Megatron 架构与 6D 并行完整指南"
+ * (walkerchi.com) §3.1 "原理"; "Megatron-LM 심층 아키텍처" (techknowgenie.com),
+ * section "열 병렬(Column Parallel)과 행 병렬(Row Parallel)의 결합" and the
+ * ColumnParallelLinear / RowParallelLinear listing in "분산 제어 소스코드 구조 패턴".
+ * All N shards run on one GPU: the column shards are column ranges of one
+ * launch, and the AllReduce is the K loop of the row-parallel GEMM, which
+ * accumulates every shard's rows of B into one fp32 accumulator before a
+ * single store.
+ *
+ * Conventions for every call:
+ *  - Matrices are row-major.  bf16 is IEEE bfloat16; accumulation is fp32.
+ *    X [T x d], A [d x F], B [F x d], bias [F], Y [T x d], with T = tokens,
+ *    F = ffn (4d in the pages' model, any multiple of N here).
+ *  - Shard i owns FFN columns [i F/N, (i+1) F/N) of A and bias and the same
+ *    rows of B; sequence chunk j owns token rows [j T/N, (j+1) T/N).
+ *  - Device pointers are owned by the caller and must stay valid until the
+ *    work queued on `stream` has finished.  Arrays of chunk pointers
+ *    (`X_chunks`, `Y_chunks`, ...) are HOST arrays of N device pointers, read
+ *    during the call only.  The library allocates no device memory per call:
+ *    scratch comes from the caller's workspace (size: tpmlp_workspace_size).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and never synchronise the host, except
+ *    tpmlp_get_device_status.
+ *  - Argument errors are returned before anything is launched: NULL where a
+ *    pointer is required, tokens < 0, d or ffn < 1, N outside [1, 64],
+ *    ffn % N != 0, and for bf16: d % 8 != 0, (ffn / N) % 8 != 0, a device
+ *    pointer not 16-byte aligned; for the sequence-parallel calls T % N != 0;
+ *    a workspace smaller than required (TPMLP_ERR_WORKSPACE).  tokens == 0 is
+ *    a valid empty call that launches nothing.
+ *  - A failed launch returns TPMLP_ERR_CUDA.  Kernels never trap: every wait
+ *    inside them is bounded (default 1 s, environment TPMLP_WAIT_TIMEOUT_MS);
+ *    a wait that runs out records a device error word and the kernel exits,
+ *    reported later by tpmlp_get_device_status as TPMLP_ERR_TIMEOUT.
+ *  - Thread-compatible: concurrent calls from several host threads are safe;
+ *    the only shared state is the per-device error word and cached device
+ *    attributes.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TPMLP_API __attribute__((visibility("default")))
+#else
+#define TPMLP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tpmlp_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  TPMLP_OK = 0,
+  TPMLP_ERR_INVALID_ARG = 1,
+  TPMLP_ERR_UNSUPPORTED = 2,
+  TPMLP_ERR_CUDA = 3,
+  TPMLP_ERR_TIMEOUT = 4,
+  TPMLP_ERR_WORKSPACE = 5
+} tpmlp_status;
+
+typedef enum { TPMLP_BF16 = 0, TPMLP_FP32 = 1 } tpmlp_dtype;
+
+/* Problem shape.  ffn is the FFN width F (4d on the pages); n_shards is N,
+ * the tensor-parallel degree and, for the sequence-parallel calls, the number
+ * of sequence chunks.  dtype is a tpmlp_dtype. */
+typedef struct {
+  int64_t tokens;
+  int64_t d;
+  int64_t ffn;
+  int32_t n_shards;
+  int32_t dtype;
+} tpmlp_shape;
+
+/* Operations whose workspace size can be queried. */
+enum {
+  TPMLP_OP_FWD = 0,            /* tpmlp_forward */
+  TPMLP_OP_SP_FWD = 1,         /* tpmlp_sp_forward, TPMLP_RS_FUSED */
+  TPMLP_OP_SP_FWD_PARTIALS = 2,/* tpmlp_sp_forward, TPMLP_RS_PARTIALS */
+  TPMLP_OP_BWD = 3,            /* tpmlp_backward */
+  TPMLP_OP_SP_BWD = 4,         /* tpmlp_sp_backward */
+  TPMLP_OP_DH_GELUPRIME = 5,   /* tpmlp_gemm_dh_geluprime with a dbias output */
+  TPMLP_OP_LN_BWD = 6          /* tpmlp_layernorm_backward */
+};
+
+/* Reduce-scatter modes of tpmlp_sp_forward. */
+enum {
+  TPMLP_RS_FUSED = 0,    /* the row-parallel GEMM stores each output row into its chunk */
+  TPMLP_RS_PARTIALS = 1  /* per-shard bf16 partials, then tpmlp_reduce_scatter; needs (ffn/N) % 64 == 0 */
+};
+
+/* Human-readable name of a status code (static string). */
+TPMLP_API const char* tpmlp_status_string(tpmlp_status s);
+
+/* Bytes of workspace `op` needs for `shape` (host arithmetic only, no CUDA
+ * call).  The workspace is any 256-byte aligned device buffer of at least that
+ * size; its contents need no initialisation and are clobbered. */
+TPMLP_API tpmlp_status tpmlp_workspace_size(const tpmlp_shape* shape, int op, size_t* bytes);
+
+/* Synchronise `stream`, then read and clear the current device's error word.
+ * Returns TPMLP_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
+ * call (and writes the failing wait site to *site when site != NULL),
+ * TPMLP_ERR_CUDA if the stream reports a CUDA error, else TPMLP_OK. */
+TPMLP_API tpmlp_status tpmlp_get_device_status(tpmlp_stream_t stream, uint32_t* site);
+
+/* ------------------------------------------------------------------ block calls */
+
+/* Tensor-parallel MLP forward ("6D" guide §3.1; deep-dive page, column/row
+ * parallel section, eq. Output = Z W2 = sum_i Z_i W2_i).
+ *   X [T x d], A [d x F], B [F x d], bias [F] or NULL (the column layer's
+ *   bias, split with A's columns), Y [T x d] out.
+ *   Hpre_out: NULL, or [T x F] receiving the pre-activation X A + b (bf16)
+ *   for a later tpmlp_backward.
+ * bf16: tcgen05 GEMM with bias + exact erf-GeLU in the epilogue into H
+ * (workspace), then the row-parallel GEMM summing all N shards in TMEM.
+ * fp32 (shape->dtype == TPMLP_FP32): all pointers are fp32, CUDA-core FFMA;
+ * Hpre_out must be NULL. */
+TPMLP_API tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
+                           void* Y, void* Hpre_out, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Sequence-parallel block forward (deep-dive page, section "All-Reduce 통신의
+ * All-Gather 및 Reduce-Scatter 분해"; SequenceParallelLayerNorm in the listing):
+ * LayerNorm of every S/N chunk (fp32 statistics, biased variance, eps inside
+ * the square root, scale gamma and shift beta), All-Gather of the chunks,
+ * the MLP, Reduce-Scatter of the shard partials back to chunks.
+ *   X_chunks: host array of N pointers, each [T/N x d]; gamma, beta [d];
+ *   Y_chunks: host array of N pointers, each [T/N x d] out; rs_mode:
+ *   TPMLP_RS_FUSED or TPMLP_RS_PARTIALS; Hpre_out: NULL or [T x F].
+ * bf16 only. */
+TPMLP_API tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                              const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
+                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* workspace,
+                              size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* MLP backward, the chain rule of the forward (the pages name two backward
+ * AllReduces per block, glossary page, tensor-parallel section):
+ *   Hpre = X A + b (the given Hpre, or recomputed when Hpre == NULL),
+ *   dHpre = (dY B^T) * GeLU'(Hpre), dB = GeLU(Hpre)^T dY, dA = X^T dHpre,
+ *   dbias = column sums of dHpre (if dbias != NULL), and
+ *   dX = sum_i dHpre_i A_i^T  (the backward AllReduce, as one K loop).
+ * Outputs dX [T x d], dA [d x F], dB [F x d], dbias [F] are bf16.  bf16 only. */
+TPMLP_API tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* bias, const void* Hpre,
+                            const void* dY, const tpmlp_shape* shape, void* dX, void* dA, void* dB, void* dbias,
+                            void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Sequence-parallel block backward: All-Gather of the dY chunks (the mirror
+ * of the forward Reduce-Scatter), the MLP backward on the re-normalised
+ * gathered input, Reduce-Scatter of the input gradient to chunks (the mirror
+ * of the forward All-Gather), LayerNorm backward per chunk.
+ *   dX_chunks: host array of N pointers [T/N x d] (bf16) out;
+ *   dgamma, dbeta: [d] fp32 out, summed over all chunks; dA, dB, dbias as in
+ *   tpmlp_backward.  bf16 only. */
+TPMLP_API tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                               const void* A, const void* B, const void* bias, const void* Hpre,
+                               const void* const* dY_chunks, const tpmlp_shape* shape, void* const* dX_chunks,
+                               void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
+                               size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* ------------------------------------------------------------------ single steps (bf16)
+ * Each step is one kernel launch (plus a small fixed-order reduction where
+ * noted); the block calls above are sequences of these.  They take explicit
+ * buffers instead of a workspace. */
+
+/* Column-parallel GEMM of all N shards with bias + exact GeLU fused:
+ * H = GeLU(X A + b), optionally Hpre = X A + b.  X [T x d], A [d x F],
+ * bias [F] or NULL, H [T x F], Hpre [T x F] or NULL. */
+TPMLP_API tpmlp_status tpmlp_gemm1_bias_gelu(const void* X, const void* A, const void* bias, const tpmlp_shape* shape,
+                                   void* H, void* Hpre, tpmlp_stream_t stream);
+
+/* Row-parallel GEMM with the in-kernel shard reduction: Y = sum_i H_i B_i.
+ * H [T x F], B [F x d].  Y_chunks == NULL: Y [T x d].  Y_chunks != NULL
+ * (host array of N pointers, T % N == 0): row r is stored to chunk r / (T/N),
+ * the Reduce-Scatter fused into the store; Y is then ignored. */
+TPMLP_API tpmlp_status tpmlp_gemm2_shard_accum(const void* H, const void* B, const tpmlp_shape* shape, void* Y,
+                                     void* const* Y_chunks, tpmlp_stream_t stream);
+
+/* Per-shard partial outputs of the row-parallel layer, P_i = H_i B_i, as the
+ * pages' ranks produce them before their collective.  P [N x T x d] bf16;
+ * requires (ffn / N) % 64 == 0. */
+TPMLP_API tpmlp_status tpmlp_gemm2_partials(const void* H, const void* B, const tpmlp_shape* shape, void* P,
+                                  tpmlp_stream_t stream);
+
+/* Reduce-Scatter of explicit partials: Y_chunk_j = bf16(sum_{i<N} P_i[rows of
+ * chunk j]) summed in fp32 in shard order.  P [N x T x d]; Y_chunks host array
+ * of N pointers [T/N x d]; T % N == 0. */
+TPMLP_API tpmlp_status tpmlp_reduce_scatter(const void* P, const tpmlp_shape* shape, void* const* Y_chunks,
+                                  tpmlp_stream_t stream);
+
+/* LayerNorm of every chunk into its row slot of the gathered activation:
+ * Xg[j T/N + r] = LN(X_chunks[j][r]).  Xg [T x d]; T % N == 0. */
+TPMLP_API tpmlp_status tpmlp_layernorm_gather(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                    const tpmlp_shape* shape, void* Xg, tpmlp_stream_t stream);
+
+/* dHpre = (dY B^T) * GeLU'(Hpre) and H = GeLU(Hpre) in one GEMM epilogue;
+ * with dbias != NULL also dbias = column sums of dHpre (workspace: size of
+ * TPMLP_OP_DH_GELUPRIME).  dY [T x d], B [F x d], Hpre/dHpre/H [T x F]. */
+TPMLP_API tpmlp_status tpmlp_gemm_dh_geluprime(const void* dY, const void* B, const void* Hpre, const tpmlp_shape* shape,
+                                     void* dHpre, void* H, void* dbias, void* workspace, size_t workspace_bytes,
+                                     tpmlp_stream_t stream);
+
+/* Weight gradient of the row-parallel layer: dB = H^T dY.  H [T x F], dY [T x d], dB [F x d]. */
+TPMLP_API tpmlp_status tpmlp_gemm_wgrad_b(const void* H, const void* dY, const tpmlp_shape* shape, void* dB,
+                                tpmlp_stream_t stream);
+
+/* Weight gradient of the column-parallel layer: dA = X^T dHpre.  X [T x d], dHpre [T x F], dA [d x F]. */
+TPMLP_API tpmlp_status tpmlp_gemm_wgrad_a(const void* X, const void* dHpre, const tpmlp_shape* shape, void* dA,
+                                tpmlp_stream_t stream);
+
+/* Input gradient with the backward shard reduction: dX = sum_i dHpre_i A_i^T.
+ * dHpre [T x F], A [d x F], dX [T x d]. */
+TPMLP_API tpmlp_status tpmlp_gemm_dx_shard_accum(const void* dHpre, const void* A, const tpmlp_shape* shape, void* dX,
+                                       tpmlp_stream_t stream);
+
+/* LayerNorm backward per chunk: with xhat = (x - mean) rstd and g = dXg gamma,
+ * dx = rstd (g - mean(g) - xhat mean(g xhat)); dgamma = sum dXg xhat and
+ * dbeta = sum dXg over all T rows (fp32 [d]).  X_chunks / dX_chunks host
+ * arrays of N pointers [T/N x d]; dXg [T x d] is the gradient of the gathered
+ * LayerNorm output.  Workspace: size of TPMLP_OP_LN_BWD. */
+TPMLP_API tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, const void* gamma, float eps, const void* dXg,
+                                      const tpmlp_shape* shape, void* const* dX_chunks, void* dgamma, void* dbeta,
+                                      void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Failure-detection self test: launches one CTA that waits on a barrier no
+ * thread ever arrives at, with a limit of `budget_us` microseconds (1 to
+ * 1000000).  The wait runs out, the kernel records the timeout and exits;
+ * tpmlp_get_device_status then returns TPMLP_ERR_TIMEOUT.  Nothing traps. */
+TPMLP_API tpmlp_status tpmlp_selftest_wait_timeout(uint32_t budget_us, tpmlp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

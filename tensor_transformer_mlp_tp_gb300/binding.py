@@ -1,0 +1,261 @@
+"""Python binding of ``libtpmlp.so`` (the C ABI in ``include/tpmlp.h``).
+
+Argument marshalling only: every function here checks nothing the library
+does not check itself, computes nothing, and calls exactly one ABI entry
+point with the same name.  Tensors are torch tensors on the current CUDA
+device; shapes are read from them.  PyTorch is used only for device memory
+(the workspace) and streams.  If the library is missing the first call
+raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtpmlp.so")
+_lib = None
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
+BF16, FP32 = 0, 1
+OP_FWD, OP_SP_FWD, OP_SP_FWD_PARTIALS, OP_BWD, OP_SP_BWD, OP_DH_GELUPRIME, OP_LN_BWD = range(7)
+RS_FUSED, RS_PARTIALS = 0, 1
+
+
+class TpMlpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int64), ("d", ctypes.c_int64), ("ffn", ctypes.c_int64),
+                ("n_shards", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_SP = ctypes.POINTER(Shape)
+_SIGS = {
+    "tpmlp_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "tpmlp_workspace_size": ([_SP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "tpmlp_get_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+    "tpmlp_forward": ([_P, _P, _P, _P, _SP, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_sp_forward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _SP, _PP, ctypes.c_int, _P, _P, ctypes.c_size_t,
+                          _P], ctypes.c_int),
+    "tpmlp_backward": ([_P, _P, _P, _P, _P, _P, _SP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_sp_backward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _P, _PP, _SP, _PP, _P, _P, _P, _P, _P, _P,
+                           ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_gemm1_bias_gelu": ([_P, _P, _P, _SP, _P, _P, _P], ctypes.c_int),
+    "tpmlp_gemm2_shard_accum": ([_P, _P, _SP, _P, _PP, _P], ctypes.c_int),
+    "tpmlp_gemm2_partials": ([_P, _P, _SP, _P, _P], ctypes.c_int),
+    "tpmlp_reduce_scatter": ([_P, _SP, _PP, _P], ctypes.c_int),
+    "tpmlp_layernorm_gather": ([_PP, _P, _P, ctypes.c_float, _SP, _P, _P], ctypes.c_int),
+    "tpmlp_gemm_dh_geluprime": ([_P, _P, _P, _SP, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_gemm_wgrad_b": ([_P, _P, _SP, _P, _P], ctypes.c_int),
+    "tpmlp_gemm_wgrad_a": ([_P, _P, _SP, _P, _P], ctypes.c_int),
+    "tpmlp_gemm_dx_shard_accum": ([_P, _P, _SP, _P, _P], ctypes.c_int),
+    "tpmlp_layernorm_backward": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P, ctypes.c_size_t, _P],
+                                 ctypes.c_int),
+    "tpmlp_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
+}
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with tensor_transformer_mlp_tp_gb300.build "
+                               "(the CUDA path has no fallback)")
+        l = ctypes.CDLL(_LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(l, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = l
+    return _lib
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def status_string(status: int) -> str:
+    return lib().tpmlp_status_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise TpMlpError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _ptrs(ts):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    return ctypes.cast(arr, _PP), arr
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def make_shape(tokens: int, d: int, ffn: int, n_shards: int, dtype: int = BF16) -> Shape:
+    return Shape(tokens, d, ffn, n_shards, dtype)
+
+
+def _dtype_code(t) -> int:
+    return FP32 if t.dtype == torch.float32 else BF16
+
+
+def tpmlp_workspace_size(shape: Shape, op: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("tpmlp_workspace_size", lib().tpmlp_workspace_size(ctypes.byref(shape), op, ctypes.byref(n)))
+    return n.value
+
+
+def workspace(shape: Shape, op: int, device=None) -> torch.Tensor:
+    """A device buffer large enough for `op` (torch allocation; contents undefined)."""
+    return torch.empty(max(tpmlp_workspace_size(shape, op), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def tpmlp_get_device_status(stream=None):
+    site = ctypes.c_uint32(0)
+    st = lib().tpmlp_get_device_status(_stream(stream), ctypes.byref(site))
+    return st, site.value
+
+
+# ----------------------------------------------------------------------------- block calls
+
+def tpmlp_forward(X, A, B, bias, N, Y, Hpre_out=None, ws=None, stream=None):
+    T, d = X.shape
+    shape = make_shape(T, d, A.shape[1], N, _dtype_code(X))
+    ws = workspace(shape, OP_FWD, X.device) if ws is None else ws
+    _check("tpmlp_forward", lib().tpmlp_forward(_ptr(X), _ptr(A), _ptr(B), _ptr(bias), ctypes.byref(shape), _ptr(Y),
+                                                _ptr(Hpre_out), _ptr(ws), ws.numel(), _stream(stream)))
+    return Y
+
+
+def tpmlp_sp_forward(X_chunks, gamma, beta, A, B, N, Y_chunks, bias=None, eps=1e-5, rs_mode=RS_FUSED,
+                     Hpre_out=None, ws=None, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, A.shape[1], N)
+    op = OP_SP_FWD if rs_mode == RS_FUSED else OP_SP_FWD_PARTIALS
+    ws = workspace(shape, op, A.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    yp, _ya = _ptrs(Y_chunks)
+    _check("tpmlp_sp_forward", lib().tpmlp_sp_forward(xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias),
+                                                      ctypes.byref(shape), yp, rs_mode, _ptr(Hpre_out), _ptr(ws),
+                                                      ws.numel(), _stream(stream)))
+    return Y_chunks
+
+
+def tpmlp_backward(X, A, B, bias, Hpre, dY, N, dX, dA, dB, dbias=None, ws=None, stream=None):
+    T, d = X.shape
+    shape = make_shape(T, d, A.shape[1], N)
+    ws = workspace(shape, OP_BWD, X.device) if ws is None else ws
+    _check("tpmlp_backward", lib().tpmlp_backward(_ptr(X), _ptr(A), _ptr(B), _ptr(bias), _ptr(Hpre), _ptr(dY),
+                                                  ctypes.byref(shape), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(dbias),
+                                                  _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def tpmlp_sp_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_chunks, dA, dB, dgamma, dbeta,
+                      bias=None, dbias=None, eps=1e-5, ws=None, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, A.shape[1], N)
+    ws = workspace(shape, OP_SP_BWD, A.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    dyp, _dya = _ptrs(dY_chunks)
+    dxp, _dxa = _ptrs(dX_chunks)
+    _check("tpmlp_sp_backward", lib().tpmlp_sp_backward(
+        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _ptr(Hpre), dyp, ctypes.byref(shape), dxp,
+        _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- single steps
+
+def tpmlp_gemm1_bias_gelu(X, A, bias, N, H, Hpre=None, stream=None):
+    shape = make_shape(X.shape[0], X.shape[1], A.shape[1], N)
+    _check("tpmlp_gemm1_bias_gelu", lib().tpmlp_gemm1_bias_gelu(_ptr(X), _ptr(A), _ptr(bias), ctypes.byref(shape),
+                                                                _ptr(H), _ptr(Hpre), _stream(stream)))
+
+
+def tpmlp_gemm2_shard_accum(H, B, N, Y=None, Y_chunks=None, stream=None):
+    shape = make_shape(H.shape[0], B.shape[1], H.shape[1], N)
+    if Y_chunks is not None:
+        yp, _ya = _ptrs(Y_chunks)
+    else:
+        yp = None
+    _check("tpmlp_gemm2_shard_accum", lib().tpmlp_gemm2_shard_accum(_ptr(H), _ptr(B), ctypes.byref(shape), _ptr(Y),
+                                                                    yp, _stream(stream)))
+
+
+def tpmlp_gemm2_partials(H, B, N, P, stream=None):
+    shape = make_shape(H.shape[0], B.shape[1], H.shape[1], N)
+    _check("tpmlp_gemm2_partials", lib().tpmlp_gemm2_partials(_ptr(H), _ptr(B), ctypes.byref(shape), _ptr(P),
+                                                              _stream(stream)))
+
+
+def tpmlp_reduce_scatter(P, N, Y_chunks, stream=None):
+    _, T, d = P.shape
+    shape = make_shape(T, d, 8 * N, N)  # ffn unused by this step
+    yp, _ya = _ptrs(Y_chunks)
+    _check("tpmlp_reduce_scatter", lib().tpmlp_reduce_scatter(_ptr(P), ctypes.byref(shape), yp, _stream(stream)))
+
+
+def tpmlp_layernorm_gather(X_chunks, gamma, beta, N, Xg, eps=1e-5, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
+    xp, _xa = _ptrs(X_chunks)
+    _check("tpmlp_layernorm_gather", lib().tpmlp_layernorm_gather(xp, _ptr(gamma), _ptr(beta), eps,
+                                                                  ctypes.byref(shape), _ptr(Xg), _stream(stream)))
+
+
+def tpmlp_gemm_dh_geluprime(dY, B, Hpre, N, dHpre, H, dbias=None, ws=None, stream=None):
+    shape = make_shape(dY.shape[0], dY.shape[1], B.shape[0], N)
+    if dbias is not None and ws is None:
+        ws = workspace(shape, OP_DH_GELUPRIME, dY.device)
+    _check("tpmlp_gemm_dh_geluprime", lib().tpmlp_gemm_dh_geluprime(
+        _ptr(dY), _ptr(B), _ptr(Hpre), ctypes.byref(shape), _ptr(dHpre), _ptr(H), _ptr(dbias), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def tpmlp_gemm_wgrad_b(H, dY, N, dB, stream=None):
+    shape = make_shape(H.shape[0], dY.shape[1], H.shape[1], N)
+    _check("tpmlp_gemm_wgrad_b", lib().tpmlp_gemm_wgrad_b(_ptr(H), _ptr(dY), ctypes.byref(shape), _ptr(dB),
+                                                          _stream(stream)))
+
+
+def tpmlp_gemm_wgrad_a(X, dHpre, N, dA, stream=None):
+    shape = make_shape(X.shape[0], X.shape[1], dHpre.shape[1], N)
+    _check("tpmlp_gemm_wgrad_a", lib().tpmlp_gemm_wgrad_a(_ptr(X), _ptr(dHpre), ctypes.byref(shape), _ptr(dA),
+                                                          _stream(stream)))
+
+
+def tpmlp_gemm_dx_shard_accum(dHpre, A, N, dX, stream=None):
+    shape = make_shape(dHpre.shape[0], A.shape[0], dHpre.shape[1], N)
+    _check("tpmlp_gemm_dx_shard_accum", lib().tpmlp_gemm_dx_shard_accum(_ptr(dHpre), _ptr(A), ctypes.byref(shape),
+                                                                        _ptr(dX), _stream(stream)))
+
+
+def tpmlp_layernorm_backward(X_chunks, gamma, dXg, N, dX_chunks, dgamma, dbeta, eps=1e-5, ws=None, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
+    ws = workspace(shape, OP_LN_BWD, dXg.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    dxp, _dxa = _ptrs(dX_chunks)
+    _check("tpmlp_layernorm_backward", lib().tpmlp_layernorm_backward(
+        xp, _ptr(gamma), eps, _ptr(dXg), ctypes.byref(shape), dxp, _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def tpmlp_selftest_wait_timeout(budget_us: int, stream=None):
+    _check("tpmlp_selftest_wait_timeout", lib().tpmlp_selftest_wait_timeout(budget_us, _stream(stream)))

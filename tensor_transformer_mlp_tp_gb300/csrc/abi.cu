@@ -1,0 +1,665 @@
+// C ABI of libtpmlp: argument validation, workspace carving and the launch
+// sequences of the block calls.  Everything here is host code except the
+// device error words and the wait-timeout self test.
+#include <climits>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tpmlp.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+
+__device__ unsigned int g_err_words[kErrWords];
+
+namespace {
+
+// One CTA waits on a barrier nobody arrives at; the bounded wait gives up,
+// records kErrTimeout and the kernel returns.
+__global__ void k_wait_timeout_selftest(unsigned int* err, unsigned long long budget_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtx wc{&abort_flag, err, budget_ns};
+    (void)wait_bounded(&bar, 0, wc, 99u);
+  }
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct DevState {
+  bool init = false;
+  DeviceCtx ctx{};
+};
+std::mutex g_mu;
+DevState g_dev[64];
+
+unsigned long long timeout_ns_from_env() {
+  const char* s = std::getenv("TPMLP_WAIT_TIMEOUT_MS");
+  if (s != nullptr) {
+    const long long ms = std::atoll(s);
+    if (ms > 0) return static_cast<unsigned long long>(ms) * 1000000ull;
+  }
+  return 1000000000ull;
+}
+
+tpmlp_status device_ctx(DeviceCtx* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TPMLP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& st = g_dev[dev];
+  if (!st.init) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_words) != cudaSuccess) return TPMLP_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return TPMLP_ERR_CUDA;
+    st.ctx.err = static_cast<unsigned int*>(p);
+    st.ctx.sm_count = sms;
+    st.ctx.timeout_ns = timeout_ns_from_env();
+    st.init = true;
+  }
+  *out = st.ctx;
+  return TPMLP_OK;
+}
+
+tpmlp_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TPMLP_OK;
+  if (e == cudaErrorNotSupported) return TPMLP_ERR_UNSUPPORTED;
+  return TPMLP_ERR_CUDA;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks common to every call.  `sp` adds T % N == 0.
+tpmlp_status check_shape(const tpmlp_shape* s, bool sp, bool bf16_only) {
+  if (s == nullptr) return TPMLP_ERR_INVALID_ARG;
+  if (s->tokens < 0 || s->d < 1 || s->ffn < 1 || s->n_shards < 1 || s->n_shards > kMaxShards)
+    return TPMLP_ERR_INVALID_ARG;
+  if (s->dtype != TPMLP_BF16 && s->dtype != TPMLP_FP32) return TPMLP_ERR_INVALID_ARG;
+  if (s->ffn % s->n_shards != 0) return TPMLP_ERR_INVALID_ARG;
+  if (sp && s->tokens % s->n_shards != 0) return TPMLP_ERR_INVALID_ARG;
+  if (s->tokens > INT_MAX / 2 || s->d > INT_MAX / 2 || s->ffn > INT_MAX / 2) return TPMLP_ERR_UNSUPPORTED;
+  if (s->dtype == TPMLP_BF16) {
+    if (s->d % 8 != 0 || (s->ffn / s->n_shards) % 8 != 0) return TPMLP_ERR_INVALID_ARG;
+  } else if (bf16_only) {
+    return TPMLP_ERR_UNSUPPORTED;
+  }
+  return TPMLP_OK;
+}
+
+bool ptrs_ok(std::initializer_list<const void*> required) {
+  for (const void* p : required)
+    if (p == nullptr || !al16(p)) return false;
+  return true;
+}
+
+bool opt_ok(const void* p) { return p == nullptr || al16(p); }
+
+bool chunks_ok(const void* const* c, int n) {
+  if (c == nullptr) return false;
+  for (int i = 0; i < n; ++i)
+    if (c[i] == nullptr || !al16(c[i])) return false;
+  return true;
+}
+
+// Sizes of the workspace regions (bytes, each 256-aligned).
+struct Sizes {
+  size_t td, tf, ptd, colsum, lnbwd;
+};
+
+constexpr int kLnBwdMaxBlocks = 512;
+
+Sizes sizes_of(const tpmlp_shape* s) {
+  const size_t T = static_cast<size_t>(s->tokens), d = static_cast<size_t>(s->d), F = static_cast<size_t>(s->ffn);
+  const size_t el = s->dtype == TPMLP_FP32 ? 4 : 2;
+  Sizes z;
+  z.td = align_up(T * d * el);
+  z.tf = align_up(T * F * el);
+  z.ptd = align_up(static_cast<size_t>(s->n_shards) * T * d * 2);
+  const size_t m_blocks = (T + kBM - 1) / kBM;
+  z.colsum = align_up(4 * m_blocks * F * 4);
+  const size_t blocks = static_cast<size_t>(layernorm_bwd_blocks(static_cast<int>(T), kLnBwdMaxBlocks));
+  z.lnbwd = align_up(blocks * 2 * d * 4);
+  return z;
+}
+
+size_t ws_bytes(const tpmlp_shape* s, int op) {
+  const Sizes z = sizes_of(s);
+  switch (op) {
+    case TPMLP_OP_FWD: return z.tf;
+    case TPMLP_OP_SP_FWD: return z.td + z.tf;
+    case TPMLP_OP_SP_FWD_PARTIALS: return z.td + z.tf + z.ptd;
+    case TPMLP_OP_BWD: return 3 * z.tf + z.colsum;
+    case TPMLP_OP_SP_BWD: return 3 * z.tf + z.colsum + 3 * z.td + z.lnbwd;
+    case TPMLP_OP_DH_GELUPRIME: return z.colsum;
+    case TPMLP_OP_LN_BWD: return z.lnbwd;
+    default: return 0;
+  }
+}
+
+// Bump allocator over the caller's workspace.
+struct Carve {
+  uint8_t* base;
+  size_t used = 0;
+  explicit Carve(void* p) : base(static_cast<uint8_t*>(p)) {}
+  void* take(size_t bytes) {
+    void* p = base + used;
+    used += bytes;
+    return p;
+  }
+};
+
+ChunkPtrs to_chunks(void* const* c, int n) {
+  ChunkPtrs r{};
+  for (int i = 0; i < n; ++i) r.p[i] = c[i];
+  return r;
+}
+
+ConstChunkPtrs to_const_chunks(const void* const* c, int n) {
+  ConstChunkPtrs r{};
+  for (int i = 0; i < n; ++i) r.p[i] = c[i];
+  return r;
+}
+
+// ------------------------------------------------------------------ step implementations (validated inputs)
+
+cudaError_t do_gemm1(const DeviceCtx& c, const void* X, const void* A, const void* bias, const tpmlp_shape* s,
+                     void* H, void* Hpre, int epi, cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->ffn);
+  g.K = static_cast<int>(s->d);
+  g.a = {X, s->d, false};
+  g.b = {A, s->ffn, true};
+  g.epi = epi;
+  g.out0 = H;
+  g.ld0 = s->ffn;
+  g.out1 = Hpre;
+  g.ld1 = s->ffn;
+  g.bias = bias;
+  return launch_gemm(g, c, st);
+}
+
+cudaError_t do_gemm2(const DeviceCtx& c, const void* H, const void* B, const tpmlp_shape* s, void* Y,
+                     void* const* Y_chunks, cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->d);
+  g.K = static_cast<int>(s->ffn);
+  g.a = {H, s->ffn, false};
+  g.b = {B, s->d, true};
+  g.epi = kEpiStore;
+  g.out0 = Y;
+  g.ld0 = s->d;
+  if (Y_chunks != nullptr) {
+    g.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
+    g.chunks = to_chunks(Y_chunks, s->n_shards);
+  }
+  return launch_gemm(g, c, st);
+}
+
+cudaError_t do_gemm2_partials(const DeviceCtx& c, const void* H, const void* B, const tpmlp_shape* s, void* P,
+                              cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->d);
+  g.K = static_cast<int>(s->ffn);
+  g.a = {H, s->ffn, false};
+  g.b = {B, s->d, true};
+  g.epi = kEpiStore;
+  g.shards = s->n_shards;
+  g.out0 = P;
+  g.ld0 = s->d;
+  g.shard_stride0 = s->tokens * s->d;
+  return launch_gemm(g, c, st);
+}
+
+cudaError_t do_reduce_scatter(const DeviceCtx& c, const void* P, const tpmlp_shape* s, void* const* Y_chunks,
+                              cudaStream_t st) {
+  RowParams r{};
+  r.out_chunks = to_chunks(Y_chunks, s->n_shards);
+  r.rows = static_cast<int>(s->tokens);
+  r.d = static_cast<int>(s->d);
+  r.n_chunks = s->n_shards;
+  r.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
+  r.src = P;
+  r.shard_stride = s->tokens * s->d;
+  return launch_reduce_scatter(r, c, st);
+}
+
+cudaError_t do_layernorm(const DeviceCtx& c, const void* const* X_chunks, const void* gamma, const void* beta,
+                         float eps, const tpmlp_shape* s, void* Xg, cudaStream_t st) {
+  RowParams r{};
+  r.in_chunks = to_const_chunks(X_chunks, s->n_shards);
+  r.rows = static_cast<int>(s->tokens);
+  r.d = static_cast<int>(s->d);
+  r.n_chunks = s->n_shards;
+  r.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
+  r.eps = eps;
+  r.gamma = gamma;
+  r.beta = beta;
+  r.dst = Xg;
+  return launch_layernorm_fwd(r, c, st);
+}
+
+cudaError_t do_dh(const DeviceCtx& c, const void* dY, const void* B, const void* Hpre, const tpmlp_shape* s,
+                  void* dHpre, void* H, void* dbias, float* colsum, cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->ffn);
+  g.K = static_cast<int>(s->d);
+  g.a = {dY, s->d, false};
+  g.b = {B, s->d, false};
+  g.epi = kEpiDGelu;
+  g.out0 = dHpre;
+  g.ld0 = s->ffn;
+  g.out1 = H;
+  g.ld1 = s->ffn;
+  g.aux = Hpre;
+  g.ld_aux = s->ffn;
+  g.colsum = dbias != nullptr ? colsum : nullptr;
+  cudaError_t e = launch_gemm(g, c, st);
+  if (e != cudaSuccess || dbias == nullptr) return e;
+  const int m_blocks = static_cast<int>((s->tokens + kBM - 1) / kBM);
+  return launch_column_sum(colsum, 4 * m_blocks, static_cast<int>(s->ffn), dbias, true, st);
+}
+
+cudaError_t do_wgrad_b(const DeviceCtx& c, const void* H, const void* dY, const tpmlp_shape* s, void* dB,
+                       cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->ffn);
+  g.N = static_cast<int>(s->d);
+  g.K = static_cast<int>(s->tokens);
+  g.a = {H, s->ffn, true};
+  g.b = {dY, s->d, true};
+  g.epi = kEpiStore;
+  g.out0 = dB;
+  g.ld0 = s->d;
+  return launch_gemm(g, c, st);
+}
+
+cudaError_t do_wgrad_a(const DeviceCtx& c, const void* X, const void* dHpre, const tpmlp_shape* s, void* dA,
+                       cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->d);
+  g.N = static_cast<int>(s->ffn);
+  g.K = static_cast<int>(s->tokens);
+  g.a = {X, s->d, true};
+  g.b = {dHpre, s->ffn, true};
+  g.epi = kEpiStore;
+  g.out0 = dA;
+  g.ld0 = s->ffn;
+  return launch_gemm(g, c, st);
+}
+
+cudaError_t do_dx(const DeviceCtx& c, const void* dHpre, const void* A, const tpmlp_shape* s, void* dX,
+                  cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->d);
+  g.K = static_cast<int>(s->ffn);
+  g.a = {dHpre, s->ffn, false};
+  g.b = {A, s->ffn, false};
+  g.epi = kEpiStore;
+  g.out0 = dX;
+  g.ld0 = s->d;
+  return launch_gemm(g, c, st);
+}
+
+cudaError_t do_ln_bwd(const DeviceCtx& c, const void* const* X_chunks, const void* gamma, float eps, const void* dXg,
+                      const tpmlp_shape* s, void* const* dX_chunks, void* dgamma, void* dbeta, float* partial,
+                      cudaStream_t st) {
+  RowParams r{};
+  r.in_chunks = to_const_chunks(X_chunks, s->n_shards);
+  r.out_chunks = to_chunks(dX_chunks, s->n_shards);
+  r.rows = static_cast<int>(s->tokens);
+  r.d = static_cast<int>(s->d);
+  r.n_chunks = s->n_shards;
+  r.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
+  r.eps = eps;
+  r.gamma = gamma;
+  r.src = dXg;
+  r.partial = partial;
+  (void)c;
+  return launch_layernorm_bwd(r, kLnBwdMaxBlocks, static_cast<float*>(dgamma), static_cast<float*>(dbeta), st);
+}
+
+// Backward core shared by tpmlp_backward and tpmlp_sp_backward.
+cudaError_t backward_core(const DeviceCtx& c, const void* X, const void* A, const void* B, const void* bias,
+                          const void* Hpre, const void* dY, const tpmlp_shape* s, void* dX, void* dA, void* dB,
+                          void* dbias, Carve& ws, cudaStream_t st) {
+  const Sizes z = sizes_of(s);
+  void* hpre_ws = ws.take(z.tf);
+  void* dhpre = ws.take(z.tf);
+  void* h = ws.take(z.tf);
+  float* colsum = static_cast<float*>(ws.take(z.colsum));
+  cudaError_t e = cudaSuccess;
+  if (Hpre == nullptr) {
+    e = do_gemm1(c, X, A, bias, s, hpre_ws, nullptr, kEpiBias, st);
+    if (e != cudaSuccess) return e;
+    Hpre = hpre_ws;
+  }
+  if ((e = do_dh(c, dY, B, Hpre, s, dhpre, h, dbias, colsum, st)) != cudaSuccess) return e;
+  if ((e = do_wgrad_b(c, h, dY, s, dB, st)) != cudaSuccess) return e;
+  if ((e = do_wgrad_a(c, X, dhpre, s, dA, st)) != cudaSuccess) return e;
+  return do_dx(c, dhpre, A, s, dX, st);
+}
+
+}  // namespace
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+extern "C" {
+
+const char* tpmlp_status_string(tpmlp_status s) {
+  switch (s) {
+    case TPMLP_OK: return "ok";
+    case TPMLP_ERR_INVALID_ARG: return "invalid argument";
+    case TPMLP_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case TPMLP_ERR_CUDA: return "CUDA error";
+    case TPMLP_ERR_TIMEOUT: return "device wait timed out";
+    case TPMLP_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+tpmlp_status tpmlp_workspace_size(const tpmlp_shape* shape, int op, size_t* bytes) {
+  if (bytes == nullptr) return TPMLP_ERR_INVALID_ARG;
+  const bool sp = op == TPMLP_OP_SP_FWD || op == TPMLP_OP_SP_FWD_PARTIALS || op == TPMLP_OP_SP_BWD ||
+                  op == TPMLP_OP_LN_BWD;
+  const bool bf16_only = op != TPMLP_OP_FWD;
+  tpmlp_status st = check_shape(shape, sp, bf16_only);
+  if (st != TPMLP_OK) return st;
+  if (op < TPMLP_OP_FWD || op > TPMLP_OP_LN_BWD) return TPMLP_ERR_INVALID_ARG;
+  *bytes = ws_bytes(shape, op);
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_get_device_status(tpmlp_stream_t stream, uint32_t* site) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return TPMLP_ERR_CUDA;
+  unsigned int w[kErrWords];
+  if (cudaMemcpyFromSymbol(w, g_err_words, sizeof(w)) != cudaSuccess) return TPMLP_ERR_CUDA;
+  if (site != nullptr) *site = w[1];
+  if (w[0] == 0) return TPMLP_OK;
+  unsigned int zero[kErrWords] = {0, 0, 0, 0};
+  if (cudaMemcpyToSymbol(g_err_words, zero, sizeof(zero)) != cudaSuccess) return TPMLP_ERR_CUDA;
+  return (w[0] & kErrTimeout) ? TPMLP_ERR_TIMEOUT : TPMLP_ERR_CUDA;
+}
+
+tpmlp_status tpmlp_selftest_wait_timeout(uint32_t budget_us, tpmlp_stream_t stream) {
+  if (budget_us < 1 || budget_us > 1000000) return TPMLP_ERR_INVALID_ARG;
+  DeviceCtx c;
+  tpmlp_status st = device_ctx(&c);
+  if (st != TPMLP_OK) return st;
+  k_wait_timeout_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      c.err, static_cast<unsigned long long>(budget_us) * 1000ull);
+  return cuda_status(cudaGetLastError());
+}
+
+tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
+                           void* Y, void* Hpre_out, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, false);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({X, A, B, Y}) || !opt_ok(bias) || !opt_ok(Hpre_out)) return TPMLP_ERR_INVALID_ARG;
+  if (shape->dtype == TPMLP_FP32 && Hpre_out != nullptr) return TPMLP_ERR_UNSUPPORTED;
+  if (shape->tokens == 0) return TPMLP_OK;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_FWD))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (shape->dtype == TPMLP_FP32) {
+    return cuda_status(launch_mlp_fp32(static_cast<const float*>(X), static_cast<const float*>(A),
+                                       static_cast<const float*>(B), static_cast<const float*>(bias),
+                                       static_cast<int>(shape->tokens), static_cast<int>(shape->d),
+                                       static_cast<int>(shape->ffn), static_cast<float*>(workspace),
+                                       static_cast<float*>(Y), s));
+  }
+  cudaError_t e = do_gemm1(c, X, A, bias, shape, workspace, Hpre_out, kEpiBiasGelu, s);
+  if (e == cudaSuccess) e = do_gemm2(c, workspace, B, shape, Y, nullptr, s);
+  return cuda_status(e);
+}
+
+tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                              const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
+                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* workspace,
+                              size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !opt_ok(Hpre_out)) return TPMLP_ERR_INVALID_ARG;
+  if (!chunks_ok(X_chunks, shape->n_shards) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
+  if (!(eps >= 0.f)) return TPMLP_ERR_INVALID_ARG;
+  if (rs_mode != TPMLP_RS_FUSED && rs_mode != TPMLP_RS_PARTIALS) return TPMLP_ERR_INVALID_ARG;
+  if (rs_mode == TPMLP_RS_PARTIALS && (shape->ffn / shape->n_shards) % kBK != 0) return TPMLP_ERR_UNSUPPORTED;
+  if (shape->tokens == 0) return TPMLP_OK;
+  const int op = rs_mode == TPMLP_RS_FUSED ? TPMLP_OP_SP_FWD : TPMLP_OP_SP_FWD_PARTIALS;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, op)) return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Sizes z = sizes_of(shape);
+  Carve ws(workspace);
+  void* Xg = ws.take(z.td);
+  void* H = ws.take(z.tf);
+  cudaError_t e = do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, s);
+  if (e == cudaSuccess) e = do_gemm1(c, Xg, A, bias, shape, H, Hpre_out, kEpiBiasGelu, s);
+  if (e == cudaSuccess) {
+    if (rs_mode == TPMLP_RS_FUSED) {
+      e = do_gemm2(c, H, B, shape, nullptr, Y_chunks, s);
+    } else {
+      void* P = ws.take(z.ptd);
+      e = do_gemm2_partials(c, H, B, shape, P, s);
+      if (e == cudaSuccess) e = do_reduce_scatter(c, P, shape, Y_chunks, s);
+    }
+  }
+  return cuda_status(e);
+}
+
+tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* bias, const void* Hpre,
+                            const void* dY, const tpmlp_shape* shape, void* dX, void* dA, void* dB, void* dbias,
+                            void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({X, A, B, dY, dX, dA, dB}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(dbias))
+    return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;  // dA, dB, dbias of an empty batch: left to the caller (zeros)
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_BWD))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  Carve ws(workspace);
+  return cuda_status(backward_core(c, X, A, B, bias, Hpre, dY, shape, dX, dA, dB, dbias, ws,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                               const void* A, const void* B, const void* bias, const void* Hpre,
+                               const void* const* dY_chunks, const tpmlp_shape* shape, void* const* dX_chunks,
+                               void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
+                               size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({gamma, beta, A, B, dA, dB, dgamma, dbeta}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(dbias))
+    return TPMLP_ERR_INVALID_ARG;
+  const int n = shape->n_shards;
+  if (!chunks_ok(X_chunks, n) || !chunks_ok(dY_chunks, n) || !chunks_ok(dX_chunks, n)) return TPMLP_ERR_INVALID_ARG;
+  if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
+  if (!(eps >= 0.f)) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_SP_BWD))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Sizes z = sizes_of(shape);
+  Carve ws(workspace);
+  void* Xg = ws.take(z.td);
+  void* dYg = ws.take(z.td);
+  void* dXg = ws.take(z.td);
+  float* lnpart = static_cast<float*>(ws.take(z.lnbwd));
+  cudaError_t e = do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  // The All-Gather of dY is free when the chunks already lie back to back.
+  const size_t chunk_bytes = static_cast<size_t>(shape->tokens / n) * shape->d * 2;
+  bool contiguous = true;
+  for (int j = 1; j < n; ++j)
+    contiguous = contiguous && static_cast<const uint8_t*>(dY_chunks[j]) ==
+                                   static_cast<const uint8_t*>(dY_chunks[0]) + j * chunk_bytes;
+  const void* dY = dY_chunks[0];
+  if (!contiguous) {
+    RowParams r{};
+    r.in_chunks = to_const_chunks(dY_chunks, n);
+    r.rows = static_cast<int>(shape->tokens);
+    r.d = static_cast<int>(shape->d);
+    r.n_chunks = n;
+    r.rows_per_chunk = static_cast<int>(shape->tokens / n);
+    r.dst = dYg;
+    if ((e = launch_gather_rows(r, c, s)) != cudaSuccess) return cuda_status(e);
+    dY = dYg;
+  }
+  e = backward_core(c, Xg, A, B, bias, Hpre, dY, shape, dXg, dA, dB, dbias, ws, s);
+  if (e == cudaSuccess) e = do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta, lnpart, s);
+  return cuda_status(e);
+}
+
+// ------------------------------------------------------------------ single steps
+
+tpmlp_status tpmlp_gemm1_bias_gelu(const void* X, const void* A, const void* bias, const tpmlp_shape* shape, void* H,
+                                   void* Hpre, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({X, A, H}) || !opt_ok(bias) || !opt_ok(Hpre)) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_gemm1(c, X, A, bias, shape, H, Hpre, kEpiBiasGelu, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm2_shard_accum(const void* H, const void* B, const tpmlp_shape* shape, void* Y,
+                                     void* const* Y_chunks, tpmlp_stream_t stream) {
+  const bool chunked = Y_chunks != nullptr;
+  tpmlp_status st = check_shape(shape, chunked, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({H, B})) return TPMLP_ERR_INVALID_ARG;
+  if (chunked ? !chunks_ok(Y_chunks, shape->n_shards) : !ptrs_ok({Y})) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_gemm2(c, H, B, shape, Y, Y_chunks, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm2_partials(const void* H, const void* B, const tpmlp_shape* shape, void* P,
+                                  tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({H, B, P})) return TPMLP_ERR_INVALID_ARG;
+  if ((shape->ffn / shape->n_shards) % kBK != 0) return TPMLP_ERR_UNSUPPORTED;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_gemm2_partials(c, H, B, shape, P, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_reduce_scatter(const void* P, const tpmlp_shape* shape, void* const* Y_chunks,
+                                  tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({P}) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_reduce_scatter(c, P, shape, Y_chunks, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_layernorm_gather(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                    const tpmlp_shape* shape, void* Xg, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({gamma, beta, Xg}) || !chunks_ok(X_chunks, shape->n_shards) || !(eps >= 0.f))
+    return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm_dh_geluprime(const void* dY, const void* B, const void* Hpre, const tpmlp_shape* shape,
+                                     void* dHpre, void* H, void* dbias, void* workspace, size_t workspace_bytes,
+                                     tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({dY, B, Hpre, dHpre, H}) || !opt_ok(dbias)) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  if (dbias != nullptr && (workspace == nullptr || !al16(workspace) ||
+                           workspace_bytes < ws_bytes(shape, TPMLP_OP_DH_GELUPRIME)))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_dh(c, dY, B, Hpre, shape, dHpre, H, dbias, static_cast<float*>(workspace),
+                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm_wgrad_b(const void* H, const void* dY, const tpmlp_shape* shape, void* dB,
+                                tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({H, dY, dB})) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_wgrad_b(c, H, dY, shape, dB, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm_wgrad_a(const void* X, const void* dHpre, const tpmlp_shape* shape, void* dA,
+                                tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({X, dHpre, dA})) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_wgrad_a(c, X, dHpre, shape, dA, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm_dx_shard_accum(const void* dHpre, const void* A, const tpmlp_shape* shape, void* dX,
+                                       tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({dHpre, A, dX})) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_dx(c, dHpre, A, shape, dX, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, const void* gamma, float eps, const void* dXg,
+                                      const tpmlp_shape* shape, void* const* dX_chunks, void* dgamma, void* dbeta,
+                                      void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (!ptrs_ok({gamma, dXg, dgamma, dbeta}) || !chunks_ok(X_chunks, shape->n_shards) ||
+      !chunks_ok(dX_chunks, shape->n_shards) || !(eps >= 0.f))
+    return TPMLP_ERR_INVALID_ARG;
+  if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
+  if (shape->tokens == 0) return TPMLP_OK;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_LN_BWD))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta,
+                               static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Constants and kernel-parameter structs shared by the host launchers and
+// the kernels of libtpmlp.  No torch types, no allocation.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace tpmlp {
+
+constexpr int kMaxShards = 64;  // N, the number of column/row shards (and of SP chunks)
+
+// Device error words: [0] = OR of error bits, [1] = first failing wait site.
+constexpr int kErrWords = 4;
+constexpr uint32_t kErrTimeout = 1u;
+
+// Wait sites reported in error word [1] (one id per wait in the GEMM kernel).
+enum WaitSite : uint32_t {
+  kSiteProducerEmpty = 1,
+  kSiteMmaFull = 2,
+  kSiteMmaTmemEmpty = 3,
+  kSiteEpiTmemFull = 4,
+};
+
+// GEMM tile: BM x BN output, BK-deep k-blocks (64 bf16 = one 128-byte swizzle row).
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kUmmaK = 16;
+
+// Epilogues of the tcgen05 GEMM.
+enum Epilogue : int {
+  kEpiBiasGelu = 0,   // out0 = bf16(GeLU(acc + bias)); out1 (optional) = bf16(acc + bias)
+  kEpiBias = 1,       // out0 = bf16(acc + bias)
+  kEpiStore = 2,      // out0 = bf16(acc), optional row -> chunk remap, optional per-shard partials
+  kEpiDGelu = 3,      // out0 = bf16(acc * GeLU'(aux)); out1 = bf16(GeLU(aux)); optional column sums
+};
+
+struct ChunkPtrs {
+  void* p[kMaxShards];
+};
+
+struct ConstChunkPtrs {
+  const void* p[kMaxShards];
+};
+
+// Parameters of one tcgen05 GEMM launch: C[M x N] = sum_k A[m, k] * B[k, n].
+// A and B are read through TMA tensor maps.  A "K-major" operand has k as
+// its contiguous dimension; an "MN-major" one has m (or n) contiguous.
+struct GemmParams {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  int M, N, K;
+  int m_blocks, n_blocks;
+  int k_blocks_per_shard;   // k-blocks summed into one accumulator
+  int shards;               // >1: per-shard partial outputs (tile space x shards, K split evenly)
+  int group_m;              // raster: tiles walk group_m row blocks before the next column block
+  void* out0;
+  long long ld0;
+  void* out1;
+  long long ld1;
+  long long shard_stride0;  // elements between consecutive shards' partial outputs
+  const void* bias;         // [N] bf16 or nullptr
+  const void* aux;          // [M x N] bf16 (pre-activation) for kEpiDGelu
+  long long ld_aux;
+  float* colsum;            // [4 * m_blocks x N] fp32 column partial sums, or nullptr
+  int rows_per_chunk;       // >0: row r of C goes to chunk r / rows_per_chunk
+  ChunkPtrs chunks;
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+// Row-wise kernels (LayerNorm forward/backward, reduce-scatter).
+struct RowParams {
+  ConstChunkPtrs in_chunks;   // N chunk pointers, each [rows_per_chunk x d] bf16
+  ChunkPtrs out_chunks;
+  int rows;                   // total rows T
+  int d;
+  int n_chunks;
+  int rows_per_chunk;
+  float eps;
+  const void* gamma;          // [d] bf16
+  const void* beta;           // [d] bf16
+  const void* src;            // contiguous [rows x d] bf16 input (gathered tensor / partials)
+  void* dst;                  // contiguous [rows x d] bf16 output
+  float* partial;             // column partial sums [blocks x 2d] fp32 (LayerNorm backward)
+  long long shard_stride;     // elements between partials (reduce-scatter)
+};
+
+}  // namespace tpmlp

@@ -1,0 +1,61 @@
+// Host-side launchers shared by the translation units of libtpmlp (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace tpmlp {
+
+// One operand of C = A * B as it is stored in memory.
+//  mn_major == false: stored [MN x K], K contiguous, `ld` elements between rows.
+//  mn_major == true : stored [K x MN], M (or N) contiguous, `ld` elements between rows.
+struct Operand {
+  const void* ptr;
+  long long ld;
+  bool mn_major;
+};
+
+struct GemmLaunch {
+  int M = 0, N = 0, K = 0;
+  Operand a{}, b{};
+  int epi = kEpiStore;
+  int shards = 1;
+  void* out0 = nullptr;
+  long long ld0 = 0;
+  void* out1 = nullptr;
+  long long ld1 = 0;
+  long long shard_stride0 = 0;
+  const void* bias = nullptr;
+  const void* aux = nullptr;
+  long long ld_aux = 0;
+  float* colsum = nullptr;
+  int rows_per_chunk = 0;
+  ChunkPtrs chunks{};
+};
+
+struct DeviceCtx {
+  unsigned int* err;           // device error words
+  unsigned long long timeout_ns;
+  int sm_count;
+};
+
+// Returns cudaErrorNotSupported for operand/epilogue combinations without a kernel.
+cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s);
+
+cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
+// LayerNorm backward with at most `max_blocks` CTAs; r.partial must hold
+// layernorm_bwd_blocks(rows, max_blocks) x 2 d floats.
+cudaError_t launch_layernorm_bwd(const RowParams& r, int max_blocks, float* dgamma, float* dbeta, cudaStream_t s);
+int layernorm_bwd_blocks(int rows, int max_blocks);
+// Largest d the LayerNorm backward supports (its 2 d fp32 accumulators live in shared memory).
+constexpr int kLnBwdMaxD = 16384;
+cudaError_t launch_reduce_scatter(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
+cudaError_t launch_gather_rows(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
+// out[c] = sum_r partial[r * cols + c] over r < rows, fixed order; bf16 or fp32 output.
+cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s);
+
+cudaError_t launch_mlp_fp32(const float* X, const float* A, const float* B, const float* bias, int T, int d, int F,
+                            float* H, float* Y, cudaStream_t s);
+
+}  // namespace tpmlp

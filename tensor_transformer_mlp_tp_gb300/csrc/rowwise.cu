@@ -1,0 +1,371 @@
+// HBM-bound row kernels of the sequence-parallel block:
+//   LayerNorm of each S/N chunk written straight into its row slot of the
+//   gathered activation (the All-Gather is a layout, not a copy);
+//   LayerNorm backward per chunk with deterministic dgamma/dbeta partials;
+//   the explicit Reduce-Scatter over per-shard bf16 partials;
+//   a row gather and a fixed-order column sum.
+// All global traffic is 16-byte vectors; reductions are warp shuffles.
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ const __nv_bfloat16* chunk_row(const RowParams& p, int row) {
+  const int j = row / p.rows_per_chunk;
+  return static_cast<const __nv_bfloat16*>(p.in_chunks.p[j]) +
+         static_cast<long long>(row - j * p.rows_per_chunk) * p.d;
+}
+
+__device__ __forceinline__ __nv_bfloat16* out_chunk_row(const RowParams& p, int row) {
+  const int j = row / p.rows_per_chunk;
+  return static_cast<__nv_bfloat16*>(p.out_chunks.p[j]) + static_cast<long long>(row - j * p.rows_per_chunk) * p.d;
+}
+
+// ----------------------------------------------------------------------------- LayerNorm forward
+
+// WPR warps per row, the row held in registers: V 16-byte vectors per lane
+// (d = 256 V WPR).  Mean first, then the biased variance from the centred
+// values (two passes over registers), rstd = rsqrt(var + eps), one bf16
+// rounding at the output.
+template <int V, int WPR>
+__device__ __forceinline__ float row_sum(float v, float* red, int warp) {
+  v = warp_sum(v);
+  if constexpr (WPR == 1) {
+    return v;
+  } else {
+    if ((threadIdx.x & 31) == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    const int first = warp - warp % WPR;
+#pragma unroll
+    for (int k = 0; k < WPR; ++k) t += red[first + k];
+    __syncthreads();
+    return t;
+  }
+}
+
+template <int V, int WPR>
+__global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
+  __shared__ float red[4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (4 / WPR) + warp / WPR;
+  const int sub = warp % WPR;
+  const bool valid = row < p.rows;
+  const uint4* src = valid ? reinterpret_cast<const uint4*>(chunk_row(p, row)) : nullptr;
+  uint4 x[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) x[v] = valid ? __ldg(src + (sub * V + v) * 32 + lane) : make_uint4(0, 0, 0, 0);
+  float s = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    float f[8];
+    unpack8(x[v], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += f[e];
+  }
+  const float mean = row_sum<V, WPR>(s, red, warp) / static_cast<float>(p.d);
+  float q = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    float f[8];
+    unpack8(x[v], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float c = f[e] - mean;
+      q += c * c;
+    }
+  }
+  const float rstd = rsqrtf(row_sum<V, WPR>(q, red, warp) / static_cast<float>(p.d) + p.eps);
+  if (!valid) return;
+  const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
+  const uint4* b4 = reinterpret_cast<const uint4*>(p.beta);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + static_cast<long long>(row) * p.d);
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int idx = (sub * V + v) * 32 + lane;
+    float f[8], g[8], b[8], o[8];
+    unpack8(x[v], f);
+    unpack8(__ldg(g4 + idx), g);
+    unpack8(__ldg(b4 + idx), b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+    dst[idx] = pack8(o);
+  }
+}
+
+// Any d that is a multiple of 8: one warp per row, three sweeps over the row
+// (the second and third hit L1/L2).
+__global__ void __launch_bounds__(128) k_layernorm_fwd_any(const RowParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= p.rows) return;
+  const int nv = p.d / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(chunk_row(p, row));
+  float s = 0.f;
+  for (int v = lane; v < nv; v += 32) {
+    float f[8];
+    unpack8(__ldg(src + v), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += f[e];
+  }
+  const float mean = warp_sum(s) / static_cast<float>(p.d);
+  float q = 0.f;
+  for (int v = lane; v < nv; v += 32) {
+    float f[8];
+    unpack8(__ldg(src + v), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float c = f[e] - mean;
+      q += c * c;
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(q) / static_cast<float>(p.d) + p.eps);
+  const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
+  const uint4* b4 = reinterpret_cast<const uint4*>(p.beta);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + static_cast<long long>(row) * p.d);
+  for (int v = lane; v < nv; v += 32) {
+    float f[8], g[8], b[8], o[8];
+    unpack8(__ldg(src + v), f);
+    unpack8(__ldg(g4 + v), g);
+    unpack8(__ldg(b4 + v), b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+    dst[v] = pack8(o);
+  }
+}
+
+// ----------------------------------------------------------------------------- LayerNorm backward
+
+// Rows in groups of 8 (one warp each), grid-stride.  Phase 1 (per warp):
+// mean, rstd, mean(g) and mean(g * xhat) with g = dy * gamma, then
+// dx = rstd * (g - mean(g) - xhat * mean(g * xhat)) to the row's chunk.
+// Phase 2 (per thread, its own columns): dgamma += dy * xhat, dbeta += dy,
+// accumulated in shared memory without atomics; each block finally writes
+// its [2 d] partial row, which a fixed-order column sum reduces.
+constexpr int kLnBwdRowsPerGroup = 8;
+
+__global__ void __launch_bounds__(256) k_layernorm_bwd(const RowParams p) {
+  extern __shared__ float acc[];  // [2 d]: dgamma, dbeta
+  __shared__ float s_mean[kLnBwdRowsPerGroup], s_rstd[kLnBwdRowsPerGroup];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv = p.d / 8;
+  for (int c = threadIdx.x; c < 2 * p.d; c += blockDim.x) acc[c] = 0.f;
+  const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
+  const int groups = (p.rows + kLnBwdRowsPerGroup - 1) / kLnBwdRowsPerGroup;
+  for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+    const int row = grp * kLnBwdRowsPerGroup + warp;
+    if (row < p.rows) {
+      const uint4* x4 = reinterpret_cast<const uint4*>(chunk_row(p, row));
+      const uint4* dy4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.src) +
+                                                        static_cast<long long>(row) * p.d);
+      float s = 0.f;
+      for (int v = lane; v < nv; v += 32) {
+        float f[8];
+        unpack8(__ldg(x4 + v), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += f[e];
+      }
+      const float mean = warp_sum(s) / static_cast<float>(p.d);
+      float q = 0.f, sg = 0.f, sgc = 0.f;
+      for (int v = lane; v < nv; v += 32) {
+        float f[8], dy[8], g[8];
+        unpack8(__ldg(x4 + v), f);
+        unpack8(__ldg(dy4 + v), dy);
+        unpack8(__ldg(g4 + v), g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float c = f[e] - mean;
+          const float gg = dy[e] * g[e];
+          q += c * c;
+          sg += gg;
+          sgc += gg * c;
+        }
+      }
+      q = warp_sum(q);
+      sg = warp_sum(sg);
+      sgc = warp_sum(sgc);
+      const float rstd = rsqrtf(q / static_cast<float>(p.d) + p.eps);
+      const float m1 = sg / static_cast<float>(p.d);
+      const float m2 = rstd * sgc / static_cast<float>(p.d);
+      uint4* dx4 = reinterpret_cast<uint4*>(out_chunk_row(p, row));
+      for (int v = lane; v < nv; v += 32) {
+        float f[8], dy[8], g[8], o[8];
+        unpack8(__ldg(x4 + v), f);
+        unpack8(__ldg(dy4 + v), dy);
+        unpack8(__ldg(g4 + v), g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = rstd * (dy[e] * g[e] - m1 - (f[e] - mean) * rstd * m2);
+        dx4[v] = pack8(o);
+      }
+      if (lane == 0) {
+        s_mean[warp] = mean;
+        s_rstd[warp] = rstd;
+      }
+    }
+    __syncthreads();
+    const int rows_here = min(kLnBwdRowsPerGroup, p.rows - grp * kLnBwdRowsPerGroup);
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float dg[8], db[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dg[e] = db[e] = 0.f;
+      for (int r = 0; r < rows_here; ++r) {
+        const int row = grp * kLnBwdRowsPerGroup + r;
+        float f[8], dy[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(chunk_row(p, row)) + v), f);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.src) +
+                                                     static_cast<long long>(row) * p.d) + v), dy);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          dg[e] += dy[e] * (f[e] - s_mean[r]) * s_rstd[r];
+          db[e] += dy[e];
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[v * 8 + e] += dg[e];
+        acc[p.d + v * 8 + e] += db[e];
+      }
+    }
+    __syncthreads();
+  }
+  for (int c = threadIdx.x; c < 2 * p.d; c += blockDim.x)
+    p.partial[static_cast<long long>(blockIdx.x) * 2 * p.d + c] = acc[c];
+}
+
+// ----------------------------------------------------------------------------- reduce-scatter, gather, column sum
+
+// Y_chunk_j[r] = bf16(sum_{i<N} P_i[j T/N + r]) in fp32, shard 0 first.
+__global__ void __launch_bounds__(256) k_reduce_scatter(const RowParams p) {
+  const long long nvec = static_cast<long long>(p.rows) * p.d / 8;
+  const uint4* src = static_cast<const uint4*>(p.src);
+  const long long sstride = p.shard_stride / 8;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nvec;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float a[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[e] = 0.f;
+    for (int s = 0; s < p.n_chunks; ++s) {
+      float f[8];
+      unpack8(__ldg(src + s * sstride + i), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[e] += f[e];
+    }
+    const long long el = i * 8;
+    const int row = static_cast<int>(el / p.d);
+    const int col = static_cast<int>(el - static_cast<long long>(row) * p.d);
+    reinterpret_cast<uint4*>(out_chunk_row(p, row) + col)[0] = pack8(a);
+  }
+}
+
+// Contiguous dst[T x d] <- the N chunk pointers.
+__global__ void __launch_bounds__(256) k_gather_rows(const RowParams p) {
+  const long long nvec = static_cast<long long>(p.rows) * p.d / 8;
+  uint4* dst = static_cast<uint4*>(p.dst);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nvec;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long el = i * 8;
+    const int row = static_cast<int>(el / p.d);
+    const int col = static_cast<int>(el - static_cast<long long>(row) * p.d);
+    dst[i] = __ldg(reinterpret_cast<const uint4*>(chunk_row(p, row) + col));
+  }
+}
+
+__global__ void __launch_bounds__(256) k_column_sum(const float* partial, int rows, int cols, long long stride,
+                                                     void* out, int out_bf16) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float s = 0.f;
+  for (int r = 0; r < rows; ++r) s += partial[static_cast<long long>(r) * stride + c];
+  if (out_bf16)
+    static_cast<__nv_bfloat16*>(out)[c] = __float2bfloat16_rn(s);
+  else
+    static_cast<float*>(out)[c] = s;
+}
+
+int stream_grid(long long work_items, int sm_count) {
+  const long long per = 256;
+  long long g = (work_items + per - 1) / per;
+  const long long cap = static_cast<long long>(sm_count) * 8;
+  if (g > cap) g = cap;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
+  (void)ctx;
+  if (r.rows <= 0) return cudaSuccess;
+  const int grid4 = (r.rows + 3) / 4;
+  const int grid2 = (r.rows + 1) / 2;
+  switch (r.d) {
+    case 256: k_layernorm_fwd_reg<1, 1><<<grid4, 128, 0, s>>>(r); break;
+    case 512: k_layernorm_fwd_reg<2, 1><<<grid4, 128, 0, s>>>(r); break;
+    case 1024: k_layernorm_fwd_reg<4, 1><<<grid4, 128, 0, s>>>(r); break;
+    case 2048: k_layernorm_fwd_reg<8, 1><<<grid4, 128, 0, s>>>(r); break;
+    case 4096: k_layernorm_fwd_reg<16, 1><<<grid4, 128, 0, s>>>(r); break;
+    case 8192: k_layernorm_fwd_reg<16, 2><<<grid2, 128, 0, s>>>(r); break;
+    default: k_layernorm_fwd_any<<<grid4, 128, 0, s>>>(r); break;
+  }
+  return cudaGetLastError();
+}
+
+int layernorm_bwd_blocks(int rows, int max_blocks) {
+  const int groups = (rows + kLnBwdRowsPerGroup - 1) / kLnBwdRowsPerGroup;
+  return groups < max_blocks ? (groups < 1 ? 1 : groups) : max_blocks;
+}
+
+cudaError_t launch_layernorm_bwd(const RowParams& r, int max_blocks, float* dgamma, float* dbeta, cudaStream_t s) {
+  if (r.rows <= 0) return cudaSuccess;
+  const int grid = layernorm_bwd_blocks(r.rows, max_blocks);
+  const size_t smem = static_cast<size_t>(2) * r.d * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_layernorm_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k_layernorm_bwd<<<grid, 256, smem, s>>>(r);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // dgamma = column sums of partial[:, 0:d], dbeta = column sums of partial[:, d:2d]
+  const int cb = (r.d + 255) / 256;
+  k_column_sum<<<cb, 256, 0, s>>>(r.partial, grid, r.d, 2LL * r.d, dgamma, 0);
+  k_column_sum<<<cb, 256, 0, s>>>(r.partial + r.d, grid, r.d, 2LL * r.d, dbeta, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_scatter(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
+  if (r.rows <= 0) return cudaSuccess;
+  k_reduce_scatter<<<stream_grid(static_cast<long long>(r.rows) * r.d / 8, ctx.sm_count), 256, 0, s>>>(r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
+  if (r.rows <= 0) return cudaSuccess;
+  k_gather_rows<<<stream_grid(static_cast<long long>(r.rows) * r.d / 8, ctx.sm_count), 256, 0, s>>>(r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s) {
+  if (cols <= 0 || out == nullptr) return cudaSuccess;
+  k_column_sum<<<(cols + 255) / 256, 256, 0, s>>>(partial, rows, cols, cols, out, out_bf16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace tpmlp

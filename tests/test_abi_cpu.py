@@ -1,0 +1,120 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+``include/tpmlp.h`` declares, and its host-side validation and workspace
+arithmetic behave as documented.  No call here reaches the CUDA runtime: each
+one is rejected by argument checks or is pure host arithmetic."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tensor_transformer_mlp_tp_gb300 import binding, build, inputs
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tpmlp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"TPMLP_API\s+[\w\s\*]+?\b(tpmlp_\w+)\s*\(", text)
+
+
+def test_header_declares_the_block_calls():
+    names = declared_functions()
+    for required in ("tpmlp_forward", "tpmlp_sp_forward", "tpmlp_backward", "tpmlp_sp_backward",
+                     "tpmlp_workspace_size", "tpmlp_get_device_status", "tpmlp_status_string"):
+        assert required in names
+    assert len(names) == len(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in binding._SIGS, f"binding lacks {name}"
+
+
+def test_only_abi_symbols_exported(lib):
+    # the statically linked CUDA runtime stays private to the library
+    with pytest.raises(AttributeError):
+        getattr(lib, "cudaLaunchKernel")
+
+
+def test_status_strings(lib):
+    assert binding.status_string(binding.OK) == "ok"
+    assert binding.status_string(binding.ERR_TIMEOUT) == "device wait timed out"
+    assert binding.status_string(99) == "unknown status"
+
+
+def _ws(shape, op):
+    n = ctypes.c_size_t(0)
+    st = binding.lib().tpmlp_workspace_size(ctypes.byref(shape), op, ctypes.byref(n))
+    return st, n.value
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_workspace_sizes(lib):
+    for w in inputs.WORKLOADS.values():
+        if w.dtype != "bf16":
+            continue
+        s = binding.make_shape(w.T, w.d, w.F, w.N)
+        st, fwd = _ws(s, binding.OP_FWD)
+        assert st == binding.OK and fwd == _r256(w.T * w.F * 2)          # H, bf16
+        st, spf = _ws(s, binding.OP_SP_FWD)
+        assert st == binding.OK and spf == fwd + _r256(w.T * w.d * 2)    # + gathered LayerNorm output
+        st, spp = _ws(s, binding.OP_SP_FWD_PARTIALS)
+        assert st == binding.OK and spp == spf + _r256(w.N * w.T * w.d * 2)
+        st, bwd = _ws(s, binding.OP_BWD)
+        assert st == binding.OK and bwd >= 3 * w.T * w.F * 2
+        st, spb = _ws(s, binding.OP_SP_BWD)
+        assert st == binding.OK and spb > bwd
+    s = binding.make_shape(128, 64, 256, 2, binding.FP32)
+    assert _ws(s, binding.OP_FWD) == (binding.OK, 128 * 256 * 4)
+    assert _ws(s, binding.OP_SP_FWD)[0] == binding.ERR_UNSUPPORTED
+    assert _ws(binding.make_shape(0, 64, 256, 2), binding.OP_FWD) == (binding.OK, 0)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(tokens=-1), dict(d=0), dict(ffn=0), dict(n_shards=0), dict(n_shards=65), dict(ffn=100, n_shards=3),
+    dict(d=60), dict(ffn=100, n_shards=5), dict(dtype=7)])
+def test_invalid_shapes(lib, bad):
+    kw = dict(tokens=256, d=64, ffn=256, n_shards=2, dtype=binding.BF16)
+    kw.update(bad)
+    s = binding.make_shape(kw["tokens"], kw["d"], kw["ffn"], kw["n_shards"], kw["dtype"])
+    assert _ws(s, binding.OP_FWD)[0] == binding.ERR_INVALID_ARG
+
+
+def test_sp_requires_divisible_tokens(lib):
+    s = binding.make_shape(100, 64, 256, 8)
+    assert _ws(s, binding.OP_SP_FWD)[0] == binding.ERR_INVALID_ARG
+    assert _ws(s, binding.OP_FWD)[0] == binding.OK
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    L = binding.lib()
+    s = binding.make_shape(256, 64, 256, 2)
+    good = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    ws = ctypes.c_void_p(1 << 24)
+    args = lambda X, A, B, Y: (X, A, B, None, ctypes.byref(s), Y, None, ws, 1 << 30, None)
+    assert L.tpmlp_forward(*args(None, good, good, good)) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_forward(*args(good, good, good, None)) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_forward(*args(odd, good, good, good)) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_forward(good, good, good, None, ctypes.byref(s), good, None, ws, 16, None) == binding.ERR_WORKSPACE
+    assert L.tpmlp_gemm2_partials(good, good, ctypes.byref(binding.make_shape(256, 64, 96, 2)), good, None) \
+        == binding.ERR_UNSUPPORTED                                      # (ffn / N) % 64 != 0
+    assert L.tpmlp_selftest_wait_timeout(0, None) == binding.ERR_INVALID_ARG
+
+
+def test_empty_batch_needs_no_device(lib):
+    L = binding.lib()
+    s = binding.make_shape(0, 64, 256, 2)
+    good = ctypes.c_void_p(1 << 20)
+    assert L.tpmlp_forward(good, good, good, None, ctypes.byref(s), good, None, None, 0, None) == binding.OK
