@@ -1,0 +1,482 @@
+"""Throughput of the tensor-parallel MLP block on GB300 (one JSON line on stdout).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole hot path over one batch: for the default
+workload ``sp_block_fwd_bwd`` (T=8192 tokens in N=8 sequence chunks, d=4096,
+F=16384) that is LayerNorm+gather, the column-parallel GEMM with bias+GeLU,
+the row-parallel GEMM with the in-kernel shard reduction and fused
+reduce-scatter store, then the backward: LayerNorm recompute, dY B^T * GeLU',
+dB = H^T dY, dA = Xg^T dHpre, dXg = dHpre A^T and the LayerNorm backward.
+Every kernel is timed with CUDA events on the stream it is launched on.
+``e2e`` repeats the step through the block calls of the C ABI with the
+activations copied from / to pinned host memory inside the timed region.
+The ``reference`` implementation is the CPU fp64 oracle on a bounded sample
+of the same workload.
+"""
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tensor_transformer_mlp_tp_gb300 import inputs  # noqa: E402
+
+METRIC = "TP-MLP block bf16 TFLOP/s and tokens/s at 1 GB300; % of dense BF16 / HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def useful_flops(w):
+    """Algorithmic GEMM flops of one step: 2 T d F per GEMM; 2 forward GEMMs, 4 backward GEMMs."""
+    per_gemm = 2.0 * w.T * w.d * w.F
+    return per_gemm * (6 if w.backward else 2)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="tpmlp_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) leg
+
+_SAMPLE_CACHE = {}
+
+
+def _cached_draw(w, name, seed, rows=None):
+    key = (w.name, name, seed, None if rows is None else (int(rows[0]), len(rows)))
+    if key not in _SAMPLE_CACHE:
+        _SAMPLE_CACHE[key] = inputs.draw(w, name, seed, rows=rows)
+    return _SAMPLE_CACHE[key]
+
+
+def oracle_sample(w, seed=0, tokens=None):
+    """Run the oracle on `tokens` rows of workload `w` (for the SP block: the first tokens/N rows of every
+    chunk) with the full weights; returns (seconds of oracle work, tokens, flops)."""
+    import oracle
+
+    N = w.N
+    tokens = tokens or w.T
+    rows_per_chunk = max(1, tokens // N) if w.sp else tokens
+    tok = rows_per_chunk * N if w.sp else tokens
+    if w.sp:
+        # the same chunk-local rows of every chunk
+        sel = np.concatenate([np.arange(j * w.rows_per_chunk, j * w.rows_per_chunk + rows_per_chunk)
+                              for j in range(N)])
+    else:
+        sel = np.arange(tok)
+    X = _cached_draw(w, "X", seed, rows=sel)[1]
+    A = _cached_draw(w, "A", seed)[1]
+    B = _cached_draw(w, "B", seed)[1]
+    b = _cached_draw(w, "bias", seed)
+    b = None if b is None else b[1]
+    if w.sp:
+        g = _cached_draw(w, "gamma", seed)[1]
+        be = _cached_draw(w, "beta", seed)[1]
+        chunks = [X[j * rows_per_chunk:(j + 1) * rows_per_chunk] for j in range(N)]
+        dyc = None
+        if w.backward:
+            dY = _cached_draw(w, "dY", seed, rows=sel)[1]
+            dyc = [dY[j * rows_per_chunk:(j + 1) * rows_per_chunk] for j in range(N)]
+        t0 = time.perf_counter()
+        oracle.sp_forward(chunks, g, be, 1e-5, A, B, b, N)
+        if w.backward:
+            oracle.sp_backward(chunks, g, be, 1e-5, A, B, b, dyc, N)
+    else:
+        t0 = time.perf_counter()
+        oracle.mlp_tp(X, A, B, b, N)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * tok * w.d * w.F * (6 if w.backward else 2)
+    return dt, tok, flops
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    tokens = args.oracle_tokens
+    for _ in range(args.warmup):
+        oracle_sample(w, tokens=tokens)
+    times, tok, flops = [], 0, 0.0
+    for _ in range(args.steps):
+        dt, tok, flops = oracle_sample(w, tokens=tokens)
+        times.append(dt)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    sample = (f"{tok} of {w.T} tokens ({tok // w.N if w.sp else tok} rows per chunk) with the full "
+              f"d={w.d}, F={w.F} weights, numpy float64 (BLAS matmul on {cores} threads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "tokens_per_s": tok * args.steps / total,
+            "config": {"workload": w.name, "tokens": w.T, "d": w.d, "ffn": w.F, "n_shards": w.N,
+                       "sample_tokens": tok},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU leg
+
+class Step:
+    """Device buffers of one workload and the sequence of ABI step calls of one step."""
+
+    def __init__(self, w, torch, binding, seed=0):
+        self.w, self.torch, self.b = w, torch, binding
+        dev = "cuda"
+        T, d, F, N = w.T, w.d, w.F, w.N
+
+        def up(name):
+            r = inputs.draw(w, name, seed)
+            if r is None:
+                return None
+            return torch.from_numpy(np.ascontiguousarray(r[0]).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        self.X = up("X")
+        self.A = up("A")
+        self.B = up("B")
+        self.bias = up("bias")
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.H = torch.empty(T, F, **bf)
+        self.Y = torch.empty(T, d, **bf)
+        self.rows = T // N
+        if w.sp:
+            self.gamma, self.beta = up("gamma"), up("beta")
+            self.Xg = torch.empty(T, d, **bf)
+            self.Xc = list(self.X.split(self.rows))
+            self.Yc = list(self.Y.split(self.rows))
+        if w.backward:
+            self.dY = up("dY")
+            self.dYc = list(self.dY.split(self.rows))
+            self.Hpre = torch.empty(T, F, **bf)
+            self.dHpre = torch.empty(T, F, **bf)
+            self.Hb = torch.empty(T, F, **bf)
+            self.dXg = torch.empty(T, d, **bf)
+            self.dX = torch.empty(T, d, **bf)
+            self.dXc = list(self.dX.split(self.rows))
+            self.dA = torch.empty(d, F, **bf)
+            self.dB = torch.empty(F, d, **bf)
+            self.dgamma = torch.empty(d, dtype=torch.float32, device=dev)
+            self.dbeta = torch.empty(d, dtype=torch.float32, device=dev)
+            self.lnws = binding.workspace(binding.make_shape(T, d, F, N), binding.OP_LN_BWD)
+
+    def kernels(self):
+        """(name, launches, algorithmic work per launch, unit) of each timed segment of a step."""
+        w = self.w
+        g = 2.0 * w.T * w.d * w.F
+        ln = 2.0 * w.T * w.d * 2          # read x, write y (bf16)
+        segs = []
+        if w.sp:
+            segs.append(("layernorm_gather", 1, ln, "B"))
+        segs += [("gemm1_bias_gelu", 1, g, "F"), ("gemm2_shard_accum" + ("_rs_store" if w.sp else ""), 1, g, "F")]
+        if w.backward:
+            segs += [("layernorm_recompute", 1, ln, "B"), ("gemm_dh_geluprime", 1, g, "F"), ("gemm_wgrad_b", 1, g, "F"),
+                     ("gemm_wgrad_a", 1, g, "F"), ("gemm_dx_shard_accum", 1, g, "F"),
+                     ("layernorm_backward", 3, 3.0 * w.T * w.d * 2, "B")]
+        return segs
+
+    def run(self, ev=None):
+        """Launch one step; if `ev` (a list of events) is given, record ev[i] after segment i (ev[0] before)."""
+        b, w, N = self.b, self.w, self.w.N
+        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+        i = 0
+        rec(i)
+        if w.sp:
+            b.tpmlp_layernorm_gather(self.Xc, self.gamma, self.beta, N, self.Xg)
+            i += 1; rec(i)
+            x_in = self.Xg
+        else:
+            x_in = self.X
+        b.tpmlp_gemm1_bias_gelu(x_in, self.A, self.bias, N, self.H, self.Hpre if w.backward else None)
+        i += 1; rec(i)
+        if w.sp:
+            b.tpmlp_gemm2_shard_accum(self.H, self.B, N, Y_chunks=self.Yc)
+        else:
+            b.tpmlp_gemm2_shard_accum(self.H, self.B, N, Y=self.Y)
+        i += 1; rec(i)
+        if w.backward:
+            b.tpmlp_layernorm_gather(self.Xc, self.gamma, self.beta, N, self.Xg)
+            i += 1; rec(i)
+            b.tpmlp_gemm_dh_geluprime(self.dY, self.B, self.Hpre, N, self.dHpre, self.Hb)
+            i += 1; rec(i)
+            b.tpmlp_gemm_wgrad_b(self.Hb, self.dY, N, self.dB)
+            i += 1; rec(i)
+            b.tpmlp_gemm_wgrad_a(self.Xg, self.dHpre, N, self.dA)
+            i += 1; rec(i)
+            b.tpmlp_gemm_dx_shard_accum(self.dHpre, self.A, N, self.dXg)
+            i += 1; rec(i)
+            b.tpmlp_layernorm_backward(self.Xc, self.gamma, self.dXg, N, self.dXc, self.dgamma, self.dbeta,
+                                       ws=self.lnws)
+            i += 1; rec(i)
+        return i
+
+    def launches_per_step(self):
+        return sum(n for _, n, _, _ in self.kernels())
+
+
+def run_e2e(step, args, torch, binding):
+    """The same step through the block calls, activations from/to pinned host memory inside the timed region."""
+    w = step.w
+    N = w.N
+    X_h = step.X.cpu().pin_memory()
+    Y_h = torch.empty_like(step.Y, device="cpu").pin_memory()
+    h2d = X_h.numel() * 2
+    d2h = Y_h.numel() * 2
+    if w.backward:
+        dY_h = step.dY.cpu().pin_memory()
+        dX_h = torch.empty_like(step.dX, device="cpu").pin_memory()
+        h2d += dY_h.numel() * 2
+        d2h += dX_h.numel() * 2
+    Xd = torch.empty_like(step.X)
+    dYd = torch.empty_like(step.dY) if w.backward else None
+    shape = binding.make_shape(w.T, w.d, w.F, N)
+    ws_f = binding.workspace(shape, binding.OP_SP_FWD if w.sp else binding.OP_FWD)
+    ws_b = binding.workspace(shape, binding.OP_SP_BWD) if w.backward else None
+
+    def one():
+        Xd.copy_(X_h, non_blocking=True)
+        if w.sp:
+            binding.tpmlp_sp_forward(list(Xd.split(step.rows)), step.gamma, step.beta, step.A, step.B, N, step.Yc,
+                                     bias=step.bias, Hpre_out=step.Hpre if w.backward else None, ws=ws_f)
+        else:
+            binding.tpmlp_forward(Xd, step.A, step.B, step.bias, N, step.Y, ws=ws_f)
+        Y_h.copy_(step.Y, non_blocking=True)
+        if w.backward:
+            dYd.copy_(dY_h, non_blocking=True)
+            binding.tpmlp_sp_backward(list(Xd.split(step.rows)), step.gamma, step.beta, step.A, step.B, step.Hpre,
+                                      list(dYd.split(step.rows)), N, step.dXc, step.dA, step.dB, step.dgamma,
+                                      step.dbeta, bias=step.bias, ws=ws_b)
+            dX_h.copy_(step.dX, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return ms, h2d, d2h
+
+
+def run_ours(args, w):
+    import torch
+
+    from tensor_transformer_mlp_tp_gb300 import binding, build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(binding.lib_path()):
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.lib()
+
+    step = Step(w, torch, binding)
+    segs = step.kernels()
+    nseg = len(segs)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    st, site = binding.tpmlp_get_device_status()
+    if st != binding.OK:
+        raise RuntimeError(f"device status after warm-up: {binding.status_string(st)} (site {site})")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            step.run(events[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    seg_ms = [0.0] * nseg
+    for k in range(args.steps):
+        for i in range(nseg):
+            seg_ms[i] += events[k][i].elapsed_time(events[k][i + 1])
+    total_ms = events[0][0].elapsed_time(events[-1][nseg])
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st, site = binding.tpmlp_get_device_status()
+    if st != binding.OK:
+        raise RuntimeError(f"device status after timing: {binding.status_string(st)} (site {site})")
+
+    pk, pk_kind = peaks()
+    flops = useful_flops(w)
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    tokens_per_s = w.T * args.steps * world / (total_ms * 1e-3)
+
+    kern = {}
+    dom = None
+    for (name, nl, work, unit), ms in zip(segs, seg_ms):
+        avg = ms / args.steps
+        if unit == "F":
+            ach = work / (avg * 1e-3) / 1e12
+            peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+            kern[name] = {"ms": round(avg, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / peak, 3)}
+            if dom is None or avg > dom[1]:
+                dom = (name, avg, work, ach, peak)
+        else:
+            ach = work / (avg * 1e-3) / 1e9
+            kern[name] = {"ms": round(avg, 4), "GB/s": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 3),
+                          "launches": nl}
+    e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
+    st, site = binding.tpmlp_get_device_status()
+    if st != binding.OK:
+        raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
+    e2e_ms_t = torch.tensor([e2e_ms], dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(e2e_ms_t, op=dist.ReduceOp.MAX)
+    e2e_ms = float(e2e_ms_t.item())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, tok, fl = oracle_sample(w, tokens=args.oracle_tokens)
+        cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "tokens_per_s": tok / dt, "seconds": round(dt, 2),
+               "sample": f"{tok} of {w.T} tokens through the fp64 oracle with the full d={w.d}, F={w.F} weights "
+                         f"(numpy float64, BLAS matmul on {cores} threads)"}
+    clocks = clk.summary()
+    if rank != 0:
+        dist.destroy_process_group() if dist is not None else None
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": round(tokens_per_s, 1),
+        "config": {"workload": w.name, "tokens": w.T, "batch": w.batch, "seq": w.seq, "d": w.d, "ffn": w.F,
+                   "n_shards": w.N, "sequence_parallel": w.sp, "backward": w.backward,
+                   "parallelism": f"tp{w.N} shards on one GPU" + (f", {world} replicas" if world > 1 else ""),
+                   "l2": "inputs larger than L2 (weights alone 2 x d x F x 2 bytes)",
+                   "host_wall_s": round(wall, 3)},
+        "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": round(dom[3], 1), "peak": dom[4],
+                     "unit": "TFLOP/s", "frac": round(dom[3] / dom[4], 3), "traffic": None,
+                     "peak_kind": f"{pk_kind} bf16 sustained"},
+        "kernels": kern,
+        "e2e": {"value": round(flops * args.steps * world / (e2e_ms * args.steps * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "what": "block calls (tpmlp_sp_forward/backward) with X, dY copied from pinned host memory and Y, dX "
+                        "copied back each step; weights and their gradients stay in HBM"},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sp_block_fwd_bwd", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--oracle-tokens", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = inputs.WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        raise SystemExit("bench.py measures the bf16 workloads")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

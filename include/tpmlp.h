@@ -32,7 +32,9 @@
  *    ffn % N != 0, and for bf16: d % 8 != 0, (ffn / N) % 8 != 0, a device
  *    pointer not 16-byte aligned; for the sequence-parallel calls T % N != 0;
  *    a workspace smaller than required (TPMLP_ERR_WORKSPACE).  tokens == 0 is
- *    a valid empty call that launches nothing.
+ *    a valid empty call: it launches nothing, leaves every output untouched
+ *    (weight gradients of an empty batch are the caller's zeros) and accepts
+ *    NULL pointers.
  *  - A failed launch returns TPMLP_ERR_CUDA.  Kernels never trap: every wait
  *    inside them is bounded (default 1 s, environment TPMLP_WAIT_TIMEOUT_MS);
  *    a wait that runs out records a device error word and the kernel exits,

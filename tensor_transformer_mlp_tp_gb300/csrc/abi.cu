@@ -381,6 +381,7 @@ tpmlp_status tpmlp_workspace_size(const tpmlp_shape* shape, int op, size_t* byte
   const bool bf16_only = op != TPMLP_OP_FWD;
   tpmlp_status st = check_shape(shape, sp, bf16_only);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (op < TPMLP_OP_FWD || op > TPMLP_OP_LN_BWD) return TPMLP_ERR_INVALID_ARG;
   *bytes = ws_bytes(shape, op);
   return TPMLP_OK;
@@ -412,9 +413,9 @@ tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const vo
                            void* Y, void* Hpre_out, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, false);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({X, A, B, Y}) || !opt_ok(bias) || !opt_ok(Hpre_out)) return TPMLP_ERR_INVALID_ARG;
   if (shape->dtype == TPMLP_FP32 && Hpre_out != nullptr) return TPMLP_ERR_UNSUPPORTED;
-  if (shape->tokens == 0) return TPMLP_OK;
   if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_FWD))
     return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;
@@ -438,12 +439,12 @@ tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, co
                               size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !opt_ok(Hpre_out)) return TPMLP_ERR_INVALID_ARG;
   if (!chunks_ok(X_chunks, shape->n_shards) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
   if (!(eps >= 0.f)) return TPMLP_ERR_INVALID_ARG;
   if (rs_mode != TPMLP_RS_FUSED && rs_mode != TPMLP_RS_PARTIALS) return TPMLP_ERR_INVALID_ARG;
   if (rs_mode == TPMLP_RS_PARTIALS && (shape->ffn / shape->n_shards) % kBK != 0) return TPMLP_ERR_UNSUPPORTED;
-  if (shape->tokens == 0) return TPMLP_OK;
   const int op = rs_mode == TPMLP_RS_FUSED ? TPMLP_OP_SP_FWD : TPMLP_OP_SP_FWD_PARTIALS;
   if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, op)) return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;
@@ -472,9 +473,9 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
                             void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({X, A, B, dY, dX, dA, dB}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(dbias))
     return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;  // dA, dB, dbias of an empty batch: left to the caller (zeros)
   if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_BWD))
     return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;
@@ -491,13 +492,13 @@ tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, c
                                size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({gamma, beta, A, B, dA, dB, dgamma, dbeta}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(dbias))
     return TPMLP_ERR_INVALID_ARG;
   const int n = shape->n_shards;
   if (!chunks_ok(X_chunks, n) || !chunks_ok(dY_chunks, n) || !chunks_ok(dX_chunks, n)) return TPMLP_ERR_INVALID_ARG;
   if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
   if (!(eps >= 0.f)) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_SP_BWD))
     return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;
@@ -540,8 +541,8 @@ tpmlp_status tpmlp_gemm1_bias_gelu(const void* X, const void* A, const void* bia
                                    void* Hpre, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({X, A, H}) || !opt_ok(bias) || !opt_ok(Hpre)) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_gemm1(c, X, A, bias, shape, H, Hpre, kEpiBiasGelu, reinterpret_cast<cudaStream_t>(stream)));
@@ -552,9 +553,9 @@ tpmlp_status tpmlp_gemm2_shard_accum(const void* H, const void* B, const tpmlp_s
   const bool chunked = Y_chunks != nullptr;
   tpmlp_status st = check_shape(shape, chunked, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({H, B})) return TPMLP_ERR_INVALID_ARG;
   if (chunked ? !chunks_ok(Y_chunks, shape->n_shards) : !ptrs_ok({Y})) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_gemm2(c, H, B, shape, Y, Y_chunks, reinterpret_cast<cudaStream_t>(stream)));
@@ -564,9 +565,9 @@ tpmlp_status tpmlp_gemm2_partials(const void* H, const void* B, const tpmlp_shap
                                   tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({H, B, P})) return TPMLP_ERR_INVALID_ARG;
   if ((shape->ffn / shape->n_shards) % kBK != 0) return TPMLP_ERR_UNSUPPORTED;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_gemm2_partials(c, H, B, shape, P, reinterpret_cast<cudaStream_t>(stream)));
@@ -576,8 +577,8 @@ tpmlp_status tpmlp_reduce_scatter(const void* P, const tpmlp_shape* shape, void*
                                   tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({P}) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_reduce_scatter(c, P, shape, Y_chunks, reinterpret_cast<cudaStream_t>(stream)));
@@ -587,9 +588,9 @@ tpmlp_status tpmlp_layernorm_gather(const void* const* X_chunks, const void* gam
                                     const tpmlp_shape* shape, void* Xg, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({gamma, beta, Xg}) || !chunks_ok(X_chunks, shape->n_shards) || !(eps >= 0.f))
     return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, reinterpret_cast<cudaStream_t>(stream)));
@@ -600,8 +601,8 @@ tpmlp_status tpmlp_gemm_dh_geluprime(const void* dY, const void* B, const void* 
                                      tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({dY, B, Hpre, dHpre, H}) || !opt_ok(dbias)) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   if (dbias != nullptr && (workspace == nullptr || !al16(workspace) ||
                            workspace_bytes < ws_bytes(shape, TPMLP_OP_DH_GELUPRIME)))
     return TPMLP_ERR_WORKSPACE;
@@ -615,8 +616,8 @@ tpmlp_status tpmlp_gemm_wgrad_b(const void* H, const void* dY, const tpmlp_shape
                                 tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({H, dY, dB})) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_wgrad_b(c, H, dY, shape, dB, reinterpret_cast<cudaStream_t>(stream)));
@@ -626,8 +627,8 @@ tpmlp_status tpmlp_gemm_wgrad_a(const void* X, const void* dHpre, const tpmlp_sh
                                 tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({X, dHpre, dA})) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_wgrad_a(c, X, dHpre, shape, dA, reinterpret_cast<cudaStream_t>(stream)));
@@ -637,8 +638,8 @@ tpmlp_status tpmlp_gemm_dx_shard_accum(const void* dHpre, const void* A, const t
                                        tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({dHpre, A, dX})) return TPMLP_ERR_INVALID_ARG;
-  if (shape->tokens == 0) return TPMLP_OK;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_dx(c, dHpre, A, shape, dX, reinterpret_cast<cudaStream_t>(stream)));
@@ -649,11 +650,11 @@ tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, const void* g
                                       void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({gamma, dXg, dgamma, dbeta}) || !chunks_ok(X_chunks, shape->n_shards) ||
       !chunks_ok(dX_chunks, shape->n_shards) || !(eps >= 0.f))
     return TPMLP_ERR_INVALID_ARG;
   if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
-  if (shape->tokens == 0) return TPMLP_OK;
   if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_LN_BWD))
     return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;

@@ -159,12 +159,18 @@ def test_reduce_scatter_random(N):
         assert Y[j].intact()
 
 
-@pytest.mark.parametrize("T,d,N", [(256, 128, 4), (384, 192, 8), (128, 256, 2)])
+@pytest.mark.parametrize("T,d,N", [(256, 128, 4), (384, 192, 8), (128, 256, 2), (384, 128, 8)])
 @pytest.mark.parametrize("rs_mode", [binding.RS_FUSED, binding.RS_PARTIALS])
 def test_sp_forward(T, d, N, rs_mode):
     w = inputs.small_workload(T, d, N, sp=True, bias=(0.0, 0.02))
     X, g, b, A, B, bias = _draw(w, "X", "gamma", "beta", "A", "B", "bias")
     Yc = [Guarded((T // N, d)) for _ in range(N)]
+    if rs_mode == binding.RS_PARTIALS and (4 * d // N) % 64:
+        with pytest.raises(binding.TpMlpError) as e:   # partials need 64-column shard widths
+            binding.tpmlp_sp_forward(list(dev(X[0]).split(T // N)), dev(g[0]), dev(b[0]), dev(A[0]), dev(B[0]), N,
+                                     [y.t for y in Yc], bias=dev(bias[0]), rs_mode=rs_mode)
+        assert e.value.status == binding.ERR_UNSUPPORTED
+        return
     binding.tpmlp_sp_forward(list(dev(X[0]).split(T // N)), dev(g[0]), dev(b[0]), dev(A[0]), dev(B[0]), N,
                              [y.t for y in Yc], bias=dev(bias[0]), rs_mode=rs_mode)
     torch.cuda.synchronize()
