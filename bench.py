@@ -71,7 +71,7 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -242,7 +242,7 @@ class Step:
         if w.backward:
             segs += [("layernorm_recompute", 1, ln, "B"), ("gemm_dh_geluprime", 1, g, "F"), ("gemm_wgrad_b", 1, g, "F"),
                      ("gemm_wgrad_a", 1, g, "F"), ("gemm_dx_shard_accum", 1, g, "F"),
-                     ("layernorm_backward", 3, 3.0 * w.T * w.d * 2, "B")]
+                     ("layernorm_backward", 2, 3.0 * w.T * w.d * 2, "B")]
         return segs
 
     def run(self, ev=None):
@@ -462,7 +462,7 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sp_block_fwd_bwd", choices=sorted(inputs.WORKLOADS))

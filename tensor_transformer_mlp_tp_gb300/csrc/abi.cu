@@ -117,7 +117,7 @@ struct Sizes {
   size_t td, tf, ptd, colsum, lnbwd;
 };
 
-constexpr int kLnBwdMaxBlocks = 512;
+constexpr int kLnBwdMaxBlocks = 304;  // 2 blocks per SM of a 152-SM GB300
 
 Sizes sizes_of(const tpmlp_shape* s) {
   const size_t T = static_cast<size_t>(s->tokens), d = static_cast<size_t>(s->d), F = static_cast<size_t>(s->ffn);

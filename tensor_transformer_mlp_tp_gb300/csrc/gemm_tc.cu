@@ -2,19 +2,21 @@
 // kernel instantiation for each (operand majorness, epilogue) the MLP uses.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
-#include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "launch.h"
 
 namespace tpmlp {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;       // single CTA: 48 KB per k-block
+constexpr int kPairStages = 6;   // CTA pair: 32 KB per CTA per k-block
 constexpr int kEpiWarps = 4;
 constexpr int kBN = 256;
-constexpr int kGroupM = 16;
+constexpr int kGroupM = 16;      // raster group, in 128-row blocks
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -55,6 +57,63 @@ cudaError_t run(const GemmParams& p, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Largest number of co-resident CTA pairs of `kern` on the current device (cached per device).
+template <typename K>
+int max_pairs(K kern, int smem, int threads, int dev_cache_slot, int* cache) {
+  if (cache[dev_cache_slot] > 0) return cache[dev_cache_slot];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) n = 1;
+  cache[dev_cache_slot] = n;
+  return n;
+}
+
+template <bool AMN, bool BMN, int EPI>
+cudaError_t run_pair(const GemmParams& p, cudaStream_t s) {
+  using S = PairShape<kBN, kPairStages, kEpiWarps>;
+  auto kern = k_gemm_tc2<kBN, AMN, BMN, EPI, kPairStages, kEpiWarps>;
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+  if (e != cudaSuccess) return e;
+  const int pairs = max_pairs(kern, S::kSmem, S::kThreads, dev & 63, cache);
+  const long long tiles = static_cast<long long>(p.m_blocks) * p.n_blocks * p.shards;
+  const int grid_pairs = static_cast<int>(tiles < pairs ? tiles : pairs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * grid_pairs);
+  cfg.blockDim = dim3(S::kThreads);
+  cfg.dynamicSmemBytes = S::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+bool pair_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("TPMLP_GEMM_PAIR");
+    return v == nullptr || v[0] != '0';
+  }();
+  return on;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s) {
@@ -64,19 +123,22 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
   // A operand (the M side): box of 128 rows x 64 k (K-major) or 64 m x 64 k rows (MN-major).
   bool ok = g.a.mn_major ? make_map(&p.tmA, g.a.ptr, g.M, g.K, g.a.ld, 64, kBK)
                          : make_map(&p.tmA, g.a.ptr, g.K, g.M, g.a.ld, kBK, kBM);
+  // CTA pairs whenever there are at least two 128-row blocks; each CTA then loads half of B's columns.
+  const bool pair = pair_enabled() && g.M > kBM;
+  const int b_rows = pair ? kBN / 2 : kBN;
   ok = ok && (g.b.mn_major ? make_map(&p.tmB, g.b.ptr, g.N, g.K, g.b.ld, 64, kBK)
-                           : make_map(&p.tmB, g.b.ptr, g.K, g.N, g.b.ld, kBK, kBN));
+                           : make_map(&p.tmB, g.b.ptr, g.K, g.N, g.b.ld, kBK, b_rows));
   if (!ok) return cudaErrorInvalidValue;
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
-  p.m_blocks = (g.M + kBM - 1) / kBM;
+  p.m_blocks = pair ? (g.M + 2 * kBM - 1) / (2 * kBM) : (g.M + kBM - 1) / kBM;
   p.n_blocks = (g.N + kBN - 1) / kBN;
   p.shards = g.shards < 1 ? 1 : g.shards;
   const int k_blocks = (g.K + kBK - 1) / kBK;
   if (p.shards > 1 && (k_blocks % p.shards != 0 || g.K % (p.shards * kBK) != 0)) return cudaErrorInvalidValue;
   p.k_blocks_per_shard = k_blocks / p.shards;
-  p.group_m = kGroupM;
+  p.group_m = pair ? kGroupM / 2 : kGroupM;
   p.out0 = g.out0;
   p.ld0 = g.ld0;
   p.out1 = g.out1;
@@ -94,6 +156,27 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
   const int grid = static_cast<int>(tiles < ctx.sm_count ? tiles : ctx.sm_count);
 
   const bool amn = g.a.mn_major, bmn = g.b.mn_major;
+  if (pair) {
+    switch (g.epi) {
+      case kEpiBiasGelu:
+        if (!amn && bmn) return run_pair<false, true, kEpiBiasGelu>(p, s);
+        break;
+      case kEpiBias:
+        if (!amn && bmn) return run_pair<false, true, kEpiBias>(p, s);
+        break;
+      case kEpiStore:
+        if (!amn && bmn) return run_pair<false, true, kEpiStore>(p, s);
+        if (amn && bmn) return run_pair<true, true, kEpiStore>(p, s);
+        if (!amn && !bmn) return run_pair<false, false, kEpiStore>(p, s);
+        break;
+      case kEpiDGelu:
+        if (!amn && !bmn) return run_pair<false, false, kEpiDGelu>(p, s);
+        break;
+      default:
+        break;
+    }
+    return cudaErrorNotSupported;
+  }
   switch (g.epi) {
     case kEpiBiasGelu:
       if (!amn && bmn) return run<false, true, kEpiBiasGelu>(p, grid, s);

@@ -81,6 +81,22 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* row_ptr, int col
   }
 }
 
+// Raw 64-byte load of 32 bf16 (zeros past N or for rows past M), unpacked later.
+__device__ __forceinline__ void load_raw32(const __nv_bfloat16* row_ptr, int col0, int N, bool ok, uint4 (&u)[4]) {
+  const uint4* s = reinterpret_cast<const uint4*>(row_ptr + col0);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) u[g] = (ok && col0 + 8 * g < N) ? __ldg(s + g) : make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void unpack_row32(const uint4 (&u)[4], float (&x)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float2 a = unpack_bf16x2(u[g].x), b = unpack_bf16x2(u[g].y), c = unpack_bf16x2(u[g].z), e = unpack_bf16x2(u[g].w);
+    x[8 * g + 0] = a.x; x[8 * g + 1] = a.y; x[8 * g + 2] = b.x; x[8 * g + 3] = b.y;
+    x[8 * g + 4] = c.x; x[8 * g + 5] = c.y; x[8 * g + 6] = e.x; x[8 * g + 7] = e.y;
+  }
+}
+
 // Sum of each of the 32 columns over the warp's 32 rows, by recursive halving
 // (31 shuffles).  Lane l ends with the sum of column l; the order of the
 // additions is fixed, so the result is deterministic.
@@ -99,8 +115,8 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], uint32_t lane)
 }
 
 template <int EPI>
-__device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32], int row, int col0, int shard,
-                                            int mb, int quad, uint32_t lane) {
+__device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32], const uint4 (&aux_raw)[4], int row,
+                                            int col0, int shard, int mb, int quad, uint32_t lane) {
   const bool row_ok = row < p.M;
   if constexpr (EPI == kEpiBiasGelu || EPI == kEpiBias) {
     if (p.bias != nullptr) {
@@ -129,20 +145,20 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       store_row32(dst, col0, p.N, v);
     }
   } else if constexpr (EPI == kEpiDGelu) {
+    // v = dH = dY B^T; aux = Hpre.  One erf per element serves both GeLU and GeLU'.
     float h[32];
-    if (row_ok) {
-      load_row32(static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row) * p.ld_aux, col0, p.N, h);
-    } else {
+    unpack_row32(aux_raw, h);
+    float g[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) h[i] = 0.f;
+    for (int i = 0; i < 32; ++i) {
+      const float x = h[i];
+      const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
+      const float pdf = 0.39894228040143268f * expf(-0.5f * x * x);
+      g[i] = x * cdf;
+      v[i] = row_ok ? v[i] * (cdf + x * pdf) : 0.f;
     }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = row_ok ? v[i] * gelu_prime_f(h[i]) : 0.f;
     if (row_ok) {
       store_row32(static_cast<__nv_bfloat16*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v);
-      float g[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = gelu_f(h[i]);
       store_row32(static_cast<__nv_bfloat16*>(p.out1) + static_cast<long long>(row) * p.ld1, col0, p.N, g);
     }
     if (p.colsum != nullptr) {
@@ -313,11 +329,25 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc(const __grid
       if (!ok) break;
       tc_fence_after_sync();
       const int row = mb * kBM + quad * 32 + static_cast<int>(lane);
+      const int c_begin = part * kColsPerPart, c_end = (part + 1) * kColsPerPart;
+      // The pre-activation operand of the GeLU' epilogue is fetched one chunk ahead.
+      const __nv_bfloat16* aux_row = nullptr;
+      uint4 aux_next[4] = {};
+      if constexpr (EPI == kEpiDGelu) {
+        aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
+        load_raw32(aux_row, nb * BN + c_begin, p.N, row < p.M, aux_next);
+      }
 #pragma unroll 1
-      for (int c = part * kColsPerPart; c < (part + 1) * kColsPerPart; c += 32) {
+      for (int c = c_begin; c < c_end; c += 32) {
+        uint4 aux_cur[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) aux_cur[g] = aux_next[g];
+        if constexpr (EPI == kEpiDGelu) {
+          if (c + 32 < c_end) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
+        }
         float v[32];
         tmem_load_32cols(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + c), v);
-        epilogue_32<EPI>(p, v, row, nb * BN + c, shard, mb, quad, lane);
+        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb, quad, lane);
       }
       tc_fence_before_sync();
       __syncwarp();

@@ -1,0 +1,242 @@
+// The tcgen05 GEMM on CTA pairs (cta_group::2): a cluster of two CTAs on two
+// SMs computes a 256 x BN output tile with one 256 x BN x 16 UMMA per k-step.
+//
+// CTA r of the pair (r = %cluster_ctarank) loads rows [128 r, 128 r + 128) of
+// the A tile and columns [r BN/2, (r+1) BN/2) of the B tile, 32 KB per k-block
+// for BN = 256 instead of the 48 KB a single CTA needs for a 128 x 256 tile:
+// a third less L2 -> SM traffic per flop and room for a deeper ring.  Each
+// CTA's TMEM holds its 128 rows of the accumulator (double-buffered), and each
+// CTA runs its own epilogue on them.
+//
+// Synchronisation:
+//   full[s]    lives in the even CTA; both CTAs' TMA copies count their bytes
+//              on it (cta_group::2 copies may signal the peer's barrier), the
+//              even CTA arms it with the pair's total.
+//   empty[s]   one per CTA; the MMA commit multicasts to both.
+//   tfull[a]   one per CTA; the MMA commit multicasts to both.
+//   tempty[a]  lives in the even CTA; every epilogue warp of both CTAs arrives.
+// Only the even CTA's warp 1 issues MMAs.  Waits are bounded as in the
+// single-CTA kernel; the pair meets at a cluster barrier before TMEM is
+// released and before either CTA exits (the even CTA's MMAs read the odd
+// CTA's shared memory).
+#pragma once
+
+#include "gemm_tc.cuh"
+
+namespace tpmlp {
+
+template <int BN, int STAGES, int EPI_WARPS>
+struct PairShape {
+  static_assert(BN == 128 || BN == 256, "BN");
+  static constexpr int kHalfN = BN / 2;
+  static constexpr int kATile = 128 * kBK * 2;     // this CTA's 128 rows of A
+  static constexpr int kBTile = kHalfN * kBK * 2;  // this CTA's half of the B columns
+  static constexpr int kStage = kATile + kBTile;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kThreads = 64 + 32 * EPI_WARPS;
+  static constexpr int kSmem = 1024 + STAGES * kStage + 256;
+};
+
+template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS>
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __grid_constant__ GemmParams p) {
+  using S = PairShape<BN, STAGES, EPI_WARPS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * S::kATile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * S::kBTile);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull + a, 1);
+      mbar_init(tempty + a, 2 * EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, S::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or copy
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  const int num_tiles = p.m_blocks * p.n_blocks * p.shards;  // m_blocks counts 256-row pair tiles
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ producer (both CTAs)
+      const uint64_t pol_a = policy_evict_normal();
+      const uint64_t pol_b = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;
+      bool ok = true;
+      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+        int shard, mb, nb;
+        tile_coords(p, tile, shard, mb, nb);
+        const int kb0 = shard * p.k_blocks_per_shard;
+        const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+        const int n0 = nb * BN + static_cast<int>(rank) * S::kHalfN;
+        for (int kb = 0; kb < p.k_blocks_per_shard; ++kb) {
+          if (!wait_bounded(empty + stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(full + stage, 2 * S::kStage);
+          const uint32_t bar = mapa_shared(smem_u32(full + stage), 0);
+          const int k0 = (kb0 + kb) * kBK;
+          uint8_t* a_dst = sA + stage * S::kATile;
+          uint8_t* b_dst = sB + stage * S::kBTile;
+          if constexpr (!A_MN) {
+            tma_load_2d_pair(a_dst, &p.tmA, bar, k0, m0, pol_a);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tma_load_2d_pair(a_dst + j * 64 * kBK * 2, &p.tmA, bar, m0 + 64 * j, k0, pol_a);
+          }
+          if constexpr (!B_MN) {
+            tma_load_2d_pair(b_dst, &p.tmB, bar, k0, n0, pol_b);
+          } else {
+#pragma unroll
+            for (int j = 0; j < S::kHalfN / 64; ++j)
+              tma_load_2d_pair(b_dst + j * 64 * kBK * 2, &p.tmB, bar, n0 + 64 * j, k0, pol_b);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Copies in flight must land before shared memory is released.  The even
+      // CTA's full barriers count both CTAs' bytes; the odd CTA is held at the
+      // closing cluster barrier until the even CTA has drained.
+      if (leader)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) wait_drain(full + s, (issued_parity >> s) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------------ MMA issuer (even CTA)
+      constexpr uint32_t idesc = idesc_bf16_f32(256, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!wait_bounded(tempty + acc, acc_phase ^ 1u, wc, kSiteMmaTmemEmpty)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.k_blocks_per_shard; ++kb) {
+          if (!wait_bounded(full + stage, phase, wc, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smem_u32(sA + stage * S::kATile);
+          const uint32_t b_base = smem_u32(sB + stage * S::kBTile);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a_base + k * 2048, 64 * kBK * 2, 1024)
+                                     : sdesc_sw128(a_base + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b_base + k * 2048, 64 * kBK * 2, 1024)
+                                     : sdesc_sw128(b_base + k * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair_multicast(empty + stage, 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(tfull + acc, 0x3);
+      }
+      umma_commit_pair(drain);
+      wait_drain(drain, 0, p.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------------- epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    constexpr int kSplit = EPI_WARPS / 4;
+    constexpr int kColsPerPart = BN / kSplit;
+    const int part = ew / 4;
+    int local = 0;
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+      int shard, mb, nb;
+      tile_coords(p, tile, shard, mb, nb);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tfull + acc, acc_phase, wc, kSiteEpiTmemFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int mb128 = mb * 2 + static_cast<int>(rank);
+      const int row = mb128 * 128 + quad * 32 + static_cast<int>(lane);
+      const int c_begin = part * kColsPerPart, c_end = (part + 1) * kColsPerPart;
+      const __nv_bfloat16* aux_row = nullptr;
+      uint4 aux_next[4] = {};
+      if constexpr (EPI == kEpiDGelu) {
+        aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
+        load_raw32(aux_row, nb * BN + c_begin, p.N, row < p.M, aux_next);
+      }
+#pragma unroll 1
+      for (int c = c_begin; c < c_end; c += 32) {
+        uint4 aux_cur[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) aux_cur[g] = aux_next[g];
+        if constexpr (EPI == kEpiDGelu) {
+          if (c + 32 < c_end) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
+        }
+        float v[32];
+        tmem_load_32cols(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + c), v);
+        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
+    }
+  }
+
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, S::kTmemCols);
+  }
+}
+
+}  // namespace tpmlp

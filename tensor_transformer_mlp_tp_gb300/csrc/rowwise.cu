@@ -289,16 +289,31 @@ __global__ void __launch_bounds__(256) k_gather_rows(const RowParams p) {
   }
 }
 
-__global__ void __launch_bounds__(256) k_column_sum(const float* partial, int rows, int cols, long long stride,
-                                                     void* out, int out_bf16) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
+// out[c] = sum over r < rows of partial[r * stride + c], for c < cols; columns c < split go to
+// out0[c], the rest to out1[c - split].  32 columns per block, rows split over the 8 warps and
+// combined in warp order: a fixed summation order, so the result is deterministic.
+__global__ void __launch_bounds__(256) k_column_sum(const float* __restrict__ partial, int rows, int cols,
+                                                     long long stride, void* out0, void* out1, int split,
+                                                     int out_bf16) {
+  __shared__ float red[8][33];
+  const int lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int r = 0; r < rows; ++r) s += partial[static_cast<long long>(r) * stride + c];
-  if (out_bf16)
-    static_cast<__nv_bfloat16*>(out)[c] = __float2bfloat16_rn(s);
-  else
-    static_cast<float*>(out)[c] = s;
+  if (c < cols)
+    for (int r = slice; r < rows; r += 8) s += partial[static_cast<long long>(r) * stride + c];
+  red[slice][lane] = s;
+  __syncthreads();
+  if (slice == 0 && c < cols) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += red[k][lane];
+    void* out = c < split ? out0 : out1;
+    const int oc = c < split ? c : c - split;
+    if (out_bf16)
+      static_cast<__nv_bfloat16*>(out)[oc] = __float2bfloat16_rn(t);
+    else
+      static_cast<float*>(out)[oc] = t;
+  }
 }
 
 int stream_grid(long long work_items, int sm_count) {
@@ -344,9 +359,7 @@ cudaError_t launch_layernorm_bwd(const RowParams& r, int max_blocks, float* dgam
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // dgamma = column sums of partial[:, 0:d], dbeta = column sums of partial[:, d:2d]
-  const int cb = (r.d + 255) / 256;
-  k_column_sum<<<cb, 256, 0, s>>>(r.partial, grid, r.d, 2LL * r.d, dgamma, 0);
-  k_column_sum<<<cb, 256, 0, s>>>(r.partial + r.d, grid, r.d, 2LL * r.d, dbeta, 0);
+  k_column_sum<<<(2 * r.d + 31) / 32, 256, 0, s>>>(r.partial, grid, 2 * r.d, 2LL * r.d, dgamma, dbeta, r.d, 0);
   return cudaGetLastError();
 }
 
@@ -364,7 +377,7 @@ cudaError_t launch_gather_rows(const RowParams& r, const DeviceCtx& ctx, cudaStr
 
 cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s) {
   if (cols <= 0 || out == nullptr) return cudaSuccess;
-  k_column_sum<<<(cols + 255) / 256, 256, 0, s>>>(partial, rows, cols, cols, out, out_bf16 ? 1 : 0);
+  k_column_sum<<<(cols + 31) / 32, 256, 0, s>>>(partial, rows, cols, cols, out, out, cols, out_bf16 ? 1 : 0);
   return cudaGetLastError();
 }
 
