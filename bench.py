@@ -56,7 +56,7 @@ def useful_flops(w):
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -86,7 +86,17 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self):
+    @staticmethod
+    def _epoch(stamp):
+        import datetime
+        try:
+            return time.mktime(datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timetuple()) + \
+                float("0." + stamp.rsplit(".", 1)[1])
+        except (ValueError, IndexError):
+            return None
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in samples taken between t0 and t1 (epoch seconds)."""
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
@@ -96,6 +106,9 @@ class ClockSampler:
                 if len(parts) >= 9:
                     rows.append(parts)
         os.unlink(self.path)
+        if t0 is not None:
+            inside = [r for r in rows if (lambda e: e is not None and t0 - 0.1 <= e <= t1 + 0.1)(self._epoch(r[0]))]
+            rows = inside or rows[-3:]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -220,7 +233,6 @@ class Step:
             self.dYc = list(self.dY.split(self.rows))
             self.Hpre = torch.empty(T, F, **bf)
             self.dHpre = torch.empty(T, F, **bf)
-            self.Hb = torch.empty(T, F, **bf)
             self.dXg = torch.empty(T, d, **bf)
             self.dX = torch.empty(T, d, **bf)
             self.dXc = list(self.dX.split(self.rows))
@@ -267,9 +279,9 @@ class Step:
         if w.backward:
             b.tpmlp_layernorm_gather(self.Xc, self.gamma, self.beta, N, self.Xg)
             i += 1; rec(i)
-            b.tpmlp_gemm_dh_geluprime(self.dY, self.B, self.Hpre, N, self.dHpre, self.Hb)
+            b.tpmlp_gemm_dh_geluprime(self.dY, self.B, self.Hpre, N, self.dHpre)
             i += 1; rec(i)
-            b.tpmlp_gemm_wgrad_b(self.Hb, self.dY, N, self.dB)
+            b.tpmlp_gemm_wgrad_b(self.H, self.dY, N, self.dB)
             i += 1; rec(i)
             b.tpmlp_gemm_wgrad_a(self.Xg, self.dHpre, N, self.dA)
             i += 1; rec(i)
@@ -307,7 +319,8 @@ def run_e2e(step, args, torch, binding):
         Xd.copy_(X_h, non_blocking=True)
         if w.sp:
             binding.tpmlp_sp_forward(list(Xd.split(step.rows)), step.gamma, step.beta, step.A, step.B, N, step.Yc,
-                                     bias=step.bias, Hpre_out=step.Hpre if w.backward else None, ws=ws_f)
+                                     bias=step.bias, Hpre_out=step.Hpre if w.backward else None,
+                                     H_out=step.H if w.backward else None, ws=ws_f)
         else:
             binding.tpmlp_forward(Xd, step.A, step.B, step.bias, N, step.Y, ws=ws_f)
         Y_h.copy_(step.Y, non_blocking=True)
@@ -315,7 +328,7 @@ def run_e2e(step, args, torch, binding):
             dYd.copy_(dY_h, non_blocking=True)
             binding.tpmlp_sp_backward(list(Xd.split(step.rows)), step.gamma, step.beta, step.A, step.B, step.Hpre,
                                       list(dYd.split(step.rows)), N, step.dXc, step.dA, step.dB, step.dgamma,
-                                      step.dbeta, bias=step.bias, ws=ws_b)
+                                      step.dbeta, bias=step.bias, H=step.H, ws=ws_b)
             dX_h.copy_(step.dX, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -371,10 +384,13 @@ def run_ours(args, w):
     with ClockSampler(local) as clk:
         time.sleep(0.3)
         t0 = time.perf_counter()
+        e0 = time.time()
         for k in range(args.steps):
             step.run(events[k])
         torch.cuda.synchronize()
+        e1 = time.time()
         wall = time.perf_counter() - t0
+        time.sleep(0.15)
     if dist is not None:
         dist.barrier()
     seg_ms = [0.0] * nseg
@@ -426,7 +442,7 @@ def run_ours(args, w):
                "tokens_per_s": tok / dt, "seconds": round(dt, 2),
                "sample": f"{tok} of {w.T} tokens through the fp64 oracle with the full d={w.d}, F={w.F} weights "
                          f"(numpy float64, BLAS matmul on {cores} threads)"}
-    clocks = clk.summary()
+    clocks = clk.summary(e0, e1)
     if rank != 0:
         dist.destroy_process_group() if dist is not None else None
         return

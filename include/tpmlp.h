@@ -121,13 +121,16 @@ TPMLP_API tpmlp_status tpmlp_get_device_status(tpmlp_stream_t stream, uint32_t* 
  *   X [T x d], A [d x F], B [F x d], bias [F] or NULL (the column layer's
  *   bias, split with A's columns), Y [T x d] out.
  *   Hpre_out: NULL, or [T x F] receiving the pre-activation X A + b (bf16)
- *   for a later tpmlp_backward.
+ *   for a later tpmlp_backward.  H_out: NULL, or [T x F] receiving
+ *   H = GeLU(X A + b) (otherwise H lives in the workspace); passing it to the
+ *   backward saves recomputing it there.
  * bf16: tcgen05 GEMM with bias + exact erf-GeLU in the epilogue into H
  * (workspace), then the row-parallel GEMM summing all N shards in TMEM.
  * fp32 (shape->dtype == TPMLP_FP32): all pointers are fp32, CUDA-core FFMA;
  * Hpre_out must be NULL. */
-TPMLP_API tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
-                           void* Y, void* Hpre_out, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+TPMLP_API tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const void* bias,
+                                     const tpmlp_shape* shape, void* Y, void* Hpre_out, void* H_out, void* workspace,
+                                     size_t workspace_bytes, tpmlp_stream_t stream);
 
 /* Sequence-parallel block forward (deep-dive page, section "All-Reduce 통신의
  * All-Gather 및 Reduce-Scatter 분해"; SequenceParallelLayerNorm in the listing):
@@ -136,36 +139,39 @@ TPMLP_API tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B
  * the MLP, Reduce-Scatter of the shard partials back to chunks.
  *   X_chunks: host array of N pointers, each [T/N x d]; gamma, beta [d];
  *   Y_chunks: host array of N pointers, each [T/N x d] out; rs_mode:
- *   TPMLP_RS_FUSED or TPMLP_RS_PARTIALS; Hpre_out: NULL or [T x F].
- * bf16 only. */
+ *   TPMLP_RS_FUSED or TPMLP_RS_PARTIALS; Hpre_out, H_out: NULL or [T x F]
+ *   as in tpmlp_forward.  bf16 only. */
 TPMLP_API tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
-                              const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
-                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* workspace,
-                              size_t workspace_bytes, tpmlp_stream_t stream);
+                                        const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
+                                        void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out,
+                                        void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
 
 /* MLP backward, the chain rule of the forward (the pages name two backward
  * AllReduces per block, glossary page, tensor-parallel section):
  *   Hpre = X A + b (the given Hpre, or recomputed when Hpre == NULL),
- *   dHpre = (dY B^T) * GeLU'(Hpre), dB = GeLU(Hpre)^T dY, dA = X^T dHpre,
+ *   H = GeLU(Hpre) (the forward's H when H != NULL and Hpre != NULL, else
+ *   derived here), dHpre = (dY B^T) * GeLU'(Hpre), dB = H^T dY, dA = X^T dHpre,
  *   dbias = column sums of dHpre (if dbias != NULL), and
  *   dX = sum_i dHpre_i A_i^T  (the backward AllReduce, as one K loop).
  * Outputs dX [T x d], dA [d x F], dB [F x d], dbias [F] are bf16.  bf16 only. */
-TPMLP_API tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* bias, const void* Hpre,
-                            const void* dY, const tpmlp_shape* shape, void* dX, void* dA, void* dB, void* dbias,
-                            void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+TPMLP_API tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* bias,
+                                      const void* Hpre, const void* H, const void* dY, const tpmlp_shape* shape,
+                                      void* dX, void* dA, void* dB, void* dbias, void* workspace,
+                                      size_t workspace_bytes, tpmlp_stream_t stream);
 
 /* Sequence-parallel block backward: All-Gather of the dY chunks (the mirror
  * of the forward Reduce-Scatter), the MLP backward on the re-normalised
  * gathered input, Reduce-Scatter of the input gradient to chunks (the mirror
  * of the forward All-Gather), LayerNorm backward per chunk.
  *   dX_chunks: host array of N pointers [T/N x d] (bf16) out;
- *   dgamma, dbeta: [d] fp32 out, summed over all chunks; dA, dB, dbias as in
- *   tpmlp_backward.  bf16 only. */
+ *   dgamma, dbeta: [d] fp32 out, summed over all chunks; Hpre, H, dA, dB,
+ *   dbias as in tpmlp_backward.  bf16 only. */
 TPMLP_API tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
-                               const void* A, const void* B, const void* bias, const void* Hpre,
-                               const void* const* dY_chunks, const tpmlp_shape* shape, void* const* dX_chunks,
-                               void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
-                               size_t workspace_bytes, tpmlp_stream_t stream);
+                                         const void* A, const void* B, const void* bias, const void* Hpre,
+                                         const void* H, const void* const* dY_chunks, const tpmlp_shape* shape,
+                                         void* const* dX_chunks, void* dA, void* dB, void* dbias, void* dgamma,
+                                         void* dbeta, void* workspace, size_t workspace_bytes,
+                                         tpmlp_stream_t stream);
 
 /* ------------------------------------------------------------------ single steps (bf16)
  * Each step is one kernel launch (plus a small fixed-order reduction where
@@ -202,9 +208,10 @@ TPMLP_API tpmlp_status tpmlp_reduce_scatter(const void* P, const tpmlp_shape* sh
 TPMLP_API tpmlp_status tpmlp_layernorm_gather(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                                     const tpmlp_shape* shape, void* Xg, tpmlp_stream_t stream);
 
-/* dHpre = (dY B^T) * GeLU'(Hpre) and H = GeLU(Hpre) in one GEMM epilogue;
- * with dbias != NULL also dbias = column sums of dHpre (workspace: size of
- * TPMLP_OP_DH_GELUPRIME).  dY [T x d], B [F x d], Hpre/dHpre/H [T x F]. */
+/* dHpre = (dY B^T) * GeLU'(Hpre) in one GEMM epilogue; with H != NULL also
+ * H = GeLU(Hpre); with dbias != NULL also dbias = column sums of dHpre
+ * (workspace: size of TPMLP_OP_DH_GELUPRIME).  dY [T x d], B [F x d],
+ * Hpre/dHpre/H [T x F]. */
 TPMLP_API tpmlp_status tpmlp_gemm_dh_geluprime(const void* dY, const void* B, const void* Hpre, const tpmlp_shape* shape,
                                      void* dHpre, void* H, void* dbias, void* workspace, size_t workspace_bytes,
                                      tpmlp_stream_t stream);

@@ -334,23 +334,30 @@ cudaError_t do_ln_bwd(const DeviceCtx& c, const void* const* X_chunks, const voi
   return launch_layernorm_bwd(r, kLnBwdMaxBlocks, static_cast<float*>(dgamma), static_cast<float*>(dbeta), st);
 }
 
-// Backward core shared by tpmlp_backward and tpmlp_sp_backward.
+// Backward core shared by tpmlp_backward and tpmlp_sp_backward.  With Hpre
+// and H from the forward only the four backward GEMMs run; without Hpre, one
+// GEMM1 recomputes both.
 cudaError_t backward_core(const DeviceCtx& c, const void* X, const void* A, const void* B, const void* bias,
-                          const void* Hpre, const void* dY, const tpmlp_shape* s, void* dX, void* dA, void* dB,
-                          void* dbias, Carve& ws, cudaStream_t st) {
+                          const void* Hpre, const void* H, const void* dY, const tpmlp_shape* s, void* dX, void* dA,
+                          void* dB, void* dbias, Carve& ws, cudaStream_t st) {
   const Sizes z = sizes_of(s);
   void* hpre_ws = ws.take(z.tf);
   void* dhpre = ws.take(z.tf);
-  void* h = ws.take(z.tf);
+  void* h_ws = ws.take(z.tf);
   float* colsum = static_cast<float*>(ws.take(z.colsum));
   cudaError_t e = cudaSuccess;
+  void* h_out = nullptr;  // H emitted by the GeLU' epilogue only when nobody supplied it
   if (Hpre == nullptr) {
-    e = do_gemm1(c, X, A, bias, s, hpre_ws, nullptr, kEpiBias, st);
+    e = do_gemm1(c, X, A, bias, s, h_ws, hpre_ws, kEpiBiasGelu, st);
     if (e != cudaSuccess) return e;
     Hpre = hpre_ws;
+    H = h_ws;
+  } else if (H == nullptr) {
+    h_out = h_ws;
+    H = h_ws;
   }
-  if ((e = do_dh(c, dY, B, Hpre, s, dhpre, h, dbias, colsum, st)) != cudaSuccess) return e;
-  if ((e = do_wgrad_b(c, h, dY, s, dB, st)) != cudaSuccess) return e;
+  if ((e = do_dh(c, dY, B, Hpre, s, dhpre, h_out, dbias, colsum, st)) != cudaSuccess) return e;
+  if ((e = do_wgrad_b(c, H, dY, s, dB, st)) != cudaSuccess) return e;
   if ((e = do_wgrad_a(c, X, dhpre, s, dA, st)) != cudaSuccess) return e;
   return do_dx(c, dhpre, A, s, dX, st);
 }
@@ -410,12 +417,13 @@ tpmlp_status tpmlp_selftest_wait_timeout(uint32_t budget_us, tpmlp_stream_t stre
 }
 
 tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
-                           void* Y, void* Hpre_out, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+                           void* Y, void* Hpre_out, void* H_out, void* workspace, size_t workspace_bytes,
+                           tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, false);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (!ptrs_ok({X, A, B, Y}) || !opt_ok(bias) || !opt_ok(Hpre_out)) return TPMLP_ERR_INVALID_ARG;
-  if (shape->dtype == TPMLP_FP32 && Hpre_out != nullptr) return TPMLP_ERR_UNSUPPORTED;
+  if (!ptrs_ok({X, A, B, Y}) || !opt_ok(bias) || !opt_ok(Hpre_out) || !opt_ok(H_out)) return TPMLP_ERR_INVALID_ARG;
+  if (shape->dtype == TPMLP_FP32 && (Hpre_out != nullptr || H_out != nullptr)) return TPMLP_ERR_UNSUPPORTED;
   if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_FWD))
     return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;
@@ -428,19 +436,21 @@ tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const vo
                                        static_cast<int>(shape->ffn), static_cast<float*>(workspace),
                                        static_cast<float*>(Y), s));
   }
-  cudaError_t e = do_gemm1(c, X, A, bias, shape, workspace, Hpre_out, kEpiBiasGelu, s);
-  if (e == cudaSuccess) e = do_gemm2(c, workspace, B, shape, Y, nullptr, s);
+  void* H = H_out != nullptr ? H_out : workspace;
+  cudaError_t e = do_gemm1(c, X, A, bias, shape, H, Hpre_out, kEpiBiasGelu, s);
+  if (e == cudaSuccess) e = do_gemm2(c, H, B, shape, Y, nullptr, s);
   return cuda_status(e);
 }
 
 tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                               const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
-                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* workspace,
+                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out, void* workspace,
                               size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !opt_ok(Hpre_out)) return TPMLP_ERR_INVALID_ARG;
+  if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !opt_ok(Hpre_out) || !opt_ok(H_out))
+    return TPMLP_ERR_INVALID_ARG;
   if (!chunks_ok(X_chunks, shape->n_shards) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
   if (!(eps >= 0.f)) return TPMLP_ERR_INVALID_ARG;
   if (rs_mode != TPMLP_RS_FUSED && rs_mode != TPMLP_RS_PARTIALS) return TPMLP_ERR_INVALID_ARG;
@@ -454,6 +464,7 @@ tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, co
   Carve ws(workspace);
   void* Xg = ws.take(z.td);
   void* H = ws.take(z.tf);
+  if (H_out != nullptr) H = H_out;
   cudaError_t e = do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, s);
   if (e == cudaSuccess) e = do_gemm1(c, Xg, A, bias, shape, H, Hpre_out, kEpiBiasGelu, s);
   if (e == cudaSuccess) {
@@ -469,31 +480,32 @@ tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, co
 }
 
 tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* bias, const void* Hpre,
-                            const void* dY, const tpmlp_shape* shape, void* dX, void* dA, void* dB, void* dbias,
-                            void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+                            const void* H, const void* dY, const tpmlp_shape* shape, void* dX, void* dA, void* dB,
+                            void* dbias, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (!ptrs_ok({X, A, B, dY, dX, dA, dB}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(dbias))
+  if (!ptrs_ok({X, A, B, dY, dX, dA, dB}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(H) || !opt_ok(dbias))
     return TPMLP_ERR_INVALID_ARG;
   if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_BWD))
     return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   Carve ws(workspace);
-  return cuda_status(backward_core(c, X, A, B, bias, Hpre, dY, shape, dX, dA, dB, dbias, ws,
+  return cuda_status(backward_core(c, X, A, B, bias, Hpre, H, dY, shape, dX, dA, dB, dbias, ws,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
-                               const void* A, const void* B, const void* bias, const void* Hpre,
+                               const void* A, const void* B, const void* bias, const void* Hpre, const void* H,
                                const void* const* dY_chunks, const tpmlp_shape* shape, void* const* dX_chunks,
                                void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
                                size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (!ptrs_ok({gamma, beta, A, B, dA, dB, dgamma, dbeta}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(dbias))
+  if (!ptrs_ok({gamma, beta, A, B, dA, dB, dgamma, dbeta}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(H) ||
+      !opt_ok(dbias))
     return TPMLP_ERR_INVALID_ARG;
   const int n = shape->n_shards;
   if (!chunks_ok(X_chunks, n) || !chunks_ok(dY_chunks, n) || !chunks_ok(dX_chunks, n)) return TPMLP_ERR_INVALID_ARG;
@@ -530,7 +542,7 @@ tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, c
     if ((e = launch_gather_rows(r, c, s)) != cudaSuccess) return cuda_status(e);
     dY = dYg;
   }
-  e = backward_core(c, Xg, A, B, bias, Hpre, dY, shape, dXg, dA, dB, dbias, ws, s);
+  e = backward_core(c, Xg, A, B, bias, Hpre, H, dY, shape, dXg, dA, dB, dbias, ws, s);
   if (e == cudaSuccess) e = do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta, lnpart, s);
   return cuda_status(e);
 }
@@ -602,7 +614,7 @@ tpmlp_status tpmlp_gemm_dh_geluprime(const void* dY, const void* B, const void* 
   tpmlp_status st = check_shape(shape, false, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (!ptrs_ok({dY, B, Hpre, dHpre, H}) || !opt_ok(dbias)) return TPMLP_ERR_INVALID_ARG;
+  if (!ptrs_ok({dY, B, Hpre, dHpre}) || !opt_ok(H) || !opt_ok(dbias)) return TPMLP_ERR_INVALID_ARG;
   if (dbias != nullptr && (workspace == nullptr || !al16(workspace) ||
                            workspace_bytes < ws_bytes(shape, TPMLP_OP_DH_GELUPRIME)))
     return TPMLP_ERR_WORKSPACE;

@@ -145,21 +145,24 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       store_row32(dst, col0, p.N, v);
     }
   } else if constexpr (EPI == kEpiDGelu) {
-    // v = dH = dY B^T; aux = Hpre.  One erf per element serves both GeLU and GeLU'.
+    // v = dH = dY B^T; aux = Hpre.  dHpre = dH * (Phi(h) + h phi(h)); with out1 also H = h Phi(h),
+    // one erf serving both.
     float h[32];
     unpack_row32(aux_raw, h);
+    const bool want_h = p.out1 != nullptr;
     float g[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float x = h[i];
       const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
-      const float pdf = 0.39894228040143268f * expf(-0.5f * x * x);
+      const float pdf = 0.39894228040143268f * __expf(-0.5f * x * x);
       g[i] = x * cdf;
       v[i] = row_ok ? v[i] * (cdf + x * pdf) : 0.f;
     }
     if (row_ok) {
       store_row32(static_cast<__nv_bfloat16*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v);
-      store_row32(static_cast<__nv_bfloat16*>(p.out1) + static_cast<long long>(row) * p.ld1, col0, p.N, g);
+      if (want_h)
+        store_row32(static_cast<__nv_bfloat16*>(p.out1) + static_cast<long long>(row) * p.ld1, col0, p.N, g);
     }
     if (p.colsum != nullptr) {
       const float s = warp_column_sums(v, lane);

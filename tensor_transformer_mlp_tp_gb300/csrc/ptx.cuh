@@ -54,14 +54,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about kSuspendHintNs elapse, instead of spinning on the barrier.
+constexpr uint32_t kSuspendHintNs = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -87,10 +91,10 @@ __device__ __forceinline__ void record_error(const WaitCtx& w, uint32_t bit, uin
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t n = 1;; ++n) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*w.abort) return false;
-    if ((n & 15u) == 0u && global_timer_ns() - t0 > w.budget_ns) {
+    if (global_timer_ns() - t0 > w.budget_ns) {
       record_error(w, kErrTimeout, site);
       return false;
     }

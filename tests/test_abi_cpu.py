@@ -103,11 +103,11 @@ def test_null_and_misaligned_pointers_rejected(lib):
     good = ctypes.c_void_p(1 << 20)
     odd = ctypes.c_void_p((1 << 20) + 2)
     ws = ctypes.c_void_p(1 << 24)
-    args = lambda X, A, B, Y: (X, A, B, None, ctypes.byref(s), Y, None, ws, 1 << 30, None)
+    args = lambda X, A, B, Y: (X, A, B, None, ctypes.byref(s), Y, None, None, ws, 1 << 30, None)
     assert L.tpmlp_forward(*args(None, good, good, good)) == binding.ERR_INVALID_ARG
     assert L.tpmlp_forward(*args(good, good, good, None)) == binding.ERR_INVALID_ARG
     assert L.tpmlp_forward(*args(odd, good, good, good)) == binding.ERR_INVALID_ARG
-    assert L.tpmlp_forward(good, good, good, None, ctypes.byref(s), good, None, ws, 16, None) == binding.ERR_WORKSPACE
+    assert L.tpmlp_forward(good, good, good, None, ctypes.byref(s), good, None, None, ws, 16, None) == binding.ERR_WORKSPACE
     assert L.tpmlp_gemm2_partials(good, good, ctypes.byref(binding.make_shape(256, 64, 96, 2)), good, None) \
         == binding.ERR_UNSUPPORTED                                      # (ffn / N) % 64 != 0
     assert L.tpmlp_selftest_wait_timeout(0, None) == binding.ERR_INVALID_ARG
@@ -117,4 +117,4 @@ def test_empty_batch_needs_no_device(lib):
     L = binding.lib()
     s = binding.make_shape(0, 64, 256, 2)
     good = ctypes.c_void_p(1 << 20)
-    assert L.tpmlp_forward(good, good, good, None, ctypes.byref(s), good, None, None, 0, None) == binding.OK
+    assert L.tpmlp_forward(good, good, good, None, ctypes.byref(s), good, None, None, None, 0, None) == binding.OK

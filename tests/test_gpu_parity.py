@@ -180,18 +180,20 @@ def test_sp_forward(T, d, N, rs_mode):
 
 
 @pytest.mark.parametrize("T,d,N", [(300, 192, 4), (256, 128, 8), (130, 64, 2)])
-@pytest.mark.parametrize("saved_hpre", [True, False])
-def test_backward(T, d, N, saved_hpre):
+@pytest.mark.parametrize("saved", ["none", "hpre", "hpre_h"])
+def test_backward(T, d, N, saved):
     w = inputs.small_workload(T, d, N, backward=True, bias=(0.0, 0.2))
     X, A, B, b, dY = _draw(w, "X", "A", "B", "bias", "dY")
     F = 4 * d
     Xd, Ad, Bd, bd = dev(X[0]), dev(A[0]), dev(B[0]), dev(b[0])
-    Hpre = None
-    if saved_hpre:
+    Hpre = H = None
+    if saved != "none":
         Hpre = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
-        binding.tpmlp_forward(Xd, Ad, Bd, bd, N, torch.empty(T, d, dtype=torch.bfloat16, device="cuda"), Hpre)
+        Hs = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+        binding.tpmlp_forward(Xd, Ad, Bd, bd, N, torch.empty(T, d, dtype=torch.bfloat16, device="cuda"), Hpre, Hs)
+        H = Hs if saved == "hpre_h" else None
     dX, dA, dB, db = Guarded((T, d)), Guarded((d, F)), Guarded((F, d)), Guarded((F,))
-    binding.tpmlp_backward(Xd, Ad, Bd, bd, Hpre, dev(dY[0]), N, dX.t, dA.t, dB.t, db.t)
+    binding.tpmlp_backward(Xd, Ad, Bd, bd, Hpre, dev(dY[0]), N, dX.t, dA.t, dB.t, db.t, H=H)
     torch.cuda.synchronize()
     ref = oracle.mlp_backward_tp(X[1], A[1], B[1], b[1], dY[1], N)
     for name, got, r in [("dX", dX, ref["dX"]), ("dA", dA, ref["dA"]), ("dB", dB, ref["dB"]), ("db", db, ref["db"])]:
@@ -209,13 +211,15 @@ def test_sp_backward(T, d, N):
     # dY chunks as separate allocations: exercises the gather of non-contiguous chunks
     dys = [dev(c) for c in _chunks(dY[0], N)]
     Hpre = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    Hs = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
     Y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
-    binding.tpmlp_sp_forward(xs, dev(g[0]), dev(b[0]), dev(A[0]), dev(B[0]), N, list(Y.split(rows)), Hpre_out=Hpre)
+    binding.tpmlp_sp_forward(xs, dev(g[0]), dev(b[0]), dev(A[0]), dev(B[0]), N, list(Y.split(rows)), Hpre_out=Hpre,
+                             H_out=Hs)
     dX = [Guarded((rows, d)) for _ in range(N)]
     dA, dB = Guarded((d, F)), Guarded((F, d))
     dgam, dbet = Guarded((d,), torch.float32), Guarded((d,), torch.float32)
     binding.tpmlp_sp_backward(xs, dev(g[0]), dev(b[0]), dev(A[0]), dev(B[0]), Hpre, dys, N, [x.t for x in dX], dA.t,
-                              dB.t, dgam.t, dbet.t)
+                              dB.t, dgam.t, dbet.t, H=Hs)
     torch.cuda.synchronize()
     ref = oracle.sp_backward(_chunks(X[1], N), g[1], b[1], 1e-5, A[1], B[1], None, _chunks(dY[1], N), N)
     assert_bf16_close("dX", np.concatenate([f64(x.t) for x in dX]), np.concatenate(ref["dX_chunks"]))
