@@ -238,6 +238,21 @@ TPMLP_API tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, con
                                       const tpmlp_shape* shape, void* const* dX_chunks, void* dgamma, void* dbeta,
                                       void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* LayerNorm backward exactly as tpmlp_layernorm_backward, for callers that
+ * cannot allocate device memory: it takes no workspace.  (This entry point
+ * has no counterpart on the pages; it is an interface convenience.)  The
+ * per-block dgamma/dbeta partial sums live in a fixed 9.5 MiB array inside
+ * the library's device image, which every GPU that loads the library keeps
+ * until the process exits.  d > 8192 returns TPMLP_ERR_UNSUPPORTED before
+ * anything is launched.  All calls on a device share that array: calls whose
+ * kernels overlap on the GPU (e.g. on unordered streams) race on it and give
+ * wrong dgamma/dbeta.  The first call on a device looks the array up with
+ * that device current; make it before any stream capture. */
+TPMLP_API tpmlp_status tpmlp_layernorm_backward_noalloc(const void* const* X_chunks, const void* gamma, float eps,
+                                                        const void* dXg, const tpmlp_shape* shape,
+                                                        void* const* dX_chunks, void* dgamma, void* dbeta,
+                                                        tpmlp_stream_t stream);
+
 /* Failure-detection self test: launches one CTA that waits on a barrier no
  * thread ever arrives at, with a limit of `budget_us` microseconds (1 to
  * 1000000).  The wait runs out, the kernel records the timeout and exits;

@@ -58,6 +58,7 @@ _SIGS = {
     "tpmlp_gemm_dx_shard_accum": ([_P, _P, _SP, _P, _P], ctypes.c_int),
     "tpmlp_layernorm_backward": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P, ctypes.c_size_t, _P],
                                  ctypes.c_int),
+    "tpmlp_layernorm_backward_noalloc": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P], ctypes.c_int),
     "tpmlp_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
 }
 
@@ -255,6 +256,16 @@ def tpmlp_layernorm_backward(X_chunks, gamma, dXg, N, dX_chunks, dgamma, dbeta, 
     _check("tpmlp_layernorm_backward", lib().tpmlp_layernorm_backward(
         xp, _ptr(gamma), eps, _ptr(dXg), ctypes.byref(shape), dxp, _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def tpmlp_layernorm_backward_noalloc(X_chunks, gamma, dXg, N, dX_chunks, dgamma, dbeta, eps=1e-5, stream=None):
+    """LayerNorm backward without a workspace (scratch is a fixed array inside the library)."""
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
+    xp, _xa = _ptrs(X_chunks)
+    dxp, _dxa = _ptrs(dX_chunks)
+    _check("tpmlp_layernorm_backward_noalloc", lib().tpmlp_layernorm_backward_noalloc(
+        xp, _ptr(gamma), eps, _ptr(dXg), ctypes.byref(shape), dxp, _ptr(dgamma), _ptr(dbeta), _stream(stream)))
 
 
 def tpmlp_selftest_wait_timeout(budget_us: int, stream=None):
