@@ -20,6 +20,7 @@ os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
 os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
 
 import argparse  # noqa: E402
+import hashlib  # noqa: E402
 import json  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
@@ -45,6 +46,46 @@ def peaks():
             d = json.load(fh)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest():
+    """Short sha256 of the CUDA sources the kernels are built from (keys the committed ncu traffic table)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_transformer_mlp_tp_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(segment):
+    """DRAM bytes per launch of `segment` from the committed ncu capture, or None if the kernels changed since."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    if d.get("source_digest") != kernel_source_digest():
+        return None
+    return d.get("bytes_per_launch", {}).get(segment)
+
+
+def max_over_ranks(value, dist):
+    """The largest `value` over all ranks (every rank gets it); the value itself without a process group."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_step, steps, world, max_ms):
+    """Work of all ranks (each rank does `work_per_step` per step) per second of the slowest rank."""
+    return work_per_step * steps * world / (max_ms * 1e-3)
 
 
 def useful_flops(w):
@@ -429,19 +470,15 @@ def run_ours(args, w):
     for k in range(args.steps):
         for i in range(nseg):
             seg_ms[i] += events[k][i].elapsed_time(events[k][i + 1])
-    total_ms = events[0][0].elapsed_time(events[-1][nseg])
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(events[0][0].elapsed_time(events[-1][nseg]), dist)
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after timing: {binding.status_string(st)} (site {site})")
 
     pk, pk_kind = peaks()
     flops = useful_flops(w)
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
-    tokens_per_s = w.T * args.steps * world / (total_ms * 1e-3)
+    value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
+    tokens_per_s = whole_job_rate(w.T, args.steps, world, total_ms)
 
     kern = {}
     dom = None
@@ -450,21 +487,19 @@ def run_ours(args, w):
         if unit == "F":
             ach = work / (avg * 1e-3) / 1e12
             peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-            kern[name] = {"ms": round(avg, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / peak, 3)}
+            kern[name] = {"ms": round(avg, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / peak, 3),
+                          "dram_bytes": measured_traffic(name)}
             if dom is None or avg > dom[1]:
                 dom = (name, avg, work, ach, peak)
         else:
             ach = work / (avg * 1e-3) / 1e9
             kern[name] = {"ms": round(avg, 4), "GB/s": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 3),
-                          "launches": nl}
+                          "launches": nl, "dram_bytes": measured_traffic(name)}
     e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
-    e2e_ms_t = torch.tensor([e2e_ms], dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(e2e_ms_t, op=dist.ReduceOp.MAX)
-    e2e_ms = float(e2e_ms_t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -489,10 +524,10 @@ def run_ours(args, w):
                    "l2": "inputs larger than L2 (weights alone 2 x d x F x 2 bytes)",
                    "host_wall_s": round(wall, 3)},
         "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": round(dom[3], 1), "peak": dom[4],
-                     "unit": "TFLOP/s", "frac": round(dom[3] / dom[4], 3), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(dom[3] / dom[4], 3), "traffic": measured_traffic(dom[0]),
                      "peak_kind": f"{pk_kind} bf16 sustained"},
         "kernels": kern,
-        "e2e": {"value": round(flops * args.steps * world / (e2e_ms * args.steps * 1e-3) / 1e12, 2),
+        "e2e": {"value": round(whole_job_rate(flops, args.steps, world, e2e_ms * args.steps) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "what": "block calls (tpmlp_sp_forward/backward) with X, dY copied from pinned host memory and Y, dX "
