@@ -19,6 +19,8 @@ enum WaitSite : uint32_t {
   kSiteMmaFull = 2,
   kSiteMmaTmemEmpty = 3,
   kSiteEpiTmemFull = 4,
+  kSiteEpiStageDrained = 5,
+  kSiteEpiStageFilled = 6,
 };
 
 // GEMM tile: BM x BN output, BK-deep k-blocks (64 bf16 = one 128-byte swizzle row).

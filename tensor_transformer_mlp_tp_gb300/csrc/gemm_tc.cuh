@@ -146,7 +146,7 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
     }
   } else if constexpr (EPI == kEpiDGelu) {
     // v = dH = dY B^T; aux = Hpre.  dHpre = dH * (Phi(h) + h phi(h)); with out1 also H = h Phi(h),
-    // one erf serving both.
+    // Phi and phi sharing one exponential.
     float h[32];
     unpack_row32(aux_raw, h);
     const bool want_h = p.out1 != nullptr;
@@ -154,10 +154,9 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float x = h[i];
-      const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
-      const float pdf = 0.39894228040143268f * __expf(-0.5f * x * x);
-      g[i] = x * cdf;
-      v[i] = row_ok ? v[i] * (cdf + x * pdf) : 0.f;
+      const NormalCdfPdf n = normal_cdf_pdf(x);
+      g[i] = x * n.cdf;
+      v[i] = row_ok ? v[i] * (n.cdf + x * n.pdf) : 0.f;
     }
     if (row_ok) {
       store_row32(static_cast<__nv_bfloat16*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v);
@@ -326,6 +325,16 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc(const __grid
       tile_coords(p, tile, shard, mb, nb);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      if constexpr (EPI == kEpiDGelu) {
+        // While this tile's MMAs run, pull the warp's 32 rows of the pre-activation tile into L2.
+        const int prow = mb * kBM + quad * 32 + static_cast<int>(lane);
+        const int pcol = nb * BN + part * kColsPerPart;
+        if (prow < p.M && pcol < p.N) {
+          const int ncols = min(kColsPerPart, p.N - pcol);
+          prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(prow) * p.ld_aux + pcol,
+                           static_cast<uint32_t>(ncols) * 2u);
+        }
+      }
       int ok = 1;
       if (lane == 0) ok = wait_bounded(tfull + acc, acc_phase, wc, kSiteEpiTmemFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -15,6 +15,14 @@
 //   empty[s]   one per CTA; the MMA commit multicasts to both.
 //   tfull[a]   one per CTA; the MMA commit multicasts to both.
 //   tempty[a]  lives in the even CTA; every epilogue warp of both CTAs arrives.
+// Epilogue warps: warps 2..5 own the four TMEM lane quadrants (quadrant =
+// warp % 4).  The quadrant-0 and quadrant-1 warps share SM sub-partitions with
+// the TMA producer (warp 0) and the MMA issuer (warp 1); measured on GB300, the
+// ALU stream of a GeLU epilogue next to the MMA issuer slows the MMAs by ~8%.
+// So those two warps only copy their accumulator rows TMEM -> shared memory
+// (a swizzled double buffer per quadrant, `filled`/`drained` barriers), and
+// helper warps 6 and 7 (sub-partitions 2 and 3) run the epilogue math and the
+// stores for them.
 // Only the even CTA's warp 1 issues MMAs.  Waits are bounded as in the
 // single-CTA kernel; the pair meets at a cluster barrier before TMEM is
 // released and before either CTA exits (the even CTA's MMAs read the odd
@@ -33,23 +41,28 @@ struct PairShape {
   static constexpr int kBTile = kHalfN * kBK * 2;  // this CTA's half of the B columns
   static constexpr int kStage = kATile + kBTile;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kThreads = 64 + 32 * EPI_WARPS;
-  static constexpr int kSmem = 1024 + STAGES * kStage + 256;
+  static constexpr int kThreads = 64 + 32 * EPI_WARPS + 64;     // + two helper warps
+  static constexpr int kStaging = 2 * 2 * 32 * 32 * 4;            // [quadrant 0/1][buffer][32 rows][32 fp32]
+  static constexpr int kSmem = 1024 + STAGES * kStage + kStaging + 256;
+  static_assert(EPI_WARPS == 4, "one epilogue warp per TMEM lane quadrant");
 };
 
 template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS>
-__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __grid_constant__ GemmParams p) {
   using S = PairShape<BN, STAGES, EPI_WARPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * S::kATile;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * S::kBTile);
+  float* staging = reinterpret_cast<float*>(sB + STAGES * S::kBTile);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(staging) + S::kStaging);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* filled = drain + 1;    // [quadrant 0/1][buffer]
+  uint64_t* drained = filled + 4;  // [quadrant 0/1][buffer]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -67,6 +80,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gri
       mbar_init(tempty + a, 2 * EPI_WARPS);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(filled + i, 1);
+      mbar_init(drained + i, 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -187,46 +204,102 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gri
     }
   } else {
     // -------------------------------------------------------------------- epilogue (both CTAs)
-    const int ew = warp - 2;
-    const int quad = warp & 3;
-    constexpr int kSplit = EPI_WARPS / 4;
-    constexpr int kColsPerPart = BN / kSplit;
-    const int part = ew / 4;
+    const bool quad_warp = warp < 6;
+    const int quad = quad_warp ? (warp & 3) : (warp - 6);  // helper 6 serves quadrant 0, helper 7 quadrant 1
+    const bool reader = quad_warp && quad < 2;             // copies TMEM -> staging only
+    const bool helper = !quad_warp;                        // epilogue math on staged rows
+    float* stage_base = staging + quad * (2 * 32 * 32);    // valid for quadrants 0 and 1
+    uint32_t chunk_ctr = 0;
     int local = 0;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+    bool ok_all = true;
+    for (int tile = cluster_id; ok_all && tile < num_tiles; tile += num_clusters, ++local) {
       int shard, mb, nb;
       tile_coords(p, tile, shard, mb, nb);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      int ok = 1;
-      if (lane == 0) ok = wait_bounded(tfull + acc, acc_phase, wc, kSiteEpiTmemFull) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after_sync();
       const int mb128 = mb * 2 + static_cast<int>(rank);
       const int row = mb128 * 128 + quad * 32 + static_cast<int>(lane);
-      const int c_begin = part * kColsPerPart, c_end = (part + 1) * kColsPerPart;
+      if constexpr (EPI == kEpiDGelu) {
+        // While this tile's MMAs run, pull the warp's 32 rows of the pre-activation tile into L2.
+        if (!reader && row < p.M) {
+          const int pcol = nb * BN;
+          const int ncols = min(BN, p.N - pcol);
+          prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row) * p.ld_aux + pcol,
+                           static_cast<uint32_t>(ncols) * 2u);
+        }
+      }
+      if (!helper) {
+        int ok = 1;
+        if (lane == 0) ok = wait_bounded(tfull + acc, acc_phase, wc, kSiteEpiTmemFull) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after_sync();
+      }
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       const __nv_bfloat16* aux_row = nullptr;
       uint4 aux_next[4] = {};
       if constexpr (EPI == kEpiDGelu) {
-        aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
-        load_raw32(aux_row, nb * BN + c_begin, p.N, row < p.M, aux_next);
+        if (!reader) {
+          aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
+          load_raw32(aux_row, nb * BN, p.N, row < p.M, aux_next);
+        }
       }
 #pragma unroll 1
-      for (int c = c_begin; c < c_end; c += 32) {
+      for (int c = 0; c < BN; c += 32, ++chunk_ctr) {
+        const uint32_t buf = chunk_ctr & 1u, par = (chunk_ctr >> 1) & 1u;
+        float* sbuf = stage_base + buf * (32 * 32) + lane * 32;
+        float v[32];
+        if (reader) {
+          int ok = 1;
+          if (lane == 0) ok = wait_bounded(drained + quad * 2 + buf, par ^ 1u, wc, kSiteEpiStageDrained) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            ok_all = false;
+            break;
+          }
+          tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
+          // row `lane` of the staged chunk, 16-byte pieces swizzled by (lane & 7): conflict-free per quarter warp
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(sbuf + ((j ^ (lane & 7)) * 4)) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(filled + quad * 2 + buf);
+          continue;
+        }
         uint4 aux_cur[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) aux_cur[g] = aux_next[g];
         if constexpr (EPI == kEpiDGelu) {
-          if (c + 32 < c_end) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
+          if (c + 32 < BN) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
         }
-        float v[32];
-        tmem_load_32cols(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + c), v);
+        if (helper) {
+          int ok = 1;
+          if (lane == 0) ok = wait_bounded(filled + quad * 2 + buf, par, wc, kSiteEpiStageFilled) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            ok_all = false;
+            break;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 f = *reinterpret_cast<const float4*>(sbuf + ((j ^ (lane & 7)) * 4));
+            v[4 * j] = f.x;
+            v[4 * j + 1] = f.y;
+            v[4 * j + 2] = f.z;
+            v[4 * j + 3] = f.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(drained + quad * 2 + buf);
+        } else {
+          tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
+        }
         epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane);
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
+      if (!helper && ok_all) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
+      }
     }
   }
 

@@ -129,6 +129,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into L2, asynchronously.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // L2 cache-policy constants for the .L2::cache_hint operand (createpolicy
 // fractions are not needed: one policy per operand class).
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -232,14 +238,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 
 // ----------------------------------------------------------------------------- small math
 
-// Exact GeLU x * Phi(x) and its derivative Phi(x) + x * phi(x), in fp32 with
-// CUDA's erff/expf.
-__device__ __forceinline__ float gelu_f(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+// Exact GeLU x * Phi(x) and its derivative Phi(x) + x * phi(x), in fp32.
+// Phi(x) = (1 + erf(x / sqrt 2)) / 2 with erf from Abramowitz & Stegun,
+// Handbook of Mathematical Functions, eq. 7.1.26 (Hastings' rational
+// approximation, |error in erf| <= 1.5e-7 for all real arguments):
+//   erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),  t = 1 / (1 + p z),  z >= 0,
+// and erf(-z) = -erf(z).  With z = |x| / sqrt 2, exp(-z^2) = exp(-x^2 / 2) is
+// also what the normal density phi(x) needs, so GeLU' costs one exponential.
+struct NormalCdfPdf {
+  float cdf, pdf;
+};
+
+__device__ __forceinline__ NormalCdfPdf normal_cdf_pdf(float x) {
+  constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
+                  kA4 = -1.453152027f, kA5 = 1.061405429f;
+  const float e = __expf(-0.5f * x * x);                               // exp(-z^2)
+  const float t = __fdividef(1.0f, fmaf(kP * 0.70710678118654752f, fabsf(x), 1.0f));
+  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kA5, kA4), kA3), kA2), kA1);
+  const float tail = 0.5f * poly * e;                                  // Phi(-|x|)
+  return {x >= 0.f ? 1.0f - tail : tail, 0.39894228040143268f * e};
+}
+
+__device__ __forceinline__ float gelu_f(float x) { return x * normal_cdf_pdf(x).cdf; }
 
 __device__ __forceinline__ float gelu_prime_f(float x) {
-  const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
-  const float pdf = 0.39894228040143268f * expf(-0.5f * x * x);
-  return cdf + x * pdf;
+  const NormalCdfPdf n = normal_cdf_pdf(x);
+  return n.cdf + x * n.pdf;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -4,6 +4,8 @@ Shapes span several 128 x 256 output tiles and several 64-deep k-blocks, with
 ragged tails in every GEMM dimension, N in {1, 2, 4, 8}.  Integer-valued
 inputs make the shard reduction exact, so those cases compare bit for bit.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -280,3 +282,42 @@ def test_wait_timeout_selftest_reports_and_clears():
     assert st == binding.OK
     # the context stays usable
     test_forward(128, 64, 2, False)
+
+
+def _exact_gelu(x):
+    return 0.5 * x * (1.0 + np.vectorize(math.erf)(x / math.sqrt(2.0)))
+
+
+def _exact_gelu_prime(x):
+    return 0.5 * (1.0 + np.vectorize(math.erf)(x / math.sqrt(2.0))) + x * np.exp(-0.5 * x * x) / math.sqrt(2 * math.pi)
+
+
+def test_device_gelu_and_gelu_prime_pointwise():
+    """Pre-activations set exactly (one nonzero input column, unit weights), so H = GeLU(x) and
+    dHpre = GeLU'(x) can be compared point by point with the closed forms: within half a bf16 ulp of the
+    result plus 1e-6 absolute."""
+    T, d, N = 512, 64, 2
+    F = 256
+    xs = np.linspace(-8.0, 8.0, T).astype(np.float32)
+    xb = inputs.f32_to_bf16_bits(xs)
+    xv = inputs.bf16_bits_to_f64(xb)
+    X = np.zeros((T, d), dtype=np.uint16)
+    X[:, 0] = xb
+    A = np.zeros((d, F), dtype=np.uint16)
+    A[0, :] = inputs.f32_to_bf16_bits(np.ones(F, dtype=np.float32))
+    H = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    Hp = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    binding.tpmlp_gemm1_bias_gelu(dev(X), dev(A), None, N, H, Hp)
+    # dH = dY B^T = 1: dY = e_0 rows, B[:, 0] = 1
+    dY = np.zeros((T, d), dtype=np.uint16)
+    dY[:, 0] = inputs.f32_to_bf16_bits(np.ones(T, dtype=np.float32))
+    B = np.zeros((F, d), dtype=np.uint16)
+    B[:, 0] = inputs.f32_to_bf16_bits(np.ones(F, dtype=np.float32))
+    dHp = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    binding.tpmlp_gemm_dh_geluprime(dev(dY), dev(B), Hp, N, dHp)
+    torch.cuda.synchronize()
+    assert np.array_equal(f64(Hp)[:, 0], xv)
+    for got, ref in [(f64(H), _exact_gelu(xv)), (f64(dHp), _exact_gelu_prime(xv))]:
+        err = np.abs(got - ref[:, None])
+        bound = np.abs(ref[:, None]) * 2.0 ** -8 + 1e-6
+        assert np.all(err <= bound), float(np.max(err - bound))
