@@ -6,8 +6,9 @@ A step is one pass of the whole hot path over one batch: for the default
 workload ``sp_block_fwd_bwd`` (T=8192 tokens in N=8 sequence chunks, d=4096,
 F=16384) that is LayerNorm+gather, the column-parallel GEMM with bias+GeLU,
 the row-parallel GEMM with the in-kernel shard reduction and fused
-reduce-scatter store, then the backward: LayerNorm recompute, dY B^T * GeLU',
-dB = H^T dY, dA = Xg^T dHpre, dXg = dHpre A^T and the LayerNorm backward.
+reduce-scatter store, then the backward on the forward's saved activations
+(Xg, H, Hpre): dY B^T * GeLU', dB = H^T dY, dA = Xg^T dHpre, dXg = dHpre A^T
+and the LayerNorm backward.
 Every kernel is timed with CUDA events on the stream it is launched on.
 ``e2e`` repeats the step through the block calls of the C ABI with the
 activations copied from / to pinned host memory inside the timed region.
@@ -293,9 +294,9 @@ class Step:
             segs.append(("layernorm_gather", 1, ln, "B"))
         segs += [("gemm1_bias_gelu", 1, g, "F"), ("gemm2_shard_accum" + ("_rs_store" if w.sp else ""), 1, g, "F")]
         if w.backward:
-            segs += [("layernorm_recompute", 1, ln, "B"), ("gemm_dh_geluprime", 1, g, "F"), ("gemm_wgrad_b", 1, g, "F"),
+            segs += [("gemm_dh_geluprime", 1, g, "F"), ("gemm_wgrad_b", 1, g, "F"),
                      ("gemm_wgrad_a", 1, g, "F"), ("gemm_dx_shard_accum", 1, g, "F"),
-                     ("layernorm_backward", 2, 3.0 * w.T * w.d * 2, "B")]
+                     ("layernorm_backward", 3, 3.0 * w.T * w.d * 2, "B")]
         return segs
 
     def run(self, ev=None):
@@ -318,8 +319,7 @@ class Step:
             b.tpmlp_gemm2_shard_accum(self.H, self.B, N, Y=self.Y)
         i += 1; rec(i)
         if w.backward:
-            b.tpmlp_layernorm_gather(self.Xc, self.gamma, self.beta, N, self.Xg)
-            i += 1; rec(i)
+            # the forward's gathered LayerNorm output Xg, H and Hpre are the saved activations
             b.tpmlp_gemm_dh_geluprime(self.dY, self.B, self.Hpre, N, self.dHpre)
             i += 1; rec(i)
             b.tpmlp_gemm_wgrad_b(self.H, self.dY, N, self.dB)
@@ -393,7 +393,7 @@ def run_e2e(step, args, torch, binding):
             comp.wait_event(dx_out)
             binding.tpmlp_sp_backward(list(Xd[b].split(step.rows)), step.gamma, step.beta, step.A, step.B,
                                       step.Hpre, list(dYd[b].split(step.rows)), N, step.dXc, step.dA, step.dB,
-                                      step.dgamma, step.dbeta, bias=step.bias, H=step.H, ws=ws_b)
+                                      step.dgamma, step.dbeta, bias=step.bias, H=step.H, Xg=step.Xg, ws=ws_b)
             bwd_done.record(comp)
             copy.wait_event(bwd_done)
             with torch.cuda.stream(copy):
@@ -415,6 +415,50 @@ def run_e2e(step, args, torch, binding):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     return ms, h2d, d2h
+
+
+def time_calls(torch, fn, reps, warmup=3):
+    """Average ms of `fn` over `reps` back-to-back calls, CUDA events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_other_rows(step, torch, binding, pk):
+    """Rows of the hot path the step does not run: the explicit reduce-scatter (per-shard bf16 partials, then
+    the reduce-scatter kernel) on the step's shapes, and the fp32 path on the tiny fp32 workload."""
+    w = step.w
+    out = {}
+    if w.sp and (w.F // w.N) % 64 == 0:
+        P = torch.empty(w.N, w.T, w.d, dtype=torch.bfloat16, device="cuda")
+        Yc = [torch.empty(w.T // w.N, w.d, dtype=torch.bfloat16, device="cuda") for _ in range(w.N)]
+        g = 2.0 * w.T * w.d * w.F
+        ms_p = time_calls(torch, lambda: binding.tpmlp_gemm2_partials(step.H, step.B, w.N, P), 10)
+        ms_rs = time_calls(torch, lambda: binding.tpmlp_reduce_scatter(P, w.N, Yc), 20)
+        rs_bytes = (w.N + 1) * w.T * w.d * 2.0
+        out["gemm2_partials"] = {"ms": round(ms_p, 4), "TFLOP/s": round(g / (ms_p * 1e-3) / 1e12, 1),
+                                 "frac": round(g / (ms_p * 1e-3) / 1e12 / pk.get("bf16_tflops_sustained",
+                                                                                  pk["bf16_tflops"]), 3)}
+        out["reduce_scatter_explicit"] = {"ms": round(ms_rs, 4), "GB/s": round(rs_bytes / (ms_rs * 1e-3) / 1e9, 1),
+                                          "frac": round(rs_bytes / (ms_rs * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+                                          "bytes_per_launch": rs_bytes}
+        del P, Yc
+    t = inputs.WORKLOADS["tiny_fp32_fwd"]
+    f32 = lambda name: torch.from_numpy(np.ascontiguousarray(inputs.draw(t, name)[0])).cuda()
+    X, A, B, b = f32("X"), f32("A"), f32("B"), f32("bias")
+    Y = torch.empty(t.T, t.d, dtype=torch.float32, device="cuda")
+    ws = binding.workspace(binding.make_shape(t.T, t.d, t.F, t.N, binding.FP32), binding.OP_FWD)
+    ms = time_calls(torch, lambda: binding.tpmlp_forward(X, A, B, b, t.N, Y, ws=ws), 200)
+    out["fp32_tiny_forward"] = {"us": round(ms * 1e3, 2), "GFLOP/s": round(4.0 * t.T * t.d * t.F / (ms * 1e-3) / 1e9, 1),
+                                "workload": t.name, "bound": "launch latency (2 launches of a few CTAs)"}
+    return out
 
 
 def run_ours(args, w):
@@ -500,6 +544,10 @@ def run_ours(args, w):
     if st != binding.OK:
         raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
     e2e_ms = max_over_ranks(e2e_ms, dist)
+    other = run_other_rows(step, torch, binding, peaks()[0])
+    st, site = binding.tpmlp_get_device_status()
+    if st != binding.OK:
+        raise RuntimeError(f"device status after the other rows: {binding.status_string(st)} (site {site})")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -533,6 +581,7 @@ def run_ours(args, w):
                 "what": "block calls (tpmlp_sp_forward/backward) with X, dY copied from pinned host memory and Y, dX "
                         "copied back each step on a second stream, double-buffered so copies overlap the previous "
                         "step's kernels; weights and their gradients stay in HBM"},
+        "other_rows": other,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
     }

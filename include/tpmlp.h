@@ -140,11 +140,13 @@ TPMLP_API tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B
  *   X_chunks: host array of N pointers, each [T/N x d]; gamma, beta [d];
  *   Y_chunks: host array of N pointers, each [T/N x d] out; rs_mode:
  *   TPMLP_RS_FUSED or TPMLP_RS_PARTIALS; Hpre_out, H_out: NULL or [T x F]
- *   as in tpmlp_forward.  bf16 only. */
+ *   as in tpmlp_forward; Xg_out: NULL or [T x d] receiving the gathered
+ *   LayerNorm output (otherwise it lives in the workspace).  bf16 only. */
 TPMLP_API tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                                         const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
                                         void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out,
-                                        void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+                                        void* Xg_out, void* workspace, size_t workspace_bytes,
+                                        tpmlp_stream_t stream);
 
 /* MLP backward, the chain rule of the forward (the pages name two backward
  * AllReduces per block, glossary page, tensor-parallel section):
@@ -165,10 +167,12 @@ TPMLP_API tpmlp_status tpmlp_backward(const void* X, const void* A, const void* 
  * of the forward All-Gather), LayerNorm backward per chunk.
  *   dX_chunks: host array of N pointers [T/N x d] (bf16) out;
  *   dgamma, dbeta: [d] fp32 out, summed over all chunks; Hpre, H, dA, dB,
- *   dbias as in tpmlp_backward.  bf16 only. */
+ *   dbias as in tpmlp_backward; Xg: NULL (the LayerNorm output is
+ *   recomputed) or the forward's Xg_out.  bf16 only. */
 TPMLP_API tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                                          const void* A, const void* B, const void* bias, const void* Hpre,
-                                         const void* H, const void* const* dY_chunks, const tpmlp_shape* shape,
+                                         const void* H, const void* Xg, const void* const* dY_chunks,
+                                         const tpmlp_shape* shape,
                                          void* const* dX_chunks, void* dA, void* dB, void* dbias, void* dgamma,
                                          void* dbeta, void* workspace, size_t workspace_bytes,
                                          tpmlp_stream_t stream);

@@ -42,11 +42,11 @@ _SIGS = {
     "tpmlp_workspace_size": ([_SP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "tpmlp_get_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "tpmlp_forward": ([_P, _P, _P, _P, _SP, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
-    "tpmlp_sp_forward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _SP, _PP, ctypes.c_int, _P, _P, _P,
+    "tpmlp_sp_forward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _SP, _PP, ctypes.c_int, _P, _P, _P, _P,
                           ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_backward": ([_P, _P, _P, _P, _P, _P, _P, _SP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
-    "tpmlp_sp_backward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _PP, _SP, _PP, _P, _P, _P, _P, _P, _P,
-                           ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_sp_backward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _PP, _SP, _PP, _P, _P, _P, _P, _P,
+                           _P, ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_gemm1_bias_gelu": ([_P, _P, _P, _SP, _P, _P, _P], ctypes.c_int),
     "tpmlp_gemm2_shard_accum": ([_P, _P, _SP, _P, _PP, _P], ctypes.c_int),
     "tpmlp_gemm2_partials": ([_P, _P, _SP, _P, _P], ctypes.c_int),
@@ -146,7 +146,7 @@ def tpmlp_forward(X, A, B, bias, N, Y, Hpre_out=None, H_out=None, ws=None, strea
 
 
 def tpmlp_sp_forward(X_chunks, gamma, beta, A, B, N, Y_chunks, bias=None, eps=1e-5, rs_mode=RS_FUSED,
-                     Hpre_out=None, H_out=None, ws=None, stream=None):
+                     Hpre_out=None, H_out=None, Xg_out=None, ws=None, stream=None):
     rows, d = X_chunks[0].shape
     shape = make_shape(rows * N, d, A.shape[1], N)
     op = OP_SP_FWD if rs_mode == RS_FUSED else OP_SP_FWD_PARTIALS
@@ -155,7 +155,7 @@ def tpmlp_sp_forward(X_chunks, gamma, beta, A, B, N, Y_chunks, bias=None, eps=1e
     yp, _ya = _ptrs(Y_chunks)
     _check("tpmlp_sp_forward", lib().tpmlp_sp_forward(xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias),
                                                       ctypes.byref(shape), yp, rs_mode, _ptr(Hpre_out), _ptr(H_out),
-                                                      _ptr(ws), ws.numel(), _stream(stream)))
+                                                      _ptr(Xg_out), _ptr(ws), ws.numel(), _stream(stream)))
     return Y_chunks
 
 
@@ -169,7 +169,7 @@ def tpmlp_backward(X, A, B, bias, Hpre, dY, N, dX, dA, dB, dbias=None, H=None, w
 
 
 def tpmlp_sp_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_chunks, dA, dB, dgamma, dbeta,
-                      bias=None, dbias=None, eps=1e-5, H=None, ws=None, stream=None):
+                      bias=None, dbias=None, eps=1e-5, H=None, Xg=None, ws=None, stream=None):
     rows, d = X_chunks[0].shape
     shape = make_shape(rows * N, d, A.shape[1], N)
     ws = workspace(shape, OP_SP_BWD, A.device) if ws is None else ws
@@ -177,7 +177,8 @@ def tpmlp_sp_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_chunks
     dyp, _dya = _ptrs(dY_chunks)
     dxp, _dxa = _ptrs(dX_chunks)
     _check("tpmlp_sp_backward", lib().tpmlp_sp_backward(
-        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _ptr(Hpre), _ptr(H), dyp, ctypes.byref(shape), dxp,
+        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _ptr(Hpre), _ptr(H), _ptr(Xg), dyp,
+        ctypes.byref(shape), dxp,
         _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
 
 

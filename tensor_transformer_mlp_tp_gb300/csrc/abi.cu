@@ -72,6 +72,14 @@ tpmlp_status device_ctx(DeviceCtx* out) {
   return TPMLP_OK;
 }
 
+}  // namespace
+
+cudaError_t current_device_ctx(DeviceCtx* out) {
+  return device_ctx(out) == TPMLP_OK ? cudaSuccess : cudaErrorUnknown;
+}
+
+namespace {
+
 tpmlp_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return TPMLP_OK;
   if (e == cudaErrorNotSupported) return TPMLP_ERR_UNSUPPORTED;
@@ -117,7 +125,6 @@ struct Sizes {
   size_t td, tf, ptd, colsum, lnbwd;
 };
 
-constexpr int kLnBwdMaxBlocks = 304;  // 2 blocks per SM of a 152-SM GB300
 
 Sizes sizes_of(const tpmlp_shape* s) {
   const size_t T = static_cast<size_t>(s->tokens), d = static_cast<size_t>(s->d), F = static_cast<size_t>(s->ffn);
@@ -128,8 +135,7 @@ Sizes sizes_of(const tpmlp_shape* s) {
   z.ptd = align_up(static_cast<size_t>(s->n_shards) * T * d * 2);
   const size_t m_blocks = (T + kBM - 1) / kBM;
   z.colsum = align_up(4 * m_blocks * F * 4);
-  const size_t blocks = static_cast<size_t>(layernorm_bwd_blocks(static_cast<int>(T), kLnBwdMaxBlocks));
-  z.lnbwd = align_up(blocks * 2 * d * 4);
+  z.lnbwd = align_up(layernorm_bwd_scratch_floats(static_cast<int>(T), static_cast<int>(d)) * 4);
   return z;
 }
 
@@ -329,9 +335,8 @@ cudaError_t do_ln_bwd(const DeviceCtx& c, const void* const* X_chunks, const voi
   r.eps = eps;
   r.gamma = gamma;
   r.src = dXg;
-  r.partial = partial;
-  (void)c;
-  return launch_layernorm_bwd(r, kLnBwdMaxBlocks, static_cast<float*>(dgamma), static_cast<float*>(dbeta), st);
+  return launch_layernorm_bwd(r, partial, layernorm_bwd_scratch_floats(r.rows, r.d), c, static_cast<float*>(dgamma),
+                              static_cast<float*>(dbeta), st);
 }
 
 // Backward core shared by tpmlp_backward and tpmlp_sp_backward.  With Hpre
@@ -444,12 +449,12 @@ tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const vo
 
 tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                               const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
-                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out, void* workspace,
-                              size_t workspace_bytes, tpmlp_stream_t stream) {
+                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out, void* Xg_out,
+                              void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !opt_ok(Hpre_out) || !opt_ok(H_out))
+  if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !opt_ok(Hpre_out) || !opt_ok(H_out) || !opt_ok(Xg_out))
     return TPMLP_ERR_INVALID_ARG;
   if (!chunks_ok(X_chunks, shape->n_shards) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
   if (!(eps >= 0.f)) return TPMLP_ERR_INVALID_ARG;
@@ -465,6 +470,7 @@ tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, co
   void* Xg = ws.take(z.td);
   void* H = ws.take(z.tf);
   if (H_out != nullptr) H = H_out;
+  if (Xg_out != nullptr) Xg = Xg_out;
   cudaError_t e = do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, s);
   if (e == cudaSuccess) e = do_gemm1(c, Xg, A, bias, shape, H, Hpre_out, kEpiBiasGelu, s);
   if (e == cudaSuccess) {
@@ -498,14 +504,15 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
 
 tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                                const void* A, const void* B, const void* bias, const void* Hpre, const void* H,
-                               const void* const* dY_chunks, const tpmlp_shape* shape, void* const* dX_chunks,
+                               const void* Xg_saved, const void* const* dY_chunks, const tpmlp_shape* shape,
+                               void* const* dX_chunks,
                                void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
                                size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({gamma, beta, A, B, dA, dB, dgamma, dbeta}) || !opt_ok(bias) || !opt_ok(Hpre) || !opt_ok(H) ||
-      !opt_ok(dbias))
+      !opt_ok(Xg_saved) || !opt_ok(dbias))
     return TPMLP_ERR_INVALID_ARG;
   const int n = shape->n_shards;
   if (!chunks_ok(X_chunks, n) || !chunks_ok(dY_chunks, n) || !chunks_ok(dX_chunks, n)) return TPMLP_ERR_INVALID_ARG;
@@ -522,8 +529,13 @@ tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, c
   void* dYg = ws.take(z.td);
   void* dXg = ws.take(z.td);
   float* lnpart = static_cast<float*>(ws.take(z.lnbwd));
-  cudaError_t e = do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, s);
-  if (e != cudaSuccess) return cuda_status(e);
+  cudaError_t e = cudaSuccess;
+  if (Xg_saved != nullptr) {
+    Xg = const_cast<void*>(Xg_saved);
+  } else {
+    e = do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   // The All-Gather of dY is free when the chunks already lie back to back.
   const size_t chunk_bytes = static_cast<size_t>(shape->tokens / n) * shape->d * 2;
   bool contiguous = true;

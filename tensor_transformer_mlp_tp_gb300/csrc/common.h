@@ -85,6 +85,15 @@ struct RowParams {
   void* dst;                  // contiguous [rows x d] bf16 output
   float* partial;             // column partial sums [blocks x 2d] fp32 (LayerNorm backward)
   long long shard_stride;     // elements between partials (reduce-scatter)
+  float* stats;               // [rows x 2] fp32 mean, rstd (LayerNorm backward)
+  int rows_per_block;         // rows summed by one column-partial block (LayerNorm backward)
+  int slots;                  // shared-memory row slots of the streaming kernels
+  unsigned int* err;          // device error words
+  unsigned long long timeout_ns;
 };
+
+// Wait sites of the row-streaming kernels.
+constexpr uint32_t kSiteRowProducer = 16;
+constexpr uint32_t kSiteRowConsumer = 17;
 
 }  // namespace tpmlp

@@ -44,10 +44,15 @@ struct DeviceCtx {
 cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s);
 
 cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
-// LayerNorm backward with at most `max_blocks` CTAs; r.partial must hold
-// layernorm_bwd_blocks(rows, max_blocks) x 2 d floats.
-cudaError_t launch_layernorm_bwd(const RowParams& r, int max_blocks, float* dgamma, float* dbeta, cudaStream_t s);
+// LayerNorm backward using `scratch` (cap_floats floats: row statistics and dgamma/dbeta column partials).
+// layernorm_bwd_scratch_floats(rows, d) is the size of the default layout; a smaller scratch still works
+// (wider column blocks) down to 2 rows + 2 d floats.
+cudaError_t launch_layernorm_bwd(const RowParams& r, float* scratch, size_t cap_floats, const DeviceCtx& ctx,
+                                 float* dgamma, float* dbeta, cudaStream_t s);
+size_t layernorm_bwd_scratch_floats(int rows, int d);
 int layernorm_bwd_blocks(int rows, int max_blocks);
+// The device context (error words, SM count, wait budget) of the current device.
+cudaError_t current_device_ctx(DeviceCtx* out);
 // Largest d the LayerNorm backward supports (its 2 d fp32 accumulators live in shared memory).
 constexpr int kLnBwdMaxD = 16384;
 cudaError_t launch_reduce_scatter(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);

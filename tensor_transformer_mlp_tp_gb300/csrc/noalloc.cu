@@ -11,7 +11,8 @@
 // is part of the library's device image, so the call itself allocates nothing.
 //
 // Limits and sharing:
-//  - The array holds kNoAllocBlocks x 2 x kNoAllocMaxD floats (9.5 MiB).  Every
+//  - The array holds kNoAllocBlocks x 2 x kNoAllocMaxD floats (9.5 MiB): the
+//    row statistics and dgamma/dbeta column partials of the backward.  Every
 //    GPU that loads the library keeps it until the process exits.
 //  - d above kNoAllocMaxD is rejected with TPMLP_ERR_UNSUPPORTED before
 //    anything is launched.
@@ -82,6 +83,8 @@ extern "C" tpmlp_status tpmlp_layernorm_backward_noalloc(const void* const* X_ch
     if (!aligned16(X_chunks[i]) || !aligned16(dX_chunks[i])) return TPMLP_ERR_INVALID_ARG;
   float* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return TPMLP_ERR_CUDA;
+  DeviceCtx ctx;
+  if (current_device_ctx(&ctx) != cudaSuccess) return TPMLP_ERR_CUDA;
   RowParams r{};
   for (int i = 0; i < n; ++i) {
     r.in_chunks.p[i] = X_chunks[i];
@@ -94,8 +97,8 @@ extern "C" tpmlp_status tpmlp_layernorm_backward_noalloc(const void* const* X_ch
   r.eps = eps;
   r.gamma = gamma;
   r.src = dXg;
-  r.partial = scratch;  // at most kNoAllocBlocks x 2 d floats: within the array for d <= kNoAllocMaxD
-  const cudaError_t e = launch_layernorm_bwd(r, kNoAllocBlocks, static_cast<float*>(dgamma),
+  // the launcher lays its statistics and partial sums out within the array's kNoAllocFloats
+  const cudaError_t e = launch_layernorm_bwd(r, scratch, kNoAllocFloats, ctx, static_cast<float*>(dgamma),
                                              static_cast<float*>(dbeta), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA;
 }

@@ -251,6 +251,198 @@ __global__ void __launch_bounds__(256) k_layernorm_bwd(const RowParams p) {
     p.partial[static_cast<long long>(blockIdx.x) * 2 * p.d + c] = acc[c];
 }
 
+// ----------------------------------------------------------------------------- streamed row kernels
+//
+// Persistent CTAs (one per SM).  Warp 0 is the producer: one lane streams the
+// CTA's rows (row blockIdx.x + i * gridDim.x for i = 0, 1, ...) into a ring of
+// shared-memory slots with 1-D bulk copies, completion counted on `full[slot]`.
+// Warps 1..8 are consumers: consumer c takes rows i = c, c + 8, ..., copies
+// the row from its slot into registers (V 16-byte vectors per lane), frees the
+// slot (`empty[slot]`) and computes.  Every wait is bounded.
+
+constexpr int kStreamConsumers = 8;
+constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
+
+__device__ __forceinline__ uint8_t* align128(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 127) & ~uintptr_t(127));
+}
+
+// Producer loop shared by the streamed kernels: `copies` rows of `row_bytes`
+// per slot (the second, if any, from `src2` rows of the same index).
+__device__ __forceinline__ void stream_producer(const RowParams& p, uint8_t* ring, uint32_t slot_bytes,
+                                                uint32_t row_bytes, uint64_t* full, uint64_t* empty, int n_rows,
+                                                const WaitCtx& wc, bool second) {
+  uint32_t issued_mask = 0, issued_parity = 0;
+  for (int i = 0; i < n_rows; ++i) {
+    const int slot = i % p.slots;
+    const uint32_t ph = static_cast<uint32_t>(i / p.slots) & 1u;
+    if (!wait_bounded(empty + slot, ph ^ 1u, wc, kSiteRowProducer)) break;
+    const int row = blockIdx.x + i * gridDim.x;
+    mbar_arrive_expect_tx(full + slot, second ? 2 * row_bytes : row_bytes);
+    bulk_load(ring + slot * slot_bytes, chunk_row(p, row), row_bytes, full + slot);
+    if (second)
+      bulk_load(ring + slot * slot_bytes + row_bytes,
+                static_cast<const __nv_bfloat16*>(p.src) + static_cast<long long>(row) * p.d, row_bytes, full + slot);
+    if (slot < 32) {
+      issued_mask |= 1u << slot;
+      issued_parity = (issued_parity & ~(1u << slot)) | (ph << slot);
+    }
+  }
+  // copies in flight must land before the CTA exits
+  for (int s = 0; s < p.slots && s < 32; ++s)
+    if (issued_mask & (1u << s)) wait_drain(full + s, (issued_parity >> s) & 1u, p.timeout_ns);
+}
+
+__device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, const WaitCtx& wc) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, wc, kSiteRowConsumer) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// LayerNorm backward, row part: per row dx = rstd (g - mean(g) - xhat mean(g xhat)), g = dy gamma, and
+// the row's (mean, rstd) for the column part.  x and dy rows stream through the ring; d = 256 V.
+template <int V>
+__global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_rows_stream(const RowParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = align128(smem_raw);
+  const uint32_t row_bytes = static_cast<uint32_t>(p.d) * 2u;
+  uint4* gam = reinterpret_cast<uint4*>(ring + p.slots * 2 * row_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(gam + p.d / 8);
+  uint64_t* empty = full + p.slots;
+  int* abort_flag = reinterpret_cast<int*>(empty + p.slots);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.slots; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  for (int i = threadIdx.x; i < p.d / 8; i += blockDim.x) gam[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma) + i);
+  __syncthreads();
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  const int n_rows = p.rows > static_cast<int>(blockIdx.x)
+                         ? (p.rows - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / gridDim.x
+                         : 0;
+  if (warp == 0) {
+    if (lane == 0) stream_producer(p, ring, 2 * row_bytes, row_bytes, full, empty, n_rows, wc, true);
+  } else {
+    for (int i = warp - 1; i < n_rows; i += kStreamConsumers) {
+      const int slot = i % p.slots;
+      if (!stream_wait(full + slot, static_cast<uint32_t>(i / p.slots) & 1u, wc)) break;
+      const uint4* xs = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes);
+      const uint4* ds = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes + row_bytes);
+      // x in registers; dy re-read from the slot (kept until the last pass) to stay clear of spills at V = 16
+      uint4 xv[V];
+#pragma unroll
+      for (int v = 0; v < V; ++v) xv[v] = xs[v * 32 + lane];
+      float s = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        float f[8];
+        unpack8(xv[v], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += f[e];
+      }
+      const float mean = warp_sum(s) / static_cast<float>(p.d);
+      float q = 0.f, sg = 0.f, sgc = 0.f;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        float f[8], dy[8], g[8];
+        unpack8(xv[v], f);
+        unpack8(ds[v * 32 + lane], dy);
+        unpack8(gam[v * 32 + lane], g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float c = f[e] - mean;
+          const float gg = dy[e] * g[e];
+          q += c * c;
+          sg += gg;
+          sgc += gg * c;
+        }
+      }
+      q = warp_sum(q);
+      sg = warp_sum(sg);
+      sgc = warp_sum(sgc);
+      const float rstd = rsqrtf(q / static_cast<float>(p.d) + p.eps);
+      const float m1 = sg / static_cast<float>(p.d);
+      const float m2 = rstd * sgc / static_cast<float>(p.d);
+      const int row = blockIdx.x + i * gridDim.x;
+      uint4* dx4 = reinterpret_cast<uint4*>(out_chunk_row(p, row));
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        float f[8], dy[8], g[8], o[8];
+        unpack8(xv[v], f);
+        unpack8(ds[v * 32 + lane], dy);
+        unpack8(gam[v * 32 + lane], g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = rstd * (dy[e] * g[e] - m1 - (f[e] - mean) * rstd * m2);
+        dx4[v * 32 + lane] = pack8(o);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + slot);
+      if (lane == 0) reinterpret_cast<float2*>(p.stats)[row] = make_float2(mean, rstd);
+    }
+  }
+  __syncthreads();
+}
+
+// LayerNorm backward, column part: block (bx, by) sums dgamma += dy xhat and dbeta += dy over rows
+// [by R, by R + R) for the 8 columns of each thread's 16-byte vector; partial row `by` of [blocks x 2d].
+__global__ void __launch_bounds__(256) k_layernorm_bwd_columns(const RowParams p) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= p.d / 8) return;
+  const int r0 = blockIdx.y * p.rows_per_block;
+  const int r1 = min(p.rows, r0 + p.rows_per_block);
+  float dg[8], db[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) dg[e] = db[e] = 0.f;
+  const float2* st = reinterpret_cast<const float2*>(p.stats);
+  int r = r0;
+  for (; r + 4 <= r1; r += 4) {
+    uint4 xr[4], dr[4];
+    float2 sr[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      xr[k] = __ldg(reinterpret_cast<const uint4*>(chunk_row(p, r + k)) + v);
+      dr[k] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.src) +
+                                                   static_cast<long long>(r + k) * p.d) + v);
+      sr[k] = st[r + k];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float f[8], dy[8];
+      unpack8(xr[k], f);
+      unpack8(dr[k], dy);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        dg[e] += dy[e] * (f[e] - sr[k].x) * sr[k].y;
+        db[e] += dy[e];
+      }
+    }
+  }
+  for (; r < r1; ++r) {
+    float f[8], dy[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(chunk_row(p, r)) + v), f);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.src) +
+                                                 static_cast<long long>(r) * p.d) + v), dy);
+    const float2 sr = st[r];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      dg[e] += dy[e] * (f[e] - sr.x) * sr.y;
+      db[e] += dy[e];
+    }
+  }
+  float* out = p.partial + static_cast<long long>(blockIdx.y) * 2 * p.d + v * 8;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    out[e] = dg[e];
+    out[p.d + e] = db[e];
+  }
+}
+
 // ----------------------------------------------------------------------------- reduce-scatter, gather, column sum
 
 // Y_chunk_j[r] = bf16(sum_{i<N} P_i[j T/N + r]) in fp32, shard 0 first.
@@ -326,6 +518,24 @@ int stream_grid(long long work_items, int sm_count) {
 
 }  // namespace
 
+template <typename K>
+static cudaError_t launch_stream(K kern, const RowParams& r, size_t smem, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kStreamThreads, smem, s>>>(r);
+  return cudaGetLastError();
+}
+
+// Shared-memory row slots for rows of `slot_bytes`: about 128 KB of rows in flight per SM.
+static int stream_slots(size_t slot_bytes) {
+  const size_t n = (128u * 1024u) / slot_bytes;
+  return static_cast<int>(n < 2 ? 2 : (n > 32 ? 32 : n));
+}
+
+// LayerNorm forward: one warp per row (two for d = 8192) with the row in
+// registers.  (A shared-memory-streamed variant was measured slower on GB300 in
+// the SP step: between GEMMs this kernel's bandwidth is held by the write-back
+// of the dirty L2 lines the previous kernels leave, not by its load latency.)
 cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
   (void)ctx;
   if (r.rows <= 0) return cudaSuccess;
@@ -348,8 +558,67 @@ int layernorm_bwd_blocks(int rows, int max_blocks) {
   return groups < max_blocks ? (groups < 1 ? 1 : groups) : max_blocks;
 }
 
-cudaError_t launch_layernorm_bwd(const RowParams& r, int max_blocks, float* dgamma, float* dbeta, cudaStream_t s) {
-  if (r.rows <= 0) return cudaSuccess;
+namespace {
+
+constexpr int kLnBwdColumnRows = 64;     // rows per column-partial block of the streamed backward
+constexpr int kLnBwdMaxBlocksOld = 304;  // CTAs of the register-free backward
+
+bool lnbwd_streamed(int d) {
+  const int V = d % 256 == 0 ? d / 256 : 0;
+  return V == 1 || V == 2 || V == 4 || V == 8 || V == 16;
+}
+
+size_t align64(size_t x) { return (x + 63) / 64 * 64; }
+
+}  // namespace
+
+size_t layernorm_bwd_scratch_floats(int rows, int d) {
+  if (lnbwd_streamed(d))
+    return align64(2 * static_cast<size_t>(rows)) +
+           static_cast<size_t>((rows + kLnBwdColumnRows - 1) / kLnBwdColumnRows) * 2 * d;
+  return static_cast<size_t>(layernorm_bwd_blocks(rows, kLnBwdMaxBlocksOld)) * 2 * d;
+}
+
+cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap_floats, const DeviceCtx& ctx,
+                                 float* dgamma, float* dbeta, cudaStream_t s) {
+  if (r0.rows <= 0) return cudaSuccess;
+  RowParams r = r0;
+  r.err = ctx.err;
+  r.timeout_ns = ctx.timeout_ns;
+  if (lnbwd_streamed(r.d) && cap_floats >= align64(2 * static_cast<size_t>(r.rows)) + 2 * static_cast<size_t>(r.d)) {
+    // scratch: [rows x 2] statistics, then [blocks x 2 d] column partials; widen the column blocks if the
+    // scratch is smaller than the default layout needs
+    r.stats = scratch;
+    r.partial = scratch + align64(2 * static_cast<size_t>(r.rows));
+    const size_t room = cap_floats - align64(2 * static_cast<size_t>(r.rows));
+    int rpb = kLnBwdColumnRows;
+    while (static_cast<size_t>((r.rows + rpb - 1) / rpb) * 2 * r.d > room) rpb *= 2;
+    r.rows_per_block = rpb;
+    const size_t row_bytes = static_cast<size_t>(r.d) * 2;
+    r.slots = stream_slots(2 * row_bytes);
+    const size_t smem = 128 + r.slots * 2 * row_bytes + row_bytes + 16 * static_cast<size_t>(r.slots) + 16;
+    const int grid = r.rows < ctx.sm_count ? r.rows : ctx.sm_count;
+    cudaError_t e;
+    switch (r.d / 256) {
+      case 1: e = launch_stream(k_layernorm_bwd_rows_stream<1>, r, smem, grid, s); break;
+      case 2: e = launch_stream(k_layernorm_bwd_rows_stream<2>, r, smem, grid, s); break;
+      case 4: e = launch_stream(k_layernorm_bwd_rows_stream<4>, r, smem, grid, s); break;
+      case 8: e = launch_stream(k_layernorm_bwd_rows_stream<8>, r, smem, grid, s); break;
+      default: e = launch_stream(k_layernorm_bwd_rows_stream<16>, r, smem, grid, s); break;
+    }
+    if (e != cudaSuccess) return e;
+    const int blocks = (r.rows + rpb - 1) / rpb;
+    k_layernorm_bwd_columns<<<dim3((r.d / 8 + 255) / 256, blocks), 256, 0, s>>>(r);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_column_sum<<<(2 * r.d + 31) / 32, 256, 0, s>>>(r.partial, blocks, 2 * r.d, 2LL * r.d, dgamma, dbeta, r.d, 0);
+    return cudaGetLastError();
+  }
+  // any other width: per-block shared-memory accumulation of dgamma/dbeta
+  int max_blocks = static_cast<int>(cap_floats / (2 * static_cast<size_t>(r.d)));
+  if (max_blocks > kLnBwdMaxBlocksOld) max_blocks = kLnBwdMaxBlocksOld;
+  if (max_blocks < 1) return cudaErrorInvalidValue;
+  r.partial = scratch;
   const int grid = layernorm_bwd_blocks(r.rows, max_blocks);
   const size_t smem = static_cast<size_t>(2) * r.d * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(k_layernorm_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize,

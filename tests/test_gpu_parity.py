@@ -204,7 +204,8 @@ def test_backward(T, d, N, saved):
 
 
 @pytest.mark.parametrize("T,d,N", [(256, 128, 4), (384, 192, 8), (64, 256, 2)])
-def test_sp_backward(T, d, N):
+@pytest.mark.parametrize("save_xg", [False, True])
+def test_sp_backward(T, d, N, save_xg):
     w = inputs.small_workload(T, d, N, sp=True, backward=True, bias=None)
     X, g, b, A, B, dY = _draw(w, "X", "gamma", "beta", "A", "B", "dY")
     F = 4 * d
@@ -215,13 +216,14 @@ def test_sp_backward(T, d, N):
     Hpre = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
     Hs = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
     Y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    Xg = torch.empty(T, d, dtype=torch.bfloat16, device="cuda") if save_xg else None
     binding.tpmlp_sp_forward(xs, dev(g[0]), dev(b[0]), dev(A[0]), dev(B[0]), N, list(Y.split(rows)), Hpre_out=Hpre,
-                             H_out=Hs)
+                             H_out=Hs, Xg_out=Xg)
     dX = [Guarded((rows, d)) for _ in range(N)]
     dA, dB = Guarded((d, F)), Guarded((F, d))
     dgam, dbet = Guarded((d,), torch.float32), Guarded((d,), torch.float32)
     binding.tpmlp_sp_backward(xs, dev(g[0]), dev(b[0]), dev(A[0]), dev(B[0]), Hpre, dys, N, [x.t for x in dX], dA.t,
-                              dB.t, dgam.t, dbet.t, H=Hs)
+                              dB.t, dgam.t, dbet.t, H=Hs, Xg=Xg)
     torch.cuda.synchronize()
     ref = oracle.sp_backward(_chunks(X[1], N), g[1], b[1], 1e-5, A[1], B[1], None, _chunks(dY[1], N), N)
     assert_bf16_close("dX", np.concatenate([f64(x.t) for x in dX]), np.concatenate(ref["dX_chunks"]))
@@ -321,3 +323,22 @@ def test_device_gelu_and_gelu_prime_pointwise():
         err = np.abs(got - ref[:, None])
         bound = np.abs(ref[:, None]) * 2.0 ** -8 + 1e-6
         assert np.all(err <= bound), float(np.max(err - bound))
+
+
+@pytest.mark.parametrize("T,d,N", [(1000, 1024, 8), (96, 2048, 4), (64, 512, 2), (200, 4096, 8), (24, 136, 3)])
+def test_layernorm_backward_step(T, d, N):
+    """The LayerNorm backward step alone (streamed row kernel + column partials, or the generic kernel)."""
+    w = inputs.small_workload(T, d, N, sp=True, backward=True, name=f"lnbwd_{T}_{d}_{N}")
+    X, g = inputs.draw(w, "X"), inputs.draw(w, "gamma")
+    dXg = inputs.draw(w, "dY")
+    rows = T // N
+    dX = [Guarded((rows, d)) for _ in range(N)]
+    dga, dbe = Guarded((d,), torch.float32), Guarded((d,), torch.float32)
+    binding.tpmlp_layernorm_backward(list(dev(X[0]).split(rows)), dev(g[0]), dev(dXg[0]), N, [x.t for x in dX],
+                                     dga.t, dbe.t)
+    torch.cuda.synchronize()
+    refs = [oracle.layer_norm_backward(X[1][lo:hi], g[1], 1e-5, dXg[1][lo:hi]) for lo, hi in oracle.chunk_ranges(T, N)]
+    assert_bf16_close("dX", np.concatenate([f64(x.t) for x in dX]), np.concatenate([r[0] for r in refs]))
+    assert_bf16_close("dgamma", f64(dga.t), sum(r[1] for r in refs))
+    assert_bf16_close("dbeta", f64(dbe.t), sum(r[2] for r in refs))
+    assert all(x.intact() for x in dX + [dga, dbe])
