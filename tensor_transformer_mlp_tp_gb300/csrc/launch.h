@@ -44,9 +44,9 @@ struct DeviceCtx {
 cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s);
 
 cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
-// LayerNorm backward using `scratch` (cap_floats floats: row statistics and dgamma/dbeta column partials).
-// layernorm_bwd_scratch_floats(rows, d) is the size of the default layout; a smaller scratch still works
-// (wider column blocks) down to 2 rows + 2 d floats.
+// LayerNorm backward using `scratch` (cap_floats floats of dgamma/dbeta block partials, 2 d per block).
+// layernorm_bwd_scratch_floats(rows, d) covers the default block count; a smaller scratch runs fewer
+// blocks, down to one (2 d floats).
 cudaError_t launch_layernorm_bwd(const RowParams& r, float* scratch, size_t cap_floats, const DeviceCtx& ctx,
                                  float* dgamma, float* dbeta, cudaStream_t s);
 size_t layernorm_bwd_scratch_floats(int rows, int d);

@@ -299,10 +299,25 @@ __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, cons
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// LayerNorm backward, row part: per row dx = rstd (g - mean(g) - xhat mean(g xhat)), g = dy gamma, and
-// the row's (mean, rstd) for the column part.  x and dy rows stream through the ring; d = 256 V.
-template <int V>
-__global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_rows_stream(const RowParams p) {
+// LayerNorm backward in one pass over x and dy.  Teams of TW warps (8 / TW
+// teams per CTA) each take one row of the ring at a time; thread j of a team
+// owns the 16-byte column vectors j + k·32·TW, k < VT (d = 256 TW VT).  Row
+// statistics come from warp shuffles plus one team barrier per reduction
+// (double-buffered scratch, two barriers per row); dx goes to the row's chunk;
+// dgamma and dbeta for the thread's columns accumulate in registers over all
+// rows the team processes.  At the end the teams' sums are added in team order
+// into the CTA's partial row [2 d], which a fixed-order column sum reduces.
+__device__ __forceinline__ void team_sync(int team, int tw) {
+  if (tw == 1) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * tw) : "memory");
+  }
+}
+
+template <int VT, int TW>
+__global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const RowParams p) {
+  constexpr int kTeams = kStreamConsumers / TW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align128(smem_raw);
   const uint32_t row_bytes = static_cast<uint32_t>(p.d) * 2u;
@@ -310,11 +325,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_rows_stream
   uint64_t* full = reinterpret_cast<uint64_t*>(gam + p.d / 8);
   uint64_t* empty = full + p.slots;
   int* abort_flag = reinterpret_cast<int*>(empty + p.slots);
+  __shared__ float red1[2][kStreamConsumers];
+  __shared__ float red3[2][kStreamConsumers][3];
+  __shared__ int vote[2][kStreamConsumers];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.slots; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
+      mbar_init(empty + s, TW);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -326,34 +344,66 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_rows_stream
   const int n_rows = p.rows > static_cast<int>(blockIdx.x)
                          ? (p.rows - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / gridDim.x
                          : 0;
+  const int cw = warp - 1;        // consumer warp index
+  const int team = cw / TW;
+  const int tw = cw % TW;         // warp within the team
+  const int j = tw * 32 + lane;   // thread within the team
+  float dg[VT][8], db[VT][8];
+#pragma unroll
+  for (int k = 0; k < VT; ++k)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dg[k][e] = db[k][e] = 0.f;
   if (warp == 0) {
     if (lane == 0) stream_producer(p, ring, 2 * row_bytes, row_bytes, full, empty, n_rows, wc, true);
   } else {
-    for (int i = warp - 1; i < n_rows; i += kStreamConsumers) {
+    int parity_buf = 0;
+    for (int i = team; i < n_rows; i += kTeams, parity_buf ^= 1) {
       const int slot = i % p.slots;
-      if (!stream_wait(full + slot, static_cast<uint32_t>(i / p.slots) & 1u, wc)) break;
+      // Every warp of the team waits (bounded) on its own; the outcomes are voted at the first team
+      // barrier, so the team leaves the loop together and no warp is left waiting at a barrier.
+      const bool ok = stream_wait(full + slot, static_cast<uint32_t>(i / p.slots) & 1u, wc);
       const uint4* xs = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes);
       const uint4* ds = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes + row_bytes);
-      // x in registers; dy re-read from the slot (kept until the last pass) to stay clear of spills at V = 16
-      uint4 xv[V];
+      uint4 xv[VT], dv[VT];
 #pragma unroll
-      for (int v = 0; v < V; ++v) xv[v] = xs[v * 32 + lane];
+      for (int k = 0; k < VT; ++k) {
+        xv[k] = ok ? xs[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
+        dv[k] = ok ? ds[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(empty + slot);
       float s = 0.f;
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
+      for (int k = 0; k < VT; ++k) {
         float f[8];
-        unpack8(xv[v], f);
+        unpack8(xv[k], f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) s += f[e];
       }
-      const float mean = warp_sum(s) / static_cast<float>(p.d);
+      s = warp_sum(s);
+      bool team_ok = ok;
+      if (TW > 1) {
+        if (lane == 0) {
+          red1[parity_buf][cw] = s;
+          vote[parity_buf][cw] = ok ? 1 : 0;
+        }
+        team_sync(team, TW);
+        s = 0.f;
+#pragma unroll
+        for (int w = 0; w < TW; ++w) {
+          s += red1[parity_buf][team * TW + w];
+          team_ok = team_ok && vote[parity_buf][team * TW + w] != 0;
+        }
+      }
+      if (!team_ok) break;
+      const float mean = s / static_cast<float>(p.d);
       float q = 0.f, sg = 0.f, sgc = 0.f;
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
+      for (int k = 0; k < VT; ++k) {
         float f[8], dy[8], g[8];
-        unpack8(xv[v], f);
-        unpack8(ds[v * 32 + lane], dy);
-        unpack8(gam[v * 32 + lane], g);
+        unpack8(xv[k], f);
+        unpack8(dv[k], dy);
+        unpack8(gam[j + k * 32 * TW], g);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float c = f[e] - mean;
@@ -366,80 +416,62 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_rows_stream
       q = warp_sum(q);
       sg = warp_sum(sg);
       sgc = warp_sum(sgc);
+      if (TW > 1) {
+        if (lane == 0) {
+          red3[parity_buf][cw][0] = q;
+          red3[parity_buf][cw][1] = sg;
+          red3[parity_buf][cw][2] = sgc;
+        }
+        team_sync(team, TW);
+        q = sg = sgc = 0.f;
+#pragma unroll
+        for (int w = 0; w < TW; ++w) {
+          q += red3[parity_buf][team * TW + w][0];
+          sg += red3[parity_buf][team * TW + w][1];
+          sgc += red3[parity_buf][team * TW + w][2];
+        }
+      }
       const float rstd = rsqrtf(q / static_cast<float>(p.d) + p.eps);
       const float m1 = sg / static_cast<float>(p.d);
       const float m2 = rstd * sgc / static_cast<float>(p.d);
       const int row = blockIdx.x + i * gridDim.x;
       uint4* dx4 = reinterpret_cast<uint4*>(out_chunk_row(p, row));
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
+      for (int k = 0; k < VT; ++k) {
         float f[8], dy[8], g[8], o[8];
-        unpack8(xv[v], f);
-        unpack8(ds[v * 32 + lane], dy);
-        unpack8(gam[v * 32 + lane], g);
+        unpack8(xv[k], f);
+        unpack8(dv[k], dy);
+        unpack8(gam[j + k * 32 * TW], g);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = rstd * (dy[e] * g[e] - m1 - (f[e] - mean) * rstd * m2);
-        dx4[v * 32 + lane] = pack8(o);
+        for (int e = 0; e < 8; ++e) {
+          const float xhat = (f[e] - mean) * rstd;
+          o[e] = rstd * (dy[e] * g[e] - m1 - xhat * m2);
+          dg[k][e] += dy[e] * xhat;
+          db[k][e] += dy[e];
+        }
+        dx4[j + k * 32 * TW] = pack8(o);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty + slot);
-      if (lane == 0) reinterpret_cast<float2*>(p.stats)[row] = make_float2(mean, rstd);
+    }
+  }
+  __syncthreads();  // the producer has drained its copies: the ring is free for the team sums
+  float* acc = reinterpret_cast<float*>(ring);  // [kTeams][2 d]
+  if (warp > 0) {
+#pragma unroll
+    for (int k = 0; k < VT; ++k) {
+      const int col = (j + k * 32 * TW) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[team * 2 * p.d + col + e] = dg[k][e];
+        acc[team * 2 * p.d + p.d + col + e] = db[k][e];
+      }
     }
   }
   __syncthreads();
-}
-
-// LayerNorm backward, column part: block (bx, by) sums dgamma += dy xhat and dbeta += dy over rows
-// [by R, by R + R) for the 8 columns of each thread's 16-byte vector; partial row `by` of [blocks x 2d].
-__global__ void __launch_bounds__(256) k_layernorm_bwd_columns(const RowParams p) {
-  const int v = blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= p.d / 8) return;
-  const int r0 = blockIdx.y * p.rows_per_block;
-  const int r1 = min(p.rows, r0 + p.rows_per_block);
-  float dg[8], db[8];
+  for (int c = threadIdx.x; c < 2 * p.d; c += blockDim.x) {
+    float t = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) dg[e] = db[e] = 0.f;
-  const float2* st = reinterpret_cast<const float2*>(p.stats);
-  int r = r0;
-  for (; r + 4 <= r1; r += 4) {
-    uint4 xr[4], dr[4];
-    float2 sr[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      xr[k] = __ldg(reinterpret_cast<const uint4*>(chunk_row(p, r + k)) + v);
-      dr[k] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.src) +
-                                                   static_cast<long long>(r + k) * p.d) + v);
-      sr[k] = st[r + k];
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float f[8], dy[8];
-      unpack8(xr[k], f);
-      unpack8(dr[k], dy);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        dg[e] += dy[e] * (f[e] - sr[k].x) * sr[k].y;
-        db[e] += dy[e];
-      }
-    }
-  }
-  for (; r < r1; ++r) {
-    float f[8], dy[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(chunk_row(p, r)) + v), f);
-    unpack8(__ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.src) +
-                                                 static_cast<long long>(r) * p.d) + v), dy);
-    const float2 sr = st[r];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      dg[e] += dy[e] * (f[e] - sr.x) * sr.y;
-      db[e] += dy[e];
-    }
-  }
-  float* out = p.partial + static_cast<long long>(blockIdx.y) * 2 * p.d + v * 8;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    out[e] = dg[e];
-    out[p.d + e] = db[e];
+    for (int tm = 0; tm < kTeams; ++tm) t += acc[tm * 2 * p.d + c];
+    p.partial[static_cast<long long>(blockIdx.x) * 2 * p.d + c] = t;
   }
 }
 
@@ -560,22 +592,32 @@ int layernorm_bwd_blocks(int rows, int max_blocks) {
 
 namespace {
 
-constexpr int kLnBwdColumnRows = 64;     // rows per column-partial block of the streamed backward
-constexpr int kLnBwdMaxBlocksOld = 304;  // CTAs of the register-free backward
+constexpr int kLnBwdMaxBlocksOld = 304;   // CTAs of the generic backward
+constexpr int kLnBwdMaxBlocksFused = 256; // upper bound on the fused backward's CTAs (one per SM)
 
-bool lnbwd_streamed(int d) {
-  const int V = d % 256 == 0 ? d / 256 : 0;
-  return V == 1 || V == 2 || V == 4 || V == 8 || V == 16;
+// (team warps, vectors per thread) of the fused backward for row width d, or {0, 0}.
+struct TeamShape {
+  int tw, vt;
+};
+TeamShape fused_shape(int d) {
+  switch (d) {
+    case 256: return {1, 1};
+    case 512: return {2, 1};
+    case 1024: return {4, 1};
+    case 2048: return {4, 2};
+    case 4096: return {4, 4};
+    case 8192: return {8, 4};
+    default: return {0, 0};
+  }
 }
-
-size_t align64(size_t x) { return (x + 63) / 64 * 64; }
 
 }  // namespace
 
 size_t layernorm_bwd_scratch_floats(int rows, int d) {
-  if (lnbwd_streamed(d))
-    return align64(2 * static_cast<size_t>(rows)) +
-           static_cast<size_t>((rows + kLnBwdColumnRows - 1) / kLnBwdColumnRows) * 2 * d;
+  if (fused_shape(d).tw > 0) {
+    const int blocks = rows < kLnBwdMaxBlocksFused ? (rows < 1 ? 1 : rows) : kLnBwdMaxBlocksFused;
+    return static_cast<size_t>(blocks) * 2 * d;
+  }
   return static_cast<size_t>(layernorm_bwd_blocks(rows, kLnBwdMaxBlocksOld)) * 2 * d;
 }
 
@@ -585,40 +627,37 @@ cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap
   RowParams r = r0;
   r.err = ctx.err;
   r.timeout_ns = ctx.timeout_ns;
-  if (lnbwd_streamed(r.d) && cap_floats >= align64(2 * static_cast<size_t>(r.rows)) + 2 * static_cast<size_t>(r.d)) {
-    // scratch: [rows x 2] statistics, then [blocks x 2 d] column partials; widen the column blocks if the
-    // scratch is smaller than the default layout needs
-    r.stats = scratch;
-    r.partial = scratch + align64(2 * static_cast<size_t>(r.rows));
-    const size_t room = cap_floats - align64(2 * static_cast<size_t>(r.rows));
-    int rpb = kLnBwdColumnRows;
-    while (static_cast<size_t>((r.rows + rpb - 1) / rpb) * 2 * r.d > room) rpb *= 2;
-    r.rows_per_block = rpb;
-    const size_t row_bytes = static_cast<size_t>(r.d) * 2;
-    r.slots = stream_slots(2 * row_bytes);
-    const size_t smem = 128 + r.slots * 2 * row_bytes + row_bytes + 16 * static_cast<size_t>(r.slots) + 16;
-    const int grid = r.rows < ctx.sm_count ? r.rows : ctx.sm_count;
-    cudaError_t e;
-    switch (r.d / 256) {
-      case 1: e = launch_stream(k_layernorm_bwd_rows_stream<1>, r, smem, grid, s); break;
-      case 2: e = launch_stream(k_layernorm_bwd_rows_stream<2>, r, smem, grid, s); break;
-      case 4: e = launch_stream(k_layernorm_bwd_rows_stream<4>, r, smem, grid, s); break;
-      case 8: e = launch_stream(k_layernorm_bwd_rows_stream<8>, r, smem, grid, s); break;
-      default: e = launch_stream(k_layernorm_bwd_rows_stream<16>, r, smem, grid, s); break;
+  r.partial = scratch;
+  const size_t per_block = 2 * static_cast<size_t>(r.d);
+  const TeamShape ts = fused_shape(r.d);
+  if (ts.tw > 0) {
+    int grid = r.rows < ctx.sm_count ? r.rows : ctx.sm_count;
+    if (grid > kLnBwdMaxBlocksFused) grid = kLnBwdMaxBlocksFused;
+    if (static_cast<size_t>(grid) * per_block > cap_floats) grid = static_cast<int>(cap_floats / per_block);
+    if (grid >= 1) {
+      const size_t row_bytes = static_cast<size_t>(r.d) * 2;
+      r.slots = stream_slots(2 * row_bytes);
+      size_t smem = 128 + r.slots * 2 * row_bytes + row_bytes + 16 * static_cast<size_t>(r.slots) + 16;
+      const size_t team_sums = static_cast<size_t>(kStreamConsumers / ts.tw) * per_block * 4 + 128;
+      if (smem < team_sums) smem = team_sums;
+      cudaError_t e;
+      switch (r.d) {
+        case 256: e = launch_stream(k_layernorm_bwd_fused<1, 1>, r, smem, grid, s); break;
+        case 512: e = launch_stream(k_layernorm_bwd_fused<1, 2>, r, smem, grid, s); break;
+        case 1024: e = launch_stream(k_layernorm_bwd_fused<1, 4>, r, smem, grid, s); break;
+        case 2048: e = launch_stream(k_layernorm_bwd_fused<2, 4>, r, smem, grid, s); break;
+        case 4096: e = launch_stream(k_layernorm_bwd_fused<4, 4>, r, smem, grid, s); break;
+        default: e = launch_stream(k_layernorm_bwd_fused<4, 8>, r, smem, grid, s); break;
+      }
+      if (e != cudaSuccess) return e;
+      k_column_sum<<<(2 * r.d + 31) / 32, 256, 0, s>>>(r.partial, grid, 2 * r.d, 2LL * r.d, dgamma, dbeta, r.d, 0);
+      return cudaGetLastError();
     }
-    if (e != cudaSuccess) return e;
-    const int blocks = (r.rows + rpb - 1) / rpb;
-    k_layernorm_bwd_columns<<<dim3((r.d / 8 + 255) / 256, blocks), 256, 0, s>>>(r);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    k_column_sum<<<(2 * r.d + 31) / 32, 256, 0, s>>>(r.partial, blocks, 2 * r.d, 2LL * r.d, dgamma, dbeta, r.d, 0);
-    return cudaGetLastError();
   }
   // any other width: per-block shared-memory accumulation of dgamma/dbeta
-  int max_blocks = static_cast<int>(cap_floats / (2 * static_cast<size_t>(r.d)));
+  int max_blocks = static_cast<int>(cap_floats / per_block);
   if (max_blocks > kLnBwdMaxBlocksOld) max_blocks = kLnBwdMaxBlocksOld;
   if (max_blocks < 1) return cudaErrorInvalidValue;
-  r.partial = scratch;
   const int grid = layernorm_bwd_blocks(r.rows, max_blocks);
   const size_t smem = static_cast<size_t>(2) * r.d * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(k_layernorm_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
