@@ -49,28 +49,37 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest():
-    """Short sha256 of the CUDA sources the kernels are built from (keys the committed ncu traffic table)."""
-    h = hashlib.sha256()
+_GEMM_SOURCES = ("common.h", "ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_tc.cu")
+_ROW_SOURCES = ("common.h", "ptx.cuh", "launch.h", "rowwise.cu")
+
+
+def kernel_source_digest(segment=None):
+    """Short sha256 of the CUDA sources a segment's kernels are built from (all sources without a segment);
+    keys the committed ncu traffic table."""
     csrc = os.path.join(ROOT, "tensor_transformer_mlp_tp_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    if segment is None:
+        files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    else:
+        files = _GEMM_SOURCES if segment.startswith("gemm") else _ROW_SOURCES
+    h = hashlib.sha256()
+    for f in files:
+        h.update(f.encode())
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(segment):
-    """DRAM bytes per launch of `segment` from the committed ncu capture, or None if the kernels changed since."""
+    """DRAM bytes per launch of `segment` from the committed ncu capture, or None if its kernels changed since."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
-    if d.get("source_digest") != kernel_source_digest():
+    entry = d.get("segments", {}).get(segment)
+    if entry is None or entry.get("source_digest") != kernel_source_digest(segment):
         return None
-    return d.get("bytes_per_launch", {}).get(segment)
+    return entry.get("bytes_per_launch")
 
 
 def max_over_ranks(value, dist):
@@ -296,7 +305,7 @@ class Step:
         if w.backward:
             segs += [("gemm_dh_geluprime", 1, g, "F"), ("gemm_wgrad_b", 1, g, "F"),
                      ("gemm_wgrad_a", 1, g, "F"), ("gemm_dx_shard_accum", 1, g, "F"),
-                     ("layernorm_backward", 3, 3.0 * w.T * w.d * 2, "B")]
+                     ("layernorm_backward", 2, 3.0 * w.T * w.d * 2, "B")]
         return segs
 
     def run(self, ev=None):
