@@ -56,6 +56,11 @@ reason in the design notes):
   block the mirror collectives: AllGather of dY, ReduceScatter of the input
   gradient.  dgamma and dbeta sum over all chunks.
 * Non-divisible sizes (``F % N``, ``T % N``) are rejected, not truncated.
+* The RMS norm variant follows the SequenceParallelLayerNorm listing as
+  written: fp32 mean of squares, ``rsqrt(ms + eps)``, the normalised row
+  rounded to bf16 before the weight multiply (the listing's ``.to(dtype)``).
+  Here the normalised value is computed in float64 and then rounded to bf16
+  (round to nearest, ties to even, 8 significant bits).
 
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` (values
 printed on the pages, closed forms, invariants, brute force, library
@@ -195,6 +200,24 @@ def sp_forward(X_chunks, gamma, beta, eps, A, B, b, N: int, return_intermediates
     if return_intermediates:
         return Y_chunks, {"Xg": Xg, "partials": parts}
     return Y_chunks
+
+
+def round_bf16(x):
+    """Round to the nearest bfloat16 value (8 significant bits, ties to even), returned as float64.
+
+    ``x = m·2**e`` with ``0.5 <= |m| < 1``; ``m·2**8`` rounded half-to-even and scaled back.  Values
+    stay inside bf16's normal range here (no overflow or subnormal handling).
+    """
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def rms_norm(x, weight, eps: float = 1e-5):
+    """The norm of the SequenceParallelLayerNorm listing ([DEEP] "분산 제어 소스코드 구조 패턴"):
+    ``x·rsqrt(mean(x²) + eps)`` rounded to bf16, then times ``weight``."""
+    x = np.asarray(x, dtype=np.float64)
+    rstd = 1.0 / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+    return round_bf16(x * rstd) * np.asarray(weight, dtype=np.float64)
 
 
 # --------------------------------------------------------------------------- backward (chain rule)

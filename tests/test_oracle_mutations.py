@@ -90,7 +90,19 @@ def _sp_backward_last_chunk_dgamma(*args, **kw):
     return out
 
 
+def _rms_norm_no_rounding(x, weight, eps=1e-5):
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * weight
+
+
+def _round_bf16_truncate(x):
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(np.trunc(m * 256.0), e - 8)
+
+
 CASES = [
+    ("rms_norm", _rms_norm_no_rounding, lambda: pins.test_rms_norm_bruteforce_rows()),
+    ("round_bf16", _round_bf16_truncate, lambda: pins.test_round_bf16_ties_and_witnesses()),
     ("gelu", _gelu_tanh, lambda: pins.test_gelu_textbook_values()),
     ("gelu", _gelu_tanh, lambda: pins.test_mlp_bruteforce_d8(3, 2)),
     ("gelu_prime", _gelu_prime_no_pdf, lambda: pins.test_gelu_prime_finite_difference()),

@@ -340,3 +340,49 @@ def test_bf16_inputs_are_exact_in_fp64():
     bits, vals = inputs.draw(w, "X")
     ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
     assert np.array_equal(vals, ref)
+
+
+# --------------------------------------------------------------------------- bf16 rounding and the RMS norm of the listing
+
+def _bf16_bruteforce(v):
+    """Round a Python float to bf16 through its float32 bit pattern (RNE on the low 16 bits)."""
+    import struct
+    b = struct.unpack("<I", struct.pack("<f", v))[0]
+    low = b & 0xFFFF
+    hi = b >> 16
+    if low > 0x8000 or (low == 0x8000 and (hi & 1)):
+        hi += 1
+    return struct.unpack("<f", struct.pack("<I", hi << 16))[0]
+
+
+def test_round_bf16_ties_and_witnesses():
+    assert oracle.round_bf16(1.0 + 2.0 ** -8) == 1.0                # tie, even neighbour below
+    assert oracle.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6  # tie, even neighbour above
+    assert oracle.round_bf16(-(1.0 + 2.0 ** -7)) == -(1.0 + 2.0 ** -7)  # representable
+    xs = RNG.normal(0, 10, 2000).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(oracle.round_bf16(xs.astype(np.float64)), ref)
+    assert np.array_equal(oracle.round_bf16(xs.astype(np.float64)), [_bf16_bruteforce(float(v)) for v in xs])
+
+
+def test_rms_norm_bruteforce_rows():
+    x = RNG.normal(0.3, 2.0, (5, 12))
+    w = oracle.round_bf16(1 + 0.1 * RNG.normal(size=12))
+    got = oracle.rms_norm(x, w, 1e-5)
+    for r in range(5):
+        ms = sum(v * v for v in x[r]) / 12
+        rs = 1.0 / math.sqrt(ms + 1e-5)
+        ref = [_bf16_bruteforce(float(np.float32(v * rs))) * w[c] for c, v in enumerate(x[r])]
+        np.testing.assert_allclose(got[r], ref, rtol=0, atol=1e-12)
+
+
+def test_rms_norm_torch_witness_and_closed_form():
+    x = RNG.normal(0, 1, (64, 256))
+    w = oracle.round_bf16(1 + 0.02 * RNG.normal(size=256))
+    xt = torch.from_numpy(x)
+    rstd = torch.rsqrt((xt * xt).mean(-1, keepdim=True) + 1e-5)
+    ref = (xt * rstd).to(torch.bfloat16).double() * torch.from_numpy(w)
+    np.testing.assert_allclose(oracle.rms_norm(x, w, 1e-5), ref.numpy(), rtol=0, atol=1e-12)
+    # a constant row c: x / rms = sign(c) / sqrt(1 + eps/c^2), which rounds to +-1 in bf16
+    c = np.full((1, 256), -3.0)
+    np.testing.assert_array_equal(oracle.rms_norm(c, w, 1e-5)[0], -w)
