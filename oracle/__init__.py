@@ -56,6 +56,17 @@ reason in the design notes):
   block the mirror collectives: AllGather of dY, ReduceScatter of the input
   gradient.  dgamma and dbeta sum over all chunks.
 * Non-divisible sizes (``F % N``, ``T % N``) are rejected, not truncated.
+* The rest of the sequence-parallel region (bias of the row layer, Dropout,
+  residual) reads: ``Y_j = X_j + dropout(Z_j + b2)``.  ``Z_j`` is chunk j
+  of the reduced MLP output and ``b2`` is the row layer's bias, added after
+  the reduction as the RowParallelLinear listing does.  Dropout lives in the
+  sequence-split region (SP section, [GLOSS] SP paragraph).  The residual,
+  which the pages never mention, is the block input ``X_j``.  Dropout keeps
+  an element with probability ``1 - p`` and scales kept elements by
+  ``1/(1 - p)``.  The pages give no generator, so the keep decision is drawn
+  from Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random
+  numbers: as easy as 1, 2, 3", SC 2011) on the element's index in the
+  gathered ``[T x d]`` output (details at :func:`dropout_keep`).
 * The RMS norm variant follows the SequenceParallelLayerNorm listing as
   written: fp32 mean of squares, ``rsqrt(ms + eps)``, the normalised row
   rounded to bf16 before the weight multiply (the listing's ``.to(dtype)``).
@@ -220,6 +231,93 @@ def rms_norm(x, weight, eps: float = 1e-5):
     return round_bf16(x * rstd) * np.asarray(weight, dtype=np.float64)
 
 
+# --------------------------------------------------------------------------- dropout generator
+
+# Philox4x64 round multipliers and key increments (Salmon et al., SC 2011, table of Philox parameters).
+PHILOX4X64_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)
+PHILOX4X64_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)
+_MASK64 = (1 << 64) - 1
+_LO32 = np.uint64(0xFFFFFFFF)
+_S32 = np.uint64(32)
+
+
+def _mulhilo64(m: int, x):
+    """High and low 64-bit halves of the 128-bit products ``m·x`` (``x`` a uint64 array), by 32-bit limbs."""
+    a_lo, a_hi = np.uint64(m & 0xFFFFFFFF), np.uint64(m >> 32)
+    x_lo, x_hi = x & _LO32, x >> _S32
+    with np.errstate(over="ignore"):
+        ll, lh, hl, hh = a_lo * x_lo, a_lo * x_hi, a_hi * x_lo, a_hi * x_hi
+        mid = (ll >> _S32) + (lh & _LO32) + (hl & _LO32)
+        hi = hh + (lh >> _S32) + (hl >> _S32) + (mid >> _S32)
+        lo = np.uint64(m) * x
+    return hi, lo
+
+
+def philox4x64(counter, key, rounds: int = 10):
+    """Philox4x64-``rounds`` blocks: ``counter`` [..., 4] uint64, ``key`` = (k0, k1) -> [..., 4] uint64.
+
+    One round takes ``(hi0, lo0) = M0·x0`` and ``(hi1, lo1) = M1·x2`` and sets
+    ``x = (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0)``; the key advances by the
+    Weyl increments ``(W0, W1)`` between rounds (the first round uses the key
+    as given).
+    """
+    c = np.asarray(counter, dtype=np.uint64)
+    x = [c[..., i] for i in range(4)]
+    k0, k1 = int(key[0]) & _MASK64, int(key[1]) & _MASK64
+    for r in range(rounds):
+        if r:
+            k0 = (k0 + PHILOX4X64_W[0]) & _MASK64
+            k1 = (k1 + PHILOX4X64_W[1]) & _MASK64
+        hi0, lo0 = _mulhilo64(PHILOX4X64_M[0], x[0])
+        hi1, lo1 = _mulhilo64(PHILOX4X64_M[1], x[2])
+        x = [hi1 ^ x[1] ^ np.uint64(k0), lo1, hi0 ^ x[3] ^ np.uint64(k1), lo0]
+    return np.stack(x, axis=-1)
+
+
+def dropout_threshold(p) -> int:
+    """Keep threshold for drop probability ``p`` (taken as float32): ``floor((1 - p)·2**32)``."""
+    p = float(np.float32(p))
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must lie in [0, 1)")
+    return math.floor((1.0 - p) * 2.0 ** 32)
+
+
+def dropout_keep(rows: int, d: int, row0: int, p, seed: int, offset: int):
+    """Keep mask of rows ``[row0, row0 + rows)`` of a ``[T x d]`` output.
+
+    Element ``(r, c)`` has index ``e = r·d + c``.  Block ``e // 8`` is one
+    Philox4x64-10 call with counter ``(e // 8, offset, 0, 0)`` and key
+    ``(seed, 0)``; element ``e`` takes 32 bits of it: word ``(e % 8) // 2``,
+    its low half for even ``e`` and its high half for odd ``e``.  The element
+    is kept when those 32 bits, read as an unsigned integer, are below
+    :func:`dropout_threshold`.
+    """
+    r = np.arange(row0, row0 + rows, dtype=np.uint64)[:, None]
+    e = r * np.uint64(d) + np.arange(d, dtype=np.uint64)[None, :]
+    ctr = np.zeros(e.shape + (4,), dtype=np.uint64)
+    ctr[..., 0] = e >> np.uint64(3)
+    ctr[..., 1] = np.uint64(offset)
+    words = philox4x64(ctr, (seed, 0))
+    lane = e & np.uint64(7)
+    w = np.take_along_axis(words, (lane >> np.uint64(1)).astype(np.intp)[..., None], axis=-1)[..., 0]
+    u = (w >> (_S32 * (lane & np.uint64(1)))) & _LO32
+    return u < np.uint64(dropout_threshold(p)) if dropout_threshold(p) < 2 ** 32 else np.ones(e.shape, dtype=bool)
+
+
+def sp_block_forward(X_chunks, gamma, beta, eps, A, B, b, b2, p, seed: int, offset: int, N: int):
+    """The whole sequence-parallel region: ``Y_j = X_j + dropout(Z_j + b2)``, ``Z_j`` = :func:`sp_forward`."""
+    Z = sp_forward(X_chunks, gamma, beta, eps, A, B, b, N)
+    T = sum(np.asarray(x).shape[0] for x in X_chunks)
+    d = np.asarray(X_chunks[0]).shape[1]
+    bias2 = _bias_or_zero(b2, d)
+    scale = 1.0 / (1.0 - float(np.float32(p)))
+    out = []
+    for (lo, hi), xj, zj in zip(chunk_ranges(T, N), X_chunks, Z):
+        keep = dropout_keep(hi - lo, d, lo, p, seed, offset)
+        out.append(np.asarray(xj, dtype=np.float64) + np.where(keep, (zj + bias2) * scale, 0.0))
+    return out
+
+
 # --------------------------------------------------------------------------- backward (chain rule)
 
 def mlp_backward(X, A, B, b, dY):
@@ -303,3 +401,22 @@ def sp_backward(X_chunks, gamma, beta, eps, A, B, b, dY_chunks, N: int):
         dbeta = dbeta + dbe
     return {"dX_chunks": dX_chunks, "dA": g["dA"], "dB": g["dB"], "db": g["db"],
             "dgamma": dgamma, "dbeta": dbeta, "dXg_chunks": dXg_chunks}
+
+
+def sp_block_backward(X_chunks, gamma, beta, eps, A, B, b, p, seed: int, offset: int, dY_chunks, N: int):
+    """Gradients of :func:`sp_block_forward`.
+
+    ``dZ_j = dY_j ⊙ keep_j / (1 - p)``; ``db2 = Σ_j Σ_rows dZ_j``; the MLP and
+    norm gradients are :func:`sp_backward` driven by ``dZ``; the residual
+    adds ``dY_j`` to the input gradient of chunk j.
+    """
+    T = sum(np.asarray(x).shape[0] for x in X_chunks)
+    d = np.asarray(X_chunks[0]).shape[1]
+    scale = 1.0 / (1.0 - float(np.float32(p)))
+    dZ = [np.where(dropout_keep(hi - lo, d, lo, p, seed, offset), np.asarray(dy, dtype=np.float64) * scale, 0.0)
+          for (lo, hi), dy in zip(chunk_ranges(T, N), dY_chunks)]
+    g = sp_backward(X_chunks, gamma, beta, eps, A, B, b, dZ, N)
+    g["dX_chunks"] = [dx + np.asarray(dy, dtype=np.float64) for dx, dy in zip(g["dX_chunks"], dY_chunks)]
+    g["db2"] = sum(z.sum(axis=0) for z in dZ)
+    g["dZ_chunks"] = dZ
+    return g

@@ -100,7 +100,34 @@ def _round_bf16_truncate(x):
     return np.ldexp(np.trunc(m * 256.0), e - 8)
 
 
+def _philox_bump_first(counter, key, rounds=10):
+    k = ((int(key[0]) + oracle.PHILOX4X64_W[0]) % 2 ** 64, (int(key[1]) + oracle.PHILOX4X64_W[1]) % 2 ** 64)
+    return _orig["philox4x64"](counter, k, rounds)
+
+
+def _dropout_keep_halves_swapped(rows, d, row0, p, seed, offset):
+    # odd elements take the low half and even ones the high half: flip each pair of columns
+    base = _orig["dropout_keep"](rows, d, row0, p, seed, offset)
+    return base.reshape(rows, d // 2, 2)[:, :, ::-1].reshape(rows, d)
+
+
+def _sp_block_forward_unscaled(X_chunks, gamma, beta, eps, A, B, b, b2, p, seed, offset, N):
+    Y = _orig["sp_block_forward"](X_chunks, gamma, beta, eps, A, B, b, b2, p, seed, offset, N)
+    s = 1.0 - float(np.float32(p))
+    return [x + (y - x) * s for x, y in zip(X_chunks, Y)]
+
+
+def _sp_block_backward_no_residual(X_chunks, gamma, beta, eps, A, B, b, p, seed, offset, dY_chunks, N):
+    g = _orig["sp_block_backward"](X_chunks, gamma, beta, eps, A, B, b, p, seed, offset, dY_chunks, N)
+    g["dX_chunks"] = [dx - dy for dx, dy in zip(g["dX_chunks"], dY_chunks)]
+    return g
+
+
 CASES = [
+    ("philox4x64", _philox_bump_first, lambda: pins.test_philox_matches_numpy_bit_generator()),
+    ("dropout_keep", _dropout_keep_halves_swapped, lambda: pins.test_dropout_keep_bits_come_from_the_stated_block_and_half(0.5)),
+    ("sp_block_forward", _sp_block_forward_unscaled, lambda: pins.test_sp_block_forward_torch_witness(2, 0.25)),
+    ("sp_block_backward", _sp_block_backward_no_residual, lambda: pins.test_sp_block_backward_autograd_witness(2, 0.25)),
     ("rms_norm", _rms_norm_no_rounding, lambda: pins.test_rms_norm_bruteforce_rows()),
     ("round_bf16", _round_bf16_truncate, lambda: pins.test_round_bf16_ties_and_witnesses()),
     ("gelu", _gelu_tanh, lambda: pins.test_gelu_textbook_values()),

@@ -386,3 +386,117 @@ def test_rms_norm_torch_witness_and_closed_form():
     # a constant row c: x / rms = sign(c) / sqrt(1 + eps/c^2), which rounds to +-1 in bf16
     c = np.full((1, 256), -3.0)
     np.testing.assert_array_equal(oracle.rms_norm(c, w, 1e-5)[0], -w)
+
+
+# --------------------------------------------------------------------------- dropout generator and the whole SP region
+
+def _numpy_philox_block(counter, key):
+    """One Philox4x64-10 block from numpy's bit generator, which advances its counter before each block."""
+    c = [int(v) for v in counter]
+    assert c[0] >= 1, "the witness steps counter word 0 back by one"
+    c[0] -= 1
+    g = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=np.array(c, dtype=np.uint64))
+    return g.random_raw(4)
+
+
+def test_philox_matches_numpy_bit_generator():
+    rng = np.random.default_rng(11)
+    ctrs = rng.integers(1, 2 ** 63, size=(24, 4), dtype=np.uint64)
+    ctrs[:4, 1:] = 0
+    keys = rng.integers(0, 2 ** 63, size=(24, 2), dtype=np.uint64)
+    keys[0] = 0
+    for c, k in zip(ctrs, keys):
+        got = oracle.philox4x64(c[None, :], (int(k[0]), int(k[1])))[0]
+        assert np.array_equal(got, _numpy_philox_block(c, k)), (c, k)
+    # a vector of counters under one key equals the blocks one by one
+    many = oracle.philox4x64(ctrs, (7, 9))
+    for c, row in zip(ctrs, many):
+        assert np.array_equal(row, _numpy_philox_block(c, (7, 9)))
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5, 0.875])
+def test_dropout_keep_bits_come_from_the_stated_block_and_half(p):
+    """Each element's keep bit, recomputed from numpy's Philox blocks by the stated word/half rule."""
+    rows, d, row0, seed, offset = 5, 24, 3, 1234567, 42
+    keep = oracle.dropout_keep(rows, d, row0, p, seed, offset)
+    thr = math.floor((1.0 - float(np.float32(p))) * 2 ** 32)
+    for r in range(rows):
+        for c in range(d):
+            e = (row0 + r) * d + c
+            w = int(_numpy_philox_block((e // 8, offset, 0, 0), (seed, 0))[(e % 8) // 2])
+            u = (w >> (32 * (e % 2))) & 0xFFFFFFFF
+            assert keep[r, c] == (u < thr), (r, c)
+
+
+def test_dropout_keep_invariants():
+    assert oracle.dropout_threshold(0.0) == 2 ** 32
+    assert oracle.dropout_threshold(0.5) == 2 ** 31
+    assert oracle.dropout_threshold(0.25) == 3 * 2 ** 30
+    with pytest.raises(ValueError):
+        oracle.dropout_threshold(1.0)
+    assert oracle.dropout_keep(16, 64, 0, 0.0, 3, 0).all()
+    T, d, p = 512, 256, 0.1
+    full = oracle.dropout_keep(T, d, 0, p, 99, 5)
+    n = full.size
+    assert abs(full.mean() - (1 - p)) < 6 * math.sqrt(p * (1 - p) / n)
+    # the mask of a chunk is the slice of the whole output's mask (global element index)
+    assert np.array_equal(full[128:256], oracle.dropout_keep(128, d, 128, p, 99, 5))
+    # another offset (the next step) draws an independent mask
+    other = oracle.dropout_keep(T, d, 0, p, 99, 6)
+    agree = (full == other).mean()
+    expect = p * p + (1 - p) * (1 - p)
+    assert abs(agree - expect) < 6 * math.sqrt(expect * (1 - expect) / n)
+
+
+def _block_problem(T, d, F):
+    X = RNG.normal(size=(T, d))
+    gam = 1 + 0.1 * RNG.normal(size=d)
+    bet = 0.1 * RNG.normal(size=d)
+    _, A, B, b = _rand_block(1, d, F)
+    b2 = 0.1 * RNG.normal(size=d)
+    return X, gam, bet, A, B, b, b2
+
+
+def _torch_block(tt, keep, p, d):
+    X, gam, bet, A, B, b, b2 = tt
+    xn = torch.nn.functional.layer_norm(X, (d,), gam, bet, eps=1e-5)
+    Z = torch.nn.functional.gelu(xn @ A + b, approximate="none") @ B + b2
+    return X + Z * torch.from_numpy(keep.astype(np.float64)) / (1.0 - float(np.float32(p)))
+
+
+@pytest.mark.parametrize("N,p", [(1, 0.1), (2, 0.25), (4, 0.5)])
+def test_sp_block_forward_torch_witness(N, p):
+    T, d, F = 4 * N, 16, 64
+    X, gam, bet, A, B, b, b2 = _block_problem(T, d, F)
+    keep = oracle.dropout_keep(T, d, 0, p, 77, 3)
+    ref = _torch_block([torch.tensor(v) for v in (X, gam, bet, A, B, b, b2)], keep, p, d).numpy()
+    cr = oracle.chunk_ranges(T, N)
+    Y = oracle.sp_block_forward([X[lo:hi] for lo, hi in cr], gam, bet, 1e-5, A, B, b, b2, p, 77, 3, N)
+    assert rel(np.concatenate(Y), ref) < 1e-12
+
+
+def test_sp_block_forward_without_dropout_is_residual_plus_sp_forward():
+    T, d, F, N = 16, 8, 32, 4
+    X, gam, bet, A, B, b, _ = _block_problem(T, d, F)
+    cr = oracle.chunk_ranges(T, N)
+    Xc = [X[lo:hi] for lo, hi in cr]
+    Y = oracle.sp_block_forward(Xc, gam, bet, 1e-5, A, B, b, None, 0.0, 1, 0, N)
+    Z = oracle.sp_forward(Xc, gam, bet, 1e-5, A, B, b, N)
+    for y, x, z in zip(Y, Xc, Z):
+        assert np.array_equal(y, x + z)
+
+
+@pytest.mark.parametrize("N,p", [(1, 0.0), (2, 0.25), (4, 0.5)])
+def test_sp_block_backward_autograd_witness(N, p):
+    T, d, F = 4 * N, 16, 64
+    X, gam, bet, A, B, b, b2 = _block_problem(T, d, F)
+    dY = RNG.normal(size=(T, d))
+    keep = oracle.dropout_keep(T, d, 0, p, 5, 8)
+    tt = [torch.tensor(v, requires_grad=True) for v in (X, gam, bet, A, B, b, b2)]
+    _torch_block(tt, keep, p, d).backward(torch.from_numpy(dY))
+    cr = oracle.chunk_ranges(T, N)
+    g = oracle.sp_block_backward([X[lo:hi] for lo, hi in cr], gam, bet, 1e-5, A, B, b, p, 5, 8,
+                                 [dY[lo:hi] for lo, hi in cr], N)
+    assert rel(np.concatenate(g["dX_chunks"]), tt[0].grad.numpy()) < 1e-12
+    for key, i in (("dgamma", 1), ("dbeta", 2), ("dA", 3), ("dB", 4), ("db", 5), ("db2", 6)):
+        assert rel(g[key], tt[i].grad.numpy()) < 1e-12, key
