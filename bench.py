@@ -442,7 +442,8 @@ def time_calls(torch, fn, reps, warmup=3):
 
 def run_other_rows(step, torch, binding, pk):
     """Rows of the hot path the step does not run: the explicit reduce-scatter (per-shard bf16 partials, then
-    the reduce-scatter kernel) on the step's shapes, and the fp32 path on the tiny fp32 workload."""
+    the reduce-scatter kernel) and the RMS norm variant on the step's shapes, and the fp32 path on the tiny
+    fp32 workload."""
     w = step.w
     out = {}
     if w.sp and (w.F // w.N) % 64 == 0:
@@ -459,6 +460,18 @@ def run_other_rows(step, torch, binding, pk):
                                           "frac": round(rs_bytes / (ms_rs * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
                                           "bytes_per_launch": rs_bytes}
         del P, Yc
+    if w.sp:
+        # the RMS norm variant of the gathered norm, and the LayerNorm beside it timed the same way; the calls
+        # alternate between (X -> Xg) and (dY -> dXg) so each reads 2 T d bytes the previous call did not touch
+        # (256 MB of inputs and outputs in all, about twice the L2)
+        nb = 4.0 * w.T * w.d
+        for name, fn in (("rmsnorm_gather", binding.tpmlp_rmsnorm_gather),
+                         ("layernorm_gather_isolated", binding.tpmlp_layernorm_gather)):
+            extra = (step.gamma,) if name.startswith("rms") else (step.gamma, step.beta)
+            pair = lambda: (fn(step.Xc, *extra, w.N, step.Xg), fn(step.dYc, *extra, w.N, step.dXg))
+            ms = time_calls(torch, pair, 20) / 2.0
+            out[name] = {"ms": round(ms, 4), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
+                         "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes_per_launch": nb}
     t = inputs.WORKLOADS["tiny_fp32_fwd"]
     f32 = lambda name: torch.from_numpy(np.ascontiguousarray(inputs.draw(t, name)[0])).cuda()
     X, A, B, b = f32("X"), f32("A"), f32("B"), f32("bias")

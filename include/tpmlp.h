@@ -212,6 +212,15 @@ TPMLP_API tpmlp_status tpmlp_reduce_scatter(const void* P, const tpmlp_shape* sh
 TPMLP_API tpmlp_status tpmlp_layernorm_gather(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                                     const tpmlp_shape* shape, void* Xg, tpmlp_stream_t stream);
 
+/* The RMS norm the deep-dive page's SequenceParallelLayerNorm listing
+ * computes ("분산 제어 소스코드 구조 패턴"), written into the gathered buffer like
+ * tpmlp_layernorm_gather: per row rstd = rsqrt(mean(x^2) + eps) in fp32,
+ * n = bf16(x rstd) (the listing's cast back to the input dtype), then
+ * Xg = bf16(n * weight).  No mean subtraction, no shift.  weight [d] bf16,
+ * Xg [T x d]; T % N == 0. */
+TPMLP_API tpmlp_status tpmlp_rmsnorm_gather(const void* const* X_chunks, const void* weight, float eps,
+                                            const tpmlp_shape* shape, void* Xg, tpmlp_stream_t stream);
+
 /* dHpre = (dY B^T) * GeLU'(Hpre) in one GEMM epilogue; with H != NULL also
  * H = GeLU(Hpre); with dbias != NULL also dbias = column sums of dHpre
  * (workspace: size of TPMLP_OP_DH_GELUPRIME).  dY [T x d], B [F x d],

@@ -52,6 +52,7 @@ _SIGS = {
     "tpmlp_gemm2_partials": ([_P, _P, _SP, _P, _P], ctypes.c_int),
     "tpmlp_reduce_scatter": ([_P, _SP, _PP, _P], ctypes.c_int),
     "tpmlp_layernorm_gather": ([_PP, _P, _P, ctypes.c_float, _SP, _P, _P], ctypes.c_int),
+    "tpmlp_rmsnorm_gather": ([_PP, _P, ctypes.c_float, _SP, _P, _P], ctypes.c_int),
     "tpmlp_gemm_dh_geluprime": ([_P, _P, _P, _SP, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_gemm_wgrad_b": ([_P, _P, _SP, _P, _P], ctypes.c_int),
     "tpmlp_gemm_wgrad_a": ([_P, _P, _SP, _P, _P], ctypes.c_int),
@@ -219,6 +220,14 @@ def tpmlp_layernorm_gather(X_chunks, gamma, beta, N, Xg, eps=1e-5, stream=None):
     xp, _xa = _ptrs(X_chunks)
     _check("tpmlp_layernorm_gather", lib().tpmlp_layernorm_gather(xp, _ptr(gamma), _ptr(beta), eps,
                                                                   ctypes.byref(shape), _ptr(Xg), _stream(stream)))
+
+
+def tpmlp_rmsnorm_gather(X_chunks, weight, N, Xg, eps=1e-5, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
+    xp, _xa = _ptrs(X_chunks)
+    _check("tpmlp_rmsnorm_gather", lib().tpmlp_rmsnorm_gather(xp, _ptr(weight), eps, ctypes.byref(shape), _ptr(Xg),
+                                                              _stream(stream)))
 
 
 def tpmlp_gemm_dh_geluprime(dY, B, Hpre, N, dHpre, H=None, dbias=None, ws=None, stream=None):

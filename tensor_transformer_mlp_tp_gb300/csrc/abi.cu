@@ -620,6 +620,25 @@ tpmlp_status tpmlp_layernorm_gather(const void* const* X_chunks, const void* gam
   return cuda_status(do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+tpmlp_status tpmlp_rmsnorm_gather(const void* const* X_chunks, const void* weight, float eps,
+                                  const tpmlp_shape* shape, void* Xg, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({weight, Xg}) || !chunks_ok(X_chunks, shape->n_shards) || !(eps >= 0.f))
+    return TPMLP_ERR_INVALID_ARG;
+  RowParams r{};
+  r.in_chunks = to_const_chunks(X_chunks, shape->n_shards);
+  r.rows = static_cast<int>(shape->tokens);
+  r.d = static_cast<int>(shape->d);
+  r.n_chunks = shape->n_shards;
+  r.rows_per_chunk = static_cast<int>(shape->tokens / shape->n_shards);
+  r.eps = eps;
+  r.gamma = weight;
+  r.dst = Xg;
+  return cuda_status(launch_rmsnorm_fwd(r, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 tpmlp_status tpmlp_gemm_dh_geluprime(const void* dY, const void* B, const void* Hpre, const tpmlp_shape* shape,
                                      void* dHpre, void* H, void* dbias, void* workspace, size_t workspace_bytes,
                                      tpmlp_stream_t stream) {

@@ -44,6 +44,8 @@ struct DeviceCtx {
 cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s);
 
 cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
+// The RMS norm of the SequenceParallelLayerNorm listing (gamma = the weight; beta unused).
+cudaError_t launch_rmsnorm_fwd(const RowParams& r, cudaStream_t s);
 // LayerNorm backward using `scratch` (cap_floats floats of dgamma/dbeta block partials, 2 d per block).
 // layernorm_bwd_scratch_floats(rows, d) covers the default block count; a smaller scratch runs fewer
 // blocks, down to one (2 d floats).

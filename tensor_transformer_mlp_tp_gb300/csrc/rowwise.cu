@@ -63,7 +63,9 @@ __device__ __forceinline__ float row_sum(float v, float* red, int warp) {
   }
 }
 
-template <int V, int WPR>
+// RMS = true: the norm of the SequenceParallelLayerNorm listing instead:
+// rstd = rsqrt(mean(x^2) + eps), n = bf16(x rstd), y = bf16(n * gamma).
+template <int V, int WPR, bool RMS = false>
 __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
   __shared__ float red[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -74,15 +76,18 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
   uint4 x[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) x[v] = valid ? __ldg(src + (sub * V + v) * 32 + lane) : make_uint4(0, 0, 0, 0);
-  float s = 0.f;
+  float mean = 0.f;
+  if constexpr (!RMS) {
+    float s = 0.f;
 #pragma unroll
-  for (int v = 0; v < V; ++v) {
-    float f[8];
-    unpack8(x[v], f);
+    for (int v = 0; v < V; ++v) {
+      float f[8];
+      unpack8(x[v], f);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) s += f[e];
+      for (int e = 0; e < 8; ++e) s += f[e];
+    }
+    mean = row_sum<V, WPR>(s, red, warp) / static_cast<float>(p.d);
   }
-  const float mean = row_sum<V, WPR>(s, red, warp) / static_cast<float>(p.d);
   float q = 0.f;
 #pragma unroll
   for (int v = 0; v < V; ++v) {
@@ -102,32 +107,42 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
 #pragma unroll
   for (int v = 0; v < V; ++v) {
     const int idx = (sub * V + v) * 32 + lane;
-    float f[8], g[8], b[8], o[8];
+    float f[8], g[8], o[8];
     unpack8(x[v], f);
     unpack8(__ldg(g4 + idx), g);
-    unpack8(__ldg(b4 + idx), b);
+    if constexpr (RMS) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+      for (int e = 0; e < 8; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(f[e] * rstd)) * g[e];
+    } else {
+      float b[8];
+      unpack8(__ldg(b4 + idx), b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+    }
     dst[idx] = pack8(o);
   }
 }
 
 // Any d that is a multiple of 8: one warp per row, three sweeps over the row
 // (the second and third hit L1/L2).
+template <bool RMS = false>
 __global__ void __launch_bounds__(128) k_layernorm_fwd_any(const RowParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
   if (row >= p.rows) return;
   const int nv = p.d / 8;
   const uint4* src = reinterpret_cast<const uint4*>(chunk_row(p, row));
-  float s = 0.f;
-  for (int v = lane; v < nv; v += 32) {
-    float f[8];
-    unpack8(__ldg(src + v), f);
+  float mean = 0.f;
+  if constexpr (!RMS) {
+    float s = 0.f;
+    for (int v = lane; v < nv; v += 32) {
+      float f[8];
+      unpack8(__ldg(src + v), f);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) s += f[e];
+      for (int e = 0; e < 8; ++e) s += f[e];
+    }
+    mean = warp_sum(s) / static_cast<float>(p.d);
   }
-  const float mean = warp_sum(s) / static_cast<float>(p.d);
   float q = 0.f;
   for (int v = lane; v < nv; v += 32) {
     float f[8];
@@ -143,12 +158,18 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_any(const RowParams p) {
   const uint4* b4 = reinterpret_cast<const uint4*>(p.beta);
   uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + static_cast<long long>(row) * p.d);
   for (int v = lane; v < nv; v += 32) {
-    float f[8], g[8], b[8], o[8];
+    float f[8], g[8], o[8];
     unpack8(__ldg(src + v), f);
     unpack8(__ldg(g4 + v), g);
-    unpack8(__ldg(b4 + v), b);
+    if constexpr (RMS) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+      for (int e = 0; e < 8; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(f[e] * rstd)) * g[e];
+    } else {
+      float b[8];
+      unpack8(__ldg(b4 + v), b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+    }
     dst[v] = pack8(o);
   }
 }
@@ -580,7 +601,21 @@ cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaS
     case 2048: k_layernorm_fwd_reg<8, 1><<<grid4, 128, 0, s>>>(r); break;
     case 4096: k_layernorm_fwd_reg<16, 1><<<grid4, 128, 0, s>>>(r); break;
     case 8192: k_layernorm_fwd_reg<16, 2><<<grid2, 128, 0, s>>>(r); break;
-    default: k_layernorm_fwd_any<<<grid4, 128, 0, s>>>(r); break;
+    default: k_layernorm_fwd_any<false><<<grid4, 128, 0, s>>>(r); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_fwd(const RowParams& r, cudaStream_t s) {
+  if (r.rows <= 0) return cudaSuccess;
+  const int grid4 = (r.rows + 3) / 4;
+  const int grid2 = (r.rows + 1) / 2;
+  switch (r.d) {
+    case 1024: k_layernorm_fwd_reg<4, 1, true><<<grid4, 128, 0, s>>>(r); break;
+    case 2048: k_layernorm_fwd_reg<8, 1, true><<<grid4, 128, 0, s>>>(r); break;
+    case 4096: k_layernorm_fwd_reg<16, 1, true><<<grid4, 128, 0, s>>>(r); break;
+    case 8192: k_layernorm_fwd_reg<16, 2, true><<<grid2, 128, 0, s>>>(r); break;
+    default: k_layernorm_fwd_any<true><<<grid4, 128, 0, s>>>(r); break;
   }
   return cudaGetLastError();
 }

@@ -342,3 +342,19 @@ def test_layernorm_backward_step(T, d, N):
     assert_bf16_close("dgamma", f64(dga.t), sum(r[1] for r in refs))
     assert_bf16_close("dbeta", f64(dbe.t), sum(r[2] for r in refs))
     assert all(x.intact() for x in dX + [dga, dbe])
+
+
+@pytest.mark.parametrize("T,d,N", [(256, 4096, 8), (96, 8192, 4), (200, 1024, 8), (24, 136, 3)])
+def test_rmsnorm_gather(T, d, N):
+    """The listing's RMS norm, with its bf16 rounding of x * rstd before the weight."""
+    w = inputs.small_workload(T, d, N, sp=True, name=f"rms_{T}_{d}_{N}")
+    X, g = inputs.draw(w, "X"), inputs.draw(w, "gamma")
+    Xg = Guarded((T, d))
+    binding.tpmlp_rmsnorm_gather(list(dev(X[0]).split(T // N)), dev(g[0]), N, Xg.t)
+    torch.cuda.synchronize()
+    ref = oracle.all_gather([oracle.rms_norm(c, g[1], 1e-5) for c in _chunks(X[1], N)])
+    assert_bf16_close("Xg", f64(Xg.t), ref)
+    # both sides round x * rstd to bf16: elementwise within one output rounding plus a rare one-ulp flip
+    err = np.abs(f64(Xg.t) - ref)
+    assert np.mean(err <= np.abs(ref) * 2.0 ** -8 + 1e-30) > 0.999
+    assert Xg.intact()
