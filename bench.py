@@ -472,6 +472,28 @@ def run_other_rows(step, torch, binding, pk):
             ms = time_calls(torch, pair, 20) / 2.0
             out[name] = {"ms": round(ms, 4), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
                          "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes_per_launch": nb}
+    if w.sp:
+        # the rest of the sequence-parallel region on the step's shapes: the row-parallel GEMM with row bias,
+        # dropout (p = 0.1) and residual in its chunked store, and the dropout backward (+ row-bias gradient)
+        g = 2.0 * w.T * w.d * w.F
+        b2 = step.gamma  # any [d] bf16 vector serves as the row bias here
+        ms_t = time_calls(torch, lambda: binding.tpmlp_gemm2_bias_dropout_add(
+            step.H, step.B, w.N, step.Yc, bias2=b2, p=0.1, seed=1, offset=2, R_chunks=step.Xc), 10)
+        out["gemm2_bias_dropout_add"] = {"ms": round(ms_t, 4), "TFLOP/s": round(g / (ms_t * 1e-3) / 1e12, 1),
+                                         "frac": round(g / (ms_t * 1e-3) / 1e12 / pk.get("bf16_tflops_sustained",
+                                                                                          pk["bf16_tflops"]), 3)}
+        if w.backward:
+            db2 = torch.empty(w.d, dtype=torch.bfloat16, device="cuda")
+            dws = binding.workspace(binding.make_shape(w.T, w.d, w.F, w.N), binding.OP_DROPOUT_BWD)
+            nb = 4.0 * w.T * w.d
+            pair = lambda: (binding.tpmlp_dropout_backward(step.dYc, w.N, step.dXg, dbias2=db2, p=0.1, seed=1,
+                                                           offset=2, ws=dws),
+                            binding.tpmlp_dropout_backward(step.Yc, w.N, step.Xg, dbias2=db2, p=0.1, seed=1,
+                                                           offset=3, ws=dws))
+            ms_d = time_calls(torch, pair, 20) / 2.0
+            out["dropout_backward"] = {"ms": round(ms_d, 4), "GB/s": round(nb / (ms_d * 1e-3) / 1e9, 1),
+                                       "frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+                                       "bytes_per_launch": nb, "launches": 2}
     t = inputs.WORKLOADS["tiny_fp32_fwd"]
     f32 = lambda name: torch.from_numpy(np.ascontiguousarray(inputs.draw(t, name)[0])).cuda()
     X, A, B, b = f32("X"), f32("A"), f32("B"), f32("bias")

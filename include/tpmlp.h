@@ -91,8 +91,27 @@ enum {
   TPMLP_OP_BWD = 3,            /* tpmlp_backward */
   TPMLP_OP_SP_BWD = 4,         /* tpmlp_sp_backward */
   TPMLP_OP_DH_GELUPRIME = 5,   /* tpmlp_gemm_dh_geluprime with a dbias output */
-  TPMLP_OP_LN_BWD = 6          /* tpmlp_layernorm_backward */
+  TPMLP_OP_LN_BWD = 6,         /* tpmlp_layernorm_backward, tpmlp_layernorm_backward_add */
+  TPMLP_OP_SP_BLOCK_BWD = 7,   /* tpmlp_sp_block_backward */
+  TPMLP_OP_DROPOUT_BWD = 8     /* tpmlp_dropout_backward with a dbias2 output */
 };
+
+/* Dropout of the sequence-parallel region.  The pages name Dropout in the
+ * sequence-split region (deep-dive page, section "All-Reduce 통신의 All-Gather
+ * 및 Reduce-Scatter 분해"; glossary page, sequence-parallel paragraph) and give
+ * neither a rate nor a generator.  p: drop probability in [0, 1), float32.
+ * Element (r, c) of the gathered [T x d] output, index e = r d + c, is kept
+ * when 32 bits of Philox4x64-10 (Salmon et al., SC 2011) with counter
+ * (e / 8, offset, 0, 0) and key (seed, 0) -- word (e % 8) / 2, low half for
+ * even e, high half for odd e -- are below floor((1 - p) 2^32); kept elements
+ * are scaled by 1 / (1 - p).  The same (p, seed, offset) in the backward
+ * regenerates the forward's mask; advance offset per step for a new mask.
+ * A NULL tpmlp_dropout pointer means p = 0. */
+typedef struct {
+  float p;
+  uint64_t seed;
+  uint64_t offset;
+} tpmlp_dropout;
 
 /* Reduce-scatter modes of tpmlp_sp_forward. */
 enum {
@@ -177,6 +196,36 @@ TPMLP_API tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void
                                          void* dbeta, void* workspace, size_t workspace_bytes,
                                          tpmlp_stream_t stream);
 
+/* The whole sequence-parallel region of the MLP block (deep-dive page:
+ * RowParallelLinear in "분산 제어 소스코드 구조 패턴" adds its bias after the
+ * reduction; the SP section keeps Dropout in the sequence-split region):
+ *   Y_j = X_j + dropout(Z_j + bias2),
+ * Z_j chunk j of the reduced MLP output of tpmlp_sp_forward, bias2 [d] the
+ * row layer's bias or NULL, X_j the block input chunk (the residual, which
+ * the pages do not mention).  With TPMLP_RS_FUSED the row bias, dropout and
+ * residual run in the row-parallel GEMM's chunked store; with
+ * TPMLP_RS_PARTIALS in the reduce-scatter kernel.  Workspace, Hpre_out,
+ * H_out and Xg_out as in tpmlp_sp_forward.  bf16 only. */
+TPMLP_API tpmlp_status tpmlp_sp_block_forward(const void* const* X_chunks, const void* gamma, const void* beta,
+                                              float eps, const void* A, const void* B, const void* bias,
+                                              const void* bias2, const tpmlp_dropout* dropout,
+                                              const tpmlp_shape* shape, void* const* Y_chunks, int rs_mode,
+                                              void* Hpre_out, void* H_out, void* Xg_out, void* workspace,
+                                              size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Backward of tpmlp_sp_block_forward (chain rule): dZ = dY * keep / (1 - p)
+ * gathered to [T x d], dbias2 = column sums of dZ ([d] bf16, or NULL), the
+ * MLP and LayerNorm backward of tpmlp_sp_backward driven by dZ, and the
+ * residual's gradient dY_j added to dX_j.  `dropout` must equal the
+ * forward's.  Workspace: size of TPMLP_OP_SP_BLOCK_BWD.  bf16 only. */
+TPMLP_API tpmlp_status tpmlp_sp_block_backward(const void* const* X_chunks, const void* gamma, const void* beta,
+                                               float eps, const void* A, const void* B, const void* bias,
+                                               const tpmlp_dropout* dropout, const void* Hpre, const void* H,
+                                               const void* Xg, const void* const* dY_chunks,
+                                               const tpmlp_shape* shape, void* const* dX_chunks, void* dA, void* dB,
+                                               void* dbias, void* dbias2, void* dgamma, void* dbeta,
+                                               void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
 /* ------------------------------------------------------------------ single steps (bf16)
  * Each step is one kernel launch (plus a small fixed-order reduction where
  * noted); the block calls above are sequences of these.  They take explicit
@@ -195,6 +244,15 @@ TPMLP_API tpmlp_status tpmlp_gemm1_bias_gelu(const void* X, const void* A, const
 TPMLP_API tpmlp_status tpmlp_gemm2_shard_accum(const void* H, const void* B, const tpmlp_shape* shape, void* Y,
                                      void* const* Y_chunks, tpmlp_stream_t stream);
 
+/* tpmlp_gemm2_shard_accum into chunks with the rest of the sequence-parallel
+ * region in its store: Y_j = R_j + dropout(sum_i H_i B_i + bias2) for the
+ * rows of chunk j.  bias2 [d] or NULL; dropout as tpmlp_dropout (NULL: p = 0);
+ * R_chunks: host array of N residual chunk pointers [T/N x d], or NULL. */
+TPMLP_API tpmlp_status tpmlp_gemm2_bias_dropout_add(const void* H, const void* B, const void* bias2,
+                                                    const tpmlp_dropout* dropout, const void* const* R_chunks,
+                                                    const tpmlp_shape* shape, void* const* Y_chunks,
+                                                    tpmlp_stream_t stream);
+
 /* Per-shard partial outputs of the row-parallel layer, P_i = H_i B_i, as the
  * pages' ranks produce them before their collective.  P [N x T x d] bf16;
  * requires (ffn / N) % 64 == 0. */
@@ -206,6 +264,23 @@ TPMLP_API tpmlp_status tpmlp_gemm2_partials(const void* H, const void* B, const 
  * of N pointers [T/N x d]; T % N == 0. */
 TPMLP_API tpmlp_status tpmlp_reduce_scatter(const void* P, const tpmlp_shape* shape, void* const* Y_chunks,
                                   tpmlp_stream_t stream);
+
+/* tpmlp_reduce_scatter with the rest of the sequence-parallel region:
+ * Y_j = R_j + dropout(sum_i P_i[rows of chunk j] + bias2), in fp32, one
+ * rounding.  bias2, dropout and R_chunks as in tpmlp_gemm2_bias_dropout_add. */
+TPMLP_API tpmlp_status tpmlp_reduce_scatter_bias_dropout_add(const void* P, const void* bias2,
+                                                             const tpmlp_dropout* dropout,
+                                                             const void* const* R_chunks, const tpmlp_shape* shape,
+                                                             void* const* Y_chunks, tpmlp_stream_t stream);
+
+/* Dropout backward of the sequence-parallel region, gathering the chunks:
+ * dZ[j T/N + r] = dY_chunks[j][r] * keep / (1 - p) ([T x d] bf16); with
+ * dbias2 != NULL also dbias2 [d] bf16 = the fixed-order column sums of dZ
+ * (before its rounding; workspace: size of TPMLP_OP_DROPOUT_BWD).  dropout
+ * as tpmlp_dropout (NULL: p = 0, a plain gather). */
+TPMLP_API tpmlp_status tpmlp_dropout_backward(const void* const* dY_chunks, const tpmlp_dropout* dropout,
+                                              const tpmlp_shape* shape, void* dZ, void* dbias2, void* workspace,
+                                              size_t workspace_bytes, tpmlp_stream_t stream);
 
 /* LayerNorm of every chunk into its row slot of the gathered activation:
  * Xg[j T/N + r] = LN(X_chunks[j][r]).  Xg [T x d]; T % N == 0. */
@@ -250,6 +325,16 @@ TPMLP_API tpmlp_status tpmlp_gemm_dx_shard_accum(const void* dHpre, const void* 
 TPMLP_API tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, const void* gamma, float eps, const void* dXg,
                                       const tpmlp_shape* shape, void* const* dX_chunks, void* dgamma, void* dbeta,
                                       void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* tpmlp_layernorm_backward with the residual's gradient added to the input
+ * gradient: dX_chunks[j] = LN backward(dXg rows of chunk j) + R_chunks[j]
+ * (R_chunks: host array of N pointers [T/N x d]).  Workspace: size of
+ * TPMLP_OP_LN_BWD. */
+TPMLP_API tpmlp_status tpmlp_layernorm_backward_add(const void* const* X_chunks, const void* gamma, float eps,
+                                                    const void* dXg, const void* const* R_chunks,
+                                                    const tpmlp_shape* shape, void* const* dX_chunks, void* dgamma,
+                                                    void* dbeta, void* workspace, size_t workspace_bytes,
+                                                    tpmlp_stream_t stream);
 
 /* LayerNorm backward exactly as tpmlp_layernorm_backward, for callers that
  * cannot allocate device memory: it takes no workspace.  (This entry point

@@ -19,7 +19,8 @@ _lib = None
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
 BF16, FP32 = 0, 1
-OP_FWD, OP_SP_FWD, OP_SP_FWD_PARTIALS, OP_BWD, OP_SP_BWD, OP_DH_GELUPRIME, OP_LN_BWD = range(7)
+(OP_FWD, OP_SP_FWD, OP_SP_FWD_PARTIALS, OP_BWD, OP_SP_BWD, OP_DH_GELUPRIME, OP_LN_BWD, OP_SP_BLOCK_BWD,
+ OP_DROPOUT_BWD) = range(9)
 RS_FUSED, RS_PARTIALS = 0, 1
 
 
@@ -34,9 +35,14 @@ class Shape(ctypes.Structure):
                 ("n_shards", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
+class Dropout(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+
+
 _P = ctypes.c_void_p
 _PP = ctypes.POINTER(ctypes.c_void_p)
 _SP = ctypes.POINTER(Shape)
+_DP = ctypes.POINTER(Dropout)
 _SIGS = {
     "tpmlp_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tpmlp_workspace_size": ([_SP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
@@ -61,6 +67,15 @@ _SIGS = {
                                  ctypes.c_int),
     "tpmlp_layernorm_backward_noalloc": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P], ctypes.c_int),
     "tpmlp_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
+    "tpmlp_sp_block_forward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _P, _DP, _SP, _PP, ctypes.c_int, _P, _P, _P,
+                                _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_sp_block_backward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _DP, _P, _P, _P, _PP, _SP, _PP, _P, _P, _P,
+                                 _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_gemm2_bias_dropout_add": ([_P, _P, _P, _DP, _PP, _SP, _PP, _P], ctypes.c_int),
+    "tpmlp_reduce_scatter_bias_dropout_add": ([_P, _P, _DP, _PP, _SP, _PP, _P], ctypes.c_int),
+    "tpmlp_dropout_backward": ([_PP, _DP, _SP, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_layernorm_backward_add": ([_PP, _P, ctypes.c_float, _P, _PP, _SP, _PP, _P, _P, _P, ctypes.c_size_t, _P],
+                                     ctypes.c_int),
 }
 
 
@@ -100,6 +115,14 @@ def _ptr(t):
 def _ptrs(ts):
     arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
     return ctypes.cast(arr, _PP), arr
+
+
+def _dropout(p, seed, offset):
+    return None if p is None else ctypes.byref(Dropout(p, seed, offset))
+
+
+def _opt_ptrs(ts):
+    return (None, None) if ts is None else _ptrs(ts)
 
 
 def _stream(stream):
@@ -183,6 +206,37 @@ def tpmlp_sp_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_chunks
         _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
 
 
+def tpmlp_sp_block_forward(X_chunks, gamma, beta, A, B, N, Y_chunks, bias=None, bias2=None, p=None, seed=0, offset=0,
+                           eps=1e-5, rs_mode=RS_FUSED, Hpre_out=None, H_out=None, Xg_out=None, ws=None, stream=None):
+    """Y_j = X_j + dropout(Z_j + bias2); p=None passes a NULL dropout (p = 0)."""
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, A.shape[1], N)
+    op = OP_SP_FWD if rs_mode == RS_FUSED else OP_SP_FWD_PARTIALS
+    ws = workspace(shape, op, A.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    yp, _ya = _ptrs(Y_chunks)
+    _check("tpmlp_sp_block_forward", lib().tpmlp_sp_block_forward(
+        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _ptr(bias2), _dropout(p, seed, offset),
+        ctypes.byref(shape), yp, rs_mode, _ptr(Hpre_out), _ptr(H_out), _ptr(Xg_out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return Y_chunks
+
+
+def tpmlp_sp_block_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_chunks, dA, dB, dgamma, dbeta,
+                            bias=None, dbias=None, dbias2=None, p=None, seed=0, offset=0, eps=1e-5, H=None, Xg=None,
+                            ws=None, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, A.shape[1], N)
+    ws = workspace(shape, OP_SP_BLOCK_BWD, A.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    dyp, _dya = _ptrs(dY_chunks)
+    dxp, _dxa = _ptrs(dX_chunks)
+    _check("tpmlp_sp_block_backward", lib().tpmlp_sp_block_backward(
+        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _dropout(p, seed, offset), _ptr(Hpre),
+        _ptr(H), _ptr(Xg), dyp, ctypes.byref(shape), dxp, _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dbias2),
+        _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
+
+
 # ----------------------------------------------------------------------------- single steps
 
 def tpmlp_gemm1_bias_gelu(X, A, bias, N, H, Hpre=None, stream=None):
@@ -201,6 +255,15 @@ def tpmlp_gemm2_shard_accum(H, B, N, Y=None, Y_chunks=None, stream=None):
                                                                     yp, _stream(stream)))
 
 
+def tpmlp_gemm2_bias_dropout_add(H, B, N, Y_chunks, bias2=None, p=None, seed=0, offset=0, R_chunks=None,
+                                 stream=None):
+    shape = make_shape(H.shape[0], B.shape[1], H.shape[1], N)
+    yp, _ya = _ptrs(Y_chunks)
+    rp, _ra = _opt_ptrs(R_chunks)
+    _check("tpmlp_gemm2_bias_dropout_add", lib().tpmlp_gemm2_bias_dropout_add(
+        _ptr(H), _ptr(B), _ptr(bias2), _dropout(p, seed, offset), rp, ctypes.byref(shape), yp, _stream(stream)))
+
+
 def tpmlp_gemm2_partials(H, B, N, P, stream=None):
     shape = make_shape(H.shape[0], B.shape[1], H.shape[1], N)
     _check("tpmlp_gemm2_partials", lib().tpmlp_gemm2_partials(_ptr(H), _ptr(B), ctypes.byref(shape), _ptr(P),
@@ -212,6 +275,27 @@ def tpmlp_reduce_scatter(P, N, Y_chunks, stream=None):
     shape = make_shape(T, d, 8 * N, N)  # ffn unused by this step
     yp, _ya = _ptrs(Y_chunks)
     _check("tpmlp_reduce_scatter", lib().tpmlp_reduce_scatter(_ptr(P), ctypes.byref(shape), yp, _stream(stream)))
+
+
+def tpmlp_reduce_scatter_bias_dropout_add(P, N, Y_chunks, bias2=None, p=None, seed=0, offset=0, R_chunks=None,
+                                          stream=None):
+    _, T, d = P.shape
+    shape = make_shape(T, d, 8 * N, N)  # ffn unused by this step
+    yp, _ya = _ptrs(Y_chunks)
+    rp, _ra = _opt_ptrs(R_chunks)
+    _check("tpmlp_reduce_scatter_bias_dropout_add", lib().tpmlp_reduce_scatter_bias_dropout_add(
+        _ptr(P), _ptr(bias2), _dropout(p, seed, offset), rp, ctypes.byref(shape), yp, _stream(stream)))
+
+
+def tpmlp_dropout_backward(dY_chunks, N, dZ, dbias2=None, p=None, seed=0, offset=0, ws=None, stream=None):
+    rows, d = dY_chunks[0].shape
+    shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
+    if dbias2 is not None and ws is None:
+        ws = workspace(shape, OP_DROPOUT_BWD, dZ.device)
+    dyp, _dya = _ptrs(dY_chunks)
+    _check("tpmlp_dropout_backward", lib().tpmlp_dropout_backward(
+        dyp, _dropout(p, seed, offset), ctypes.byref(shape), _ptr(dZ), _ptr(dbias2), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def tpmlp_layernorm_gather(X_chunks, gamma, beta, N, Xg, eps=1e-5, stream=None):
@@ -266,6 +350,19 @@ def tpmlp_layernorm_backward(X_chunks, gamma, dXg, N, dX_chunks, dgamma, dbeta, 
     _check("tpmlp_layernorm_backward", lib().tpmlp_layernorm_backward(
         xp, _ptr(gamma), eps, _ptr(dXg), ctypes.byref(shape), dxp, _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def tpmlp_layernorm_backward_add(X_chunks, gamma, dXg, R_chunks, N, dX_chunks, dgamma, dbeta, eps=1e-5, ws=None,
+                                 stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
+    ws = workspace(shape, OP_LN_BWD, dXg.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    rp, _ra = _ptrs(R_chunks)
+    dxp, _dxa = _ptrs(dX_chunks)
+    _check("tpmlp_layernorm_backward_add", lib().tpmlp_layernorm_backward_add(
+        xp, _ptr(gamma), eps, _ptr(dXg), rp, ctypes.byref(shape), dxp, _ptr(dgamma), _ptr(dbeta), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def tpmlp_layernorm_backward_noalloc(X_chunks, gamma, dXg, N, dX_chunks, dgamma, dbeta, eps=1e-5, stream=None):

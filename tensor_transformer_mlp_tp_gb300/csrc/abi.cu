@@ -2,6 +2,7 @@
 // sequences of the block calls.  Everything here is host code except the
 // device error words and the wait-timeout self test.
 #include <climits>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -122,7 +123,7 @@ bool chunks_ok(const void* const* c, int n) {
 
 // Sizes of the workspace regions (bytes, each 256-aligned).
 struct Sizes {
-  size_t td, tf, ptd, colsum, lnbwd;
+  size_t td, tf, ptd, colsum, lnbwd, dropcol;
 };
 
 
@@ -136,6 +137,7 @@ Sizes sizes_of(const tpmlp_shape* s) {
   const size_t m_blocks = (T + kBM - 1) / kBM;
   z.colsum = align_up(4 * m_blocks * F * 4);
   z.lnbwd = align_up(layernorm_bwd_scratch_floats(static_cast<int>(T), static_cast<int>(d)) * 4);
+  z.dropcol = align_up(dropout_bwd_scratch_floats(static_cast<int>(T), static_cast<int>(d)) * 4);
   return z;
 }
 
@@ -149,6 +151,8 @@ size_t ws_bytes(const tpmlp_shape* s, int op) {
     case TPMLP_OP_SP_BWD: return 3 * z.tf + z.colsum + 3 * z.td + z.lnbwd;
     case TPMLP_OP_DH_GELUPRIME: return z.colsum;
     case TPMLP_OP_LN_BWD: return z.lnbwd;
+    case TPMLP_OP_SP_BLOCK_BWD: return 3 * z.tf + z.colsum + 3 * z.td + z.lnbwd + z.dropcol;
+    case TPMLP_OP_DROPOUT_BWD: return z.dropcol;
     default: return 0;
   }
 }
@@ -177,6 +181,34 @@ ConstChunkPtrs to_const_chunks(const void* const* c, int n) {
   return r;
 }
 
+// The rest of the sequence-parallel region: row bias, dropout (p in [0, 1), float32) and residual chunks.
+tpmlp_status make_tail(const void* bias2, const tpmlp_dropout* drop, const void* const* R_chunks, int n, SpTail* t) {
+  if (!opt_ok(bias2)) return TPMLP_ERR_INVALID_ARG;
+  const float p = drop != nullptr ? drop->p : 0.f;
+  if (!(p >= 0.f && p < 1.f)) return TPMLP_ERR_INVALID_ARG;
+  if (R_chunks != nullptr && !chunks_ok(R_chunks, n)) return TPMLP_ERR_INVALID_ARG;
+  *t = SpTail{};
+  t->on = true;
+  t->bias2 = bias2;
+  if (R_chunks != nullptr) t->residual = to_const_chunks(R_chunks, n);
+  const double keep = 1.0 - static_cast<double>(p);
+  t->thr = static_cast<unsigned long long>(std::floor(keep * 4294967296.0));
+  t->scale = static_cast<float>(1.0 / keep);
+  t->seed = drop != nullptr ? drop->seed : 0;
+  t->offset = drop != nullptr ? drop->offset : 0;
+  return TPMLP_OK;
+}
+
+void apply_tail(RowParams& r, const SpTail& t) {
+  r.tail = 1;
+  r.bias2 = t.bias2;
+  r.add_chunks = t.residual;
+  r.drop_scale = t.scale;
+  r.drop_seed = t.seed;
+  r.drop_offset = t.offset;
+  r.drop_thr = t.thr;
+}
+
 // ------------------------------------------------------------------ step implementations (validated inputs)
 
 cudaError_t do_gemm1(const DeviceCtx& c, const void* X, const void* A, const void* bias, const tpmlp_shape* s,
@@ -197,7 +229,7 @@ cudaError_t do_gemm1(const DeviceCtx& c, const void* X, const void* A, const voi
 }
 
 cudaError_t do_gemm2(const DeviceCtx& c, const void* H, const void* B, const tpmlp_shape* s, void* Y,
-                     void* const* Y_chunks, cudaStream_t st) {
+                     void* const* Y_chunks, cudaStream_t st, const SpTail* tail = nullptr) {
   GemmLaunch g;
   g.M = static_cast<int>(s->tokens);
   g.N = static_cast<int>(s->d);
@@ -210,6 +242,7 @@ cudaError_t do_gemm2(const DeviceCtx& c, const void* H, const void* B, const tpm
   if (Y_chunks != nullptr) {
     g.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
     g.chunks = to_chunks(Y_chunks, s->n_shards);
+    if (tail != nullptr) g.tail = *tail;
   }
   return launch_gemm(g, c, st);
 }
@@ -231,7 +264,7 @@ cudaError_t do_gemm2_partials(const DeviceCtx& c, const void* H, const void* B, 
 }
 
 cudaError_t do_reduce_scatter(const DeviceCtx& c, const void* P, const tpmlp_shape* s, void* const* Y_chunks,
-                              cudaStream_t st) {
+                              cudaStream_t st, const SpTail* tail = nullptr) {
   RowParams r{};
   r.out_chunks = to_chunks(Y_chunks, s->n_shards);
   r.rows = static_cast<int>(s->tokens);
@@ -240,6 +273,7 @@ cudaError_t do_reduce_scatter(const DeviceCtx& c, const void* P, const tpmlp_sha
   r.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
   r.src = P;
   r.shard_stride = s->tokens * s->d;
+  if (tail != nullptr) apply_tail(r, *tail);
   return launch_reduce_scatter(r, c, st);
 }
 
@@ -324,8 +358,9 @@ cudaError_t do_dx(const DeviceCtx& c, const void* dHpre, const void* A, const tp
 
 cudaError_t do_ln_bwd(const DeviceCtx& c, const void* const* X_chunks, const void* gamma, float eps, const void* dXg,
                       const tpmlp_shape* s, void* const* dX_chunks, void* dgamma, void* dbeta, float* partial,
-                      cudaStream_t st) {
+                      cudaStream_t st, const void* const* add_chunks = nullptr) {
   RowParams r{};
+  if (add_chunks != nullptr) r.add_chunks = to_const_chunks(add_chunks, s->n_shards);
   r.in_chunks = to_const_chunks(X_chunks, s->n_shards);
   r.out_chunks = to_chunks(dX_chunks, s->n_shards);
   r.rows = static_cast<int>(s->tokens);
@@ -337,6 +372,20 @@ cudaError_t do_ln_bwd(const DeviceCtx& c, const void* const* X_chunks, const voi
   r.src = dXg;
   return launch_layernorm_bwd(r, partial, layernorm_bwd_scratch_floats(r.rows, r.d), c, static_cast<float*>(dgamma),
                               static_cast<float*>(dbeta), st);
+}
+
+// dZ = keep * dY / (1 - p) gathered to [T x d]; dbias2 (optional) = column sums through `partial`.
+cudaError_t do_dropout_bwd(const void* const* dY_chunks, const SpTail& t, const tpmlp_shape* s, void* dZ,
+                           void* dbias2, float* partial, cudaStream_t st) {
+  RowParams r{};
+  r.in_chunks = to_const_chunks(dY_chunks, s->n_shards);
+  r.rows = static_cast<int>(s->tokens);
+  r.d = static_cast<int>(s->d);
+  r.n_chunks = s->n_shards;
+  r.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
+  r.dst = dZ;
+  apply_tail(r, t);
+  return launch_dropout_bwd(r, partial, dbias2, st);
 }
 
 // Backward core shared by tpmlp_backward and tpmlp_sp_backward.  With Hpre
@@ -389,12 +438,12 @@ const char* tpmlp_status_string(tpmlp_status s) {
 tpmlp_status tpmlp_workspace_size(const tpmlp_shape* shape, int op, size_t* bytes) {
   if (bytes == nullptr) return TPMLP_ERR_INVALID_ARG;
   const bool sp = op == TPMLP_OP_SP_FWD || op == TPMLP_OP_SP_FWD_PARTIALS || op == TPMLP_OP_SP_BWD ||
-                  op == TPMLP_OP_LN_BWD;
+                  op == TPMLP_OP_LN_BWD || op == TPMLP_OP_SP_BLOCK_BWD || op == TPMLP_OP_DROPOUT_BWD;
   const bool bf16_only = op != TPMLP_OP_FWD;
   tpmlp_status st = check_shape(shape, sp, bf16_only);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (op < TPMLP_OP_FWD || op > TPMLP_OP_LN_BWD) return TPMLP_ERR_INVALID_ARG;
+  if (op < TPMLP_OP_FWD || op > TPMLP_OP_DROPOUT_BWD) return TPMLP_ERR_INVALID_ARG;
   *bytes = ws_bytes(shape, op);
   return TPMLP_OK;
 }
@@ -447,10 +496,12 @@ tpmlp_status tpmlp_forward(const void* X, const void* A, const void* B, const vo
   return cuda_status(e);
 }
 
-tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
-                              const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
-                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out, void* Xg_out,
-                              void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+// tpmlp_sp_forward, and with `tail` (validated, residual = X_chunks) tpmlp_sp_block_forward.
+static tpmlp_status sp_forward_impl(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                    const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
+                                    void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out, void* Xg_out,
+                                    void* workspace, size_t workspace_bytes, tpmlp_stream_t stream,
+                                    const SpTail* tail) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
@@ -475,14 +526,37 @@ tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, co
   if (e == cudaSuccess) e = do_gemm1(c, Xg, A, bias, shape, H, Hpre_out, kEpiBiasGelu, s);
   if (e == cudaSuccess) {
     if (rs_mode == TPMLP_RS_FUSED) {
-      e = do_gemm2(c, H, B, shape, nullptr, Y_chunks, s);
+      e = do_gemm2(c, H, B, shape, nullptr, Y_chunks, s, tail);
     } else {
       void* P = ws.take(z.ptd);
       e = do_gemm2_partials(c, H, B, shape, P, s);
-      if (e == cudaSuccess) e = do_reduce_scatter(c, P, shape, Y_chunks, s);
+      if (e == cudaSuccess) e = do_reduce_scatter(c, P, shape, Y_chunks, s, tail);
     }
   }
   return cuda_status(e);
+}
+
+tpmlp_status tpmlp_sp_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                              const void* A, const void* B, const void* bias, const tpmlp_shape* shape,
+                              void* const* Y_chunks, int rs_mode, void* Hpre_out, void* H_out, void* Xg_out,
+                              void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+  return sp_forward_impl(X_chunks, gamma, beta, eps, A, B, bias, shape, Y_chunks, rs_mode, Hpre_out, H_out, Xg_out,
+                         workspace, workspace_bytes, stream, nullptr);
+}
+
+tpmlp_status tpmlp_sp_block_forward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                    const void* A, const void* B, const void* bias, const void* bias2,
+                                    const tpmlp_dropout* dropout, const tpmlp_shape* shape, void* const* Y_chunks,
+                                    int rs_mode, void* Hpre_out, void* H_out, void* Xg_out, void* workspace,
+                                    size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!chunks_ok(X_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
+  SpTail tail;
+  if ((st = make_tail(bias2, dropout, X_chunks, shape->n_shards, &tail)) != TPMLP_OK) return st;
+  return sp_forward_impl(X_chunks, gamma, beta, eps, A, B, bias, shape, Y_chunks, rs_mode, Hpre_out, H_out, Xg_out,
+                         workspace, workspace_bytes, stream, &tail);
 }
 
 tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const void* bias, const void* Hpre,
@@ -502,12 +576,13 @@ tpmlp_status tpmlp_backward(const void* X, const void* A, const void* B, const v
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
-tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
-                               const void* A, const void* B, const void* bias, const void* Hpre, const void* H,
-                               const void* Xg_saved, const void* const* dY_chunks, const tpmlp_shape* shape,
-                               void* const* dX_chunks,
-                               void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
-                               size_t workspace_bytes, tpmlp_stream_t stream) {
+// tpmlp_sp_backward, and with `tail` (validated) tpmlp_sp_block_backward.
+static tpmlp_status sp_backward_impl(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                     const void* A, const void* B, const void* bias, const void* Hpre, const void* H,
+                                     const void* Xg_saved, const void* const* dY_chunks, const tpmlp_shape* shape,
+                                     void* const* dX_chunks, void* dA, void* dB, void* dbias, void* dgamma,
+                                     void* dbeta, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream,
+                                     const SpTail* tail, void* dbias2) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
@@ -518,8 +593,9 @@ tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, c
   if (!chunks_ok(X_chunks, n) || !chunks_ok(dY_chunks, n) || !chunks_ok(dX_chunks, n)) return TPMLP_ERR_INVALID_ARG;
   if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
   if (!(eps >= 0.f)) return TPMLP_ERR_INVALID_ARG;
-  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_SP_BWD))
-    return TPMLP_ERR_WORKSPACE;
+  if (!opt_ok(dbias2)) return TPMLP_ERR_INVALID_ARG;
+  const int op = tail != nullptr ? TPMLP_OP_SP_BLOCK_BWD : TPMLP_OP_SP_BWD;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, op)) return TPMLP_ERR_WORKSPACE;
   DeviceCtx c;
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -536,27 +612,61 @@ tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, c
     e = do_layernorm(c, X_chunks, gamma, beta, eps, shape, Xg, s);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  // The All-Gather of dY is free when the chunks already lie back to back.
-  const size_t chunk_bytes = static_cast<size_t>(shape->tokens / n) * shape->d * 2;
-  bool contiguous = true;
-  for (int j = 1; j < n; ++j)
-    contiguous = contiguous && static_cast<const uint8_t*>(dY_chunks[j]) ==
-                                   static_cast<const uint8_t*>(dY_chunks[0]) + j * chunk_bytes;
   const void* dY = dY_chunks[0];
-  if (!contiguous) {
-    RowParams r{};
-    r.in_chunks = to_const_chunks(dY_chunks, n);
-    r.rows = static_cast<int>(shape->tokens);
-    r.d = static_cast<int>(shape->d);
-    r.n_chunks = n;
-    r.rows_per_chunk = static_cast<int>(shape->tokens / n);
-    r.dst = dYg;
-    if ((e = launch_gather_rows(r, c, s)) != cudaSuccess) return cuda_status(e);
+  if (tail != nullptr) {
+    // the dropout backward gathers dZ = keep * dY / (1 - p) (and dbias2); the MLP backward runs on dZ and
+    // the residual's gradient dY joins the input gradient in the LayerNorm backward
+    float* dropcol = static_cast<float*>(ws.take(z.dropcol));
+    if ((e = do_dropout_bwd(dY_chunks, *tail, shape, dYg, dbias2, dropcol, s)) != cudaSuccess) return cuda_status(e);
     dY = dYg;
+  } else {
+    // The All-Gather of dY is free when the chunks already lie back to back.
+    const size_t chunk_bytes = static_cast<size_t>(shape->tokens / n) * shape->d * 2;
+    bool contiguous = true;
+    for (int j = 1; j < n; ++j)
+      contiguous = contiguous && static_cast<const uint8_t*>(dY_chunks[j]) ==
+                                     static_cast<const uint8_t*>(dY_chunks[0]) + j * chunk_bytes;
+    if (!contiguous) {
+      RowParams r{};
+      r.in_chunks = to_const_chunks(dY_chunks, n);
+      r.rows = static_cast<int>(shape->tokens);
+      r.d = static_cast<int>(shape->d);
+      r.n_chunks = n;
+      r.rows_per_chunk = static_cast<int>(shape->tokens / n);
+      r.dst = dYg;
+      if ((e = launch_gather_rows(r, c, s)) != cudaSuccess) return cuda_status(e);
+      dY = dYg;
+    }
   }
   e = backward_core(c, Xg, A, B, bias, Hpre, H, dY, shape, dXg, dA, dB, dbias, ws, s);
-  if (e == cudaSuccess) e = do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta, lnpart, s);
+  if (e == cudaSuccess)
+    e = do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta, lnpart, s,
+                  tail != nullptr ? dY_chunks : nullptr);
   return cuda_status(e);
+}
+
+tpmlp_status tpmlp_sp_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                               const void* A, const void* B, const void* bias, const void* Hpre, const void* H,
+                               const void* Xg_saved, const void* const* dY_chunks, const tpmlp_shape* shape,
+                               void* const* dX_chunks, void* dA, void* dB, void* dbias, void* dgamma, void* dbeta,
+                               void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
+  return sp_backward_impl(X_chunks, gamma, beta, eps, A, B, bias, Hpre, H, Xg_saved, dY_chunks, shape, dX_chunks, dA,
+                          dB, dbias, dgamma, dbeta, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+tpmlp_status tpmlp_sp_block_backward(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                     const void* A, const void* B, const void* bias, const tpmlp_dropout* dropout,
+                                     const void* Hpre, const void* H, const void* Xg, const void* const* dY_chunks,
+                                     const tpmlp_shape* shape, void* const* dX_chunks, void* dA, void* dB,
+                                     void* dbias, void* dbias2, void* dgamma, void* dbeta, void* workspace,
+                                     size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  SpTail tail;
+  if ((st = make_tail(nullptr, dropout, nullptr, shape->n_shards, &tail)) != TPMLP_OK) return st;
+  return sp_backward_impl(X_chunks, gamma, beta, eps, A, B, bias, Hpre, H, Xg, dY_chunks, shape, dX_chunks, dA, dB,
+                          dbias, dgamma, dbeta, workspace, workspace_bytes, stream, &tail, dbias2);
 }
 
 // ------------------------------------------------------------------ single steps
@@ -704,6 +814,69 @@ tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, const void* g
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta,
                                static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm2_bias_dropout_add(const void* H, const void* B, const void* bias2, const tpmlp_dropout* dropout,
+                                          const void* const* R_chunks, const tpmlp_shape* shape,
+                                          void* const* Y_chunks, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({H, B}) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
+  SpTail tail;
+  if ((st = make_tail(bias2, dropout, R_chunks, shape->n_shards, &tail)) != TPMLP_OK) return st;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_gemm2(c, H, B, shape, nullptr, Y_chunks, reinterpret_cast<cudaStream_t>(stream), &tail));
+}
+
+tpmlp_status tpmlp_reduce_scatter_bias_dropout_add(const void* P, const void* bias2, const tpmlp_dropout* dropout,
+                                                   const void* const* R_chunks, const tpmlp_shape* shape,
+                                                   void* const* Y_chunks, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({P}) || !chunks_ok(Y_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
+  SpTail tail;
+  if ((st = make_tail(bias2, dropout, R_chunks, shape->n_shards, &tail)) != TPMLP_OK) return st;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_reduce_scatter(c, P, shape, Y_chunks, reinterpret_cast<cudaStream_t>(stream), &tail));
+}
+
+tpmlp_status tpmlp_dropout_backward(const void* const* dY_chunks, const tpmlp_dropout* dropout,
+                                    const tpmlp_shape* shape, void* dZ, void* dbias2, void* workspace,
+                                    size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({dZ}) || !opt_ok(dbias2) || !chunks_ok(dY_chunks, shape->n_shards)) return TPMLP_ERR_INVALID_ARG;
+  SpTail tail;
+  if ((st = make_tail(nullptr, dropout, nullptr, shape->n_shards, &tail)) != TPMLP_OK) return st;
+  if (dbias2 != nullptr && (workspace == nullptr || !al16(workspace) ||
+                            workspace_bytes < ws_bytes(shape, TPMLP_OP_DROPOUT_BWD)))
+    return TPMLP_ERR_WORKSPACE;
+  return cuda_status(do_dropout_bwd(dY_chunks, tail, shape, dZ, dbias2, static_cast<float*>(workspace),
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_layernorm_backward_add(const void* const* X_chunks, const void* gamma, float eps, const void* dXg,
+                                          const void* const* R_chunks, const tpmlp_shape* shape,
+                                          void* const* dX_chunks, void* dgamma, void* dbeta, void* workspace,
+                                          size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({gamma, dXg, dgamma, dbeta}) || !chunks_ok(X_chunks, shape->n_shards) ||
+      !chunks_ok(dX_chunks, shape->n_shards) || !chunks_ok(R_chunks, shape->n_shards) || !(eps >= 0.f))
+    return TPMLP_ERR_INVALID_ARG;
+  if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_LN_BWD))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta,
+                               static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream), R_chunks));
 }
 
 }  // extern "C"

@@ -66,6 +66,13 @@ struct GemmParams {
   float* colsum;            // [4 * m_blocks x N] fp32 column partial sums, or nullptr
   int rows_per_chunk;       // >0: row r of C goes to chunk r / rows_per_chunk
   ChunkPtrs chunks;
+  // Sequence-parallel tail of the chunked store (kEpiStore with rows_per_chunk > 0 and tail != 0):
+  // out = res + keep * (acc + bias) * drop_scale, bias = the row layer's [N] bias or nullptr,
+  // res = the residual rows in chunk layout (res_chunks.p[0] == nullptr: none), keep from philox.cuh.
+  int tail;
+  float drop_scale;
+  unsigned long long drop_seed, drop_offset, drop_thr;  // drop_thr = 2^32 keeps every element
+  ConstChunkPtrs res_chunks;
   unsigned int* err;
   unsigned long long timeout_ns;
 };
@@ -88,6 +95,13 @@ struct RowParams {
   float* stats;               // [rows x 2] fp32 mean, rstd (LayerNorm backward)
   int rows_per_block;         // rows summed by one column-partial block (LayerNorm backward)
   int slots;                  // shared-memory row slots of the streaming kernels
+  // Sequence-parallel tail (reduce-scatter: out = add + keep * (sum + bias2) * drop_scale;
+  // dropout backward: dst = keep * in * drop_scale; LayerNorm backward: dx += add)
+  int tail;                   // nonzero: apply the tail below
+  const void* bias2;          // [d] bf16 or nullptr
+  ConstChunkPtrs add_chunks;  // N chunk pointers [rows_per_chunk x d] bf16, or p[0] == nullptr
+  float drop_scale;
+  unsigned long long drop_seed, drop_offset, drop_thr;
   unsigned int* err;          // device error words
   unsigned long long timeout_ns;
 };

@@ -150,6 +150,13 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
   p.colsum = g.colsum;
   p.rows_per_chunk = g.rows_per_chunk;
   p.chunks = g.chunks;
+  p.tail = g.tail.on && g.rows_per_chunk > 0 && g.epi == kEpiStore ? 1 : 0;
+  if (p.tail) p.bias = g.tail.bias2;
+  p.drop_scale = g.tail.scale;
+  p.drop_seed = g.tail.seed;
+  p.drop_offset = g.tail.offset;
+  p.drop_thr = g.tail.thr;
+  p.res_chunks = g.tail.residual;
   p.err = ctx.err;
   p.timeout_ns = ctx.timeout_ns;
   const long long tiles = static_cast<long long>(p.m_blocks) * p.n_blocks * p.shards;

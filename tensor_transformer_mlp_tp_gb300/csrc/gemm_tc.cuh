@@ -24,6 +24,7 @@
 // releases its TMEM before exiting.
 #pragma once
 
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace tpmlp {
@@ -114,6 +115,38 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], uint32_t lane)
   return v[0];
 }
 
+// The sequence-parallel tail on 32 columns of one output row:
+// v = res + keep * (v + bias2) * scale, res from the residual chunk of the row.
+__device__ __forceinline__ void sp_tail_32(const GemmParams& p, float (&v)[32], int row, int col0) {
+  if (p.bias != nullptr) {
+    float b[32];
+    load_row32(static_cast<const __nv_bfloat16*>(p.bias), col0, p.N, b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += b[i];
+  }
+  if (p.drop_thr < kKeepAll) {
+    // element index row * N + col0 is a multiple of 8 (N % 8 == 0, col0 % 32 == 0): four whole blocks
+    const unsigned long long q0 = (static_cast<unsigned long long>(row) * p.N + col0) >> 3;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t m = dropout_keep8(q0 + g, p.drop_offset, p.drop_seed, p.drop_thr);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[8 * g + j] = (m >> j) & 1u ? v[8 * g + j] * p.drop_scale : 0.f;
+    }
+  } else if (p.drop_scale != 1.f) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= p.drop_scale;
+  }
+  if (p.res_chunks.p[0] != nullptr) {
+    const int j = row / p.rows_per_chunk;
+    float r[32];
+    load_row32(static_cast<const __nv_bfloat16*>(p.res_chunks.p[j]) + static_cast<long long>(row - j * p.rows_per_chunk) * p.N,
+               col0, p.N, r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += r[i];
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32], const uint4 (&aux_raw)[4], int row,
                                             int col0, int shard, int mb, int quad, uint32_t lane) {
@@ -137,6 +170,7 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
     if (row_ok) {
       __nv_bfloat16* dst;
       if (p.rows_per_chunk > 0) {
+        if (p.tail) sp_tail_32(p, v, row, col0);
         const int j = row / p.rows_per_chunk;
         dst = static_cast<__nv_bfloat16*>(p.chunks.p[j]) + static_cast<long long>(row - j * p.rows_per_chunk) * p.ld0;
       } else {

@@ -16,6 +16,17 @@ struct Operand {
   bool mn_major;
 };
 
+// The rest of the sequence-parallel region after the row-parallel reduction:
+// out = residual + keep * (sum + bias2) * scale (philox.cuh decides keep).
+struct SpTail {
+  bool on = false;
+  const void* bias2 = nullptr;    // [d] bf16 or nullptr
+  ConstChunkPtrs residual{};      // chunk layout, or residual.p[0] == nullptr
+  float scale = 1.f;              // 1 / (1 - p)
+  unsigned long long seed = 0, offset = 0;
+  unsigned long long thr = 1ull << 32;  // floor((1 - p) 2^32); 2^32 keeps all
+};
+
 struct GemmLaunch {
   int M = 0, N = 0, K = 0;
   Operand a{}, b{};
@@ -32,6 +43,7 @@ struct GemmLaunch {
   float* colsum = nullptr;
   int rows_per_chunk = 0;
   ChunkPtrs chunks{};
+  SpTail tail{};  // only with the chunked store
 };
 
 struct DeviceCtx {
@@ -59,6 +71,10 @@ cudaError_t current_device_ctx(DeviceCtx* out);
 constexpr int kLnBwdMaxD = 16384;
 cudaError_t launch_reduce_scatter(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
 cudaError_t launch_gather_rows(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);
+// Dropout backward: dst [rows x d] (contiguous) = keep * in_chunks * drop_scale; with `partial`
+// (dropout_bwd_scratch_floats) also dbias2 [d] bf16 = the column sums of dst before rounding.
+cudaError_t launch_dropout_bwd(const RowParams& r, float* partial, void* dbias2, cudaStream_t s);
+size_t dropout_bwd_scratch_floats(int rows, int d);
 // out[c] = sum_r partial[r * cols + c] over r < rows, fixed order; bf16 or fp32 output.
 cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s);
 

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 
 #include "launch.h"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace tpmlp {
@@ -33,6 +34,33 @@ __device__ __forceinline__ const __nv_bfloat16* chunk_row(const RowParams& p, in
   const int j = row / p.rows_per_chunk;
   return static_cast<const __nv_bfloat16*>(p.in_chunks.p[j]) +
          static_cast<long long>(row - j * p.rows_per_chunk) * p.d;
+}
+
+__device__ __forceinline__ const __nv_bfloat16* add_chunk_row(const RowParams& p, int row) {
+  const int j = row / p.rows_per_chunk;
+  return static_cast<const __nv_bfloat16*>(p.add_chunks.p[j]) +
+         static_cast<long long>(row - j * p.rows_per_chunk) * p.d;
+}
+
+// The sequence-parallel tail on 8 elements of vector q (= element index / 8) of row `row`, column `col`.
+__device__ __forceinline__ void sp_tail_8(const RowParams& p, float (&a)[8], long long q, int row, int col) {
+  if (p.bias2 != nullptr) {
+    float b[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.bias2) + col)), b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[e] += b[e];
+  }
+  const uint32_t m = p.drop_thr < kKeepAll
+                         ? dropout_keep8(static_cast<unsigned long long>(q), p.drop_offset, p.drop_seed, p.drop_thr)
+                         : 0xFFu;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) a[e] = (m >> e) & 1u ? a[e] * p.drop_scale : 0.f;
+  if (p.add_chunks.p[0] != nullptr) {
+    float r[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(add_chunk_row(p, row) + col)), r);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[e] += r[e];
+  }
 }
 
 __device__ __forceinline__ __nv_bfloat16* out_chunk_row(const RowParams& p, int row) {
@@ -235,6 +263,12 @@ __global__ void __launch_bounds__(256) k_layernorm_bwd(const RowParams p) {
         unpack8(__ldg(g4 + v), g);
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = rstd * (dy[e] * g[e] - m1 - (f[e] - mean) * rstd * m2);
+        if (p.add_chunks.p[0] != nullptr) {
+          float a[8];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(add_chunk_row(p, row)) + v), a);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] += a[e];
+        }
         dx4[v] = pack8(o);
       }
       if (lane == 0) {
@@ -336,7 +370,8 @@ __device__ __forceinline__ void team_sync(int team, int tw) {
   }
 }
 
-template <int VT, int TW>
+// ADD: dx += the rows of p.add_chunks (the residual's gradient), loaded while the row statistics reduce.
+template <int VT, int TW, bool ADD = false>
 __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const RowParams p) {
   constexpr int kTeams = kStreamConsumers / TW;
   extern __shared__ uint8_t smem_raw[];
@@ -393,6 +428,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const
       }
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(empty + slot);
+      uint4 av[VT];
+      if constexpr (ADD) {
+        const uint4* a4 = reinterpret_cast<const uint4*>(add_chunk_row(p, blockIdx.x + i * gridDim.x));
+#pragma unroll
+        for (int k = 0; k < VT; ++k) av[k] = ok ? __ldg(a4 + j + k * 32 * TW) : make_uint4(0, 0, 0, 0);
+      }
       float s = 0.f;
 #pragma unroll
       for (int k = 0; k < VT; ++k) {
@@ -470,6 +511,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const
           dg[k][e] += dy[e] * xhat;
           db[k][e] += dy[e];
         }
+        if constexpr (ADD) {
+          float a[8];
+          unpack8(av[k], a);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] += a[e];
+        }
         dx4[j + k * 32 * TW] = pack8(o);
       }
     }
@@ -517,7 +564,52 @@ __global__ void __launch_bounds__(256) k_reduce_scatter(const RowParams p) {
     const long long el = i * 8;
     const int row = static_cast<int>(el / p.d);
     const int col = static_cast<int>(el - static_cast<long long>(row) * p.d);
+    if (p.tail) sp_tail_8(p, a, i, row, col);
     reinterpret_cast<uint4*>(out_chunk_row(p, row) + col)[0] = pack8(a);
+  }
+}
+
+// Dropout backward: dst[r] = keep * dY[r] * scale (gathered rows); per block of p.rows_per_block rows
+// the fp32 column sums of those values go to partial[blockIdx.y][d] for the row bias gradient.
+constexpr int kDropRows = 16;   // rows per block unless the grid's y extent (65535) needs more
+constexpr int kDropVecs = 256;  // 16-byte vectors per block row (2048 columns)
+
+__global__ void __launch_bounds__(kDropVecs) k_dropout_bwd(const RowParams p) {
+  const int nv = p.d / 8;
+  const int v = blockIdx.x * kDropVecs + threadIdx.x;
+  if (v >= nv) return;
+  const int r0 = blockIdx.y * p.rows_per_block;
+  const int r1 = min(p.rows, r0 + p.rows_per_block);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  uint4* dst = static_cast<uint4*>(p.dst);
+  for (int rb = r0; rb < r1; rb += 4) {
+    uint4 raw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      raw[u] = rb + u < r1 ? __ldg(reinterpret_cast<const uint4*>(chunk_row(p, rb + u)) + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (rb + u >= r1) break;
+      const long long q = static_cast<long long>(rb + u) * nv + v;
+      const uint32_t m = p.drop_thr < kKeepAll
+                             ? dropout_keep8(static_cast<unsigned long long>(q), p.drop_offset, p.drop_seed, p.drop_thr)
+                             : 0xFFu;
+      float f[8];
+      unpack8(raw[u], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        f[e] = (m >> e) & 1u ? f[e] * p.drop_scale : 0.f;
+        acc[e] += f[e];
+      }
+      dst[q] = pack8(f);
+    }
+  }
+  if (p.partial != nullptr) {
+    float4* out = reinterpret_cast<float4*>(p.partial + static_cast<long long>(blockIdx.y) * p.d + 8 * v);
+    out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
@@ -676,13 +768,24 @@ cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap
       const size_t team_sums = static_cast<size_t>(kStreamConsumers / ts.tw) * per_block * 4 + 128;
       if (smem < team_sums) smem = team_sums;
       cudaError_t e;
-      switch (r.d) {
-        case 256: e = launch_stream(k_layernorm_bwd_fused<1, 1>, r, smem, grid, s); break;
-        case 512: e = launch_stream(k_layernorm_bwd_fused<1, 2>, r, smem, grid, s); break;
-        case 1024: e = launch_stream(k_layernorm_bwd_fused<1, 4>, r, smem, grid, s); break;
-        case 2048: e = launch_stream(k_layernorm_bwd_fused<2, 4>, r, smem, grid, s); break;
-        case 4096: e = launch_stream(k_layernorm_bwd_fused<4, 4>, r, smem, grid, s); break;
-        default: e = launch_stream(k_layernorm_bwd_fused<4, 8>, r, smem, grid, s); break;
+      if (r.add_chunks.p[0] == nullptr) {
+        switch (r.d) {
+          case 256: e = launch_stream(k_layernorm_bwd_fused<1, 1>, r, smem, grid, s); break;
+          case 512: e = launch_stream(k_layernorm_bwd_fused<1, 2>, r, smem, grid, s); break;
+          case 1024: e = launch_stream(k_layernorm_bwd_fused<1, 4>, r, smem, grid, s); break;
+          case 2048: e = launch_stream(k_layernorm_bwd_fused<2, 4>, r, smem, grid, s); break;
+          case 4096: e = launch_stream(k_layernorm_bwd_fused<4, 4>, r, smem, grid, s); break;
+          default: e = launch_stream(k_layernorm_bwd_fused<4, 8>, r, smem, grid, s); break;
+        }
+      } else {
+        switch (r.d) {
+          case 256: e = launch_stream(k_layernorm_bwd_fused<1, 1, true>, r, smem, grid, s); break;
+          case 512: e = launch_stream(k_layernorm_bwd_fused<1, 2, true>, r, smem, grid, s); break;
+          case 1024: e = launch_stream(k_layernorm_bwd_fused<1, 4, true>, r, smem, grid, s); break;
+          case 2048: e = launch_stream(k_layernorm_bwd_fused<2, 4, true>, r, smem, grid, s); break;
+          case 4096: e = launch_stream(k_layernorm_bwd_fused<4, 4, true>, r, smem, grid, s); break;
+          default: e = launch_stream(k_layernorm_bwd_fused<4, 8, true>, r, smem, grid, s); break;
+        }
       }
       if (e != cudaSuccess) return e;
       k_column_sum<<<(2 * r.d + 31) / 32, 256, 0, s>>>(r.partial, grid, 2 * r.d, 2LL * r.d, dgamma, dbeta, r.d, 0);
@@ -710,6 +813,28 @@ cudaError_t launch_reduce_scatter(const RowParams& r, const DeviceCtx& ctx, cuda
   if (r.rows <= 0) return cudaSuccess;
   k_reduce_scatter<<<stream_grid(static_cast<long long>(r.rows) * r.d / 8, ctx.sm_count), 256, 0, s>>>(r);
   return cudaGetLastError();
+}
+
+int dropout_rows_per_block(int rows) {
+  const int need = (rows + 65534) / 65535;
+  return need <= kDropRows ? kDropRows : need;
+}
+
+size_t dropout_bwd_scratch_floats(int rows, int d) {
+  const int rpb = dropout_rows_per_block(rows);
+  return static_cast<size_t>((rows + rpb - 1) / rpb) * static_cast<size_t>(d);
+}
+
+cudaError_t launch_dropout_bwd(const RowParams& r, float* partial, void* dbias2, cudaStream_t s) {
+  if (r.rows <= 0) return cudaSuccess;
+  RowParams q = r;
+  q.partial = dbias2 != nullptr ? partial : nullptr;
+  q.rows_per_block = dropout_rows_per_block(r.rows);
+  const dim3 grid((r.d / 8 + kDropVecs - 1) / kDropVecs, (r.rows + q.rows_per_block - 1) / q.rows_per_block);
+  k_dropout_bwd<<<grid, kDropVecs, 0, s>>>(q);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || dbias2 == nullptr) return e;
+  return launch_column_sum(partial, static_cast<int>(grid.y), r.d, dbias2, true, s);
 }
 
 cudaError_t launch_gather_rows(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {

@@ -118,3 +118,58 @@ def test_empty_batch_needs_no_device(lib):
     s = binding.make_shape(0, 64, 256, 2)
     good = ctypes.c_void_p(1 << 20)
     assert L.tpmlp_forward(good, good, good, None, ctypes.byref(s), good, None, None, None, 0, None) == binding.OK
+
+
+def test_sp_region_workspace_sizes(lib):
+    for w in inputs.WORKLOADS.values():
+        if w.dtype != "bf16" or not w.sp:
+            continue
+        s = binding.make_shape(w.T, w.d, w.F, w.N)
+        dropcol = _r256(-(-w.T // 16) * w.d * 4)       # fp32 column partials, one row per 16 token rows
+        assert _ws(s, binding.OP_DROPOUT_BWD) == (binding.OK, dropcol)
+        st, spb = _ws(s, binding.OP_SP_BWD)
+        assert _ws(s, binding.OP_SP_BLOCK_BWD) == (binding.OK, spb + dropcol)
+    assert _ws(binding.make_shape(256, 64, 256, 2), 9)[0] == binding.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("p", [1.0, -0.25, float("nan"), float("inf")])
+def test_dropout_probability_outside_zero_one_rejected(lib, p):
+    L = binding.lib()
+    s = binding.make_shape(256, 64, 256, 2)
+    good = ctypes.c_void_p(1 << 20)
+    chunks = (ctypes.c_void_p * 2)(1 << 20, 1 << 21)
+    cp = ctypes.cast(chunks, binding._PP)
+    drop = ctypes.byref(binding.Dropout(p, 1, 2))
+    assert L.tpmlp_dropout_backward(cp, drop, ctypes.byref(s), good, None, None, 0, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_gemm2_bias_dropout_add(good, good, None, drop, None, ctypes.byref(s), cp, None) \
+        == binding.ERR_INVALID_ARG
+    assert L.tpmlp_reduce_scatter_bias_dropout_add(good, None, drop, None, ctypes.byref(s), cp, None) \
+        == binding.ERR_INVALID_ARG
+
+
+def test_sp_region_argument_checks(lib):
+    L = binding.lib()
+    s = binding.make_shape(256, 64, 256, 2)
+    good = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    chunks = (ctypes.c_void_p * 2)(1 << 20, 1 << 21)
+    cp = ctypes.cast(chunks, binding._PP)
+    bad_chunks = ctypes.cast((ctypes.c_void_p * 2)(1 << 20, None), binding._PP)
+    drop = ctypes.byref(binding.Dropout(0.1, 1, 2))
+    # misaligned row bias, a missing residual chunk
+    assert L.tpmlp_gemm2_bias_dropout_add(good, good, odd, drop, None, ctypes.byref(s), cp, None) \
+        == binding.ERR_INVALID_ARG
+    assert L.tpmlp_reduce_scatter_bias_dropout_add(good, None, drop, bad_chunks, ctypes.byref(s), cp, None) \
+        == binding.ERR_INVALID_ARG
+    # dbias2 wanted without a workspace
+    assert L.tpmlp_dropout_backward(cp, drop, ctypes.byref(s), good, good, None, 0, None) == binding.ERR_WORKSPACE
+    # the residual-gradient LayerNorm backward needs its residual chunks
+    assert L.tpmlp_layernorm_backward_add(cp, good, 1e-5, good, None, ctypes.byref(s), cp, good, good, good, 1 << 30,
+                                          None) == binding.ERR_INVALID_ARG
+    # empty batch: nothing launched, NULL pointers accepted
+    e = binding.make_shape(0, 64, 256, 2)
+    assert L.tpmlp_sp_block_forward(None, None, None, 1e-5, None, None, None, None, drop, ctypes.byref(e), None, 0,
+                                    None, None, None, None, 0, None) == binding.OK
+    assert L.tpmlp_sp_block_backward(None, None, None, 1e-5, None, None, None, drop, None, None, None, None,
+                                     ctypes.byref(e), None, None, None, None, None, None, None, None, 0, None) \
+        == binding.OK
