@@ -73,6 +73,21 @@ reason in the design notes):
   Here the normalised value is computed in float64 and then rounded to bf16
   (round to nearest, ties to even, 8 significant bits).
 
+* FP8 ([DEEP] section "FP8 하이브리드 정밀도 및 지연 스케일링(Delayed Scaling)"):
+  forward matmul operands in E4M3 (1 sign, 4 exponent bits, 3 mantissa
+  bits), each tensor multiplied by its scale factor ``S`` before the cast,
+  ``q = E4M3(x·S)``, and the product divided by both scales afterwards.
+  E4M3 is read as the OCP 8-bit format without infinities (bias 7, largest
+  finite value 448, subnormals down to 2**-9); the cast rounds to nearest,
+  ties to even, and saturates at ±448.  ``x·S`` is formed in float32, as the
+  GPU forms it.  Delayed scaling: the page predicts the next step's scale
+  from the moving average of the amaxes recorded in earlier steps; here the
+  average is the mean of a fixed-length amax history and ``S = 448 / mean``
+  (``2**-margin`` headroom optional; ``S = 1`` while the history is zero).
+  Which tensors run in FP8 in the forward: the gathered norm output, both
+  weights and the GeLU output ``H`` (the operands of the two GEMMs); the
+  bias and GeLU act on the dequantised fp32 product.
+
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` (values
 printed on the pages, closed forms, invariants, brute force, library
 witnesses and finite differences); none is parity-unpinned.
@@ -315,6 +330,80 @@ def sp_block_forward(X_chunks, gamma, beta, eps, A, B, b, b2, p, seed: int, offs
     for (lo, hi), xj, zj in zip(chunk_ranges(T, N), X_chunks, Z):
         keep = dropout_keep(hi - lo, d, lo, p, seed, offset)
         out.append(np.asarray(xj, dtype=np.float64) + np.where(keep, (zj + bias2) * scale, 0.0))
+    return out
+
+
+# --------------------------------------------------------------------------- FP8 (E4M3) forward with delayed scaling
+
+E4M3_MAX = 448.0
+
+
+def round_e4m3(x):
+    """Nearest E4M3 value, ties to even, magnitudes above 448 saturated to 448; returned as float64.
+
+    ``|x| = m·2**e`` with ``0.5 <= m < 1``; a normal E4M3 number ``1.fff·2**E`` has
+    quantum ``2**(E-3)`` with ``E = e - 1``; below ``2**-6`` the subnormals keep the
+    quantum ``2**-9``.  Rounding ``|x|/quantum`` half-to-even rounds the last mantissa
+    bit to even.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)
+    quantum = np.ldexp(1.0, np.maximum(e - 1, -6) - 3)
+    r = np.minimum(np.rint(a / quantum) * quantum, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def quantize_e4m3(x, scale):
+    """``E4M3(x·S)`` with the product formed in float32 (``x`` taken to float32 first)."""
+    return round_e4m3(np.asarray(x, dtype=np.float32) * np.float32(scale))
+
+
+def fp8_scale(amax_history, fp8_max: float = E4M3_MAX, margin: int = 0) -> float:
+    """Delayed scaling: ``S = fp8_max / mean(history) / 2**margin``; 1 while the mean is not positive."""
+    est = float(np.mean(np.asarray(amax_history, dtype=np.float64)))
+    if not est > 0.0 or not math.isfinite(est):
+        return 1.0
+    return fp8_max / est / 2.0 ** margin
+
+
+def roll_amax_history(amax_history, amax):
+    """The history after a step: the oldest entry drops out, this step's amax is appended."""
+    h = np.asarray(amax_history, dtype=np.float64)
+    return np.concatenate([h[1:], [float(amax)]])
+
+
+def mlp_fp8(X, A, B, b, N: int, scales):
+    """The MLP with E4M3 GEMM operands: ``scales = (S_X, S_A, S_B, S_H)``.
+
+    ``H = GeLU((q_X·q_A)/(S_X S_A) + b)``, ``Y = Σ_i (q_H,i·q_B,i)/(S_H S_B)`` over the
+    N row shards of the second layer (one shard sum, as :func:`mlp_tp`).  Also
+    returns the amaxes a step records: ``max|X|``, ``max|A|``, ``max|B|``,
+    ``max|H|`` (before the casts).
+    """
+    sx, sa, sb, sh = scales
+    X = np.asarray(X, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    qx, qa, qb = quantize_e4m3(X, sx), quantize_e4m3(A, sa), quantize_e4m3(B, sb)
+    H = gelu((qx @ qa) / (float(np.float32(sx)) * float(np.float32(sa))) + _bias_or_zero(b, A.shape[1]))
+    qh = quantize_e4m3(H, sh)
+    F = A.shape[1]
+    parts = [(qh[:, lo:hi] @ qb[lo:hi, :]) / (float(np.float32(sh)) * float(np.float32(sb)))
+             for lo, hi in shard_ranges(F, N)]
+    amax = {"X": float(np.max(np.abs(X), initial=0.0)), "A": float(np.max(np.abs(A), initial=0.0)),
+            "B": float(np.max(np.abs(B), initial=0.0)), "H": float(np.max(np.abs(H), initial=0.0))}
+    return {"Y": all_reduce(parts), "H": H, "qH": qh, "amax": amax}
+
+
+def sp_forward_fp8(X_chunks, gamma, beta, eps, A, B, b, N: int, scales):
+    """:func:`sp_forward` with the E4M3 GEMMs of :func:`mlp_fp8`: LayerNorm per chunk,
+    gather, the FP8 MLP, reduce-scatter of its row-shard partials."""
+    Xg = all_gather([layer_norm(c, gamma, beta, eps) for c in X_chunks])
+    out = mlp_fp8(Xg, A, B, b, N, scales)
+    T = Xg.shape[0]
+    out["Y_chunks"] = [out["Y"][lo:hi] for lo, hi in chunk_ranges(T, N)]
+    out["Xg"] = Xg
     return out
 
 

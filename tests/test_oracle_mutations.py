@@ -123,7 +123,28 @@ def _sp_block_backward_no_residual(X_chunks, gamma, beta, eps, A, B, b, p, seed,
     return g
 
 
+def _round_e4m3_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)
+    q = np.ldexp(1.0, np.maximum(e - 1, -6) - 3)
+    return np.copysign(np.minimum(np.floor(a / q + 0.5) * q, 448.0), x)
+
+
+def _fp8_scale_max(h, fp8_max=448.0, margin=0):
+    m = float(np.max(h))
+    return 1.0 if m <= 0 else fp8_max / m / 2.0 ** margin
+
+
+def _mlp_fp8_one_descale(X, A, B, b, N, scales):
+    sx, sa, sb, sh = scales
+    return _orig["mlp_fp8"](X, A, B, b, N, (sx, sa, sb * 2.0, sh))
+
+
 CASES = [
+    ("round_e4m3", _round_e4m3_ties_away, lambda: pins.test_round_e4m3_bruteforce_and_ties()),
+    ("fp8_scale", _fp8_scale_max, lambda: pins.test_fp8_delayed_scale_closed_forms()),
+    ("mlp_fp8", _mlp_fp8_one_descale, lambda: pins.test_mlp_fp8_torch_witness()),
     ("philox4x64", _philox_bump_first, lambda: pins.test_philox_matches_numpy_bit_generator()),
     ("dropout_keep", _dropout_keep_halves_swapped, lambda: pins.test_dropout_keep_bits_come_from_the_stated_block_and_half(0.5)),
     ("sp_block_forward", _sp_block_forward_unscaled, lambda: pins.test_sp_block_forward_torch_witness(2, 0.25)),

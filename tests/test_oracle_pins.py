@@ -500,3 +500,114 @@ def test_sp_block_backward_autograd_witness(N, p):
     assert rel(np.concatenate(g["dX_chunks"]), tt[0].grad.numpy()) < 1e-12
     for key, i in (("dgamma", 1), ("dbeta", 2), ("dA", 3), ("dB", 4), ("db", 5), ("db2", 6)):
         assert rel(g[key], tt[i].grad.numpy()) < 1e-12, key
+
+
+# --------------------------------------------------------------------------- E4M3 and the FP8 forward
+
+def _e4m3_table():
+    """Every finite E4M3 value with its code, decoded from the format's definition (bias 7, 3 mantissa bits,
+    exponent field 0 = subnormal, code S.1111.111 = NaN)."""
+    vals = []
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        ex, man = (code >> 3) & 0xF, code & 0x7
+        if ex == 0xF and man == 0x7:
+            continue
+        v = man / 8.0 * 2.0 ** -6 if ex == 0 else (1.0 + man / 8.0) * 2.0 ** (ex - 7)
+        vals.append((sign * v, code))
+    return vals
+
+
+def _e4m3_bruteforce(x):
+    if abs(x) > 448.0:
+        return math.copysign(448.0, x)
+    best = None
+    for v, code in _e4m3_table():
+        dist = abs(v - x)
+        if best is None or dist < best[0] or (dist == best[0] and (code & 1) == 0 and (best[1] & 1) == 1):
+            best = (dist, code, v)
+    return best[2]
+
+
+def test_round_e4m3_bruteforce_and_ties():
+    table = sorted({v for v, _ in _e4m3_table()})
+    assert len(table) == 253 and max(table) == 448.0 and min(v for v in table if v > 0) == 2.0 ** -9
+    rng = np.random.default_rng(21)
+    xs = list(rng.normal(size=300) * 10.0 ** rng.uniform(-3.5, 2.8, size=300))
+    pos = [v for v in table if v >= 0]
+    xs += [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]          # every midpoint: ties to even
+    xs += [-(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]
+    xs += [449.0, 465.0, 1e6, -1e6, 0.0, 2.0 ** -10, 3 * 2.0 ** -11]
+    got = oracle.round_e4m3(np.array(xs))
+    for x, g in zip(xs, got):
+        assert g == _e4m3_bruteforce(x), x
+
+
+def test_round_e4m3_torch_witness():
+    rng = np.random.default_rng(22)
+    x = (rng.normal(size=4000) * 10.0 ** rng.uniform(-3, 2.6, size=4000)).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_e4m3(x), ref)
+    q = oracle.quantize_e4m3(x, 0.75)
+    assert np.array_equal(q, torch.from_numpy(x * np.float32(0.75)).to(torch.float8_e4m3fn).to(torch.float64).numpy())
+
+
+def test_fp8_delayed_scale_closed_forms():
+    assert oracle.fp8_scale(np.full(16, 3.5)) == 448.0 / 3.5
+    assert oracle.fp8_scale(np.full(16, 3.5), margin=2) == 448.0 / 3.5 / 4
+    assert oracle.fp8_scale([1.0, 2.0, 3.0, 6.0]) == 448.0 / 3.0        # the mean, not the max
+    assert oracle.fp8_scale(np.zeros(8)) == 1.0
+    h = oracle.roll_amax_history([1.0, 2.0, 3.0], 7.0)
+    assert list(h) == [2.0, 3.0, 7.0]
+
+
+def test_mlp_fp8_is_exact_on_representable_inputs():
+    """Inputs on the E4M3 grid with power-of-two scales quantise to themselves, H = GeLU(...) does not, so
+    compare the first layer exactly and the whole block against the textbook MLP on the quantised H."""
+    rng = np.random.default_rng(23)
+    grid = np.array(sorted({v for v, _ in _e4m3_table() if abs(v) <= 4.0}))
+    T, d, F, N = 8, 16, 32, 4
+    X = rng.choice(grid, size=(T, d))
+    A = rng.choice(grid, size=(d, F)) / 8.0
+    B = rng.choice(grid, size=(F, d)) / 16.0
+    b = rng.choice(grid, size=F)
+    scales = (2.0, 8.0, 16.0, 4.0)
+    out = oracle.mlp_fp8(X, A, B, b, N, scales)
+    assert np.allclose(out["H"], oracle.gelu(X @ A + b), rtol=0, atol=1e-12)
+    assert np.allclose(out["Y"], out["qH"] @ B / 4.0, rtol=1e-13, atol=1e-13)
+    assert out["amax"]["A"] == np.max(np.abs(A)) and out["amax"]["H"] == np.max(np.abs(out["H"]))
+
+
+def test_mlp_fp8_torch_witness():
+    """The FP8 MLP against torch: float32 products, torch's float8_e4m3fn cast, float64 matmuls."""
+    T, d, F, N = 12, 16, 64, 4
+    X, A, B, b = _rand_block(T, d, F)
+    scales = (448.0 / np.max(np.abs(X)), 448.0 / np.max(np.abs(A)), 448.0 / np.max(np.abs(B)), 40.0)
+
+    def q(v, s):
+        return (torch.from_numpy(np.asarray(v, dtype=np.float32)) * torch.tensor(np.float32(s))).to(
+            torch.float8_e4m3fn).to(torch.float64)
+
+    f32 = lambda s: float(np.float32(s))
+    H = torch.nn.functional.gelu(q(X, scales[0]) @ q(A, scales[1]) / (f32(scales[0]) * f32(scales[1])) +
+                                 torch.from_numpy(b), approximate="none")
+    Y = q(H.numpy(), scales[3]) @ q(B, scales[2]) / (f32(scales[3]) * f32(scales[2]))
+    out = oracle.mlp_fp8(X, A, B, b, N, scales)
+    assert rel(out["H"], H.numpy()) < 1e-12
+    assert rel(out["Y"], Y.numpy()) < 1e-12
+    # and the quantisation error is of the format's size: a few 2**-4 relative steps, not more
+    assert 1e-3 < rel(out["Y"], oracle.mlp_reference(X, A, B, b)) < 0.1
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_sp_forward_fp8_is_mlp_fp8_on_the_gathered_norm(N):
+    T, d, F = 4 * N, 16, 64
+    X = RNG.normal(size=(T, d))
+    gam, bet = 1 + 0.1 * RNG.normal(size=d), 0.1 * RNG.normal(size=d)
+    _, A, B, b = _rand_block(1, d, F)
+    scales = (100.0, 2000.0, 2000.0, 50.0)
+    cr = oracle.chunk_ranges(T, N)
+    out = oracle.sp_forward_fp8([X[lo:hi] for lo, hi in cr], gam, bet, 1e-5, A, B, b, N, scales)
+    ref = oracle.mlp_fp8(oracle.layer_norm(X, gam, bet, 1e-5), A, B, b, N, scales)
+    assert np.array_equal(np.concatenate(out["Y_chunks"]), ref["Y"])
