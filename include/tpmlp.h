@@ -93,7 +93,8 @@ enum {
   TPMLP_OP_DH_GELUPRIME = 5,   /* tpmlp_gemm_dh_geluprime with a dbias output */
   TPMLP_OP_LN_BWD = 6,         /* tpmlp_layernorm_backward, tpmlp_layernorm_backward_add */
   TPMLP_OP_SP_BLOCK_BWD = 7,   /* tpmlp_sp_block_backward */
-  TPMLP_OP_DROPOUT_BWD = 8     /* tpmlp_dropout_backward with a dbias2 output */
+  TPMLP_OP_DROPOUT_BWD = 8,    /* tpmlp_dropout_backward with a dbias2 output */
+  TPMLP_OP_SP_FWD_FP8 = 9      /* tpmlp_sp_forward_fp8 */
 };
 
 /* Dropout of the sequence-parallel region.  The pages name Dropout in the
@@ -225,6 +226,80 @@ TPMLP_API tpmlp_status tpmlp_sp_block_backward(const void* const* X_chunks, cons
                                                const tpmlp_shape* shape, void* const* dX_chunks, void* dA, void* dB,
                                                void* dbias, void* dbias2, void* dgamma, void* dbeta,
                                                void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* ------------------------------------------------------------------ FP8 (E4M3) forward
+ * Deep-dive page, section "FP8 하이브리드 정밀도 및 지연 스케일링(Delayed Scaling)":
+ * forward matmul operands in E4M3, each tensor scaled by its factor S before
+ * the cast, q = E4M3(x S) (float32 product, round to nearest even, saturating
+ * at +-448: the OCP E4M3 format without infinities), and the GEMM's fp32
+ * accumulator divided by both scales.  Delayed scaling: the scales a step
+ * uses come from the amaxes of earlier steps (the mean of an amax history,
+ * the page's moving average); the step records its own amaxes for the next.
+ * Scales and amaxes are device memory, so a step needs no host round trip.
+ * E4M3 buffers are row-major bytes; d and F must be multiples of 16. */
+
+/* Delayed-scaling state of the FP8 forward, four tensors in the order
+ * X (the gathered norm output), A, B, H (the GeLU output):
+ *   scale[4]    the factors this step casts with (device, fp32),
+ *   amax[4]     this step's max |x| before the casts, max-combined by the
+ *               kernels (device, fp32; zero it before the first step),
+ *   history[4 x history_len]  earlier amaxes (device, fp32).
+ * tpmlp_fp8_update_scales ends a step: each history shifts by one and takes
+ * amax[i], scale[i] = 448 / mean(history[i]) / 2^margin (1 while the mean is
+ * not positive), amax[i] = 0. */
+typedef struct {
+  float* scale;
+  float* amax;
+  float* history;
+  int32_t history_len;
+  int32_t margin;
+} tpmlp_fp8_state;
+
+/* dst = E4M3(src * (*scale)); src [rows x cols] bf16 row-major, dst
+ * [rows x cols] bytes, or [cols x rows] with transpose != 0 (the K-major
+ * layout the FP8 GEMMs read for a weight stored [K x N]).  *amax is
+ * max-combined with max |src|.  rows, cols multiples of 16. */
+TPMLP_API tpmlp_status tpmlp_cast_e4m3(const void* src, int64_t rows, int64_t cols, int transpose, const float* scale,
+                                       void* dst, float* amax, tpmlp_stream_t stream);
+
+/* tpmlp_layernorm_gather writing E4M3(LN(x) * (*scale)) bytes into Xq
+ * [T x d]; *amax max-combined with max |LN(x)|.  d in {256, 512, 1024, 2048,
+ * 4096, 8192}. */
+TPMLP_API tpmlp_status tpmlp_layernorm_gather_e4m3(const void* const* X_chunks, const void* gamma, const void* beta,
+                                                   float eps, const tpmlp_shape* shape, const float* scale, void* Xq,
+                                                   float* amax, tpmlp_stream_t stream);
+
+/* Column-parallel GEMM on E4M3 operands: P = (Xq AqT^T) / (sx sa) + bias,
+ * Hq = E4M3(GeLU(P) * (*scale_h)), *amax_h max-combined with max |GeLU(P)|;
+ * Hpre (NULL or [T x F] bf16) = P.  Xq [T x d], AqT [F x d] (A transposed,
+ * from tpmlp_cast_e4m3), Hq [T x F] bytes. */
+TPMLP_API tpmlp_status tpmlp_gemm1_e4m3(const void* Xq, const void* AqT, const void* bias, const tpmlp_shape* shape,
+                                        const float* scale_x, const float* scale_a, const float* scale_h, void* Hq,
+                                        float* amax_h, void* Hpre, tpmlp_stream_t stream);
+
+/* Row-parallel GEMM on E4M3 operands with the in-kernel shard reduction:
+ * Y = sum_i (Hq_i BqT_i^T) / (sh sb) in bf16, into Y [T x d] or, with
+ * Y_chunks, into the N sequence chunks as tpmlp_gemm2_shard_accum.
+ * BqT [d x F] (B transposed). */
+TPMLP_API tpmlp_status tpmlp_gemm2_e4m3(const void* Hq, const void* BqT, const tpmlp_shape* shape,
+                                        const float* scale_h, const float* scale_b, void* Y, void* const* Y_chunks,
+                                        tpmlp_stream_t stream);
+
+/* End of an FP8 step: the delayed-scaling update of `state` (see
+ * tpmlp_fp8_state) for its four tensors. */
+TPMLP_API tpmlp_status tpmlp_fp8_update_scales(const tpmlp_fp8_state* state, tpmlp_stream_t stream);
+
+/* The sequence-parallel block forward with E4M3 GEMMs: the weights are cast
+ * (transposed) with scale[1], scale[2]; the LayerNorm writes E4M3 with
+ * scale[0]; GEMM1 dequantises, adds the bias, applies GeLU and casts H with
+ * scale[3]; GEMM2 reduces the shards in TMEM and stores bf16 Y chunks; then
+ * tpmlp_fp8_update_scales.  Workspace: size of TPMLP_OP_SP_FWD_FP8.  bf16
+ * X, gamma, beta, A, B, bias and Y as in tpmlp_sp_forward. */
+TPMLP_API tpmlp_status tpmlp_sp_forward_fp8(const void* const* X_chunks, const void* gamma, const void* beta,
+                                            float eps, const void* A, const void* B, const void* bias,
+                                            const tpmlp_fp8_state* state, const tpmlp_shape* shape,
+                                            void* const* Y_chunks, void* workspace, size_t workspace_bytes,
+                                            tpmlp_stream_t stream);
 
 /* ------------------------------------------------------------------ single steps (bf16)
  * Each step is one kernel launch (plus a small fixed-order reduction where

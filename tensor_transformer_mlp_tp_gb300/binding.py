@@ -20,7 +20,7 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
 BF16, FP32 = 0, 1
 (OP_FWD, OP_SP_FWD, OP_SP_FWD_PARTIALS, OP_BWD, OP_SP_BWD, OP_DH_GELUPRIME, OP_LN_BWD, OP_SP_BLOCK_BWD,
- OP_DROPOUT_BWD) = range(9)
+ OP_DROPOUT_BWD, OP_SP_FWD_FP8) = range(10)
 RS_FUSED, RS_PARTIALS = 0, 1
 
 
@@ -39,10 +39,16 @@ class Dropout(ctypes.Structure):
     _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
 
 
+class Fp8State(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_void_p), ("amax", ctypes.c_void_p), ("history", ctypes.c_void_p),
+                ("history_len", ctypes.c_int32), ("margin", ctypes.c_int32)]
+
+
 _P = ctypes.c_void_p
 _PP = ctypes.POINTER(ctypes.c_void_p)
 _SP = ctypes.POINTER(Shape)
 _DP = ctypes.POINTER(Dropout)
+_FP = ctypes.POINTER(Fp8State)
 _SIGS = {
     "tpmlp_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tpmlp_workspace_size": ([_SP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
@@ -76,6 +82,13 @@ _SIGS = {
     "tpmlp_dropout_backward": ([_PP, _DP, _SP, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_layernorm_backward_add": ([_PP, _P, ctypes.c_float, _P, _PP, _SP, _PP, _P, _P, _P, ctypes.c_size_t, _P],
                                      ctypes.c_int),
+    "tpmlp_cast_e4m3": ([_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P, _P, _P], ctypes.c_int),
+    "tpmlp_layernorm_gather_e4m3": ([_PP, _P, _P, ctypes.c_float, _SP, _P, _P, _P, _P], ctypes.c_int),
+    "tpmlp_gemm1_e4m3": ([_P, _P, _P, _SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "tpmlp_gemm2_e4m3": ([_P, _P, _SP, _P, _P, _P, _PP, _P], ctypes.c_int),
+    "tpmlp_fp8_update_scales": ([_FP, _P], ctypes.c_int),
+    "tpmlp_sp_forward_fp8": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _FP, _SP, _PP, _P, ctypes.c_size_t, _P],
+                             ctypes.c_int),
 }
 
 
@@ -373,6 +386,57 @@ def tpmlp_layernorm_backward_noalloc(X_chunks, gamma, dXg, N, dX_chunks, dgamma,
     dxp, _dxa = _ptrs(dX_chunks)
     _check("tpmlp_layernorm_backward_noalloc", lib().tpmlp_layernorm_backward_noalloc(
         xp, _ptr(gamma), eps, _ptr(dXg), ctypes.byref(shape), dxp, _ptr(dgamma), _ptr(dbeta), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3) forward
+
+def fp8_state(scale, amax, history, margin=0):
+    """A tpmlp_fp8_state over device fp32 tensors scale [4], amax [4], history [4 x L]."""
+    return Fp8State(scale.data_ptr(), amax.data_ptr(), history.data_ptr(), history.shape[-1], margin)
+
+
+def tpmlp_cast_e4m3(src, scale, dst, amax, transpose=False, stream=None):
+    rows, cols = src.shape
+    _check("tpmlp_cast_e4m3", lib().tpmlp_cast_e4m3(_ptr(src), rows, cols, 1 if transpose else 0, _ptr(scale),
+                                                    _ptr(dst), _ptr(amax), _stream(stream)))
+
+
+def tpmlp_layernorm_gather_e4m3(X_chunks, gamma, beta, N, scale, Xq, amax, eps=1e-5, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, 16 * N, N)  # ffn unused by this step
+    xp, _xa = _ptrs(X_chunks)
+    _check("tpmlp_layernorm_gather_e4m3", lib().tpmlp_layernorm_gather_e4m3(
+        xp, _ptr(gamma), _ptr(beta), eps, ctypes.byref(shape), _ptr(scale), _ptr(Xq), _ptr(amax), _stream(stream)))
+
+
+def tpmlp_gemm1_e4m3(Xq, AqT, bias, N, scale_x, scale_a, scale_h, Hq, amax_h, Hpre=None, stream=None):
+    shape = make_shape(Xq.shape[0], Xq.shape[1], AqT.shape[0], N)
+    _check("tpmlp_gemm1_e4m3", lib().tpmlp_gemm1_e4m3(
+        _ptr(Xq), _ptr(AqT), _ptr(bias), ctypes.byref(shape), _ptr(scale_x), _ptr(scale_a), _ptr(scale_h), _ptr(Hq),
+        _ptr(amax_h), _ptr(Hpre), _stream(stream)))
+
+
+def tpmlp_gemm2_e4m3(Hq, BqT, N, scale_h, scale_b, Y=None, Y_chunks=None, stream=None):
+    shape = make_shape(Hq.shape[0], BqT.shape[0], Hq.shape[1], N)
+    yp, _ya = _opt_ptrs(Y_chunks)
+    _check("tpmlp_gemm2_e4m3", lib().tpmlp_gemm2_e4m3(_ptr(Hq), _ptr(BqT), ctypes.byref(shape), _ptr(scale_h),
+                                                      _ptr(scale_b), _ptr(Y), yp, _stream(stream)))
+
+
+def tpmlp_fp8_update_scales(state, stream=None):
+    _check("tpmlp_fp8_update_scales", lib().tpmlp_fp8_update_scales(ctypes.byref(state), _stream(stream)))
+
+
+def tpmlp_sp_forward_fp8(X_chunks, gamma, beta, A, B, N, Y_chunks, state, bias=None, eps=1e-5, ws=None, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, A.shape[1], N)
+    ws = workspace(shape, OP_SP_FWD_FP8, A.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    yp, _ya = _ptrs(Y_chunks)
+    _check("tpmlp_sp_forward_fp8", lib().tpmlp_sp_forward_fp8(
+        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), ctypes.byref(state), ctypes.byref(shape), yp,
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return Y_chunks
 
 
 def tpmlp_selftest_wait_timeout(budget_us: int, stream=None):

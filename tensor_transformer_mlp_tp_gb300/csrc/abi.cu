@@ -123,7 +123,7 @@ bool chunks_ok(const void* const* c, int n) {
 
 // Sizes of the workspace regions (bytes, each 256-aligned).
 struct Sizes {
-  size_t td, tf, ptd, colsum, lnbwd, dropcol;
+  size_t td, tf, ptd, colsum, lnbwd, dropcol, td8, tf8, df8;
 };
 
 
@@ -138,6 +138,9 @@ Sizes sizes_of(const tpmlp_shape* s) {
   z.colsum = align_up(4 * m_blocks * F * 4);
   z.lnbwd = align_up(layernorm_bwd_scratch_floats(static_cast<int>(T), static_cast<int>(d)) * 4);
   z.dropcol = align_up(dropout_bwd_scratch_floats(static_cast<int>(T), static_cast<int>(d)) * 4);
+  z.td8 = align_up(T * d);
+  z.tf8 = align_up(T * F);
+  z.df8 = align_up(d * F);
   return z;
 }
 
@@ -153,6 +156,7 @@ size_t ws_bytes(const tpmlp_shape* s, int op) {
     case TPMLP_OP_LN_BWD: return z.lnbwd;
     case TPMLP_OP_SP_BLOCK_BWD: return 3 * z.tf + z.colsum + 3 * z.td + z.lnbwd + z.dropcol;
     case TPMLP_OP_DROPOUT_BWD: return z.dropcol;
+    case TPMLP_OP_SP_FWD_FP8: return 2 * z.df8 + z.td8 + z.tf8;
     default: return 0;
   }
 }
@@ -388,6 +392,79 @@ cudaError_t do_dropout_bwd(const void* const* dY_chunks, const SpTail& t, const 
   return launch_dropout_bwd(r, partial, dbias2, st);
 }
 
+// FP8 shape rule on top of check_shape: byte rows of E4M3 tensors are multiples of 16 bytes.
+tpmlp_status check_fp8(const tpmlp_shape* s) {
+  return s->d % 16 == 0 && s->ffn % 16 == 0 ? TPMLP_OK : TPMLP_ERR_INVALID_ARG;
+}
+
+bool fp8_ln_width(int64_t d) { return d == 256 || d == 512 || d == 1024 || d == 2048 || d == 4096 || d == 8192; }
+
+cudaError_t do_ln_e4m3(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                       const tpmlp_shape* s, const float* scale, void* Xq, float* amax, cudaStream_t st) {
+  RowParams r{};
+  r.in_chunks = to_const_chunks(X_chunks, s->n_shards);
+  r.rows = static_cast<int>(s->tokens);
+  r.d = static_cast<int>(s->d);
+  r.n_chunks = s->n_shards;
+  r.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
+  r.eps = eps;
+  r.gamma = gamma;
+  r.beta = beta;
+  r.dst = Xq;
+  return launch_layernorm_fwd_e4m3(r, scale, amax, st);
+}
+
+cudaError_t do_gemm1_e4m3(const DeviceCtx& c, const void* Xq, const void* AqT, const void* bias, const tpmlp_shape* s,
+                          const float* sx, const float* sa, const float* sh, void* Hq, float* amax_h, void* Hpre,
+                          cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->ffn);
+  g.K = static_cast<int>(s->d);
+  g.a = {Xq, s->d, false};
+  g.b = {AqT, s->d, false};
+  g.epi = kEpiBiasGeluQ;
+  g.fp8 = true;
+  g.scale_a = sx;
+  g.scale_b = sa;
+  g.scale_out = sh;
+  g.amax_out = amax_h;
+  g.out0 = Hq;
+  g.ld0 = s->ffn;
+  g.out1 = Hpre;
+  g.ld1 = s->ffn;
+  g.bias = bias;
+  return launch_gemm(g, c, st);
+}
+
+cudaError_t do_gemm2_e4m3(const DeviceCtx& c, const void* Hq, const void* BqT, const tpmlp_shape* s, const float* sh,
+                          const float* sb, void* Y, void* const* Y_chunks, cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->d);
+  g.K = static_cast<int>(s->ffn);
+  g.a = {Hq, s->ffn, false};
+  g.b = {BqT, s->ffn, false};
+  g.epi = kEpiStore;
+  g.fp8 = true;
+  g.scale_a = sh;
+  g.scale_b = sb;
+  g.out0 = Y;
+  g.ld0 = s->d;
+  if (Y_chunks != nullptr) {
+    g.rows_per_chunk = static_cast<int>(s->tokens / s->n_shards);
+    g.chunks = to_chunks(Y_chunks, s->n_shards);
+  }
+  return launch_gemm(g, c, st);
+}
+
+bool fp8_state_ok(const tpmlp_fp8_state* f) {
+  return f != nullptr && f->scale != nullptr && f->amax != nullptr && f->history != nullptr &&
+         f->history_len >= 1 && f->history_len <= (1 << 20) && f->margin >= 0 && f->margin <= 64 &&
+         (reinterpret_cast<uintptr_t>(f->scale) & 3u) == 0 && (reinterpret_cast<uintptr_t>(f->amax) & 3u) == 0 &&
+         (reinterpret_cast<uintptr_t>(f->history) & 3u) == 0;
+}
+
 // Backward core shared by tpmlp_backward and tpmlp_sp_backward.  With Hpre
 // and H from the forward only the four backward GEMMs run; without Hpre, one
 // GEMM1 recomputes both.
@@ -438,12 +515,14 @@ const char* tpmlp_status_string(tpmlp_status s) {
 tpmlp_status tpmlp_workspace_size(const tpmlp_shape* shape, int op, size_t* bytes) {
   if (bytes == nullptr) return TPMLP_ERR_INVALID_ARG;
   const bool sp = op == TPMLP_OP_SP_FWD || op == TPMLP_OP_SP_FWD_PARTIALS || op == TPMLP_OP_SP_BWD ||
-                  op == TPMLP_OP_LN_BWD || op == TPMLP_OP_SP_BLOCK_BWD || op == TPMLP_OP_DROPOUT_BWD;
+                  op == TPMLP_OP_LN_BWD || op == TPMLP_OP_SP_BLOCK_BWD || op == TPMLP_OP_DROPOUT_BWD ||
+                  op == TPMLP_OP_SP_FWD_FP8;
   const bool bf16_only = op != TPMLP_OP_FWD;
   tpmlp_status st = check_shape(shape, sp, bf16_only);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (op < TPMLP_OP_FWD || op > TPMLP_OP_DROPOUT_BWD) return TPMLP_ERR_INVALID_ARG;
+  if (op < TPMLP_OP_FWD || op > TPMLP_OP_SP_FWD_FP8) return TPMLP_ERR_INVALID_ARG;
+  if (op == TPMLP_OP_SP_FWD_FP8 && (shape->d % 16 != 0 || shape->ffn % 16 != 0)) return TPMLP_ERR_INVALID_ARG;
   *bytes = ws_bytes(shape, op);
   return TPMLP_OK;
 }
@@ -877,6 +956,108 @@ tpmlp_status tpmlp_layernorm_backward_add(const void* const* X_chunks, const voi
   if ((st = device_ctx(&c)) != TPMLP_OK) return st;
   return cuda_status(do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta,
                                static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream), R_chunks));
+}
+
+// ------------------------------------------------------------------ FP8 forward
+
+tpmlp_status tpmlp_cast_e4m3(const void* src, int64_t rows, int64_t cols, int transpose, const float* scale, void* dst,
+                             float* amax, tpmlp_stream_t stream) {
+  if (rows < 0 || cols < 0 || rows % 16 != 0 || cols % 16 != 0 || rows > INT_MAX / 2 || cols > INT_MAX / 2)
+    return TPMLP_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return TPMLP_OK;
+  if (!ptrs_ok({src, dst}) || scale == nullptr || amax == nullptr) return TPMLP_ERR_INVALID_ARG;
+  if (transpose && (rows + 63) / 64 > 65535) return TPMLP_ERR_UNSUPPORTED;
+  return cuda_status(launch_cast_e4m3(src, static_cast<int>(rows), static_cast<int>(cols), transpose != 0, scale, dst,
+                                      amax, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_layernorm_gather_e4m3(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                         const tpmlp_shape* shape, const float* scale, void* Xq, float* amax,
+                                         tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if ((st = check_fp8(shape)) != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({gamma, beta, Xq}) || !chunks_ok(X_chunks, shape->n_shards) || !(eps >= 0.f) || scale == nullptr ||
+      amax == nullptr)
+    return TPMLP_ERR_INVALID_ARG;
+  if (!fp8_ln_width(shape->d)) return TPMLP_ERR_UNSUPPORTED;
+  return cuda_status(do_ln_e4m3(X_chunks, gamma, beta, eps, shape, scale, Xq, amax,
+                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm1_e4m3(const void* Xq, const void* AqT, const void* bias, const tpmlp_shape* shape,
+                              const float* scale_x, const float* scale_a, const float* scale_h, void* Hq,
+                              float* amax_h, void* Hpre, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if ((st = check_fp8(shape)) != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({Xq, AqT, Hq}) || !opt_ok(bias) || !opt_ok(Hpre) || scale_x == nullptr || scale_a == nullptr ||
+      scale_h == nullptr)
+    return TPMLP_ERR_INVALID_ARG;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_gemm1_e4m3(c, Xq, AqT, bias, shape, scale_x, scale_a, scale_h, Hq, amax_h, Hpre,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm2_e4m3(const void* Hq, const void* BqT, const tpmlp_shape* shape, const float* scale_h,
+                              const float* scale_b, void* Y, void* const* Y_chunks, tpmlp_stream_t stream) {
+  const bool chunked = Y_chunks != nullptr;
+  tpmlp_status st = check_shape(shape, chunked, true);
+  if (st != TPMLP_OK) return st;
+  if ((st = check_fp8(shape)) != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({Hq, BqT}) || scale_h == nullptr || scale_b == nullptr) return TPMLP_ERR_INVALID_ARG;
+  if (chunked ? !chunks_ok(Y_chunks, shape->n_shards) : !ptrs_ok({Y})) return TPMLP_ERR_INVALID_ARG;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_gemm2_e4m3(c, Hq, BqT, shape, scale_h, scale_b, Y, Y_chunks,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_fp8_update_scales(const tpmlp_fp8_state* state, tpmlp_stream_t stream) {
+  if (!fp8_state_ok(state)) return TPMLP_ERR_INVALID_ARG;
+  return cuda_status(launch_fp8_update(state->scale, state->amax, state->history, 4, state->history_len, 448.f,
+                                       state->margin, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_sp_forward_fp8(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
+                                  const void* A, const void* B, const void* bias, const tpmlp_fp8_state* state,
+                                  const tpmlp_shape* shape, void* const* Y_chunks, void* workspace,
+                                  size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if ((st = check_fp8(shape)) != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !chunks_ok(X_chunks, shape->n_shards) ||
+      !chunks_ok(Y_chunks, shape->n_shards) || !(eps >= 0.f) || !fp8_state_ok(state))
+    return TPMLP_ERR_INVALID_ARG;
+  if (!fp8_ln_width(shape->d) || (shape->ffn + 63) / 64 > 65535 || (shape->d + 63) / 64 > 65535)
+    return TPMLP_ERR_UNSUPPORTED;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_SP_FWD_FP8))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Sizes z = sizes_of(shape);
+  Carve ws(workspace);
+  void* AqT = ws.take(z.df8);
+  void* BqT = ws.take(z.df8);
+  void* Xq = ws.take(z.td8);
+  void* Hq = ws.take(z.tf8);
+  float* sc = state->scale;
+  float* am = state->amax;
+  const int d = static_cast<int>(shape->d), F = static_cast<int>(shape->ffn);
+  cudaError_t e = launch_cast_e4m3(A, d, F, true, sc + 1, AqT, am + 1, s);
+  if (e == cudaSuccess) e = launch_cast_e4m3(B, F, d, true, sc + 2, BqT, am + 2, s);
+  if (e == cudaSuccess) e = do_ln_e4m3(X_chunks, gamma, beta, eps, shape, sc + 0, Xq, am + 0, s);
+  if (e == cudaSuccess) e = do_gemm1_e4m3(c, Xq, AqT, bias, shape, sc + 0, sc + 1, sc + 3, Hq, am + 3, nullptr, s);
+  if (e == cudaSuccess) e = do_gemm2_e4m3(c, Hq, BqT, shape, sc + 3, sc + 2, nullptr, Y_chunks, s);
+  if (e == cudaSuccess)
+    e = launch_fp8_update(state->scale, state->amax, state->history, 4, state->history_len, 448.f, state->margin, s);
+  return cuda_status(e);
 }
 
 }  // extern "C"

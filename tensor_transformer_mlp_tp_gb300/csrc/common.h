@@ -34,6 +34,8 @@ enum Epilogue : int {
   kEpiBias = 1,       // out0 = bf16(acc + bias)
   kEpiStore = 2,      // out0 = bf16(acc), optional row -> chunk remap, optional per-shard partials
   kEpiDGelu = 3,      // out0 = bf16(acc * GeLU'(aux)); out1 = bf16(GeLU(aux)); optional column sums
+  kEpiBiasGeluQ = 4,  // out0 = E4M3(GeLU(acc + bias) * scale_out), amax_out = max |GeLU(acc + bias)|;
+                      // out1 (optional) = bf16(acc + bias)
 };
 
 struct ChunkPtrs {
@@ -73,6 +75,12 @@ struct GemmParams {
   float drop_scale;
   unsigned long long drop_seed, drop_offset, drop_thr;  // drop_thr = 2^32 keeps every element
   ConstChunkPtrs res_chunks;
+  // FP8 operands: the accumulator is divided by (*scale_a) (*scale_b); kEpiBiasGeluQ quantises with
+  // *scale_out and max-combines its amax into *amax_out.
+  const float* scale_a;
+  const float* scale_b;
+  const float* scale_out;
+  float* amax_out;
   unsigned int* err;
   unsigned long long timeout_ns;
 };
@@ -102,6 +110,8 @@ struct RowParams {
   ConstChunkPtrs add_chunks;  // N chunk pointers [rows_per_chunk x d] bf16, or p[0] == nullptr
   float drop_scale;
   unsigned long long drop_seed, drop_offset, drop_thr;
+  const float* qscale;        // E4M3 outputs: quantisation scale (device), and the amax they max-combine into
+  float* amax;
   unsigned int* err;          // device error words
   unsigned long long timeout_ns;
 };

@@ -32,17 +32,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major matrix of `outer` rows of `inner`
-// elements (`ld` elements apart), 128-byte swizzle, zero fill out of bounds.
+// 2-D tensor map over a row-major matrix of `outer` rows of `inner` elements
+// (`ld` elements apart; bf16, or bytes for E4M3), 128-byte swizzle, zero fill out of bounds.
 bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long ld, int box_inner,
-              int box_outer) {
+              int box_outer, bool bytes = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (bytes ? 1 : 2)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+            dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -78,10 +79,10 @@ int max_pairs(K kern, int smem, int threads, int dev_cache_slot, int* cache) {
   return n;
 }
 
-template <bool AMN, bool BMN, int EPI>
+template <bool AMN, bool BMN, int EPI, bool FP8 = false>
 cudaError_t run_pair(const GemmParams& p, cudaStream_t s) {
   using S = PairShape<kBN, kPairStages, kEpiWarps>;
-  auto kern = k_gemm_tc2<kBN, AMN, BMN, EPI, kPairStages, kEpiWarps>;
+  auto kern = k_gemm_tc2<kBN, AMN, BMN, EPI, kPairStages, kEpiWarps, FP8>;
   static int cache[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -116,8 +117,56 @@ bool pair_enabled() {
 
 }  // namespace
 
+// E4M3 GEMMs: always the CTA pair (a lone 128-row block leaves the odd CTA's rows to zero fill), both
+// operands K-major, 128-element k-blocks.
+static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s) {
+  if (g.a.mn_major || g.b.mn_major || g.shards > 1) return cudaErrorNotSupported;
+  if (g.scale_a == nullptr || g.scale_b == nullptr) return cudaErrorInvalidValue;
+  if (g.epi == kEpiBiasGeluQ && g.scale_out == nullptr) return cudaErrorInvalidValue;
+  constexpr int kKb = 128;
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  bool ok = make_map(&p.tmA, g.a.ptr, g.K, g.M, g.a.ld, kKb, kBM, true) &&
+            make_map(&p.tmB, g.b.ptr, g.K, g.N, g.b.ld, kKb, kBN / 2, true);
+  if (!ok) return cudaErrorInvalidValue;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.m_blocks = (g.M + 2 * kBM - 1) / (2 * kBM);
+  p.n_blocks = (g.N + kBN - 1) / kBN;
+  p.shards = 1;
+  p.k_blocks_per_shard = (g.K + kKb - 1) / kKb;
+  p.group_m = kGroupM / 2;
+  p.out0 = g.out0;
+  p.ld0 = g.ld0;
+  p.out1 = g.out1;
+  p.ld1 = g.ld1;
+  p.bias = g.bias;
+  p.rows_per_chunk = g.rows_per_chunk;
+  p.chunks = g.chunks;
+  p.tail = g.tail.on && g.rows_per_chunk > 0 && g.epi == kEpiStore ? 1 : 0;
+  if (p.tail) p.bias = g.tail.bias2;
+  p.drop_scale = g.tail.scale;
+  p.drop_seed = g.tail.seed;
+  p.drop_offset = g.tail.offset;
+  p.drop_thr = g.tail.thr;
+  p.res_chunks = g.tail.residual;
+  p.scale_a = g.scale_a;
+  p.scale_b = g.scale_b;
+  p.scale_out = g.scale_out;
+  p.amax_out = g.amax_out;
+  p.err = ctx.err;
+  p.timeout_ns = ctx.timeout_ns;
+  switch (g.epi) {
+    case kEpiBiasGeluQ: return run_pair<false, false, kEpiBiasGeluQ, true>(p, s);
+    case kEpiStore: return run_pair<false, false, kEpiStore, true>(p, s);
+    default: return cudaErrorNotSupported;
+  }
+}
+
 cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return cudaSuccess;
+  if (g.fp8) return launch_gemm_fp8(g, ctx, s);
   GemmParams p;
   memset(&p, 0, sizeof(p));
   // A operand (the M side): box of 128 rows x 64 k (K-major) or 64 m x 64 k rows (MN-major).

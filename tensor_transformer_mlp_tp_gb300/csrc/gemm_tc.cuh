@@ -24,6 +24,7 @@
 // releases its TMEM before exiting.
 #pragma once
 
+#include "fp8.cuh"
 #include "philox.cuh"
 #include "ptx.cuh"
 
@@ -115,6 +116,26 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], uint32_t lane)
   return v[0];
 }
 
+// Per-thread epilogue state: the FP8 dequantisation factor, the output scale and the running amax.
+struct EpiState {
+  float descale;
+  float scale_out;
+  float amax;
+};
+
+// E4M3(x * s) for 32 values -> 32 bytes of one row (columns at or beyond N, a multiple of 16, skipped).
+__device__ __forceinline__ void store_row32_e4m3(uint8_t* row_ptr, int col0, int N, const float (&x)[32], float s) {
+  uint4* d = reinterpret_cast<uint4*>(row_ptr + col0);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    if (col0 + 16 * g < N) {
+      const float* y = x + 16 * g;
+      d[g] = make_uint4(e4m3x4(y[0], y[1], y[2], y[3], s), e4m3x4(y[4], y[5], y[6], y[7], s),
+                        e4m3x4(y[8], y[9], y[10], y[11], s), e4m3x4(y[12], y[13], y[14], y[15], s));
+    }
+  }
+}
+
 // The sequence-parallel tail on 32 columns of one output row:
 // v = res + keep * (v + bias2) * scale, res from the residual chunk of the row.
 __device__ __forceinline__ void sp_tail_32(const GemmParams& p, float (&v)[32], int row, int col0) {
@@ -149,9 +170,31 @@ __device__ __forceinline__ void sp_tail_32(const GemmParams& p, float (&v)[32], 
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32], const uint4 (&aux_raw)[4], int row,
-                                            int col0, int shard, int mb, int quad, uint32_t lane) {
+                                            int col0, int shard, int mb, int quad, uint32_t lane, EpiState& st) {
   const bool row_ok = row < p.M;
-  if constexpr (EPI == kEpiBiasGelu || EPI == kEpiBias) {
+  if (st.descale != 1.f) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= st.descale;
+  }
+  if constexpr (EPI == kEpiBiasGeluQ) {
+    if (p.bias != nullptr) {
+      float b[32];
+      load_row32(static_cast<const __nv_bfloat16*>(p.bias), col0, p.N, b);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += b[i];
+    }
+    if (row_ok) {
+      if (p.out1 != nullptr)
+        store_row32(static_cast<__nv_bfloat16*>(p.out1) + static_cast<long long>(row) * p.ld1, col0, p.N, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = gelu_f(v[i]);
+        if (col0 + i < p.N) st.amax = fmaxf(st.amax, fabsf(v[i]));
+      }
+      store_row32_e4m3(static_cast<uint8_t*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v,
+                       st.scale_out);
+    }
+  } else if constexpr (EPI == kEpiBiasGelu || EPI == kEpiBias) {
     if (p.bias != nullptr) {
       float b[32];
       load_row32(static_cast<const __nv_bfloat16*>(p.bias), col0, p.N, b);
@@ -353,6 +396,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc(const __grid
     constexpr int kSplit = EPI_WARPS / 4;           // warps sharing a quadrant split the columns
     constexpr int kColsPerPart = BN / kSplit;
     const int part = ew / 4;
+    EpiState est{1.f, 1.f, 0.f};  // the single-CTA kernel runs bf16 operands only
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       int shard, mb, nb;
@@ -393,7 +437,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1) k_gemm_tc(const __grid
         }
         float v[32];
         tmem_load_32cols(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + c), v);
-        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb, quad, lane);
+        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb, quad, lane, est);
       }
       tc_fence_before_sync();
       __syncwarp();

@@ -47,8 +47,13 @@ struct PairShape {
   static_assert(EPI_WARPS == 4, "one epilogue warp per TMEM lane quadrant");
 };
 
-template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS>
+// FP8: E4M3 A and B (both K-major), .kind::f8f6f4; a 128-byte k-block row then holds 128 elements and
+// one UMMA covers 32 of them, so shared-memory layouts, descriptors and byte counts are those of bf16.
+template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS, bool FP8 = false>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __grid_constant__ GemmParams p) {
+  static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
+  static_assert(FP8 || EPI != kEpiBiasGeluQ, "the quantising epilogue follows FP8 operands");
+  constexpr int kKElems = FP8 ? 128 : kBK;  // elements of one 128-byte k-block row
   using S = PairShape<BN, STAGES, EPI_WARPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
           }
           if (leader) mbar_arrive_expect_tx(full + stage, 2 * S::kStage);
           const uint32_t bar = mapa_shared(smem_u32(full + stage), 0);
-          const int k0 = (kb0 + kb) * kBK;
+          const int k0 = (kb0 + kb) * kKElems;
           uint8_t* a_dst = sA + stage * S::kATile;
           uint8_t* b_dst = sB + stage * S::kBTile;
           if constexpr (!A_MN) {
@@ -163,7 +168,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------------ MMA issuer (even CTA)
-      constexpr uint32_t idesc = idesc_bf16_f32(256, BN, A_MN, B_MN);
+      constexpr uint32_t idesc = FP8 ? idesc_f8_f32(256, BN, kFmtE4M3, kFmtE4M3, false, false)
+                                     : idesc_bf16_f32(256, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -188,7 +194,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
                                      : sdesc_sw128(a_base + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b_base + k * 2048, 64 * kBK * 2, 1024)
                                      : sdesc_sw128(b_base + k * 32, 16, 1024);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (FP8) {
+              umma_f8_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            } else {
+              umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair_multicast(empty + stage, 0x3);
           if (++stage == STAGES) {
@@ -209,6 +219,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
     const bool reader = quad_warp && quad < 2;             // copies TMEM -> staging only
     const bool helper = !quad_warp;                        // epilogue math on staged rows
     float* stage_base = staging + quad * (2 * 32 * 32);    // valid for quadrants 0 and 1
+    EpiState est{1.f, 1.f, 0.f};
+    if constexpr (FP8) est.descale = 1.f / (__ldg(p.scale_a) * __ldg(p.scale_b));
+    if constexpr (EPI == kEpiBiasGeluQ) est.scale_out = __ldg(p.scale_out);
     uint32_t chunk_ctr = 0;
     int local = 0;
     bool ok_all = true;
@@ -293,13 +306,16 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
         } else {
           tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
         }
-        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane);
+        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est);
       }
       if (!helper && ok_all) {
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
       }
+    }
+    if constexpr (EPI == kEpiBiasGeluQ) {
+      if (p.amax_out != nullptr) amax_combine_warp(p.amax_out, est.amax);
     }
   }
 

@@ -44,6 +44,12 @@ struct GemmLaunch {
   int rows_per_chunk = 0;
   ChunkPtrs chunks{};
   SpTail tail{};  // only with the chunked store
+  // E4M3 operands (both K-major, row strides multiples of 16 bytes): dequantised by the two scales
+  bool fp8 = false;
+  const float* scale_a = nullptr;
+  const float* scale_b = nullptr;
+  const float* scale_out = nullptr;  // kEpiBiasGeluQ
+  float* amax_out = nullptr;         // kEpiBiasGeluQ
 };
 
 struct DeviceCtx {
@@ -77,6 +83,18 @@ cudaError_t launch_dropout_bwd(const RowParams& r, float* partial, void* dbias2,
 size_t dropout_bwd_scratch_floats(int rows, int d);
 // out[c] = sum_r partial[r * cols + c] over r < rows, fixed order; bf16 or fp32 output.
 cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s);
+
+// E4M3 casts.  dst = E4M3(src * (*scale)) for src [rows x cols] bf16 (row-major), written [rows x cols]
+// or, with `transpose`, [cols x rows]; *amax is max-combined with max |src|.  Row lengths multiples of 16.
+cudaError_t launch_cast_e4m3(const void* src, int rows, int cols, bool transpose, const float* scale, void* dst,
+                             float* amax, cudaStream_t s);
+// LayerNorm of every chunk, written as E4M3(LN(x) * (*scale)) into the gathered [T x d] byte buffer
+// r.dst; *amax max-combined with max |LN(x)|.
+cudaError_t launch_layernorm_fwd_e4m3(const RowParams& r, const float* scale, float* amax, cudaStream_t s);
+// Delayed scaling: for each of n tensors, history[i][0..len) shifts by one and takes amax[i];
+// scale[i] = fp8_max / mean(history[i]) / 2^margin (1 while the mean is not positive); amax[i] = 0.
+cudaError_t launch_fp8_update(float* scale, float* amax, float* history, int n, int len, float fp8_max, int margin,
+                              cudaStream_t s);
 
 cudaError_t launch_mlp_fp32(const float* X, const float* A, const float* B, const float* bias, int T, int d, int F,
                             float* H, float* Y, cudaStream_t s);

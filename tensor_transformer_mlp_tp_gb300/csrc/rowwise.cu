@@ -7,6 +7,7 @@
 // All global traffic is 16-byte vectors; reductions are warp shuffles.
 #include <cuda_bf16.h>
 
+#include "fp8.cuh"
 #include "launch.h"
 #include "philox.cuh"
 #include "ptx.cuh"
@@ -93,7 +94,9 @@ __device__ __forceinline__ float row_sum(float v, float* red, int warp) {
 
 // RMS = true: the norm of the SequenceParallelLayerNorm listing instead:
 // rstd = rsqrt(mean(x^2) + eps), n = bf16(x rstd), y = bf16(n * gamma).
-template <int V, int WPR, bool RMS = false>
+// Q8 = true: the fp32 LayerNorm value y is written as E4M3(y * (*p.qscale)) (one byte) and max |y| is
+// max-combined into *p.amax.
+template <int V, int WPR, bool RMS = false, bool Q8 = false>
 __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
   __shared__ float red[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,27 +131,39 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
     }
   }
   const float rstd = rsqrtf(row_sum<V, WPR>(q, red, warp) / static_cast<float>(p.d) + p.eps);
-  if (!valid) return;
   const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
   const uint4* b4 = reinterpret_cast<const uint4*>(p.beta);
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + static_cast<long long>(row) * p.d);
+  const long long row_off = static_cast<long long>(valid ? row : 0) * p.d;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + row_off);
+  uint2* dst8 = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.dst) + row_off);
+  float qs = 1.f, amax = 0.f;
+  if constexpr (Q8) qs = __ldg(p.qscale);
+  if (valid) {
 #pragma unroll
-  for (int v = 0; v < V; ++v) {
-    const int idx = (sub * V + v) * 32 + lane;
-    float f[8], g[8], o[8];
-    unpack8(x[v], f);
-    unpack8(__ldg(g4 + idx), g);
-    if constexpr (RMS) {
+    for (int v = 0; v < V; ++v) {
+      const int idx = (sub * V + v) * 32 + lane;
+      float f[8], g[8], o[8];
+      unpack8(x[v], f);
+      unpack8(__ldg(g4 + idx), g);
+      if constexpr (RMS) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(f[e] * rstd)) * g[e];
-    } else {
-      float b[8];
-      unpack8(__ldg(b4 + idx), b);
+        for (int e = 0; e < 8; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(f[e] * rstd)) * g[e];
+      } else {
+        float b[8];
+        unpack8(__ldg(b4 + idx), b);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+        for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+      }
+      if constexpr (Q8) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(o[e]));
+        dst8[idx] = e4m3x8(o, qs);
+      } else {
+        dst[idx] = pack8(o);
+      }
     }
-    dst[idx] = pack8(o);
   }
+  if constexpr (Q8) amax_combine_warp(p.amax, amax);
 }
 
 // Any d that is a multiple of 8: one warp per row, three sweeps over the row
@@ -653,6 +668,97 @@ __global__ void __launch_bounds__(256) k_column_sum(const float* __restrict__ pa
   }
 }
 
+// ----------------------------------------------------------------------------- E4M3 casts and delayed scaling
+
+// dst[i] = E4M3(src[i] * s), 16 elements (two 16-byte loads, one 16-byte store) per step, grid-stride.
+__global__ void __launch_bounds__(256) k_cast_e4m3(const __nv_bfloat16* __restrict__ src, long long n16,
+                                                   const float* scale, uint8_t* __restrict__ dst, float* amax) {
+  const float s = __ldg(scale);
+  float m = 0.f;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float a[8], b[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(src) + 2 * i), a);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(src) + 2 * i + 1), b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fmaxf(fabsf(a[e]), fabsf(b[e])));
+    const uint2 lo = e4m3x8(a, s), hi = e4m3x8(b, s);
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
+  amax_combine_warp(amax, m);
+}
+
+// Transposing cast: src [rows x cols] -> dst [cols x rows], 64 x 64 tiles through shared memory
+// (rows, cols multiples of 16).  Loads: 16-byte vectors along the source row; stores: 16 bytes of one
+// destination row (16 consecutive source rows of one column).
+constexpr int kCastTile = 64;
+__global__ void __launch_bounds__(256) k_cast_e4m3_t(const __nv_bfloat16* __restrict__ src, int rows, int cols,
+                                                     const float* scale, uint8_t* __restrict__ dst, float* amax) {
+  __shared__ float tile[kCastTile][kCastTile + 1];
+  const float s = __ldg(scale);
+  const int r0 = blockIdx.y * kCastTile, c0 = blockIdx.x * kCastTile;
+  const int t = threadIdx.x;
+  float m = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = t / 8 + 32 * h, cv = (t % 8) * 8;
+    float f[8];
+    if (r0 + r < rows && c0 + cv < cols) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * cols + c0 + cv)), f);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      m = fmaxf(m, fabsf(f[e]));
+      tile[r][cv + e] = f[e];
+    }
+  }
+  __syncthreads();
+  const int oc = t / 4, rb = (t % 4) * 16;  // destination row c0 + oc, bytes [r0 + rb, r0 + rb + 16)
+  if (c0 + oc < cols && r0 + rb < rows) {
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = tile[rb + i][oc];
+    uint4 o;
+    o.x = e4m3x4(f[0], f[1], f[2], f[3], s);
+    o.y = e4m3x4(f[4], f[5], f[6], f[7], s);
+    o.z = e4m3x4(f[8], f[9], f[10], f[11], s);
+    o.w = e4m3x4(f[12], f[13], f[14], f[15], s);
+    *reinterpret_cast<uint4*>(dst + static_cast<long long>(c0 + oc) * rows + r0 + rb) = o;
+  }
+  amax_combine_warp(amax, m);
+}
+
+// One warp per tensor: shift the history by one (oldest out, this step's amax in), mean in a fixed order,
+// next scale = fp8_max / mean / 2^margin (1 while the mean is not positive), reset this step's amax.
+__global__ void __launch_bounds__(128) k_fp8_update(float* scale, float* amax, float* history, int n, int len,
+                                                    float fp8_max, int margin) {
+  const int lane = threadIdx.x & 31;
+  for (int i = threadIdx.x >> 5; i < n; i += blockDim.x >> 5) {
+    float* h = history + static_cast<long long>(i) * len;
+    const float cur = amax[i];
+    for (int base = 0; base < len; base += 32) {
+      const int j = base + lane;
+      float v = 0.f;
+      if (j < len) v = j + 1 < len ? h[j + 1] : cur;
+      __syncwarp();
+      if (j < len) h[j] = v;
+      __syncwarp();
+    }
+    float sum = 0.f;
+    for (int j = lane; j < len; j += 32) sum += h[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+      const float mean = sum / static_cast<float>(len);
+      scale[i] = mean > 0.f && isfinite(mean) ? fp8_max / mean / exp2f(static_cast<float>(margin)) : 1.f;
+      amax[i] = 0.f;
+    }
+  }
+}
+
 int stream_grid(long long work_items, int sm_count) {
   const long long per = 256;
   long long g = (work_items + per - 1) / per;
@@ -694,6 +800,25 @@ cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaS
     case 4096: k_layernorm_fwd_reg<16, 1><<<grid4, 128, 0, s>>>(r); break;
     case 8192: k_layernorm_fwd_reg<16, 2><<<grid2, 128, 0, s>>>(r); break;
     default: k_layernorm_fwd_any<false><<<grid4, 128, 0, s>>>(r); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm_fwd_e4m3(const RowParams& r0, const float* scale, float* amax, cudaStream_t s) {
+  if (r0.rows <= 0) return cudaSuccess;
+  RowParams r = r0;
+  r.qscale = scale;
+  r.amax = amax;
+  const int grid4 = (r.rows + 3) / 4;
+  const int grid2 = (r.rows + 1) / 2;
+  switch (r.d) {
+    case 256: k_layernorm_fwd_reg<1, 1, false, true><<<grid4, 128, 0, s>>>(r); break;
+    case 512: k_layernorm_fwd_reg<2, 1, false, true><<<grid4, 128, 0, s>>>(r); break;
+    case 1024: k_layernorm_fwd_reg<4, 1, false, true><<<grid4, 128, 0, s>>>(r); break;
+    case 2048: k_layernorm_fwd_reg<8, 1, false, true><<<grid4, 128, 0, s>>>(r); break;
+    case 4096: k_layernorm_fwd_reg<16, 1, false, true><<<grid4, 128, 0, s>>>(r); break;
+    case 8192: k_layernorm_fwd_reg<16, 2, false, true><<<grid2, 128, 0, s>>>(r); break;
+    default: return cudaErrorNotSupported;
   }
   return cudaGetLastError();
 }
@@ -846,6 +971,32 @@ cudaError_t launch_gather_rows(const RowParams& r, const DeviceCtx& ctx, cudaStr
 cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s) {
   if (cols <= 0 || out == nullptr) return cudaSuccess;
   k_column_sum<<<(cols + 31) / 32, 256, 0, s>>>(partial, rows, cols, cols, out, out, cols, out_bf16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+
+cudaError_t launch_cast_e4m3(const void* src, int rows, int cols, bool transpose, const float* scale, void* dst,
+                             float* amax, cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (transpose) {
+    const dim3 grid((cols + kCastTile - 1) / kCastTile, (rows + kCastTile - 1) / kCastTile);
+    if (grid.y > 65535) return cudaErrorInvalidValue;
+    k_cast_e4m3_t<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, scale,
+                                       static_cast<uint8_t*>(dst), amax);
+  } else {
+    const long long n16 = static_cast<long long>(rows) * cols / 16;
+    long long g = (n16 + 255) / 256;
+    if (g > 152 * 8) g = 152 * 8;
+    k_cast_e4m3<<<static_cast<int>(g), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), n16, scale,
+                                                    static_cast<uint8_t*>(dst), amax);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_update(float* scale, float* amax, float* history, int n, int len, float fp8_max, int margin,
+                              cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  k_fp8_update<<<1, 128, 0, s>>>(scale, amax, history, n, len, fp8_max, margin);
   return cudaGetLastError();
 }
 

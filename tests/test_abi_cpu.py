@@ -129,7 +129,7 @@ def test_sp_region_workspace_sizes(lib):
         assert _ws(s, binding.OP_DROPOUT_BWD) == (binding.OK, dropcol)
         st, spb = _ws(s, binding.OP_SP_BWD)
         assert _ws(s, binding.OP_SP_BLOCK_BWD) == (binding.OK, spb + dropcol)
-    assert _ws(binding.make_shape(256, 64, 256, 2), 9)[0] == binding.ERR_INVALID_ARG
+    assert _ws(binding.make_shape(256, 64, 256, 2), 10)[0] == binding.ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("p", [1.0, -0.25, float("nan"), float("inf")])
@@ -173,3 +173,26 @@ def test_sp_region_argument_checks(lib):
     assert L.tpmlp_sp_block_backward(None, None, None, 1e-5, None, None, None, drop, None, None, None, None,
                                      ctypes.byref(e), None, None, None, None, None, None, None, None, 0, None) \
         == binding.OK
+
+
+def test_fp8_workspace_and_argument_checks(lib):
+    for w in inputs.WORKLOADS.values():
+        if w.dtype != "bf16" or not w.sp:
+            continue
+        s = binding.make_shape(w.T, w.d, w.F, w.N)
+        assert _ws(s, binding.OP_SP_FWD_FP8) == (binding.OK, 2 * _r256(w.d * w.F) + _r256(w.T * w.d) +
+                                                  _r256(w.T * w.F))
+    assert _ws(binding.make_shape(256, 72, 288, 2), binding.OP_SP_FWD_FP8)[0] == binding.ERR_INVALID_ARG  # d % 16
+    L = binding.lib()
+    good = ctypes.c_void_p(1 << 20)
+    # rows or columns not multiples of 16, a missing scale or amax
+    assert L.tpmlp_cast_e4m3(good, 24, 64, 0, good, good, good, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_cast_e4m3(good, 32, 64, 1, None, good, good, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_cast_e4m3(good, 32, 64, 1, good, good, None, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_cast_e4m3(None, 0, 64, 0, None, None, None, None) == binding.OK
+    st = binding.Fp8State(1 << 20, 1 << 21, 1 << 22, 0, 0)          # history length 0
+    assert L.tpmlp_fp8_update_scales(ctypes.byref(st), None) == binding.ERR_INVALID_ARG
+    s = binding.make_shape(256, 96, 384, 2)                          # LayerNorm width without an E4M3 kernel
+    chunks = ctypes.cast((ctypes.c_void_p * 2)(1 << 20, 1 << 21), binding._PP)
+    assert L.tpmlp_layernorm_gather_e4m3(chunks, good, good, 1e-5, ctypes.byref(s), good, good, good, None) \
+        == binding.ERR_UNSUPPORTED
