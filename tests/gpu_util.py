@@ -47,16 +47,25 @@ def assert_fp32_close(name, got, ref):
 GUARD = 4096  # elements of guard band on each side of an output buffer
 
 
+# guard pattern per element size (one byte for E4M3 buffers)
+_PATTERN = {1: 0x3B, 2: 0x7F3B, 4: 0x7F3B}
+
+
+def _bits_dtype(dtype):
+    return {1: torch.uint8, 2: torch.int16, 4: torch.int32}[dtype.itemsize]
+
+
 class Guarded:
     """An output buffer with guard bands before and after it, filled with a pattern that no kernel writes."""
 
     def __init__(self, shape, dtype=torch.bfloat16):
         n = int(np.prod(shape))
         self.raw = torch.empty(n + 2 * GUARD, dtype=dtype, device="cuda")
-        self.raw.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).fill_(0x7F3B)
+        self.raw.view(_bits_dtype(dtype)).fill_(_PATTERN[dtype.itemsize])
         self.t = self.raw[GUARD:GUARD + n].view(*shape)
 
     def intact(self):
-        bits = self.raw.view(torch.int16 if self.raw.dtype == torch.bfloat16 else torch.int32)
+        bits = self.raw.view(_bits_dtype(self.raw.dtype))
         n = self.raw.numel()
-        return bool((bits[:GUARD] == 0x7F3B).all()) and bool((bits[n - GUARD:] == 0x7F3B).all())
+        pat = _PATTERN[self.raw.dtype.itemsize]
+        return bool((bits[:GUARD] == pat).all()) and bool((bits[n - GUARD:] == pat).all())
