@@ -86,7 +86,12 @@ reason in the design notes):
   (``2**-margin`` headroom optional; ``S = 1`` while the history is zero).
   Which tensors run in FP8 in the forward: the gathered norm output, both
   weights and the GeLU output ``H`` (the operands of the two GEMMs); the
-  bias and GeLU act on the dequantised fp32 product.
+  bias and GeLU act on the dequantised fp32 product.  In the backward the
+  gradients that enter GEMMs (``dY`` and ``dHpre``) are cast to E5M2 (1
+  sign, 5 exponent bits with bias 15, 2 mantissa bits, largest finite 57344,
+  subnormals down to 2**-16; same rounding and saturation), the forward's
+  E4M3 operands are reused, and the bias gradient and GeLU' act on fp32
+  values.
 
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` (values
 printed on the pages, closed forms, invariants, brute force, library
@@ -354,6 +359,28 @@ def round_e4m3(x):
     return np.copysign(r, x)
 
 
+E5M2_MAX = 57344.0
+
+
+def round_e5m2(x):
+    """Nearest E5M2 value, ties to even, magnitudes above 57344 saturated to 57344; returned as float64.
+
+    As :func:`round_e4m3` with two mantissa bits (quantum ``2**(E-2)``) and normal exponents
+    down to ``E = -14`` (subnormal quantum ``2**-16``).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)
+    quantum = np.ldexp(1.0, np.maximum(e - 1, -14) - 2)
+    r = np.minimum(np.rint(a / quantum) * quantum, E5M2_MAX)
+    return np.copysign(r, x)
+
+
+def quantize_e5m2(x, scale):
+    """``E5M2(x·S)`` with the product formed in float32."""
+    return round_e5m2(np.asarray(x, dtype=np.float32) * np.float32(scale))
+
+
 def quantize_e4m3(x, scale):
     """``E4M3(x·S)`` with the product formed in float32 (``x`` taken to float32 first)."""
     return round_e4m3(np.asarray(x, dtype=np.float32) * np.float32(scale))
@@ -394,6 +421,52 @@ def mlp_fp8(X, A, B, b, N: int, scales):
     amax = {"X": float(np.max(np.abs(X), initial=0.0)), "A": float(np.max(np.abs(A), initial=0.0)),
             "B": float(np.max(np.abs(B), initial=0.0)), "H": float(np.max(np.abs(H), initial=0.0))}
     return {"Y": all_reduce(parts), "H": H, "qH": qh, "amax": amax}
+
+
+def mlp_backward_fp8(X, A, B, b, dY, N: int, scales, grad_scales):
+    """Backward of :func:`mlp_fp8` with E5M2 gradients: ``grad_scales = (S_dY, S_dHpre)``.
+
+    With the forward's ``q_X, q_A, q_B``, ``Hpre = (q_X·q_A)/(S_X S_A) + b``, ``H = GeLU(Hpre)``,
+    ``q_H = E4M3(H·S_H)`` and ``q_dY = E5M2(dY·S_dY)``:
+    ``dHpre = (q_dY·q_Bᵀ)/(S_dY S_B) ⊙ GeLU'(Hpre)``, ``q_g = E5M2(dHpre·S_dHpre)``,
+    ``dB = (q_Hᵀ·q_dY)/(S_H S_dY)``, ``dA = (q_Xᵀ·q_g)/(S_X S_dHpre)``, ``db = Σ_rows dHpre``,
+    ``dX = Σ_i (q_g,i·q_A,iᵀ)/(S_dHpre S_A)`` (the backward shard sum).  Also the amaxes of
+    ``dY`` and ``dHpre``.
+    """
+    sx, sa, sb, sh = (float(np.float32(v)) for v in scales)
+    sdy, sg = (float(np.float32(v)) for v in grad_scales)
+    X = np.asarray(X, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    qx, qa, qb = quantize_e4m3(X, sx), quantize_e4m3(A, sa), quantize_e4m3(B, sb)
+    Hpre = (qx @ qa) / (sx * sa) + _bias_or_zero(b, A.shape[1])
+    qh = quantize_e4m3(gelu(Hpre), sh)
+    qdy = quantize_e5m2(dY, sdy)
+    dHpre = (qdy @ qb.T) / (sdy * sb) * gelu_prime(Hpre)
+    qg = quantize_e5m2(dHpre, sg)
+    F = A.shape[1]
+    dX_parts = [(qg[:, lo:hi] @ qa[:, lo:hi].T) / (sg * sa) for lo, hi in shard_ranges(F, N)]
+    return {"dX": all_reduce(dX_parts), "dX_parts": dX_parts, "dA": (qx.T @ qg) / (sx * sg),
+            "dB": (qh.T @ qdy) / (sh * sdy), "db": dHpre.sum(axis=0), "dHpre": dHpre, "qdHpre": qg,
+            "amax": {"dY": float(np.max(np.abs(dY), initial=0.0)), "dHpre": float(np.max(np.abs(dHpre), initial=0.0))}}
+
+
+def sp_backward_fp8(X_chunks, gamma, beta, eps, A, B, b, dY_chunks, N: int, scales, grad_scales):
+    """:func:`sp_backward` with the FP8 GEMMs of :func:`mlp_backward_fp8`: gather the norm output and
+    dY, the FP8 MLP backward, reduce-scatter of the input-gradient shard partials, LayerNorm backward
+    per chunk (on the unquantised gradient)."""
+    Xg = all_gather([layer_norm(c, gamma, beta, eps) for c in X_chunks])
+    g = mlp_backward_fp8(Xg, A, B, b, all_gather(dY_chunks), N, scales, grad_scales)
+    dXg_chunks = reduce_scatter(g["dX_parts"], N)
+    dX_chunks, dgamma, dbeta = [], 0.0, 0.0
+    for xc, dyc in zip(X_chunks, dXg_chunks):
+        dx, dga, dbe = layer_norm_backward(xc, gamma, eps, dyc)
+        dX_chunks.append(dx)
+        dgamma = dgamma + dga
+        dbeta = dbeta + dbe
+    g.update({"dX_chunks": dX_chunks, "dgamma": dgamma, "dbeta": dbeta, "dXg_chunks": dXg_chunks})
+    return g
 
 
 def sp_forward_fp8(X_chunks, gamma, beta, eps, A, B, b, N: int, scales):

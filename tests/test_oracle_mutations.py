@@ -141,7 +141,20 @@ def _mlp_fp8_one_descale(X, A, B, b, N, scales):
     return _orig["mlp_fp8"](X, A, B, b, N, (sx, sa, sb * 2.0, sh))
 
 
+def _round_e5m2_three_bits(x):
+    return _orig["round_e4m3"](x)
+
+
+def _mlp_backward_fp8_wrong_dB_scale(X, A, B, b, dY, N, scales, grad_scales):
+    g = _orig["mlp_backward_fp8"](X, A, B, b, dY, N, scales, grad_scales)
+    g["dB"] = g["dB"] * float(np.float32(scales[3]))      # the H scale left out of the dequantisation
+    return g
+
+
 CASES = [
+    ("round_e5m2", _round_e5m2_three_bits, lambda: pins.test_round_e5m2_bruteforce_and_torch()),
+    ("mlp_backward_fp8", _mlp_backward_fp8_wrong_dB_scale,
+     lambda: pins.test_mlp_backward_fp8_error_is_the_formats_size()),
     ("round_e4m3", _round_e4m3_ties_away, lambda: pins.test_round_e4m3_bruteforce_and_ties()),
     ("fp8_scale", _fp8_scale_max, lambda: pins.test_fp8_delayed_scale_closed_forms()),
     ("mlp_fp8", _mlp_fp8_one_descale, lambda: pins.test_mlp_fp8_torch_witness()),

@@ -611,3 +611,114 @@ def test_sp_forward_fp8_is_mlp_fp8_on_the_gathered_norm(N):
     out = oracle.sp_forward_fp8([X[lo:hi] for lo, hi in cr], gam, bet, 1e-5, A, B, b, N, scales)
     ref = oracle.mlp_fp8(oracle.layer_norm(X, gam, bet, 1e-5), A, B, b, N, scales)
     assert np.array_equal(np.concatenate(out["Y_chunks"]), ref["Y"])
+
+
+# --------------------------------------------------------------------------- E5M2 and the FP8 backward
+
+def _e5m2_table():
+    """Every finite E5M2 value with its code: bias 15, 2 mantissa bits, exponent field 0 = subnormal,
+    exponent field 31 = infinities and NaNs (excluded)."""
+    vals = []
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        ex, man = (code >> 2) & 0x1F, code & 0x3
+        if ex == 0x1F:
+            continue
+        v = man / 4.0 * 2.0 ** -14 if ex == 0 else (1.0 + man / 4.0) * 2.0 ** (ex - 15)
+        vals.append((sign * v, code))
+    return vals
+
+
+def test_round_e5m2_bruteforce_and_torch():
+    table = _e5m2_table()
+    pos = sorted({v for v, _ in table if v >= 0})
+    assert max(pos) == 57344.0 and pos[1] == 2.0 ** -16
+
+    def brute(x):
+        if abs(x) > 57344.0:
+            return math.copysign(57344.0, x)
+        best = None
+        for v, code in table:
+            dist = abs(v - x)
+            if best is None or dist < best[0] or (dist == best[0] and (code & 1) == 0 and (best[1] & 1) == 1):
+                best = (dist, code, v)
+        return best[2]
+
+    rng = np.random.default_rng(24)
+    xs = list(rng.normal(size=200) * 10.0 ** rng.uniform(-5, 4.5, size=200))
+    xs += [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])] + [6e4, -1e7, 0.0]
+    got = oracle.round_e5m2(np.array(xs))
+    for x, g in zip(xs, got):
+        assert g == brute(x), x
+    x = (rng.normal(size=3000) * 10.0 ** rng.uniform(-4, 4, size=3000)).astype(np.float32)
+    assert np.array_equal(oracle.round_e5m2(x), torch.from_numpy(x).to(torch.float8_e5m2).to(torch.float64).numpy())
+
+
+def _fp8_backward_problem(T=12, d=16, F=64):
+    """A problem with every scale set from its tensor's amax, as delayed scaling settles to."""
+    X, A, B, b = _rand_block(T, d, F)
+    dY = RNG.normal(size=(T, d))
+    s3 = (448.0 / np.max(np.abs(X)), 448.0 / np.max(np.abs(A)), 448.0 / np.max(np.abs(B)))
+    scales = (*s3, 448.0 / oracle.mlp_fp8(X, A, B, b, 1, (*s3, 1.0))["amax"]["H"])
+    first = oracle.mlp_backward_fp8(X, A, B, b, dY, 1, scales, (1.0, 1.0))["amax"]
+    return X, A, B, b, dY, scales, (57344.0 / first["dY"], 57344.0 / first["dHpre"])
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_mlp_backward_fp8_with_exact_casts_is_the_chain_rule(N, monkeypatch):
+    """With the casts made exact (identity rounding) the scales must cancel and the FP8 backward must be
+    the pinned chain-rule backward: any wrong scale, transposed operand or misplaced factor shows."""
+    X, A, B, b, dY, scales, gscales = _fp8_backward_problem()
+    monkeypatch.setattr(oracle, "round_e4m3", lambda v: np.asarray(v, dtype=np.float64))
+    monkeypatch.setattr(oracle, "round_e5m2", lambda v: np.asarray(v, dtype=np.float64))
+    g = oracle.mlp_backward_fp8(X, A, B, b, dY, N, scales, gscales)
+    # the only roundings left are the float32 products x*S; compare at float32 precision
+    ref = oracle.mlp_backward(X.astype(np.float32), A.astype(np.float32), B.astype(np.float32), b,
+                              dY.astype(np.float32))
+    for k in ("dX", "dA", "dB", "db"):
+        assert rel(g[k], ref[k]) < 1e-5, k
+
+
+def test_fp8_backward_cast_formats_follow_the_page():
+    """E4M3 for activations and weights, E5M2 for the gradients entering GEMMs: spy on the two casts."""
+    X, A, B, b, dY, scales, gscales = _fp8_backward_problem()
+    seen = {"e4m3": [], "e5m2": []}
+    r4, r5 = oracle.round_e4m3, oracle.round_e5m2
+    try:
+        oracle.round_e4m3 = lambda v: (seen["e4m3"].append(np.shape(v)), r4(v))[1]
+        oracle.round_e5m2 = lambda v: (seen["e5m2"].append(np.shape(v)), r5(v))[1]
+        oracle.mlp_backward_fp8(X, A, B, b, dY, 2, scales, gscales)
+    finally:
+        oracle.round_e4m3, oracle.round_e5m2 = r4, r5
+    T, d = X.shape
+    F = A.shape[1]
+    assert sorted(seen["e4m3"]) == sorted([(T, d), (d, F), (F, d), (T, F)])     # X, A, B, H
+    assert sorted(seen["e5m2"]) == sorted([(T, d), (T, F)])                     # dY, dHpre
+
+
+def test_mlp_backward_fp8_error_is_the_formats_size():
+    X, A, B, b, dY, scales, gscales = _fp8_backward_problem(T=32, d=32, F=128)
+    g = oracle.mlp_backward_fp8(X, A, B, b, dY, 4, scales, gscales)
+    ref = oracle.mlp_backward(X, A, B, b, dY)
+    # E5M2 keeps 2 mantissa bits (up to 12.5% per element); through two GEMMs the errors stay near 10%
+    for k in ("dX", "dA", "dB"):
+        assert 1e-3 < rel(g[k], ref[k]) < 0.2, k
+    assert rel(g["db"], ref["db"]) < 0.2
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_sp_backward_fp8_is_mlp_backward_fp8_on_the_gathered_norm(N):
+    T, d, F = 4 * N, 16, 64
+    X = RNG.normal(size=(T, d))
+    gam, bet = 1 + 0.1 * RNG.normal(size=d), 0.1 * RNG.normal(size=d)
+    _, A, B, b = _rand_block(1, d, F)
+    dY = RNG.normal(size=(T, d))
+    scales, gscales = (100.0, 2000.0, 2000.0, 50.0), (1000.0, 2.0 ** 12)
+    cr = oracle.chunk_ranges(T, N)
+    g = oracle.sp_backward_fp8([X[lo:hi] for lo, hi in cr], gam, bet, 1e-5, A, B, b, [dY[lo:hi] for lo, hi in cr],
+                               N, scales, gscales)
+    ref = oracle.mlp_backward_fp8(oracle.layer_norm(X, gam, bet, 1e-5), A, B, b, dY, N, scales, gscales)
+    for k in ("dA", "dB", "db"):
+        assert np.array_equal(g[k], ref[k]), k
+    for (lo, hi), dx in zip(cr, g["dX_chunks"]):
+        assert np.array_equal(dx, oracle.layer_norm_backward(X[lo:hi], gam, 1e-5, ref["dX"][lo:hi])[0])
