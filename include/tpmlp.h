@@ -94,7 +94,8 @@ enum {
   TPMLP_OP_LN_BWD = 6,         /* tpmlp_layernorm_backward, tpmlp_layernorm_backward_add */
   TPMLP_OP_SP_BLOCK_BWD = 7,   /* tpmlp_sp_block_backward */
   TPMLP_OP_DROPOUT_BWD = 8,    /* tpmlp_dropout_backward with a dbias2 output */
-  TPMLP_OP_SP_FWD_FP8 = 9      /* tpmlp_sp_forward_fp8 */
+  TPMLP_OP_SP_FWD_FP8 = 9,     /* tpmlp_sp_forward_fp8 */
+  TPMLP_OP_SP_BWD_FP8 = 10     /* tpmlp_sp_backward_fp8 */
 };
 
 /* Dropout of the sequence-parallel region.  The pages name Dropout in the
@@ -292,14 +293,72 @@ TPMLP_API tpmlp_status tpmlp_fp8_update_scales(const tpmlp_fp8_state* state, tpm
 /* The sequence-parallel block forward with E4M3 GEMMs: the weights are cast
  * (transposed) with scale[1], scale[2]; the LayerNorm writes E4M3 with
  * scale[0]; GEMM1 dequantises, adds the bias, applies GeLU and casts H with
- * scale[3]; GEMM2 reduces the shards in TMEM and stores bf16 Y chunks; then
- * tpmlp_fp8_update_scales.  Workspace: size of TPMLP_OP_SP_FWD_FP8.  bf16
- * X, gamma, beta, A, B, bias and Y as in tpmlp_sp_forward. */
+ * scale[3]; GEMM2 reduces the shards in TMEM and stores bf16 Y chunks.  The
+ * scales are not updated here: call tpmlp_fp8_update_scales(state) when the
+ * step is over (after tpmlp_sp_backward_fp8, which reads the same scales).
+ * Hpre_out ([T x F] bf16), Xq_out ([T x d] E4M3), Hq_out ([T x F] E4M3):
+ * NULL, or buffers that keep what the FP8 backward needs (otherwise they live
+ * in the workspace).  Workspace: size of TPMLP_OP_SP_FWD_FP8.  bf16 X, gamma,
+ * beta, A, B, bias and Y as in tpmlp_sp_forward. */
 TPMLP_API tpmlp_status tpmlp_sp_forward_fp8(const void* const* X_chunks, const void* gamma, const void* beta,
                                             float eps, const void* A, const void* B, const void* bias,
                                             const tpmlp_fp8_state* state, const tpmlp_shape* shape,
-                                            void* const* Y_chunks, void* workspace, size_t workspace_bytes,
-                                            tpmlp_stream_t stream);
+                                            void* const* Y_chunks, void* Hpre_out, void* Xq_out, void* Hq_out,
+                                            void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* ------------------------------------------------------------------ FP8 backward (E5M2 gradients)
+ * The page's hybrid: the gradients that enter GEMMs (dY and dHpre) in E5M2
+ * (bias 15, 2 mantissa bits, largest finite 57344, same rounding and
+ * saturation as the E4M3 casts), the forward's E4M3 operands reused.  Every
+ * FP8 GEMM reads both operands K-major; the operands the weight-gradient
+ * GEMMs need transposed are byte-transposed copies. */
+
+/* dst = E5M2(src * (*scale)), layouts and amax as tpmlp_cast_e4m3. */
+TPMLP_API tpmlp_status tpmlp_cast_e5m2(const void* src, int64_t rows, int64_t cols, int transpose, const float* scale,
+                                       void* dst, float* amax, tpmlp_stream_t stream);
+
+/* dst [cols x rows] = the transpose of src [rows x cols], both one byte per
+ * element (E4M3 or E5M2 codes); rows, cols multiples of 16. */
+TPMLP_API tpmlp_status tpmlp_transpose_bytes(const void* src, int64_t rows, int64_t cols, void* dst,
+                                             tpmlp_stream_t stream);
+
+/* The GeLU' GEMM on FP8 operands: g = (dYq Bq^T) / (sdy sb) * GeLU'(Hpre),
+ * dHq = E5M2(g * (*scale_g)), *amax_g max-combined with max |g|, dbias
+ * (NULL or [F] bf16) = column sums of g (workspace: size of
+ * TPMLP_OP_DH_GELUPRIME).  dYq [T x d] E5M2, Bq [F x d] E4M3 (B as stored,
+ * from tpmlp_cast_e4m3 without transpose), Hpre [T x F] bf16, dHq [T x F]. */
+TPMLP_API tpmlp_status tpmlp_gemm_dh_geluprime_e5m2(const void* dYq, const void* Bq, const void* Hpre,
+                                                    const tpmlp_shape* shape, const float* scale_dy,
+                                                    const float* scale_b, const float* scale_g, void* dHq,
+                                                    float* amax_g, void* dbias, void* workspace,
+                                                    size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* C = (A8 B8^T) / ((*scale_a) (*scale_b)) in bf16, one fp32 accumulator over
+ * K.  A8 [M x K] and B8 [N x K] row-major bytes in format a_fmt / b_fmt
+ * (0 = E4M3, 1 = E5M2); C [M x N] with ldc elements between rows.  K % 16 ==
+ * 0, N % 8 == 0, ldc % 8 == 0, ldc >= N.  The weight-gradient and input-
+ * gradient GEMMs of the FP8 backward are this call. */
+TPMLP_API tpmlp_status tpmlp_gemm_fp8(const void* A8, int a_fmt, const void* B8, int b_fmt, int64_t M, int64_t N,
+                                      int64_t K, const float* scale_a, const float* scale_b, void* C, int64_t ldc,
+                                      tpmlp_stream_t stream);
+
+/* Backward of tpmlp_sp_forward_fp8: dY gathered and cast to E5M2 (both
+ * layouts) with grad->scale[0]; the weights cast to E4M3 as stored with the
+ * forward's scale[1], scale[2]; the GeLU' GEMM (dHq in E5M2 with
+ * grad->scale[1], dbias); dB = (Hq^T dYq), dA = (Xq^T dHq), dXg = (dHq A^T)
+ * on FP8 operands; the LayerNorm backward (bf16) to dX chunks, dgamma,
+ * dbeta; then the delayed-scale update of `grad` (two tensors, dY and dHpre,
+ * E5M2's largest value 57344 in place of 448).  `fwd` is the forward's state
+ * (its scales unchanged since the forward); Hpre, Xq, Hq the forward's saved
+ * outputs.  T, d, F multiples of 16.  Workspace: size of
+ * TPMLP_OP_SP_BWD_FP8. */
+TPMLP_API tpmlp_status tpmlp_sp_backward_fp8(const void* const* X_chunks, const void* gamma, float eps, const void* A,
+                                             const void* B, const void* Hpre, const void* Xq, const void* Hq,
+                                             const void* const* dY_chunks, const tpmlp_fp8_state* fwd,
+                                             const tpmlp_fp8_state* grad, const tpmlp_shape* shape,
+                                             void* const* dX_chunks, void* dA, void* dB, void* dbias, void* dgamma,
+                                             void* dbeta, void* workspace, size_t workspace_bytes,
+                                             tpmlp_stream_t stream);
 
 /* ------------------------------------------------------------------ single steps (bf16)
  * Each step is one kernel launch (plus a small fixed-order reduction where

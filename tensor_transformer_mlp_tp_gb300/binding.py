@@ -20,7 +20,8 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
 BF16, FP32 = 0, 1
 (OP_FWD, OP_SP_FWD, OP_SP_FWD_PARTIALS, OP_BWD, OP_SP_BWD, OP_DH_GELUPRIME, OP_LN_BWD, OP_SP_BLOCK_BWD,
- OP_DROPOUT_BWD, OP_SP_FWD_FP8) = range(10)
+ OP_DROPOUT_BWD, OP_SP_FWD_FP8, OP_SP_BWD_FP8) = range(11)
+E4M3, E5M2 = 0, 1
 RS_FUSED, RS_PARTIALS = 0, 1
 
 
@@ -87,8 +88,16 @@ _SIGS = {
     "tpmlp_gemm1_e4m3": ([_P, _P, _P, _SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "tpmlp_gemm2_e4m3": ([_P, _P, _SP, _P, _P, _P, _PP, _P], ctypes.c_int),
     "tpmlp_fp8_update_scales": ([_FP, _P], ctypes.c_int),
-    "tpmlp_sp_forward_fp8": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _FP, _SP, _PP, _P, ctypes.c_size_t, _P],
-                             ctypes.c_int),
+    "tpmlp_sp_forward_fp8": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _FP, _SP, _PP, _P, _P, _P, _P,
+                              ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_cast_e5m2": ([_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P, _P, _P], ctypes.c_int),
+    "tpmlp_transpose_bytes": ([_P, ctypes.c_int64, ctypes.c_int64, _P, _P], ctypes.c_int),
+    "tpmlp_gemm_dh_geluprime_e5m2": ([_P, _P, _P, _SP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+                                     ctypes.c_int),
+    "tpmlp_gemm_fp8": ([_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P,
+                        _P, ctypes.c_int64, _P], ctypes.c_int),
+    "tpmlp_sp_backward_fp8": ([_PP, _P, ctypes.c_float, _P, _P, _P, _P, _P, _PP, _FP, _FP, _SP, _PP, _P, _P, _P, _P,
+                               _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
 }
 
 
@@ -427,7 +436,9 @@ def tpmlp_fp8_update_scales(state, stream=None):
     _check("tpmlp_fp8_update_scales", lib().tpmlp_fp8_update_scales(ctypes.byref(state), _stream(stream)))
 
 
-def tpmlp_sp_forward_fp8(X_chunks, gamma, beta, A, B, N, Y_chunks, state, bias=None, eps=1e-5, ws=None, stream=None):
+def tpmlp_sp_forward_fp8(X_chunks, gamma, beta, A, B, N, Y_chunks, state, bias=None, eps=1e-5, Hpre_out=None,
+                         Xq_out=None, Hq_out=None, ws=None, stream=None):
+    """The E4M3 block forward; the scales are updated by tpmlp_fp8_update_scales once the step is over."""
     rows, d = X_chunks[0].shape
     shape = make_shape(rows * N, d, A.shape[1], N)
     ws = workspace(shape, OP_SP_FWD_FP8, A.device) if ws is None else ws
@@ -435,8 +446,51 @@ def tpmlp_sp_forward_fp8(X_chunks, gamma, beta, A, B, N, Y_chunks, state, bias=N
     yp, _ya = _ptrs(Y_chunks)
     _check("tpmlp_sp_forward_fp8", lib().tpmlp_sp_forward_fp8(
         xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), ctypes.byref(state), ctypes.byref(shape), yp,
-        _ptr(ws), ws.numel(), _stream(stream)))
+        _ptr(Hpre_out), _ptr(Xq_out), _ptr(Hq_out), _ptr(ws), ws.numel(), _stream(stream)))
     return Y_chunks
+
+
+def tpmlp_cast_e5m2(src, scale, dst, amax, transpose=False, stream=None):
+    rows, cols = src.shape
+    _check("tpmlp_cast_e5m2", lib().tpmlp_cast_e5m2(_ptr(src), rows, cols, 1 if transpose else 0, _ptr(scale),
+                                                    _ptr(dst), _ptr(amax), _stream(stream)))
+
+
+def tpmlp_transpose_bytes(src, dst, stream=None):
+    rows, cols = src.shape
+    _check("tpmlp_transpose_bytes", lib().tpmlp_transpose_bytes(_ptr(src), rows, cols, _ptr(dst), _stream(stream)))
+
+
+def tpmlp_gemm_dh_geluprime_e5m2(dYq, Bq, Hpre, N, scale_dy, scale_b, scale_g, dHq, amax_g, dbias=None, ws=None,
+                                 stream=None):
+    shape = make_shape(dYq.shape[0], dYq.shape[1], Bq.shape[0], N)
+    if dbias is not None and ws is None:
+        ws = workspace(shape, OP_DH_GELUPRIME, dYq.device)
+    _check("tpmlp_gemm_dh_geluprime_e5m2", lib().tpmlp_gemm_dh_geluprime_e5m2(
+        _ptr(dYq), _ptr(Bq), _ptr(Hpre), ctypes.byref(shape), _ptr(scale_dy), _ptr(scale_b), _ptr(scale_g), _ptr(dHq),
+        _ptr(amax_g), _ptr(dbias), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def tpmlp_gemm_fp8(A8, a_fmt, B8, b_fmt, scale_a, scale_b, C, stream=None):
+    """C [M x N] bf16 = (A8 [M x K] . B8 [N x K]^T) / (scale_a scale_b); formats E4M3 / E5M2."""
+    M, K = A8.shape
+    N = B8.shape[0]
+    _check("tpmlp_gemm_fp8", lib().tpmlp_gemm_fp8(_ptr(A8), a_fmt, _ptr(B8), b_fmt, M, N, K, _ptr(scale_a),
+                                                  _ptr(scale_b), _ptr(C), C.stride(0), _stream(stream)))
+
+
+def tpmlp_sp_backward_fp8(X_chunks, gamma, A, B, Hpre, Xq, Hq, dY_chunks, N, fwd_state, grad_state, dX_chunks, dA, dB,
+                          dgamma, dbeta, dbias=None, eps=1e-5, ws=None, stream=None):
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, A.shape[1], N)
+    ws = workspace(shape, OP_SP_BWD_FP8, A.device) if ws is None else ws
+    xp, _xa = _ptrs(X_chunks)
+    dyp, _dya = _ptrs(dY_chunks)
+    dxp, _dxa = _ptrs(dX_chunks)
+    _check("tpmlp_sp_backward_fp8", lib().tpmlp_sp_backward_fp8(
+        xp, _ptr(gamma), eps, _ptr(A), _ptr(B), _ptr(Hpre), _ptr(Xq), _ptr(Hq), dyp, ctypes.byref(fwd_state),
+        ctypes.byref(grad_state), ctypes.byref(shape), dxp, _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dgamma),
+        _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def tpmlp_selftest_wait_timeout(budget_us: int, stream=None):

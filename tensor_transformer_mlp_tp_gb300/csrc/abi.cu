@@ -157,6 +157,7 @@ size_t ws_bytes(const tpmlp_shape* s, int op) {
     case TPMLP_OP_SP_BLOCK_BWD: return 3 * z.tf + z.colsum + 3 * z.td + z.lnbwd + z.dropcol;
     case TPMLP_OP_DROPOUT_BWD: return z.dropcol;
     case TPMLP_OP_SP_FWD_FP8: return 2 * z.df8 + z.td8 + z.tf8;
+    case TPMLP_OP_SP_BWD_FP8: return 2 * z.td + 3 * z.td8 + 2 * z.df8 + 3 * z.tf8 + z.colsum + z.lnbwd;
     default: return 0;
   }
 }
@@ -458,6 +459,53 @@ cudaError_t do_gemm2_e4m3(const DeviceCtx& c, const void* Hq, const void* BqT, c
   return launch_gemm(g, c, st);
 }
 
+cudaError_t do_dh_e5m2(const DeviceCtx& c, const void* dYq, const void* Bq, const void* Hpre, const tpmlp_shape* s,
+                       const float* sdy, const float* sb, const float* sg, void* dHq, float* amax_g, void* dbias,
+                       float* colsum, cudaStream_t st) {
+  GemmLaunch g;
+  g.M = static_cast<int>(s->tokens);
+  g.N = static_cast<int>(s->ffn);
+  g.K = static_cast<int>(s->d);
+  g.a = {dYq, s->d, false};
+  g.b = {Bq, s->d, false};
+  g.epi = kEpiDGeluQ;
+  g.fp8 = true;
+  g.a_fmt = 1;
+  g.b_fmt = 0;
+  g.scale_a = sdy;
+  g.scale_b = sb;
+  g.scale_out = sg;
+  g.amax_out = amax_g;
+  g.out0 = dHq;
+  g.ld0 = s->ffn;
+  g.aux = Hpre;
+  g.ld_aux = s->ffn;
+  g.colsum = dbias != nullptr ? colsum : nullptr;
+  cudaError_t e = launch_gemm(g, c, st);
+  if (e != cudaSuccess || dbias == nullptr) return e;
+  const int m_blocks = static_cast<int>((s->tokens + kBM - 1) / kBM);  // 4 partial rows per 128-row block
+  return launch_column_sum(colsum, 4 * m_blocks, static_cast<int>(s->ffn), dbias, true, st);
+}
+
+cudaError_t do_gemm_fp8(const DeviceCtx& c, const void* A8, int a_fmt, const void* B8, int b_fmt, int M, int N, int K,
+                        const float* sa, const float* sb, void* C, long long ldc, cudaStream_t st) {
+  GemmLaunch g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.a = {A8, K, false};
+  g.b = {B8, K, false};
+  g.epi = kEpiStore;
+  g.fp8 = true;
+  g.a_fmt = a_fmt;
+  g.b_fmt = b_fmt;
+  g.scale_a = sa;
+  g.scale_b = sb;
+  g.out0 = C;
+  g.ld0 = ldc;
+  return launch_gemm(g, c, st);
+}
+
 bool fp8_state_ok(const tpmlp_fp8_state* f) {
   return f != nullptr && f->scale != nullptr && f->amax != nullptr && f->history != nullptr &&
          f->history_len >= 1 && f->history_len <= (1 << 20) && f->margin >= 0 && f->margin <= 64 &&
@@ -516,13 +564,15 @@ tpmlp_status tpmlp_workspace_size(const tpmlp_shape* shape, int op, size_t* byte
   if (bytes == nullptr) return TPMLP_ERR_INVALID_ARG;
   const bool sp = op == TPMLP_OP_SP_FWD || op == TPMLP_OP_SP_FWD_PARTIALS || op == TPMLP_OP_SP_BWD ||
                   op == TPMLP_OP_LN_BWD || op == TPMLP_OP_SP_BLOCK_BWD || op == TPMLP_OP_DROPOUT_BWD ||
-                  op == TPMLP_OP_SP_FWD_FP8;
+                  op == TPMLP_OP_SP_FWD_FP8 || op == TPMLP_OP_SP_BWD_FP8;
   const bool bf16_only = op != TPMLP_OP_FWD;
   tpmlp_status st = check_shape(shape, sp, bf16_only);
   if (st != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
-  if (op < TPMLP_OP_FWD || op > TPMLP_OP_SP_FWD_FP8) return TPMLP_ERR_INVALID_ARG;
-  if (op == TPMLP_OP_SP_FWD_FP8 && (shape->d % 16 != 0 || shape->ffn % 16 != 0)) return TPMLP_ERR_INVALID_ARG;
+  if (op < TPMLP_OP_FWD || op > TPMLP_OP_SP_BWD_FP8) return TPMLP_ERR_INVALID_ARG;
+  if ((op == TPMLP_OP_SP_FWD_FP8 || op == TPMLP_OP_SP_BWD_FP8) && (shape->d % 16 != 0 || shape->ffn % 16 != 0))
+    return TPMLP_ERR_INVALID_ARG;
+  if (op == TPMLP_OP_SP_BWD_FP8 && shape->tokens % 16 != 0) return TPMLP_ERR_INVALID_ARG;
   *bytes = ws_bytes(shape, op);
   return TPMLP_OK;
 }
@@ -1025,14 +1075,15 @@ tpmlp_status tpmlp_fp8_update_scales(const tpmlp_fp8_state* state, tpmlp_stream_
 
 tpmlp_status tpmlp_sp_forward_fp8(const void* const* X_chunks, const void* gamma, const void* beta, float eps,
                                   const void* A, const void* B, const void* bias, const tpmlp_fp8_state* state,
-                                  const tpmlp_shape* shape, void* const* Y_chunks, void* workspace,
-                                  size_t workspace_bytes, tpmlp_stream_t stream) {
+                                  const tpmlp_shape* shape, void* const* Y_chunks, void* Hpre_out, void* Xq_out,
+                                  void* Hq_out, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if ((st = check_fp8(shape)) != TPMLP_OK) return st;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   if (!ptrs_ok({gamma, beta, A, B}) || !opt_ok(bias) || !chunks_ok(X_chunks, shape->n_shards) ||
-      !chunks_ok(Y_chunks, shape->n_shards) || !(eps >= 0.f) || !fp8_state_ok(state))
+      !chunks_ok(Y_chunks, shape->n_shards) || !(eps >= 0.f) || !fp8_state_ok(state) || !opt_ok(Hpre_out) ||
+      !opt_ok(Xq_out) || !opt_ok(Hq_out))
     return TPMLP_ERR_INVALID_ARG;
   if (!fp8_ln_width(shape->d) || (shape->ffn + 63) / 64 > 65535 || (shape->d + 63) / 64 > 65535)
     return TPMLP_ERR_UNSUPPORTED;
@@ -1047,16 +1098,154 @@ tpmlp_status tpmlp_sp_forward_fp8(const void* const* X_chunks, const void* gamma
   void* BqT = ws.take(z.df8);
   void* Xq = ws.take(z.td8);
   void* Hq = ws.take(z.tf8);
+  if (Xq_out != nullptr) Xq = Xq_out;
+  if (Hq_out != nullptr) Hq = Hq_out;
   float* sc = state->scale;
   float* am = state->amax;
   const int d = static_cast<int>(shape->d), F = static_cast<int>(shape->ffn);
   cudaError_t e = launch_cast_e4m3(A, d, F, true, sc + 1, AqT, am + 1, s);
   if (e == cudaSuccess) e = launch_cast_e4m3(B, F, d, true, sc + 2, BqT, am + 2, s);
   if (e == cudaSuccess) e = do_ln_e4m3(X_chunks, gamma, beta, eps, shape, sc + 0, Xq, am + 0, s);
-  if (e == cudaSuccess) e = do_gemm1_e4m3(c, Xq, AqT, bias, shape, sc + 0, sc + 1, sc + 3, Hq, am + 3, nullptr, s);
+  if (e == cudaSuccess) e = do_gemm1_e4m3(c, Xq, AqT, bias, shape, sc + 0, sc + 1, sc + 3, Hq, am + 3, Hpre_out, s);
   if (e == cudaSuccess) e = do_gemm2_e4m3(c, Hq, BqT, shape, sc + 3, sc + 2, nullptr, Y_chunks, s);
+  return cuda_status(e);
+}
+
+tpmlp_status tpmlp_cast_e5m2(const void* src, int64_t rows, int64_t cols, int transpose, const float* scale, void* dst,
+                             float* amax, tpmlp_stream_t stream) {
+  if (rows < 0 || cols < 0 || rows % 16 != 0 || cols % 16 != 0 || rows > INT_MAX / 2 || cols > INT_MAX / 2)
+    return TPMLP_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return TPMLP_OK;
+  if (!ptrs_ok({src, dst}) || scale == nullptr || amax == nullptr) return TPMLP_ERR_INVALID_ARG;
+  if (transpose && (rows + 63) / 64 > 65535) return TPMLP_ERR_UNSUPPORTED;
+  return cuda_status(launch_cast_fp8(src, static_cast<int>(rows), static_cast<int>(cols), transpose != 0, 1, scale,
+                                     dst, amax, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_transpose_bytes(const void* src, int64_t rows, int64_t cols, void* dst, tpmlp_stream_t stream) {
+  if (rows < 0 || cols < 0 || rows % 16 != 0 || cols % 16 != 0 || rows > INT_MAX / 2 || cols > INT_MAX / 2)
+    return TPMLP_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return TPMLP_OK;
+  if (!ptrs_ok({src, dst})) return TPMLP_ERR_INVALID_ARG;
+  if ((rows + 63) / 64 > 65535) return TPMLP_ERR_UNSUPPORTED;
+  return cuda_status(launch_transpose_bytes(src, static_cast<int>(rows), static_cast<int>(cols), dst,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm_dh_geluprime_e5m2(const void* dYq, const void* Bq, const void* Hpre, const tpmlp_shape* shape,
+                                          const float* scale_dy, const float* scale_b, const float* scale_g,
+                                          void* dHq, float* amax_g, void* dbias, void* workspace,
+                                          size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, false, true);
+  if (st != TPMLP_OK) return st;
+  if ((st = check_fp8(shape)) != TPMLP_OK) return st;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({dYq, Bq, Hpre, dHq}) || !opt_ok(dbias) || scale_dy == nullptr || scale_b == nullptr ||
+      scale_g == nullptr)
+    return TPMLP_ERR_INVALID_ARG;
+  if (dbias != nullptr && (workspace == nullptr || !al16(workspace) ||
+                           workspace_bytes < ws_bytes(shape, TPMLP_OP_DH_GELUPRIME)))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_dh_e5m2(c, dYq, Bq, Hpre, shape, scale_dy, scale_b, scale_g, dHq, amax_g, dbias,
+                                static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_gemm_fp8(const void* A8, int a_fmt, const void* B8, int b_fmt, int64_t M, int64_t N, int64_t K,
+                            const float* scale_a, const float* scale_b, void* C, int64_t ldc, tpmlp_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || M > INT_MAX / 2 || N > INT_MAX / 2 || K > INT_MAX / 2 || K % 16 != 0 ||
+      N % 8 != 0 || ldc < N || ldc % 8 != 0 || (a_fmt != 0 && a_fmt != 1) || (b_fmt != 0 && b_fmt != 1))
+    return TPMLP_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return TPMLP_OK;
+  if (!ptrs_ok({A8, B8, C}) || scale_a == nullptr || scale_b == nullptr || K == 0) return TPMLP_ERR_INVALID_ARG;
+  DeviceCtx c;
+  tpmlp_status st;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  return cuda_status(do_gemm_fp8(c, A8, a_fmt, B8, b_fmt, static_cast<int>(M), static_cast<int>(N),
+                                 static_cast<int>(K), scale_a, scale_b, C, ldc,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_sp_backward_fp8(const void* const* X_chunks, const void* gamma, float eps, const void* A,
+                                   const void* B, const void* Hpre, const void* Xq, const void* Hq,
+                                   const void* const* dY_chunks, const tpmlp_fp8_state* fwd,
+                                   const tpmlp_fp8_state* grad, const tpmlp_shape* shape, void* const* dX_chunks,
+                                   void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
+                                   size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if ((st = check_fp8(shape)) != TPMLP_OK) return st;
+  if (shape->tokens % 16 != 0) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  const int n = shape->n_shards;
+  if (!ptrs_ok({gamma, A, B, Hpre, Xq, Hq, dA, dB, dgamma, dbeta}) || !opt_ok(dbias) || !chunks_ok(X_chunks, n) ||
+      !chunks_ok(dY_chunks, n) || !chunks_ok(dX_chunks, n) || !(eps >= 0.f) || !fp8_state_ok(fwd) ||
+      !fp8_state_ok(grad))
+    return TPMLP_ERR_INVALID_ARG;
+  if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
+  const int T = static_cast<int>(shape->tokens), d = static_cast<int>(shape->d), F = static_cast<int>(shape->ffn);
+  if ((T + 63) / 64 > 65535 || (F + 63) / 64 > 65535 || (d + 63) / 64 > 65535) return TPMLP_ERR_UNSUPPORTED;
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < ws_bytes(shape, TPMLP_OP_SP_BWD_FP8))
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Sizes z = sizes_of(shape);
+  Carve ws(workspace);
+  void* dYg = ws.take(z.td);
+  void* dXg = ws.take(z.td);
+  void* dYq = ws.take(z.td8);
+  void* dYqT = ws.take(z.td8);
+  void* XqT = ws.take(z.td8);
+  void* Aq = ws.take(z.df8);
+  void* Bq = ws.take(z.df8);
+  void* dHq = ws.take(z.tf8);
+  void* HqT = ws.take(z.tf8);
+  void* dHqT = ws.take(z.tf8);
+  float* colsum = static_cast<float*>(ws.take(z.colsum));
+  float* lnpart = static_cast<float*>(ws.take(z.lnbwd));
+  const float* fs = fwd->scale;
+  float* fa = fwd->amax;
+  const float* gs = grad->scale;
+  float* ga = grad->amax;
+  // dY gathered (free when the chunks lie back to back), then E5M2 in both layouts
+  cudaError_t e = cudaSuccess;
+  const void* dY = dY_chunks[0];
+  const size_t chunk_bytes = static_cast<size_t>(T / n) * d * 2;
+  bool contiguous = true;
+  for (int j = 1; j < n; ++j)
+    contiguous = contiguous && static_cast<const uint8_t*>(dY_chunks[j]) ==
+                                   static_cast<const uint8_t*>(dY_chunks[0]) + j * chunk_bytes;
+  if (!contiguous) {
+    RowParams r{};
+    r.in_chunks = to_const_chunks(dY_chunks, n);
+    r.rows = T;
+    r.d = d;
+    r.n_chunks = n;
+    r.rows_per_chunk = T / n;
+    r.dst = dYg;
+    if ((e = launch_gather_rows(r, c, s)) != cudaSuccess) return cuda_status(e);
+    dY = dYg;
+  }
+  if (e == cudaSuccess) e = launch_cast_fp8(dY, T, d, false, 1, gs + 0, dYq, ga + 0, s);
+  if (e == cudaSuccess) e = launch_cast_fp8(dY, T, d, true, 1, gs + 0, dYqT, ga + 0, s);
+  // the weights as stored, E4M3 with the forward's scales
+  if (e == cudaSuccess) e = launch_cast_fp8(A, d, F, false, 0, fs + 1, Aq, fa + 1, s);
+  if (e == cudaSuccess) e = launch_cast_fp8(B, F, d, false, 0, fs + 2, Bq, fa + 2, s);
+  // dHpre = (dY B^T) * GeLU'(Hpre) in E5M2, and db
+  if (e == cudaSuccess) e = do_dh_e5m2(c, dYq, Bq, Hpre, shape, gs + 0, fs + 2, gs + 1, dHq, ga + 1, dbias, colsum, s);
+  // K-major copies for the weight gradients (K = T)
+  if (e == cudaSuccess) e = launch_transpose_bytes(Hq, T, F, HqT, s);
+  if (e == cudaSuccess) e = launch_transpose_bytes(Xq, T, d, XqT, s);
+  if (e == cudaSuccess) e = launch_transpose_bytes(dHq, T, F, dHqT, s);
+  // dB = H^T dY [F x d]; dA = Xg^T dHpre [d x F]; dXg = dHpre A^T [T x d] (the backward shard sum over K = F)
+  if (e == cudaSuccess) e = do_gemm_fp8(c, HqT, 0, dYqT, 1, F, d, T, fs + 3, gs + 0, dB, d, s);
+  if (e == cudaSuccess) e = do_gemm_fp8(c, XqT, 0, dHqT, 1, d, F, T, fs + 0, gs + 1, dA, F, s);
+  if (e == cudaSuccess) e = do_gemm_fp8(c, dHq, 1, Aq, 0, T, d, F, gs + 1, fs + 1, dXg, d, s);
+  if (e == cudaSuccess) e = do_ln_bwd(c, X_chunks, gamma, eps, dXg, shape, dX_chunks, dgamma, dbeta, lnpart, s);
   if (e == cudaSuccess)
-    e = launch_fp8_update(state->scale, state->amax, state->history, 4, state->history_len, 448.f, state->margin, s);
+    e = launch_fp8_update(grad->scale, grad->amax, grad->history, 2, grad->history_len, 57344.f, grad->margin, s);
   return cuda_status(e);
 }
 

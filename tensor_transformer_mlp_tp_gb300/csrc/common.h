@@ -36,6 +36,8 @@ enum Epilogue : int {
   kEpiDGelu = 3,      // out0 = bf16(acc * GeLU'(aux)); out1 = bf16(GeLU(aux)); optional column sums
   kEpiBiasGeluQ = 4,  // out0 = E4M3(GeLU(acc + bias) * scale_out), amax_out = max |GeLU(acc + bias)|;
                       // out1 (optional) = bf16(acc + bias)
+  kEpiDGeluQ = 5,     // g = acc * GeLU'(aux): out0 = E5M2(g * scale_out), amax_out = max |g|, optional
+                      // column sums of g
 };
 
 struct ChunkPtrs {
@@ -81,6 +83,7 @@ struct GemmParams {
   const float* scale_b;
   const float* scale_out;
   float* amax_out;
+  int a_fmt, b_fmt;           // 8-bit operand formats (0 = E4M3, 1 = E5M2)
   unsigned int* err;
   unsigned long long timeout_ns;
 };

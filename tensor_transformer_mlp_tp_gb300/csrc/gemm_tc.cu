@@ -122,7 +122,8 @@ bool pair_enabled() {
 static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s) {
   if (g.a.mn_major || g.b.mn_major || g.shards > 1) return cudaErrorNotSupported;
   if (g.scale_a == nullptr || g.scale_b == nullptr) return cudaErrorInvalidValue;
-  if (g.epi == kEpiBiasGeluQ && g.scale_out == nullptr) return cudaErrorInvalidValue;
+  if ((g.epi == kEpiBiasGeluQ || g.epi == kEpiDGeluQ) && g.scale_out == nullptr) return cudaErrorInvalidValue;
+  if (g.a_fmt < 0 || g.a_fmt > 1 || g.b_fmt < 0 || g.b_fmt > 1) return cudaErrorInvalidValue;
   constexpr int kKb = 128;
   GemmParams p;
   memset(&p, 0, sizeof(p));
@@ -142,6 +143,9 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   p.out1 = g.out1;
   p.ld1 = g.ld1;
   p.bias = g.bias;
+  p.aux = g.aux;
+  p.ld_aux = g.ld_aux;
+  p.colsum = g.colsum;
   p.rows_per_chunk = g.rows_per_chunk;
   p.chunks = g.chunks;
   p.tail = g.tail.on && g.rows_per_chunk > 0 && g.epi == kEpiStore ? 1 : 0;
@@ -151,6 +155,8 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   p.drop_offset = g.tail.offset;
   p.drop_thr = g.tail.thr;
   p.res_chunks = g.tail.residual;
+  p.a_fmt = g.a_fmt;
+  p.b_fmt = g.b_fmt;
   p.scale_a = g.scale_a;
   p.scale_b = g.scale_b;
   p.scale_out = g.scale_out;
@@ -159,6 +165,7 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   p.timeout_ns = ctx.timeout_ns;
   switch (g.epi) {
     case kEpiBiasGeluQ: return run_pair<false, false, kEpiBiasGeluQ, true>(p, s);
+    case kEpiDGeluQ: return run_pair<false, false, kEpiDGeluQ, true>(p, s);
     case kEpiStore: return run_pair<false, false, kEpiStore, true>(p, s);
     default: return cudaErrorNotSupported;
   }

@@ -123,15 +123,17 @@ struct EpiState {
   float amax;
 };
 
-// E4M3(x * s) for 32 values -> 32 bytes of one row (columns at or beyond N, a multiple of 16, skipped).
-__device__ __forceinline__ void store_row32_e4m3(uint8_t* row_ptr, int col0, int N, const float (&x)[32], float s) {
+// FP8(x * s) for 32 values -> 32 bytes of one row (columns at or beyond N, a multiple of 16, skipped);
+// FMT 0 = E4M3, 1 = E5M2.
+template <int FMT>
+__device__ __forceinline__ void store_row32_fp8(uint8_t* row_ptr, int col0, int N, const float (&x)[32], float s) {
   uint4* d = reinterpret_cast<uint4*>(row_ptr + col0);
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     if (col0 + 16 * g < N) {
       const float* y = x + 16 * g;
-      d[g] = make_uint4(e4m3x4(y[0], y[1], y[2], y[3], s), e4m3x4(y[4], y[5], y[6], y[7], s),
-                        e4m3x4(y[8], y[9], y[10], y[11], s), e4m3x4(y[12], y[13], y[14], y[15], s));
+      d[g] = make_uint4(fp8x4<FMT>(y[0], y[1], y[2], y[3], s), fp8x4<FMT>(y[4], y[5], y[6], y[7], s),
+                        fp8x4<FMT>(y[8], y[9], y[10], y[11], s), fp8x4<FMT>(y[12], y[13], y[14], y[15], s));
     }
   }
 }
@@ -191,8 +193,8 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
         v[i] = gelu_f(v[i]);
         if (col0 + i < p.N) st.amax = fmaxf(st.amax, fabsf(v[i]));
       }
-      store_row32_e4m3(static_cast<uint8_t*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v,
-                       st.scale_out);
+      store_row32_fp8<0>(static_cast<uint8_t*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v,
+                         st.scale_out);
     }
   } else if constexpr (EPI == kEpiBiasGelu || EPI == kEpiBias) {
     if (p.bias != nullptr) {
@@ -221,6 +223,27 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       }
       store_row32(dst, col0, p.N, v);
     }
+  } else if constexpr (EPI == kEpiDGeluQ) {
+    // v = dH (dequantised); aux = Hpre.  g = dH * GeLU'(Hpre) -> E5M2 with the output scale, amax, column sums.
+    float h[32];
+    unpack_row32(aux_raw, h);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float x = h[i];
+      const NormalCdfPdf n = normal_cdf_pdf(x);
+      v[i] = row_ok && col0 + i < p.N ? v[i] * (n.cdf + x * n.pdf) : 0.f;
+      st.amax = fmaxf(st.amax, fabsf(v[i]));
+    }
+    if (row_ok)
+      store_row32_fp8<1>(static_cast<uint8_t*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v,
+                         st.scale_out);
+    if (p.colsum != nullptr) {
+      const float s = warp_column_sums(v, lane);
+      const int col = col0 + static_cast<int>(lane);
+      // a 128-row block that starts at or past row M (the odd CTA of a last, half-empty pair tile) writes
+      // nothing: the partial rows stay 4 per 128-row block of M
+      if (col < p.N && mb * kBM < p.M) p.colsum[static_cast<long long>(mb * 4 + quad) * p.N + col] = s;
+    }
   } else if constexpr (EPI == kEpiDGelu) {
     // v = dH = dY B^T; aux = Hpre.  dHpre = dH * (Phi(h) + h phi(h)); with out1 also H = h Phi(h),
     // Phi and phi sharing one exponential.
@@ -243,7 +266,9 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
     if (p.colsum != nullptr) {
       const float s = warp_column_sums(v, lane);
       const int col = col0 + static_cast<int>(lane);
-      if (col < p.N) p.colsum[static_cast<long long>(mb * 4 + quad) * p.N + col] = s;
+      // a 128-row block that starts at or past row M (the odd CTA of a last, half-empty pair tile) writes
+      // nothing: the partial rows stay 4 per 128-row block of M
+      if (col < p.N && mb * kBM < p.M) p.colsum[static_cast<long long>(mb * 4 + quad) * p.N + col] = s;
     }
   }
 }

@@ -52,7 +52,8 @@ struct PairShape {
 template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS, bool FP8 = false>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __grid_constant__ GemmParams p) {
   static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
-  static_assert(FP8 || EPI != kEpiBiasGeluQ, "the quantising epilogue follows FP8 operands");
+  static_assert(FP8 || (EPI != kEpiBiasGeluQ && EPI != kEpiDGeluQ), "the quantising epilogues follow FP8 operands");
+  constexpr bool kAux = EPI == kEpiDGelu || EPI == kEpiDGeluQ;  // reads the pre-activation tile
   constexpr int kKElems = FP8 ? 128 : kBK;  // elements of one 128-byte k-block row
   using S = PairShape<BN, STAGES, EPI_WARPS>;
   extern __shared__ uint8_t smem_raw[];
@@ -168,8 +169,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------------ MMA issuer (even CTA)
-      constexpr uint32_t idesc = FP8 ? idesc_f8_f32(256, BN, kFmtE4M3, kFmtE4M3, false, false)
-                                     : idesc_bf16_f32(256, BN, A_MN, B_MN);
+      const uint32_t idesc = FP8 ? idesc_f8_f32(256, BN, static_cast<uint32_t>(p.a_fmt),
+                                                static_cast<uint32_t>(p.b_fmt), false, false)
+                                 : idesc_bf16_f32(256, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
     float* stage_base = staging + quad * (2 * 32 * 32);    // valid for quadrants 0 and 1
     EpiState est{1.f, 1.f, 0.f};
     if constexpr (FP8) est.descale = 1.f / (__ldg(p.scale_a) * __ldg(p.scale_b));
-    if constexpr (EPI == kEpiBiasGeluQ) est.scale_out = __ldg(p.scale_out);
+    if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) est.scale_out = __ldg(p.scale_out);
     uint32_t chunk_ctr = 0;
     int local = 0;
     bool ok_all = true;
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
       const uint32_t acc_phase = (local >> 1) & 1;
       const int mb128 = mb * 2 + static_cast<int>(rank);
       const int row = mb128 * 128 + quad * 32 + static_cast<int>(lane);
-      if constexpr (EPI == kEpiDGelu) {
+      if constexpr (kAux) {
         // While this tile's MMAs run, pull the warp's 32 rows of the pre-activation tile into L2.
         if (!reader && row < p.M) {
           const int pcol = nb * BN;
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       const __nv_bfloat16* aux_row = nullptr;
       uint4 aux_next[4] = {};
-      if constexpr (EPI == kEpiDGelu) {
+      if constexpr (kAux) {
         if (!reader) {
           aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
           load_raw32(aux_row, nb * BN, p.N, row < p.M, aux_next);
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
         uint4 aux_cur[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) aux_cur[g] = aux_next[g];
-        if constexpr (EPI == kEpiDGelu) {
+        if constexpr (kAux) {
           if (c + 32 < BN) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
         }
         if (helper) {
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
       }
     }
-    if constexpr (EPI == kEpiBiasGeluQ) {
+    if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) {
       if (p.amax_out != nullptr) amax_combine_warp(p.amax_out, est.amax);
     }
   }

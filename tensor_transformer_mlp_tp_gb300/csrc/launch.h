@@ -48,8 +48,9 @@ struct GemmLaunch {
   bool fp8 = false;
   const float* scale_a = nullptr;
   const float* scale_b = nullptr;
-  const float* scale_out = nullptr;  // kEpiBiasGeluQ
-  float* amax_out = nullptr;         // kEpiBiasGeluQ
+  const float* scale_out = nullptr;  // kEpiBiasGeluQ, kEpiDGeluQ
+  float* amax_out = nullptr;         // kEpiBiasGeluQ, kEpiDGeluQ
+  int a_fmt = 0, b_fmt = 0;          // 0 = E4M3, 1 = E5M2
 };
 
 struct DeviceCtx {
@@ -88,6 +89,11 @@ cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* ou
 // or, with `transpose`, [cols x rows]; *amax is max-combined with max |src|.  Row lengths multiples of 16.
 cudaError_t launch_cast_e4m3(const void* src, int rows, int cols, bool transpose, const float* scale, void* dst,
                              float* amax, cudaStream_t s);
+// The same cast to E5M2 (fmt 1) or E4M3 (fmt 0).
+cudaError_t launch_cast_fp8(const void* src, int rows, int cols, bool transpose, int fmt, const float* scale,
+                            void* dst, float* amax, cudaStream_t s);
+// dst [cols x rows] bytes = the transpose of src [rows x cols] bytes (rows, cols multiples of 16).
+cudaError_t launch_transpose_bytes(const void* src, int rows, int cols, void* dst, cudaStream_t s);
 // LayerNorm of every chunk, written as E4M3(LN(x) * (*scale)) into the gathered [T x d] byte buffer
 // r.dst; *amax max-combined with max |LN(x)|.
 cudaError_t launch_layernorm_fwd_e4m3(const RowParams& r, const float* scale, float* amax, cudaStream_t s);

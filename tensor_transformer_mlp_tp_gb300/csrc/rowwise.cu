@@ -670,9 +670,11 @@ __global__ void __launch_bounds__(256) k_column_sum(const float* __restrict__ pa
 
 // ----------------------------------------------------------------------------- E4M3 casts and delayed scaling
 
-// dst[i] = E4M3(src[i] * s), 16 elements (two 16-byte loads, one 16-byte store) per step, grid-stride.
-__global__ void __launch_bounds__(256) k_cast_e4m3(const __nv_bfloat16* __restrict__ src, long long n16,
-                                                   const float* scale, uint8_t* __restrict__ dst, float* amax) {
+// dst[i] = FP8(src[i] * s), 16 elements (two 16-byte loads, one 16-byte store) per step, grid-stride.
+// FMT 0 = E4M3, 1 = E5M2.
+template <int FMT>
+__global__ void __launch_bounds__(256) k_cast_fp8(const __nv_bfloat16* __restrict__ src, long long n16,
+                                                  const float* scale, uint8_t* __restrict__ dst, float* amax) {
   const float s = __ldg(scale);
   float m = 0.f;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
@@ -682,7 +684,7 @@ __global__ void __launch_bounds__(256) k_cast_e4m3(const __nv_bfloat16* __restri
     unpack8(__ldg(reinterpret_cast<const uint4*>(src) + 2 * i + 1), b);
 #pragma unroll
     for (int e = 0; e < 8; ++e) m = fmaxf(m, fmaxf(fabsf(a[e]), fabsf(b[e])));
-    const uint2 lo = e4m3x8(a, s), hi = e4m3x8(b, s);
+    const uint2 lo = fp8x8<FMT>(a, s), hi = fp8x8<FMT>(b, s);
     reinterpret_cast<uint4*>(dst)[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
   }
   amax_combine_warp(amax, m);
@@ -692,8 +694,9 @@ __global__ void __launch_bounds__(256) k_cast_e4m3(const __nv_bfloat16* __restri
 // (rows, cols multiples of 16).  Loads: 16-byte vectors along the source row; stores: 16 bytes of one
 // destination row (16 consecutive source rows of one column).
 constexpr int kCastTile = 64;
-__global__ void __launch_bounds__(256) k_cast_e4m3_t(const __nv_bfloat16* __restrict__ src, int rows, int cols,
-                                                     const float* scale, uint8_t* __restrict__ dst, float* amax) {
+template <int FMT>
+__global__ void __launch_bounds__(256) k_cast_fp8_t(const __nv_bfloat16* __restrict__ src, int rows, int cols,
+                                                    const float* scale, uint8_t* __restrict__ dst, float* amax) {
   __shared__ float tile[kCastTile][kCastTile + 1];
   const float s = __ldg(scale);
   const int r0 = blockIdx.y * kCastTile, c0 = blockIdx.x * kCastTile;
@@ -722,13 +725,38 @@ __global__ void __launch_bounds__(256) k_cast_e4m3_t(const __nv_bfloat16* __rest
 #pragma unroll
     for (int i = 0; i < 16; ++i) f[i] = tile[rb + i][oc];
     uint4 o;
-    o.x = e4m3x4(f[0], f[1], f[2], f[3], s);
-    o.y = e4m3x4(f[4], f[5], f[6], f[7], s);
-    o.z = e4m3x4(f[8], f[9], f[10], f[11], s);
-    o.w = e4m3x4(f[12], f[13], f[14], f[15], s);
+    o.x = fp8x4<FMT>(f[0], f[1], f[2], f[3], s);
+    o.y = fp8x4<FMT>(f[4], f[5], f[6], f[7], s);
+    o.z = fp8x4<FMT>(f[8], f[9], f[10], f[11], s);
+    o.w = fp8x4<FMT>(f[12], f[13], f[14], f[15], s);
     *reinterpret_cast<uint4*>(dst + static_cast<long long>(c0 + oc) * rows + r0 + rb) = o;
   }
   amax_combine_warp(amax, m);
+}
+
+// dst [cols x rows] = transpose of src [rows x cols], bytes; 64 x 64 tiles, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) k_transpose_bytes(const uint8_t* __restrict__ src, int rows, int cols,
+                                                         uint8_t* __restrict__ dst) {
+  __shared__ uint8_t tile[kCastTile][kCastTile + 4];
+  const int r0 = blockIdx.y * kCastTile, c0 = blockIdx.x * kCastTile;
+  const int t = threadIdx.x;
+  {
+    const int r = t / 4, cb = (t % 4) * 16;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r0 + r < rows && c0 + cb < cols)
+      v = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * cols + c0 + cb));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) tile[r][cb + i] = static_cast<uint8_t>(w[i / 4] >> (8 * (i % 4)));
+  }
+  __syncthreads();
+  const int oc = t / 4, rb = (t % 4) * 16;
+  if (c0 + oc < cols && r0 + rb < rows) {
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i / 4] |= static_cast<uint32_t>(tile[rb + i][oc]) << (8 * (i % 4));
+    *reinterpret_cast<uint4*>(dst + static_cast<long long>(c0 + oc) * rows + r0 + rb) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 // One warp per tensor: shift the history by one (oldest out, this step's amax in), mean in a fixed order,
@@ -975,21 +1003,43 @@ cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* ou
 }
 
 
-cudaError_t launch_cast_e4m3(const void* src, int rows, int cols, bool transpose, const float* scale, void* dst,
-                             float* amax, cudaStream_t s) {
+cudaError_t launch_cast_fp8(const void* src, int rows, int cols, bool transpose, int fmt, const float* scale,
+                            void* dst, float* amax, cudaStream_t s) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
+  if (fmt != 0 && fmt != 1) return cudaErrorInvalidValue;
+  const auto* in = static_cast<const __nv_bfloat16*>(src);
+  auto* out = static_cast<uint8_t*>(dst);
   if (transpose) {
     const dim3 grid((cols + kCastTile - 1) / kCastTile, (rows + kCastTile - 1) / kCastTile);
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    k_cast_e4m3_t<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, scale,
-                                       static_cast<uint8_t*>(dst), amax);
+    if (fmt == 0) {
+      k_cast_fp8_t<0><<<grid, 256, 0, s>>>(in, rows, cols, scale, out, amax);
+    } else {
+      k_cast_fp8_t<1><<<grid, 256, 0, s>>>(in, rows, cols, scale, out, amax);
+    }
   } else {
     const long long n16 = static_cast<long long>(rows) * cols / 16;
     long long g = (n16 + 255) / 256;
     if (g > 152 * 8) g = 152 * 8;
-    k_cast_e4m3<<<static_cast<int>(g), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), n16, scale,
-                                                    static_cast<uint8_t*>(dst), amax);
+    if (fmt == 0) {
+      k_cast_fp8<0><<<static_cast<int>(g), 256, 0, s>>>(in, n16, scale, out, amax);
+    } else {
+      k_cast_fp8<1><<<static_cast<int>(g), 256, 0, s>>>(in, n16, scale, out, amax);
+    }
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_e4m3(const void* src, int rows, int cols, bool transpose, const float* scale, void* dst,
+                             float* amax, cudaStream_t s) {
+  return launch_cast_fp8(src, rows, cols, transpose, 0, scale, dst, amax, s);
+}
+
+cudaError_t launch_transpose_bytes(const void* src, int rows, int cols, void* dst, cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const dim3 grid((cols + kCastTile - 1) / kCastTile, (rows + kCastTile - 1) / kCastTile);
+  if (grid.y > 65535) return cudaErrorInvalidValue;
+  k_transpose_bytes<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(src), rows, cols, static_cast<uint8_t*>(dst));
   return cudaGetLastError();
 }
 

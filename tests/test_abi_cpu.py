@@ -129,7 +129,7 @@ def test_sp_region_workspace_sizes(lib):
         assert _ws(s, binding.OP_DROPOUT_BWD) == (binding.OK, dropcol)
         st, spb = _ws(s, binding.OP_SP_BWD)
         assert _ws(s, binding.OP_SP_BLOCK_BWD) == (binding.OK, spb + dropcol)
-    assert _ws(binding.make_shape(256, 64, 256, 2), 10)[0] == binding.ERR_INVALID_ARG
+    assert _ws(binding.make_shape(256, 64, 256, 2), 11)[0] == binding.ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("p", [1.0, -0.25, float("nan"), float("inf")])
@@ -196,3 +196,20 @@ def test_fp8_workspace_and_argument_checks(lib):
     chunks = ctypes.cast((ctypes.c_void_p * 2)(1 << 20, 1 << 21), binding._PP)
     assert L.tpmlp_layernorm_gather_e4m3(chunks, good, good, 1e-5, ctypes.byref(s), good, good, good, None) \
         == binding.ERR_UNSUPPORTED
+
+
+def test_fp8_backward_workspace_and_argument_checks(lib):
+    w = inputs.WORKLOADS["sp_block_fwd_bwd"]
+    s = binding.make_shape(w.T, w.d, w.F, w.N)
+    st, n = _ws(s, binding.OP_SP_BWD_FP8)
+    td, td8, tf8, df8 = _r256(w.T * w.d * 2), _r256(w.T * w.d), _r256(w.T * w.F), _r256(w.d * w.F)
+    assert st == binding.OK and n > 2 * td + 3 * td8 + 2 * df8 + 3 * tf8
+    assert _ws(binding.make_shape(200, 64, 256, 2), binding.OP_SP_BWD_FP8)[0] == binding.ERR_INVALID_ARG  # T % 16
+    L = binding.lib()
+    good = ctypes.c_void_p(1 << 20)
+    # formats other than E4M3 / E5M2, K not a multiple of 16, ldc < N
+    assert L.tpmlp_gemm_fp8(good, 2, good, 0, 256, 256, 256, good, good, good, 256, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_gemm_fp8(good, 0, good, 1, 256, 256, 200, good, good, good, 256, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_gemm_fp8(good, 0, good, 1, 256, 256, 256, good, good, good, 128, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_gemm_fp8(None, 0, None, 1, 0, 256, 256, None, None, None, 256, None) == binding.OK
+    assert L.tpmlp_transpose_bytes(good, 24, 64, good, None) == binding.ERR_INVALID_ARG

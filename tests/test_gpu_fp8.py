@@ -44,16 +44,36 @@ def f32dev(x):
     return torch.tensor(np.asarray(x, dtype=np.float32).reshape(-1), device="cuda")
 
 
-def _code_step_agreement(got, ref, min_equal=0.999):
-    """Codes equal on all but a tiny fraction; the rest one E4M3 step apart (neighbouring values)."""
+def _code_step_agreement(got, ref, min_equal=0.999, mant_bits=3, min_quantum=2.0 ** -9):
+    """Codes equal on all but a tiny fraction; the rest one format step apart (neighbouring values).
+    E4M3: 3 mantissa bits, smallest quantum 2**-9; E5M2: 2 bits, 2**-16."""
     eq = got == ref
     assert eq.mean() >= min_equal, eq.mean()
     if not eq.all():
         g, r = got[~eq], ref[~eq]
         hi = np.maximum(np.abs(g), np.abs(r))
-        # one step of E4M3 is at most 2**-3 of the larger magnitude (2**-9 for subnormals)
-        assert np.all(np.abs(g - r) <= np.maximum(hi * 2.0 ** -3, 2.0 ** -9) + 1e-30)
+        # one step is at most 2**-mant_bits of the larger magnitude (the subnormal quantum below that)
+        assert np.all(np.abs(g - r) <= np.maximum(hi * 2.0 ** -mant_bits, min_quantum) + 1e-30)
         assert np.all(np.sign(g) * np.sign(r) >= 0)
+
+
+def e5m2_values(t):
+    return t.cpu().view(torch.float8_e5m2).to(torch.float64).numpy()
+
+
+def e5m2_bytes(values):
+    t = torch.from_numpy(np.ascontiguousarray(values, dtype=np.float32)).to(torch.float8_e5m2)
+    assert np.array_equal(t.to(torch.float64).numpy(), values)
+    return t.view(torch.uint8).cuda()
+
+
+def assert_fp8_close(name, got, ref, maxrel=0.1, frob=2e-2):
+    """Block-level FP8 tolerance: where the GPU's fp32 value and the oracle's fp64 value of a tensor fall on
+    two sides of a rounding midpoint the two casts differ by one format step (up to 2**-3 of the element for
+    E4M3, 2**-2 for E5M2); a fraction of a percent of such flips moves the GEMM results by about 1%."""
+    from gpu_util import errors
+    m, f = errors(got, ref)
+    assert np.all(np.isfinite(got)) and m <= maxrel and f <= frob, f"{name}: max {m:.3e} frob {f:.3e}"
 
 
 @pytest.mark.parametrize("rows,cols,transpose", [(256, 1024, True), (4096, 320, True), (48, 80, True),
@@ -181,6 +201,7 @@ def test_sp_forward_fp8_block(T, d, F, N):
     Y = [Guarded((T // N, d)) for _ in range(N)]
     binding.tpmlp_sp_forward_fp8(list(dev(X[0]).split(T // N)), dev(g[0]), dev(be[0]), dev(A[0]), dev(B[0]), N,
                                  [y.t for y in Y], state, bias=dev(b[0]))
+    binding.tpmlp_fp8_update_scales(state)          # the step is over: delayed-scale update
     torch.cuda.synchronize()
     got = np.concatenate([f64(y.t) for y in Y])
     assert_bf16_close("Y (fp8)", got, np.concatenate(ref["Y_chunks"]))
@@ -197,3 +218,123 @@ def test_sp_forward_fp8_block(T, d, F, N):
         assert abs(float(scale[i].item()) / expect - 1) < 1e-5, k
     assert float(amax.abs().sum().item()) == 0.0
     assert all(y.intact() for y in Y)
+
+
+
+# ----------------------------------------------------------------------------- FP8 backward (E5M2 gradients)
+
+@pytest.mark.parametrize("rows,cols,transpose", [(256, 1024, True), (48, 80, True), (256, 1024, False)])
+def test_cast_e5m2_codes_are_bit_exact(rows, cols, transpose):
+    w = inputs.small_workload(64, 64, 2, name=f"cast5_{rows}_{cols}")
+    G = inputs.draw(w, "G", shape=(rows, cols), dist=(0.0, 3.0))
+    S = 57344.0 / np.max(np.abs(G[1])) * 0.5
+    scale, amax = f32dev([S]), torch.zeros(1, device="cuda")
+    out = torch.empty((cols, rows) if transpose else (rows, cols), dtype=torch.uint8, device="cuda")
+    binding.tpmlp_cast_e5m2(dev(G[0]), scale, out, amax, transpose=transpose)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_e5m2(G[1], S)
+    assert np.array_equal(e5m2_values(out), ref.T if transpose else ref)
+    assert float(amax.item()) == np.max(np.abs(G[1]))
+
+
+@pytest.mark.parametrize("rows,cols", [(256, 1024), (4096, 48), (80, 16)])
+def test_transpose_bytes(rows, cols):
+    src = torch.randint(0, 256, (rows, cols), dtype=torch.uint8, device="cuda")
+    dst = torch.empty(cols, rows, dtype=torch.uint8, device="cuda")
+    binding.tpmlp_transpose_bytes(src, dst)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), src.cpu().t().contiguous())
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [(binding.E4M3, binding.E5M2), (binding.E5M2, binding.E4M3),
+                                         (binding.E4M3, binding.E4M3), (binding.E5M2, binding.E5M2)])
+@pytest.mark.parametrize("M,N,K", [(512, 256, 1024), (320, 1056, 512), (64, 512, 2048)])
+def test_gemm_fp8_mixed_formats(a_fmt, b_fmt, M, N, K):
+    """Operands given as exact codes: the product of the codes divided by the scales, fp32 accumulation."""
+    w = inputs.small_workload(64, 64, 2, name=f"gq_{M}_{N}_{K}_{a_fmt}{b_fmt}")
+    Av = inputs.draw(w, "A8", shape=(M, K), dist=(0.0, 1.0))[1]
+    Bv = inputs.draw(w, "B8", shape=(N, K), dist=(0.0, 1.0))[1]
+    sa, sb = 64.0, 2048.0 / 3
+    q = {binding.E4M3: oracle.quantize_e4m3, binding.E5M2: oracle.quantize_e5m2}
+    enc = {binding.E4M3: e4m3_bytes, binding.E5M2: e5m2_bytes}
+    qa, qb = q[a_fmt](Av, sa), q[b_fmt](Bv, sb)
+    C = Guarded((M, N))
+    binding.tpmlp_gemm_fp8(enc[a_fmt](qa), a_fmt, enc[b_fmt](qb), b_fmt, f32dev([sa]), f32dev([sb]), C.t)
+    torch.cuda.synchronize()
+    ref = qa @ qb.T / (float(np.float32(sa)) * float(np.float32(sb)))
+    assert_bf16_close("C", f64(C.t), ref)
+    assert C.intact()
+
+
+@pytest.mark.parametrize("T,d,F,N", [(512, 256, 1024, 4), (320, 512, 1056, 4), (64, 1024, 2048, 2)])
+def test_gemm_dh_geluprime_e5m2(T, d, F, N):
+    w = inputs.small_workload(T, d, N, F=F, backward=True, name=f"dhq_{T}_{d}_{F}")
+    dY, B = inputs.draw(w, "dY"), inputs.draw(w, "B")
+    Hpre = inputs.draw(w, "Hpre", shape=(T, F), dist=(0.0, 2.0))
+    sdy, sb = 57344.0 / np.max(np.abs(dY[1])) / 2, 448.0 / np.max(np.abs(B[1]))
+    qdy, qb = oracle.quantize_e5m2(dY[1], sdy), oracle.quantize_e4m3(B[1], sb)
+    g = qdy @ qb.T / (float(np.float32(sdy)) * float(np.float32(sb))) * oracle.gelu_prime(Hpre[1])
+    sg = 57344.0 / np.max(np.abs(g)) / 2
+    dHq = Guarded((T, F), torch.uint8)
+    db = Guarded((F,))
+    amax = torch.zeros(1, device="cuda")
+    binding.tpmlp_gemm_dh_geluprime_e5m2(e5m2_bytes(qdy), e4m3_bytes(qb), dev(Hpre[0]), N, f32dev([sdy]),
+                                         f32dev([sb]), f32dev([sg]), dHq.t, amax, dbias=db.t)
+    torch.cuda.synchronize()
+    _code_step_agreement(e5m2_values(dHq.t), oracle.quantize_e5m2(g, sg), mant_bits=2, min_quantum=2.0 ** -16)
+    assert_bf16_close("db", f64(db.t), g.sum(axis=0))
+    assert abs(float(amax.item()) / np.max(np.abs(g)) - 1) < 1e-5
+    assert dHq.intact() and db.intact()
+
+
+@pytest.mark.parametrize("T,d,F,N", [(512, 256, 1024, 4), (256, 1024, 4096, 8), (64, 512, 1056, 2)])
+def test_sp_forward_backward_fp8_block(T, d, F, N):
+    """FP8 forward with saved Hpre / Xq / Hq, FP8 backward with E5M2 gradients, then both updates."""
+    w = inputs.small_workload(T, d, N, F=F, sp=True, backward=True, bias=(0.0, 0.2), name=f"spqb_{T}_{d}_{F}")
+    X, A, B, b, g, be, dY = (inputs.draw(w, n) for n in ("X", "A", "B", "bias", "gamma", "beta", "dY"))
+    Xo, dYo = _chunks(X[1], N), _chunks(dY[1], N)
+    first = oracle.sp_forward_fp8(Xo, g[1], be[1], 1e-5, A[1], B[1], b[1], N, (1.0, 1.0, 1.0, 1.0))["amax"]
+    s3 = [float(np.float32(448.0 / first[k])) for k in ("X", "A", "B")]
+    am = oracle.sp_forward_fp8(Xo, g[1], be[1], 1e-5, A[1], B[1], b[1], N, (*s3, 1.0))["amax"]
+    scales = (*s3, float(np.float32(448.0 / am["H"])))
+    gam = oracle.sp_backward_fp8(Xo, g[1], be[1], 1e-5, A[1], B[1], b[1], dYo, N, scales, (1.0, 1.0))["amax"]
+    gscales = (float(np.float32(57344.0 / gam["dY"] / 2)), float(np.float32(57344.0 / gam["dHpre"] / 2)))
+    ref = oracle.sp_backward_fp8(Xo, g[1], be[1], 1e-5, A[1], B[1], b[1], dYo, N, scales, gscales)
+
+    L = 4
+    fwd = binding.fp8_state(f32dev(scales), torch.zeros(4, device="cuda"), torch.ones(4, L, device="cuda"))
+    grad_scale, grad_amax = f32dev(gscales), torch.zeros(2, device="cuda")
+    grad_hist = torch.ones(2, L, device="cuda")
+    grad = binding.fp8_state(grad_scale, grad_amax, grad_hist)
+    rows = T // N
+    Xc = list(dev(X[0]).split(rows))
+    Ad, Bd, gd = dev(A[0]), dev(B[0]), dev(g[0])
+    Y = [torch.empty(rows, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    Hpre = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    Xq = torch.empty(T, d, dtype=torch.uint8, device="cuda")
+    Hq = torch.empty(T, F, dtype=torch.uint8, device="cuda")
+    binding.tpmlp_sp_forward_fp8(Xc, gd, dev(be[0]), Ad, Bd, N, Y, fwd, bias=dev(b[0]), Hpre_out=Hpre, Xq_out=Xq,
+                                 Hq_out=Hq)
+    dX = [Guarded((rows, d)) for _ in range(N)]
+    dA, dB, db = Guarded((d, F)), Guarded((F, d)), Guarded((F,))
+    dga, dbe = Guarded((d,), torch.float32), Guarded((d,), torch.float32)
+    binding.tpmlp_sp_backward_fp8(Xc, gd, Ad, Bd, Hpre, Xq, Hq, list(dev(dY[0]).split(rows)), N, fwd, grad,
+                                  [x.t for x in dX], dA.t, dB.t, dga.t, dbe.t, dbias=db.t)
+    torch.cuda.synchronize()
+    assert_fp8_close("dX", np.concatenate([f64(x.t) for x in dX]), np.concatenate(ref["dX_chunks"]))
+    for name, t, r in (("dA", dA, ref["dA"]), ("dB", dB, ref["dB"]), ("db", db, ref["db"]),
+                       ("dgamma", dga, ref["dgamma"]), ("dbeta", dbe, ref["dbeta"])):
+        assert_fp8_close(name, f64(t.t), r)
+    # against the unquantised backward the error is the formats' size
+    exact = oracle.sp_backward(Xo, g[1], be[1], 1e-5, A[1], B[1], b[1], dYo, N)
+    for name, got in (("dA", f64(dA.t)), ("dB", f64(dB.t))):
+        err = np.linalg.norm(got - exact[name]) / np.linalg.norm(exact[name])
+        assert err < 0.2, (name, err)
+    # the gradient state was updated (E5M2 maximum 57344), this step's amaxes reset
+    for i, k in enumerate(("dY", "dHpre")):
+        h = grad_hist[i].cpu().double().numpy()
+        assert abs(h[-1] / ref["amax"][k] - 1) < 1e-3, k
+        expect = oracle.fp8_scale(oracle.roll_amax_history(np.ones(L), ref["amax"][k]), fp8_max=57344.0)
+        assert abs(float(grad_scale[i].item()) / expect - 1) < 1e-3, k
+    assert float(grad_amax.abs().sum().item()) == 0.0
+    assert all(t.intact() for t in dX + [dA, dB, db, dga, dbe])
