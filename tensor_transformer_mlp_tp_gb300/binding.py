@@ -400,8 +400,12 @@ def tpmlp_layernorm_backward_noalloc(X_chunks, gamma, dXg, N, dX_chunks, dgamma,
 # ----------------------------------------------------------------------------- FP8 (E4M3) forward
 
 def fp8_state(scale, amax, history, margin=0):
-    """A tpmlp_fp8_state over device fp32 tensors scale [4], amax [4], history [4 x L]."""
-    return Fp8State(scale.data_ptr(), amax.data_ptr(), history.data_ptr(), history.shape[-1], margin)
+    """A tpmlp_fp8_state over device fp32 tensors scale [n], amax [n], history [n x L] (n = 4 for the
+    forward's X, A, B, H; 2 for the backward's dY, dHpre).  The returned struct holds references to the
+    tensors, so their memory stays allocated while the struct is alive."""
+    st = Fp8State(scale.data_ptr(), amax.data_ptr(), history.data_ptr(), history.shape[-1], margin)
+    st._tensors = (scale, amax, history)
+    return st
 
 
 def tpmlp_cast_e4m3(src, scale, dst, amax, transpose=False, stream=None):
