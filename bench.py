@@ -440,46 +440,79 @@ def time_calls(torch, fn, reps, warmup=3):
     return e0.elapsed_time(e1) / reps
 
 
-def run_fp8_forward(step, torch, binding, pk):
-    """The E4M3 forward on the step's shapes: weight casts, E4M3 LayerNorm, both E4M3 GEMMs and the
-    delayed-scale update, timed as a whole and per kernel.  The E4M3 tensor peak is the measured
-    sustained bf16 peak times the nominal dense FP8 : BF16 ratio of 2."""
+def run_fp8_step(step, torch, binding, pk):
+    """The FP8 path on the step's shapes: the E4M3 forward (weight casts, E4M3 LayerNorm, both E4M3 GEMMs),
+    the backward with E5M2 gradients (dY casts, weight casts, the E5M2 GeLU' GEMM, three byte transposes,
+    three FP8 GEMMs, the bf16 LayerNorm backward) and both delayed-scale updates, timed as a whole and per
+    GEMM.  The FP8 tensor peak is the measured sustained bf16 peak times the nominal dense FP8 : BF16
+    ratio of 2."""
     w = step.w
     T, d, F, N = w.T, w.d, w.F, w.N
     u8 = dict(dtype=torch.uint8, device="cuda")
-    scale = torch.ones(4, device="cuda")
-    amax = torch.zeros(4, device="cuda")
-    history = torch.zeros(4, 16, device="cuda")
-    state = binding.fp8_state(scale, amax, history)
-    ws = binding.workspace(binding.make_shape(T, d, F, N), binding.OP_SP_FWD_FP8)
-    # calibrate: a few steps fill the history, so the timed steps run on delayed scales of the real amaxes
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    fwd = binding.fp8_state(torch.ones(4, device="cuda"), torch.zeros(4, device="cuda"),
+                            torch.zeros(4, 16, device="cuda"))
+    grad = binding.fp8_state(torch.ones(2, device="cuda"), torch.zeros(2, device="cuda"),
+                             torch.zeros(2, 16, device="cuda"))
+    shape = binding.make_shape(T, d, F, N)
+    wsf = binding.workspace(shape, binding.OP_SP_FWD_FP8)
+    wsb = binding.workspace(shape, binding.OP_SP_BWD_FP8)
+    Hpre, Xq, Hq = torch.empty(T, F, **bf), torch.empty(T, d, **u8), torch.empty(T, F, **u8)
+    dA, dB, db = torch.empty(d, F, **bf), torch.empty(F, d, **bf), torch.empty(F, **bf)
+    dga, dbe = torch.empty(d, device="cuda"), torch.empty(d, device="cuda")
+
+    def forward():
+        binding.tpmlp_sp_forward_fp8(step.Xc, step.gamma, step.beta, step.A, step.B, N, step.Yc, fwd, bias=step.bias,
+                                     Hpre_out=Hpre, Xq_out=Xq, Hq_out=Hq, ws=wsf)
+
+    def train_step():
+        forward()
+        binding.tpmlp_sp_backward_fp8(step.Xc, step.gamma, step.A, step.B, Hpre, Xq, Hq, step.dYc, N, fwd, grad,
+                                      step.dXc, dA, dB, dga, dbe, dbias=db, ws=wsb)
+        binding.tpmlp_fp8_update_scales(fwd)
+
+    def forward_only():
+        forward()
+        binding.tpmlp_fp8_update_scales(fwd)
+
+    # calibrate: the first steps fill the amax histories, so the timed steps run on delayed scales of
+    # the real amaxes
     for _ in range(16):
-        binding.tpmlp_sp_forward_fp8(step.Xc, step.gamma, step.beta, step.A, step.B, N, step.Yc, state,
-                                     bias=step.bias, ws=ws)
-    ms_blk = time_calls(torch, lambda: binding.tpmlp_sp_forward_fp8(step.Xc, step.gamma, step.beta, step.A, step.B,
-                                                                     N, step.Yc, state, bias=step.bias, ws=ws), 20)
+        train_step()
+    ms_step = time_calls(torch, train_step, 10)
+    ms_fwd = time_calls(torch, forward_only, 10)
+    sc, am = fwd._tensors[0], fwd._tensors[1]
+    gsc, gam = grad._tensors[0], grad._tensors[1]
     AqT, BqT = torch.empty(F, d, **u8), torch.empty(d, F, **u8)
-    Xq, Hq = torch.empty(T, d, **u8), torch.empty(T, F, **u8)
-    sc = [scale[i:i + 1] for i in range(4)]
-    am = [amax[i:i + 1] for i in range(4)]
-    ms_ca = time_calls(torch, lambda: binding.tpmlp_cast_e4m3(step.A, sc[1], AqT, am[1], transpose=True), 10)
-    ms_cb = time_calls(torch, lambda: binding.tpmlp_cast_e4m3(step.B, sc[2], BqT, am[2], transpose=True), 10)
-    ms_ln = time_calls(torch, lambda: binding.tpmlp_layernorm_gather_e4m3(step.Xc, step.gamma, step.beta, N, sc[0],
-                                                                         Xq, am[0]), 20)
-    ms_g1 = time_calls(torch, lambda: binding.tpmlp_gemm1_e4m3(Xq, AqT, step.bias, N, sc[0], sc[1], sc[3], Hq,
-                                                                am[3]), 10)
-    ms_g2 = time_calls(torch, lambda: binding.tpmlp_gemm2_e4m3(Hq, BqT, N, sc[3], sc[2], Y_chunks=step.Yc), 10)
+    ms_ca = time_calls(torch, lambda: binding.tpmlp_cast_e4m3(step.A, sc[1:2], AqT, am[1:2], transpose=True), 10)
+    ms_cb = time_calls(torch, lambda: binding.tpmlp_cast_e4m3(step.B, sc[2:3], BqT, am[2:3], transpose=True), 10)
+    ms_g1 = time_calls(torch, lambda: binding.tpmlp_gemm1_e4m3(Xq, AqT, step.bias, N, sc[0:1], sc[1:2], sc[3:4], Hq,
+                                                                am[3:4]), 10)
+    ms_g2 = time_calls(torch, lambda: binding.tpmlp_gemm2_e4m3(Hq, BqT, N, sc[3:4], sc[2:3], Y_chunks=step.Yc), 10)
+    dYq, Bq, dHq = torch.empty(T, d, **u8), torch.empty(F, d, **u8), torch.empty(T, F, **u8)
+    binding.tpmlp_cast_e5m2(step.dY, gsc[0:1], dYq, gam[0:1])
+    binding.tpmlp_cast_e4m3(step.B, sc[2:3], Bq, am[2:3])
+    ms_dh = time_calls(torch, lambda: binding.tpmlp_gemm_dh_geluprime_e5m2(dYq, Bq, Hpre, N, gsc[0:1], sc[2:3],
+                                                                            gsc[1:2], dHq, gam[1:2]), 10)
+    HqT, dYqT = torch.empty(F, T, **u8), torch.empty(d, T, **u8)
+    ms_tr = time_calls(torch, lambda: binding.tpmlp_transpose_bytes(Hq, HqT), 10)
+    binding.tpmlp_cast_e5m2(step.dY, gsc[0:1], dYqT, gam[0:1], transpose=True)
+    ms_wb = time_calls(torch, lambda: binding.tpmlp_gemm_fp8(HqT, binding.E4M3, dYqT, binding.E5M2, sc[3:4],
+                                                              gsc[0:1], dB), 10)
     g = 2.0 * T * d * F
     peak8 = 2.0 * pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     tf = lambda ms: round(g / (ms * 1e-3) / 1e12, 1)
-    return {"ms": round(ms_blk, 4), "TFLOP/s": round(2 * g / (ms_blk * 1e-3) / 1e12, 1),
-            "launches": 6, "what": "tpmlp_sp_forward_fp8: 2 weight casts, E4M3 LayerNorm, 2 E4M3 GEMMs, scale update",
-            "gemm1_e4m3": {"ms": round(ms_g1, 4), "TFLOP/s": tf(ms_g1), "frac": round(tf(ms_g1) / peak8, 3)},
-            "gemm2_e4m3": {"ms": round(ms_g2, 4), "TFLOP/s": tf(ms_g2), "frac": round(tf(ms_g2) / peak8, 3)},
-            "cast_weights_ms": round(ms_ca + ms_cb, 4),
+    kern = lambda ms: {"ms": round(ms, 4), "TFLOP/s": tf(ms), "frac": round(tf(ms) / peak8, 3)}
+    return {"step_ms": round(ms_step, 4), "step_TFLOP/s": round(6 * g / (ms_step * 1e-3) / 1e12, 1),
+            "forward_ms": round(ms_fwd, 4), "forward_TFLOP/s": round(2 * g / (ms_fwd * 1e-3) / 1e12, 1),
+            "what": "tpmlp_sp_forward_fp8 + tpmlp_sp_backward_fp8 + tpmlp_fp8_update_scales (E4M3 forward, E5M2 "
+                    "gradients, delayed scaling), the flops of the six GEMMs over the whole step",
+            "gemm1_e4m3": kern(ms_g1), "gemm2_e4m3": kern(ms_g2), "dh_geluprime_e5m2": kern(ms_dh),
+            "wgrad_b_e4m3_e5m2": kern(ms_wb),
+            "cast_weights_transposed_ms": round(ms_ca + ms_cb, 4),
             "cast_weights_GB/s": round(3.0 * 2 * d * F / ((ms_ca + ms_cb) * 1e-3) / 1e9, 1),
-            "layernorm_e4m3_ms": round(ms_ln, 4),
-            "peak_e4m3_tflops": round(peak8, 1), "peak_kind": "2 x measured bf16 sustained (nominal FP8:BF16 ratio)"}
+            "transpose_H_ms": round(ms_tr, 4), "transpose_H_GB/s": round(2.0 * T * F / (ms_tr * 1e-3) / 1e9, 1),
+            "peak_fp8_tflops": round(peak8, 1), "peak_kind": "2 x measured bf16 sustained (nominal FP8:BF16 ratio)"}
 
 
 def run_other_rows(step, torch, binding, pk):
@@ -536,8 +569,9 @@ def run_other_rows(step, torch, binding, pk):
             out["dropout_backward"] = {"ms": round(ms_d, 4), "GB/s": round(nb / (ms_d * 1e-3) / 1e9, 1),
                                        "frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
                                        "bytes_per_launch": nb, "launches": 2}
-    if w.sp and w.d % 16 == 0 and w.F % 16 == 0 and w.d in (256, 512, 1024, 2048, 4096, 8192):
-        out["fp8_forward"] = run_fp8_forward(step, torch, binding, pk)
+    if (w.sp and w.backward and w.T % 16 == 0 and w.d % 16 == 0 and w.F % 16 == 0 and
+            w.d in (256, 512, 1024, 2048, 4096, 8192)):
+        out["fp8"] = run_fp8_step(step, torch, binding, pk)
     t = inputs.WORKLOADS["tiny_fp32_fwd"]
     f32 = lambda name: torch.from_numpy(np.ascontiguousarray(inputs.draw(t, name)[0])).cuda()
     X, A, B, b = f32("X"), f32("A"), f32("B"), f32("bias")
