@@ -54,6 +54,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
   static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
   static_assert(FP8 || (EPI != kEpiBiasGeluQ && EPI != kEpiDGeluQ), "the quantising epilogues follow FP8 operands");
   constexpr bool kAux = EPI == kEpiDGelu || EPI == kEpiDGeluQ;  // reads the pre-activation tile
+  // FP8 GEMMs with a GeLU / GeLU' epilogue are epilogue-bound at the doubled MMA rate: there every epilogue
+  // warp reads TMEM itself and the math is spread over all four SM sub-partitions (see the epilogue).
+  constexpr bool kBalanced = FP8 && (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ);
+  constexpr int kTemptyArrivals = 2 * (kBalanced ? EPI_WARPS + 2 : EPI_WARPS);
   constexpr int kKElems = FP8 ? 128 : kBK;  // elements of one 128-byte k-block row
   using S = PairShape<BN, STAGES, EPI_WARPS>;
   extern __shared__ uint8_t smem_raw[];
@@ -83,7 +87,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, 1);
-      mbar_init(tempty + a, 2 * EPI_WARPS);
+      mbar_init(tempty + a, kTemptyArrivals);
     }
     mbar_init(drain, 1);
     for (int i = 0; i < 4; ++i) {
@@ -214,6 +218,61 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
       umma_commit_pair(drain);
       wait_drain(drain, 0, p.timeout_ns);
     }
+  } else if constexpr (kBalanced) {
+    // -------------------------------------------------------------------- epilogue, balanced (both CTAs)
+    // Warps 2..5 own TMEM lane quadrants 2, 3, 0, 1; warps 6 and 7 (lane quadrants 2 and 3 as well) take
+    // the upper half of the columns of quadrants 2 and 3.  Sub-partition w % 4 then runs one quadrant's
+    // worth of math: warp 4 (next to the TMA producer) and warp 5 (next to the MMA issuer) all columns of
+    // theirs, warps 2 + 6 and 3 + 7 half each.
+    const int quad = warp & 3;
+    const int c_begin = warp >= 6 ? BN / 2 : 0;
+    const int c_end = (warp == 2 || warp == 3) ? BN / 2 : BN;
+    EpiState est{1.f / (__ldg(p.scale_a) * __ldg(p.scale_b)), __ldg(p.scale_out), 0.f};
+    int local = 0;
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+      int shard, mb, nb;
+      tile_coords(p, tile, shard, mb, nb);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      const int mb128 = mb * 2 + static_cast<int>(rank);
+      const int row = mb128 * 128 + quad * 32 + static_cast<int>(lane);
+      const __nv_bfloat16* aux_row = nullptr;
+      uint4 aux_next[4] = {};
+      if constexpr (kAux) {
+        // pull this warp's rows and columns of the pre-activation tile into L2 while the tile's MMAs run
+        const int pcol = nb * BN + c_begin;
+        const int ncols = min(c_end - c_begin, p.N - pcol);
+        if (row < p.M && ncols > 0)
+          prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row) * p.ld_aux + pcol,
+                           static_cast<uint32_t>(ncols) * 2u);
+      }
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tfull + acc, acc_phase, wc, kSiteEpiTmemFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (kAux) {
+        aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
+        load_raw32(aux_row, nb * BN + c_begin, p.N, row < p.M, aux_next);
+      }
+#pragma unroll 1
+      for (int c = c_begin; c < c_end; c += 32) {
+        uint4 aux_cur[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) aux_cur[g] = aux_next[g];
+        if constexpr (kAux) {
+          if (c + 32 < c_end) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
+        }
+        float v[32];
+        tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
+        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
+    }
+    if (p.amax_out != nullptr) amax_combine_warp(p.amax_out, est.amax);
   } else {
     // -------------------------------------------------------------------- epilogue (both CTAs)
     const bool quad_warp = warp < 6;

@@ -734,28 +734,33 @@ __global__ void __launch_bounds__(256) k_cast_fp8_t(const __nv_bfloat16* __restr
   amax_combine_warp(amax, m);
 }
 
-// dst [cols x rows] = transpose of src [rows x cols], bytes; 64 x 64 tiles, 16-byte loads and stores.
+// dst [cols x rows] = transpose of src [rows x cols], bytes, in registers.  A thread loads 16 bytes from
+// each of 4 consecutive rows, transposes the four 4 x 4 byte blocks with byte permutes and stores 16
+// words of 4 bytes (4 consecutive source rows of one column each).  A block covers 256 rows x 64 columns:
+// thread t takes rows 4 (t / 4) .. + 3 and columns 16 (t % 4) .. + 15; the stores of one destination row
+// by the 64 threads with the same t % 4 are 256 consecutive bytes.
+constexpr int kTrRows = 256, kTrCols = 64;
 __global__ void __launch_bounds__(256) k_transpose_bytes(const uint8_t* __restrict__ src, int rows, int cols,
                                                          uint8_t* __restrict__ dst) {
-  __shared__ uint8_t tile[kCastTile][kCastTile + 4];
-  const int r0 = blockIdx.y * kCastTile, c0 = blockIdx.x * kCastTile;
   const int t = threadIdx.x;
-  {
-    const int r = t / 4, cb = (t % 4) * 16;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r0 + r < rows && c0 + cb < cols)
-      v = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * cols + c0 + cb));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const int r = blockIdx.y * kTrRows + 4 * (t / 4);
+  const int c = blockIdx.x * kTrCols + 16 * (t % 4);
+  if (r >= rows || c >= cols) return;  // rows % 4 == 0 and cols % 16 == 0: a strip is wholly in or out
+  uint4 v[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) tile[r][cb + i] = static_cast<uint8_t>(w[i / 4] >> (8 * (i % 4)));
-  }
-  __syncthreads();
-  const int oc = t / 4, rb = (t % 4) * 16;
-  if (c0 + oc < cols && r0 + rb < rows) {
-    uint32_t w[4] = {0, 0, 0, 0};
+  for (int k = 0; k < 4; ++k) v[k] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r + k) * cols + c));
+  const uint32_t w[4][4] = {{v[0].x, v[0].y, v[0].z, v[0].w}, {v[1].x, v[1].y, v[1].z, v[1].w},
+                            {v[2].x, v[2].y, v[2].z, v[2].w}, {v[3].x, v[3].y, v[3].z, v[3].w}};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i / 4] |= static_cast<uint32_t>(tile[rb + i][oc]) << (8 * (i % 4));
-    *reinterpret_cast<uint4*>(dst + static_cast<long long>(c0 + oc) * rows + r0 + rb) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int q = 0; q < 4; ++q) {
+    // block q: bytes 4q .. 4q+3 of the four rows; word k of row k holds (row k, columns 4q .. 4q+3)
+    const uint32_t lo01 = __byte_perm(w[0][q], w[1][q], 0x5140), hi01 = __byte_perm(w[0][q], w[1][q], 0x7362);
+    const uint32_t lo23 = __byte_perm(w[2][q], w[3][q], 0x5140), hi23 = __byte_perm(w[2][q], w[3][q], 0x7362);
+    const uint32_t o[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                           __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      *reinterpret_cast<uint32_t*>(dst + static_cast<long long>(c + 4 * q + m) * rows + r) = o[m];
   }
 }
 
@@ -1037,7 +1042,7 @@ cudaError_t launch_cast_e4m3(const void* src, int rows, int cols, bool transpose
 
 cudaError_t launch_transpose_bytes(const void* src, int rows, int cols, void* dst, cudaStream_t s) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const dim3 grid((cols + kCastTile - 1) / kCastTile, (rows + kCastTile - 1) / kCastTile);
+  const dim3 grid((cols + kTrCols - 1) / kTrCols, (rows + kTrRows - 1) / kTrRows);
   if (grid.y > 65535) return cudaErrorInvalidValue;
   k_transpose_bytes<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(src), rows, cols, static_cast<uint8_t*>(dst));
   return cudaGetLastError();
