@@ -166,6 +166,175 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
   if constexpr (Q8) amax_combine_warp(p.amax, amax);
 }
 
+// LayerNorm forward, persistent and software-pipelined: each warp owns rows w, w + W, w + 2W, ...
+// (W = warps in the grid) and holds two rows in registers, loading the next while it normalises the
+// current, so the loads of the whole SM stay in flight while it computes (a launch-per-row-group kernel
+// instead idles the memory system during each group's compute phase).  d = 256 V.
+template <int V>
+__device__ __forceinline__ void ln_row_load(const RowParams& p, int row, int lane, uint4 (&x)[V]) {
+  if (row < p.rows) {
+    const uint4* src = reinterpret_cast<const uint4*>(chunk_row(p, row));
+#pragma unroll
+    for (int v = 0; v < V; ++v) x[v] = __ldg(src + v * 32 + lane);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void ln_row_store(const RowParams& p, int row, int lane, const uint4 (&x)[V],
+                                             const uint4* g4, const uint4* b4) {
+  float s = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    float f[8];
+    unpack8(x[v], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += f[e];
+  }
+  const float mean = warp_sum(s) / static_cast<float>(p.d);
+  float q = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    float f[8];
+    unpack8(x[v], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float c = f[e] - mean;
+      q += c * c;
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(q) / static_cast<float>(p.d) + p.eps);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + static_cast<long long>(row) * p.d);
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int idx = v * 32 + lane;
+    float f[8], g[8], b[8], o[8];
+    unpack8(x[v], f);
+    unpack8(g4[idx], g);
+    unpack8(b4[idx], b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+    dst[idx] = pack8(o);
+  }
+}
+
+template <int V>
+__global__ void __launch_bounds__(128) k_layernorm_fwd_pipe(const RowParams p) {
+  __shared__ uint4 gbs[2 * 32 * V];  // gamma, beta
+  for (int i = threadIdx.x; i < 32 * V; i += blockDim.x) {
+    gbs[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma) + i);
+    gbs[32 * V + i] = __ldg(reinterpret_cast<const uint4*>(p.beta) + i);
+  }
+  __syncthreads();
+  const uint4* g4 = gbs;
+  const uint4* b4 = gbs + 32 * V;
+  const int lane = threadIdx.x & 31;
+  const int W = gridDim.x * (blockDim.x >> 5);
+  int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  uint4 a[V], b[V];
+  ln_row_load<V>(p, row, lane, a);
+  // two rows per trip so that the two register sets keep fixed roles
+  while (row < p.rows) {
+    ln_row_load<V>(p, row + W, lane, b);
+    ln_row_store<V>(p, row, lane, a, g4, b4);
+    row += W;
+    if (row >= p.rows) break;
+    ln_row_load<V>(p, row + W, lane, a);
+    ln_row_store<V>(p, row, lane, b, g4, b4);
+    row += W;
+  }
+}
+
+// The same with two warps per row (warps 2k and 2k + 1 of a block, each 128 V columns of the 256 V):
+// the row statistics combine through shared memory and a named barrier per warp pair, double-buffered by
+// row parity.  d = 512 V.
+template <int V>
+__device__ __forceinline__ void ln_half_load(const RowParams& p, int row, int half, int lane, uint4 (&x)[V]) {
+  if (row < p.rows) {
+    const uint4* src = reinterpret_cast<const uint4*>(chunk_row(p, row)) + half * 32 * V;
+#pragma unroll
+    for (int v = 0; v < V; ++v) x[v] = __ldg(src + v * 32 + lane);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void ln_half_store(const RowParams& p, int row, int half, int pair, int lane, int par,
+                                              const uint4 (&x)[V], const uint4* g4, const uint4* b4,
+                                              float (*red)[4][2]) {
+  const int bar = 1 + pair;
+  float s = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    float f[8];
+    unpack8(x[v], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += f[e];
+  }
+  s = warp_sum(s);
+  if (lane == 0) red[par][pair * 2 + half][0] = s;
+  asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+  const float mean = (red[par][pair * 2][0] + red[par][pair * 2 + 1][0]) / static_cast<float>(p.d);
+  float q = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    float f[8];
+    unpack8(x[v], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float c = f[e] - mean;
+      q += c * c;
+    }
+  }
+  q = warp_sum(q);
+  if (lane == 0) red[par][pair * 2 + half][1] = q;
+  asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+  const float rstd = rsqrtf((red[par][pair * 2][1] + red[par][pair * 2 + 1][1]) / static_cast<float>(p.d) + p.eps);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + static_cast<long long>(row) * p.d) +
+               half * 32 * V;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int idx = half * 32 * V + v * 32 + lane;
+    float f[8], g[8], b[8], o[8];
+    unpack8(x[v], f);
+    unpack8(g4[idx], g);
+    unpack8(b4[idx], b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+    dst[v * 32 + lane] = pack8(o);
+  }
+}
+
+template <int V>
+__global__ void __launch_bounds__(128) k_layernorm_fwd_pipe2(const RowParams p) {
+  __shared__ uint4 gbs[2 * 64 * V];   // gamma, beta
+  __shared__ float red[2][4][2];      // [row parity][warp][sum, centred sum of squares]
+  for (int i = threadIdx.x; i < 64 * V; i += blockDim.x) {
+    gbs[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma) + i);
+    gbs[64 * V + i] = __ldg(reinterpret_cast<const uint4*>(p.beta) + i);
+  }
+  __syncthreads();
+  const uint4* g4 = gbs;
+  const uint4* b4 = gbs + 64 * V;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = warp >> 1, half = warp & 1;
+  const int W = gridDim.x * (blockDim.x >> 6);  // warp pairs in the grid
+  int row = blockIdx.x * (blockDim.x >> 6) + pair;
+  uint4 a[V], b[V];
+  ln_half_load<V>(p, row, half, lane, a);
+  int par = 0;
+  // both warps of a pair see the same rows, so they leave the loop together (the barriers stay matched)
+  while (row < p.rows) {
+    ln_half_load<V>(p, row + W, half, lane, b);
+    ln_half_store<V>(p, row, half, pair, lane, par, a, g4, b4, red);
+    row += W;
+    par ^= 1;
+    if (row >= p.rows) break;
+    ln_half_load<V>(p, row + W, half, lane, a);
+    ln_half_store<V>(p, row, half, pair, lane, par, b, g4, b4, red);
+    row += W;
+    par ^= 1;
+  }
+}
+
 // Any d that is a multiple of 8: one warp per row, three sweeps over the row
 // (the second and third hit L1/L2).
 template <bool RMS = false>
@@ -820,9 +989,54 @@ static int stream_slots(size_t slot_bytes) {
 // registers.  (A shared-memory-streamed variant was measured slower on GB300 in
 // the SP step: between GEMMs this kernel's bandwidth is held by the write-back
 // of the dirty L2 lines the previous kernels leave, not by its load latency.)
+// Persistent launch of a pipelined LayerNorm kernel, or cudaErrorNotReady when the grid would give each
+// warp (pair) fewer than kLnPipeMinRows rows: below that the exposed first load and the tail outweigh the
+// overlap (measured on GB300: at T = 8192, d = 4096 the launch-per-group kernel is 7% faster; at T = 65536
+// the pipelined one reaches 0.94 of HBM against 0.80).
+constexpr int kLnPipeMinRows = 24;
+
+template <typename K>
+static cudaError_t launch_ln_persistent(K kern, int rows_per_block, const RowParams& r, const DeviceCtx& ctx,
+                                        cudaStream_t s, int* per_sm_cache) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (per_sm_cache[dev & 63] == 0) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, 0);
+    if (e != cudaSuccess) return e;
+    per_sm_cache[dev & 63] = n < 1 ? 1 : n;
+  }
+  const long long grid = static_cast<long long>(per_sm_cache[dev & 63]) * ctx.sm_count;
+  if (static_cast<long long>(r.rows) < grid * rows_per_block * kLnPipeMinRows) return cudaErrorNotReady;
+  kern<<<static_cast<int>(grid), 128, 0, s>>>(r);
+  return cudaGetLastError();
+}
+
+template <int V>
+static cudaError_t launch_ln_pipe(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
+  static int per_sm[64] = {0};
+  return launch_ln_persistent(k_layernorm_fwd_pipe<V>, 4, r, ctx, s, per_sm);
+}
+
+template <int V>
+static cudaError_t launch_ln_pipe2(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
+  static int per_sm[64] = {0};
+  return launch_ln_persistent(k_layernorm_fwd_pipe2<V>, 2, r, ctx, s, per_sm);
+}
+
 cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
-  (void)ctx;
   if (r.rows <= 0) return cudaSuccess;
+  {
+    cudaError_t e = cudaErrorNotReady;
+    switch (r.d) {
+      case 1024: e = launch_ln_pipe<4>(r, ctx, s); break;
+      case 2048: e = launch_ln_pipe<8>(r, ctx, s); break;
+      case 4096: e = launch_ln_pipe2<8>(r, ctx, s); break;
+      default: break;
+    }
+    if (e != cudaErrorNotReady) return e;  // launched (or failed); otherwise too few rows per warp
+  }
   const int grid4 = (r.rows + 3) / 4;
   const int grid2 = (r.rows + 1) / 2;
   switch (r.d) {

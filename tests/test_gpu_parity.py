@@ -358,3 +358,18 @@ def test_rmsnorm_gather(T, d, N):
     err = np.abs(f64(Xg.t) - ref)
     assert np.mean(err <= np.abs(ref) * 2.0 ** -8 + 1e-30) > 0.999
     assert Xg.intact()
+
+
+@pytest.mark.parametrize("T,d,N", [(32768, 4096, 8), (49152, 2048, 8), (81920, 1024, 8)])
+def test_layernorm_gather_long_sequences(T, d, N):
+    """Enough rows per warp that the persistent, software-pipelined LayerNorm runs; a seeded sample of
+    rows (including the first and last of every chunk) is checked against the oracle."""
+    w = inputs.small_workload(T, d, N, sp=True, name=f"lnlong_{T}_{d}")
+    X, g, b = _draw(w, "X", "gamma", "beta")
+    Xg = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    binding.tpmlp_layernorm_gather(list(dev(X[0]).split(T // N)), dev(g[0]), dev(b[0]), N, Xg)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(T)
+    rows = np.unique(np.concatenate([rng.integers(0, T, 384), np.arange(0, T, T // N), np.arange(T // N - 1, T, T // N)]))
+    ref = oracle.layer_norm(X[1][rows], g[1], b[1], 1e-5)
+    assert_bf16_close("Xg sample", f64(Xg[torch.from_numpy(rows).cuda()]), ref)
