@@ -569,6 +569,21 @@ def run_other_rows(step, torch, binding, pk):
             out["dropout_backward"] = {"ms": round(ms_d, 4), "GB/s": round(nb / (ms_d * 1e-3) / 1e9, 1),
                                        "frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
                                        "bytes_per_launch": nb, "launches": 2}
+    if w.sp and w.d in (1024, 2048, 4096):
+        # the LayerNorm forward on a sequence 8x as long (same d): enough rows per warp for the persistent,
+        # software-pipelined kernel, whose start-up the step's 8192 rows do not amortise
+        Tl = 8 * w.T
+        xl = [torch.empty(Tl, w.d, dtype=torch.bfloat16, device="cuda").normal_() for _ in range(2)]
+        yl = [torch.empty(Tl, w.d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        nb = 4.0 * Tl * w.d
+        pair = lambda: [binding.tpmlp_layernorm_gather(list(xl[k].split(Tl // w.N)), step.gamma, step.beta, w.N, yl[k])
+                        for k in range(2)]
+        ms = time_calls(torch, pair, 10) / 2.0
+        out["layernorm_gather_long_sequence"] = {"tokens": Tl, "ms": round(ms, 4),
+                                                 "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
+                                                 "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+                                                 "bytes_per_launch": nb}
+        del xl, yl
     if (w.sp and w.backward and w.T % 16 == 0 and w.d % 16 == 0 and w.F % 16 == 0 and
             w.d in (256, 512, 1024, 2048, 4096, 8192)):
         out["fp8"] = run_fp8_step(step, torch, binding, pk)
