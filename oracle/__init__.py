@@ -93,6 +93,18 @@ reason in the design notes):
   E4M3 operands are reused, and the bias gradient and GeLU' act on fp32
   values.
 
+* Attention ([6D] §3.2 "Attention 的 TP"; [GLOSS] tensor-parallel section;
+  [DEEP] column/row-parallel section, multi-head attention paragraph): the
+  Q, K, V projections are split by columns along heads, each shard computes
+  complete attention for its heads, the output projection is split by rows
+  (the same heads) and an AllReduce sums the shards.  Readings: attention
+  is ``softmax(Q Kᵀ / sqrt(hd)) V`` per head and sequence, optionally causal
+  (position s attends to positions <= s); the projection weight is one
+  ``[d x 3d]`` matrix whose columns are Q, K, V in that order, head h taking
+  columns ``h·hd .. (h+1)·hd`` of each; tokens are sequence-major
+  (``[S, batch, hidden]``, row ``s·B + b``) and attend only within their
+  batch element; the output projection's bias is added once, after the sum.
+
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` (values
 printed on the pages, closed forms, invariants, brute force, library
 witnesses and finite differences); none is parity-unpinned.
@@ -478,6 +490,63 @@ def sp_forward_fp8(X_chunks, gamma, beta, eps, A, B, b, N: int, scales):
     out["Y_chunks"] = [out["Y"][lo:hi] for lo, hi in chunk_ranges(T, N)]
     out["Xg"] = Xg
     return out
+
+
+# --------------------------------------------------------------------------- tensor-parallel attention
+
+def attention_head(Q, K, V, causal: bool):
+    """``softmax(Q·Kᵀ/sqrt(hd))·V`` for one head of one sequence: Q, K, V ``[S x hd]``; with ``causal``
+    position s sees keys 0..s only."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    scores = Q @ K.T / math.sqrt(Q.shape[1])
+    if causal:
+        S = Q.shape[0]
+        scores = np.where(np.tril(np.ones((S, S), dtype=bool)), scores, -np.inf)
+    scores = scores - scores.max(axis=1, keepdims=True)
+    w = np.exp(scores)
+    return (w / w.sum(axis=1, keepdims=True)) @ V
+
+
+def head_ranges(H: int, N: int) -> list[tuple[int, int]]:
+    """Heads of shard i: ``[i·H/N, (i+1)·H/N)`` (H % N == 0)."""
+    if N <= 0 or H % N != 0:
+        raise ValueError("the heads must split evenly over the shards")
+    return [(i * H // N, (i + 1) * H // N) for i in range(N)]
+
+
+def attention_tp(X, Wqkv, bqkv, Wo, bo, H: int, N: int, B: int, causal: bool, return_parts: bool = False):
+    """The tensor-parallel attention block: ``Y = Σ_i O_i·Wo[rows of shard i] + bo``.
+
+    ``X [T x d]`` with ``T = S·B`` (row ``s·B + b``); ``Wqkv [d x 3d]``, ``bqkv [3d]`` or None;
+    ``Wo [d x d]``, ``bo [d]`` or None.  Shard i projects its heads' Q, K, V columns, computes their
+    attention per batch element, and multiplies by its rows of ``Wo``; the shards' partials are summed
+    (the AllReduce) and ``bo`` is added once.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    Wqkv = np.asarray(Wqkv, dtype=np.float64)
+    Wo = np.asarray(Wo, dtype=np.float64)
+    T, d = X.shape
+    if T % B != 0 or d % H != 0:
+        raise ValueError("T must be a multiple of the batch and d of the head count")
+    hd = d // H
+    bias_qkv = np.zeros(3 * d) if bqkv is None else np.asarray(bqkv, dtype=np.float64)
+    parts, Os = [], []
+    for lo, hi in head_ranges(H, N):
+        O_i = np.zeros((T, (hi - lo) * hd))
+        for h in range(lo, hi):
+            cols = [slice(part * d + h * hd, part * d + (h + 1) * hd) for part in range(3)]
+            Qh, Kh, Vh = (X @ Wqkv[:, c] + bias_qkv[c] for c in cols)
+            for b in range(B):
+                rows = slice(b, T, B)
+                O_i[rows, (h - lo) * hd:(h - lo + 1) * hd] = attention_head(Qh[rows], Kh[rows], Vh[rows], causal)
+        Os.append(O_i)
+        parts.append(O_i @ Wo[lo * hd:hi * hd, :])
+    Y = all_reduce(parts) + (0.0 if bo is None else np.asarray(bo, dtype=np.float64))
+    if return_parts:
+        return Y, {"O": np.concatenate(Os, axis=1), "partials": parts}
+    return Y
 
 
 # --------------------------------------------------------------------------- backward (chain rule)

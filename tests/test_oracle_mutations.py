@@ -151,7 +151,27 @@ def _mlp_backward_fp8_wrong_dB_scale(X, A, B, b, dY, N, scales, grad_scales):
     return g
 
 
+def _attention_head_unscaled(Q, K, V, causal):
+    Q = np.asarray(Q, dtype=np.float64)
+    return _orig["attention_head"](Q * np.sqrt(Q.shape[1]), K, V, causal)
+
+
+def _attention_head_mask_off_by_one(Q, K, V, causal):
+    Q, K, V = (np.asarray(a, dtype=np.float64) for a in (Q, K, V))
+    if not causal:
+        return _orig["attention_head"](Q, K, V, False)
+    S = Q.shape[0]
+    sc = Q @ K.T / np.sqrt(Q.shape[1])
+    sc = np.where(np.tril(np.ones((S, S), dtype=bool), k=1), sc, -np.inf)   # also sees the next token
+    w = np.exp(sc - sc.max(axis=1, keepdims=True))
+    return (w / w.sum(axis=1, keepdims=True)) @ V
+
+
 CASES = [
+    ("attention_head", _attention_head_unscaled, lambda: pins.test_attention_head_torch_witness(False)),
+    ("attention_head", _attention_head_mask_off_by_one, lambda: pins.test_attention_head_bruteforce()),
+    ("head_ranges", lambda H, N: [(lo, hi) for lo, hi in _orig["head_ranges"](H, N)][::-1],
+     lambda: pins.test_attention_tp_shard_sum_is_the_unsharded_block()),
     ("round_e5m2", _round_e5m2_three_bits, lambda: pins.test_round_e5m2_bruteforce_and_torch()),
     ("mlp_backward_fp8", _mlp_backward_fp8_wrong_dB_scale,
      lambda: pins.test_mlp_backward_fp8_error_is_the_formats_size()),

@@ -722,3 +722,87 @@ def test_sp_backward_fp8_is_mlp_backward_fp8_on_the_gathered_norm(N):
         assert np.array_equal(g[k], ref[k]), k
     for (lo, hi), dx in zip(cr, g["dX_chunks"]):
         assert np.array_equal(dx, oracle.layer_norm_backward(X[lo:hi], gam, 1e-5, ref["dX"][lo:hi])[0])
+
+
+# --------------------------------------------------------------------------- tensor-parallel attention
+
+def _attn_problem(S=6, B=2, d=16, H=4, seed=0):
+    rng = np.random.default_rng(seed)
+    X = rng.normal(size=(S * B, d))
+    Wqkv = rng.normal(size=(d, 3 * d)) * 0.4
+    bqkv = rng.normal(size=3 * d) * 0.1
+    Wo = rng.normal(size=(d, d)) * 0.3
+    bo = rng.normal(size=d) * 0.1
+    return X, Wqkv, bqkv, Wo, bo
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_head_torch_witness(causal):
+    rng = np.random.default_rng(5)
+    Q, K, V = (rng.normal(size=(7, 4)) for _ in range(3))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        *(torch.from_numpy(a)[None, None] for a in (Q, K, V)), is_causal=causal)[0, 0].numpy()
+    assert rel(oracle.attention_head(Q, K, V, causal), ref) < 1e-13
+
+
+def test_attention_head_bruteforce():
+    """Pure-Python loops over a 3 x 2 head: scaled scores, max-subtracted exponentials, weighted sum."""
+    Q = [[0.5, -1.0], [1.5, 0.25], [-0.75, 2.0]]
+    K = [[1.0, 0.5], [-0.5, 1.0], [0.25, -1.5]]
+    V = [[1.0, 2.0], [-3.0, 0.5], [0.0, -1.0]]
+    for causal in (False, True):
+        out = []
+        for s in range(3):
+            keys = range(s + 1) if causal else range(3)
+            sc = [sum(Q[s][e] * K[t][e] for e in range(2)) / math.sqrt(2) for t in keys]
+            m = max(sc)
+            w = [math.exp(x - m) for x in sc]
+            z = sum(w)
+            out.append([sum(w[i] * V[t][e] for i, t in enumerate(keys)) / z for e in range(2)])
+        assert np.allclose(oracle.attention_head(np.array(Q), np.array(K), np.array(V), causal), out,
+                           rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_tp_torch_witness(causal):
+    """The whole block against torch: linear projections, SDPA per (batch, head), output projection."""
+    S, B, d, H = 6, 2, 16, 4
+    X, Wqkv, bqkv, Wo, bo = _attn_problem(S, B, d, H)
+    hd = d // H
+    x = torch.from_numpy(X).reshape(S, B, d)
+    qkv = x @ torch.from_numpy(Wqkv) + torch.from_numpy(bqkv)               # [S, B, 3d]
+    q, k, v = (qkv[..., p * d:(p + 1) * d].reshape(S, B, H, hd).permute(1, 2, 0, 3) for p in range(3))
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal)  # [B, H, S, hd]
+    o = o.permute(2, 0, 1, 3).reshape(S * B, d)
+    ref = (o @ torch.from_numpy(Wo) + torch.from_numpy(bo)).numpy()
+    for N in (1, 2, 4):
+        assert rel(oracle.attention_tp(X, Wqkv, bqkv, Wo, bo, H, N, B, causal), ref) < 1e-12
+
+
+def test_attention_tp_shard_sum_is_the_unsharded_block():
+    X, Wqkv, bqkv, Wo, bo = _attn_problem(S=5, B=3, d=24, H=6)
+    one = oracle.attention_tp(X, Wqkv, bqkv, Wo, bo, 6, 1, 3, True)
+    for N in (2, 3, 6):
+        Y, parts = oracle.attention_tp(X, Wqkv, bqkv, Wo, bo, 6, N, 3, True, return_parts=True)
+        assert rel(Y, one) < 1e-13
+        assert len(parts["partials"]) == N
+    assert oracle.head_ranges(32, 8)[3] == (12, 16)
+    with pytest.raises(ValueError):
+        oracle.head_ranges(6, 4)
+
+
+def test_attention_causal_outputs_ignore_later_tokens():
+    S, B, d, H = 6, 2, 16, 4
+    X, Wqkv, bqkv, Wo, bo = _attn_problem(S, B, d, H)
+    Y = oracle.attention_tp(X, Wqkv, bqkv, Wo, bo, H, 2, B, True)
+    X2 = X.copy()
+    X2[4 * B:] += 3.0                                  # change positions 4 and 5 of every batch element
+    Y2 = oracle.attention_tp(X2, Wqkv, bqkv, Wo, bo, H, 2, B, True)
+    assert np.array_equal(Y[:4 * B], Y2[:4 * B])
+    assert not np.allclose(Y[4 * B:], Y2[4 * B:])
+    # and batch elements do not see each other
+    X3 = X.copy()
+    X3[1::B] += 1.0                                    # batch element 1 only
+    Y3 = oracle.attention_tp(X3, Wqkv, bqkv, Wo, bo, H, 2, B, False)
+    Y0 = oracle.attention_tp(X, Wqkv, bqkv, Wo, bo, H, 2, B, False)
+    assert np.array_equal(Y3[0::B], Y0[0::B])
