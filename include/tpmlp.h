@@ -485,6 +485,41 @@ TPMLP_API tpmlp_status tpmlp_layernorm_backward_noalloc(const void* const* X_chu
                                                         void* const* dX_chunks, void* dgamma, void* dbeta,
                                                         tpmlp_stream_t stream);
 
+/* ------------------------------------------------------------------ tensor-parallel attention
+ * "6D" guide §3.2 (attention TP splits by heads: 32 heads at TP = 8 give each
+ * GPU 4 heads), the glossary page's tensor-parallel section and the deep-dive
+ * page's multi-head attention paragraph: the Q, K, V projections are split by
+ * columns along heads, every shard computes complete attention for its heads,
+ * the output projection is split by rows and the shards' partial outputs are
+ * summed.  Here all N shards run on one GPU: one GEMM projects every head, the
+ * attention core handles every (batch, head), and the output projection's K
+ * loop walks the shards' head rows into one TMEM accumulator.
+ * Layout: tokens sequence-major, row s B + b (the listing's [S, batch, hidden]);
+ * QKV [T x 3d] with columns Q | K | V, head h at columns h hd .. (h+1) hd of
+ * each part; O [T x d] heads side by side; d = H hd.  Head dimension 128. */
+
+/* Bytes of workspace tpmlp_attention_tp_forward needs (QKV and O buffers).
+ * head_dim other than 128 returns TPMLP_ERR_UNSUPPORTED. */
+TPMLP_API tpmlp_status tpmlp_attention_workspace_size(int64_t S, int64_t B, int64_t H, int64_t head_dim,
+                                                      size_t* bytes);
+
+/* Attention core: for every batch element b and head h,
+ * O[:, h] = softmax(Q_h K_h^T / sqrt(hd)) V_h over that batch element's S
+ * positions, causal (position s sees keys <= s) when causal == 1.  fp32
+ * scores and accumulation, bf16 in and out.  QKV [S B x 3 H hd], O [S B x H hd]. */
+TPMLP_API tpmlp_status tpmlp_attention_core(const void* QKV, int64_t S, int64_t B, int64_t H, int64_t head_dim,
+                                            int causal, void* O, tpmlp_stream_t stream);
+
+/* The attention block: QKV = X Wqkv + bqkv (bqkv [3d] or NULL), O = attention
+ * core, Y = O Wo + bo (Wo [d x d] row-split by heads, bo [d] or NULL, added
+ * after the shard sum).  X, Y [S B x d]; Wqkv [d x 3d]; H % n_shards == 0.
+ * QKV_out, O_out: NULL or buffers that keep the intermediates.  Workspace:
+ * tpmlp_attention_workspace_size. */
+TPMLP_API tpmlp_status tpmlp_attention_tp_forward(const void* X, const void* Wqkv, const void* bqkv, const void* Wo,
+                                                  const void* bo, int64_t S, int64_t B, int64_t H, int32_t n_shards,
+                                                  int causal, void* Y, void* QKV_out, void* O_out, void* workspace,
+                                                  size_t workspace_bytes, tpmlp_stream_t stream);
+
 /* Failure-detection self test: launches one CTA that waits on a barrier no
  * thread ever arrives at, with a limit of `budget_us` microseconds (1 to
  * 1000000).  The wait runs out, the kernel records the timeout and exits;

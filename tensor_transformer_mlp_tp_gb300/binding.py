@@ -96,6 +96,12 @@ _SIGS = {
                                      ctypes.c_int),
     "tpmlp_gemm_fp8": ([_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P,
                         _P, ctypes.c_int64, _P], ctypes.c_int),
+    "tpmlp_attention_workspace_size": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "tpmlp_attention_core": ([_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P],
+                             ctypes.c_int),
+    "tpmlp_attention_tp_forward": ([_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                    ctypes.c_int, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_sp_backward_fp8": ([_PP, _P, ctypes.c_float, _P, _P, _P, _P, _P, _PP, _FP, _FP, _SP, _PP, _P, _P, _P, _P,
                                _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
 }
@@ -495,6 +501,29 @@ def tpmlp_sp_backward_fp8(X_chunks, gamma, A, B, Hpre, Xq, Hq, dY_chunks, N, fwd
         xp, _ptr(gamma), eps, _ptr(A), _ptr(B), _ptr(Hpre), _ptr(Xq), _ptr(Hq), dyp, ctypes.byref(fwd_state),
         ctypes.byref(grad_state), ctypes.byref(shape), dxp, _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dgamma),
         _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- tensor-parallel attention
+
+def tpmlp_attention_workspace_size(S, B, H, head_dim=128):
+    n = ctypes.c_size_t(0)
+    _check("tpmlp_attention_workspace_size", lib().tpmlp_attention_workspace_size(S, B, H, head_dim, ctypes.byref(n)))
+    return n.value
+
+
+def tpmlp_attention_core(QKV, S, B, H, O, causal=False, head_dim=128, stream=None):
+    _check("tpmlp_attention_core", lib().tpmlp_attention_core(_ptr(QKV), S, B, H, head_dim, 1 if causal else 0, _ptr(O),
+                                                              _stream(stream)))
+
+
+def tpmlp_attention_tp_forward(X, Wqkv, Wo, S, B, H, N, Y, bqkv=None, bo=None, causal=False, QKV_out=None,
+                               O_out=None, ws=None, stream=None):
+    if ws is None:
+        ws = torch.empty(max(tpmlp_attention_workspace_size(S, B, H), 256), dtype=torch.uint8, device=X.device)
+    _check("tpmlp_attention_tp_forward", lib().tpmlp_attention_tp_forward(
+        _ptr(X), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo), S, B, H, N, 1 if causal else 0, _ptr(Y), _ptr(QKV_out),
+        _ptr(O_out), _ptr(ws), ws.numel(), _stream(stream)))
+    return Y
 
 
 def tpmlp_selftest_wait_timeout(budget_us: int, stream=None):

@@ -1,0 +1,479 @@
+// Tensor-parallel attention: the per-head attention core on tcgen05, and the
+// block (QKV projection, attention, output projection with the shard sum).
+//
+// Attention core (one CTA per 128-query tile of one batch element and head,
+// head dim 128): softmax(Q K^T / sqrt(hd)) V with an online softmax over
+// 128-key tiles.
+//   warp 0   TMA producer: Q once, then K and V tiles into a 2-stage ring;
+//            Q, K, V come straight out of the QKV projection's [S, B, 3, H, hd]
+//            layout through 4-D tensor maps (two 64-element boxes per row).
+//   warp 1   MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//            buffers, then O_tile = P_{j-1} V_{j-1} once the softmax warps have
+//            written P_{j-1}; V is the MN-major B operand.
+//   warps 2..5  softmax: thread t of the four owns query row t (TMEM lane t).
+//            Per key tile: pass 1 reads S from TMEM for the row maximum, the
+//            previous tile's P V is added into the fp32 row accumulator o[128]
+//            (rescaled by exp2(m_old - m_new)), pass 2 reads S again, writes
+//            P = exp2(S - m) in bf16 into shared memory in the 128-byte-
+//            swizzled K-major layout and sums it into the row's denominator.
+// Causal attention visits key tiles 0..i for query tile i and masks inside
+// the diagonal tile; keys at or past S are masked.  Every wait is bounded
+// (error word + abort flag), and the CTA drains its copies and MMAs before
+// it releases TMEM.
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "../../include/tpmlp.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+namespace {
+
+constexpr int kHd = 128;            // head dimension this kernel is laid out for
+constexpr int kQTile = 128;         // queries per CTA (one per TMEM lane)
+constexpr int kKTile = 128;         // keys per step
+constexpr int kKvStages = 2;
+constexpr int kAtom = 128 * 128;    // one 64-element-wide swizzled column of a 128-row tile: 16 KB
+constexpr int kTileBytes = 2 * kAtom;  // a 128 x 128 bf16 tile: two atom columns
+constexpr int kThreads = 192;
+constexpr uint32_t kSiteAttnQ = 32, kSiteAttnKv = 33, kSiteAttnS = 34, kSiteAttnP = 35, kSiteAttnSEmpty = 36,
+                   kSiteAttnKvEmpty = 37, kSiteAttnPv = 38;
+
+struct AttnParams {
+  CUtensorMap tmQ, tmK, tmV;
+  void* out;          // [T x d] bf16, row s B + b, columns h hd .. (h+1) hd
+  int S, B, H;
+  int n_qtiles;
+  int causal;
+  float scale_log2;   // log2(e) / sqrt(hd)
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// Rows s0 .. s0 + 127 of one part (Q, K or V) of head h, batch b: two boxes of 64 elements.
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int h, int b, int s0) {
+  tma_load_4d(dst, map, bar, 0, h, b, s0);
+  tma_load_4d(dst + kAtom, map, bar, 64, h, b, s0);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + kTileBytes;
+  uint8_t* sV = sK + kKvStages * kTileBytes;
+  uint8_t* sP = sV + kKvStages * kTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTileBytes);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = q_full + 1;
+  uint64_t* kv_empty = kv_full + kKvStages;
+  uint64_t* s_full = kv_empty + kKvStages;
+  uint64_t* s_empty = s_full + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* pv_done = p_full + 1;
+  uint64_t* drain = pv_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  // longest causal tiles first: the last query tiles have the most key tiles
+  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x % p.n_qtiles);
+  const int bh = static_cast<int>(blockIdx.x / p.n_qtiles);
+  const int b = bh % p.B, h = bh / p.B;
+  const int n_kt_all = (p.S + kKTile - 1) / kKTile;
+  const int nk = p.causal ? min(n_kt_all, qt + 1) : n_kt_all;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full + s, 1);
+      mbar_init(s_empty + s, 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ producer
+      mbar_arrive_expect_tx(q_full, kTileBytes);
+      load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
+      uint32_t issued = 0, parity = 0;
+      for (int j = 0; j < nk; ++j) {
+        const int st = j % kKvStages;
+        const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
+        if (!wait_bounded(kv_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(kv_full + st, 2 * kTileBytes);
+        load_tile(sK + st * kTileBytes, &p.tmK, kv_full + st, h, b, j * kKTile);
+        load_tile(sV + st * kTileBytes, &p.tmV, kv_full + st, h, b, j * kKTile);
+        issued |= 1u << st;
+        parity = (parity & ~(1u << st)) | (ph << st);
+      }
+      // copies in flight land before shared memory is released
+      wait_drain(q_full, 0, p.timeout_ns);
+      for (int s = 0; s < kKvStages; ++s)
+        if (issued & (1u << s)) wait_drain(kv_full + s, (parity >> s) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kQTile, kKTile, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kQTile, kHd, false, true);
+      const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP);
+      const uint32_t o_tmem = tmem_base + 256;
+      bool ok = wait_bounded(q_full, 0, wc, kSiteAttnQ);
+      if (ok) tc_fence_after_sync();
+      // one step: S_j (when j < nk), then P_{j-1} V_{j-1} (when j >= 1)
+      for (int j = 0; ok && j <= nk; ++j) {
+        if (j < nk) {
+          const int sb = j & 1;
+          const int st = j % kKvStages;
+          if (!wait_bounded(s_empty + sb, (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
+          if (!wait_bounded(kv_full + st, static_cast<uint32_t>(j / kKvStages) & 1u, wc, kSiteAttnKv)) break;
+          tc_fence_after_sync();
+          const uint32_t k_base = smem_u32(sK + st * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base + sb * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full + sb);
+        }
+        if (j >= 1) {
+          const int jj = j - 1;
+          const int st = jj % kKvStages;
+          if (!wait_bounded(p_full, static_cast<uint32_t>(jj) & 1u, wc, kSiteAttnP)) break;
+          tc_fence_after_sync();
+          const uint32_t v_base = smem_u32(sV + st * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kKTile / 16; ++kk) {
+            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(o_tmem, sdesc_sw128(p_base + a_off, 16, 1024), sdesc_sw128(v_base + kk * 2048, kAtom, 1024),
+                      idesc_pv, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(pv_done);
+          umma_commit(kv_empty + st);
+        }
+      }
+      umma_commit(drain);
+      wait_drain(drain, 0, p.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------------- softmax (warps 2..5)
+    const int quad = warp & 3;
+    const int r = quad * 32 + static_cast<int>(lane);  // row within the tile = TMEM lane
+    const int q = qt * kQTile + r;                      // query position
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    float o[kHd];
+#pragma unroll
+    for (int e = 0; e < kHd; ++e) o[e] = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      const int sb = j & 1;
+      int w_ok = 1;
+      if (lane == 0) w_ok = wait_bounded(s_full + sb, static_cast<uint32_t>(j >> 1) & 1u, wc, kSiteAttnS) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t s_tmem = lane_base + static_cast<uint32_t>(sb * 128);
+      const int key0 = j * kKTile;
+      // a key is visible when it is in the sequence and, for causal attention, not after the query
+      const int key_end = p.causal ? min(p.S, q + 1) : p.S;
+      // pass 1: row maximum of this tile (scaled to log2 units)
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_load_32cols(s_tmem + static_cast<uint32_t>(32 * c), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (key0 + 32 * c + i < key_end) mx = fmaxf(mx, v[i] * p.scale_log2);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;  // a row with nothing visible yet keeps p = 0
+      const float alpha = m == -INFINITY ? 0.f : exp2f(m - m_use);
+      // the previous tile's P V, rescaled into the running accumulator (its P buffer is then free)
+      if (j >= 1) {
+        if (lane == 0) w_ok = wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < kHd / 32; ++c) {
+          float v[32];
+          tmem_load_32cols(lane_base + 256u + static_cast<uint32_t>(32 * c), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = o[32 * c + i] * alpha_prev + v[i];
+        }
+      }
+      // pass 2: P = exp2(S scale - m) in bf16 into the swizzled K-major tile, row sum
+      float psum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_load_32cols(s_tmem + static_cast<uint32_t>(32 * c), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float pv = key0 + 32 * c + i < key_end ? exp2f(v[i] * p.scale_log2 - m_use) : 0.f;
+          v[i] = pv;
+          psum += pv;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int chunk = 4 * c + g;  // 8-key chunk 0..15
+          uint8_t* dst = sP + (chunk >> 3) * kAtom + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(pack_bf16x2(v[8 * g], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                         pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+        }
+      }
+      l = l * alpha + psum;
+      m = m_new;
+      alpha_prev = alpha;
+      // S buffer and P tile handed over: TMEM reads complete, shared-memory writes visible to the MMAs
+      tc_fence_before_sync();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(s_empty + sb);
+        mbar_arrive(p_full);
+      }
+    }
+    if (ok && nk > 0) {
+      int w_ok = 1;
+      if (lane == 0) w_ok = wait_bounded(pv_done, static_cast<uint32_t>(nk - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0;
+      if (ok) {
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < kHd / 32; ++c) {
+          float v[32];
+          tmem_load_32cols(lane_base + 256u + static_cast<uint32_t>(32 * c), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = o[32 * c + i] * alpha_prev + v[i];
+        }
+      }
+    }
+    if (ok && q < p.S) {
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                            (static_cast<long long>(q) * p.B + b) * (static_cast<long long>(p.H) * kHd) +
+                                            static_cast<long long>(h) * kHd);
+#pragma unroll
+      for (int g = 0; g < kHd / 8; ++g) {
+        const float* y = o + 8 * g;
+        dst[g] = make_uint4(pack_bf16x2(y[0] * inv_l, y[1] * inv_l), pack_bf16x2(y[2] * inv_l, y[3] * inv_l),
+                            pack_bf16x2(y[4] * inv_l, y[5] * inv_l), pack_bf16x2(y[6] * inv_l, y[7] * inv_l));
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 4-D map over one part (Q, K or V) of the projection output [S, B, 3, H, hd]: dims (e, h, b, s).
+bool make_part_map(CUtensorMap* m, const void* qkv, int part, int S, int B, int H) {
+  auto fn = attn_encode_fn();
+  if (fn == nullptr) return false;
+  const long long d = static_cast<long long>(H) * kHd;
+  const void* base = static_cast<const __nv_bfloat16*>(qkv) + part * d;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHd), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B),
+                        static_cast<cuuint64_t>(S)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHd) * 2, static_cast<cuuint64_t>(3 * d) * 2,
+                           static_cast<cuuint64_t>(3 * d) * 2 * static_cast<cuuint64_t>(B)};
+  cuuint32_t box[4] = {64, 1, 1, 128};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kAttnSmem = 1024 + (2 + 2 * kKvStages) * kTileBytes + 256;
+
+cudaError_t launch_attention(const void* qkv, int S, int B, int H, bool causal, void* out, const DeviceCtx& ctx,
+                             cudaStream_t s) {
+  if (S <= 0) return cudaSuccess;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_part_map(&p.tmQ, qkv, 0, S, B, H) || !make_part_map(&p.tmK, qkv, 1, S, B, H) ||
+      !make_part_map(&p.tmV, qkv, 2, S, B, H))
+    return cudaErrorInvalidValue;
+  p.out = out;
+  p.S = S;
+  p.B = B;
+  p.H = H;
+  p.n_qtiles = (S + kQTile - 1) / kQTile;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHd)));
+  p.err = ctx.err;
+  p.timeout_ns = ctx.timeout_ns;
+  const long long grid = static_cast<long long>(p.n_qtiles) * B * H;
+  if (grid > INT_MAX) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(k_attention_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kAttnSmem));
+  if (e != cudaSuccess) return e;
+  k_attention_fwd<<<static_cast<int>(grid), kThreads, kAttnSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tpmlp_status attn_check(int64_t S, int64_t B, int64_t H, int64_t head_dim) {
+  if (S < 0 || B < 1 || H < 1 || head_dim < 1) return TPMLP_ERR_INVALID_ARG;
+  if (head_dim != kHd) return TPMLP_ERR_UNSUPPORTED;
+  if (S > INT_MAX / 4 || B > 65535 || H > 65535 || S * B > INT_MAX / 4 || H * kHd > 65536)
+    return TPMLP_ERR_UNSUPPORTED;
+  return TPMLP_OK;
+}
+
+tpmlp_status to_status(cudaError_t e) {
+  if (e == cudaSuccess) return TPMLP_OK;
+  if (e == cudaErrorNotSupported) return TPMLP_ERR_UNSUPPORTED;
+  return TPMLP_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+extern "C" {
+
+tpmlp_status tpmlp_attention_workspace_size(int64_t S, int64_t B, int64_t H, int64_t head_dim, size_t* bytes) {
+  if (bytes == nullptr) return TPMLP_ERR_INVALID_ARG;
+  const tpmlp_status st = attn_check(S, B, H, head_dim);
+  if (st != TPMLP_OK) return st;
+  const size_t T = static_cast<size_t>(S) * static_cast<size_t>(B), d = static_cast<size_t>(H * head_dim);
+  *bytes = align256(T * 3 * d * 2) + align256(T * d * 2);
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_attention_core(const void* QKV, int64_t S, int64_t B, int64_t H, int64_t head_dim, int causal,
+                                  void* O, tpmlp_stream_t stream) {
+  tpmlp_status st = attn_check(S, B, H, head_dim);
+  if (st != TPMLP_OK) return st;
+  if (causal != 0 && causal != 1) return TPMLP_ERR_INVALID_ARG;
+  if (S == 0) return TPMLP_OK;
+  if (!al16(QKV) || !al16(O)) return TPMLP_ERR_INVALID_ARG;
+  DeviceCtx c;
+  if (current_device_ctx(&c) != cudaSuccess) return TPMLP_ERR_CUDA;
+  return to_status(launch_attention(QKV, static_cast<int>(S), static_cast<int>(B), static_cast<int>(H), causal == 1,
+                                    O, c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tpmlp_status tpmlp_attention_tp_forward(const void* X, const void* Wqkv, const void* bqkv, const void* Wo,
+                                        const void* bo, int64_t S, int64_t B, int64_t H, int32_t n_shards,
+                                        int causal, void* Y, void* QKV_out, void* O_out, void* workspace,
+                                        size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = attn_check(S, B, H, kHd);
+  if (st != TPMLP_OK) return st;
+  if (n_shards < 1 || H % n_shards != 0 || (causal != 0 && causal != 1)) return TPMLP_ERR_INVALID_ARG;
+  if (S == 0) return TPMLP_OK;
+  if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(Y) || (bqkv != nullptr && !al16(bqkv)) ||
+      (bo != nullptr && !al16(bo)) || (QKV_out != nullptr && !al16(QKV_out)) || (O_out != nullptr && !al16(O_out)))
+    return TPMLP_ERR_INVALID_ARG;
+  size_t need = 0;
+  tpmlp_attention_workspace_size(S, B, H, kHd, &need);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if (current_device_ctx(&c) != cudaSuccess) return TPMLP_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int T = static_cast<int>(S * B), d = static_cast<int>(H * kHd);
+  void* qkv = workspace;
+  void* o = static_cast<uint8_t*>(workspace) + align256(static_cast<size_t>(T) * 3 * d * 2);
+  if (QKV_out != nullptr) qkv = QKV_out;
+  if (O_out != nullptr) o = O_out;
+  // column-parallel projection: all shards' Q, K, V columns in one GEMM (bias fused)
+  GemmLaunch g1;
+  g1.M = T;
+  g1.N = 3 * d;
+  g1.K = d;
+  g1.a = {X, d, false};
+  g1.b = {Wqkv, 3 * d, true};
+  g1.epi = kEpiBias;
+  g1.out0 = qkv;
+  g1.ld0 = 3 * d;
+  g1.bias = bqkv;
+  cudaError_t e = launch_gemm(g1, c, s);
+  if (e == cudaSuccess) e = launch_attention(qkv, static_cast<int>(S), static_cast<int>(B), static_cast<int>(H),
+                                             causal == 1, o, c, s);
+  // row-parallel output projection: the K loop walks the shards' head rows into one accumulator, then
+  // the row layer's bias
+  if (e == cudaSuccess) {
+    GemmLaunch g2;
+    g2.M = T;
+    g2.N = d;
+    g2.K = d;
+    g2.a = {o, d, false};
+    g2.b = {Wo, d, true};
+    g2.epi = kEpiBias;
+    g2.out0 = Y;
+    g2.ld0 = d;
+    g2.bias = bo;
+    e = launch_gemm(g2, c, s);
+  }
+  return to_status(e);
+}
+
+}  // extern "C"

@@ -213,3 +213,21 @@ def test_fp8_backward_workspace_and_argument_checks(lib):
     assert L.tpmlp_gemm_fp8(good, 0, good, 1, 256, 256, 256, good, good, good, 128, None) == binding.ERR_INVALID_ARG
     assert L.tpmlp_gemm_fp8(None, 0, None, 1, 0, 256, 256, None, None, None, 256, None) == binding.OK
     assert L.tpmlp_transpose_bytes(good, 24, 64, good, None) == binding.ERR_INVALID_ARG
+
+
+def test_attention_workspace_and_argument_checks(lib):
+    L = binding.lib()
+    n = ctypes.c_size_t(0)
+    assert L.tpmlp_attention_workspace_size(4096, 2, 32, 128, ctypes.byref(n)) == binding.OK
+    T, d = 4096 * 2, 32 * 128
+    assert n.value == _r256(T * 3 * d * 2) + _r256(T * d * 2)
+    assert L.tpmlp_attention_workspace_size(4096, 2, 32, 64, ctypes.byref(n)) == binding.ERR_UNSUPPORTED
+    assert L.tpmlp_attention_workspace_size(-1, 2, 32, 128, ctypes.byref(n)) == binding.ERR_INVALID_ARG
+    good = ctypes.c_void_p(1 << 20)
+    # heads not divisible by the shards; a causal flag other than 0 / 1; misaligned pointers
+    assert L.tpmlp_attention_tp_forward(good, good, None, good, None, 256, 1, 6, 4, 0, good, None, None, good, 1 << 30,
+                                        None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_attention_core(good, 256, 1, 4, 128, 2, good, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_attention_core(ctypes.c_void_p((1 << 20) + 2), 256, 1, 4, 128, 0, good, None) \
+        == binding.ERR_INVALID_ARG
+    assert L.tpmlp_attention_core(None, 0, 1, 4, 128, 1, None, None) == binding.OK      # empty sequence
