@@ -515,6 +515,35 @@ def run_fp8_step(step, torch, binding, pk):
             "peak_fp8_tflops": round(peak8, 1), "peak_kind": "2 x measured bf16 sustained (nominal FP8:BF16 ratio)"}
 
 
+def run_attention(step, torch, binding, pk):
+    """The tensor-parallel attention block on the step's width: d / 128 heads of 128 split over the N
+    shards, the step's tokens as 2 sequences (sequence-major), causal; the attention core and the whole
+    block (projection GEMM, core, output projection with the shard sum) timed on their own."""
+    w = step.w
+    d, N = w.d, w.N
+    H, B = d // 128, 2
+    S = w.T // B
+    T = S * B
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    X = step.X[:T]
+    Wqkv = torch.empty(d, 3 * d, **bf).normal_(0.0, d ** -0.5)
+    Wo = torch.empty(d, d, **bf).normal_(0.0, d ** -0.5)
+    bqkv, bo = torch.zeros(3 * d, **bf), torch.zeros(d, **bf)
+    Y, QKV, O = torch.empty(T, d, **bf), torch.empty(T, 3 * d, **bf), torch.empty(T, d, **bf)
+    ws = torch.empty(binding.tpmlp_attention_workspace_size(S, B, H), dtype=torch.uint8, device="cuda")
+    block = lambda: binding.tpmlp_attention_tp_forward(X, Wqkv, Wo, S, B, H, N, Y, bqkv=bqkv, bo=bo, causal=True,
+                                                       QKV_out=QKV, O_out=O, ws=ws)
+    ms_blk = time_calls(torch, block, 10)
+    ms_core = time_calls(torch, lambda: binding.tpmlp_attention_core(QKV, S, B, H, O, causal=True), 10)
+    core_flops = 4.0 * 128 * B * H * S * (S + 1) / 2          # Q K^T and P V over the visible (causal) pairs
+    gemm_flops = 2.0 * T * d * 3 * d + 2.0 * T * d * d
+    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    return {"workload": f"S={S} x B={B}, d={d}, {H} heads of 128 over N={N} shards, causal",
+            "block_ms": round(ms_blk, 4), "block_TFLOP/s": round((core_flops + gemm_flops) / (ms_blk * 1e-3) / 1e12, 1),
+            "core_ms": round(ms_core, 4), "core_TFLOP/s": round(core_flops / (ms_core * 1e-3) / 1e12, 1),
+            "core_frac": round(core_flops / (ms_core * 1e-3) / 1e12 / peak, 3)}
+
+
 def run_other_rows(step, torch, binding, pk):
     """Rows of the hot path the step does not run: the explicit reduce-scatter (per-shard bf16 partials, then
     the reduce-scatter kernel) and the RMS norm variant on the step's shapes, and the fp32 path on the tiny
@@ -587,6 +616,8 @@ def run_other_rows(step, torch, binding, pk):
     if (w.sp and w.backward and w.T % 16 == 0 and w.d % 16 == 0 and w.F % 16 == 0 and
             w.d in (256, 512, 1024, 2048, 4096, 8192)):
         out["fp8"] = run_fp8_step(step, torch, binding, pk)
+    if w.d % 128 == 0 and w.T % 2 == 0:
+        out["attention_tp"] = run_attention(step, torch, binding, pk)
     t = inputs.WORKLOADS["tiny_fp32_fwd"]
     f32 = lambda name: torch.from_numpy(np.ascontiguousarray(inputs.draw(t, name)[0])).cuda()
     X, A, B, b = f32("X"), f32("A"), f32("B"), f32("bias")

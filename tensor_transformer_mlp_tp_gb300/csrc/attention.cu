@@ -41,7 +41,7 @@ constexpr int kKTile = 128;         // keys per step
 constexpr int kKvStages = 2;
 constexpr int kAtom = 128 * 128;    // one 64-element-wide swizzled column of a 128-row tile: 16 KB
 constexpr int kTileBytes = 2 * kAtom;  // a 128 x 128 bf16 tile: two atom columns
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
 constexpr uint32_t kSiteAttnQ = 32, kSiteAttnKv = 33, kSiteAttnS = 34, kSiteAttnP = 35, kSiteAttnSEmpty = 36,
                    kSiteAttnKvEmpty = 37, kSiteAttnPv = 38;
 
@@ -65,6 +65,82 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 32 lanes x 32 fp32 columns from TMEM without waiting (tcgen05.wait::ld before the registers are used).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// The same into float registers.
+__device__ __forceinline__ void tmem_ld32f_nowait(uint32_t taddr, float (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]), "=f"(r[8]),
+        "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]), "=f"(r[16]),
+        "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]), "=f"(r[24]),
+        "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Bounded wait without a suspend-time hint: the per-tile handoffs between producer, MMA issuer and softmax
+// warps are short and on the critical path, where a sleeping wait's wake-up would add to every tile.
+__device__ __forceinline__ bool spin_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  if (spin_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (spin_try_wait(bar, parity)) return true;
+    if (*w.abort) return false;
+    if (global_timer_ns() - t0 > w.budget_ns) {
+      record_error(w, kErrTimeout, site);
+      return false;
+    }
+  }
+}
+
+// 2^x with the hardware's approximate base-2 exponential (flushes subnormal results to zero); the
+// softmax exponents here are <= 8 and underflow to 0 harmlessly.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Rows s0 .. s0 + 127 of one part (Q, K or V) of head h, batch b: two boxes of 64 elements.
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int h, int b, int s0) {
   tma_load_4d(dst, map, bar, 0, h, b, s0);
@@ -77,16 +153,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + kTileBytes;
   uint8_t* sV = sK + kKvStages * kTileBytes;
-  uint8_t* sP = sV + kKvStages * kTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTileBytes);
+  uint8_t* sP = sV + kKvStages * kTileBytes;  // two P buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kTileBytes);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = q_full + 1;
-  uint64_t* kv_empty = kv_full + kKvStages;
-  uint64_t* s_full = kv_empty + kKvStages;
+  // K and V have their own barriers: K_j is released as soon as S_j is done, V_j after P_j V_j
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_empty = k_full + kKvStages;
+  uint64_t* v_full = k_empty + kKvStages;
+  uint64_t* v_empty = v_full + kKvStages;
+  uint64_t* s_full = v_empty + kKvStages;
   uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* drain = pv_done + 1;
+  uint64_t* p_full = s_empty + 2;   // [P buffer]
+  uint64_t* pv_done = p_full + 2;   // [P buffer]: P V of the tiles that used that buffer
+  uint64_t* drain = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -102,15 +181,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(kv_full + s, 1);
-      mbar_init(kv_empty + s, 1);
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full + s, 1);
-      mbar_init(s_empty + s, 4);
+      mbar_init(s_empty + s, 8);
+      mbar_init(p_full + s, 8);
+      mbar_init(pv_done + s, 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -131,38 +212,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       // ------------------------------------------------------------------ producer
       mbar_arrive_expect_tx(q_full, kTileBytes);
       load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
-      uint32_t issued = 0, parity = 0;
+      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
       for (int j = 0; j < nk; ++j) {
         const int st = j % kKvStages;
         const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
-        if (!wait_bounded(kv_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(kv_full + st, 2 * kTileBytes);
-        load_tile(sK + st * kTileBytes, &p.tmK, kv_full + st, h, b, j * kKTile);
-        load_tile(sV + st * kTileBytes, &p.tmV, kv_full + st, h, b, j * kKTile);
-        issued |= 1u << st;
-        parity = (parity & ~(1u << st)) | (ph << st);
+        if (!wait_spin(k_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(k_full + st, kTileBytes);
+        load_tile(sK + st * kTileBytes, &p.tmK, k_full + st, h, b, j * kKTile);
+        k_issued |= 1u << st;
+        k_par = (k_par & ~(1u << st)) | (ph << st);
+        if (!wait_spin(v_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(v_full + st, kTileBytes);
+        load_tile(sV + st * kTileBytes, &p.tmV, v_full + st, h, b, j * kKTile);
+        v_issued |= 1u << st;
+        v_par = (v_par & ~(1u << st)) | (ph << st);
       }
       // copies in flight land before shared memory is released
       wait_drain(q_full, 0, p.timeout_ns);
-      for (int s = 0; s < kKvStages; ++s)
-        if (issued & (1u << s)) wait_drain(kv_full + s, (parity >> s) & 1u, p.timeout_ns);
+      for (int s = 0; s < kKvStages; ++s) {
+        if (k_issued & (1u << s)) wait_drain(k_full + s, (k_par >> s) & 1u, p.timeout_ns);
+        if (v_issued & (1u << s)) wait_drain(v_full + s, (v_par >> s) & 1u, p.timeout_ns);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------------ MMA issuer
+      // step j: S_j = Q K_j^T (j < nk) into S buffer j % 2, then O += P_{j-1} V_{j-1} (j >= 1): O stays
+      // in TMEM across the key tiles
       constexpr uint32_t idesc_s = idesc_bf16_f32(kQTile, kKTile, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kQTile, kHd, false, true);
-      const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP);
+      const uint32_t q_base = smem_u32(sQ);
       const uint32_t o_tmem = tmem_base + 256;
-      bool ok = wait_bounded(q_full, 0, wc, kSiteAttnQ);
+      bool ok = wait_spin(q_full, 0, wc, kSiteAttnQ);
       if (ok) tc_fence_after_sync();
-      // one step: S_j (when j < nk), then P_{j-1} V_{j-1} (when j >= 1)
       for (int j = 0; ok && j <= nk; ++j) {
         if (j < nk) {
           const int sb = j & 1;
           const int st = j % kKvStages;
-          if (!wait_bounded(s_empty + sb, (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
-          if (!wait_bounded(kv_full + st, static_cast<uint32_t>(j / kKvStages) & 1u, wc, kSiteAttnKv)) break;
+          if (!wait_spin(s_empty + sb, (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
+          if (!wait_spin(k_full + st, static_cast<uint32_t>(j / kKvStages) & 1u, wc, kSiteAttnKv)) break;
           tc_fence_after_sync();
           const uint32_t k_base = smem_u32(sK + st * kTileBytes);
 #pragma unroll
@@ -172,137 +260,177 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
                       idesc_s, kk > 0 ? 1u : 0u);
           }
           umma_commit(s_full + sb);
+          umma_commit(k_empty + st);
         }
         if (j >= 1) {
           const int jj = j - 1;
+          const int pb = jj & 1;
           const int st = jj % kKvStages;
-          if (!wait_bounded(p_full, static_cast<uint32_t>(jj) & 1u, wc, kSiteAttnP)) break;
+          if (!wait_spin(p_full + pb, static_cast<uint32_t>(jj >> 1) & 1u, wc, kSiteAttnP)) break;
+          if (!wait_spin(v_full + st, static_cast<uint32_t>(jj / kKvStages) & 1u, wc, kSiteAttnKv)) break;
           tc_fence_after_sync();
+          const uint32_t p_base = smem_u32(sP + pb * kTileBytes);
           const uint32_t v_base = smem_u32(sV + st * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kKTile / 16; ++kk) {
             const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
             umma_bf16(o_tmem, sdesc_sw128(p_base + a_off, 16, 1024), sdesc_sw128(v_base + kk * 2048, kAtom, 1024),
-                      idesc_pv, kk > 0 ? 1u : 0u);
+                      idesc_pv, (jj | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(pv_done);
-          umma_commit(kv_empty + st);
+          umma_commit(pv_done + pb);
+          umma_commit(v_empty + st);
         }
       }
       umma_commit(drain);
       wait_drain(drain, 0, p.timeout_ns);
     }
   } else {
-    // -------------------------------------------------------------------- softmax (warps 2..5)
+    // -------------------------------------------------------------------- softmax (warps 2..9)
+    // Warps w and w + 4 share TMEM lane quadrant w % 4 (query rows) and split every tile's keys: half 0
+    // takes keys 0..63 (P atom column 0, O columns 0..63), half 1 keys 64..127 (atom column 1, O columns
+    // 64..127).  The halves exchange the row maximum once per tile through shared memory (a named
+    // barrier per pair); their row sums combine at the end.  m is the row's reference maximum (log2
+    // units): exponents are taken against it and O, l are kept relative to it; it moves (and O, l are
+    // rescaled) only when a tile's maximum exceeds it by more than kRescaleLog2, so exp2(s - m) <= 2^8.
+    constexpr float kRescaleLog2 = 8.f;
+    __shared__ float xchg[2][kQTile];  // [half][row]: the tile's row maximum, at the end the row sum
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int pair_bar = 1 + quad;        // named barrier of the two warps of this quadrant
     const int r = quad * 32 + static_cast<int>(lane);  // row within the tile = TMEM lane
     const int q = qt * kQTile + r;                      // query position
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    float o[kHd];
-#pragma unroll
-    for (int e = 0; e < kHd; ++e) o[e] = 0.f;
-    float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
-      const int sb = j & 1;
+      const int sb = j & 1, pb = j & 1;
       int w_ok = 1;
-      if (lane == 0) w_ok = wait_bounded(s_full + sb, static_cast<uint32_t>(j >> 1) & 1u, wc, kSiteAttnS) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+      if (lane == 0) w_ok = wait_spin(s_full + sb, static_cast<uint32_t>(j >> 1) & 1u, wc, kSiteAttnS) ? 1 : 0;
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      // both warps of the pair learn each other's outcome at the barrier below, so they leave together
+      tc_fence_after_sync();
+      float sc[2][32];  // this half's 64 scores, then their log2-scaled values
+      if (w_ok) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(sb * 128 + 64 * half + 32 * c), sc[c]);
+        tmem_wait_ld();
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0 && w_ok) mbar_arrive(s_empty + sb);
+      const int key0 = j * kKTile + 64 * half;
+      const int key_end = p.causal ? min(p.S, q + 1) : p.S;  // visible keys: [0, key_end)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sc[c][i] = key0 + 32 * c + i < key_end ? sc[c][i] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sc[c][i]);
+        }
+      // Both warps of the pair pass the same named barriers: a failed wait anywhere in a tile travels to
+      // the partner as NaN through the next exchange, and the pair leaves the loop there together.
+      xchg[half][r] = ok && w_ok ? mx : NAN;
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+      const float other = xchg[half ^ 1][r];
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");  // both read before the next write
+      if (!(ok && w_ok) || __any_sync(0xffffffffu, isnan(other))) {
         ok = false;
         break;
       }
-      tc_fence_after_sync();
-      const uint32_t s_tmem = lane_base + static_cast<uint32_t>(sb * 128);
-      const int key0 = j * kKTile;
-      // a key is visible when it is in the sequence and, for causal attention, not after the query
-      const int key_end = p.causal ? min(p.S, q + 1) : p.S;
-      // pass 1: row maximum of this tile (scaled to log2 units)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_load_32cols(s_tmem + static_cast<uint32_t>(32 * c), v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key0 + 32 * c + i < key_end) mx = fmaxf(mx, v[i] * p.scale_log2);
-      }
-      const float m_new = fmaxf(m, mx);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;  // a row with nothing visible yet keeps p = 0
-      const float alpha = m == -INFINITY ? 0.f : exp2f(m - m_use);
-      // the previous tile's P V, rescaled into the running accumulator (its P buffer is then free)
-      if (j >= 1) {
-        if (lane == 0) w_ok = wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      mx = fmaxf(mx, other);
+      const bool move = mx > m + kRescaleLog2;
+      const float m_new = move ? mx : m;
+      const float alpha = move ? (m == -INFINITY ? 0.f : ex2_approx(m - m_new)) : 1.f;
+      l *= alpha;
+      // O (the tiles before j, once their P V is done) rescaled in TMEM where a row of the warp moved;
+      // each half rescales its 64 columns
+      if (j >= 1 && __any_sync(0xffffffffu, move)) {
+        const int pj = j - 1;
+        if (lane == 0)
+          w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-          ok = false;
-          break;
+          ok = false;  // finish the tile without touching TMEM or P; the next exchange ends the pair
+          continue;
         }
         tc_fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < kHd / 32; ++c) {
-          float v[32];
-          tmem_load_32cols(lane_base + 256u + static_cast<uint32_t>(32 * c), v);
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t addr = lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c);
+          uint32_t o[32];
+          tmem_ld32_nowait(addr, o);
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = o[32 * c + i] * alpha_prev + v[i];
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(addr, o);
         }
+        tmem_wait_st();
       }
-      // pass 2: P = exp2(S scale - m) in bf16 into the swizzled K-major tile, row sum
-      float psum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_load_32cols(s_tmem + static_cast<uint32_t>(32 * c), v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float pv = key0 + 32 * c + i < key_end ? exp2f(v[i] * p.scale_log2 - m_use) : 0.f;
-          v[i] = pv;
-          psum += pv;
-        }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int chunk = 4 * c + g;  // 8-key chunk 0..15
-          uint8_t* dst = sP + (chunk >> 3) * kAtom + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) =
-              make_uint4(pack_bf16x2(v[8 * g], v[8 * g + 1]), pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
-                         pack_bf16x2(v[8 * g + 4], v[8 * g + 5]), pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
-        }
-      }
-      l = l * alpha + psum;
       m = m_new;
-      alpha_prev = alpha;
-      // S buffer and P tile handed over: TMEM reads complete, shared-memory writes visible to the MMAs
+      const float m_use = m == -INFINITY ? 0.f : m;  // a row with nothing visible yet keeps p = 0
+      // P_j into buffer j % 2, once the P V that last read that buffer (tile j - 2) is done
+      if (j >= 2) {
+        const int pj = j - 2;
+        if (lane == 0)
+          w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;  // as above
+          continue;
+        }
+      }
+      uint8_t* pbuf = sP + pb * kTileBytes + half * kAtom;
+      float psum = 0.f;
+#pragma unroll
+      for (int chunk = 0; chunk < 8; ++chunk) {  // 8 keys per 16-byte chunk
+        float e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          e[i] = ex2_approx(sc[chunk >> 2][8 * (chunk & 3) + i] - m_use);
+          psum += e[i];
+        }
+        uint8_t* dst = pbuf + r * 128 + ((chunk ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                                                    pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+      }
+      l += psum;
+      // P_j (and any rescaled O) handed to the MMA: shared-memory writes visible to the async proxy
       tc_fence_before_sync();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(s_empty + sb);
-        mbar_arrive(p_full);
-      }
+      if (lane == 0) mbar_arrive(p_full + pb);
     }
-    if (ok && nk > 0) {
+    // the row sum of both halves (the pair left the loop at the same tile: the exchange buffer is free)
+    xchg[half][r] = ok ? l : NAN;
+    asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+    const float l_all = xchg[0][r] + xchg[1][r];
+    if (ok && !isnan(l_all) && nk > 0) {
+      const int pj = nk - 1;
       int w_ok = 1;
-      if (lane == 0) w_ok = wait_bounded(pv_done, static_cast<uint32_t>(nk - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0;
-      if (ok) {
+      if (lane == 0)
+        w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, w_ok, 0)) {
         tc_fence_after_sync();
+        uint32_t o[2][32];
 #pragma unroll
-        for (int c = 0; c < kHd / 32; ++c) {
-          float v[32];
-          tmem_load_32cols(lane_base + 256u + static_cast<uint32_t>(32 * c), v);
+        for (int c = 0; c < 2; ++c)
+          tmem_ld32_nowait(lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
+        tmem_wait_ld();
+        if (q < p.S) {
+          const float inv_l = l_all > 0.f ? 1.f / l_all : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                (static_cast<long long>(q) * p.B + b) *
+                                                    (static_cast<long long>(p.H) * kHd) +
+                                                static_cast<long long>(h) * kHd + 64 * half);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = o[32 * c + i] * alpha_prev + v[i];
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t* y = o[g / 4] + 8 * (g % 4);
+            dst[g] = make_uint4(pack_bf16x2(__uint_as_float(y[0]) * inv_l, __uint_as_float(y[1]) * inv_l),
+                                pack_bf16x2(__uint_as_float(y[2]) * inv_l, __uint_as_float(y[3]) * inv_l),
+                                pack_bf16x2(__uint_as_float(y[4]) * inv_l, __uint_as_float(y[5]) * inv_l),
+                                pack_bf16x2(__uint_as_float(y[6]) * inv_l, __uint_as_float(y[7]) * inv_l));
+          }
         }
-      }
-    }
-    if (ok && q < p.S) {
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                            (static_cast<long long>(q) * p.B + b) * (static_cast<long long>(p.H) * kHd) +
-                                            static_cast<long long>(h) * kHd);
-#pragma unroll
-      for (int g = 0; g < kHd / 8; ++g) {
-        const float* y = o + 8 * g;
-        dst[g] = make_uint4(pack_bf16x2(y[0] * inv_l, y[1] * inv_l), pack_bf16x2(y[2] * inv_l, y[3] * inv_l),
-                            pack_bf16x2(y[4] * inv_l, y[5] * inv_l), pack_bf16x2(y[6] * inv_l, y[7] * inv_l));
       }
     }
   }
@@ -346,7 +474,7 @@ bool make_part_map(CUtensorMap* m, const void* qkv, int part, int S, int B, int 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kAttnSmem = 1024 + (2 + 2 * kKvStages) * kTileBytes + 256;
+constexpr size_t kAttnSmem = 1024 + (3 + 2 * kKvStages) * kTileBytes + 256;
 
 cudaError_t launch_attention(const void* qkv, int S, int B, int H, bool causal, void* out, const DeviceCtx& ctx,
                              cudaStream_t s) {
