@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
       // both warps of the pair learn each other's outcome at the barrier below, so they leave together
       tc_fence_after_sync();
-      float sc[2][32];  // this half's 64 scores, then their log2-scaled values
+      float sc[2][32];  // this half's 64 raw scores
       if (w_ok) {
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -321,14 +321,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       if (lane == 0 && w_ok) mbar_arrive(s_empty + sb);
       const int key0 = j * kKTile + 64 * half;
       const int key_end = p.causal ? min(p.S, q + 1) : p.S;  // visible keys: [0, key_end)
+      // raw scores; invisible keys become -inf (only tiles that reach past some row's last key need it)
+      if (!__all_sync(0xffffffffu, key0 + 64 <= key_end)) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (key0 + 32 * c + i >= key_end) sc[c][i] = -INFINITY;
+      }
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sc[c][i] = key0 + 32 * c + i < key_end ? sc[c][i] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sc[c][i]);
-        }
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sc[c][i]);
+      mx *= p.scale_log2;  // the scale is positive: the maximum of the scaled scores
       // Both warps of the pair pass the same named barriers: a failed wait anywhere in a tile travels to
       // the partner as NaN through the next exchange, and the pair leaves the loop there together.
       xchg[half][r] = ok && w_ok ? mx : NAN;
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
         float e[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          e[i] = ex2_approx(sc[chunk >> 2][8 * (chunk & 3) + i] - m_use);
+          e[i] = ex2_approx(fmaf(sc[chunk >> 2][8 * (chunk & 3) + i], p.scale_log2, -m_use));
           psum += e[i];
         }
         uint8_t* dst = pbuf + r * 128 + ((chunk ^ (r & 7)) << 4);
