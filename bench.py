@@ -69,7 +69,7 @@ def kernel_source_digest(segment=None):
     return h.hexdigest()[:16]
 
 
-def measured_traffic(segment):
+def measured_traffic(segment, workload=None):
     """DRAM bytes per launch of `segment` from the committed ncu capture, or None if its kernels changed since."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
@@ -78,6 +78,8 @@ def measured_traffic(segment):
         d = json.load(fh)
     entry = d.get("segments", {}).get(segment)
     if entry is None or entry.get("source_digest") != kernel_source_digest(segment):
+        return None
+    if workload is not None and d.get("workload") != workload:
         return None
     return entry.get("bytes_per_launch")
 
@@ -700,13 +702,13 @@ def run_ours(args, w):
             ach = work / (avg * 1e-3) / 1e12
             peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
             kern[name] = {"ms": round(avg, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / peak, 3),
-                          "dram_bytes": measured_traffic(name)}
+                          "dram_bytes": measured_traffic(name, w.name)}
             if dom is None or avg > dom[1]:
                 dom = (name, avg, work, ach, peak)
         else:
             ach = work / (avg * 1e-3) / 1e9
             kern[name] = {"ms": round(avg, 4), "GB/s": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 3),
-                          "launches": nl, "dram_bytes": measured_traffic(name)}
+                          "launches": nl, "dram_bytes": measured_traffic(name, w.name)}
     e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
@@ -740,7 +742,7 @@ def run_ours(args, w):
                    "l2": "inputs larger than L2 (weights alone 2 x d x F x 2 bytes)",
                    "host_wall_s": round(wall, 3)},
         "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": round(dom[3], 1), "peak": dom[4],
-                     "unit": "TFLOP/s", "frac": round(dom[3] / dom[4], 3), "traffic": measured_traffic(dom[0]),
+                     "unit": "TFLOP/s", "frac": round(dom[3] / dom[4], 3), "traffic": measured_traffic(dom[0], w.name),
                      "peak_kind": f"{pk_kind} bf16 sustained"},
         "kernels": kern,
         "e2e": {"value": round(whole_job_rate(flops, args.steps, world, e2e_ms * args.steps) / 1e12, 2),

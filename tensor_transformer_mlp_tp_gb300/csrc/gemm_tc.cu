@@ -17,6 +17,7 @@ constexpr int kPairStages = 6;   // CTA pair: 32 KB per CTA per k-block
 constexpr int kEpiWarps = 4;
 constexpr int kBN = 256;
 constexpr int kGroupM = 16;      // raster group, in 128-row blocks
+constexpr int kShortK = 2048;    // at or below: the GeLU epilogue runs balanced over all four sub-partitions
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -79,10 +80,10 @@ int max_pairs(K kern, int smem, int threads, int dev_cache_slot, int* cache) {
   return n;
 }
 
-template <bool AMN, bool BMN, int EPI, bool FP8 = false>
+template <bool AMN, bool BMN, int EPI, bool FP8 = false, bool BAL = false>
 cudaError_t run_pair(const GemmParams& p, cudaStream_t s) {
   using S = PairShape<kBN, kPairStages, kEpiWarps>;
-  auto kern = k_gemm_tc2<kBN, AMN, BMN, EPI, kPairStages, kEpiWarps, FP8>;
+  auto kern = k_gemm_tc2<kBN, AMN, BMN, EPI, kPairStages, kEpiWarps, FP8, BAL>;
   static int cache[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -164,8 +165,8 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   p.err = ctx.err;
   p.timeout_ns = ctx.timeout_ns;
   switch (g.epi) {
-    case kEpiBiasGeluQ: return run_pair<false, false, kEpiBiasGeluQ, true>(p, s);
-    case kEpiDGeluQ: return run_pair<false, false, kEpiDGeluQ, true>(p, s);
+    case kEpiBiasGeluQ: return run_pair<false, false, kEpiBiasGeluQ, true, true>(p, s);
+    case kEpiDGeluQ: return run_pair<false, false, kEpiDGeluQ, true, true>(p, s);
     case kEpiStore: return run_pair<false, false, kEpiStore, true>(p, s);
     default: return cudaErrorNotSupported;
   }
@@ -222,6 +223,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
   if (pair) {
     switch (g.epi) {
       case kEpiBiasGelu:
+        // with a short K the bias + GeLU epilogue outlasts a tile's MMAs: spread it over all sub-partitions
+        if (!amn && bmn && g.K <= kShortK) return run_pair<false, true, kEpiBiasGelu, false, true>(p, s);
         if (!amn && bmn) return run_pair<false, true, kEpiBiasGelu>(p, s);
         break;
       case kEpiBias:

@@ -49,14 +49,17 @@ struct PairShape {
 
 // FP8: E4M3 A and B (both K-major), .kind::f8f6f4; a 128-byte k-block row then holds 128 elements and
 // one UMMA covers 32 of them, so shared-memory layouts, descriptors and byte counts are those of bf16.
-template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS, bool FP8 = false>
+// BAL: every epilogue warp reads TMEM itself and the epilogue math is spread over all four SM
+// sub-partitions (for epilogue-bound launches: short K or the FP8 rate); otherwise the two warps on the
+// TMA and MMA sub-partitions only copy TMEM to shared memory for the helper warps.
+template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS, bool FP8 = false, bool BAL = false>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __grid_constant__ GemmParams p) {
   static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
   static_assert(FP8 || (EPI != kEpiBiasGeluQ && EPI != kEpiDGeluQ), "the quantising epilogues follow FP8 operands");
   constexpr bool kAux = EPI == kEpiDGelu || EPI == kEpiDGeluQ;  // reads the pre-activation tile
   // FP8 GEMMs with a GeLU / GeLU' epilogue are epilogue-bound at the doubled MMA rate: there every epilogue
   // warp reads TMEM itself and the math is spread over all four SM sub-partitions (see the epilogue).
-  constexpr bool kBalanced = FP8 && (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ);
+  constexpr bool kBalanced = BAL;
   constexpr int kTemptyArrivals = 2 * (kBalanced ? EPI_WARPS + 2 : EPI_WARPS);
   constexpr int kKElems = FP8 ? 128 : kBK;  // elements of one 128-byte k-block row
   using S = PairShape<BN, STAGES, EPI_WARPS>;
@@ -227,7 +230,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
     const int quad = warp & 3;
     const int c_begin = warp >= 6 ? BN / 2 : 0;
     const int c_end = (warp == 2 || warp == 3) ? BN / 2 : BN;
-    EpiState est{1.f / (__ldg(p.scale_a) * __ldg(p.scale_b)), __ldg(p.scale_out), 0.f};
+    EpiState est{1.f, 1.f, 0.f};
+    if constexpr (FP8) est.descale = 1.f / (__ldg(p.scale_a) * __ldg(p.scale_b));
+    if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) est.scale_out = __ldg(p.scale_out);
     int local = 0;
     for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
       int shard, mb, nb;
@@ -272,7 +277,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
     }
-    if (p.amax_out != nullptr) amax_combine_warp(p.amax_out, est.amax);
+    if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) {
+      if (p.amax_out != nullptr) amax_combine_warp(p.amax_out, est.amax);
+    }
   } else {
     // -------------------------------------------------------------------- epilogue (both CTAs)
     const bool quad_warp = warp < 6;
