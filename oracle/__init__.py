@@ -549,6 +549,66 @@ def attention_tp(X, Wqkv, bqkv, Wo, bo, H: int, N: int, B: int, causal: bool, re
     return Y
 
 
+def attention_head_backward(Q, K, V, dO, causal: bool):
+    """Gradients of :func:`attention_head` (chain rule): with ``P = softmax(Q Kᵀ/√hd)`` and ``O = P V``,
+    ``dV = Pᵀ dO``, ``dP = dO Vᵀ``, ``dS = P ⊙ (dP - D)`` with ``D = rowsum(dO ⊙ O)``,
+    ``dQ = dS K / √hd``, ``dK = dSᵀ Q / √hd``."""
+    Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
+    hd = Q.shape[1]
+    scores = Q @ K.T / math.sqrt(hd)
+    if causal:
+        S = Q.shape[0]
+        scores = np.where(np.tril(np.ones((S, S), dtype=bool)), scores, -np.inf)
+    scores = scores - scores.max(axis=1, keepdims=True)
+    P = np.exp(scores)
+    P = P / P.sum(axis=1, keepdims=True)
+    O = P @ V
+    dV = P.T @ dO
+    dP = dO @ V.T
+    D = (dO * O).sum(axis=1, keepdims=True)
+    dS = P * (dP - D)
+    return dS @ K / math.sqrt(hd), dS.T @ Q / math.sqrt(hd), dV
+
+
+def attention_tp_backward(X, Wqkv, bqkv, Wo, bo, H: int, N: int, B: int, causal: bool, dY):
+    """Gradients of :func:`attention_tp` (chain rule), shard by shard as the forward splits the work:
+    ``dO_i = dY Wo[rows of shard i]ᵀ``, ``dWo[rows of shard i] = O_iᵀ dY``, ``dbo = Σ_rows dY``; per
+    head the attention backward; the projection ``dWqkv = Xᵀ dQKV``, ``dbqkv = Σ_rows dQKV`` and
+    ``dX = Σ_i dQKV_i Wqkv_iᵀ`` (the backward AllReduce over the shards' columns)."""
+    X = np.asarray(X, dtype=np.float64)
+    Wqkv = np.asarray(Wqkv, dtype=np.float64)
+    Wo = np.asarray(Wo, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    T, d = X.shape
+    hd = d // H
+    bias_qkv = np.zeros(3 * d) if bqkv is None else np.asarray(bqkv, dtype=np.float64)
+    QKV = X @ Wqkv + bias_qkv
+    dQKV = np.zeros_like(QKV)
+    dWo = np.zeros_like(Wo)
+    dX_parts = []
+    for lo, hi in head_ranges(H, N):
+        cols = np.concatenate([np.arange(part * d + lo * hd, part * d + hi * hd) for part in range(3)])
+        O_i = np.zeros((T, (hi - lo) * hd))
+        for h in range(lo, hi):
+            c = [slice(part * d + h * hd, part * d + (h + 1) * hd) for part in range(3)]
+            for b in range(B):
+                rows = slice(b, T, B)
+                O_i[rows, (h - lo) * hd:(h - lo + 1) * hd] = attention_head(QKV[rows, c[0]], QKV[rows, c[1]],
+                                                                             QKV[rows, c[2]], causal)
+        dO_i = dY @ Wo[lo * hd:hi * hd, :].T
+        dWo[lo * hd:hi * hd, :] = O_i.T @ dY
+        for h in range(lo, hi):
+            c = [slice(part * d + h * hd, part * d + (h + 1) * hd) for part in range(3)]
+            for b in range(B):
+                rows = slice(b, T, B)
+                dq, dk, dv = attention_head_backward(QKV[rows, c[0]], QKV[rows, c[1]], QKV[rows, c[2]],
+                                                     dO_i[rows, (h - lo) * hd:(h - lo + 1) * hd], causal)
+                dQKV[rows, c[0]], dQKV[rows, c[1]], dQKV[rows, c[2]] = dq, dk, dv
+        dX_parts.append(dQKV[:, cols] @ Wqkv[:, cols].T)
+    return {"dX": all_reduce(dX_parts), "dWqkv": X.T @ dQKV, "dbqkv": dQKV.sum(axis=0), "dWo": dWo,
+            "dbo": dY.sum(axis=0), "dQKV": dQKV}
+
+
 # --------------------------------------------------------------------------- backward (chain rule)
 
 def mlp_backward(X, A, B, b, dY):

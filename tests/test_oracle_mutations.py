@@ -167,7 +167,21 @@ def _attention_head_mask_off_by_one(Q, K, V, causal):
     return (w / w.sum(axis=1, keepdims=True)) @ V
 
 
+def _attention_head_backward_no_D(Q, K, V, dO, causal):
+    Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
+    hd = Q.shape[1]
+    sc = Q @ K.T / np.sqrt(hd)
+    if causal:
+        sc = np.where(np.tril(np.ones(sc.shape, dtype=bool)), sc, -np.inf)
+    P = np.exp(sc - sc.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    dS = P * (dO @ V.T)                                    # the softmax Jacobian's -D term dropped
+    return dS @ K / np.sqrt(hd), dS.T @ Q / np.sqrt(hd), P.T @ dO
+
+
 CASES = [
+    ("attention_head_backward", _attention_head_backward_no_D,
+     lambda: pins.test_attention_head_backward_autograd_witness(True)),
     ("attention_head", _attention_head_unscaled, lambda: pins.test_attention_head_torch_witness(False)),
     ("attention_head", _attention_head_mask_off_by_one, lambda: pins.test_attention_head_bruteforce()),
     ("head_ranges", lambda H, N: [(lo, hi) for lo, hi in _orig["head_ranges"](H, N)][::-1],

@@ -806,3 +806,50 @@ def test_attention_causal_outputs_ignore_later_tokens():
     Y3 = oracle.attention_tp(X3, Wqkv, bqkv, Wo, bo, H, 2, B, False)
     Y0 = oracle.attention_tp(X, Wqkv, bqkv, Wo, bo, H, 2, B, False)
     assert np.array_equal(Y3[0::B], Y0[0::B])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_head_backward_autograd_witness(causal):
+    rng = np.random.default_rng(9)
+    Q, K, V, dO = (rng.normal(size=(7, 4)) for _ in range(4))
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (Q, K, V))
+    torch.nn.functional.scaled_dot_product_attention(tq[None, None], tk[None, None], tv[None, None],
+                                                     is_causal=causal)[0, 0].backward(torch.from_numpy(dO))
+    dq, dk, dv = oracle.attention_head_backward(Q, K, V, dO, causal)
+    assert rel(dq, tq.grad.numpy()) < 1e-12
+    assert rel(dk, tk.grad.numpy()) < 1e-12
+    assert rel(dv, tv.grad.numpy()) < 1e-12
+
+
+@pytest.mark.parametrize("causal,N", [(True, 2), (False, 4)])
+def test_attention_tp_backward_autograd_witness(causal, N):
+    S, B, d, H = 6, 2, 16, 4
+    X, Wqkv, bqkv, Wo, bo = _attn_problem(S, B, d, H, seed=3)
+    dY = np.random.default_rng(4).normal(size=(S * B, d))
+    hd = d // H
+    tt = [torch.tensor(a, requires_grad=True) for a in (X, Wqkv, bqkv, Wo, bo)]
+    qkv = (tt[0] @ tt[1] + tt[2]).reshape(S, B, 3 * d)
+    q, k, v = (qkv[..., p * d:(p + 1) * d].reshape(S, B, H, hd).permute(1, 2, 0, 3) for p in range(3))
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal).permute(2, 0, 1, 3)
+    (o.reshape(S * B, d) @ tt[3] + tt[4]).backward(torch.from_numpy(dY))
+    g = oracle.attention_tp_backward(X, Wqkv, bqkv, Wo, bo, H, N, B, causal, dY)
+    for key, i in (("dX", 0), ("dWqkv", 1), ("dbqkv", 2), ("dWo", 3), ("dbo", 4)):
+        assert rel(g[key], tt[i].grad.numpy()) < 1e-12, key
+
+
+def test_attention_head_backward_finite_difference():
+    """Central differences of a scalar loss <dO, O> for a few entries of Q, K and V."""
+    rng = np.random.default_rng(10)
+    Q, K, V, dO = (rng.normal(size=(5, 3)) for _ in range(4))
+    dq, dk, dv = oracle.attention_head_backward(Q, K, V, dO, True)
+    loss = lambda q, k, v: float((oracle.attention_head(q, k, v, True) * dO).sum())
+    eps = 1e-6
+    for name, A, G in (("Q", Q, dq), ("K", K, dk), ("V", V, dv)):
+        for (i, j) in ((0, 0), (2, 1), (4, 2)):
+            Ap, Am = A.copy(), A.copy()
+            Ap[i, j] += eps
+            Am[i, j] -= eps
+            args_p = [Ap if n == name else M for n, M in (("Q", Q), ("K", K), ("V", V))]
+            args_m = [Am if n == name else M for n, M in (("Q", Q), ("K", K), ("V", V))]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - G[i, j]) < 1e-7 * max(1.0, abs(fd)), (name, i, j)
