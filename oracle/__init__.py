@@ -549,10 +549,11 @@ def attention_tp(X, Wqkv, bqkv, Wo, bo, H: int, N: int, B: int, causal: bool, re
     return Y
 
 
-def attention_head_backward(Q, K, V, dO, causal: bool):
+def attention_head_backward(Q, K, V, dO, causal: bool, O=None):
     """Gradients of :func:`attention_head` (chain rule): with ``P = softmax(Q Kᵀ/√hd)`` and ``O = P V``,
     ``dV = Pᵀ dO``, ``dP = dO Vᵀ``, ``dS = P ⊙ (dP - D)`` with ``D = rowsum(dO ⊙ O)``,
-    ``dQ = dS K / √hd``, ``dK = dSᵀ Q / √hd``."""
+    ``dQ = dS K / √hd``, ``dK = dSᵀ Q / √hd``.  ``O``: None for the exact forward output, or the output
+    as the forward saved it (e.g. rounded to bf16), from which ``D`` is then formed."""
     Q, K, V, dO = (np.asarray(a, dtype=np.float64) for a in (Q, K, V, dO))
     hd = Q.shape[1]
     scores = Q @ K.T / math.sqrt(hd)
@@ -562,7 +563,7 @@ def attention_head_backward(Q, K, V, dO, causal: bool):
     scores = scores - scores.max(axis=1, keepdims=True)
     P = np.exp(scores)
     P = P / P.sum(axis=1, keepdims=True)
-    O = P @ V
+    O = P @ V if O is None else np.asarray(O, dtype=np.float64)
     dV = P.T @ dO
     dP = dO @ V.T
     D = (dO * O).sum(axis=1, keepdims=True)

@@ -837,6 +837,27 @@ def test_attention_tp_backward_autograd_witness(causal, N):
         assert rel(g[key], tt[i].grad.numpy()) < 1e-12, key
 
 
+def test_attention_head_backward_saved_output():
+    """D formed from a saved (perturbed) output O': the exact gradients' softmax rows sum to zero, so with
+    a key column held at a constant c, dQ's column is then -c·rowsum(dO ⊙ (O' - O))/√hd; dV does not
+    depend on D; passing the exact output reproduces the default."""
+    rng = np.random.default_rng(11)
+    Q, K, V, dO = (rng.normal(size=(6, 4)) for _ in range(4))
+    c = 1.5
+    K[:, 0] = c
+    O = oracle.attention_head(Q, K, V, True)
+    exact = oracle.attention_head_backward(Q, K, V, dO, True)
+    same = oracle.attention_head_backward(Q, K, V, dO, True, O=O)
+    for a, b in zip(exact, same):
+        assert rel(a, b) < 1e-13
+    assert np.max(np.abs(exact[0][:, 0])) < 1e-12
+    O_saved = O + 0.01 * rng.normal(size=O.shape)
+    dq, dk, dv = oracle.attention_head_backward(Q, K, V, dO, True, O=O_saved)
+    delta = (dO * (O_saved - O)).sum(axis=1)
+    assert np.allclose(dq[:, 0], -c * delta / 2.0, atol=1e-12, rtol=0)  # sqrt(hd) = 2
+    assert rel(dv, exact[2]) < 1e-14
+
+
 def test_attention_head_backward_finite_difference():
     """Central differences of a scalar loss <dO, O> for a few entries of Q, K and V."""
     rng = np.random.default_rng(10)
