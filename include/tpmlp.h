@@ -506,19 +506,57 @@ TPMLP_API tpmlp_status tpmlp_attention_workspace_size(int64_t S, int64_t B, int6
 /* Attention core: for every batch element b and head h,
  * O[:, h] = softmax(Q_h K_h^T / sqrt(hd)) V_h over that batch element's S
  * positions, causal (position s sees keys <= s) when causal == 1.  fp32
- * scores and accumulation, bf16 in and out.  QKV [S B x 3 H hd], O [S B x H hd]. */
+ * scores and accumulation, bf16 in and out.  QKV [S B x 3 H hd], O [S B x H hd].
+ * LSE: NULL, or fp32 [B H x S_pad] with S_pad = 128 ceil(S / 128) (16-byte
+ * aligned): row (b H + h) entry s = log2 of sum_k exp2(q_s . k_k log2(e) /
+ * sqrt(hd)) over the keys s sees, the statistics the backward re-uses;
+ * entries S .. S_pad - 1 are left unwritten. */
 TPMLP_API tpmlp_status tpmlp_attention_core(const void* QKV, int64_t S, int64_t B, int64_t H, int64_t head_dim,
-                                            int causal, void* O, tpmlp_stream_t stream);
+                                            int causal, void* O, float* LSE, tpmlp_stream_t stream);
+
+/* Bytes of workspace for tpmlp_attention_core_backward (the first part:
+ * B H S_pad floats) and tpmlp_attention_tp_backward (all of it: also dO,
+ * dQKV and column-sum partials). */
+TPMLP_API tpmlp_status tpmlp_attention_backward_workspace_size(int64_t S, int64_t B, int64_t H, int64_t head_dim,
+                                                               size_t* bytes);
+
+/* Attention core backward (the chain rule through softmax, per batch element
+ * and head): with P = softmax(Q K^T / sqrt(hd)) re-formed from LSE,
+ * D = rowsum(dO . O), dV = P^T dO, dS = P . (dO V^T - D),
+ * dQ = dS K / sqrt(hd), dK = dS^T Q / sqrt(hd).  QKV, O, LSE: the forward's
+ * (LSE as tpmlp_attention_core writes it); dO [S B x H hd]; dQKV [S B x 3 H hd]
+ * receives dQ | dK | dV in QKV's layout.  fp32 accumulation; deterministic
+ * (no atomics).  Workspace 256-byte aligned. */
+TPMLP_API tpmlp_status tpmlp_attention_core_backward(const void* QKV, const void* O, const void* dO,
+                                                     const float* LSE, int64_t S, int64_t B, int64_t H,
+                                                     int64_t head_dim, int causal, void* dQKV, void* workspace,
+                                                     size_t workspace_bytes, tpmlp_stream_t stream);
 
 /* The attention block: QKV = X Wqkv + bqkv (bqkv [3d] or NULL), O = attention
  * core, Y = O Wo + bo (Wo [d x d] row-split by heads, bo [d] or NULL, added
  * after the shard sum).  X, Y [S B x d]; Wqkv [d x 3d]; H % n_shards == 0.
- * QKV_out, O_out: NULL or buffers that keep the intermediates.  Workspace:
- * tpmlp_attention_workspace_size. */
+ * QKV_out, O_out, LSE_out: NULL or buffers that keep the intermediates (what
+ * tpmlp_attention_tp_backward needs).  Workspace: tpmlp_attention_workspace_size. */
 TPMLP_API tpmlp_status tpmlp_attention_tp_forward(const void* X, const void* Wqkv, const void* bqkv, const void* Wo,
                                                   const void* bo, int64_t S, int64_t B, int64_t H, int32_t n_shards,
-                                                  int causal, void* Y, void* QKV_out, void* O_out, void* workspace,
-                                                  size_t workspace_bytes, tpmlp_stream_t stream);
+                                                  int causal, void* Y, void* QKV_out, void* O_out, float* LSE_out,
+                                                  void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Backward of the attention block (the same glossary and deep-dive sections:
+ * the conjugate of the forward's column/row split).  Row-parallel output
+ * projection: dO = dY Wo^T (every shard's rows of Wo), dWo = O^T dY,
+ * dbo = column sums of dY; the core backward into dQKV; column-parallel
+ * projection: dWqkv = X^T dQKV, dbqkv = column sums of dQKV, and
+ * dX = dQKV Wqkv^T, whose K loop over the 3d columns adds every shard's
+ * contribution (the backward all-reduce).  QKV, O, LSE: saved by
+ * tpmlp_attention_tp_forward.  dbqkv, dbo: NULL to skip.  dQKV_out: NULL, or a
+ * [S B x 3d] buffer that receives dQKV.  bf16 outputs, fp32 accumulation.
+ * Workspace: tpmlp_attention_backward_workspace_size, 256-byte aligned. */
+TPMLP_API tpmlp_status tpmlp_attention_tp_backward(const void* X, const void* Wqkv, const void* Wo, const void* QKV,
+                                                   const void* O, const float* LSE, const void* dY, int64_t S,
+                                                   int64_t B, int64_t H, int32_t n_shards, int causal, void* dX,
+                                                   void* dWqkv, void* dbqkv, void* dWo, void* dbo, void* dQKV_out,
+                                                   void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
 
 /* Failure-detection self test: launches one CTA that waits on a barrier no
  * thread ever arrives at, with a limit of `budget_us` microseconds (1 to

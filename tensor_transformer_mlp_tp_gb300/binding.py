@@ -98,10 +98,17 @@ _SIGS = {
                         _P, ctypes.c_int64, _P], ctypes.c_int),
     "tpmlp_attention_workspace_size": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
-    "tpmlp_attention_core": ([_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P],
-                             ctypes.c_int),
+    "tpmlp_attention_core": ([_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P,
+                              _P], ctypes.c_int),
+    "tpmlp_attention_backward_workspace_size": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "tpmlp_attention_core_backward": ([_P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_int, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_attention_tp_forward": ([_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
-                                    ctypes.c_int, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+                                    ctypes.c_int, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "tpmlp_attention_tp_backward": ([_P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int32, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+                                    ctypes.c_int),
     "tpmlp_sp_backward_fp8": ([_PP, _P, ctypes.c_float, _P, _P, _P, _P, _P, _PP, _FP, _FP, _SP, _PP, _P, _P, _P, _P,
                                _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
 }
@@ -511,19 +518,53 @@ def tpmlp_attention_workspace_size(S, B, H, head_dim=128):
     return n.value
 
 
-def tpmlp_attention_core(QKV, S, B, H, O, causal=False, head_dim=128, stream=None):
+def attention_lse_shape(S, B, H):
+    """Shape of the log-sum-exp statistics the attention forward saves: ``[B·H, 128·ceil(S/128)]``."""
+    return (B * H, (S + 127) // 128 * 128)
+
+
+def tpmlp_attention_core(QKV, S, B, H, O, causal=False, LSE=None, head_dim=128, stream=None):
     _check("tpmlp_attention_core", lib().tpmlp_attention_core(_ptr(QKV), S, B, H, head_dim, 1 if causal else 0, _ptr(O),
-                                                              _stream(stream)))
+                                                              _ptr(LSE), _stream(stream)))
+
+
+def tpmlp_attention_backward_workspace_size(S, B, H, head_dim=128):
+    n = ctypes.c_size_t(0)
+    _check("tpmlp_attention_backward_workspace_size",
+           lib().tpmlp_attention_backward_workspace_size(S, B, H, head_dim, ctypes.byref(n)))
+    return n.value
+
+
+def tpmlp_attention_core_backward(QKV, O, dO, LSE, S, B, H, dQKV, causal=False, head_dim=128, ws=None, stream=None):
+    if ws is None:
+        ws = torch.empty(max(tpmlp_attention_backward_workspace_size(S, B, H), 256), dtype=torch.uint8,
+                         device=QKV.device)
+    _check("tpmlp_attention_core_backward", lib().tpmlp_attention_core_backward(
+        _ptr(QKV), _ptr(O), _ptr(dO), _ptr(LSE), S, B, H, head_dim, 1 if causal else 0, _ptr(dQKV), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return dQKV
 
 
 def tpmlp_attention_tp_forward(X, Wqkv, Wo, S, B, H, N, Y, bqkv=None, bo=None, causal=False, QKV_out=None,
-                               O_out=None, ws=None, stream=None):
+                               O_out=None, LSE_out=None, ws=None, stream=None):
     if ws is None:
         ws = torch.empty(max(tpmlp_attention_workspace_size(S, B, H), 256), dtype=torch.uint8, device=X.device)
     _check("tpmlp_attention_tp_forward", lib().tpmlp_attention_tp_forward(
         _ptr(X), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo), S, B, H, N, 1 if causal else 0, _ptr(Y), _ptr(QKV_out),
-        _ptr(O_out), _ptr(ws), ws.numel(), _stream(stream)))
+        _ptr(O_out), _ptr(LSE_out), _ptr(ws), ws.numel(), _stream(stream)))
     return Y
+
+
+def tpmlp_attention_tp_backward(X, Wqkv, Wo, QKV, O, LSE, dY, S, B, H, N, dX, dWqkv, dWo, dbqkv=None, dbo=None,
+                                causal=False, dQKV_out=None, ws=None, stream=None):
+    if ws is None:
+        ws = torch.empty(max(tpmlp_attention_backward_workspace_size(S, B, H), 256), dtype=torch.uint8,
+                         device=X.device)
+    _check("tpmlp_attention_tp_backward", lib().tpmlp_attention_tp_backward(
+        _ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(QKV), _ptr(O), _ptr(LSE), _ptr(dY), S, B, H, N, 1 if causal else 0,
+        _ptr(dX), _ptr(dWqkv), _ptr(dbqkv), _ptr(dWo), _ptr(dbo), _ptr(dQKV_out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return dX
 
 
 def tpmlp_selftest_wait_timeout(budget_us: int, stream=None):

@@ -48,6 +48,8 @@ constexpr uint32_t kSiteAttnQ = 32, kSiteAttnKv = 33, kSiteAttnS = 34, kSiteAttn
 struct AttnParams {
   CUtensorMap tmQ, tmK, tmV;
   void* out;          // [T x d] bf16, row s B + b, columns h hd .. (h+1) hd
+  float* lse;         // nullptr, or [B H x s_pad] fp32: each row's log2 of sum exp2 (scores in log2 units)
+  int s_pad;          // S rounded up to whole 128-query tiles
   int S, B, H;
   int n_qtiles;
   int causal;
@@ -422,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
         for (int c = 0; c < 2; ++c)
           tmem_ld32_nowait(lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
         tmem_wait_ld();
+        if (p.lse != nullptr && half == 0 && q < p.S)
+          p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + q] = m + log2f(l_all);
         if (q < p.S) {
           const float inv_l = l_all > 0.f ? 1.f / l_all : 0.f;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
@@ -449,6 +453,521 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   }
 }
 
+// ----------------------------------------------------------------------------- attention backward
+
+// D[b, h, s] = sum_e dO[s B + b, h hd + e] O[s B + b, h hd + e] in fp32 ([B H x s_pad]): one warp per
+// (token, head), 4 elements per lane.
+__global__ void __launch_bounds__(256) k_attention_bwd_delta(const __nv_bfloat16* __restrict__ dO,
+                                                             const __nv_bfloat16* __restrict__ O, int S, int B, int H,
+                                                             int s_pad, float* __restrict__ D) {
+  const long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (item >= static_cast<long long>(S) * B * H) return;
+  const int h = static_cast<int>(item % H);
+  const long long t = item / H;  // token row s B + b
+  const long long off = t * (static_cast<long long>(H) * kHd) + static_cast<long long>(h) * kHd + 4 * lane;
+  const uint2 a = __ldg(reinterpret_cast<const uint2*>(dO + off));
+  const uint2 c = __ldg(reinterpret_cast<const uint2*>(O + off));
+  const float2 a0 = unpack_bf16x2(a.x), a1 = unpack_bf16x2(a.y), c0 = unpack_bf16x2(c.x), c1 = unpack_bf16x2(c.y);
+  float v = a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) {
+    const int sq = static_cast<int>(t / B), b = static_cast<int>(t % B);
+    D[(static_cast<long long>(b) * H + h) * s_pad + sq] = v;
+  }
+}
+
+struct AttnBwdParams {
+  CUtensorMap tmQ, tmK, tmV, tmdO;  // 4-D maps: Q, K, V parts of QKV; dO ([S, B, H, hd], O's layout)
+  const float* lse;                 // [B H x s_pad], log2 units
+  const float* delta;               // [B H x s_pad]
+  void* dqkv;                       // [T x 3 d] bf16: dQ, dK, dV in the QKV layout
+  int S, B, H, s_pad, n_tiles, causal;
+  float scale_log2;                 // log2(e) / sqrt(hd)
+  float scale;                      // 1 / sqrt(hd)
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+// bf16 row of 64 values (this half's columns) into the swizzled K-major tile buffer: row r, columns
+// 64 half .. 64 half + 63 (one atom column).
+__device__ __forceinline__ void store_half_row(uint8_t* buf, int half, int r, const float (&v)[2][32]) {
+#pragma unroll
+  for (int chunk = 0; chunk < 8; ++chunk) {
+    const float* e = v[chunk >> 2] + 8 * (chunk & 3);
+    uint8_t* dst = buf + half * kAtom + r * 128 + ((chunk ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                                                pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+  }
+}
+
+// dQ for one 128-query tile of one (batch, head): per key tile j, S_j = Q K_j^T and dP_j = dO V_j^T in
+// TMEM; the 8 compute warps (two per lane quadrant, 64 keys each) form P = exp2(S scale - lse) and
+// dS = P (dP - D) from the saved statistics (no reductions), write dS in bf16 to shared memory, and
+// dQ += dS K_j accumulates in TMEM (K as the MN-major operand); dQ / sqrt(hd) goes to dQKV.
+__global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_constant__ AttnBwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = sQ + kTileBytes;
+  uint8_t* sK = sdO + kTileBytes;                  // 2 stages
+  uint8_t* sV = sK + kKvStages * kTileBytes;       // 2 stages
+  uint8_t* sdS = sV + kKvStages * kTileBytes;      // 1 buffer
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sdS + kTileBytes);
+  uint64_t* q_full = bars;                          // Q and dO
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_empty = k_full + kKvStages;
+  uint64_t* v_full = k_empty + kKvStages;
+  uint64_t* v_empty = v_full + kKvStages;
+  uint64_t* s_full = v_empty + kKvStages;           // S_j and dP_j in TMEM
+  uint64_t* s_empty = s_full + 1;
+  uint64_t* ds_full = s_empty + 1;
+  uint64_t* dq_done = ds_full + 1;                  // dQ += dS K done (dS buffer free)
+  uint64_t* drain = dq_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const int qt = p.n_tiles - 1 - static_cast<int>(blockIdx.x % p.n_tiles);
+  const int bh = static_cast<int>(blockIdx.x / p.n_tiles);
+  const int b = bh % p.B, h = bh / p.B;
+  const int nk = p.causal ? min(p.n_tiles, qt + 1) : p.n_tiles;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 8);
+    mbar_init(ds_full, 8);
+    mbar_init(dq_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;  // S [0, 128), dP [128, 256), dQ [256, 384)
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+      load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
+      load_tile(sdO, &p.tmdO, q_full, h, b, qt * kQTile);
+      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
+      for (int j = 0; j < nk; ++j) {
+        const int st = j % kKvStages;
+        const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
+        if (!wait_spin(v_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(v_full + st, kTileBytes);
+        load_tile(sV + st * kTileBytes, &p.tmV, v_full + st, h, b, j * kKTile);
+        v_issued |= 1u << st;
+        v_par = (v_par & ~(1u << st)) | (ph << st);
+        if (!wait_spin(k_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(k_full + st, kTileBytes);
+        load_tile(sK + st * kTileBytes, &p.tmK, k_full + st, h, b, j * kKTile);
+        k_issued |= 1u << st;
+        k_par = (k_par & ~(1u << st)) | (ph << st);
+      }
+      wait_drain(q_full, 0, p.timeout_ns);
+      for (int s = 0; s < kKvStages; ++s) {
+        if (k_issued & (1u << s)) wait_drain(k_full + s, (k_par >> s) & 1u, p.timeout_ns);
+        if (v_issued & (1u << s)) wait_drain(v_full + s, (v_par >> s) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_kk = idesc_bf16_f32(kQTile, kKTile, false, false);  // both K-major
+      constexpr uint32_t idesc_mn = idesc_bf16_f32(kQTile, kHd, false, true);       // B MN-major
+      const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sdO), ds_base = smem_u32(sdS);
+      bool ok = wait_spin(q_full, 0, wc, kSiteAttnQ);
+      if (ok) tc_fence_after_sync();
+      // step j: S_j and dP_j (j < nk), then dQ += dS_{j-1} K_{j-1} (j >= 1)
+      for (int j = 0; ok && j <= nk; ++j) {
+        if (j < nk) {
+          const int st = j % kKvStages;
+          const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
+          if (!wait_spin(s_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
+          if (!wait_spin(k_full + st, ph, wc, kSiteAttnKv)) break;
+          if (!wait_spin(v_full + st, ph, wc, kSiteAttnKv)) break;
+          tc_fence_after_sync();
+          const uint32_t k_base = smem_u32(sK + st * kTileBytes), v_base = smem_u32(sV + st * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idesc_kk,
+                      kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base + 128, sdesc_sw128(do_base + off, 16, 1024), sdesc_sw128(v_base + off, 16, 1024),
+                      idesc_kk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
+          umma_commit(v_empty + st);
+        }
+        if (j >= 1) {
+          const int jj = j - 1;
+          const int st = jj % kKvStages;
+          if (!wait_spin(ds_full, static_cast<uint32_t>(jj) & 1u, wc, kSiteAttnP)) break;
+          tc_fence_after_sync();
+          const uint32_t k_base = smem_u32(sK + st * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kKTile / 16; ++kk) {
+            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base + 256, sdesc_sw128(ds_base + a_off, 16, 1024),
+                      sdesc_sw128(k_base + kk * 2048, kAtom, 1024), idesc_mn, (jj | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(dq_done);
+          umma_commit(k_empty + st);
+        }
+      }
+      umma_commit(drain);
+      wait_drain(drain, 0, p.timeout_ns);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quad * 32 + static_cast<int>(lane);
+    const int q = qt * kQTile + r;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    const long long stat = (static_cast<long long>(b) * p.H + h) * p.s_pad + q;
+    const float lse = q < p.S ? __ldg(p.lse + stat) : 0.f;
+    const float dd = q < p.S ? __ldg(p.delta + stat) : 0.f;
+    bool ok = true;
+    for (int j = 0; ok && j < nk; ++j) {
+      int w_ok = 1;
+      if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(j) & 1u, wc, kSiteAttnS) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      float sc[2][32], dp[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(64 * half + 32 * c), sc[c]);
+        tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(64 * half + 32 * c), dp[c]);
+      }
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      const int key0 = j * kKTile + 64 * half;
+      const int key_end = q < p.S ? (p.causal ? min(p.S, q + 1) : p.S) : 0;  // padding rows: nothing
+      const bool all_visible = __all_sync(0xffffffffu, key0 + 64 <= key_end);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float pv = all_visible || key0 + 32 * c + i < key_end ? ex2_approx(fmaf(sc[c][i], p.scale_log2, -lse))
+                                                                      : 0.f;
+          sc[c][i] = pv * (dp[c][i] - dd);  // dS
+        }
+      // the dS buffer is free once the previous dQ MMA has read it
+      if (j >= 1) {
+        if (lane == 0) w_ok = wait_spin(dq_done, static_cast<uint32_t>(j - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      store_half_row(sdS, half, r, sc);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    if (ok && nk > 0) {
+      int w_ok = 1;
+      if (lane == 0) w_ok = wait_spin(dq_done, static_cast<uint32_t>(nk - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, w_ok, 0)) {
+        tc_fence_after_sync();
+        float o[2][32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
+        tmem_wait_ld();
+        if (q < p.S) {
+          const long long d3 = 3LL * p.H * kHd;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dqkv) +
+                                                (static_cast<long long>(q) * p.B + b) * d3 +
+                                                static_cast<long long>(h) * kHd + 64 * half);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const float* y = o[g / 4] + 8 * (g % 4);
+            dst[g] = make_uint4(pack_bf16x2(y[0] * p.scale, y[1] * p.scale), pack_bf16x2(y[2] * p.scale, y[3] * p.scale),
+                                pack_bf16x2(y[4] * p.scale, y[5] * p.scale), pack_bf16x2(y[6] * p.scale, y[7] * p.scale));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// dK and dV for one 128-key tile of one (batch, head): per query tile i, S^T_i = K Q_i^T and
+// dP^T_i = V dO_i^T in TMEM; the 8 compute warps (two per lane quadrant = key rows, 64 queries each) form
+// P^T = exp2(S^T scale - lse[q]) and dS^T = P^T (dP^T - D[q]), hand P^T to dV += P^T dO_i and then dS^T
+// (through the same shared buffer) to dK += dS^T Q_i; dO_i and Q_i are the MN-major operands.  Causal
+// attention visits query tiles i >= the key tile.
+__global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid_constant__ AttnBwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + kTileBytes;
+  uint8_t* sQ = sV + kTileBytes;                   // 2 stages
+  uint8_t* sdO = sQ + kKvStages * kTileBytes;      // 2 stages
+  uint8_t* sPd = sdO + kKvStages * kTileBytes;     // P^T, then dS^T
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sPd + kTileBytes);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = kv_full + 1;                  // [stage]: Q_i and dO_i
+  uint64_t* q_empty = q_full + kKvStages;
+  uint64_t* s_full = q_empty + kKvStages;          // S^T_i and dP^T_i in TMEM
+  uint64_t* s_empty = s_full + 1;
+  uint64_t* p_full = s_empty + 1;
+  uint64_t* dv_done = p_full + 1;                  // dV += P^T dO_i done (buffer free for dS^T)
+  uint64_t* ds_full = dv_done + 1;
+  uint64_t* dk_done = ds_full + 1;                 // dK += dS^T Q_i done (buffer free for the next P^T)
+  uint64_t* drain = dk_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  const int kt = static_cast<int>(blockIdx.x % p.n_tiles);  // causal: the first key tiles have the most work
+  const int bh = static_cast<int>(blockIdx.x / p.n_tiles);
+  const int b = bh % p.B, h = bh / p.B;
+  const int i0 = p.causal ? kt : 0;
+  const int nq = p.n_tiles - i0;
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(q_full + s, 1);
+      mbar_init(q_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 8);
+    mbar_init(p_full, 8);
+    mbar_init(dv_done, 1);
+    mbar_init(ds_full, 8);
+    mbar_init(dk_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;  // S^T [0, 128), dP^T [128, 256), dV [256, 384), dK [384, 512)
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * kTileBytes);
+      load_tile(sK, &p.tmK, kv_full, h, b, kt * kKTile);
+      load_tile(sV, &p.tmV, kv_full, h, b, kt * kKTile);
+      uint32_t issued = 0, par = 0;
+      for (int t = 0; t < nq; ++t) {
+        const int st = t % kKvStages;
+        const uint32_t ph = static_cast<uint32_t>(t / kKvStages) & 1u;
+        if (!wait_spin(q_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(q_full + st, 2 * kTileBytes);
+        load_tile(sQ + st * kTileBytes, &p.tmQ, q_full + st, h, b, (i0 + t) * kQTile);
+        load_tile(sdO + st * kTileBytes, &p.tmdO, q_full + st, h, b, (i0 + t) * kQTile);
+        issued |= 1u << st;
+        par = (par & ~(1u << st)) | (ph << st);
+      }
+      wait_drain(kv_full, 0, p.timeout_ns);
+      for (int s = 0; s < kKvStages; ++s)
+        if (issued & (1u << s)) wait_drain(q_full + s, (par >> s) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_kk = idesc_bf16_f32(kKTile, kQTile, false, false);
+      constexpr uint32_t idesc_mn = idesc_bf16_f32(kKTile, kHd, false, true);
+      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), pd_base = smem_u32(sPd);
+      bool ok = wait_spin(kv_full, 0, wc, kSiteAttnQ);
+      if (ok) tc_fence_after_sync();
+      // step t: S^T_t and dP^T_t (t < nq), then dV and dK of tile t - 1 (t >= 1)
+      for (int t = 0; ok && t <= nq; ++t) {
+        if (t < nq) {
+          const int st = t % kKvStages;
+          if (!wait_spin(s_empty, (static_cast<uint32_t>(t) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
+          if (!wait_spin(q_full + st, static_cast<uint32_t>(t / kKvStages) & 1u, wc, kSiteAttnKv)) break;
+          tc_fence_after_sync();
+          const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), idesc_kk,
+                      kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base + 128, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
+                      idesc_kk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
+        }
+        if (t >= 1) {
+          const int tt = t - 1;
+          const int st = tt % kKvStages;
+          const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
+          if (!wait_spin(p_full, static_cast<uint32_t>(tt) & 1u, wc, kSiteAttnP)) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < kQTile / 16; ++kk) {
+            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base + 256, sdesc_sw128(pd_base + a_off, 16, 1024),
+                      sdesc_sw128(do_base + kk * 2048, kAtom, 1024), idesc_mn, (tt | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(dv_done);
+          if (!wait_spin(ds_full, static_cast<uint32_t>(tt) & 1u, wc, kSiteAttnP)) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < kQTile / 16; ++kk) {
+            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base + 384, sdesc_sw128(pd_base + a_off, 16, 1024),
+                      sdesc_sw128(q_base + kk * 2048, kAtom, 1024), idesc_mn, (tt | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(dk_done);
+          umma_commit(q_empty + st);
+        }
+      }
+      umma_commit(drain);
+      wait_drain(drain, 0, p.timeout_ns);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r = quad * 32 + static_cast<int>(lane);
+    const int k = kt * kKTile + r;  // key position
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    const long long stat0 = (static_cast<long long>(b) * p.H + h) * p.s_pad;
+    bool ok = true;
+    for (int t = 0; t < nq; ++t) {
+      const int q0 = (i0 + t) * kQTile + 64 * half;  // this half's first query
+      int w_ok = 1;
+      if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(t) & 1u, wc, kSiteAttnS) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      float sc[2][32], dp[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(64 * half + 32 * c), sc[c]);
+        tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(64 * half + 32 * c), dp[c]);
+      }
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      // query q sees key k when q < S and (not causal or k <= q); only the diagonal and the ragged last
+      // tile need the test
+      const bool all_visible = q0 + 64 <= p.S && (!p.causal || q0 > kt * kKTile + kKTile - 1);
+      const float4* lse4 = reinterpret_cast<const float4*>(p.lse + stat0 + q0);
+      const float4* d4 = reinterpret_cast<const float4*>(p.delta + stat0 + q0);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float4 l4 = __ldg(lse4 + 8 * c + g), dd4 = __ldg(d4 + 8 * c + g);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 4 * g + u;
+            const int q = q0 + 32 * c + i;
+            const bool vis = all_visible || (q < p.S && (!p.causal || k <= q));
+            const float pv = ex2_approx(fmaf(sc[c][i], p.scale_log2, -lv[u]));
+            sc[c][i] = vis ? pv : 0.f;
+            dp[c][i] = vis ? pv * (dp[c][i] - dv[u]) : 0.f;
+          }
+        }
+      // P^T into the shared buffer once the previous tile's dK MMA has read the dS^T there
+      if (t >= 1) {
+        if (lane == 0) w_ok = wait_spin(dk_done, static_cast<uint32_t>(t - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      store_half_row(sPd, half, r, sc);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      // dS^T into the same buffer once dV has read P^T
+      if (lane == 0) w_ok = wait_spin(dv_done, static_cast<uint32_t>(t) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+        ok = false;
+        break;
+      }
+      store_half_row(sPd, half, r, dp);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    if (ok && nq > 0) {
+      int w_ok = 1;
+      if (lane == 0) w_ok = wait_spin(dk_done, static_cast<uint32_t>(nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, w_ok, 0)) {
+        tc_fence_after_sync();
+        const long long d3 = 3LL * p.H * kHd;
+        __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<long long>(k) * p.B + b) * d3 +
+                             static_cast<long long>(h) * kHd + 64 * half;
+#pragma unroll
+        for (int part = 1; part <= 2; ++part) {  // dK (TMEM 384), dV (TMEM 256)
+          float o[2][32];
+          const uint32_t col = part == 1 ? 384u : 256u;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) tmem_ld32f_nowait(lane_base + col + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
+          tmem_wait_ld();
+          const float f = part == 1 ? p.scale : 1.f;
+          if (k < p.S) {
+            uint4* dst = reinterpret_cast<uint4*>(row + part * p.H * kHd);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const float* y = o[g / 4] + 8 * (g % 4);
+              dst[g] = make_uint4(pack_bf16x2(y[0] * f, y[1] * f), pack_bf16x2(y[2] * f, y[3] * f),
+                                  pack_bf16x2(y[4] * f, y[5] * f), pack_bf16x2(y[6] * f, y[7] * f));
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -463,16 +982,15 @@ PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
   return fn;
 }
 
-// 4-D map over one part (Q, K or V) of the projection output [S, B, 3, H, hd]: dims (e, h, b, s).
-bool make_part_map(CUtensorMap* m, const void* qkv, int part, int S, int B, int H) {
+// 4-D map over per-head rows of a token-major tensor whose token row (s B + b) holds `ld` elements and
+// head h starts at element h hd of `base`: dims (e, h, b, s), boxes of 64 elements x 128 positions.
+bool make_head_map(CUtensorMap* m, const void* base, long long ld, int S, int B, int H) {
   auto fn = attn_encode_fn();
   if (fn == nullptr) return false;
-  const long long d = static_cast<long long>(H) * kHd;
-  const void* base = static_cast<const __nv_bfloat16*>(qkv) + part * d;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHd), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B),
                         static_cast<cuuint64_t>(S)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHd) * 2, static_cast<cuuint64_t>(3 * d) * 2,
-                           static_cast<cuuint64_t>(3 * d) * 2 * static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHd) * 2, static_cast<cuuint64_t>(ld) * 2,
+                           static_cast<cuuint64_t>(ld) * 2 * static_cast<cuuint64_t>(B)};
   cuuint32_t box[4] = {64, 1, 1, 128};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -480,10 +998,16 @@ bool make_part_map(CUtensorMap* m, const void* qkv, int part, int S, int B, int 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One part (Q, K or V) of the projection output [S, B, 3, H, hd].
+bool make_part_map(CUtensorMap* m, const void* qkv, int part, int S, int B, int H) {
+  const long long d = static_cast<long long>(H) * kHd;
+  return make_head_map(m, static_cast<const __nv_bfloat16*>(qkv) + part * d, 3 * d, S, B, H);
+}
+
 constexpr size_t kAttnSmem = 1024 + (3 + 2 * kKvStages) * kTileBytes + 256;
 
 cudaError_t launch_attention(const void* qkv, int S, int B, int H, bool causal, void* out, const DeviceCtx& ctx,
-                             cudaStream_t s) {
+                             cudaStream_t s, float* lse = nullptr) {
   if (S <= 0) return cudaSuccess;
   AttnParams p;
   memset(&p, 0, sizeof(p));
@@ -491,10 +1015,12 @@ cudaError_t launch_attention(const void* qkv, int S, int B, int H, bool causal, 
       !make_part_map(&p.tmV, qkv, 2, S, B, H))
     return cudaErrorInvalidValue;
   p.out = out;
+  p.lse = lse;
   p.S = S;
   p.B = B;
   p.H = H;
   p.n_qtiles = (S + kQTile - 1) / kQTile;
+  p.s_pad = p.n_qtiles * kQTile;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHd)));
   p.err = ctx.err;
@@ -508,6 +1034,50 @@ cudaError_t launch_attention(const void* qkv, int S, int B, int H, bool causal, 
   return cudaGetLastError();
 }
 
+// Attention backward: D = rowsum(dO O), then dQ (per query tile) and dK, dV (per key tile) into dqkv.
+// lse: the forward's [B H x s_pad] statistics; delta: [B H x s_pad] scratch.
+cudaError_t launch_attention_bwd(const void* qkv, const void* o, const void* dO, const float* lse, float* delta,
+                                 int S, int B, int H, bool causal, void* dqkv, const DeviceCtx& ctx, cudaStream_t s) {
+  if (S <= 0) return cudaSuccess;
+  AttnBwdParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_part_map(&p.tmQ, qkv, 0, S, B, H) || !make_part_map(&p.tmK, qkv, 1, S, B, H) ||
+      !make_part_map(&p.tmV, qkv, 2, S, B, H) ||
+      !make_head_map(&p.tmdO, dO, static_cast<long long>(H) * kHd, S, B, H))
+    return cudaErrorInvalidValue;
+  p.lse = lse;
+  p.delta = delta;
+  p.dqkv = dqkv;
+  p.S = S;
+  p.B = B;
+  p.H = H;
+  p.n_tiles = (S + kQTile - 1) / kQTile;
+  p.s_pad = p.n_tiles * kQTile;
+  p.causal = causal ? 1 : 0;
+  p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kHd)));
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHd)));
+  p.err = ctx.err;
+  p.timeout_ns = ctx.timeout_ns;
+  const long long grid = static_cast<long long>(p.n_tiles) * B * H;
+  const long long warps = static_cast<long long>(S) * B * H;
+  if (grid > INT_MAX || warps > INT_MAX / 32) return cudaErrorInvalidValue;
+  k_attention_bwd_delta<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(o), S, B, H, p.s_pad, delta);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_attention_bwd_dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kAttnSmem));
+  if (e != cudaSuccess) return e;
+  k_attention_bwd_dq<<<static_cast<int>(grid), kThreads, kAttnSmem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_attention_bwd_dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kAttnSmem));
+  if (e != cudaSuccess) return e;
+  k_attention_bwd_dkdv<<<static_cast<int>(grid), kThreads, kAttnSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -518,6 +1088,22 @@ tpmlp_status attn_check(int64_t S, int64_t B, int64_t H, int64_t head_dim) {
   if (S > INT_MAX / 4 || B > 65535 || H > 65535 || S * B > INT_MAX / 4 || H * kHd > 65536)
     return TPMLP_ERR_UNSUPPORTED;
   return TPMLP_OK;
+}
+
+// Backward workspace: D, dO, dQKV, column-sum partials.
+struct Bwd {
+  size_t delta, dO, dqkv, partial;
+};
+
+Bwd bwd_sizes(int64_t S, int64_t B, int64_t H) {
+  const size_t T = static_cast<size_t>(S) * static_cast<size_t>(B), d = static_cast<size_t>(H) * kHd;
+  const size_t s_pad = (static_cast<size_t>(S) + kQTile - 1) / kQTile * kQTile;
+  Bwd z;
+  z.delta = align256(static_cast<size_t>(B) * static_cast<size_t>(H) * s_pad * 4);
+  z.dO = align256(T * d * 2);
+  z.dqkv = align256(T * 3 * d * 2);
+  z.partial = align256(column_sum_bf16_scratch_floats(static_cast<int>(T), static_cast<int>(3 * d)) * 4);
+  return z;
 }
 
 tpmlp_status to_status(cudaError_t e) {
@@ -543,28 +1129,58 @@ tpmlp_status tpmlp_attention_workspace_size(int64_t S, int64_t B, int64_t H, int
 }
 
 tpmlp_status tpmlp_attention_core(const void* QKV, int64_t S, int64_t B, int64_t H, int64_t head_dim, int causal,
-                                  void* O, tpmlp_stream_t stream) {
+                                  void* O, float* LSE, tpmlp_stream_t stream) {
   tpmlp_status st = attn_check(S, B, H, head_dim);
   if (st != TPMLP_OK) return st;
   if (causal != 0 && causal != 1) return TPMLP_ERR_INVALID_ARG;
   if (S == 0) return TPMLP_OK;
-  if (!al16(QKV) || !al16(O)) return TPMLP_ERR_INVALID_ARG;
+  if (!al16(QKV) || !al16(O) || (LSE != nullptr && !al16(LSE))) return TPMLP_ERR_INVALID_ARG;
   DeviceCtx c;
   if (current_device_ctx(&c) != cudaSuccess) return TPMLP_ERR_CUDA;
   return to_status(launch_attention(QKV, static_cast<int>(S), static_cast<int>(B), static_cast<int>(H), causal == 1,
-                                    O, c, reinterpret_cast<cudaStream_t>(stream)));
+                                    O, c, reinterpret_cast<cudaStream_t>(stream), LSE));
+}
+
+tpmlp_status tpmlp_attention_backward_workspace_size(int64_t S, int64_t B, int64_t H, int64_t head_dim,
+                                                     size_t* bytes) {
+  if (bytes == nullptr) return TPMLP_ERR_INVALID_ARG;
+  const tpmlp_status st = attn_check(S, B, H, head_dim);
+  if (st != TPMLP_OK) return st;
+  const Bwd z = bwd_sizes(S, B, H);
+  *bytes = z.delta + z.dO + z.dqkv + z.partial;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_attention_core_backward(const void* QKV, const void* O, const void* dO, const float* LSE,
+                                           int64_t S, int64_t B, int64_t H, int64_t head_dim, int causal,
+                                           void* dQKV, void* workspace, size_t workspace_bytes,
+                                           tpmlp_stream_t stream) {
+  tpmlp_status st = attn_check(S, B, H, head_dim);
+  if (st != TPMLP_OK) return st;
+  if (causal != 0 && causal != 1) return TPMLP_ERR_INVALID_ARG;
+  if (S == 0) return TPMLP_OK;
+  if (!al16(QKV) || !al16(O) || !al16(dO) || !al16(LSE) || !al16(dQKV)) return TPMLP_ERR_INVALID_ARG;
+  const Bwd z = bwd_sizes(S, B, H);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < z.delta)
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if (current_device_ctx(&c) != cudaSuccess) return TPMLP_ERR_CUDA;
+  return to_status(launch_attention_bwd(QKV, O, dO, LSE, static_cast<float*>(workspace), static_cast<int>(S),
+                                        static_cast<int>(B), static_cast<int>(H), causal == 1, dQKV, c,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 tpmlp_status tpmlp_attention_tp_forward(const void* X, const void* Wqkv, const void* bqkv, const void* Wo,
                                         const void* bo, int64_t S, int64_t B, int64_t H, int32_t n_shards,
-                                        int causal, void* Y, void* QKV_out, void* O_out, void* workspace,
-                                        size_t workspace_bytes, tpmlp_stream_t stream) {
+                                        int causal, void* Y, void* QKV_out, void* O_out, float* LSE_out,
+                                        void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = attn_check(S, B, H, kHd);
   if (st != TPMLP_OK) return st;
   if (n_shards < 1 || H % n_shards != 0 || (causal != 0 && causal != 1)) return TPMLP_ERR_INVALID_ARG;
   if (S == 0) return TPMLP_OK;
   if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(Y) || (bqkv != nullptr && !al16(bqkv)) ||
-      (bo != nullptr && !al16(bo)) || (QKV_out != nullptr && !al16(QKV_out)) || (O_out != nullptr && !al16(O_out)))
+      (bo != nullptr && !al16(bo)) || (QKV_out != nullptr && !al16(QKV_out)) || (O_out != nullptr && !al16(O_out)) ||
+      (LSE_out != nullptr && !al16(LSE_out)))
     return TPMLP_ERR_INVALID_ARG;
   size_t need = 0;
   tpmlp_attention_workspace_size(S, B, H, kHd, &need);
@@ -591,7 +1207,7 @@ tpmlp_status tpmlp_attention_tp_forward(const void* X, const void* Wqkv, const v
   g1.bias = bqkv;
   cudaError_t e = launch_gemm(g1, c, s);
   if (e == cudaSuccess) e = launch_attention(qkv, static_cast<int>(S), static_cast<int>(B), static_cast<int>(H),
-                                             causal == 1, o, c, s);
+                                             causal == 1, o, c, s, LSE_out);
   // row-parallel output projection: the K loop walks the shards' head rows into one accumulator, then
   // the row layer's bias
   if (e == cudaSuccess) {
@@ -606,6 +1222,87 @@ tpmlp_status tpmlp_attention_tp_forward(const void* X, const void* Wqkv, const v
     g2.ld0 = d;
     g2.bias = bo;
     e = launch_gemm(g2, c, s);
+  }
+  return to_status(e);
+}
+
+tpmlp_status tpmlp_attention_tp_backward(const void* X, const void* Wqkv, const void* Wo, const void* QKV,
+                                         const void* O, const float* LSE, const void* dY, int64_t S, int64_t B,
+                                         int64_t H, int32_t n_shards, int causal, void* dX, void* dWqkv,
+                                         void* dbqkv, void* dWo, void* dbo, void* dQKV_out, void* workspace,
+                                         size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = attn_check(S, B, H, kHd);
+  if (st != TPMLP_OK) return st;
+  if (n_shards < 1 || H % n_shards != 0 || (causal != 0 && causal != 1)) return TPMLP_ERR_INVALID_ARG;
+  if (S == 0) return TPMLP_OK;
+  if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(QKV) || !al16(O) || !al16(LSE) || !al16(dY) || !al16(dX) ||
+      !al16(dWqkv) || !al16(dWo) || (dbqkv != nullptr && !al16(dbqkv)) || (dbo != nullptr && !al16(dbo)) ||
+      (dQKV_out != nullptr && !al16(dQKV_out)))
+    return TPMLP_ERR_INVALID_ARG;
+  const Bwd z = bwd_sizes(S, B, H);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < z.delta + z.dO + z.dqkv + z.partial)
+    return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if (current_device_ctx(&c) != cudaSuccess) return TPMLP_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int T = static_cast<int>(S * B), d = static_cast<int>(H * kHd);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* delta = reinterpret_cast<float*>(w);
+  void* dO = w + z.delta;
+  void* dqkv = dQKV_out != nullptr ? dQKV_out : static_cast<void*>(w + z.delta + z.dO);
+  float* partial = reinterpret_cast<float*>(w + z.delta + z.dO + z.dqkv);
+  // row-parallel output projection: dO_i = dY Wo[rows of shard i]^T for every shard at once,
+  // dWo = O^T dY, dbo = column sums of dY
+  GemmLaunch g;
+  g.M = T;
+  g.N = d;
+  g.K = d;
+  g.a = {dY, d, false};
+  g.b = {Wo, d, false};
+  g.out0 = dO;
+  g.ld0 = d;
+  cudaError_t e = launch_gemm(g, c, s);
+  if (e == cudaSuccess) {
+    GemmLaunch gw;
+    gw.M = d;
+    gw.N = d;
+    gw.K = T;
+    gw.a = {O, d, true};
+    gw.b = {dY, d, true};
+    gw.out0 = dWo;
+    gw.ld0 = d;
+    e = launch_gemm(gw, c, s);
+  }
+  if (e == cudaSuccess && dbo != nullptr) e = launch_column_sum_bf16(dY, T, d, d, partial, dbo, s);
+  // attention backward of every (batch, head)
+  if (e == cudaSuccess)
+    e = launch_attention_bwd(QKV, O, dO, LSE, delta, static_cast<int>(S), static_cast<int>(B), static_cast<int>(H),
+                             causal == 1, dqkv, c, s);
+  // column-parallel projection: dWqkv = X^T dQKV, dbqkv = column sums of dQKV, dX = dQKV Wqkv^T (the K loop
+  // walks every shard's columns: the backward shard sum)
+  if (e == cudaSuccess) {
+    GemmLaunch gw;
+    gw.M = d;
+    gw.N = 3 * d;
+    gw.K = T;
+    gw.a = {X, d, true};
+    gw.b = {dqkv, 3 * d, true};
+    gw.out0 = dWqkv;
+    gw.ld0 = 3 * d;
+    e = launch_gemm(gw, c, s);
+  }
+  if (e == cudaSuccess && dbqkv != nullptr) e = launch_column_sum_bf16(dqkv, T, 3 * d, 3 * d, partial, dbqkv, s);
+  if (e == cudaSuccess) {
+    GemmLaunch gx;
+    gx.M = T;
+    gx.N = d;
+    gx.K = 3 * d;
+    gx.a = {dqkv, 3 * d, false};
+    gx.b = {Wqkv, 3 * d, false};
+    gx.out0 = dX;
+    gx.ld0 = d;
+    e = launch_gemm(gx, c, s);
   }
   return to_status(e);
 }

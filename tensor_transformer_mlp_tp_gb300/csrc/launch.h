@@ -84,7 +84,11 @@ cudaError_t launch_dropout_bwd(const RowParams& r, float* partial, void* dbias2,
 size_t dropout_bwd_scratch_floats(int rows, int d);
 // out[c] = sum_r partial[r * cols + c] over r < rows, fixed order; bf16 or fp32 output.
 cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s);
-
+// out[c] (bf16) = sum_r src[r ld + c] for a bf16 matrix [rows x cols] (cols and ld multiples of 8), through
+// `partial` (column_sum_bf16_scratch_floats(rows, cols) floats) in a fixed order.
+cudaError_t launch_column_sum_bf16(const void* src, int rows, int cols, long long ld, float* partial, void* out,
+                                   cudaStream_t s);
+size_t column_sum_bf16_scratch_floats(int rows, int cols);
 // E4M3 casts.  dst = E4M3(src * (*scale)) for src [rows x cols] bf16 (row-major), written [rows x cols]
 // or, with `transpose`, [cols x rows]; *amax is max-combined with max |src|.  Row lengths multiples of 16.
 cudaError_t launch_cast_e4m3(const void* src, int rows, int cols, bool transpose, const float* scale, void* dst,

@@ -837,6 +837,29 @@ __global__ void __launch_bounds__(256) k_column_sum(const float* __restrict__ pa
   }
 }
 
+// partial[y, c] = sum of src[r, c] over the rows r of block row y (a bf16 matrix with row stride ld);
+// 8 columns per thread, kDropRows rows (or more) per block row.
+__global__ void __launch_bounds__(kDropVecs) k_column_partial_bf16(const __nv_bfloat16* __restrict__ src, int rows,
+                                                                   int cols, long long ld, int rows_per_block,
+                                                                   float* __restrict__ partial) {
+  const int v = blockIdx.x * kDropVecs + threadIdx.x;
+  if (v >= cols / 8) return;
+  const int r0 = blockIdx.y * rows_per_block;
+  const int r1 = min(rows, r0 + rows_per_block);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * ld) + v), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += f[e];
+  }
+  float4* out = reinterpret_cast<float4*>(partial + static_cast<long long>(blockIdx.y) * cols + 8 * v);
+  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
 // ----------------------------------------------------------------------------- E4M3 casts and delayed scaling
 
 // dst[i] = FP8(src[i] * s), 16 elements (two 16-byte loads, one 16-byte store) per step, grid-stride.
@@ -1213,6 +1236,21 @@ cudaError_t launch_gather_rows(const RowParams& r, const DeviceCtx& ctx, cudaStr
   if (r.rows <= 0) return cudaSuccess;
   k_gather_rows<<<stream_grid(static_cast<long long>(r.rows) * r.d / 8, ctx.sm_count), 256, 0, s>>>(r);
   return cudaGetLastError();
+}
+
+size_t column_sum_bf16_scratch_floats(int rows, int cols) { return dropout_bwd_scratch_floats(rows, cols); }
+
+cudaError_t launch_column_sum_bf16(const void* src, int rows, int cols, long long ld, float* partial, void* out,
+                                   cudaStream_t s) {
+  if (rows <= 0 || cols <= 0 || out == nullptr) return cudaSuccess;
+  if (cols % 8 != 0 || ld % 8 != 0) return cudaErrorInvalidValue;
+  const int rpb = dropout_rows_per_block(rows);
+  const dim3 grid((cols / 8 + kDropVecs - 1) / kDropVecs, (rows + rpb - 1) / rpb);
+  k_column_partial_bf16<<<grid, kDropVecs, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, ld, rpb,
+                                                   partial);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_column_sum(partial, static_cast<int>(grid.y), cols, out, true, s);
 }
 
 cudaError_t launch_column_sum(const float* partial, int rows, int cols, void* out, bool out_bf16, cudaStream_t s) {

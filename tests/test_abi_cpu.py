@@ -225,9 +225,44 @@ def test_attention_workspace_and_argument_checks(lib):
     assert L.tpmlp_attention_workspace_size(-1, 2, 32, 128, ctypes.byref(n)) == binding.ERR_INVALID_ARG
     good = ctypes.c_void_p(1 << 20)
     # heads not divisible by the shards; a causal flag other than 0 / 1; misaligned pointers
-    assert L.tpmlp_attention_tp_forward(good, good, None, good, None, 256, 1, 6, 4, 0, good, None, None, good, 1 << 30,
-                                        None) == binding.ERR_INVALID_ARG
-    assert L.tpmlp_attention_core(good, 256, 1, 4, 128, 2, good, None) == binding.ERR_INVALID_ARG
-    assert L.tpmlp_attention_core(ctypes.c_void_p((1 << 20) + 2), 256, 1, 4, 128, 0, good, None) \
+    assert L.tpmlp_attention_tp_forward(good, good, None, good, None, 256, 1, 6, 4, 0, good, None, None, None, good,
+                                        1 << 30, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_attention_core(good, 256, 1, 4, 128, 2, good, None, None) == binding.ERR_INVALID_ARG
+    assert L.tpmlp_attention_core(ctypes.c_void_p((1 << 20) + 2), 256, 1, 4, 128, 0, good, None, None) \
         == binding.ERR_INVALID_ARG
-    assert L.tpmlp_attention_core(None, 0, 1, 4, 128, 1, None, None) == binding.OK      # empty sequence
+    assert L.tpmlp_attention_core(good, 256, 1, 4, 128, 0, good, ctypes.c_void_p((1 << 20) + 4), None) \
+        == binding.ERR_INVALID_ARG                                                         # misaligned LSE
+    assert L.tpmlp_attention_core(None, 0, 1, 4, 128, 1, None, None, None) == binding.OK  # empty sequence
+
+
+def test_attention_backward_workspace_and_argument_checks(lib):
+    L = binding.lib()
+    n = ctypes.c_size_t(0)
+    S, B, H = 1000, 2, 4  # S_pad = 1024
+    assert L.tpmlp_attention_backward_workspace_size(S, B, H, 128, ctypes.byref(n)) == binding.OK
+    T, d = S * B, H * 128
+    rows_per_block = 16
+    partial = (T + rows_per_block - 1) // rows_per_block * 3 * d * 4
+    assert n.value == _r256(B * H * 1024 * 4) + _r256(T * d * 2) + _r256(T * 3 * d * 2) + _r256(partial)
+    assert binding.attention_lse_shape(S, B, H) == (B * H, 1024)
+    assert L.tpmlp_attention_backward_workspace_size(S, B, H, 96, ctypes.byref(n)) == binding.ERR_UNSUPPORTED
+    good = ctypes.c_void_p(1 << 20)
+    # the core backward: LSE required, a workspace of at least the D statistics
+    assert L.tpmlp_attention_core_backward(good, good, good, None, S, B, H, 128, 0, good, good, 1 << 30, None) \
+        == binding.ERR_INVALID_ARG
+    assert L.tpmlp_attention_core_backward(good, good, good, good, S, B, H, 128, 0, good, good, 1024, None) \
+        == binding.ERR_WORKSPACE
+    assert L.tpmlp_attention_core_backward(good, good, good, good, S, B, H, 128, 3, good, good, 1 << 30, None) \
+        == binding.ERR_INVALID_ARG
+    assert L.tpmlp_attention_core_backward(None, None, None, None, 0, B, H, 128, 0, None, None, 0, None) == binding.OK
+    # the block backward: shards must divide the heads; saved tensors required; workspace too small
+    args = [good] * 7 + [S, B, H, 4, 0] + [good, good, None, good, None, None, good, 1 << 30, None]
+    bad = list(args)
+    bad[10] = 3
+    assert L.tpmlp_attention_tp_backward(*bad) == binding.ERR_INVALID_ARG
+    bad = list(args)
+    bad[5] = None  # LSE
+    assert L.tpmlp_attention_tp_backward(*bad) == binding.ERR_INVALID_ARG
+    bad = list(args)
+    bad[19] = 4096
+    assert L.tpmlp_attention_tp_backward(*bad) == binding.ERR_WORKSPACE
