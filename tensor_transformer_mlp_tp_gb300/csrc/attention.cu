@@ -455,26 +455,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
 
 // ----------------------------------------------------------------------------- attention backward
 
-// D[b, h, s] = sum_e dO[s B + b, h hd + e] O[s B + b, h hd + e] in fp32 ([B H x s_pad]): one warp per
-// (token, head), 4 elements per lane.
+constexpr int kBwdComputeWarps = 16;                      // four per TMEM lane quadrant, 32 columns each
+constexpr int kBwdThreads = 32 * (2 + kBwdComputeWarps);  // producer, MMA issuer, compute warps
+
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& c) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+  float v = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = unpack_bf16x2(aw[i]), y = unpack_bf16x2(cw[i]);
+    v = fmaf(x.x, y.x, v);
+    v = fmaf(x.y, y.y, v);
+  }
+  return v;
+}
+
+// D[b, h, s] = sum_e dO[s B + b, h hd + e] O[s B + b, h hd + e] in fp32 ([B H x s_pad]).  One warp per
+// token row; each half-warp takes one head per step (16 lanes x 8 elements: 256-byte coalesced loads).
 __global__ void __launch_bounds__(256) k_attention_bwd_delta(const __nv_bfloat16* __restrict__ dO,
                                                              const __nv_bfloat16* __restrict__ O, int S, int B, int H,
                                                              int s_pad, float* __restrict__ D) {
-  const long long item = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // token row
   const int lane = threadIdx.x & 31;
-  if (item >= static_cast<long long>(S) * B * H) return;
-  const int h = static_cast<int>(item % H);
-  const long long t = item / H;  // token row s B + b
-  const long long off = t * (static_cast<long long>(H) * kHd) + static_cast<long long>(h) * kHd + 4 * lane;
-  const uint2 a = __ldg(reinterpret_cast<const uint2*>(dO + off));
-  const uint2 c = __ldg(reinterpret_cast<const uint2*>(O + off));
-  const float2 a0 = unpack_bf16x2(a.x), a1 = unpack_bf16x2(a.y), c0 = unpack_bf16x2(c.x), c1 = unpack_bf16x2(c.y);
-  float v = a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
+  if (t >= static_cast<long long>(S) * B) return;
+  const int sq = static_cast<int>(t / B), b = static_cast<int>(t % B);
+  const long long row = t * (static_cast<long long>(H) * kHd);
+  const int sub = lane >> 4;      // which head of the pair
+  const int e = 8 * (lane & 15);  // first element within the head
+#pragma unroll 2
+  for (int h0 = 0; h0 < H; h0 += 2) {
+    const int h = h0 + sub;
+    float v = 0.f;
+    if (h < H)
+      v = dot8(__ldg(reinterpret_cast<const uint4*>(dO + row + h * kHd + e)),
+               __ldg(reinterpret_cast<const uint4*>(O + row + h * kHd + e)));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) {
-    const int sq = static_cast<int>(t / B), b = static_cast<int>(t % B);
-    D[(static_cast<long long>(b) * H + h) * s_pad + sq] = v;
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((lane & 15) == 0 && h < H) D[(static_cast<long long>(b) * H + h) * s_pad + sq] = v;
   }
 }
 
@@ -490,23 +507,39 @@ struct AttnBwdParams {
   unsigned long long timeout_ns;
 };
 
-// bf16 row of 64 values (this half's columns) into the swizzled K-major tile buffer: row r, columns
-// 64 half .. 64 half + 63 (one atom column).
-__device__ __forceinline__ void store_half_row(uint8_t* buf, int half, int r, const float (&v)[2][32]) {
+// 32 bf16 values (columns 32 quarter .. 32 quarter + 31) of row r into a 128 x 128 K-major tile in the
+// 128-byte-swizzled layout: atom column quarter / 2, 16-byte chunks 4 (quarter % 2) .. + 3.
+__device__ __forceinline__ void store_quarter_row(uint8_t* buf, int quarter, int r, const float (&v)[32]) {
+  uint8_t* row = buf + (quarter >> 1) * kAtom + r * 128;
 #pragma unroll
-  for (int chunk = 0; chunk < 8; ++chunk) {
-    const float* e = v[chunk >> 2] + 8 * (chunk & 3);
-    uint8_t* dst = buf + half * kAtom + r * 128 + ((chunk ^ (r & 7)) << 4);
-    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                                                pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+  for (int c = 0; c < 4; ++c) {
+    const int chunk = 4 * (quarter & 1) + c;
+    const float* e = v + 8 * c;
+    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) =
+        make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
   }
 }
 
+// 32 columns of one TMEM row (this thread's lane) scaled by f, as bf16 into dst (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store_row32_scaled(__nv_bfloat16* dst, const float (&o)[32], float f) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const float* y = o + 8 * g;
+    d4[g] = make_uint4(pack_bf16x2(y[0] * f, y[1] * f), pack_bf16x2(y[2] * f, y[3] * f),
+                       pack_bf16x2(y[4] * f, y[5] * f), pack_bf16x2(y[6] * f, y[7] * f));
+  }
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* a) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+}
+
 // dQ for one 128-query tile of one (batch, head): per key tile j, S_j = Q K_j^T and dP_j = dO V_j^T in
-// TMEM; the 8 compute warps (two per lane quadrant, 64 keys each) form P = exp2(S scale - lse) and
+// TMEM; the 16 compute warps (four per lane quadrant, 32 keys each) form P = exp2(S scale - lse) and
 // dS = P (dP - D) from the saved statistics (no reductions), write dS in bf16 to shared memory, and
 // dQ += dS K_j accumulates in TMEM (K as the MN-major operand); dQ / sqrt(hd) goes to dQKV.
-__global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_constant__ AttnBwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __grid_constant__ AttnBwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -543,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_c
       mbar_init(v_empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_empty, 8);
-    mbar_init(ds_full, 8);
+    mbar_init(s_empty, kBwdComputeWarps);
+    mbar_init(ds_full, kBwdComputeWarps);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -640,13 +673,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_c
     }
   } else {
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int quarter = (warp - 2) >> 2;  // keys 32 quarter .. 32 quarter + 31 of every tile
     const int r = quad * 32 + static_cast<int>(lane);
     const int q = qt * kQTile + r;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     const long long stat = (static_cast<long long>(b) * p.H + h) * p.s_pad + q;
-    const float lse = q < p.S ? __ldg(p.lse + stat) : 0.f;
+    const float neg_lse = q < p.S ? -__ldg(p.lse + stat) : 0.f;
     const float dd = q < p.S ? __ldg(p.delta + stat) : 0.f;
+    const int key_end = q < p.S ? (p.causal ? min(p.S, q + 1) : p.S) : 0;  // padding rows: nothing
     bool ok = true;
     for (int j = 0; ok && j < nk; ++j) {
       int w_ok = 1;
@@ -656,27 +690,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_c
         break;
       }
       tc_fence_after_sync();
-      float sc[2][32], dp[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(64 * half + 32 * c), sc[c]);
-        tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(64 * half + 32 * c), dp[c]);
-      }
+      float sc[32], dp[32];
+      tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(32 * quarter), sc);
+      tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(32 * quarter), dp);
       tmem_wait_ld();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty);
-      const int key0 = j * kKTile + 64 * half;
-      const int key_end = q < p.S ? (p.causal ? min(p.S, q + 1) : p.S) : 0;  // padding rows: nothing
-      const bool all_visible = __all_sync(0xffffffffu, key0 + 64 <= key_end);
+      const int key0 = j * kKTile + 32 * quarter;
+      if (__all_sync(0xffffffffu, key0 + 32 <= key_end)) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+        for (int i = 0; i < 32; ++i) sc[i] = fmaf(sc[i], p.scale_log2, neg_lse);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float pv = all_visible || key0 + 32 * c + i < key_end ? ex2_approx(fmaf(sc[c][i], p.scale_log2, -lse))
-                                                                      : 0.f;
-          sc[c][i] = pv * (dp[c][i] - dd);  // dS
-        }
+        for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[i] = key0 + i < key_end ? ex2_approx(fmaf(sc[i], p.scale_log2, neg_lse)) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dp[i] = sc[i] * (dp[i] - dd);  // dS
       // the dS buffer is free once the previous dQ MMA has read it
       if (j >= 1) {
         if (lane == 0) w_ok = wait_spin(dq_done, static_cast<uint32_t>(j - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
@@ -685,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_c
           break;
         }
       }
-      store_half_row(sdS, half, r, sc);
+      store_quarter_row(sdS, quarter, r, dp);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
@@ -695,22 +727,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_c
       if (lane == 0) w_ok = wait_spin(dq_done, static_cast<uint32_t>(nk - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
       if (__shfl_sync(0xffffffffu, w_ok, 0)) {
         tc_fence_after_sync();
-        float o[2][32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
+        float o[32];
+        tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(32 * quarter), o);
         tmem_wait_ld();
-        if (q < p.S) {
-          const long long d3 = 3LL * p.H * kHd;
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dqkv) +
-                                                (static_cast<long long>(q) * p.B + b) * d3 +
-                                                static_cast<long long>(h) * kHd + 64 * half);
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const float* y = o[g / 4] + 8 * (g % 4);
-            dst[g] = make_uint4(pack_bf16x2(y[0] * p.scale, y[1] * p.scale), pack_bf16x2(y[2] * p.scale, y[3] * p.scale),
-                                pack_bf16x2(y[4] * p.scale, y[5] * p.scale), pack_bf16x2(y[6] * p.scale, y[7] * p.scale));
-          }
-        }
+        if (q < p.S)
+          store_row32_scaled(static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<long long>(q) * p.B + b) * (3LL * p.H * kHd) +
+                                 static_cast<long long>(h) * kHd + 32 * quarter,
+                             o, p.scale);
       }
     }
   }
@@ -723,11 +746,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dq(const __grid_c
 }
 
 // dK and dV for one 128-key tile of one (batch, head): per query tile i, S^T_i = K Q_i^T and
-// dP^T_i = V dO_i^T in TMEM; the 8 compute warps (two per lane quadrant = key rows, 64 queries each) form
+// dP^T_i = V dO_i^T in TMEM; the 16 compute warps (four per lane quadrant = key rows, 32 queries each) form
 // P^T = exp2(S^T scale - lse[q]) and dS^T = P^T (dP^T - D[q]), hand P^T to dV += P^T dO_i and then dS^T
 // (through the same shared buffer) to dK += dS^T Q_i; dO_i and Q_i are the MN-major operands.  Causal
 // attention visits query tiles i >= the key tile.
-__global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid_constant__ AttnBwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __grid_constant__ AttnBwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
@@ -763,10 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid
       mbar_init(q_empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_empty, 8);
-    mbar_init(p_full, 8);
+    mbar_init(s_empty, kBwdComputeWarps);
+    mbar_init(p_full, kBwdComputeWarps);
     mbar_init(dv_done, 1);
-    mbar_init(ds_full, 8);
+    mbar_init(ds_full, kBwdComputeWarps);
     mbar_init(dk_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -796,6 +819,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid
         mbar_arrive_expect_tx(q_full + st, 2 * kTileBytes);
         load_tile(sQ + st * kTileBytes, &p.tmQ, q_full + st, h, b, (i0 + t) * kQTile);
         load_tile(sdO + st * kTileBytes, &p.tmdO, q_full + st, h, b, (i0 + t) * kQTile);
+        // the tile's statistics (512 bytes each) into L1 ahead of the compute warps' loads
+        const long long st0 = (static_cast<long long>(b) * p.H + h) * p.s_pad + (i0 + t) * kQTile;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+          prefetch_l1(p.lse + st0 + 32 * l);
+          prefetch_l1(p.delta + st0 + 32 * l);
+        }
         issued |= 1u << st;
         par = (par & ~(1u << st)) | (ph << st);
       }
@@ -862,14 +892,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid
     }
   } else {
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int quarter = (warp - 2) >> 2;  // queries 32 quarter .. 32 quarter + 31 of every tile
     const int r = quad * 32 + static_cast<int>(lane);
     const int k = kt * kKTile + r;  // key position
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     const long long stat0 = (static_cast<long long>(b) * p.H + h) * p.s_pad;
     bool ok = true;
     for (int t = 0; t < nq; ++t) {
-      const int q0 = (i0 + t) * kQTile + 64 * half;  // this half's first query
+      const int q0 = (i0 + t) * kQTile + 32 * quarter;  // this warp's first query
       int w_ok = 1;
       if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(t) & 1u, wc, kSiteAttnS) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
@@ -877,37 +907,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid
         break;
       }
       tc_fence_after_sync();
-      float sc[2][32], dp[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(64 * half + 32 * c), sc[c]);
-        tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(64 * half + 32 * c), dp[c]);
-      }
+      float sc[32], dp[32];
+      tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(32 * quarter), sc);
+      tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(32 * quarter), dp);
       tmem_wait_ld();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty);
-      // query q sees key k when q < S and (not causal or k <= q); only the diagonal and the ragged last
-      // tile need the test
-      const bool all_visible = q0 + 64 <= p.S && (!p.causal || q0 > kt * kKTile + kKTile - 1);
-      const float4* lse4 = reinterpret_cast<const float4*>(p.lse + stat0 + q0);
+      const float4* l4 = reinterpret_cast<const float4*>(p.lse + stat0 + q0);
       const float4* d4 = reinterpret_cast<const float4*>(p.delta + stat0 + q0);
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
+      // query q sees key k when q < S and (not causal or k <= q); only the diagonal and the ragged last
+      // tile need the test (the condition is the same for the whole warp)
+      if (q0 + 32 <= p.S && (!p.causal || q0 >= kt * kKTile + kKTile - 1)) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const float4 l4 = __ldg(lse4 + 8 * c + g), dd4 = __ldg(d4 + 8 * c + g);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {dd4.x, dd4.y, dd4.z, dd4.w};
+          const float4 l = __ldg(l4 + g);
+          sc[4 * g] = fmaf(sc[4 * g], p.scale_log2, -l.x);
+          sc[4 * g + 1] = fmaf(sc[4 * g + 1], p.scale_log2, -l.y);
+          sc[4 * g + 2] = fmaf(sc[4 * g + 2], p.scale_log2, -l.z);
+          sc[4 * g + 3] = fmaf(sc[4 * g + 3], p.scale_log2, -l.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float4 dd = __ldg(d4 + g);
+          dp[4 * g] = sc[4 * g] * (dp[4 * g] - dd.x);
+          dp[4 * g + 1] = sc[4 * g + 1] * (dp[4 * g + 1] - dd.y);
+          dp[4 * g + 2] = sc[4 * g + 2] * (dp[4 * g + 2] - dd.z);
+          dp[4 * g + 3] = sc[4 * g + 3] * (dp[4 * g + 3] - dd.w);
+        }
+      } else {
+        // a query past S reads unwritten statistics: the selects keep them out
+        const int q_end = p.causal ? min(p.S, q0 + 32) : p.S;
+        const int q_first = p.causal ? k : 0;  // visible: q_first <= q < q_end
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float4 l = __ldg(l4 + g);
+          const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int i = 4 * g + u;
-            const int q = q0 + 32 * c + i;
-            const bool vis = all_visible || (q < p.S && (!p.causal || k <= q));
-            const float pv = ex2_approx(fmaf(sc[c][i], p.scale_log2, -lv[u]));
-            sc[c][i] = vis ? pv : 0.f;
-            dp[c][i] = vis ? pv * (dp[c][i] - dv[u]) : 0.f;
+            const int q = q0 + 4 * g + u;
+            const float pv = ex2_approx(fmaf(sc[4 * g + u], p.scale_log2, -lv[u]));
+            sc[4 * g + u] = q >= q_first && q < q_end ? pv : 0.f;
           }
         }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float4 dd = __ldg(d4 + g);
+          const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int q = q0 + 4 * g + u;
+            dp[4 * g + u] = q >= q_first && q < q_end ? sc[4 * g + u] * (dp[4 * g + u] - dv[u]) : 0.f;
+          }
+        }
+      }
       // P^T into the shared buffer once the previous tile's dK MMA has read the dS^T there
       if (t >= 1) {
         if (lane == 0) w_ok = wait_spin(dk_done, static_cast<uint32_t>(t - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
@@ -916,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid
           break;
         }
       }
-      store_half_row(sPd, half, r, sc);
+      store_quarter_row(sPd, quarter, r, sc);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
@@ -926,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid
         ok = false;
         break;
       }
-      store_half_row(sPd, half, r, dp);
+      store_quarter_row(sPd, quarter, r, dp);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
@@ -936,27 +991,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_bwd_dkdv(const __grid
       if (lane == 0) w_ok = wait_spin(dk_done, static_cast<uint32_t>(nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
       if (__shfl_sync(0xffffffffu, w_ok, 0)) {
         tc_fence_after_sync();
-        const long long d3 = 3LL * p.H * kHd;
-        __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<long long>(k) * p.B + b) * d3 +
-                             static_cast<long long>(h) * kHd + 64 * half;
-#pragma unroll
-        for (int part = 1; part <= 2; ++part) {  // dK (TMEM 384), dV (TMEM 256)
-          float o[2][32];
-          const uint32_t col = part == 1 ? 384u : 256u;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) tmem_ld32f_nowait(lane_base + col + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
-          tmem_wait_ld();
-          const float f = part == 1 ? p.scale : 1.f;
-          if (k < p.S) {
-            uint4* dst = reinterpret_cast<uint4*>(row + part * p.H * kHd);
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const float* y = o[g / 4] + 8 * (g % 4);
-              dst[g] = make_uint4(pack_bf16x2(y[0] * f, y[1] * f), pack_bf16x2(y[2] * f, y[3] * f),
-                                  pack_bf16x2(y[4] * f, y[5] * f), pack_bf16x2(y[6] * f, y[7] * f));
-            }
-          }
-        }
+        __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<long long>(k) * p.B + b) * (3LL * p.H * kHd) +
+                             static_cast<long long>(h) * kHd + 32 * quarter;
+        float o[32];
+        tmem_ld32f_nowait(lane_base + 384u + static_cast<uint32_t>(32 * quarter), o);  // dK
+        tmem_wait_ld();
+        if (k < p.S) store_row32_scaled(row + static_cast<long long>(p.H) * kHd, o, p.scale);
+        tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(32 * quarter), o);  // dV
+        tmem_wait_ld();
+        if (k < p.S) store_row32_scaled(row + 2LL * p.H * kHd, o, 1.f);
       }
     }
   }
@@ -1061,20 +1104,21 @@ cudaError_t launch_attention_bwd(const void* qkv, const void* o, const void* dO,
   const long long grid = static_cast<long long>(p.n_tiles) * B * H;
   const long long warps = static_cast<long long>(S) * B * H;
   if (grid > INT_MAX || warps > INT_MAX / 32) return cudaErrorInvalidValue;
-  k_attention_bwd_delta<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, s>>>(
+  const long long rows = static_cast<long long>(S) * B;
+  k_attention_bwd_delta<<<static_cast<int>((rows * 32 + 255) / 256), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dO), static_cast<const __nv_bfloat16*>(o), S, B, H, p.s_pad, delta);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_attention_bwd_dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kAttnSmem));
   if (e != cudaSuccess) return e;
-  k_attention_bwd_dq<<<static_cast<int>(grid), kThreads, kAttnSmem, s>>>(p);
+  k_attention_bwd_dq<<<static_cast<int>(grid), kBwdThreads, kAttnSmem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_attention_bwd_dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kAttnSmem));
   if (e != cudaSuccess) return e;
-  k_attention_bwd_dkdv<<<static_cast<int>(grid), kThreads, kAttnSmem, s>>>(p);
+  k_attention_bwd_dkdv<<<static_cast<int>(grid), kBwdThreads, kAttnSmem, s>>>(p);
   return cudaGetLastError();
 }
 
