@@ -614,9 +614,24 @@ def run_other_rows(step, torch, binding, pk):
                             binding.tpmlp_dropout_backward(step.Yc, w.N, step.Xg, dbias2=db2, p=0.1, seed=1,
                                                            offset=3, ws=dws))
             ms_d = time_calls(torch, pair, 20) / 2.0
-            out["dropout_backward"] = {"ms": round(ms_d, 4), "GB/s": round(nb / (ms_d * 1e-3) / 1e9, 1),
-                                       "frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
-                                       "bytes_per_launch": nb, "launches": 2}
+            # with the keep mask the forward saved (one bit per element, read instead of regenerated)
+            masks = []
+            for off in (2, 3):
+                mk = torch.empty(binding.keep_mask_bytes(w.T, w.d), dtype=torch.uint8, device="cuda")
+                binding.tpmlp_gemm2_bias_dropout_add(step.H, step.B, w.N, step.Yc, p=0.1, seed=1, offset=off,
+                                                     keep_mask=mk)
+                masks.append(mk)
+            pair_m = lambda: (binding.tpmlp_dropout_backward(step.dYc, w.N, step.dXg, dbias2=db2, p=0.1, seed=1,
+                                                             offset=2, ws=dws, keep_mask=masks[0]),
+                              binding.tpmlp_dropout_backward(step.Yc, w.N, step.Xg, dbias2=db2, p=0.1, seed=1,
+                                                             offset=3, ws=dws, keep_mask=masks[1]))
+            ms_m = time_calls(torch, pair_m, 20) / 2.0
+            nbm = nb + w.T * w.d / 8.0
+            out["dropout_backward"] = {"ms": round(ms_m, 4), "GB/s": round(nbm / (ms_m * 1e-3) / 1e9, 1),
+                                       "frac": round(nbm / (ms_m * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+                                       "bytes_per_launch": nbm, "launches": 2, "keep_mask": "saved by the forward",
+                                       "regenerated_mask_ms": round(ms_d, 4),
+                                       "regenerated_mask_frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
     if w.sp and w.d in (1024, 2048, 4096):
         # the LayerNorm forward on a sequence 8x as long (same d): enough rows per warp for the persistent,
         # software-pipelined kernel, whose start-up the step's 8192 rows do not amortise

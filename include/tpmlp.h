@@ -106,13 +106,19 @@ enum {
  * when 32 bits of Philox4x64-10 (Salmon et al., SC 2011) with counter
  * (e / 8, offset, 0, 0) and key (seed, 0) -- word (e % 8) / 2, low half for
  * even e, high half for odd e -- are below floor((1 - p) 2^32); kept elements
- * are scaled by 1 / (1 - p).  The same (p, seed, offset) in the backward
+  * are scaled by 1 / (1 - p).  The same (p, seed, offset) in the backward
  * regenerates the forward's mask; advance offset per step for a new mask.
+ * keep_mask: NULL, or a device buffer of ceil(T d / 8) bytes holding the mask
+ * as bits (bit e % 8 of byte e / 8 = element e kept).  With p > 0 the forward
+ * calls write it as they apply the dropout; the backward calls read it instead
+ * of regenerating the generator's bits (the same p, seed and offset must
+ * describe the mask it holds).  No alignment requirement.
  * A NULL tpmlp_dropout pointer means p = 0. */
 typedef struct {
   float p;
   uint64_t seed;
   uint64_t offset;
+  uint8_t* keep_mask;
 } tpmlp_dropout;
 
 /* Reduce-scatter modes of tpmlp_sp_forward. */

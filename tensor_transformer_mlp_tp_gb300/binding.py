@@ -37,7 +37,8 @@ class Shape(ctypes.Structure):
 
 
 class Dropout(ctypes.Structure):
-    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+                ("keep_mask", ctypes.c_void_p)]
 
 
 class Fp8State(ctypes.Structure):
@@ -152,8 +153,15 @@ def _ptrs(ts):
     return ctypes.cast(arr, _PP), arr
 
 
-def _dropout(p, seed, offset):
-    return None if p is None else ctypes.byref(Dropout(p, seed, offset))
+def _dropout(p, seed, offset, keep_mask=None):
+    if p is None:
+        return None
+    return ctypes.byref(Dropout(p, seed, offset, None if keep_mask is None else keep_mask.data_ptr()))
+
+
+def keep_mask_bytes(T, d):
+    """Bytes of a dropout keep mask for a gathered [T x d] output: one bit per element."""
+    return (T * d + 7) // 8
 
 
 def _opt_ptrs(ts):
@@ -242,7 +250,7 @@ def tpmlp_sp_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_chunks
 
 
 def tpmlp_sp_block_forward(X_chunks, gamma, beta, A, B, N, Y_chunks, bias=None, bias2=None, p=None, seed=0, offset=0,
-                           eps=1e-5, rs_mode=RS_FUSED, Hpre_out=None, H_out=None, Xg_out=None, ws=None, stream=None):
+                           eps=1e-5, rs_mode=RS_FUSED, Hpre_out=None, H_out=None, Xg_out=None, ws=None, keep_mask=None, stream=None):
     """Y_j = X_j + dropout(Z_j + bias2); p=None passes a NULL dropout (p = 0)."""
     rows, d = X_chunks[0].shape
     shape = make_shape(rows * N, d, A.shape[1], N)
@@ -251,7 +259,7 @@ def tpmlp_sp_block_forward(X_chunks, gamma, beta, A, B, N, Y_chunks, bias=None, 
     xp, _xa = _ptrs(X_chunks)
     yp, _ya = _ptrs(Y_chunks)
     _check("tpmlp_sp_block_forward", lib().tpmlp_sp_block_forward(
-        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _ptr(bias2), _dropout(p, seed, offset),
+        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _ptr(bias2), _dropout(p, seed, offset, keep_mask),
         ctypes.byref(shape), yp, rs_mode, _ptr(Hpre_out), _ptr(H_out), _ptr(Xg_out), _ptr(ws), ws.numel(),
         _stream(stream)))
     return Y_chunks
@@ -259,7 +267,7 @@ def tpmlp_sp_block_forward(X_chunks, gamma, beta, A, B, N, Y_chunks, bias=None, 
 
 def tpmlp_sp_block_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_chunks, dA, dB, dgamma, dbeta,
                             bias=None, dbias=None, dbias2=None, p=None, seed=0, offset=0, eps=1e-5, H=None, Xg=None,
-                            ws=None, stream=None):
+                            ws=None, keep_mask=None, stream=None):
     rows, d = X_chunks[0].shape
     shape = make_shape(rows * N, d, A.shape[1], N)
     ws = workspace(shape, OP_SP_BLOCK_BWD, A.device) if ws is None else ws
@@ -267,7 +275,7 @@ def tpmlp_sp_block_backward(X_chunks, gamma, beta, A, B, Hpre, dY_chunks, N, dX_
     dyp, _dya = _ptrs(dY_chunks)
     dxp, _dxa = _ptrs(dX_chunks)
     _check("tpmlp_sp_block_backward", lib().tpmlp_sp_block_backward(
-        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _dropout(p, seed, offset), _ptr(Hpre),
+        xp, _ptr(gamma), _ptr(beta), eps, _ptr(A), _ptr(B), _ptr(bias), _dropout(p, seed, offset, keep_mask), _ptr(Hpre),
         _ptr(H), _ptr(Xg), dyp, ctypes.byref(shape), dxp, _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dbias2),
         _ptr(dgamma), _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
 
@@ -291,12 +299,12 @@ def tpmlp_gemm2_shard_accum(H, B, N, Y=None, Y_chunks=None, stream=None):
 
 
 def tpmlp_gemm2_bias_dropout_add(H, B, N, Y_chunks, bias2=None, p=None, seed=0, offset=0, R_chunks=None,
-                                 stream=None):
+                                 keep_mask=None, stream=None):
     shape = make_shape(H.shape[0], B.shape[1], H.shape[1], N)
     yp, _ya = _ptrs(Y_chunks)
     rp, _ra = _opt_ptrs(R_chunks)
     _check("tpmlp_gemm2_bias_dropout_add", lib().tpmlp_gemm2_bias_dropout_add(
-        _ptr(H), _ptr(B), _ptr(bias2), _dropout(p, seed, offset), rp, ctypes.byref(shape), yp, _stream(stream)))
+        _ptr(H), _ptr(B), _ptr(bias2), _dropout(p, seed, offset, keep_mask), rp, ctypes.byref(shape), yp, _stream(stream)))
 
 
 def tpmlp_gemm2_partials(H, B, N, P, stream=None):
@@ -313,23 +321,23 @@ def tpmlp_reduce_scatter(P, N, Y_chunks, stream=None):
 
 
 def tpmlp_reduce_scatter_bias_dropout_add(P, N, Y_chunks, bias2=None, p=None, seed=0, offset=0, R_chunks=None,
-                                          stream=None):
+                                          keep_mask=None, stream=None):
     _, T, d = P.shape
     shape = make_shape(T, d, 8 * N, N)  # ffn unused by this step
     yp, _ya = _ptrs(Y_chunks)
     rp, _ra = _opt_ptrs(R_chunks)
     _check("tpmlp_reduce_scatter_bias_dropout_add", lib().tpmlp_reduce_scatter_bias_dropout_add(
-        _ptr(P), _ptr(bias2), _dropout(p, seed, offset), rp, ctypes.byref(shape), yp, _stream(stream)))
+        _ptr(P), _ptr(bias2), _dropout(p, seed, offset, keep_mask), rp, ctypes.byref(shape), yp, _stream(stream)))
 
 
-def tpmlp_dropout_backward(dY_chunks, N, dZ, dbias2=None, p=None, seed=0, offset=0, ws=None, stream=None):
+def tpmlp_dropout_backward(dY_chunks, N, dZ, dbias2=None, p=None, seed=0, offset=0, ws=None, keep_mask=None, stream=None):
     rows, d = dY_chunks[0].shape
     shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
     if dbias2 is not None and ws is None:
         ws = workspace(shape, OP_DROPOUT_BWD, dZ.device)
     dyp, _dya = _ptrs(dY_chunks)
     _check("tpmlp_dropout_backward", lib().tpmlp_dropout_backward(
-        dyp, _dropout(p, seed, offset), ctypes.byref(shape), _ptr(dZ), _ptr(dbias2), _ptr(ws),
+        dyp, _dropout(p, seed, offset, keep_mask), ctypes.byref(shape), _ptr(dZ), _ptr(dbias2), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(stream)))
 
 

@@ -201,6 +201,7 @@ tpmlp_status make_tail(const void* bias2, const tpmlp_dropout* drop, const void*
   t->scale = static_cast<float>(1.0 / keep);
   t->seed = drop != nullptr ? drop->seed : 0;
   t->offset = drop != nullptr ? drop->offset : 0;
+  t->mask = drop != nullptr ? drop->keep_mask : nullptr;
   return TPMLP_OK;
 }
 
@@ -212,6 +213,7 @@ void apply_tail(RowParams& r, const SpTail& t) {
   r.drop_seed = t.seed;
   r.drop_offset = t.offset;
   r.drop_thr = t.thr;
+  r.drop_mask = t.mask;
 }
 
 // ------------------------------------------------------------------ step implementations (validated inputs)

@@ -76,6 +76,7 @@ struct GemmParams {
   int tail;
   float drop_scale;
   unsigned long long drop_seed, drop_offset, drop_thr;  // drop_thr = 2^32 keeps every element
+  uint8_t* drop_mask;  // nullptr, or the keep bits (one byte per 8 elements) written as they are drawn
   ConstChunkPtrs res_chunks;
   // FP8 operands: the accumulator is divided by (*scale_a) (*scale_b); kEpiBiasGeluQ quantises with
   // *scale_out and max-combines its amax into *amax_out.
@@ -113,6 +114,7 @@ struct RowParams {
   ConstChunkPtrs add_chunks;  // N chunk pointers [rows_per_chunk x d] bf16, or p[0] == nullptr
   float drop_scale;
   unsigned long long drop_seed, drop_offset, drop_thr;
+  uint8_t* drop_mask;  // reduce-scatter tail: keep bits written; dropout backward: keep bits read
   const float* qscale;        // E4M3 outputs: quantisation scale (device), and the amax they max-combine into
   float* amax;
   unsigned int* err;          // device error words

@@ -155,6 +155,7 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   p.drop_seed = g.tail.seed;
   p.drop_offset = g.tail.offset;
   p.drop_thr = g.tail.thr;
+  p.drop_mask = g.tail.mask;
   p.res_chunks = g.tail.residual;
   p.a_fmt = g.a_fmt;
   p.b_fmt = g.b_fmt;
@@ -213,6 +214,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
   p.drop_seed = g.tail.seed;
   p.drop_offset = g.tail.offset;
   p.drop_thr = g.tail.thr;
+  p.drop_mask = g.tail.mask;
   p.res_chunks = g.tail.residual;
   p.err = ctx.err;
   p.timeout_ns = ctx.timeout_ns;

@@ -153,6 +153,7 @@ __device__ __forceinline__ void sp_tail_32(const GemmParams& p, float (&v)[32], 
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const uint32_t m = dropout_keep8(q0 + g, p.drop_offset, p.drop_seed, p.drop_thr);
+      if (p.drop_mask != nullptr && col0 + 8 * g < p.N) p.drop_mask[q0 + g] = static_cast<uint8_t>(m);
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[8 * g + j] = (m >> j) & 1u ? v[8 * g + j] * p.drop_scale : 0.f;
     }

@@ -25,6 +25,7 @@ struct SpTail {
   float scale = 1.f;              // 1 / (1 - p)
   unsigned long long seed = 0, offset = 0;
   unsigned long long thr = 1ull << 32;  // floor((1 - p) 2^32); 2^32 keeps all
+  uint8_t* mask = nullptr;        // keep bits: written by the forward tails, read by the dropout backward
 };
 
 struct GemmLaunch {

@@ -51,9 +51,11 @@ __device__ __forceinline__ void sp_tail_8(const RowParams& p, float (&a)[8], lon
 #pragma unroll
     for (int e = 0; e < 8; ++e) a[e] += b[e];
   }
-  const uint32_t m = p.drop_thr < kKeepAll
-                         ? dropout_keep8(static_cast<unsigned long long>(q), p.drop_offset, p.drop_seed, p.drop_thr)
-                         : 0xFFu;
+  uint32_t m = 0xFFu;
+  if (p.drop_thr < kKeepAll) {
+    m = dropout_keep8(static_cast<unsigned long long>(q), p.drop_offset, p.drop_seed, p.drop_thr);
+    if (p.drop_mask != nullptr) p.drop_mask[q] = static_cast<uint8_t>(m);
+  }
 #pragma unroll
   for (int e = 0; e < 8; ++e) a[e] = (m >> e) & 1u ? a[e] * p.drop_scale : 0.f;
   if (p.add_chunks.p[0] != nullptr) {
@@ -538,14 +540,20 @@ __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, cons
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// LayerNorm backward in one pass over x and dy.  Teams of TW warps (8 / TW
+// LayerNorm backward in one pass over x and dy.  Teams of TW warps (CONS / TW
 // teams per CTA) each take one row of the ring at a time; thread j of a team
-// owns the 16-byte column vectors j + k·32·TW, k < VT (d = 256 TW VT).  Row
-// statistics come from warp shuffles plus one team barrier per reduction
-// (double-buffered scratch, two barriers per row); dx goes to the row's chunk;
-// dgamma and dbeta for the thread's columns accumulate in registers over all
-// rows the team processes.  At the end the teams' sums are added in team order
-// into the CTA's partial row [2 d], which a fixed-order column sum reduces.
+// owns the 16-byte column vectors j + k·32·TW, k < VT (d = 256 TW VT).
+// Row statistics in one reduction round from shifted sums: with K the row's
+// first element and c = x - K, S1 = Σc, S2 = Σc², Sg = Σg, Sgc = Σg·c
+// (g = dy·γ) give mean = K + S1/d, var = S2/d - (S1/d)² and
+// Σ g·(x - mean) = Sgc - (S1/d)·Sg; the shift by a sample of the row keeps the
+// variance free of the cancellation that E[x²] - mean² suffers when the mean
+// is large against the spread.  Arithmetic on float pairs (the packed fp32
+// instructions); c stays in registers for the output pass.  dx goes to the
+// row's chunk; dγ and dβ for the thread's columns accumulate in registers over
+// all rows the team processes, and at the end the teams' sums are added in
+// team order into the CTA's partial row [2 d], which a fixed-order column sum
+// reduces.
 __device__ __forceinline__ void team_sync(int team, int tw) {
   if (tw == 1) {
     __syncwarp();
@@ -554,10 +562,32 @@ __device__ __forceinline__ void team_sync(int team, int tw) {
   }
 }
 
+__device__ __forceinline__ float2 bf2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& u, int w) { return w == 0 ? u.x : w == 1 ? u.y : w == 2 ? u.z : u.w; }
+
+// Warp sums of four values in six shuffles: afterwards lane l holds the sum of value (l >> 3) & 3 (a for
+// lanes 0-7, b for 8-15, c for 16-23, d for 24-31).
+__device__ __forceinline__ float warp_sum4(float a, float b, float c, float d) {
+  const int lane = threadIdx.x & 31;
+  const bool hi16 = (lane & 16) != 0;
+  const float k0 = (hi16 ? c : a) + __shfl_xor_sync(0xffffffffu, hi16 ? a : c, 16);
+  const float k1 = (hi16 ? d : b) + __shfl_xor_sync(0xffffffffu, hi16 ? b : d, 16);
+  const bool hi8 = (lane & 8) != 0;
+  float v = (hi8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v;
+}
+
 // ADD: dx += the rows of p.add_chunks (the residual's gradient), loaded while the row statistics reduce.
-template <int VT, int TW, bool ADD = false>
-__global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const RowParams p) {
-  constexpr int kTeams = kStreamConsumers / TW;
+// CONS consumer warps (one more warp produces).
+template <int VT, int TW, bool ADD = false, int CONS = kStreamConsumers>
+__global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(const RowParams p) {
+  constexpr int kTeams = CONS / TW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align128(smem_raw);
   const uint32_t row_bytes = static_cast<uint32_t>(p.d) * 2u;
@@ -565,9 +595,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const
   uint64_t* full = reinterpret_cast<uint64_t*>(gam + p.d / 8);
   uint64_t* empty = full + p.slots;
   int* abort_flag = reinterpret_cast<int*>(empty + p.slots);
-  __shared__ float red1[2][kStreamConsumers];
-  __shared__ float red3[2][kStreamConsumers][3];
-  __shared__ int vote[2][kStreamConsumers];
+  __shared__ float4 red4[2][CONS];
+  __shared__ int vote[2][CONS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.slots; ++s) {
@@ -588,19 +617,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const
   const int team = cw / TW;
   const int tw = cw % TW;         // warp within the team
   const int j = tw * 32 + lane;   // thread within the team
-  float dg[VT][8], db[VT][8];
+  float2 dg[VT][4], db[VT][4];
 #pragma unroll
   for (int k = 0; k < VT; ++k)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) dg[k][e] = db[k][e] = 0.f;
+    for (int w = 0; w < 4; ++w) dg[k][w] = db[k][w] = make_float2(0.f, 0.f);
   if (warp == 0) {
     if (lane == 0) stream_producer(p, ring, 2 * row_bytes, row_bytes, full, empty, n_rows, wc, true);
   } else {
+    const float inv_d = 1.f / static_cast<float>(p.d);
     int parity_buf = 0;
     for (int i = team; i < n_rows; i += kTeams, parity_buf ^= 1) {
       const int slot = i % p.slots;
-      // Every warp of the team waits (bounded) on its own; the outcomes are voted at the first team
-      // barrier, so the team leaves the loop together and no warp is left waiting at a barrier.
+      // Every warp of the team waits (bounded) on its own; the outcomes are voted at the team barrier, so
+      // the team leaves the loop together and no warp is left waiting at a barrier.
       const bool ok = stream_wait(full + slot, static_cast<uint32_t>(i / p.slots) & 1u, wc);
       const uint4* xs = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes);
       const uint4* ds = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes + row_bytes);
@@ -610,6 +640,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const
         xv[k] = ok ? xs[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
         dv[k] = ok ? ds[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
       }
+      const float shift = ok ? __uint_as_float(xs[0].x << 16) : 0.f;  // the row's first element
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(empty + slot);
       uint4 av[VT];
@@ -618,90 +649,69 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const
 #pragma unroll
         for (int k = 0; k < VT; ++k) av[k] = ok ? __ldg(a4 + j + k * 32 * TW) : make_uint4(0, 0, 0, 0);
       }
-      float s = 0.f;
+      const float2 nk = make_float2(-shift, -shift);
+      float2 s1 = make_float2(0.f, 0.f), s2 = s1, sg = s1, sgc = s1;
+      float2 c[VT][4];
 #pragma unroll
       for (int k = 0; k < VT; ++k) {
-        float f[8];
-        unpack8(xv[k], f);
+        const uint4 gk = gam[j + k * 32 * TW];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s += f[e];
+        for (int w = 0; w < 4; ++w) {
+          c[k][w] = __fadd2_rn(bf2(word(xv[k], w)), nk);
+          const float2 g = __fmul2_rn(bf2(word(dv[k], w)), bf2(word(gk, w)));
+          s1 = __fadd2_rn(s1, c[k][w]);
+          s2 = __ffma2_rn(c[k][w], c[k][w], s2);
+          sg = __fadd2_rn(sg, g);
+          sgc = __ffma2_rn(g, c[k][w], sgc);
+        }
       }
-      s = warp_sum(s);
+      const float v = warp_sum4(s1.x + s1.y, s2.x + s2.y, sg.x + sg.y, sgc.x + sgc.y);
+      float4 t;
       bool team_ok = ok;
       if (TW > 1) {
-        if (lane == 0) {
-          red1[parity_buf][cw] = s;
-          vote[parity_buf][cw] = ok ? 1 : 0;
-        }
+        if ((lane & 7) == 0) reinterpret_cast<float*>(&red4[parity_buf][cw])[lane >> 3] = v;
+        if (lane == 0) vote[parity_buf][cw] = ok ? 1 : 0;
         team_sync(team, TW);
-        s = 0.f;
+        t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < TW; ++w) {
-          s += red1[parity_buf][team * TW + w];
+          const float4 r = red4[parity_buf][team * TW + w];
+          t.x += r.x;
+          t.y += r.y;
+          t.z += r.z;
+          t.w += r.w;
           team_ok = team_ok && vote[parity_buf][team * TW + w] != 0;
         }
+      } else {
+        t = make_float4(__shfl_sync(0xffffffffu, v, 0), __shfl_sync(0xffffffffu, v, 8),
+                        __shfl_sync(0xffffffffu, v, 16), __shfl_sync(0xffffffffu, v, 24));
       }
       if (!team_ok) break;
-      const float mean = s / static_cast<float>(p.d);
-      float q = 0.f, sg = 0.f, sgc = 0.f;
-#pragma unroll
-      for (int k = 0; k < VT; ++k) {
-        float f[8], dy[8], g[8];
-        unpack8(xv[k], f);
-        unpack8(dv[k], dy);
-        unpack8(gam[j + k * 32 * TW], g);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float c = f[e] - mean;
-          const float gg = dy[e] * g[e];
-          q += c * c;
-          sg += gg;
-          sgc += gg * c;
-        }
-      }
-      q = warp_sum(q);
-      sg = warp_sum(sg);
-      sgc = warp_sum(sgc);
-      if (TW > 1) {
-        if (lane == 0) {
-          red3[parity_buf][cw][0] = q;
-          red3[parity_buf][cw][1] = sg;
-          red3[parity_buf][cw][2] = sgc;
-        }
-        team_sync(team, TW);
-        q = sg = sgc = 0.f;
-#pragma unroll
-        for (int w = 0; w < TW; ++w) {
-          q += red3[parity_buf][team * TW + w][0];
-          sg += red3[parity_buf][team * TW + w][1];
-          sgc += red3[parity_buf][team * TW + w][2];
-        }
-      }
-      const float rstd = rsqrtf(q / static_cast<float>(p.d) + p.eps);
-      const float m1 = sg / static_cast<float>(p.d);
-      const float m2 = rstd * sgc / static_cast<float>(p.d);
+      const float m = t.x * inv_d;                               // mean - K
+      const float rstd = rsqrtf(fmaxf(t.y * inv_d - m * m, 0.f) + p.eps);
+      const float m1 = t.z * inv_d;                              // mean(g)
+      const float m2 = rstd * (t.w - m * t.z) * inv_d;           // rstd mean(g (x - mean))
+      const float2 r2 = make_float2(rstd, rstd);
+      const float2 nmr = make_float2(-m * rstd, -m * rstd);      // xhat = c rstd - m rstd
+      const float2 nm1r = make_float2(-m1 * rstd, -m1 * rstd);   // dx = g rstd - m1 rstd - xhat m2 rstd
+      const float2 nm2r = make_float2(-m2 * rstd, -m2 * rstd);
       const int row = blockIdx.x + i * gridDim.x;
       uint4* dx4 = reinterpret_cast<uint4*>(out_chunk_row(p, row));
 #pragma unroll
       for (int k = 0; k < VT; ++k) {
-        float f[8], dy[8], g[8], o[8];
-        unpack8(xv[k], f);
-        unpack8(dv[k], dy);
-        unpack8(gam[j + k * 32 * TW], g);
+        const uint4 gk = gam[j + k * 32 * TW];
+        uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xhat = (f[e] - mean) * rstd;
-          o[e] = rstd * (dy[e] * g[e] - m1 - xhat * m2);
-          dg[k][e] += dy[e] * xhat;
-          db[k][e] += dy[e];
+        for (int w = 0; w < 4; ++w) {
+          const float2 xhat = __ffma2_rn(c[k][w], r2, nmr);
+          const float2 dy = bf2(word(dv[k], w));
+          float2 dx = __ffma2_rn(xhat, nm2r, __ffma2_rn(__fmul2_rn(dy, bf2(word(gk, w))), r2, nm1r));
+          dg[k][w] = __ffma2_rn(dy, xhat, dg[k][w]);
+          db[k][w] = __fadd2_rn(db[k][w], dy);
+          if constexpr (ADD) dx = __fadd2_rn(dx, bf2(word(av[k], w)));
+          o[w] = pack_bf16x2(dx.x, dx.y);
         }
-        if constexpr (ADD) {
-          float a[8];
-          unpack8(av[k], a);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] += a[e];
-        }
-        dx4[j + k * 32 * TW] = pack8(o);
+        dx4[j + k * 32 * TW] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
@@ -712,9 +722,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_layernorm_bwd_fused(const
     for (int k = 0; k < VT; ++k) {
       const int col = (j + k * 32 * TW) * 8;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        acc[team * 2 * p.d + col + e] = dg[k][e];
-        acc[team * 2 * p.d + p.d + col + e] = db[k][e];
+      for (int w = 0; w < 4; ++w) {
+        acc[team * 2 * p.d + col + 2 * w] = dg[k][w].x;
+        acc[team * 2 * p.d + col + 2 * w + 1] = dg[k][w].y;
+        acc[team * 2 * p.d + p.d + col + 2 * w] = db[k][w].x;
+        acc[team * 2 * p.d + p.d + col + 2 * w + 1] = db[k][w].y;
       }
     }
   }
@@ -753,48 +765,75 @@ __global__ void __launch_bounds__(256) k_reduce_scatter(const RowParams p) {
   }
 }
 
-// Dropout backward: dst[r] = keep * dY[r] * scale (gathered rows); per block of p.rows_per_block rows
-// the fp32 column sums of those values go to partial[blockIdx.y][d] for the row bias gradient.
-constexpr int kDropRows = 16;   // rows per block unless the grid's y extent (65535) needs more
-constexpr int kDropVecs = 256;  // 16-byte vectors per block row (2048 columns)
+// Column-sum tiling of the dropout backward and the bf16 column partials: a block of kColWarps warps
+// covers 256 columns (one 16-byte vector per lane) and kColWarps runs of `rows_per_warp` rows (one run per
+// warp, 4 loads in flight per lane); the warps' sums are added in warp order in shared memory, so each
+// block writes one fp32 partial row of its 256 columns (a fixed summation order).
+constexpr int kColWarps = 8;
+constexpr int kColWarpRows = 16;  // rows per warp unless the grid's y extent (65535) needs more
 
-__global__ void __launch_bounds__(kDropVecs) k_dropout_bwd(const RowParams p) {
+__device__ __forceinline__ void block_column_partial(const float (&acc)[8], bool active, int lane, int warp, int v,
+                                                     int cols, float* partial) {
+  __shared__ float4 red[kColWarps][32][2];
+  red[warp][lane][0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  red[warp][lane][1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (warp == 0 && active) {
+    float4 a = red[0][lane][0], b = red[0][lane][1];
+#pragma unroll
+    for (int w = 1; w < kColWarps; ++w) {
+      const float4 c = red[w][lane][0], d = red[w][lane][1];
+      a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+      b.x += d.x; b.y += d.y; b.z += d.z; b.w += d.w;
+    }
+    float4* out = reinterpret_cast<float4*>(partial + static_cast<long long>(blockIdx.y) * cols + 8 * v);
+    out[0] = a;
+    out[1] = b;
+  }
+}
+
+// Dropout backward: dst[r] = keep * dY[r] * scale (gathered rows); with p.partial, each block's column sums
+// of those values (the row bias gradient).  KEEP: 0 = every element kept (p = 0), 1 = the forward's saved
+// keep bits, 2 = the generator's bits.  The load-only variants are held to 48 registers (5 blocks per SM)
+// so enough rows are in flight; the generator's 64-bit arithmetic needs more.
+template <int KEEP>
+__global__ void __launch_bounds__(32 * kColWarps, KEEP == 2 ? 1 : 5) k_dropout_bwd(const RowParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nv = p.d / 8;
-  const int v = blockIdx.x * kDropVecs + threadIdx.x;
-  if (v >= nv) return;
-  const int r0 = blockIdx.y * p.rows_per_block;
+  const int v = blockIdx.x * 32 + lane;
+  const bool active = v < nv;
+  const int r0 = (blockIdx.y * kColWarps + warp) * p.rows_per_block;
   const int r1 = min(p.rows, r0 + p.rows_per_block);
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   uint4* dst = static_cast<uint4*>(p.dst);
-  for (int rb = r0; rb < r1; rb += 4) {
-    uint4 raw[4];
+  if (active) {
+    for (int rb = r0; rb < r1; rb += 4) {
+      uint4 raw[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      raw[u] = rb + u < r1 ? __ldg(reinterpret_cast<const uint4*>(chunk_row(p, rb + u)) + v) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 4; ++u)
+        raw[u] = rb + u < r1 ? __ldg(reinterpret_cast<const uint4*>(chunk_row(p, rb + u)) + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (rb + u >= r1) break;
-      const long long q = static_cast<long long>(rb + u) * nv + v;
-      const uint32_t m = p.drop_thr < kKeepAll
-                             ? dropout_keep8(static_cast<unsigned long long>(q), p.drop_offset, p.drop_seed, p.drop_thr)
-                             : 0xFFu;
-      float f[8];
-      unpack8(raw[u], f);
+      for (int u = 0; u < 4; ++u) {
+        if (rb + u >= r1) break;
+        const long long q = static_cast<long long>(rb + u) * nv + v;
+        uint32_t m = 0xFFu;
+        if constexpr (KEEP == 1) m = p.drop_mask[q];
+        if constexpr (KEEP == 2)
+          m = dropout_keep8(static_cast<unsigned long long>(q), p.drop_offset, p.drop_seed, p.drop_thr);
+        float f[8];
+        unpack8(raw[u], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        f[e] = (m >> e) & 1u ? f[e] * p.drop_scale : 0.f;
-        acc[e] += f[e];
+        for (int e = 0; e < 8; ++e) {
+          f[e] = (m >> e) & 1u ? f[e] * p.drop_scale : 0.f;
+          acc[e] += f[e];
+        }
+        dst[q] = pack8(f);
       }
-      dst[q] = pack8(f);
     }
   }
-  if (p.partial != nullptr) {
-    float4* out = reinterpret_cast<float4*>(p.partial + static_cast<long long>(blockIdx.y) * p.d + 8 * v);
-    out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  }
+  if (p.partial != nullptr) block_column_partial(acc, active, lane, warp, v, p.d, p.partial);
 }
 
 // Contiguous dst[T x d] <- the N chunk pointers.
@@ -820,8 +859,17 @@ __global__ void __launch_bounds__(256) k_column_sum(const float* __restrict__ pa
   const int lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
-  if (c < cols)
-    for (int r = slice; r < rows; r += 8) s += partial[static_cast<long long>(r) * stride + c];
+  if (c < cols) {
+    // four independent chains (rows slice + 8 (4 k + u)), combined in a fixed order: loads stay in flight
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    int r = slice;
+    for (; r + 24 < rows; r += 32) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] += partial[static_cast<long long>(r + 8 * u) * stride + c];
+    }
+    for (int u = 0; r < rows; r += 8, ++u) a[u & 3] += partial[static_cast<long long>(r) * stride + c];
+    s = (a[0] + a[1]) + (a[2] + a[3]);
+  }
   red[slice][lane] = s;
   __syncthreads();
   if (slice == 0 && c < cols) {
@@ -837,27 +885,36 @@ __global__ void __launch_bounds__(256) k_column_sum(const float* __restrict__ pa
   }
 }
 
-// partial[y, c] = sum of src[r, c] over the rows r of block row y (a bf16 matrix with row stride ld);
-// 8 columns per thread, kDropRows rows (or more) per block row.
-__global__ void __launch_bounds__(kDropVecs) k_column_partial_bf16(const __nv_bfloat16* __restrict__ src, int rows,
-                                                                   int cols, long long ld, int rows_per_block,
-                                                                   float* __restrict__ partial) {
-  const int v = blockIdx.x * kDropVecs + threadIdx.x;
-  if (v >= cols / 8) return;
-  const int r0 = blockIdx.y * rows_per_block;
-  const int r1 = min(rows, r0 + rows_per_block);
+// partial[y, c] = the column sums of src over block row y's rows (a bf16 matrix with row stride ld), in the
+// tiling of k_dropout_bwd.
+__global__ void __launch_bounds__(32 * kColWarps, 6) k_column_partial_bf16(const __nv_bfloat16* __restrict__ src, int rows,
+                                                                        int cols, long long ld, int rows_per_warp,
+                                                                        float* __restrict__ partial) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int v = blockIdx.x * 32 + lane;
+  const bool active = v < cols / 8;
+  const int r0 = (blockIdx.y * kColWarps + warp) * rows_per_warp;
+  const int r1 = min(rows, r0 + rows_per_warp);
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    float f[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * ld) + v), f);
+  if (active) {
+    for (int rb = r0; rb < r1; rb += 4) {
+      uint4 raw[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += f[e];
+      for (int u = 0; u < 4; ++u)
+        raw[u] = rb + u < r1 ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(rb + u) * ld) + v)
+                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float f[8];
+        unpack8(raw[u], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += f[e];
+      }
+    }
   }
-  float4* out = reinterpret_cast<float4*>(partial + static_cast<long long>(blockIdx.y) * cols + 8 * v);
-  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  block_column_partial(acc, active, lane, warp, v, cols, partial);
 }
 
 // ----------------------------------------------------------------------------- E4M3 casts and delayed scaling
@@ -995,10 +1052,11 @@ int stream_grid(long long work_items, int sm_count) {
 }  // namespace
 
 template <typename K>
-static cudaError_t launch_stream(K kern, const RowParams& r, size_t smem, int grid, cudaStream_t s) {
+static cudaError_t launch_stream(K kern, const RowParams& r, size_t smem, int grid, cudaStream_t s,
+                                 int threads = kStreamThreads) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kStreamThreads, smem, s>>>(r);
+  kern<<<grid, threads, smem, s>>>(r);
   return cudaGetLastError();
 }
 
@@ -1210,23 +1268,51 @@ cudaError_t launch_reduce_scatter(const RowParams& r, const DeviceCtx& ctx, cuda
   return cudaGetLastError();
 }
 
+// Rows per warp of the column-sum tiling: kColWarpRows, or more when the grid's y extent would pass 65535.
 int dropout_rows_per_block(int rows) {
-  const int need = (rows + 65534) / 65535;
-  return need <= kDropRows ? kDropRows : need;
+  const long long per_block_row = 65535LL * kColWarps;
+  const int need = static_cast<int>((rows + per_block_row - 1) / per_block_row);
+  return need <= kColWarpRows ? kColWarpRows : need;
+}
+
+int column_block_rows(int rows, int rows_per_warp) {
+  const int per = rows_per_warp * kColWarps;
+  return (rows + per - 1) / per;
+}
+
+// Rows per warp for one wave of `resident` blocks per SM (never fewer than dropout_rows_per_block, so the
+// partial rows stay within what dropout_bwd_scratch_floats sized).
+int rows_per_warp_one_wave(int rows, int cols, int resident) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    sms = 1;
+  const int col_blocks = (cols / 8 + 31) / 32;
+  int row_blocks = resident * sms / col_blocks;
+  if (row_blocks < 1) row_blocks = 1;
+  const int want = (rows + kColWarps * row_blocks - 1) / (kColWarps * row_blocks);
+  const int least = dropout_rows_per_block(rows);
+  return want > least ? want : least;
 }
 
 size_t dropout_bwd_scratch_floats(int rows, int d) {
-  const int rpb = dropout_rows_per_block(rows);
-  return static_cast<size_t>((rows + rpb - 1) / rpb) * static_cast<size_t>(d);
+  return static_cast<size_t>(column_block_rows(rows, dropout_rows_per_block(rows))) * static_cast<size_t>(d);
 }
 
 cudaError_t launch_dropout_bwd(const RowParams& r, float* partial, void* dbias2, cudaStream_t s) {
   if (r.rows <= 0) return cudaSuccess;
   RowParams q = r;
   q.partial = dbias2 != nullptr ? partial : nullptr;
-  q.rows_per_block = dropout_rows_per_block(r.rows);
-  const dim3 grid((r.d / 8 + kDropVecs - 1) / kDropVecs, (r.rows + q.rows_per_block - 1) / q.rows_per_block);
-  k_dropout_bwd<<<grid, kDropVecs, 0, s>>>(q);
+  q.rows_per_block = rows_per_warp_one_wave(r.rows, r.d, r.drop_thr < kKeepAll && r.drop_mask == nullptr ? 2 : 5);
+  const dim3 grid((r.d / 8 + 31) / 32, column_block_rows(r.rows, q.rows_per_block));
+  // the forward's keep bits when it saved them, else the generator's
+  if (q.drop_thr >= kKeepAll) {
+    k_dropout_bwd<0><<<grid, 32 * kColWarps, 0, s>>>(q);
+  } else if (q.drop_mask != nullptr) {
+    k_dropout_bwd<1><<<grid, 32 * kColWarps, 0, s>>>(q);
+  } else {
+    k_dropout_bwd<2><<<grid, 32 * kColWarps, 0, s>>>(q);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || dbias2 == nullptr) return e;
   return launch_column_sum(partial, static_cast<int>(grid.y), r.d, dbias2, true, s);
@@ -1244,9 +1330,9 @@ cudaError_t launch_column_sum_bf16(const void* src, int rows, int cols, long lon
                                    cudaStream_t s) {
   if (rows <= 0 || cols <= 0 || out == nullptr) return cudaSuccess;
   if (cols % 8 != 0 || ld % 8 != 0) return cudaErrorInvalidValue;
-  const int rpb = dropout_rows_per_block(rows);
-  const dim3 grid((cols / 8 + kDropVecs - 1) / kDropVecs, (rows + rpb - 1) / rpb);
-  k_column_partial_bf16<<<grid, kDropVecs, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, ld, rpb,
+  const int rpw = rows_per_warp_one_wave(rows, cols, 6);
+  const dim3 grid((cols / 8 + 31) / 32, column_block_rows(rows, rpw));
+  k_column_partial_bf16<<<grid, 32 * kColWarps, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, ld, rpw,
                                                    partial);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -125,7 +125,7 @@ def test_sp_region_workspace_sizes(lib):
         if w.dtype != "bf16" or not w.sp:
             continue
         s = binding.make_shape(w.T, w.d, w.F, w.N)
-        dropcol = _r256(-(-w.T // 16) * w.d * 4)       # fp32 column partials, one row per 16 token rows
+        dropcol = _r256(-(-w.T // 128) * w.d * 4)      # fp32 column partials, one row per 128 token rows
         assert _ws(s, binding.OP_DROPOUT_BWD) == (binding.OK, dropcol)
         st, spb = _ws(s, binding.OP_SP_BWD)
         assert _ws(s, binding.OP_SP_BLOCK_BWD) == (binding.OK, spb + dropcol)
@@ -241,7 +241,7 @@ def test_attention_backward_workspace_and_argument_checks(lib):
     S, B, H = 1000, 2, 4  # S_pad = 1024
     assert L.tpmlp_attention_backward_workspace_size(S, B, H, 128, ctypes.byref(n)) == binding.OK
     T, d = S * B, H * 128
-    rows_per_block = 16
+    rows_per_block = 128  # 8 warps x 16 rows
     partial = (T + rows_per_block - 1) // rows_per_block * 3 * d * 4
     assert n.value == _r256(B * H * 1024 * 4) + _r256(T * d * 2) + _r256(T * 3 * d * 2) + _r256(partial)
     assert binding.attention_lse_shape(S, B, H) == (B * H, 1024)
@@ -266,3 +266,11 @@ def test_attention_backward_workspace_and_argument_checks(lib):
     bad = list(args)
     bad[19] = 4096
     assert L.tpmlp_attention_tp_backward(*bad) == binding.ERR_WORKSPACE
+
+
+def test_dropout_struct_layout():
+    """tpmlp_dropout as the header lays it out: float p, then two 64-bit words and the mask pointer."""
+    D = binding.Dropout
+    assert ctypes.sizeof(D) == 32
+    assert (D.p.offset, D.seed.offset, D.offset.offset, D.keep_mask.offset) == (0, 8, 16, 24)
+    assert binding.keep_mask_bytes(3, 8) == 3 and binding.keep_mask_bytes(1, 12) == 2

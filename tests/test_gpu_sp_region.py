@@ -213,3 +213,99 @@ def test_dropout_mask_changes_with_offset_and_seed():
     assert np.array_equal(outs[0], oracle.dropout_keep(T, d, 0, 0.5, 1, 0))
     for other in outs[1:3]:
         assert 0.4 < (outs[0] == other).mean() < 0.6
+
+
+# ----------------------------------------------------------------------------- saved keep mask
+
+def _packed_keep(T, d, p):
+    """The oracle's keep mask as the bit layout the calls write: bit e % 8 of byte e / 8."""
+    return np.packbits(_keep(T, d, p).reshape(-1), bitorder="little")
+
+
+def _mask_buffer(T, d):
+    return Guarded((binding.keep_mask_bytes(T, d),), torch.uint8)
+
+
+@pytest.mark.parametrize("T,d,F,N", [(512, 384, 1536, 4), (96, 136, 544, 2)])
+def test_keep_mask_written_by_the_row_parallel_gemm(T, d, F, N):
+    """The fused store writes the keep bits it applies (bit for bit the oracle's mask; d = 136 has a
+    ragged 32-column group at each row's end)."""
+    p = 0.3
+    w = inputs.small_workload(T, d, N, F=F, sp=True, name=f"g2mask_{T}_{d}_{N}")
+    H, B = inputs.draw(w, "H", shape=(T, F), dist=(0.0, 1.0)), inputs.draw(w, "B")
+    rows = T // N
+    mask = _mask_buffer(T, d)
+    Y = [torch.empty(rows, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    binding.tpmlp_gemm2_bias_dropout_add(dev(H[0]), dev(B[0]), N, Y, p=p, seed=SEED, offset=OFFSET,
+                                         keep_mask=mask.t)
+    torch.cuda.synchronize()
+    assert np.array_equal(mask.t.cpu().numpy(), _packed_keep(T, d, p))
+    assert mask.intact()
+
+
+def test_keep_mask_written_by_the_reduce_scatter():
+    N, p = 4, 0.25
+    T, d = 64 * N, 200
+    rng = np.random.default_rng(7)
+    Pb = inputs.f32_to_bf16_bits(rng.normal(size=(N, T, d)).astype(np.float32)).reshape(N, T, d)
+    rows = T // N
+    mask = _mask_buffer(T, d)
+    Y = [torch.empty(rows, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    binding.tpmlp_reduce_scatter_bias_dropout_add(dev(Pb), N, Y, p=p, seed=SEED, offset=OFFSET, keep_mask=mask.t)
+    torch.cuda.synchronize()
+    assert np.array_equal(mask.t.cpu().numpy(), _packed_keep(T, d, p))
+    assert mask.intact()
+
+
+@pytest.mark.parametrize("T,d,N,p", [(1000, 1024, 8, 0.1), (96, 136, 3, 0.5)])
+def test_dropout_backward_reads_the_keep_mask(T, d, N, p):
+    """With the saved mask the backward gives the same bits as regenerating it; a mask that differs from
+    the generator's (all ones) is what the backward then applies."""
+    w = inputs.small_workload(T, d, N, sp=True, backward=True, name=f"dropbwd_{T}_{d}_{N}")
+    dY = inputs.draw(w, "dY")
+    rows = T // N
+    dYc = list(dev(dY[0]).split(rows))
+    mask = torch.from_numpy(_packed_keep(T, d, p)).cuda()
+    outs = []
+    for m in (None, mask):
+        dZ = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+        db2 = torch.empty(d, dtype=torch.bfloat16, device="cuda")
+        binding.tpmlp_dropout_backward(dYc, N, dZ, dbias2=db2, p=p, seed=SEED, offset=OFFSET, keep_mask=m)
+        outs.append((dZ, db2))
+    ones = torch.full((binding.keep_mask_bytes(T, d),), 255, dtype=torch.uint8, device="cuda")
+    dZ1 = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    binding.tpmlp_dropout_backward(dYc, N, dZ1, p=p, seed=SEED, offset=OFFSET, keep_mask=ones)
+    torch.cuda.synchronize()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    scale = 1.0 / (1.0 - float(np.float32(p)))
+    assert_bf16_close("dZ (mask of ones)", f64(dZ1), dY[1] * scale)
+
+
+def test_sp_block_keep_mask_forward_to_backward():
+    """The block forward saves the mask; the block backward given it matches the one that regenerates it."""
+    T, d, N, p = 256, 256, 4, 0.2
+    w = inputs.small_workload(T, d, N, sp=True, backward=True, bias=(0.0, 0.2), name="spblock_mask")
+    X, A, B, b, g, be, dY = [inputs.draw(w, n) for n in ("X", "A", "B", "bias", "gamma", "beta", "dY")]
+    F = w.F
+    rows = T // N
+    Xc = list(dev(X[0]).split(rows))
+    Ad, Bd, bd, gd, bed = dev(A[0]), dev(B[0]), dev(b[0]), dev(g[0]), dev(be[0])
+    mask = _mask_buffer(T, d)
+    Hpre = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    Y = [torch.empty(rows, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    binding.tpmlp_sp_block_forward(Xc, gd, bed, Ad, Bd, N, Y, bias=bd, p=p, seed=SEED, offset=OFFSET,
+                                   Hpre_out=Hpre, keep_mask=mask.t)
+    grads = []
+    for m in (None, mask.t):
+        dX = [torch.empty(rows, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+        dA, dB = torch.empty(d, F, dtype=torch.bfloat16, device="cuda"), torch.empty(F, d, dtype=torch.bfloat16, device="cuda")
+        dga, dbe = torch.empty(d, device="cuda"), torch.empty(d, device="cuda")
+        binding.tpmlp_sp_block_backward(Xc, gd, bed, Ad, Bd, Hpre, list(dev(dY[0]).split(rows)), N, dX, dA, dB, dga,
+                                        dbe, bias=bd, p=p, seed=SEED, offset=OFFSET, keep_mask=m)
+        grads.append(dX + [dA, dB, dga, dbe])
+    torch.cuda.synchronize()
+    assert np.array_equal(mask.t.cpu().numpy(), _packed_keep(T, d, p))
+    for a, b in zip(*grads):
+        assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a.view(torch.int16),
+                           b.view(torch.int32) if b.dtype == torch.float32 else b.view(torch.int16))
