@@ -26,6 +26,13 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
+// The two bf16 values of a 32-bit word as a float pair (low half first), and word w of a 16-byte vector.
+__device__ __forceinline__ float2 bf2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& u, int w) { return w == 0 ? u.x : w == 1 ? u.y : w == 2 ? u.z : u.w; }
+
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                     pack_bf16x2(f[6], f[7]));
@@ -77,6 +84,36 @@ __device__ __forceinline__ __nv_bfloat16* out_chunk_row(const RowParams& p, int 
 // (d = 256 V WPR).  Mean first, then the biased variance from the centred
 // values (two passes over registers), rstd = rsqrt(var + eps), one bf16
 // rounding at the output.
+// Warp sums of two values in five shuffles (lanes 0-15 end with a's, 16-31 with b's) and two broadcasts.
+__device__ __forceinline__ float2 warp_sum2(float a, float b) {
+  const bool hi = (threadIdx.x & 16) != 0;
+  float v = (hi ? b : a) + __shfl_xor_sync(0xffffffffu, hi ? a : b, 16);
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return make_float2(__shfl_sync(0xffffffffu, v, 0), __shfl_sync(0xffffffffu, v, 16));
+}
+
+// Row sums of two values over the WPR warps of a row (all threads of the block call it).
+template <int V, int WPR>
+__device__ __forceinline__ float2 row_sum2(float a, float b, float2* red2, int warp) {
+  float2 v = warp_sum2(a, b);
+  if constexpr (WPR == 1) {
+    return v;
+  } else {
+    if ((threadIdx.x & 31) == 0) red2[warp] = v;
+    __syncthreads();
+    float2 t = make_float2(0.f, 0.f);
+    const int first = warp - warp % WPR;
+#pragma unroll
+    for (int k = 0; k < WPR; ++k) {
+      t.x += red2[first + k].x;
+      t.y += red2[first + k].y;
+    }
+    __syncthreads();
+    return t;
+  }
+}
+
 template <int V, int WPR>
 __device__ __forceinline__ float row_sum(float v, float* red, int warp) {
   v = warp_sum(v);
@@ -98,9 +135,14 @@ __device__ __forceinline__ float row_sum(float v, float* red, int warp) {
 // rstd = rsqrt(mean(x^2) + eps), n = bf16(x rstd), y = bf16(n * gamma).
 // Q8 = true: the fp32 LayerNorm value y is written as E4M3(y * (*p.qscale)) (one byte) and max |y| is
 // max-combined into *p.amax.
+// A warp holds its row (V 16-byte vectors per lane) in registers; at V = 16 the register count is held to
+// what kLnRegMinBlocks resident blocks allow, so enough rows are in flight to cover the memory latency.
+constexpr int kLnRegMinBlocks = 4;
+
 template <int V, int WPR, bool RMS = false, bool Q8 = false>
-__global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
+__global__ void __launch_bounds__(128, V >= 16 ? kLnRegMinBlocks : 1) k_layernorm_fwd_reg(const RowParams p) {
   __shared__ float red[4];
+  __shared__ float2 red2[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * (4 / WPR) + warp / WPR;
   const int sub = warp % WPR;
@@ -109,30 +151,38 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
   uint4 x[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) x[v] = valid ? __ldg(src + (sub * V + v) * 32 + lane) : make_uint4(0, 0, 0, 0);
-  float mean = 0.f;
+  float mean = 0.f, rstd;
   if constexpr (!RMS) {
-    float s = 0.f;
+    // Shifted sums (K = the row's first element): Σc and Σc² of c = x - K in one reduction round give
+    // mean = K + Σc/d and var = Σc²/d - (Σc/d)², without the cancellation of E[x²] - mean² when the mean
+    // is large against the spread.
+    const float K = valid ? __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(src))) << 16)
+                          : 0.f;
+    const float2 nk = make_float2(-K, -K);
+    float2 s1 = make_float2(0.f, 0.f), s2 = s1;
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 c = __fadd2_rn(bf2(word(x[v], w)), nk);
+        s1 = __fadd2_rn(s1, c);
+        s2 = __ffma2_rn(c, c, s2);
+      }
+    const float2 t = row_sum2<V, WPR>(s1.x + s1.y, s2.x + s2.y, red2, warp);
+    const float m = t.x / static_cast<float>(p.d);
+    mean = K + m;
+    rstd = rsqrtf(fmaxf(t.y / static_cast<float>(p.d) - m * m, 0.f) + p.eps);
+  } else {
+    float q = 0.f;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       float f[8];
       unpack8(x[v], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s += f[e];
+      for (int e = 0; e < 8; ++e) q += f[e] * f[e];
     }
-    mean = row_sum<V, WPR>(s, red, warp) / static_cast<float>(p.d);
+    rstd = rsqrtf(row_sum<V, WPR>(q, red, warp) / static_cast<float>(p.d) + p.eps);
   }
-  float q = 0.f;
-#pragma unroll
-  for (int v = 0; v < V; ++v) {
-    float f[8];
-    unpack8(x[v], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float c = f[e] - mean;
-      q += c * c;
-    }
-  }
-  const float rstd = rsqrtf(row_sum<V, WPR>(q, red, warp) / static_cast<float>(p.d) + p.eps);
   const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
   const uint4* b4 = reinterpret_cast<const uint4*>(p.beta);
   const long long row_off = static_cast<long long>(valid ? row : 0) * p.d;
@@ -141,20 +191,28 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_reg(const RowParams p) {
   float qs = 1.f, amax = 0.f;
   if constexpr (Q8) qs = __ldg(p.qscale);
   if (valid) {
+    const float2 nm = make_float2(-mean, -mean), r2 = make_float2(rstd, rstd);
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int idx = (sub * V + v) * 32 + lane;
-      float f[8], g[8], o[8];
-      unpack8(x[v], f);
-      unpack8(__ldg(g4 + idx), g);
+      const uint4 gv = __ldg(g4 + idx);
+      float o[8];
       if constexpr (RMS) {
+        float f[8], g[8];
+        unpack8(x[v], f);
+        unpack8(gv, g);
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(f[e] * rstd)) * g[e];
       } else {
-        float b[8];
-        unpack8(__ldg(b4 + idx), b);
+        // (x - mean) rstd γ + β on float pairs
+        const uint4 bv = __ldg(b4 + idx);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+        for (int w = 0; w < 4; ++w) {
+          const float2 y = __ffma2_rn(__fmul2_rn(__fadd2_rn(bf2(word(x[v], w)), nm), r2), bf2(word(gv, w)),
+                                      bf2(word(bv, w)));
+          o[2 * w] = y.x;
+          o[2 * w + 1] = y.y;
+        }
       }
       if constexpr (Q8) {
 #pragma unroll
@@ -561,12 +619,6 @@ __device__ __forceinline__ void team_sync(int team, int tw) {
     asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * tw) : "memory");
   }
 }
-
-__device__ __forceinline__ float2 bf2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-__device__ __forceinline__ uint32_t word(const uint4& u, int w) { return w == 0 ? u.x : w == 1 ? u.y : w == 2 ? u.z : u.w; }
 
 // Warp sums of four values in six shuffles: afterwards lane l holds the sum of value (l >> 3) & 3 (a for
 // lanes 0-7, b for 8-15, c for 16-23, d for 24-31).

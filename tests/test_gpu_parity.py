@@ -373,3 +373,36 @@ def test_layernorm_gather_long_sequences(T, d, N):
     rows = np.unique(np.concatenate([rng.integers(0, T, 384), np.arange(0, T, T // N), np.arange(T // N - 1, T, T // N)]))
     ref = oracle.layer_norm(X[1][rows], g[1], b[1], 1e-5)
     assert_bf16_close("Xg sample", f64(Xg[torch.from_numpy(rows).cuda()]), ref)
+
+
+@pytest.mark.parametrize("d", [1024, 4096, 8192])
+def test_layernorm_backward_large_mean(d):
+    """Rows whose mean is large against their spread (x = 3000 + 50 N(0, 1) in bf16, steps of 16): the
+    streamed backward's shifted sums keep the variance, where E[x^2] - mean^2 in fp32 (about 9e6, in
+    steps of 0.5 to 1) would lose a few per cent of it."""
+    T, N = 64, 4
+    w = inputs.small_workload(T, d, N, sp=True, backward=True, name=f"lnbwd_mean_{d}")
+    g, dXg = inputs.draw(w, "gamma"), inputs.draw(w, "dY")
+    X = inputs.draw(w, "X", dist=(3000.0, 50.0))
+    rows = T // N
+    dX = [torch.empty(rows, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    dga, dbe = torch.empty(d, device="cuda"), torch.empty(d, device="cuda")
+    binding.tpmlp_layernorm_backward(list(dev(X[0]).split(rows)), dev(g[0]), dev(dXg[0]), N, dX, dga, dbe)
+    torch.cuda.synchronize()
+    refs = [oracle.layer_norm_backward(X[1][lo:hi], g[1], 1e-5, dXg[1][lo:hi]) for lo, hi in oracle.chunk_ranges(T, N)]
+    assert_bf16_close("dX", np.concatenate([f64(x) for x in dX]), np.concatenate([r[0] for r in refs]))
+    assert_bf16_close("dgamma", f64(dga), sum(r[1] for r in refs))
+
+
+@pytest.mark.parametrize("d", [1024, 4096, 8192])
+def test_layernorm_forward_large_mean(d):
+    """The gathered LayerNorm on rows whose mean is 60 times their spread (shifted one-round statistics)."""
+    T, N = 64, 4
+    w = inputs.small_workload(T, d, N, sp=True, name=f"lnfwd_mean_{d}")
+    g, b = inputs.draw(w, "gamma"), inputs.draw(w, "beta")
+    X = inputs.draw(w, "X", dist=(3000.0, 50.0))
+    Xg = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    binding.tpmlp_layernorm_gather(list(dev(X[0]).split(T // N)), dev(g[0]), dev(b[0]), N, Xg)
+    torch.cuda.synchronize()
+    ref = oracle.all_gather([oracle.layer_norm(c, g[1], b[1], 1e-5) for c in _chunks(X[1], N)])
+    assert_bf16_close("Xg", f64(Xg), ref)
