@@ -563,13 +563,19 @@ def run_attention(step, torch, binding, pk):
             "core_bwd_frac": round(core_bwd_flops / (ms_core_b * 1e-3) / 1e12 / peak, 3)}
 
 
-def run_other_rows(step, torch, binding, pk):
+OTHER_ROWS = ("reduce_scatter_explicit", "rmsnorm_gather", "layernorm_gather_isolated", "gemm2_bias_dropout_add",
+              "dropout_backward", "layernorm_gather_long_sequence", "fp8", "attention_tp", "fp32_tiny_forward")
+
+
+def run_other_rows(step, torch, binding, pk, only=None):
     """Rows of the hot path the step does not run: the explicit reduce-scatter (per-shard bf16 partials, then
-    the reduce-scatter kernel) and the RMS norm variant on the step's shapes, and the fp32 path on the tiny
-    fp32 workload."""
+    the reduce-scatter kernel), the RMS norm variant, the rest of the SP region, FP8, attention on the step's
+    shapes, and the fp32 path on the tiny fp32 workload.  `only`: one name of OTHER_ROWS (the others are
+    skipped)."""
     w = step.w
     out = {}
-    if w.sp and (w.F // w.N) % 64 == 0:
+    want = lambda name: only is None or only == name
+    if want("reduce_scatter_explicit") and w.sp and (w.F // w.N) % 64 == 0:
         P = torch.empty(w.N, w.T, w.d, dtype=torch.bfloat16, device="cuda")
         Yc = [torch.empty(w.T // w.N, w.d, dtype=torch.bfloat16, device="cuda") for _ in range(w.N)]
         g = 2.0 * w.T * w.d * w.F
@@ -583,7 +589,7 @@ def run_other_rows(step, torch, binding, pk):
                                           "frac": round(rs_bytes / (ms_rs * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
                                           "bytes_per_launch": rs_bytes}
         del P, Yc
-    if w.sp:
+    if (want("rmsnorm_gather") or want("layernorm_gather_isolated")) and w.sp:
         # the RMS norm variant of the gathered norm, and the LayerNorm beside it timed the same way; the calls
         # alternate between (X -> Xg) and (dY -> dXg) so each reads 2 T d bytes the previous call did not touch
         # (256 MB of inputs and outputs in all, about twice the L2)
@@ -595,7 +601,7 @@ def run_other_rows(step, torch, binding, pk):
             ms = time_calls(torch, pair, 20) / 2.0
             out[name] = {"ms": round(ms, 4), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
                          "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes_per_launch": nb}
-    if w.sp:
+    if (want("gemm2_bias_dropout_add") or want("dropout_backward")) and w.sp:
         # the rest of the sequence-parallel region on the step's shapes: the row-parallel GEMM with row bias,
         # dropout (p = 0.1) and residual in its chunked store, and the dropout backward (+ row-bias gradient)
         g = 2.0 * w.T * w.d * w.F
@@ -632,7 +638,7 @@ def run_other_rows(step, torch, binding, pk):
                                        "bytes_per_launch": nbm, "launches": 2, "keep_mask": "saved by the forward",
                                        "regenerated_mask_ms": round(ms_d, 4),
                                        "regenerated_mask_frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
-    if w.sp and w.d in (1024, 2048, 4096):
+    if want("layernorm_gather_long_sequence") and w.sp and w.d in (1024, 2048, 4096):
         # the LayerNorm forward on a sequence 8x as long (same d): enough rows per warp for the persistent,
         # software-pipelined kernel, whose start-up the step's 8192 rows do not amortise
         Tl = 8 * w.T
@@ -647,11 +653,13 @@ def run_other_rows(step, torch, binding, pk):
                                                  "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
                                                  "bytes_per_launch": nb}
         del xl, yl
-    if (w.sp and w.backward and w.T % 16 == 0 and w.d % 16 == 0 and w.F % 16 == 0 and
+    if want("fp8") and (w.sp and w.backward and w.T % 16 == 0 and w.d % 16 == 0 and w.F % 16 == 0 and
             w.d in (256, 512, 1024, 2048, 4096, 8192)):
         out["fp8"] = run_fp8_step(step, torch, binding, pk)
-    if w.d % 128 == 0 and w.T % 2 == 0:
+    if want("attention_tp") and w.d % 128 == 0 and w.T % 2 == 0:
         out["attention_tp"] = run_attention(step, torch, binding, pk)
+    if not want("fp32_tiny_forward"):
+        return out
     t = inputs.WORKLOADS["tiny_fp32_fwd"]
     f32 = lambda name: torch.from_numpy(np.ascontiguousarray(inputs.draw(t, name)[0])).cuda()
     X, A, B, b = f32("X"), f32("A"), f32("B"), f32("bias")
@@ -741,18 +749,19 @@ def run_ours(args, w):
             ach = work / (avg * 1e-3) / 1e9
             kern[name] = {"ms": round(avg, 4), "GB/s": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 3),
                           "launches": nl, "dram_bytes": measured_traffic(name, w.name)}
-    e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
-    st, site = binding.tpmlp_get_device_status()
-    if st != binding.OK:
-        raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
-    e2e_ms = max_over_ranks(e2e_ms, dist)
-    other = run_other_rows(step, torch, binding, peaks()[0])
+    if args.only_row is None:
+        e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
+        st, site = binding.tpmlp_get_device_status()
+        if st != binding.OK:
+            raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
+        e2e_ms = max_over_ranks(e2e_ms, dist)
+    other = run_other_rows(step, torch, binding, peaks()[0], only=args.only_row)
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after the other rows: {binding.status_string(st)} (site {site})")
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only_row is None:
         dt, tok, fl = oracle_sample(w, tokens=args.oracle_tokens)
         cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -782,7 +791,8 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h,
                 "what": "block calls (tpmlp_sp_forward/backward) with X, dY copied from pinned host memory and Y, dX "
                         "copied back each step on a second stream, double-buffered so copies overlap the previous "
-                        "step's kernels; weights and their gradients stay in HBM"},
+                        "step's kernels; weights and their gradients stay in HBM"}
+               if args.only_row is None else {"skipped": "--only-row " + args.only_row},
         "other_rows": other,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
@@ -803,6 +813,8 @@ def main():
     ap.add_argument("--workload", default="sp_block_fwd_bwd", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--oracle-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-row", choices=OTHER_ROWS, default=None,
+                    help="after the step, time only this row of other_rows (no e2e, no CPU baseline): for profiling")
     args = ap.parse_args()
     w = inputs.WORKLOADS[args.workload]
     if w.dtype != "bf16":
