@@ -108,6 +108,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 16 columns into TMEM (thread t writes its lane's 16 words).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 // Bounded wait without a suspend-time hint: the per-tile handoffs between producer, MMA issuer and softmax
 // warps are short and on the critical path, where a sleeping wait's wake-up would add to every tile.
 __device__ __forceinline__ bool spin_try_wait(uint64_t* bar, uint32_t parity) {
@@ -455,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
 
 // ----------------------------------------------------------------------------- attention backward
 
-constexpr int kBwdComputeWarps = 16;                      // four per TMEM lane quadrant, 32 columns each
+constexpr int kBwdComputeWarps = 16;
+constexpr int kDqKStages = 3;                             // K ring of the dQ kernel                      // four per TMEM lane quadrant, 32 columns each
 constexpr int kBwdThreads = 32 * (2 + kBwdComputeWarps);  // producer, MMA issuer, compute warps
 
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& c) {
@@ -507,19 +518,6 @@ struct AttnBwdParams {
   unsigned long long timeout_ns;
 };
 
-// 32 bf16 values (columns 32 quarter .. 32 quarter + 31) of row r into a 128 x 128 K-major tile in the
-// 128-byte-swizzled layout: atom column quarter / 2, 16-byte chunks 4 (quarter % 2) .. + 3.
-__device__ __forceinline__ void store_quarter_row(uint8_t* buf, int quarter, int r, const float (&v)[32]) {
-  uint8_t* row = buf + (quarter >> 1) * kAtom + r * 128;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int chunk = 4 * (quarter & 1) + c;
-    const float* e = v + 8 * c;
-    *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) =
-        make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
-  }
-}
-
 // 32 columns of one TMEM row (this thread's lane) scaled by f, as bf16 into dst (64 bytes, 16-byte aligned).
 __device__ __forceinline__ void store_row32_scaled(__nv_bfloat16* dst, const float (&o)[32], float f) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -531,33 +529,40 @@ __device__ __forceinline__ void store_row32_scaled(__nv_bfloat16* dst, const flo
   }
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* a) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+// P, dS as bf16 pairs for a TMEM A operand: word i holds elements 2i (low half) and 2i + 1.
+__device__ __forceinline__ void pack_pairs(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
 }
 
-// dQ for one 128-query tile of one (batch, head): per key tile j, S_j = Q K_j^T and dP_j = dO V_j^T in
-// TMEM; the 16 compute warps (four per lane quadrant, 32 keys each) form P = exp2(S scale - lse) and
-// dS = P (dP - D) from the saved statistics (no reductions), write dS in bf16 to shared memory, and
-// dQ += dS K_j accumulates in TMEM (K as the MN-major operand); dQ / sqrt(hd) goes to dQKV.
+// TMEM column of K-step kk (16 elements) of a bf16 operand written over fp32 scores by quarter: quarter q's
+// 32 elements sit as 16 packed columns at 32 q.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint32_t>(32 * (kk >> 1) + 8 * (kk & 1)); }
+
+// dQ for one 128-query tile of one (batch, head): per key tile j, S_j = Q K_j^T into TMEM columns 0..127 and
+// dP_j = dO V_j^T into 128..255; the 16 compute warps (four per lane quadrant = query rows, 32 keys each)
+// release S and dP as soon as they hold them in registers (so S_{j+1}, dP_{j+1} run during their math),
+// form P = exp2(S scale - lse) and dS = P (dP - D), and write dS in bf16 into one of two TMEM buffers
+// (columns 384.. and 448..); dQ += dS_j K_j takes it from there as the A operand (K as the MN-major B),
+// accumulating in columns 256..383.  dQ / sqrt(hd) goes to dQKV.
 __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __grid_constant__ AttnBwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sdO = sQ + kTileBytes;
-  uint8_t* sK = sdO + kTileBytes;                  // 2 stages
-  uint8_t* sV = sK + kKvStages * kTileBytes;       // 2 stages
-  uint8_t* sdS = sV + kKvStages * kTileBytes;      // 1 buffer
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sdS + kTileBytes);
+  uint8_t* sK = sdO + kTileBytes;                  // kDqKStages stages: K_j is held until dQ_j is done
+  uint8_t* sV = sK + kDqKStages * kTileBytes;      // 2 stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kKvStages * kTileBytes);
   uint64_t* q_full = bars;                          // Q and dO
   uint64_t* k_full = q_full + 1;
-  uint64_t* k_empty = k_full + kKvStages;
-  uint64_t* v_full = k_empty + kKvStages;
+  uint64_t* k_empty = k_full + kDqKStages;
+  uint64_t* v_full = k_empty + kDqKStages;
   uint64_t* v_empty = v_full + kKvStages;
   uint64_t* s_full = v_empty + kKvStages;           // S_j and dP_j in TMEM
-  uint64_t* s_empty = s_full + 1;
-  uint64_t* ds_full = s_empty + 1;
-  uint64_t* dq_done = ds_full + 1;                  // dQ += dS K done (dS buffer free)
-  uint64_t* drain = dq_done + 1;
+  uint64_t* s_empty = s_full + 1;                   // both read by every compute warp
+  uint64_t* ds_full = s_empty + 1;                  // [buffer]: dS_j written
+  uint64_t* dq_done = ds_full + 2;                  // [buffer]: dQ += dS_j K_j done (buffer free)
+  uint64_t* drain = dq_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -569,16 +574,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
   const int nk = p.causal ? min(p.n_tiles, qt + 1) : p.n_tiles;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kKvStages; ++s) {
+    for (int s = 0; s < kDqKStages; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < kKvStages; ++s) {
       mbar_init(v_full + s, 1);
       mbar_init(v_empty + s, 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_empty, kBwdComputeWarps);
-    mbar_init(ds_full, kBwdComputeWarps);
-    mbar_init(dq_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(ds_full + x, kBwdComputeWarps);
+      mbar_init(dq_done + x, 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -591,7 +600,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem_base = *tmem_slot;  // S [0, 128), dP [128, 256), dQ [256, 384)
+  const uint32_t tmem_base = *tmem_slot;  // S [0, 128), dP [128, 256), dQ [256, 384), dS [384, 448), [448, 512)
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
 
   if (warp == 0) {
@@ -601,42 +610,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
       load_tile(sdO, &p.tmdO, q_full, h, b, qt * kQTile);
       uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
       for (int j = 0; j < nk; ++j) {
-        const int st = j % kKvStages;
-        const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
-        if (!wait_spin(v_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(v_full + st, kTileBytes);
-        load_tile(sV + st * kTileBytes, &p.tmV, v_full + st, h, b, j * kKTile);
-        v_issued |= 1u << st;
-        v_par = (v_par & ~(1u << st)) | (ph << st);
-        if (!wait_spin(k_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(k_full + st, kTileBytes);
-        load_tile(sK + st * kTileBytes, &p.tmK, k_full + st, h, b, j * kKTile);
-        k_issued |= 1u << st;
-        k_par = (k_par & ~(1u << st)) | (ph << st);
+        const int sk = j % kDqKStages, sv = j % kKvStages;
+        const uint32_t pk = static_cast<uint32_t>(j / kDqKStages) & 1u, pv = static_cast<uint32_t>(j / kKvStages) & 1u;
+        if (!wait_spin(k_empty + sk, pk ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(k_full + sk, kTileBytes);
+        load_tile(sK + sk * kTileBytes, &p.tmK, k_full + sk, h, b, j * kKTile);
+        k_issued |= 1u << sk;
+        k_par = (k_par & ~(1u << sk)) | (pk << sk);
+        if (!wait_spin(v_empty + sv, pv ^ 1u, wc, kSiteAttnKvEmpty)) break;
+        mbar_arrive_expect_tx(v_full + sv, kTileBytes);
+        load_tile(sV + sv * kTileBytes, &p.tmV, v_full + sv, h, b, j * kKTile);
+        v_issued |= 1u << sv;
+        v_par = (v_par & ~(1u << sv)) | (pv << sv);
       }
       wait_drain(q_full, 0, p.timeout_ns);
-      for (int s = 0; s < kKvStages; ++s) {
+      for (int s = 0; s < kDqKStages; ++s)
         if (k_issued & (1u << s)) wait_drain(k_full + s, (k_par >> s) & 1u, p.timeout_ns);
+      for (int s = 0; s < kKvStages; ++s)
         if (v_issued & (1u << s)) wait_drain(v_full + s, (v_par >> s) & 1u, p.timeout_ns);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_kk = idesc_bf16_f32(kQTile, kKTile, false, false);  // both K-major
       constexpr uint32_t idesc_mn = idesc_bf16_f32(kQTile, kHd, false, true);       // B MN-major
-      const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sdO), ds_base = smem_u32(sdS);
+      const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sdO);
       bool ok = wait_spin(q_full, 0, wc, kSiteAttnQ);
       if (ok) tc_fence_after_sync();
       // step j: S_j and dP_j (j < nk), then dQ += dS_{j-1} K_{j-1} (j >= 1)
       for (int j = 0; ok && j <= nk; ++j) {
         if (j < nk) {
-          const int st = j % kKvStages;
-          const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
+          const int sk = j % kDqKStages, sv = j % kKvStages;
           if (!wait_spin(s_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
-          if (!wait_spin(k_full + st, ph, wc, kSiteAttnKv)) break;
-          if (!wait_spin(v_full + st, ph, wc, kSiteAttnKv)) break;
+          if (!wait_spin(k_full + sk, static_cast<uint32_t>(j / kDqKStages) & 1u, wc, kSiteAttnKv)) break;
+          if (!wait_spin(v_full + sv, static_cast<uint32_t>(j / kKvStages) & 1u, wc, kSiteAttnKv)) break;
           tc_fence_after_sync();
-          const uint32_t k_base = smem_u32(sK + st * kTileBytes), v_base = smem_u32(sV + st * kTileBytes);
+          const uint32_t k_base = smem_u32(sK + sk * kTileBytes), v_base = smem_u32(sV + sv * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kHd / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
@@ -650,21 +658,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
                       idesc_kk, kk > 0 ? 1u : 0u);
           }
           umma_commit(s_full);
-          umma_commit(v_empty + st);
+          umma_commit(v_empty + sv);
         }
         if (j >= 1) {
           const int jj = j - 1;
-          const int st = jj % kKvStages;
-          if (!wait_spin(ds_full, static_cast<uint32_t>(jj) & 1u, wc, kSiteAttnP)) break;
+          const int st = jj % kDqKStages;
+          const int buf = jj & 1;
+          if (!wait_spin(ds_full + buf, static_cast<uint32_t>(jj >> 1) & 1u, wc, kSiteAttnP)) break;
           tc_fence_after_sync();
           const uint32_t k_base = smem_u32(sK + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kKTile / 16; ++kk) {
-            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base + 256, sdesc_sw128(ds_base + a_off, 16, 1024),
-                      sdesc_sw128(k_base + kk * 2048, kAtom, 1024), idesc_mn, (jj | kk) != 0 ? 1u : 0u);
-          }
-          umma_commit(dq_done);
+          for (int kk = 0; kk < kKTile / 16; ++kk)
+            umma_bf16_tmem_a(tmem_base + 256, tmem_base + 384 + 64 * buf + 8 * kk,
+                             sdesc_sw128(k_base + kk * 2048, kAtom, 1024), idesc_mn, (jj | kk) != 0 ? 1u : 0u);
+          umma_commit(dq_done + buf);
           umma_commit(k_empty + st);
         }
       }
@@ -709,22 +716,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) dp[i] = sc[i] * (dp[i] - dd);  // dS
-      // the dS buffer is free once the previous dQ MMA has read it
-      if (j >= 1) {
-        if (lane == 0) w_ok = wait_spin(dq_done, static_cast<uint32_t>(j - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      uint32_t w[16];
+      pack_pairs(dp, w);
+      const int buf = j & 1;
+      // the buffer is free once the dQ MMA of tile j - 2 has read it
+      if (j >= 2) {
+        if (lane == 0) w_ok = wait_spin(dq_done + buf, static_cast<uint32_t>((j - 2) >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
           ok = false;
           break;
         }
+        tc_fence_after_sync();
       }
-      store_quarter_row(sdS, quarter, r, dp);
-      fence_proxy_async_smem();
+      tmem_st16(lane_base + 384u + static_cast<uint32_t>(64 * buf + 16 * quarter), w);
+      tmem_wait_st();
+      tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(ds_full + buf);
     }
     if (ok && nk > 0) {
+      // the last dQ commit covers every earlier MMA
       int w_ok = 1;
-      if (lane == 0) w_ok = wait_spin(dq_done, static_cast<uint32_t>(nk - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      if (lane == 0)
+        w_ok = wait_spin(dq_done + ((nk - 1) & 1), static_cast<uint32_t>((nk - 1) >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
       if (__shfl_sync(0xffffffffu, w_ok, 0)) {
         tc_fence_after_sync();
         float o[32];
@@ -745,11 +759,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
   }
 }
 
-// dK and dV for one 128-key tile of one (batch, head): per query tile i, S^T_i = K Q_i^T and
-// dP^T_i = V dO_i^T in TMEM; the 16 compute warps (four per lane quadrant = key rows, 32 queries each) form
-// P^T = exp2(S^T scale - lse[q]) and dS^T = P^T (dP^T - D[q]), hand P^T to dV += P^T dO_i and then dS^T
-// (through the same shared buffer) to dK += dS^T Q_i; dO_i and Q_i are the MN-major operands.  Causal
-// attention visits query tiles i >= the key tile.
+// dK and dV for one 128-key tile of one (batch, head): per query tile i, S^T_i = K Q_i^T into TMEM columns
+// 0..127 and dP^T_i = V dO_i^T into 128..255; the 16 compute warps (four per lane quadrant = key rows, 32
+// queries each) form P^T = exp2(S^T scale - lse[q]) and dS^T = P^T (dP^T - D[q]) and write both in bf16
+// over their own score columns; dV += P^T dO_i and dK += dS^T Q_i take them from TMEM as the A operand (dO,
+// Q as the MN-major B), accumulating in columns 256..383 and 384..511.  The columns of S^T and dP^T take the
+// next tile's scores once both of those MMAs are done.  Causal attention visits query tiles i >= the key tile.
 __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __grid_constant__ AttnBwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -757,18 +772,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
   uint8_t* sV = sK + kTileBytes;
   uint8_t* sQ = sV + kTileBytes;                   // 2 stages
   uint8_t* sdO = sQ + kKvStages * kTileBytes;      // 2 stages
-  uint8_t* sPd = sdO + kKvStages * kTileBytes;     // P^T, then dS^T
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sPd + kTileBytes);
+  float* sStat = reinterpret_cast<float*>(sdO + kKvStages * kTileBytes);  // [stage][lse, D][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kKvStages * 2 * kQTile);
   uint64_t* kv_full = bars;
   uint64_t* q_full = kv_full + 1;                  // [stage]: Q_i and dO_i
   uint64_t* q_empty = q_full + kKvStages;
   uint64_t* s_full = q_empty + kKvStages;          // S^T_i and dP^T_i in TMEM
-  uint64_t* s_empty = s_full + 1;
-  uint64_t* p_full = s_empty + 1;
-  uint64_t* dv_done = p_full + 1;                  // dV += P^T dO_i done (buffer free for dS^T)
-  uint64_t* ds_full = dv_done + 1;
-  uint64_t* dk_done = ds_full + 1;                 // dK += dS^T Q_i done (buffer free for the next P^T)
-  uint64_t* drain = dk_done + 1;
+  uint64_t* p_full = s_full + 1;                   // P^T_i and dS^T_i written by every compute warp
+  uint64_t* pd_done = p_full + 1;                  // dV and dK MMAs of tile i done (score columns free)
+  uint64_t* drain = pd_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -786,11 +798,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
       mbar_init(q_empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_empty, kBwdComputeWarps);
     mbar_init(p_full, kBwdComputeWarps);
-    mbar_init(dv_done, 1);
-    mbar_init(ds_full, kBwdComputeWarps);
-    mbar_init(dk_done, 1);
+    mbar_init(pd_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -816,16 +825,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
         const int st = t % kKvStages;
         const uint32_t ph = static_cast<uint32_t>(t / kKvStages) & 1u;
         if (!wait_spin(q_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(q_full + st, 2 * kTileBytes);
+        mbar_arrive_expect_tx(q_full + st, 2 * kTileBytes + 2 * kQTile * 4);
         load_tile(sQ + st * kTileBytes, &p.tmQ, q_full + st, h, b, (i0 + t) * kQTile);
         load_tile(sdO + st * kTileBytes, &p.tmdO, q_full + st, h, b, (i0 + t) * kQTile);
-        // the tile's statistics (512 bytes each) into L1 ahead of the compute warps' loads
+        // the tile's statistics (512 bytes each, 16-byte aligned: rows of s_pad floats, tiles of 128)
         const long long st0 = (static_cast<long long>(b) * p.H + h) * p.s_pad + (i0 + t) * kQTile;
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-          prefetch_l1(p.lse + st0 + 32 * l);
-          prefetch_l1(p.delta + st0 + 32 * l);
-        }
+        bulk_load(sStat + st * 2 * kQTile, p.lse + st0, kQTile * 4, q_full + st);
+        bulk_load(sStat + st * 2 * kQTile + kQTile, p.delta + st0, kQTile * 4, q_full + st);
         issued |= 1u << st;
         par = (par & ~(1u << st)) | (ph << st);
       }
@@ -837,55 +843,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
     if (lane == 0) {
       constexpr uint32_t idesc_kk = idesc_bf16_f32(kKTile, kQTile, false, false);
       constexpr uint32_t idesc_mn = idesc_bf16_f32(kKTile, kHd, false, true);
-      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV), pd_base = smem_u32(sPd);
+      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
       bool ok = wait_spin(kv_full, 0, wc, kSiteAttnQ);
       if (ok) tc_fence_after_sync();
-      // step t: S^T_t and dP^T_t (t < nq), then dV and dK of tile t - 1 (t >= 1)
-      for (int t = 0; ok && t <= nq; ++t) {
-        if (t < nq) {
-          const int st = t % kKvStages;
-          if (!wait_spin(s_empty, (static_cast<uint32_t>(t) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
-          if (!wait_spin(q_full + st, static_cast<uint32_t>(t / kKvStages) & 1u, wc, kSiteAttnKv)) break;
-          tc_fence_after_sync();
-          const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
+      for (int t = 0; ok && t < nq; ++t) {
+        const int st = t % kKvStages;
+        if (!wait_spin(q_full + st, static_cast<uint32_t>(t / kKvStages) & 1u, wc, kSiteAttnKv)) break;
+        if (t >= 1 && !wait_spin(pd_done, static_cast<uint32_t>(t - 1) & 1u, wc, kSiteAttnSEmpty)) break;
+        tc_fence_after_sync();
+        const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kHd / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), idesc_kk,
-                      kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < kHd / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base + 128, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
-                      idesc_kk, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full);
+        for (int kk = 0; kk < kHd / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+          umma_bf16(tmem_base, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), idesc_kk,
+                    kk > 0 ? 1u : 0u);
         }
-        if (t >= 1) {
-          const int tt = t - 1;
-          const int st = tt % kKvStages;
-          const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
-          if (!wait_spin(p_full, static_cast<uint32_t>(tt) & 1u, wc, kSiteAttnP)) break;
-          tc_fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < kQTile / 16; ++kk) {
-            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base + 256, sdesc_sw128(pd_base + a_off, 16, 1024),
-                      sdesc_sw128(do_base + kk * 2048, kAtom, 1024), idesc_mn, (tt | kk) != 0 ? 1u : 0u);
-          }
-          umma_commit(dv_done);
-          if (!wait_spin(ds_full, static_cast<uint32_t>(tt) & 1u, wc, kSiteAttnP)) break;
-          tc_fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < kQTile / 16; ++kk) {
-            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base + 384, sdesc_sw128(pd_base + a_off, 16, 1024),
-                      sdesc_sw128(q_base + kk * 2048, kAtom, 1024), idesc_mn, (tt | kk) != 0 ? 1u : 0u);
-          }
-          umma_commit(dk_done);
-          umma_commit(q_empty + st);
+        for (int kk = 0; kk < kHd / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+          umma_bf16(tmem_base + 128, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
+                    idesc_kk, kk > 0 ? 1u : 0u);
         }
+        umma_commit(s_full);
+        if (!wait_spin(p_full, static_cast<uint32_t>(t) & 1u, wc, kSiteAttnP)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < kQTile / 16; ++kk)
+          umma_bf16_tmem_a(tmem_base + 256, tmem_base + packed_col(kk), sdesc_sw128(do_base + kk * 2048, kAtom, 1024),
+                           idesc_mn, (t | kk) != 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kQTile / 16; ++kk)
+          umma_bf16_tmem_a(tmem_base + 384, tmem_base + 128 + packed_col(kk),
+                           sdesc_sw128(q_base + kk * 2048, kAtom, 1024), idesc_mn, (t | kk) != 0 ? 1u : 0u);
+        umma_commit(pd_done);
+        umma_commit(q_empty + st);
       }
       umma_commit(drain);
       wait_drain(drain, 0, p.timeout_ns);
@@ -896,7 +887,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
     const int r = quad * 32 + static_cast<int>(lane);
     const int k = kt * kKTile + r;  // key position
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    const long long stat0 = (static_cast<long long>(b) * p.H + h) * p.s_pad;
     bool ok = true;
     for (int t = 0; t < nq; ++t) {
       const int q0 = (i0 + t) * kQTile + 32 * quarter;  // this warp's first query
@@ -911,17 +901,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
       tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(32 * quarter), sc);
       tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(32 * quarter), dp);
       tmem_wait_ld();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
-      const float4* l4 = reinterpret_cast<const float4*>(p.lse + stat0 + q0);
-      const float4* d4 = reinterpret_cast<const float4*>(p.delta + stat0 + q0);
+      // the statistics of this warp's 32 queries, staged with Q and dO (all lanes read the same words)
+      const float4* l4 = reinterpret_cast<const float4*>(sStat + (t % kKvStages) * 2 * kQTile + 32 * quarter);
+      const float4* d4 = l4 + kQTile / 4;
       // query q sees key k when q < S and (not causal or k <= q); only the diagonal and the ragged last
       // tile need the test (the condition is the same for the whole warp)
       if (q0 + 32 <= p.S && (!p.causal || q0 >= kt * kKTile + kKTile - 1)) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const float4 l = __ldg(l4 + g);
+          const float4 l = l4[g];
           sc[4 * g] = fmaf(sc[4 * g], p.scale_log2, -l.x);
           sc[4 * g + 1] = fmaf(sc[4 * g + 1], p.scale_log2, -l.y);
           sc[4 * g + 2] = fmaf(sc[4 * g + 2], p.scale_log2, -l.z);
@@ -931,7 +919,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
         for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const float4 dd = __ldg(d4 + g);
+          const float4 dd = d4[g];
           dp[4 * g] = sc[4 * g] * (dp[4 * g] - dd.x);
           dp[4 * g + 1] = sc[4 * g + 1] * (dp[4 * g + 1] - dd.y);
           dp[4 * g + 2] = sc[4 * g + 2] * (dp[4 * g + 2] - dd.z);
@@ -943,7 +931,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
         const int q_first = p.causal ? k : 0;  // visible: q_first <= q < q_end
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const float4 l = __ldg(l4 + g);
+          const float4 l = l4[g];
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -954,7 +942,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
         }
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          const float4 dd = __ldg(d4 + g);
+          const float4 dd = d4[g];
           const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -963,32 +951,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
           }
         }
       }
-      // P^T into the shared buffer once the previous tile's dK MMA has read the dS^T there
-      if (t >= 1) {
-        if (lane == 0) w_ok = wait_spin(dk_done, static_cast<uint32_t>(t - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-          ok = false;
-          break;
-        }
-      }
-      store_quarter_row(sPd, quarter, r, sc);
-      fence_proxy_async_smem();
+      // P^T and dS^T in bf16 over this quarter's own score columns
+      uint32_t w[16];
+      pack_pairs(sc, w);
+      tmem_st16(lane_base + static_cast<uint32_t>(32 * quarter), w);
+      pack_pairs(dp, w);
+      tmem_st16(lane_base + 128u + static_cast<uint32_t>(32 * quarter), w);
+      tmem_wait_st();
+      tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
-      // dS^T into the same buffer once dV has read P^T
-      if (lane == 0) w_ok = wait_spin(dv_done, static_cast<uint32_t>(t) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-        ok = false;
-        break;
-      }
-      store_quarter_row(sPd, quarter, r, dp);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
     }
     if (ok && nq > 0) {
       int w_ok = 1;
-      if (lane == 0) w_ok = wait_spin(dk_done, static_cast<uint32_t>(nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+      if (lane == 0) w_ok = wait_spin(pd_done, static_cast<uint32_t>(nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
       if (__shfl_sync(0xffffffffu, w_ok, 0)) {
         tc_fence_after_sync();
         __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<long long>(k) * p.B + b) * (3LL * p.H * kHd) +
@@ -1048,6 +1024,9 @@ bool make_part_map(CUtensorMap* m, const void* qkv, int part, int S, int B, int 
 }
 
 constexpr size_t kAttnSmem = 1024 + (3 + 2 * kKvStages) * kTileBytes + 256;
+// dQ: Q, dO, 3 K stages, 2 V stages; dK/dV: K, V, 2 Q and 2 dO stages and the staged statistics
+constexpr size_t kAttnDqSmem = 1024 + (2 + kDqKStages + kKvStages) * kTileBytes + 256;
+constexpr size_t kAttnDkdvSmem = 1024 + (2 + 2 * kKvStages) * kTileBytes + kKvStages * 2 * kQTile * 4 + 256;
 
 cudaError_t launch_attention(const void* qkv, int S, int B, int H, bool causal, void* out, const DeviceCtx& ctx,
                              cudaStream_t s, float* lse = nullptr) {
@@ -1110,15 +1089,15 @@ cudaError_t launch_attention_bwd(const void* qkv, const void* o, const void* dO,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_attention_bwd_dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kAttnSmem));
+                           static_cast<int>(kAttnDqSmem));
   if (e != cudaSuccess) return e;
-  k_attention_bwd_dq<<<static_cast<int>(grid), kBwdThreads, kAttnSmem, s>>>(p);
+  k_attention_bwd_dq<<<static_cast<int>(grid), kBwdThreads, kAttnDqSmem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_attention_bwd_dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kAttnSmem));
+                           static_cast<int>(kAttnDkdvSmem));
   if (e != cudaSuccess) return e;
-  k_attention_bwd_dkdv<<<static_cast<int>(grid), kBwdThreads, kAttnSmem, s>>>(p);
+  k_attention_bwd_dkdv<<<static_cast<int>(grid), kBwdThreads, kAttnDkdvSmem, s>>>(p);
   return cudaGetLastError();
 }
 
