@@ -1,25 +1,27 @@
-// Tensor-parallel attention: the per-head attention core on tcgen05, and the
-// block (QKV projection, attention, output projection with the shard sum).
+// Tensor-parallel attention: the per-head attention core on tcgen05, forward and
+// backward, and the block (QKV projection, attention, output projection with the
+// shard sum, and its backward).
 //
-// Attention core (one CTA per 128-query tile of one batch element and head,
-// head dim 128): softmax(Q K^T / sqrt(hd)) V with an online softmax over
-// 128-key tiles.
-//   warp 0   TMA producer: Q once, then K and V tiles into a 2-stage ring;
-//            Q, K, V come straight out of the QKV projection's [S, B, 3, H, hd]
-//            layout through 4-D tensor maps (two 64-element boxes per row).
+// Forward core (one CTA per 128-query tile of one batch element and head, head
+// dim 128): softmax(Q K^T / sqrt(hd)) V with an online softmax over 128-key tiles.
+//   warp 0   TMA producer: Q once, then K and V tiles into 3-stage rings; Q, K,
+//            V come straight out of the QKV projection's [S, B, 3, H, hd] layout
+//            through 4-D tensor maps (two 64-element boxes per row).
 //   warp 1   MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//            buffers, then O_tile = P_{j-1} V_{j-1} once the softmax warps have
-//            written P_{j-1}; V is the MN-major B operand.
-//   warps 2..5  softmax: thread t of the four owns query row t (TMEM lane t).
-//            Per key tile: pass 1 reads S from TMEM for the row maximum, the
-//            previous tile's P V is added into the fp32 row accumulator o[128]
-//            (rescaled by exp2(m_old - m_new)), pass 2 reads S again, writes
-//            P = exp2(S - m) in bf16 into shared memory in the 128-byte-
-//            swizzled K-major layout and sums it into the row's denominator.
-// Causal attention visits key tiles 0..i for query tile i and masks inside
-// the diagonal tile; keys at or past S are masked.  Every wait is bounded
-// (error word + abort flag), and the CTA drains its copies and MMAs before
-// it releases TMEM.
+//            buffers, then O += P_{j-1} V_{j-1} once the softmax warps have
+//            written P_{j-1}: P from TMEM as the A operand, V the MN-major B
+//            operand, O accumulating in TMEM.
+//   warps 2..9  softmax: two warps per TMEM lane quadrant (query rows) split
+//            each tile's keys; the row maximum is exchanged through shared
+//            memory, a reference maximum moves (rescaling O in TMEM) only when a
+//            tile's maximum exceeds it by 2^8, and P = exp2(S - m) goes to TMEM
+//            in bf16 pairs; the row's denominator and log-sum-exp come at the end.
+// Backward core: D = rowsum(dO O); a dQ kernel per query tile and a dK/dV kernel
+// per key tile recompute S and dP in TMEM and write P, dS in bf16 to TMEM for the
+// gradient MMAs (described at each kernel).  Causal attention masks inside the
+// tiles that reach past a row's last key; positions at or past S are masked.
+// Every wait is bounded (error word + abort flag), and each CTA drains its copies
+// and MMAs before it releases TMEM.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -39,6 +41,7 @@ constexpr int kHd = 128;            // head dimension this kernel is laid out fo
 constexpr int kQTile = 128;         // queries per CTA (one per TMEM lane)
 constexpr int kKTile = 128;         // keys per step
 constexpr int kKvStages = 2;
+constexpr int kFwdKvStages = 3;     // K and V rings of the forward (P lives in TMEM, not shared memory)
 constexpr int kAtom = 128 * 128;    // one 64-element-wide swizzled column of a 128-row tile: 16 KB
 constexpr int kTileBytes = 2 * kAtom;  // a 128 x 128 bf16 tile: two atom columns
 constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
@@ -164,16 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + kTileBytes;
-  uint8_t* sV = sK + kKvStages * kTileBytes;
-  uint8_t* sP = sV + kKvStages * kTileBytes;  // two P buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kTileBytes);
+  uint8_t* sV = sK + kFwdKvStages * kTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kFwdKvStages * kTileBytes);
   uint64_t* q_full = bars;
   // K and V have their own barriers: K_j is released as soon as S_j is done, V_j after P_j V_j
   uint64_t* k_full = q_full + 1;
-  uint64_t* k_empty = k_full + kKvStages;
-  uint64_t* v_full = k_empty + kKvStages;
-  uint64_t* v_empty = v_full + kKvStages;
-  uint64_t* s_full = v_empty + kKvStages;
+  uint64_t* k_empty = k_full + kFwdKvStages;
+  uint64_t* v_full = k_empty + kFwdKvStages;
+  uint64_t* v_empty = v_full + kFwdKvStages;
+  uint64_t* s_full = v_empty + kFwdKvStages;
   uint64_t* s_empty = s_full + 2;
   uint64_t* p_full = s_empty + 2;   // [P buffer]
   uint64_t* pv_done = p_full + 2;   // [P buffer]: P V of the tiles that used that buffer
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kKvStages; ++s) {
+    for (int s = 0; s < kFwdKvStages; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
       mbar_init(v_full + s, 1);
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_base = *tmem_slot;  // S [0, 128) and [128, 256), O [256, 384), P [384, 448) and [448, 512)
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
 
   if (warp == 0) {
@@ -226,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
       uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
       for (int j = 0; j < nk; ++j) {
-        const int st = j % kKvStages;
-        const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
+        const int st = j % kFwdKvStages;
+        const uint32_t ph = static_cast<uint32_t>(j / kFwdKvStages) & 1u;
         if (!wait_spin(k_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
         mbar_arrive_expect_tx(k_full + st, kTileBytes);
         load_tile(sK + st * kTileBytes, &p.tmK, k_full + st, h, b, j * kKTile);
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       }
       // copies in flight land before shared memory is released
       wait_drain(q_full, 0, p.timeout_ns);
-      for (int s = 0; s < kKvStages; ++s) {
+      for (int s = 0; s < kFwdKvStages; ++s) {
         if (k_issued & (1u << s)) wait_drain(k_full + s, (k_par >> s) & 1u, p.timeout_ns);
         if (v_issued & (1u << s)) wait_drain(v_full + s, (v_par >> s) & 1u, p.timeout_ns);
       }
@@ -260,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       for (int j = 0; ok && j <= nk; ++j) {
         if (j < nk) {
           const int sb = j & 1;
-          const int st = j % kKvStages;
+          const int st = j % kFwdKvStages;
           if (!wait_spin(s_empty + sb, (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
-          if (!wait_spin(k_full + st, static_cast<uint32_t>(j / kKvStages) & 1u, wc, kSiteAttnKv)) break;
+          if (!wait_spin(k_full + st, static_cast<uint32_t>(j / kFwdKvStages) & 1u, wc, kSiteAttnKv)) break;
           tc_fence_after_sync();
           const uint32_t k_base = smem_u32(sK + st * kTileBytes);
 #pragma unroll
@@ -277,18 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
         if (j >= 1) {
           const int jj = j - 1;
           const int pb = jj & 1;
-          const int st = jj % kKvStages;
+          const int st = jj % kFwdKvStages;
           if (!wait_spin(p_full + pb, static_cast<uint32_t>(jj >> 1) & 1u, wc, kSiteAttnP)) break;
-          if (!wait_spin(v_full + st, static_cast<uint32_t>(jj / kKvStages) & 1u, wc, kSiteAttnKv)) break;
+          if (!wait_spin(v_full + st, static_cast<uint32_t>(jj / kFwdKvStages) & 1u, wc, kSiteAttnKv)) break;
           tc_fence_after_sync();
-          const uint32_t p_base = smem_u32(sP + pb * kTileBytes);
           const uint32_t v_base = smem_u32(sV + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kKTile / 16; ++kk) {
-            const uint32_t a_off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(o_tmem, sdesc_sw128(p_base + a_off, 16, 1024), sdesc_sw128(v_base + kk * 2048, kAtom, 1024),
-                      idesc_pv, (jj | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kKTile / 16; ++kk)
+            umma_bf16_tmem_a(o_tmem, tmem_base + 384 + 64 * pb + 8 * kk, sdesc_sw128(v_base + kk * 2048, kAtom, 1024),
+                             idesc_pv, (jj | kk) != 0 ? 1u : 0u);
           umma_commit(pv_done + pb);
           umma_commit(v_empty + st);
         }
@@ -397,24 +396,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
           continue;
         }
       }
-      uint8_t* pbuf = sP + pb * kTileBytes + half * kAtom;
+      // P_j in bf16 pairs into TMEM buffer j % 2 (this half's 64 keys: 32 columns), the A operand of P V
       float psum = 0.f;
+      uint32_t pw[32];
 #pragma unroll
-      for (int chunk = 0; chunk < 8; ++chunk) {  // 8 keys per 16-byte chunk
-        float e[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          e[i] = ex2_approx(fmaf(sc[chunk >> 2][8 * (chunk & 3) + i], p.scale_log2, -m_use));
-          psum += e[i];
-        }
-        uint8_t* dst = pbuf + r * 128 + ((chunk ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                                                    pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+      for (int i = 0; i < 32; ++i) {
+        const float e0 = ex2_approx(fmaf(sc[i >> 4][2 * (i & 15)], p.scale_log2, -m_use));
+        const float e1 = ex2_approx(fmaf(sc[i >> 4][2 * (i & 15) + 1], p.scale_log2, -m_use));
+        psum += e0 + e1;
+        pw[i] = pack_bf16x2(e0, e1);
       }
       l += psum;
-      // P_j (and any rescaled O) handed to the MMA: shared-memory writes visible to the async proxy
+      tmem_st32(lane_base + 384u + static_cast<uint32_t>(64 * pb + 32 * half), pw);
+      // P_j (and any rescaled O) handed to the MMA
+      tmem_wait_st();
       tc_fence_before_sync();
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + pb);
     }
@@ -1023,7 +1019,7 @@ bool make_part_map(CUtensorMap* m, const void* qkv, int part, int S, int B, int 
   return make_head_map(m, static_cast<const __nv_bfloat16*>(qkv) + part * d, 3 * d, S, B, H);
 }
 
-constexpr size_t kAttnSmem = 1024 + (3 + 2 * kKvStages) * kTileBytes + 256;
+constexpr size_t kAttnSmem = 1024 + (1 + 2 * kFwdKvStages) * kTileBytes + 256;
 // dQ: Q, dO, 3 K stages, 2 V stages; dK/dV: K, V, 2 Q and 2 dO stages and the staged statistics
 constexpr size_t kAttnDqSmem = 1024 + (2 + kDqKStages + kKvStages) * kTileBytes + 256;
 constexpr size_t kAttnDkdvSmem = 1024 + (2 + 2 * kKvStages) * kTileBytes + kKvStages * 2 * kQTile * 4 + 256;
