@@ -228,3 +228,34 @@ def test_attention_tp_backward_block(S, B, H, N, causal):
     for name, buf in (("dX", dX), ("dWqkv", dWqkv), ("dbqkv", dbqkv), ("dWo", dWo), ("dbo", dbo)):
         assert_bf16_close(name, f64(buf.t), ref[name])
         assert buf.intact(), name
+
+
+# ----------------------------------------------------------------------------- the bench's attention shape
+
+def test_attention_core_forward_backward_bench_shape():
+    """S = 4096 positions x B = 2 sequences, 32 heads of 128, causal (the attention row's shape): the whole
+    core forward and backward run, and two (batch, head) pairs (the first head of batch 0 and the last of
+    batch 1, so both corners of the grid) are checked in full against the oracle."""
+    S, B, H = 4096, 2, 32
+    d = H * HD
+    w = inputs.small_workload(64, 64, 2, name="attn_bench_shape")
+    qkv = inputs.draw(w, "QKV", shape=(S * B, 3 * d), dist=(0.0, 1.0))
+    dO = inputs.draw(w, "dO", shape=(S * B, d), dist=(0.0, 1.0))
+    QKV = dev(qkv[0])
+    O = torch.empty(S * B, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(binding.attention_lse_shape(S, B, H), dtype=torch.float32, device="cuda")
+    binding.tpmlp_attention_core(QKV, S, B, H, O, causal=True, LSE=lse)
+    dQKV = torch.empty(S * B, 3 * d, dtype=torch.bfloat16, device="cuda")
+    binding.tpmlp_attention_core_backward(QKV, O, dev(dO[0]), lse, S, B, H, dQKV, causal=True)
+    torch.cuda.synchronize()
+    Og, dQKVg = f64(O), f64(dQKV)
+    for b, h in ((0, 0), (1, H - 1)):
+        rows = slice(b, S * B, B)
+        c = [slice(part * d + h * HD, part * d + (h + 1) * HD) for part in range(3)]
+        q, k, v = (qkv[1][rows, cc] for cc in c)
+        ref_o = oracle.attention_head(q, k, v, True)
+        assert_bf16_close(f"O (b={b}, h={h})", Og[rows, h * HD:(h + 1) * HD], ref_o)
+        dq, dk, dv = oracle.attention_head_backward(q, k, v, dO[1][rows, h * HD:(h + 1) * HD], True)
+        for name, got, ref in (("dQ", dQKVg[rows, c[0]], dq), ("dK", dQKVg[rows, c[1]], dk),
+                               ("dV", dQKVg[rows, c[2]], dv)):
+            assert_bf16_close(f"{name} (b={b}, h={h})", got, ref)
