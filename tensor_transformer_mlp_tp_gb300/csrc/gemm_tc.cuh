@@ -190,10 +190,14 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       if (p.out1 != nullptr)
         store_row32(static_cast<__nv_bfloat16*>(p.out1) + static_cast<long long>(row) * p.ld1, col0, p.N, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = gelu_f(v[i]);
-        if (col0 + i < p.N) st.amax = fmaxf(st.amax, fabsf(v[i]));
+      for (int i = 0; i < 32; i += 2) {
+        const float2 y = gelu2(make_float2(v[i], v[i + 1]));
+        v[i] = y.x;
+        v[i + 1] = y.y;
       }
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < p.N) st.amax = fmaxf(st.amax, fabsf(v[i]));
       store_row32_fp8<0>(static_cast<uint8_t*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v,
                          st.scale_out);
     }
@@ -208,7 +212,11 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       if constexpr (EPI == kEpiBiasGelu) {
         if (p.out1 != nullptr) store_row32(static_cast<__nv_bfloat16*>(p.out1) + row * p.ld1, col0, p.N, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+        for (int i = 0; i < 32; i += 2) {
+          const float2 y = gelu2(make_float2(v[i], v[i + 1]));
+          v[i] = y.x;
+          v[i + 1] = y.y;
+        }
       }
       store_row32(static_cast<__nv_bfloat16*>(p.out0) + row * p.ld0, col0, p.N, v);
     }
@@ -229,12 +237,15 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
     float h[32];
     unpack_row32(aux_raw, h);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float x = h[i];
-      const NormalCdfPdf n = normal_cdf_pdf(x);
-      v[i] = row_ok && col0 + i < p.N ? v[i] * (n.cdf + x * n.pdf) : 0.f;
-      st.amax = fmaxf(st.amax, fabsf(v[i]));
+    for (int i = 0; i < 32; i += 2) {
+      const float2 x = make_float2(h[i], h[i + 1]);
+      const NormalCdfPdf2 n = normal_cdf_pdf2(x);
+      const float2 d = __fmul2_rn(make_float2(v[i], v[i + 1]), __ffma2_rn(x, n.pdf, n.cdf));  // dH GeLU'(h)
+      v[i] = row_ok && col0 + i < p.N ? d.x : 0.f;
+      v[i + 1] = row_ok && col0 + i + 1 < p.N ? d.y : 0.f;
     }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) st.amax = fmaxf(st.amax, fabsf(v[i]));
     if (row_ok)
       store_row32_fp8<1>(static_cast<uint8_t*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v,
                          st.scale_out);
@@ -253,11 +264,15 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
     const bool want_h = p.out1 != nullptr;
     float g[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float x = h[i];
-      const NormalCdfPdf n = normal_cdf_pdf(x);
-      g[i] = x * n.cdf;
-      v[i] = row_ok ? v[i] * (n.cdf + x * n.pdf) : 0.f;
+    for (int i = 0; i < 32; i += 2) {
+      const float2 x = make_float2(h[i], h[i + 1]);
+      const NormalCdfPdf2 n = normal_cdf_pdf2(x);
+      const float2 gg = __fmul2_rn(x, n.cdf);                                                  // H = h Phi(h)
+      const float2 d = __fmul2_rn(make_float2(v[i], v[i + 1]), __ffma2_rn(x, n.pdf, n.cdf));  // dH GeLU'(h)
+      g[i] = gg.x;
+      g[i + 1] = gg.y;
+      v[i] = row_ok ? d.x : 0.f;
+      v[i + 1] = row_ok ? d.y : 0.f;
     }
     if (row_ok) {
       store_row32(static_cast<__nv_bfloat16*>(p.out0) + static_cast<long long>(row) * p.ld0, col0, p.N, v);

@@ -278,9 +278,12 @@ struct NormalCdfPdf {
   float cdf, pdf;
 };
 
+// Abramowitz & Stegun eq. 7.1.26: erf(z) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+// t = 1 / (1 + p z), |error| <= 1.5e-7.
+constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
+                kA4 = -1.453152027f, kA5 = 1.061405429f;
+
 __device__ __forceinline__ NormalCdfPdf normal_cdf_pdf(float x) {
-  constexpr float kP = 0.3275911f, kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
-                  kA4 = -1.453152027f, kA5 = 1.061405429f;
   const float e = __expf(-0.5f * x * x);                               // exp(-z^2)
   const float t = __fdividef(1.0f, fmaf(kP * 0.70710678118654752f, fabsf(x), 1.0f));
   const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kA5, kA4), kA3), kA2), kA1);
@@ -289,6 +292,29 @@ __device__ __forceinline__ NormalCdfPdf normal_cdf_pdf(float x) {
 }
 
 __device__ __forceinline__ float gelu_f(float x) { return x * normal_cdf_pdf(x).cdf; }
+
+// Phi and phi of two values at once, the same formula as normal_cdf_pdf: the polynomial and the products on
+// float pairs (the packed fp32 instructions), the exponential and the reciprocal per element.
+struct NormalCdfPdf2 {
+  float2 cdf, pdf;
+};
+__device__ __forceinline__ NormalCdfPdf2 normal_cdf_pdf2(float2 x) {
+  constexpr float kP2 = kP * 0.70710678118654752f;
+  const float2 m = __fmul2_rn(__fmul2_rn(make_float2(-0.5f, -0.5f), x), x);
+  const float2 e = make_float2(__expf(m.x), __expf(m.y));  // exp(-z^2)
+  const float2 den = __ffma2_rn(make_float2(kP2, kP2), make_float2(fabsf(x.x), fabsf(x.y)), make_float2(1.f, 1.f));
+  const float2 t = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
+  float2 poly = __ffma2_rn(t, make_float2(kA5, kA5), make_float2(kA4, kA4));
+  poly = __ffma2_rn(t, poly, make_float2(kA3, kA3));
+  poly = __ffma2_rn(t, poly, make_float2(kA2, kA2));
+  poly = __ffma2_rn(t, poly, make_float2(kA1, kA1));
+  poly = __fmul2_rn(t, poly);
+  const float2 tail = __fmul2_rn(__fmul2_rn(make_float2(0.5f, 0.5f), poly), e);  // Phi(-|x|)
+  return {make_float2(x.x >= 0.f ? 1.0f - tail.x : tail.x, x.y >= 0.f ? 1.0f - tail.y : tail.y),
+          __fmul2_rn(make_float2(0.39894228040143268f, 0.39894228040143268f), e)};
+}
+
+__device__ __forceinline__ float2 gelu2(float2 x) { return __fmul2_rn(x, normal_cdf_pdf2(x).cdf); }
 
 __device__ __forceinline__ float gelu_prime_f(float x) {
   const NormalCdfPdf n = normal_cdf_pdf(x);
