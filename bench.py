@@ -600,7 +600,7 @@ def run_other_rows(step, torch, binding, pk, only=None):
                                           "frac": round(rs_bytes / (ms_rs * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
                                           "bytes_per_launch": rs_bytes}
         del P, Yc
-    if (want("rmsnorm_gather") or want("layernorm_gather_isolated")) and w.sp:
+    if (want("rmsnorm_gather") or want("layernorm_gather_isolated")) and w.sp and w.backward:
         # the RMS norm variant of the gathered norm, and the LayerNorm beside it timed the same way; the calls
         # alternate between (X -> Xg) and (dY -> dXg) so each reads 2 T d bytes the previous call did not touch
         # (256 MB of inputs and outputs in all, about twice the L2)
@@ -716,6 +716,7 @@ def run_ours(args, w):
         raise RuntimeError(f"device status after warm-up: {binding.status_string(st)} (site {site})")
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -723,11 +724,20 @@ def run_ours(args, w):
         time.sleep(0.3)
         t0 = time.perf_counter()
         e0 = time.time()
+        # the timed steps: kernels back to back (an event between two kernels would keep the second from
+        # overlapping its launch with the first's tail)
+        t_start.record()
         for k in range(args.steps):
-            step.run(events[k])
+            step.run()
+        t_end.record()
         torch.cuda.synchronize()
         e1 = time.time()
         wall = time.perf_counter() - t0
+        time.sleep(1.0)  # the clocks recover from the timed steps' load before the breakdown
+        # the per-kernel breakdown: the same number of steps with an event between consecutive kernels
+        for k in range(args.steps):
+            step.run(events[k])
+        torch.cuda.synchronize()
         time.sleep(0.15)
     if dist is not None:
         dist.barrier()
@@ -735,7 +745,7 @@ def run_ours(args, w):
     for k in range(args.steps):
         for i in range(nseg):
             seg_ms[i] += events[k][i].elapsed_time(events[k][i + 1])
-    total_ms = max_over_ranks(events[0][0].elapsed_time(events[-1][nseg]), dist)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist)
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after timing: {binding.status_string(st)} (site {site})")

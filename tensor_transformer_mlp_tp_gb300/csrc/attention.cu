@@ -148,14 +148,6 @@ __device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, const 
   }
 }
 
-// 2^x with the hardware's approximate base-2 exponential (flushes subnormal results to zero); the
-// softmax exponents here are <= 8 and underflow to 0 harmlessly.
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Rows s0 .. s0 + 127 of one part (Q, K or V) of head h, batch b: two boxes of 64 elements.
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int h, int b, int s0) {
   tma_load_4d(dst, map, bar, 0, h, b, s0);

@@ -54,6 +54,9 @@ struct ConstChunkPtrs {
 struct GemmParams {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  CUtensorMap tmC0;         // out0 / out1 as [M x N] bf16, 32 x 32 boxes, 64-byte swizzle (tma_out bits 0 / 1)
+  CUtensorMap tmC1;
+  int tma_out;              // bit 0: out0 rows leave through TMA box stores, bit 1: out1 too
   int M, N, K;
   int m_blocks, n_blocks;
   int k_blocks_per_shard;   // k-blocks summed into one accumulator

@@ -18,6 +18,11 @@ constexpr int kEpiWarps = 4;
 constexpr int kBN = 256;
 constexpr int kGroupM = 16;      // raster group, in 128-row blocks
 constexpr int kShortK = 2048;    // at or below: the GeLU epilogue runs balanced over all four sub-partitions
+// Balanced epilogues (every epilogue warp reads TMEM and does its own math): 10 warps for the bf16 GeLU
+// GEMM with a short K and for the row-parallel GEMM's store (measured on GB300, d = 1024: 10 and 14
+// warps equal, 6 warps 10% slower), 6 for the FP8 quantising epilogues (10 and 14 measured slower).
+constexpr int kBalWarps = 10;
+constexpr int kBalFp8 = 6;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -36,7 +41,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D tensor map over a row-major matrix of `outer` rows of `inner` elements
 // (`ld` elements apart; bf16, or bytes for E4M3), 128-byte swizzle, zero fill out of bounds.
 bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer, long long ld, int box_inner,
-              int box_outer, bool bytes = false) {
+              int box_outer, bool bytes = false, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
@@ -45,7 +50,7 @@ bool make_map(CUtensorMap* m, const void* base, long long inner, long long outer
   cuuint32_t estr[2] = {1, 1};
   return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
             dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -80,31 +85,36 @@ int max_pairs(K kern, int smem, int threads, int dev_cache_slot, int* cache) {
   return n;
 }
 
-template <bool AMN, bool BMN, int EPI, bool FP8 = false, bool BAL = false>
+template <int BN, bool AMN, bool BMN, int EPI, bool FP8 = false, int BAL = 0>
 cudaError_t run_pair(const GemmParams& p, cudaStream_t s) {
-  using S = PairShape<kBN, kPairStages, kEpiWarps>;
-  auto kern = k_gemm_tc2<kBN, AMN, BMN, EPI, kPairStages, kEpiWarps, FP8, BAL>;
+  using S = PairShape<BN, kPairStages, kEpiWarps, BAL>;
+  auto kern = k_gemm_tc2<BN, AMN, BMN, EPI, kPairStages, kEpiWarps, FP8, BAL>;
+  constexpr int kThreads = S::kThreads;
   static int cache[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
   if (e != cudaSuccess) return e;
-  const int pairs = max_pairs(kern, S::kSmem, S::kThreads, dev & 63, cache);
+  const int pairs = max_pairs(kern, S::kSmem, kThreads, dev & 63, cache);
   const long long tiles = static_cast<long long>(p.m_blocks) * p.n_blocks * p.shards;
   const int grid_pairs = static_cast<int>(tiles < pairs ? tiles : pairs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * grid_pairs);
-  cfg.blockDim = dim3(S::kThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = S::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel's set-up overlaps the previous kernel's tail (it waits for
+  // that kernel's completion before touching global memory)
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -166,9 +176,9 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   p.err = ctx.err;
   p.timeout_ns = ctx.timeout_ns;
   switch (g.epi) {
-    case kEpiBiasGeluQ: return run_pair<false, false, kEpiBiasGeluQ, true, true>(p, s);
-    case kEpiDGeluQ: return run_pair<false, false, kEpiDGeluQ, true, true>(p, s);
-    case kEpiStore: return run_pair<false, false, kEpiStore, true>(p, s);
+    case kEpiBiasGeluQ: return run_pair<kBN, false, false, kEpiBiasGeluQ, true, kBalFp8>(p, s);
+    case kEpiDGeluQ: return run_pair<kBN, false, false, kEpiDGeluQ, true, kBalFp8>(p, s);
+    case kEpiStore: return run_pair<kBN, false, false, kEpiStore, true>(p, s);
     default: return cudaErrorNotSupported;
   }
 }
@@ -218,6 +228,17 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
   p.res_chunks = g.tail.residual;
   p.err = ctx.err;
   p.timeout_ns = ctx.timeout_ns;
+  // bf16 outputs of the pair kernel leave through TMA box stores where a tensor map can describe them (a
+  // 16-byte aligned base and row pitch): out0 of the bias (+ GeLU) epilogues and of the plain store, and
+  // the pre-activation out1
+  p.tma_out = 0;
+  if (pair && g.out0 != nullptr &&
+      (g.epi == kEpiBiasGelu || g.epi == kEpiBias || (g.epi == kEpiStore && g.rows_per_chunk <= 0 && p.shards == 1))) {
+    constexpr CUtensorMapSwizzle kSw = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (make_map(&p.tmC0, g.out0, g.N, g.M, g.ld0, 32, 32, false, kSw)) p.tma_out = 1;
+    if (p.tma_out && g.epi == kEpiBiasGelu && g.out1 != nullptr)
+      p.tma_out = make_map(&p.tmC1, g.out1, g.N, g.M, g.ld1, 32, 32, false, kSw) ? 3 : 0;
+  }
   const long long tiles = static_cast<long long>(p.m_blocks) * p.n_blocks * p.shards;
   const int grid = static_cast<int>(tiles < ctx.sm_count ? tiles : ctx.sm_count);
 
@@ -226,19 +247,20 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
     switch (g.epi) {
       case kEpiBiasGelu:
         // with a short K the bias + GeLU epilogue outlasts a tile's MMAs: spread it over all sub-partitions
-        if (!amn && bmn && g.K <= kShortK) return run_pair<false, true, kEpiBiasGelu, false, true>(p, s);
-        if (!amn && bmn) return run_pair<false, true, kEpiBiasGelu>(p, s);
+        if (!amn && bmn && g.K <= kShortK) return run_pair<kBN, false, true, kEpiBiasGelu, false, kBalWarps>(p, s);
+        if (!amn && bmn) return run_pair<kBN, false, true, kEpiBiasGelu>(p, s);
         break;
       case kEpiBias:
-        if (!amn && bmn) return run_pair<false, true, kEpiBias>(p, s);
+        if (!amn && bmn) return run_pair<kBN, false, true, kEpiBias>(p, s);
         break;
       case kEpiStore:
-        if (!amn && bmn) return run_pair<false, true, kEpiStore>(p, s);
-        if (amn && bmn) return run_pair<true, true, kEpiStore>(p, s);
-        if (!amn && !bmn) return run_pair<false, false, kEpiStore>(p, s);
+        // the row-parallel GEMM: few, long tiles, so the last tile's epilogue is exposed
+        if (!amn && bmn) return run_pair<kBN, false, true, kEpiStore, false, kBalWarps>(p, s);
+        if (amn && bmn) return run_pair<kBN, true, true, kEpiStore>(p, s);
+        if (!amn && !bmn) return run_pair<kBN, false, false, kEpiStore>(p, s);
         break;
       case kEpiDGelu:
-        if (!amn && !bmn) return run_pair<false, false, kEpiDGelu>(p, s);
+        if (!amn && !bmn) return run_pair<kBN, false, false, kEpiDGelu>(p, s);
         break;
       default:
         break;

@@ -171,9 +171,38 @@ __device__ __forceinline__ void sp_tail_32(const GemmParams& p, float (&v)[32], 
   }
 }
 
+// The warp's 32 rows x 32 columns (row `lane` in lane `lane`) leave through one TMA box store from `buf`
+// (2 KB, 1024-byte aligned): bf16 row `lane` at buf + 64 lane, its 16-byte piece j at piece
+// j ^ ((lane >> 1) & 3) -- the tensor map's 64-byte swizzle, which also keeps each quarter warp's
+// shared-memory writes on distinct banks.  Rows at or beyond M and columns at or beyond N are clipped by
+// the copy.  The previous box store from `buf` must have finished reading it first.
+__device__ __forceinline__ void box_store_bf16_32(const CUtensorMap* map, uint8_t* buf, const float (&x)[32],
+                                                  uint32_t lane, int col0, int row0, int M, int N) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  uint8_t* r = buf + lane * 64;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 u;
+    u.x = pack_bf16x2(x[8 * j + 0], x[8 * j + 1]);
+    u.y = pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
+    u.z = pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
+    u.w = pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
+    *reinterpret_cast<uint4*>(r + ((j ^ ((lane >> 1) & 3)) << 4)) = u;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < M && col0 < N) {
+    tma_store_2d(map, buf, col0, row0);
+    bulk_commit_group();
+  }
+}
+
+// `sbuf` != nullptr: the bf16 outputs that p.tma_out marks leave through box_store_bf16_32.
 template <int EPI>
 __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32], const uint4 (&aux_raw)[4], int row,
-                                            int col0, int shard, int mb, int quad, uint32_t lane, EpiState& st) {
+                                            int col0, int shard, int mb, int quad, uint32_t lane, EpiState& st,
+                                            uint8_t* sbuf = nullptr) {
   const bool row_ok = row < p.M;
   if (st.descale != 1.f) {
 #pragma unroll
@@ -208,7 +237,19 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] += b[i];
     }
-    if (row_ok) {
+    if (sbuf != nullptr && (p.tma_out & 1)) {
+      const int row0 = row - static_cast<int>(lane);
+      if constexpr (EPI == kEpiBiasGelu) {
+        if (p.tma_out & 2) box_store_bf16_32(&p.tmC1, sbuf, v, lane, col0, row0, p.M, p.N);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 y = gelu2(make_float2(v[i], v[i + 1]));
+          v[i] = y.x;
+          v[i + 1] = y.y;
+        }
+      }
+      box_store_bf16_32(&p.tmC0, sbuf, v, lane, col0, row0, p.M, p.N);
+    } else if (row_ok) {
       if constexpr (EPI == kEpiBiasGelu) {
         if (p.out1 != nullptr) store_row32(static_cast<__nv_bfloat16*>(p.out1) + row * p.ld1, col0, p.N, v);
 #pragma unroll
@@ -221,7 +262,9 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       store_row32(static_cast<__nv_bfloat16*>(p.out0) + row * p.ld0, col0, p.N, v);
     }
   } else if constexpr (EPI == kEpiStore) {
-    if (row_ok) {
+    if (sbuf != nullptr && (p.tma_out & 1)) {
+      box_store_bf16_32(&p.tmC0, sbuf, v, lane, col0, row - static_cast<int>(lane), p.M, p.N);
+    } else if (row_ok) {
       __nv_bfloat16* dst;
       if (p.rows_per_chunk > 0) {
         if (p.tail) sp_tail_32(p, v, row, col0);

@@ -33,7 +33,7 @@
 
 namespace tpmlp {
 
-template <int BN, int STAGES, int EPI_WARPS>
+template <int BN, int STAGES, int EPI_WARPS, int BAL = 0>
 struct PairShape {
   static_assert(BN == 128 || BN == 256, "BN");
   static constexpr int kHalfN = BN / 2;
@@ -41,34 +41,43 @@ struct PairShape {
   static constexpr int kBTile = kHalfN * kBK * 2;  // this CTA's half of the B columns
   static constexpr int kStage = kATile + kBTile;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kThreads = 64 + 32 * EPI_WARPS + 64;     // + two helper warps
-  static constexpr int kStaging = 2 * 2 * 32 * 32 * 4;            // [quadrant 0/1][buffer][32 rows][32 fp32]
-  static constexpr int kSmem = 1024 + STAGES * kStage + kStaging + 256;
+  static constexpr int kThreads = BAL > 0 ? 64 + 32 * BAL : 64 + 32 * EPI_WARPS + 64;  // + two helper warps
+  // reader -> helper staging [quadrant 0/1][buffer][32 rows][32 fp32] (BAL = 0 only)
+  static constexpr int kStaging = BAL > 0 ? 0 : 2 * 2 * 32 * 32 * 4;
+  // one 2 KB TMA box-store buffer per warp that stores: the BAL epilogue warps, or warps 2, 3, 6, 7
+  static constexpr int kStoreWarps = BAL > 0 ? BAL : 4;
+  static constexpr int kStoreBuf = 32 * 32 * 2;
+  static constexpr int kSmem = 1024 + STAGES * kStage + kStaging + kStoreWarps * kStoreBuf + 256;
   static_assert(EPI_WARPS == 4, "one epilogue warp per TMEM lane quadrant");
+  static_assert(kSmem <= 232448, "shared memory per block");
 };
 
 // FP8: E4M3 A and B (both K-major), .kind::f8f6f4; a 128-byte k-block row then holds 128 elements and
 // one UMMA covers 32 of them, so shared-memory layouts, descriptors and byte counts are those of bf16.
-// BAL: every epilogue warp reads TMEM itself and the epilogue math is spread over all four SM
-// sub-partitions (for epilogue-bound launches: short K or the FP8 rate); otherwise the two warps on the
-// TMA and MMA sub-partitions only copy TMEM to shared memory for the helper warps.
-template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS, bool FP8 = false, bool BAL = false>
-__global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __grid_constant__ GemmParams p) {
+// BAL > 0: BAL epilogue warps (warps 2 .. BAL + 1), each reading TMEM itself, with the epilogue math
+// spread evenly over all four SM sub-partitions (for epilogue-bound launches: short K or the FP8 rate);
+// BAL = 0: the two warps on the TMA and MMA sub-partitions only copy TMEM to shared memory for the
+// two helper warps.
+template <int BN, bool A_MN, bool B_MN, int EPI, int STAGES, int EPI_WARPS, bool FP8 = false, int BAL = 0>
+__global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS, 1)
+    k_gemm_tc2(const __grid_constant__ GemmParams p) {
   static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
   static_assert(FP8 || (EPI != kEpiBiasGeluQ && EPI != kEpiDGeluQ), "the quantising epilogues follow FP8 operands");
   constexpr bool kAux = EPI == kEpiDGelu || EPI == kEpiDGeluQ;  // reads the pre-activation tile
   // FP8 GEMMs with a GeLU / GeLU' epilogue are epilogue-bound at the doubled MMA rate: there every epilogue
   // warp reads TMEM itself and the math is spread over all four SM sub-partitions (see the epilogue).
-  constexpr bool kBalanced = BAL;
-  constexpr int kTemptyArrivals = 2 * (kBalanced ? EPI_WARPS + 2 : EPI_WARPS);
+  static_assert(BAL == 0 || (BAL >= 4 && BAL <= 14), "balanced epilogue: 4 to 14 warps");
+  constexpr bool kBalanced = BAL > 0;
+  constexpr int kTemptyArrivals = 2 * (kBalanced ? BAL : EPI_WARPS);
   constexpr int kKElems = FP8 ? 128 : kBK;  // elements of one 128-byte k-block row
-  using S = PairShape<BN, STAGES, EPI_WARPS>;
+  using S = PairShape<BN, STAGES, EPI_WARPS, BAL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * S::kATile;
   float* staging = reinterpret_cast<float*>(sB + STAGES * S::kBTile);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(staging) + S::kStaging);
+  uint8_t* store_bufs = reinterpret_cast<uint8_t*>(staging) + S::kStaging;  // 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(store_bufs + S::kStoreWarps * S::kStoreBuf);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -104,6 +113,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
+    if (p.tma_out & 1) tma_prefetch_desc(&p.tmC0);
+    if (p.tma_out & 2) tma_prefetch_desc(&p.tmC1);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, S::kTmemCols);
@@ -114,6 +125,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
   cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or copy
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // The set-up above touches no global memory; with a programmatic launch it overlaps the previous
+  // kernel's tail.  Every global read and write below comes after that kernel has completed.  The next
+  // kernel may launch now: its blocks take an SM as this kernel's blocks leave.
+  griddep_wait();
+  griddep_launch_dependents();
 
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int num_tiles = p.m_blocks * p.n_blocks * p.shards;  // m_blocks counts 256-row pair tiles
@@ -223,13 +239,17 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
     }
   } else if constexpr (kBalanced) {
     // -------------------------------------------------------------------- epilogue, balanced (both CTAs)
-    // Warps 2..5 own TMEM lane quadrants 2, 3, 0, 1; warps 6 and 7 (lane quadrants 2 and 3 as well) take
-    // the upper half of the columns of quadrants 2 and 3.  Sub-partition w % 4 then runs one quadrant's
-    // worth of math: warp 4 (next to the TMA producer) and warp 5 (next to the MMA issuer) all columns of
-    // theirs, warps 2 + 6 and 3 + 7 half each.
+    // Warp w may read only TMEM lane quadrant w % 4, so the warps of one quadrant (w, w + 4, ...) split
+    // its BN / 32 column chunks between them; sub-partition w % 4 then runs exactly one quadrant's worth
+    // of math whatever BAL is.  With BAL = 6: warp 4 (next to the TMA producer) and warp 5 (next to the
+    // MMA issuer) take all columns of theirs, warps 2 + 6 and 3 + 7 half each.
     const int quad = warp & 3;
-    const int c_begin = warp >= 6 ? BN / 2 : 0;
-    const int c_end = (warp == 2 || warp == 3) ? BN / 2 : BN;
+    const int first = quad >= 2 ? quad : quad + 4;  // lowest epilogue warp of this quadrant
+    const int n_quad = (BAL + 2 - first + 3) / 4;    // epilogue warps of this quadrant
+    const int i_quad = (warp - first) / 4;
+    const int c_begin = 32 * (i_quad * (BN / 32) / n_quad);
+    const int c_end = 32 * ((i_quad + 1) * (BN / 32) / n_quad);
+    uint8_t* sbuf = store_bufs + (warp - 2) * S::kStoreBuf;
     EpiState est{1.f, 1.f, 0.f};
     if constexpr (FP8) est.descale = 1.f / (__ldg(p.scale_a) * __ldg(p.scale_b));
     if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) est.scale_out = __ldg(p.scale_out);
@@ -271,12 +291,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
         }
         float v[32];
         tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
-        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est);
+        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est, sbuf);
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
     }
+    if (lane == 0) bulk_wait_all();  // box stores complete before the block's shared memory is released
     if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) {
       if (p.amax_out != nullptr) amax_combine_warp(p.amax_out, est.amax);
     }
@@ -287,6 +308,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
     const bool reader = quad_warp && quad < 2;             // copies TMEM -> staging only
     const bool helper = !quad_warp;                        // epilogue math on staged rows
     float* stage_base = staging + quad * (2 * 32 * 32);    // valid for quadrants 0 and 1
+    uint8_t* obuf = reader ? nullptr : store_bufs + (warp >= 6 ? warp - 4 : warp - 2) * S::kStoreBuf;
     EpiState est{1.f, 1.f, 0.f};
     if constexpr (FP8) est.descale = 1.f / (__ldg(p.scale_a) * __ldg(p.scale_b));
     if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) est.scale_out = __ldg(p.scale_out);
@@ -374,7 +396,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
         } else {
           tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
         }
-        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est);
+        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est, obuf);
       }
       if (!helper && ok_all) {
         tc_fence_before_sync();
@@ -382,6 +404,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1) k_gemm_tc2(const __gr
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0));
       }
     }
+    if (lane == 0 && !reader) bulk_wait_all();  // box stores complete before shared memory is released
     if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) {
       if (p.amax_out != nullptr) amax_combine_warp(p.amax_out, est.amax);
     }

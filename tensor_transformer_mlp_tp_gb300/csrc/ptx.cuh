@@ -117,6 +117,27 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: the next kernel of the stream (launched with programmatic stream
+// serialisation) may begin launching; wait until the previous kernel has completed and its memory
+// operations are visible (a no-op for a kernel launched without the attribute).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 2-D tiled store shared -> global, tracked as a bulk group of the issuing thread.  c0 is the innermost
+// coordinate (a multiple of 16 bytes), c1 >= 0; elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the thread's committed bulk stores have finished reading shared memory / have completed
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // 2-D tiled load global -> shared; completion is signalled as transaction
 // bytes on `bar`.  c0 is the innermost coordinate (its byte offset must be a
 // multiple of 16, which the host guarantees by requiring 8-element multiples).
@@ -293,28 +314,57 @@ __device__ __forceinline__ NormalCdfPdf normal_cdf_pdf(float x) {
 
 __device__ __forceinline__ float gelu_f(float x) { return x * normal_cdf_pdf(x).cdf; }
 
-// Phi and phi of two values at once, the same formula as normal_cdf_pdf: the polynomial and the products on
-// float pairs (the packed fp32 instructions), the exponential and the reciprocal per element.
+// 2^x and 1/x with the hardware's approximate instructions (subnormal results flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The pair forms below follow the same eq. 7.1.26 with the 1/2 of Phi(-|x|) = (1 - erf(|x| / sqrt 2)) / 2
+// folded into the coefficients: Phi(-|x|) = t (a1/2 + t (a2/2 + ...)) exp(-x^2 / 2), t = 1 / (1 + p |x| / sqrt 2),
+// exp(-x^2 / 2) = 2^(-x^2 log2(e) / 2).  Polynomial and products on float pairs (the packed fp32
+// instructions), the exponential and the reciprocal per element.
+constexpr float kP2 = kP * 0.70710678118654752f;
+constexpr float kNegHalfLog2e = -0.72134752044448170f;  // -log2(e) / 2
+constexpr float kInvSqrt2Pi = 0.39894228040143268f;
+
+// Phi(-|x|) and exp(-x^2 / 2) of two values; `nax` = -|x|.
+__device__ __forceinline__ void normal_tail2(float2 x, float2 nax, float2& tail, float2& e) {
+  const float2 den = __ffma2_rn(make_float2(-kP2, -kP2), nax, make_float2(1.f, 1.f));
+  const float2 t = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+  const float2 m = __fmul2_rn(__fmul2_rn(make_float2(kNegHalfLog2e, kNegHalfLog2e), x), x);
+  e = make_float2(ex2_approx(m.x), ex2_approx(m.y));
+  float2 poly = __ffma2_rn(t, make_float2(0.5f * kA5, 0.5f * kA5), make_float2(0.5f * kA4, 0.5f * kA4));
+  poly = __ffma2_rn(t, poly, make_float2(0.5f * kA3, 0.5f * kA3));
+  poly = __ffma2_rn(t, poly, make_float2(0.5f * kA2, 0.5f * kA2));
+  poly = __ffma2_rn(t, poly, make_float2(0.5f * kA1, 0.5f * kA1));
+  tail = __fmul2_rn(__fmul2_rn(t, poly), e);
+}
+
 struct NormalCdfPdf2 {
   float2 cdf, pdf;
 };
 __device__ __forceinline__ NormalCdfPdf2 normal_cdf_pdf2(float2 x) {
-  constexpr float kP2 = kP * 0.70710678118654752f;
-  const float2 m = __fmul2_rn(__fmul2_rn(make_float2(-0.5f, -0.5f), x), x);
-  const float2 e = make_float2(__expf(m.x), __expf(m.y));  // exp(-z^2)
-  const float2 den = __ffma2_rn(make_float2(kP2, kP2), make_float2(fabsf(x.x), fabsf(x.y)), make_float2(1.f, 1.f));
-  const float2 t = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
-  float2 poly = __ffma2_rn(t, make_float2(kA5, kA5), make_float2(kA4, kA4));
-  poly = __ffma2_rn(t, poly, make_float2(kA3, kA3));
-  poly = __ffma2_rn(t, poly, make_float2(kA2, kA2));
-  poly = __ffma2_rn(t, poly, make_float2(kA1, kA1));
-  poly = __fmul2_rn(t, poly);
-  const float2 tail = __fmul2_rn(__fmul2_rn(make_float2(0.5f, 0.5f), poly), e);  // Phi(-|x|)
+  float2 tail, e;
+  normal_tail2(x, make_float2(-fabsf(x.x), -fabsf(x.y)), tail, e);
   return {make_float2(x.x >= 0.f ? 1.0f - tail.x : tail.x, x.y >= 0.f ? 1.0f - tail.y : tail.y),
-          __fmul2_rn(make_float2(0.39894228040143268f, 0.39894228040143268f), e)};
+          __fmul2_rn(make_float2(kInvSqrt2Pi, kInvSqrt2Pi), e)};
 }
 
-__device__ __forceinline__ float2 gelu2(float2 x) { return __fmul2_rn(x, normal_cdf_pdf2(x).cdf); }
+// GeLU of two values: x Phi(x) = max(x, 0) - |x| Phi(-|x|) (for x < 0, Phi(x) = Phi(-|x|); for x >= 0,
+// x Phi(x) = x - x Phi(-x)), one fused multiply-add after the tail instead of a select and a product.
+__device__ __forceinline__ float2 gelu2(float2 x) {
+  const float2 nax = make_float2(-fabsf(x.x), -fabsf(x.y));
+  float2 tail, e;
+  normal_tail2(x, nax, tail, e);
+  return __ffma2_rn(nax, tail, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+}
 
 __device__ __forceinline__ float gelu_prime_f(float x) {
   const NormalCdfPdf n = normal_cdf_pdf(x);
