@@ -612,6 +612,16 @@ def run_other_rows(step, torch, binding, pk, only=None):
             ms = time_calls(torch, pair, 20) / 2.0
             out[name] = {"ms": round(ms, 4), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
                          "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes_per_launch": nb}
+        # the same bytes moved by a plain device copy (torch), timed the same way: what a launch of this size
+        # reaches, beside the bandwidth peak measured on a 4 GB copy
+        src_a, src_b = torch.empty_like(step.Xg), torch.empty_like(step.dXg)
+        src_a.zero_(), src_b.zero_()
+        ms_c = time_calls(torch, lambda: (step.Xg.copy_(src_a), step.dXg.copy_(src_b)), 20) / 2.0
+        out["copy_same_bytes"] = {"ms": round(ms_c, 4), "GB/s": round(nb / (ms_c * 1e-3) / 1e9, 1),
+                                  "frac": round(nb / (ms_c * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes_per_launch": nb,
+                                  "what": "torch copy_ of one [T x d] bf16 tensor into another, alternating two "
+                                          "pairs as the norm rows do"}
+        del src_a, src_b
     if (want("gemm2_bias_dropout_add") or want("dropout_backward")) and w.sp:
         # the rest of the sequence-parallel region on the step's shapes: the row-parallel GEMM with row bias,
         # dropout (p = 0.1) and residual in its chunked store, and the dropout backward (+ row-bias gradient)
