@@ -348,6 +348,15 @@ class Step:
         return sum(n for _, n, _, _ in self.kernels())
 
 
+def e2e_what(w):
+    calls = ("tpmlp_sp_forward" if w.sp else "tpmlp_forward") + (" + tpmlp_sp_backward" if w.backward else "")
+    io = ("X, dY", "Y, dX") if w.backward else ("X", "Y")
+    return (f"block calls ({calls}) with {io[0]} copied from pinned host memory and {io[1]} copied back every step "
+            "inside the timed region; inputs go up one step ahead on one copy stream and outputs come back on "
+            "another, overlapping the kernels (X, dY and Y double-buffered on the device); weights"
+            + (" and their gradients" if w.backward else "") + " stay in HBM")
+
+
 def run_e2e(step, args, torch, binding):
     """The same step through the block calls, with each step's activations copied from pinned host memory and
     its outputs copied back inside the timed region.  Inputs go up on one copy stream into a double buffer, one
@@ -366,6 +375,10 @@ def run_e2e(step, args, torch, binding):
         d2h += dX_h.numel() * 2
     Xd = [torch.empty_like(step.X) for _ in range(2)]
     dYd = [torch.empty_like(step.dY) for _ in range(2)] if w.backward else None
+    # Y double-buffered too: without a backward between them, a forward would otherwise wait for the
+    # previous step's Y to reach the host
+    Yd = [step.Y, torch.empty_like(step.Y)]
+    Ycd = [list(y.split(step.rows)) for y in Yd] if w.sp else None
     shape = binding.make_shape(w.T, w.d, w.F, N)
     ws_f = binding.workspace(shape, binding.OP_SP_FWD if w.sp else binding.OP_FWD)
     ws_b = binding.workspace(shape, binding.OP_SP_BWD) if w.backward else None
@@ -374,8 +387,8 @@ def run_e2e(step, args, torch, binding):
     ev = lambda: torch.cuda.Event()
     used = [ev(), ev()]          # buffer b free again (its step's last kernel done)
     in_x, in_dy = [ev(), ev()], [ev(), ev()]  # buffer b holds its step's inputs
-    y_out, dx_out = ev(), ev()   # Y / dX copied to the host (their device buffers may be overwritten)
-    for e in used + in_x + in_dy + [y_out, dx_out]:
+    y_out, dx_out = [ev(), ev()], ev()  # Y (buffer b) / dX copied to the host (may be overwritten)
+    for e in used + in_x + in_dy + y_out + [dx_out]:
         e.record(comp)
 
     def inputs_up(k):
@@ -393,19 +406,19 @@ def run_e2e(step, args, torch, binding):
         if not last:
             inputs_up(k + 1)
         comp.wait_event(in_x[b])
-        comp.wait_event(y_out)
+        comp.wait_event(y_out[b])
         if w.sp:
             binding.tpmlp_sp_forward(list(Xd[b].split(step.rows)), step.gamma, step.beta, step.A, step.B, N,
-                                     step.Yc, bias=step.bias, Hpre_out=step.Hpre if w.backward else None,
+                                     Ycd[b], bias=step.bias, Hpre_out=step.Hpre if w.backward else None,
                                      H_out=step.H if w.backward else None, ws=ws_f)
         else:
-            binding.tpmlp_forward(Xd[b], step.A, step.B, step.bias, N, step.Y, ws=ws_f)
+            binding.tpmlp_forward(Xd[b], step.A, step.B, step.bias, N, Yd[b], ws=ws_f)
         fwd_done = ev()
         fwd_done.record(comp)
         down.wait_event(fwd_done)
         with torch.cuda.stream(down):
-            Y_h.copy_(step.Y, non_blocking=True)
-            y_out.record(down)
+            Y_h.copy_(Yd[b], non_blocking=True)
+            y_out[b].record(down)
         if w.backward:
             comp.wait_event(in_dy[b])
             comp.wait_event(dx_out)
@@ -431,7 +444,8 @@ def run_e2e(step, args, torch, binding):
     e0.record(comp)
     up.wait_event(e0)
     run(args.steps)
-    comp.wait_event(y_out)
+    comp.wait_event(y_out[0])
+    comp.wait_event(y_out[1])
     comp.wait_event(dx_out)
     e1.record(comp)
     torch.cuda.synchronize()
@@ -820,10 +834,7 @@ def run_ours(args, w):
         "e2e": {"value": round(whole_job_rate(flops, args.steps, world, e2e_ms * args.steps) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "what": "block calls (tpmlp_sp_forward/backward) with X, dY copied from pinned host memory and Y, dX "
-                        "copied back every step inside the timed region; inputs go up one step ahead on one copy "
-                        "stream into a double buffer, outputs come back on another, both overlapping the kernels; "
-                        "weights and their gradients stay in HBM"}
+                "what": e2e_what(w)}
                if args.only_row is None else {"skipped": "--only-row " + args.only_row},
         "other_rows": other,
         "gpu_launches": step.launches_per_step() * args.steps,
