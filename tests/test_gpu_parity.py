@@ -69,6 +69,27 @@ def test_gemm2_shard_accum(T, d, N):
     assert Y.intact()
 
 
+@pytest.mark.parametrize("T,d,F,N", [(600, 128, 4096, 8), (1000, 320, 2560, 4), (2050, 256, 8192, 8)])
+def test_gemm2_long_k_few_tiles(T, d, F, N):
+    """Long K (40 to 128 k-blocks, the shards' rows walked into one accumulator) against few output tiles,
+    ragged in T; two launches back to back (the second one's set-up overlaps the first one's tail)."""
+    w = inputs.small_workload(T, d, N, F=F)
+    Hb, _ = inputs.draw(w, "X", shape=(T, F), dist=(0.0, 0.5))
+    B = inputs.draw(w, "B")
+    Hv = inputs.bf16_bits_to_f64(Hb).reshape(T, F)
+    Hd, Bd = dev(Hb), dev(B[0])
+    Ys = [Guarded((T, d)) for _ in range(2)]
+    for Y in Ys:
+        binding.tpmlp_gemm2_shard_accum(Hd, Bd, N, Y=Y.t)
+    torch.cuda.synchronize()
+    ref = oracle.all_reduce([oracle.row_parallel_partial(Hv[:, lo:hi], B[1][lo:hi])
+                             for lo, hi in oracle.shard_ranges(F, N)])
+    for Y in Ys:
+        assert_bf16_close("Y", f64(Y.t), ref)
+        assert Y.intact()
+    assert torch.equal(Ys[0].t, Ys[1].t)
+
+
 def _int_matrix(rng, shape):
     return inputs.f32_to_bf16_bits(rng.integers(-1, 2, shape).astype(np.float32)).reshape(shape)
 
