@@ -56,12 +56,17 @@ struct GemmParams {
   CUtensorMap tmB;
   CUtensorMap tmC0;         // out0 / out1 as [M x N] bf16, 32 x 32 boxes, 64-byte swizzle (tma_out bits 0 / 1)
   CUtensorMap tmC1;
+  CUtensorMap tmB_half;     // K-major B with boxes of a quarter tile's columns (half tiles of the pair kernel)
   int tma_out;              // bit 0: out0 rows leave through TMA box stores, bit 1: out1 too
   int M, N, K;
   int m_blocks, n_blocks;
   int k_blocks_per_shard;   // k-blocks summed into one accumulator
   int shards;               // >1: per-shard partial outputs (tile space x shards, K split evenly)
   int group_m;              // raster: tiles walk group_m row blocks before the next column block
+  // CTA-pair kernel: tiles from full_units on are each split into two half-width tiles (the two halves of
+  // its columns), so that a last wave of fewer than half the pairs' tiles runs as one round of halves.
+  // Work unit u < full_units is tile u; unit full_units + 2 j + h is half h of tile full_units + j.
+  int full_units;
   void* out0;
   long long ld0;
   void* out1;

@@ -85,8 +85,16 @@ int max_pairs(K kern, int smem, int threads, int dev_cache_slot, int* cache) {
   return n;
 }
 
+// The K-major B map of half tiles was made (the launchers leave it all zero otherwise).
+bool half_map_ok(const GemmParams& p) {
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&p.tmB_half);
+  for (size_t i = 0; i < sizeof(p.tmB_half); ++i)
+    if (b[i] != 0) return true;
+  return false;
+}
+
 template <int BN, bool AMN, bool BMN, int EPI, bool FP8 = false, int BAL = 0>
-cudaError_t run_pair(const GemmParams& p, cudaStream_t s) {
+cudaError_t run_pair(GemmParams p, cudaStream_t s) {
   using S = PairShape<BN, kPairStages, kEpiWarps, BAL>;
   auto kern = k_gemm_tc2<BN, AMN, BMN, EPI, kPairStages, kEpiWarps, FP8, BAL>;
   constexpr int kThreads = S::kThreads;
@@ -98,7 +106,16 @@ cudaError_t run_pair(const GemmParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int pairs = max_pairs(kern, S::kSmem, kThreads, dev & 63, cache);
   const long long tiles = static_cast<long long>(p.m_blocks) * p.n_blocks * p.shards;
-  const int grid_pairs = static_cast<int>(tiles < pairs ? tiles : pairs);
+  long long units = tiles;
+  p.full_units = static_cast<int>(tiles);
+  // A last wave of whole tiles that would leave more than half of the pairs idle runs as one round of
+  // half-width tiles instead (each pair then finishes its share in half a tile's time).
+  const long long rem = tiles % pairs;
+  if (BN == kBN && p.shards == 1 && rem != 0 && 2 * rem <= pairs && (BMN || half_map_ok(p))) {
+    p.full_units = static_cast<int>(tiles - rem);
+    units = tiles + rem;
+  }
+  const int grid_pairs = static_cast<int>(units < pairs ? units : pairs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * grid_pairs);
   cfg.blockDim = dim3(kThreads);
@@ -141,6 +158,7 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   bool ok = make_map(&p.tmA, g.a.ptr, g.K, g.M, g.a.ld, kKb, kBM, true) &&
             make_map(&p.tmB, g.b.ptr, g.K, g.N, g.b.ld, kKb, kBN / 2, true);
   if (!ok) return cudaErrorInvalidValue;
+  if (!make_map(&p.tmB_half, g.b.ptr, g.K, g.N, g.b.ld, kKb, kBN / 4, true)) memset(&p.tmB_half, 0, sizeof(p.tmB_half));
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
@@ -197,6 +215,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t 
   ok = ok && (g.b.mn_major ? make_map(&p.tmB, g.b.ptr, g.N, g.K, g.b.ld, 64, kBK)
                            : make_map(&p.tmB, g.b.ptr, g.K, g.N, g.b.ld, kBK, b_rows));
   if (!ok) return cudaErrorInvalidValue;
+  // K-major B of half-width pair tiles: a quarter tile's columns per CTA
+  if (pair && !g.b.mn_major && !make_map(&p.tmB_half, g.b.ptr, g.K, g.N, g.b.ld, kBK, kBN / 4))
+    memset(&p.tmB_half, 0, sizeof(p.tmB_half));
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;

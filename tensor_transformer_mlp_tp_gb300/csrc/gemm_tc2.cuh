@@ -52,6 +52,22 @@ struct PairShape {
   static_assert(kSmem <= 232448, "shared memory per block");
 };
 
+// Work unit u of the pair kernel (see GemmParams::full_units): its tile, the tile's first output column
+// relative to the tile (0, or BN / 2 for the upper half) and its width (BN, or BN / 2 for a half).
+template <int BN>
+__device__ __forceinline__ void unit_of(const GemmParams& p, int u, int& tile, int& col_off, int& width) {
+  if (u < p.full_units) {
+    tile = u;
+    col_off = 0;
+    width = BN;
+  } else {
+    const int j = u - p.full_units;
+    tile = p.full_units + (j >> 1);
+    col_off = (j & 1) * (BN / 2);
+    width = BN / 2;
+  }
+}
+
 // FP8: E4M3 A and B (both K-major), .kind::f8f6f4; a 128-byte k-block row then holds 128 elements and
 // one UMMA covers 32 of them, so shared-memory layouts, descriptors and byte counts are those of bf16.
 // BAL > 0: BAL epilogue warps (warps 2 .. BAL + 1), each reading TMEM itself, with the epilogue math
@@ -113,6 +129,7 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
+    if (!B_MN && p.full_units < p.m_blocks * p.n_blocks * p.shards) tma_prefetch_desc(&p.tmB_half);
     if (p.tma_out & 1) tma_prefetch_desc(&p.tmC0);
     if (p.tma_out & 2) tma_prefetch_desc(&p.tmC1);
   }
@@ -133,6 +150,7 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
 
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int num_tiles = p.m_blocks * p.n_blocks * p.shards;  // m_blocks counts 256-row pair tiles
+  const int num_units = p.full_units + 2 * (num_tiles - p.full_units);
   const int cluster_id = blockIdx.x >> 1;
   const int num_clusters = gridDim.x >> 1;
 
@@ -145,18 +163,21 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
-      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters) {
+      for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+        int tile, col_off, width;
+        unit_of<BN>(p, u, tile, col_off, width);
         int shard, mb, nb;
         tile_coords(p, tile, shard, mb, nb);
         const int kb0 = shard * p.k_blocks_per_shard;
         const int m0 = mb * 256 + static_cast<int>(rank) * 128;
-        const int n0 = nb * BN + static_cast<int>(rank) * S::kHalfN;
+        const int n0 = nb * BN + col_off + static_cast<int>(rank) * (width / 2);  // this CTA's half of the columns
+        const uint32_t stage_bytes = static_cast<uint32_t>(S::kATile + (width / 2) * kBK * 2);
         for (int kb = 0; kb < p.k_blocks_per_shard; ++kb) {
           if (!wait_bounded(empty + stage, phase ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(full + stage, 2 * S::kStage);
+          if (leader) mbar_arrive_expect_tx(full + stage, 2 * stage_bytes);
           const uint32_t bar = mapa_shared(smem_u32(full + stage), 0);
           const int k0 = (kb0 + kb) * kKElems;
           uint8_t* a_dst = sA + stage * S::kATile;
@@ -168,10 +189,9 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
             for (int j = 0; j < 2; ++j) tma_load_2d_pair(a_dst + j * 64 * kBK * 2, &p.tmA, bar, m0 + 64 * j, k0, pol_a);
           }
           if constexpr (!B_MN) {
-            tma_load_2d_pair(b_dst, &p.tmB, bar, k0, n0, pol_b);
+            tma_load_2d_pair(b_dst, width == BN ? &p.tmB : &p.tmB_half, bar, k0, n0, pol_b);
           } else {
-#pragma unroll
-            for (int j = 0; j < S::kHalfN / 64; ++j)
+            for (int j = 0; j < width / 128; ++j)  // 64-column boxes
               tma_load_2d_pair(b_dst + j * 64 * kBK * 2, &p.tmB, bar, n0 + 64 * j, k0, pol_b);
           }
           issued |= 1u << stage;
@@ -192,14 +212,18 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------------ MMA issuer (even CTA)
-      const uint32_t idesc = FP8 ? idesc_f8_f32(256, BN, static_cast<uint32_t>(p.a_fmt),
-                                                static_cast<uint32_t>(p.b_fmt), false, false)
-                                 : idesc_bf16_f32(256, BN, A_MN, B_MN);
+      const uint32_t idesc_full = FP8 ? idesc_f8_f32(256, BN, static_cast<uint32_t>(p.a_fmt),
+                                                     static_cast<uint32_t>(p.b_fmt), false, false)
+                                      : idesc_bf16_f32(256, BN, A_MN, B_MN);
+      const uint32_t idesc_half = FP8 ? idesc_f8_f32(256, BN / 2, static_cast<uint32_t>(p.a_fmt),
+                                                     static_cast<uint32_t>(p.b_fmt), false, false)
+                                      : idesc_bf16_f32(256, BN / 2, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = cluster_id; ok && tile < num_tiles; tile += num_clusters, ++local) {
+      for (int u = cluster_id; ok && u < num_units; u += num_clusters, ++local) {
+        const uint32_t idesc = u < p.full_units ? idesc_full : idesc_half;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!wait_bounded(tempty + acc, acc_phase ^ 1u, wc, kSiteMmaTmemEmpty)) break;
@@ -254,9 +278,13 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
     if constexpr (FP8) est.descale = 1.f / (__ldg(p.scale_a) * __ldg(p.scale_b));
     if constexpr (EPI == kEpiBiasGeluQ || EPI == kEpiDGeluQ) est.scale_out = __ldg(p.scale_out);
     int local = 0;
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+    for (int u = cluster_id; u < num_units; u += num_clusters, ++local) {
+      int tile, col_off, width;
+      unit_of<BN>(p, u, tile, col_off, width);
       int shard, mb, nb;
       tile_coords(p, tile, shard, mb, nb);
+      const int n_base = nb * BN + col_off;     // the unit's first output column
+      const int c_stop = min(c_end, width);     // this warp's chunks within the unit
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const int mb128 = mb * 2 + static_cast<int>(rank);
@@ -265,8 +293,8 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
       uint4 aux_next[4] = {};
       if constexpr (kAux) {
         // pull this warp's rows and columns of the pre-activation tile into L2 while the tile's MMAs run
-        const int pcol = nb * BN + c_begin;
-        const int ncols = min(c_end - c_begin, p.N - pcol);
+        const int pcol = n_base + c_begin;
+        const int ncols = min(c_stop - c_begin, p.N - pcol);
         if (row < p.M && ncols > 0)
           prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row) * p.ld_aux + pcol,
                            static_cast<uint32_t>(ncols) * 2u);
@@ -279,19 +307,19 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
       const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       if constexpr (kAux) {
         aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
-        load_raw32(aux_row, nb * BN + c_begin, p.N, row < p.M, aux_next);
+        if (c_begin < c_stop) load_raw32(aux_row, n_base + c_begin, p.N, row < p.M, aux_next);
       }
 #pragma unroll 1
-      for (int c = c_begin; c < c_end; c += 32) {
+      for (int c = c_begin; c < c_stop; c += 32) {
         uint4 aux_cur[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) aux_cur[g] = aux_next[g];
         if constexpr (kAux) {
-          if (c + 32 < c_end) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
+          if (c + 32 < c_stop) load_raw32(aux_row, n_base + c + 32, p.N, row < p.M, aux_next);
         }
         float v[32];
         tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
-        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est, sbuf);
+        epilogue_32<EPI>(p, v, aux_cur, row, n_base + c, shard, mb128, quad, lane, est, sbuf);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -315,9 +343,12 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
     uint32_t chunk_ctr = 0;
     int local = 0;
     bool ok_all = true;
-    for (int tile = cluster_id; ok_all && tile < num_tiles; tile += num_clusters, ++local) {
+    for (int u = cluster_id; ok_all && u < num_units; u += num_clusters, ++local) {
+      int tile, col_off, width;
+      unit_of<BN>(p, u, tile, col_off, width);
       int shard, mb, nb;
       tile_coords(p, tile, shard, mb, nb);
+      const int n_base = nb * BN + col_off;     // the unit's first output column
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const int mb128 = mb * 2 + static_cast<int>(rank);
@@ -325,8 +356,8 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
       if constexpr (kAux) {
         // While this tile's MMAs run, pull the warp's 32 rows of the pre-activation tile into L2.
         if (!reader && row < p.M) {
-          const int pcol = nb * BN;
-          const int ncols = min(BN, p.N - pcol);
+          const int pcol = n_base;
+          const int ncols = min(width, p.N - pcol);
           prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row) * p.ld_aux + pcol,
                            static_cast<uint32_t>(ncols) * 2u);
         }
@@ -344,11 +375,11 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
       if constexpr (kAux) {
         if (!reader) {
           aux_row = static_cast<const __nv_bfloat16*>(p.aux) + static_cast<long long>(row < p.M ? row : 0) * p.ld_aux;
-          load_raw32(aux_row, nb * BN, p.N, row < p.M, aux_next);
+          load_raw32(aux_row, n_base, p.N, row < p.M, aux_next);
         }
       }
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32, ++chunk_ctr) {
+      for (int c = 0; c < width; c += 32, ++chunk_ctr) {
         const uint32_t buf = chunk_ctr & 1u, par = (chunk_ctr >> 1) & 1u;
         float* sbuf = stage_base + buf * (32 * 32) + lane * 32;
         float v[32];
@@ -373,7 +404,7 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
 #pragma unroll
         for (int g = 0; g < 4; ++g) aux_cur[g] = aux_next[g];
         if constexpr (kAux) {
-          if (c + 32 < BN) load_raw32(aux_row, nb * BN + c + 32, p.N, row < p.M, aux_next);
+          if (c + 32 < width) load_raw32(aux_row, n_base + c + 32, p.N, row < p.M, aux_next);
         }
         if (helper) {
           int ok = 1;
@@ -396,7 +427,7 @@ __global__ void __launch_bounds__(BAL > 0 ? 64 + 32 * BAL : 128 + 32 * EPI_WARPS
         } else {
           tmem_load_32cols(trow + static_cast<uint32_t>(c), v);
         }
-        epilogue_32<EPI>(p, v, aux_cur, row, nb * BN + c, shard, mb128, quad, lane, est, obuf);
+        epilogue_32<EPI>(p, v, aux_cur, row, n_base + c, shard, mb128, quad, lane, est, obuf);
       }
       if (!helper && ok_all) {
         tc_fence_before_sync();
