@@ -27,6 +27,12 @@
 // single-CTA kernel; the pair meets at a cluster barrier before TMEM is
 // released and before either CTA exits (the even CTA's MMAs read the odd
 // CTA's shared memory).
+// bf16 outputs that a tensor map describes leave as 32 x 32 TMA box stores
+// from a 2 KB shared-memory buffer per storing warp.  A last wave of at most
+// half the pairs' tiles runs as one round of half-width tiles (unit_of).  The
+// kernel is launched with programmatic stream serialisation: its set-up
+// overlaps the previous kernel's tail, and griddepcontrol.wait precedes its
+// first global access.
 #pragma once
 
 #include "gemm_tc.cuh"
