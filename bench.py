@@ -388,6 +388,8 @@ def run_e2e(step, args, torch, binding):
     used = [ev(), ev()]          # buffer b free again (its step's last kernel done)
     in_x, in_dy = [ev(), ev()], [ev(), ev()]  # buffer b holds its step's inputs
     y_out, dx_out = [ev(), ev()], ev()  # Y (buffer b) / dX copied to the host (may be overwritten)
+    # a step's forward / backward done (re-recorded every step: a wait takes the event's latest record)
+    fwd_done, bwd_done = ev(), ev()
     for e in used + in_x + in_dy + y_out + [dx_out]:
         e.record(comp)
 
@@ -413,7 +415,6 @@ def run_e2e(step, args, torch, binding):
                                      H_out=step.H if w.backward else None, ws=ws_f)
         else:
             binding.tpmlp_forward(Xd[b], step.A, step.B, step.bias, N, Yd[b], ws=ws_f)
-        fwd_done = ev()
         fwd_done.record(comp)
         down.wait_event(fwd_done)
         with torch.cuda.stream(down):
@@ -425,7 +426,6 @@ def run_e2e(step, args, torch, binding):
             binding.tpmlp_sp_backward(list(Xd[b].split(step.rows)), step.gamma, step.beta, step.A, step.B,
                                       step.Hpre, list(dYd[b].split(step.rows)), N, step.dXc, step.dA, step.dB,
                                       step.dgamma, step.dbeta, bias=step.bias, H=step.H, Xg=step.Xg, ws=ws_b)
-            bwd_done = ev()
             bwd_done.record(comp)
             down.wait_event(bwd_done)
             with torch.cuda.stream(down):
