@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(128, V >= 16 ? kLnRegMinBlocks : 1) k_layernor
   __shared__ float red[4];
   __shared__ float2 red2[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (4 / WPR) + warp / WPR;
+  const int row = blockIdx.x * static_cast<int>(blockDim.x >> 5) / WPR + warp / WPR;
   const int sub = warp % WPR;
   const bool valid = row < p.rows;
   const uint4* src = valid ? reinterpret_cast<const uint4*>(chunk_row(p, row)) : nullptr;
@@ -1177,7 +1177,9 @@ cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaS
     case 512: k_layernorm_fwd_reg<2, 1><<<grid4, 128, 0, s>>>(r); break;
     case 1024: k_layernorm_fwd_reg<4, 1><<<grid4, 128, 0, s>>>(r); break;
     case 2048: k_layernorm_fwd_reg<8, 1><<<grid4, 128, 0, s>>>(r); break;
-    case 4096: k_layernorm_fwd_reg<16, 1><<<grid4, 128, 0, s>>>(r); break;
+    // one-warp blocks: a row's block leaves as soon as its row is stored, so the SM takes the next row
+    // without waiting for three other warps, and the last rows spread over all SMs
+    case 4096: k_layernorm_fwd_reg<16, 1><<<r.rows, 32, 0, s>>>(r); break;
     case 8192: k_layernorm_fwd_reg<16, 2><<<grid2, 128, 0, s>>>(r); break;
     default: k_layernorm_fwd_any<false><<<grid4, 128, 0, s>>>(r); break;
   }
