@@ -435,7 +435,7 @@ def mlp_fp8(X, A, B, b, N: int, scales):
     return {"Y": all_reduce(parts), "H": H, "qH": qh, "amax": amax}
 
 
-def mlp_backward_fp8(X, A, B, b, dY, N: int, scales, grad_scales):
+def mlp_backward_fp8(X, A, B, b, dY, N: int, scales, grad_scales, saved=None):
     """Backward of :func:`mlp_fp8` with E5M2 gradients: ``grad_scales = (S_dY, S_dHpre)``.
 
     With the forward's ``q_X, q_A, q_B``, ``Hpre = (q_X·q_A)/(S_X S_A) + b``, ``H = GeLU(Hpre)``,
@@ -444,7 +444,15 @@ def mlp_backward_fp8(X, A, B, b, dY, N: int, scales, grad_scales):
     ``dB = (q_Hᵀ·q_dY)/(S_H S_dY)``, ``dA = (q_Xᵀ·q_g)/(S_X S_dHpre)``, ``db = Σ_rows dHpre``,
     ``dX = Σ_i (q_g,i·q_A,iᵀ)/(S_dHpre S_A)`` (the backward shard sum).  Also the amaxes of
     ``dY`` and ``dHpre``.
+
+    ``saved``: None, or a dict whose entries replace the values this function would form itself:
+    ``"qX"``, ``"qH"`` (E4M3 code values of the norm output and of H, as a forward saved them),
+    ``"Hpre"`` (the saved pre-activation) and ``"qdHpre"`` (E5M2 code values of the gradient that enters
+    the weight- and input-gradient GEMMs).  A backward works from the activations its forward kept; where
+    a cast's input lies within rounding of a midpoint, another implementation's saved codes can differ from
+    these by one step, and this lets the rest of the chain be formed from exactly those codes.
     """
+    saved = {} if saved is None else saved
     sx, sa, sb, sh = (float(np.float32(v)) for v in scales)
     sdy, sg = (float(np.float32(v)) for v in grad_scales)
     X = np.asarray(X, dtype=np.float64)
@@ -452,11 +460,16 @@ def mlp_backward_fp8(X, A, B, b, dY, N: int, scales, grad_scales):
     B = np.asarray(B, dtype=np.float64)
     dY = np.asarray(dY, dtype=np.float64)
     qx, qa, qb = quantize_e4m3(X, sx), quantize_e4m3(A, sa), quantize_e4m3(B, sb)
-    Hpre = (qx @ qa) / (sx * sa) + _bias_or_zero(b, A.shape[1])
-    qh = quantize_e4m3(gelu(Hpre), sh)
+    if "qX" in saved:
+        qx = np.asarray(saved["qX"], dtype=np.float64)
+    if "Hpre" in saved:
+        Hpre = np.asarray(saved["Hpre"], dtype=np.float64)
+    else:
+        Hpre = (qx @ qa) / (sx * sa) + _bias_or_zero(b, A.shape[1])
+    qh = np.asarray(saved["qH"], dtype=np.float64) if "qH" in saved else quantize_e4m3(gelu(Hpre), sh)
     qdy = quantize_e5m2(dY, sdy)
     dHpre = (qdy @ qb.T) / (sdy * sb) * gelu_prime(Hpre)
-    qg = quantize_e5m2(dHpre, sg)
+    qg = np.asarray(saved["qdHpre"], dtype=np.float64) if "qdHpre" in saved else quantize_e5m2(dHpre, sg)
     F = A.shape[1]
     dX_parts = [(qg[:, lo:hi] @ qa[:, lo:hi].T) / (sg * sa) for lo, hi in shard_ranges(F, N)]
     return {"dX": all_reduce(dX_parts), "dX_parts": dX_parts, "dA": (qx.T @ qg) / (sx * sg),
@@ -464,12 +477,12 @@ def mlp_backward_fp8(X, A, B, b, dY, N: int, scales, grad_scales):
             "amax": {"dY": float(np.max(np.abs(dY), initial=0.0)), "dHpre": float(np.max(np.abs(dHpre), initial=0.0))}}
 
 
-def sp_backward_fp8(X_chunks, gamma, beta, eps, A, B, b, dY_chunks, N: int, scales, grad_scales):
+def sp_backward_fp8(X_chunks, gamma, beta, eps, A, B, b, dY_chunks, N: int, scales, grad_scales, saved=None):
     """:func:`sp_backward` with the FP8 GEMMs of :func:`mlp_backward_fp8`: gather the norm output and
     dY, the FP8 MLP backward, reduce-scatter of the input-gradient shard partials, LayerNorm backward
-    per chunk (on the unquantised gradient)."""
+    per chunk (on the unquantised gradient).  ``saved`` as in :func:`mlp_backward_fp8`."""
     Xg = all_gather([layer_norm(c, gamma, beta, eps) for c in X_chunks])
-    g = mlp_backward_fp8(Xg, A, B, b, all_gather(dY_chunks), N, scales, grad_scales)
+    g = mlp_backward_fp8(Xg, A, B, b, all_gather(dY_chunks), N, scales, grad_scales, saved=saved)
     dXg_chunks = reduce_scatter(g["dX_parts"], N)
     dX_chunks, dgamma, dbeta = [], 0.0, 0.0
     for xc, dyc in zip(X_chunks, dXg_chunks):

@@ -706,6 +706,48 @@ def test_mlp_backward_fp8_error_is_the_formats_size():
     assert rel(g["db"], ref["db"]) < 0.2
 
 
+def test_mlp_backward_fp8_saved_operands_enter_where_the_chain_rule_puts_them():
+    """Saved codes replace the oracle's own ones tensor by tensor: its own values change nothing, and one
+    code moved by delta moves exactly the gradients that contain it, by the product the formulas give
+    (dA = q_Xᵀ q_g/(S_X S_g), dB = q_Hᵀ q_dY/(S_H S_dY), dX = q_g q_Aᵀ/(S_g S_A), db = Σ dHpre)."""
+    X, A, B, b, dY, scales, gscales = _fp8_backward_problem(T=12, d=16, F=64)
+    N = 2
+    sx, sa, sb, sh = (float(np.float32(v)) for v in scales)
+    sdy, sg = (float(np.float32(v)) for v in gscales)
+    base = oracle.mlp_backward_fp8(X, A, B, b, dY, N, scales, gscales)
+    qx = oracle.quantize_e4m3(X, scales[0])
+    qa = oracle.quantize_e4m3(A, scales[1])
+    qb = oracle.quantize_e4m3(B, scales[2])
+    Hpre = (qx @ qa) / (sx * sa) + b
+    qh = oracle.quantize_e4m3(oracle.gelu(Hpre), scales[3])
+    qdy = oracle.quantize_e5m2(dY, gscales[0])
+    own = {"qX": qx, "qH": qh, "Hpre": Hpre, "qdHpre": base["qdHpre"]}
+    same = oracle.mlp_backward_fp8(X, A, B, b, dY, N, scales, gscales, saved=own)
+    for k in ("dX", "dA", "dB", "db"):
+        assert np.array_equal(same[k], base[k]), k
+    delta = 0.5
+    for name, r, c in (("qX", 3, 5), ("qH", 4, 7), ("qdHpre", 2, 9), ("Hpre", 1, 11)):
+        moved = dict(own)
+        moved[name] = own[name].copy()
+        moved[name][r, c] += delta
+        g = oracle.mlp_backward_fp8(X, A, B, b, dY, N, scales, gscales, saved=moved)
+        diff = {k: g[k] - base[k] for k in ("dX", "dA", "dB", "db")}
+        expect = {k: np.zeros_like(base[k]) for k in diff}
+        if name == "qX":
+            expect["dA"][c, :] = delta * base["qdHpre"][r, :] / (sx * sg)
+        elif name == "qH":
+            expect["dB"][c, :] = delta * qdy[r, :] / (sh * sdy)
+        elif name == "qdHpre":
+            expect["dA"][:, c] = qx[r, :] * delta / (sx * sg)
+            expect["dX"][r, :] = delta * qa[:, c] / (sg * sa)
+        else:
+            g_up = (qdy @ qb.T)[r, c] / (sdy * sb)
+            expect["db"][c] = g_up * (oracle.gelu_prime(Hpre[r, c] + delta) - oracle.gelu_prime(Hpre[r, c]))
+        for k in diff:
+            np.testing.assert_allclose(diff[k], expect[k], rtol=1e-9, atol=1e-12 * max(1.0, np.abs(base[k]).max()),
+                                       err_msg=f"{name} -> {k}")
+
+
 @pytest.mark.parametrize("N", [1, 2, 4])
 def test_sp_backward_fp8_is_mlp_backward_fp8_on_the_gathered_norm(N):
     T, d, F = 4 * N, 16, 64
