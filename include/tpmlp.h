@@ -356,14 +356,16 @@ TPMLP_API tpmlp_status tpmlp_gemm_fp8(const void* A8, int a_fmt, const void* B8,
  * dbeta; then the delayed-scale update of `grad` (two tensors, dY and dHpre,
  * E5M2's largest value 57344 in place of 448).  `fwd` is the forward's state
  * (its scales unchanged since the forward); Hpre, Xq, Hq the forward's saved
- * outputs.  T, d, F multiples of 16.  Workspace: size of
+ * outputs.  dHq_out: NULL, or [T x F] bytes that receive the E5M2 codes of
+ * dHpre the weight- and input-gradient GEMMs read (otherwise they live in
+ * the workspace).  T, d, F multiples of 16.  Workspace: size of
  * TPMLP_OP_SP_BWD_FP8. */
 TPMLP_API tpmlp_status tpmlp_sp_backward_fp8(const void* const* X_chunks, const void* gamma, float eps, const void* A,
                                              const void* B, const void* Hpre, const void* Xq, const void* Hq,
                                              const void* const* dY_chunks, const tpmlp_fp8_state* fwd,
                                              const tpmlp_fp8_state* grad, const tpmlp_shape* shape,
                                              void* const* dX_chunks, void* dA, void* dB, void* dbias, void* dgamma,
-                                             void* dbeta, void* workspace, size_t workspace_bytes,
+                                             void* dbeta, void* dHq_out, void* workspace, size_t workspace_bytes,
                                              tpmlp_stream_t stream);
 
 /* ------------------------------------------------------------------ single steps (bf16)
@@ -466,6 +468,18 @@ TPMLP_API tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, con
                                       const tpmlp_shape* shape, void* const* dX_chunks, void* dgamma, void* dbeta,
                                       void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* tpmlp_layernorm_backward with its dgamma/dbeta block partials limited to
+ * at most max_blocks CTAs (max_blocks >= 1), so that a small workspace of
+ * max_blocks * 2 * d floats serves (workspace_bytes below that, or
+ * max_blocks < 1, returns TPMLP_ERR_WORKSPACE / TPMLP_ERR_INVALID_ARG).
+ * The results equal tpmlp_layernorm_backward's up to the order of the
+ * dgamma/dbeta sums; fewer CTAs take longer. */
+TPMLP_API tpmlp_status tpmlp_layernorm_backward_blocks(const void* const* X_chunks, const void* gamma, float eps,
+                                                       const void* dXg, const tpmlp_shape* shape,
+                                                       void* const* dX_chunks, void* dgamma, void* dbeta,
+                                                       int32_t max_blocks, void* workspace, size_t workspace_bytes,
+                                                       tpmlp_stream_t stream);
+
 /* tpmlp_layernorm_backward with the residual's gradient added to the input
  * gradient: dX_chunks[j] = LN backward(dXg rows of chunk j) + R_chunks[j]
  * (R_chunks: host array of N pointers [T/N x d]).  Workspace: size of
@@ -485,7 +499,10 @@ TPMLP_API tpmlp_status tpmlp_layernorm_backward_add(const void* const* X_chunks,
  * anything is launched.  All calls on a device share that array: calls whose
  * kernels overlap on the GPU (e.g. on unordered streams) race on it and give
  * wrong dgamma/dbeta.  The first call on a device looks the array up with
- * that device current; make it before any stream capture. */
+ * that device current; make it before any stream capture.  After a device
+ * reset (cudaDeviceReset, or another runtime in the process resetting the
+ * primary context) the device has a new context and the next call looks
+ * the array up again: that call, too, must come before any capture. */
 TPMLP_API tpmlp_status tpmlp_layernorm_backward_noalloc(const void* const* X_chunks, const void* gamma, float eps,
                                                         const void* dXg, const tpmlp_shape* shape,
                                                         void* const* dX_chunks, void* dgamma, void* dbeta,

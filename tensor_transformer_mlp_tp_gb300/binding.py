@@ -74,6 +74,8 @@ _SIGS = {
     "tpmlp_layernorm_backward": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P, ctypes.c_size_t, _P],
                                  ctypes.c_int),
     "tpmlp_layernorm_backward_noalloc": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P], ctypes.c_int),
+    "tpmlp_layernorm_backward_blocks": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, ctypes.c_int32, _P,
+                                         ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
     "tpmlp_sp_block_forward": ([_PP, _P, _P, ctypes.c_float, _P, _P, _P, _P, _DP, _SP, _PP, ctypes.c_int, _P, _P, _P,
                                 _P, ctypes.c_size_t, _P], ctypes.c_int),
@@ -111,7 +113,7 @@ _SIGS = {
                                      ctypes.c_int32, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
                                     ctypes.c_int),
     "tpmlp_sp_backward_fp8": ([_PP, _P, ctypes.c_float, _P, _P, _P, _P, _P, _PP, _FP, _FP, _SP, _PP, _P, _P, _P, _P,
-                               _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+                               _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
 }
 
 
@@ -408,6 +410,21 @@ def tpmlp_layernorm_backward_add(X_chunks, gamma, dXg, R_chunks, N, dX_chunks, d
         ws.numel(), _stream(stream)))
 
 
+def tpmlp_layernorm_backward_blocks(X_chunks, gamma, dXg, N, dX_chunks, dgamma, dbeta, max_blocks, eps=1e-5, ws=None,
+                                    stream=None):
+    """LayerNorm backward with its dgamma/dbeta partials on at most `max_blocks` CTAs (a workspace of
+    max_blocks * 2 * d floats)."""
+    rows, d = X_chunks[0].shape
+    shape = make_shape(rows * N, d, 8 * N, N)  # ffn unused by this step
+    if ws is None:
+        ws = torch.empty(max(1, max_blocks) * 2 * d * 4, dtype=torch.uint8, device=dXg.device)
+    xp, _xa = _ptrs(X_chunks)
+    dxp, _dxa = _ptrs(dX_chunks)
+    _check("tpmlp_layernorm_backward_blocks", lib().tpmlp_layernorm_backward_blocks(
+        xp, _ptr(gamma), eps, _ptr(dXg), ctypes.byref(shape), dxp, _ptr(dgamma), _ptr(dbeta), max_blocks, _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
 def tpmlp_layernorm_backward_noalloc(X_chunks, gamma, dXg, N, dX_chunks, dgamma, dbeta, eps=1e-5, stream=None):
     """LayerNorm backward without a workspace (scratch is a fixed array inside the library)."""
     rows, d = X_chunks[0].shape
@@ -505,7 +522,7 @@ def tpmlp_gemm_fp8(A8, a_fmt, B8, b_fmt, scale_a, scale_b, C, stream=None):
 
 
 def tpmlp_sp_backward_fp8(X_chunks, gamma, A, B, Hpre, Xq, Hq, dY_chunks, N, fwd_state, grad_state, dX_chunks, dA, dB,
-                          dgamma, dbeta, dbias=None, eps=1e-5, ws=None, stream=None):
+                          dgamma, dbeta, dbias=None, eps=1e-5, dHq_out=None, ws=None, stream=None):
     rows, d = X_chunks[0].shape
     shape = make_shape(rows * N, d, A.shape[1], N)
     ws = workspace(shape, OP_SP_BWD_FP8, A.device) if ws is None else ws
@@ -515,7 +532,7 @@ def tpmlp_sp_backward_fp8(X_chunks, gamma, A, B, Hpre, Xq, Hq, dY_chunks, N, fwd
     _check("tpmlp_sp_backward_fp8", lib().tpmlp_sp_backward_fp8(
         xp, _ptr(gamma), eps, _ptr(A), _ptr(B), _ptr(Hpre), _ptr(Xq), _ptr(Hq), dyp, ctypes.byref(fwd_state),
         ctypes.byref(grad_state), ctypes.byref(shape), dxp, _ptr(dA), _ptr(dB), _ptr(dbias), _ptr(dgamma),
-        _ptr(dbeta), _ptr(ws), ws.numel(), _stream(stream)))
+        _ptr(dbeta), _ptr(dHq_out), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- tensor-parallel attention

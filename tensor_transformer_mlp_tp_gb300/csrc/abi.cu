@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "../../include/tpmlp.h"
 #include "launch.h"
@@ -39,6 +40,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct DevState {
   bool init = false;
+  unsigned long long ctx_id = 0;  // the context the cached addresses belong to
   DeviceCtx ctx{};
 };
 std::mutex g_mu;
@@ -58,7 +60,9 @@ tpmlp_status device_ctx(DeviceCtx* out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TPMLP_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   DevState& st = g_dev[dev];
-  if (!st.init) {
+  // a reset device (cudaDeviceReset, or another runtime in the process resetting the primary context)
+  // comes back as a new context with the module loaded afresh: look the addresses up again
+  if (!st.init || current_context_id() != st.ctx_id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_err_words) != cudaSuccess) return TPMLP_ERR_CUDA;
     int sms = 0;
@@ -67,6 +71,7 @@ tpmlp_status device_ctx(DeviceCtx* out) {
     st.ctx.err = static_cast<unsigned int*>(p);
     st.ctx.sm_count = sms;
     st.ctx.timeout_ns = timeout_ns_from_env();
+    st.ctx_id = current_context_id();  // the lookup above made the device's context current
     st.init = true;
   }
   *out = st.ctx;
@@ -74,6 +79,28 @@ tpmlp_status device_ctx(DeviceCtx* out) {
 }
 
 }  // namespace
+
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  // the two driver calls through the runtime's entry-point query (the library links no driver library);
+  // resolved once, both or neither
+  static const std::pair<GetCurrent, GetId> fns = [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa{}, qb{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess || qb != cudaDriverEntryPointSuccess || a == nullptr || b == nullptr)
+      return std::pair<GetCurrent, GetId>(nullptr, nullptr);
+    return std::pair<GetCurrent, GetId>(reinterpret_cast<GetCurrent>(a), reinterpret_cast<GetId>(b));
+  }();
+  if (fns.first == nullptr) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (fns.first(&ctx) != 0 || ctx == nullptr || fns.second(ctx, &id) != 0) return 0;
+  return id;
+}
 
 cudaError_t current_device_ctx(DeviceCtx* out) {
   return device_ctx(out) == TPMLP_OK ? cudaSuccess : cudaErrorUnknown;
@@ -947,6 +974,36 @@ tpmlp_status tpmlp_layernorm_backward(const void* const* X_chunks, const void* g
                                static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
 }
 
+tpmlp_status tpmlp_layernorm_backward_blocks(const void* const* X_chunks, const void* gamma, float eps,
+                                             const void* dXg, const tpmlp_shape* shape, void* const* dX_chunks,
+                                             void* dgamma, void* dbeta, int32_t max_blocks, void* workspace,
+                                             size_t workspace_bytes, tpmlp_stream_t stream) {
+  tpmlp_status st = check_shape(shape, true, true);
+  if (st != TPMLP_OK) return st;
+  if (max_blocks < 1) return TPMLP_ERR_INVALID_ARG;
+  if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
+  if (!ptrs_ok({gamma, dXg, dgamma, dbeta}) || !chunks_ok(X_chunks, shape->n_shards) ||
+      !chunks_ok(dX_chunks, shape->n_shards) || !(eps >= 0.f))
+    return TPMLP_ERR_INVALID_ARG;
+  if (shape->d > kLnBwdMaxD) return TPMLP_ERR_UNSUPPORTED;
+  const size_t cap = static_cast<size_t>(max_blocks) * 2 * static_cast<size_t>(shape->d);
+  if (workspace == nullptr || !al16(workspace) || workspace_bytes < cap * sizeof(float)) return TPMLP_ERR_WORKSPACE;
+  DeviceCtx c;
+  if ((st = device_ctx(&c)) != TPMLP_OK) return st;
+  RowParams r{};
+  r.in_chunks = to_const_chunks(X_chunks, shape->n_shards);
+  r.out_chunks = to_chunks(dX_chunks, shape->n_shards);
+  r.rows = static_cast<int>(shape->tokens);
+  r.d = static_cast<int>(shape->d);
+  r.n_chunks = shape->n_shards;
+  r.rows_per_chunk = static_cast<int>(shape->tokens / shape->n_shards);
+  r.eps = eps;
+  r.gamma = gamma;
+  r.src = dXg;
+  return cuda_status(launch_layernorm_bwd(r, static_cast<float*>(workspace), cap, c, static_cast<float*>(dgamma),
+                                          static_cast<float*>(dbeta), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 tpmlp_status tpmlp_gemm2_bias_dropout_add(const void* H, const void* B, const void* bias2, const tpmlp_dropout* dropout,
                                           const void* const* R_chunks, const tpmlp_shape* shape,
                                           void* const* Y_chunks, tpmlp_stream_t stream) {
@@ -1173,15 +1230,16 @@ tpmlp_status tpmlp_sp_backward_fp8(const void* const* X_chunks, const void* gamm
                                    const void* B, const void* Hpre, const void* Xq, const void* Hq,
                                    const void* const* dY_chunks, const tpmlp_fp8_state* fwd,
                                    const tpmlp_fp8_state* grad, const tpmlp_shape* shape, void* const* dX_chunks,
-                                   void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* workspace,
-                                   size_t workspace_bytes, tpmlp_stream_t stream) {
+                                   void* dA, void* dB, void* dbias, void* dgamma, void* dbeta, void* dHq_out,
+                                   void* workspace, size_t workspace_bytes, tpmlp_stream_t stream) {
   tpmlp_status st = check_shape(shape, true, true);
   if (st != TPMLP_OK) return st;
   if ((st = check_fp8(shape)) != TPMLP_OK) return st;
   if (shape->tokens % 16 != 0) return TPMLP_ERR_INVALID_ARG;
   if (shape->tokens == 0) return TPMLP_OK;  // empty batch: nothing to launch, pointers may be NULL
   const int n = shape->n_shards;
-  if (!ptrs_ok({gamma, A, B, Hpre, Xq, Hq, dA, dB, dgamma, dbeta}) || !opt_ok(dbias) || !chunks_ok(X_chunks, n) ||
+  if (!ptrs_ok({gamma, A, B, Hpre, Xq, Hq, dA, dB, dgamma, dbeta}) || !opt_ok(dbias) || !opt_ok(dHq_out) ||
+      !chunks_ok(X_chunks, n) ||
       !chunks_ok(dY_chunks, n) || !chunks_ok(dX_chunks, n) || !(eps >= 0.f) || !fp8_state_ok(fwd) ||
       !fp8_state_ok(grad))
     return TPMLP_ERR_INVALID_ARG;
@@ -1203,6 +1261,7 @@ tpmlp_status tpmlp_sp_backward_fp8(const void* const* X_chunks, const void* gamm
   void* Aq = ws.take(z.df8);
   void* Bq = ws.take(z.df8);
   void* dHq = ws.take(z.tf8);
+  if (dHq_out != nullptr) dHq = dHq_out;  // the caller keeps the E5M2 dHpre
   void* HqT = ws.take(z.tf8);
   void* dHqT = ws.take(z.tf8);
   float* colsum = static_cast<float*>(ws.take(z.colsum));

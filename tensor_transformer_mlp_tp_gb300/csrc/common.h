@@ -12,6 +12,8 @@ constexpr int kMaxShards = 64;  // N, the number of column/row shards (and of SP
 // Device error words: [0] = OR of error bits, [1] = first failing wait site.
 constexpr int kErrWords = 4;
 constexpr uint32_t kErrTimeout = 1u;
+// A kernel refused a launch configuration it cannot run safely (and touched no memory).
+constexpr uint32_t kErrConfig = 2u;
 
 // Wait sites reported in error word [1] (one id per wait in the GEMM kernel).
 enum WaitSite : uint32_t {
@@ -132,5 +134,6 @@ struct RowParams {
 // Wait sites of the row-streaming kernels.
 constexpr uint32_t kSiteRowProducer = 16;
 constexpr uint32_t kSiteRowConsumer = 17;
+constexpr uint32_t kSiteRowConfig = 18;
 
 }  // namespace tpmlp

@@ -75,6 +75,10 @@ size_t layernorm_bwd_scratch_floats(int rows, int d);
 int layernorm_bwd_blocks(int rows, int max_blocks);
 // The device context (error words, SM count, wait budget) of the current device.
 cudaError_t current_device_ctx(DeviceCtx* out);
+// Process-unique id of the CUDA context current on this thread (the driver's cuCtxGetId), 0 when no
+// context is current or the query is unavailable.  A device reset gives the device a new context, and
+// with it a new id: addresses of the library's __device__ arrays cached under the old id are stale.
+unsigned long long current_context_id();
 // Largest d the LayerNorm backward supports (its 2 d fp32 accumulators live in shared memory).
 constexpr int kLnBwdMaxD = 16384;
 cudaError_t launch_reduce_scatter(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s);

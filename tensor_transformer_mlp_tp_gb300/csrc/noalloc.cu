@@ -22,7 +22,10 @@
 //    no ordering between them) race on the array and give wrong dgamma/dbeta.
 //  - The first call on a device looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current; make that first call
-//    before any stream capture.
+//    before any stream capture.  The address is cached per device together
+//    with the id of the context it belongs to; after a device reset (a new
+//    context) the next call looks it up again, so that first call after a
+//    reset must also come before any capture.
 #include <cstdint>
 #include <mutex>
 
@@ -40,19 +43,22 @@ static __device__ __align__(256) float g_lnbwd_scratch[kNoAllocFloats];
 
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[64] = {};
+unsigned long long g_noalloc_ctx[64] = {};  // context id each cached address belongs to
 
-// Device address of the scratch array on the current device, looked up once per device.
+// Device address of the scratch array on the current device, looked up once per device (and again when
+// the device's context has changed since, after a reset).
 cudaError_t scratch_address(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (g_noalloc_ptr[dev] == nullptr || current_context_id() != g_noalloc_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_lnbwd_scratch);
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev] = static_cast<float*>(p);
+    g_noalloc_ctx[dev] = current_context_id();  // the lookup made the device's context current
   }
   *out = g_noalloc_ptr[dev];
   return cudaSuccess;

@@ -592,6 +592,19 @@ __device__ __forceinline__ void stream_producer(const RowParams& p, uint8_t* rin
     if (issued_mask & (1u << s)) wait_drain(full + s, (issued_parity >> s) & 1u, p.timeout_ns);
 }
 
+// The ring's phase parity is one bit, so a consumer must never wait on a slot while that slot's previous
+// row is still unconsumed by someone else: each slot has to belong to one team, which takes its rows in
+// order.  Rows go to slot i % slots and to team i % teams, so that holds exactly when slots is a multiple
+// of teams.  A CTA given any other count records kErrConfig and returns before it touches memory.
+__device__ __forceinline__ bool ring_config_ok(const RowParams& p, int teams) {
+  if (p.slots >= teams && p.slots % teams == 0 && p.slots <= 32) return true;
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    atomicOr(p.err, kErrConfig);
+    atomicCAS(p.err + 1, 0u, kSiteRowConfig);
+  }
+  return false;
+}
+
 __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, const WaitCtx& wc) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, wc, kSiteRowConsumer) ? 1 : 0;
@@ -640,6 +653,7 @@ __device__ __forceinline__ float warp_sum4(float a, float b, float c, float d) {
 template <int VT, int TW, bool ADD = false, int CONS = kStreamConsumers>
 __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(const RowParams p) {
   constexpr int kTeams = CONS / TW;
+  if (!ring_config_ok(p, kTeams)) return;  // uniform over the CTA: no barrier is left waiting
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align128(smem_raw);
   const uint32_t row_bytes = static_cast<uint32_t>(p.d) * 2u;
@@ -788,6 +802,129 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
 #pragma unroll
     for (int tm = 0; tm < kTeams; ++tm) t += acc[tm * 2 * p.d + c];
     p.partial[static_cast<long long>(blockIdx.x) * 2 * p.d + c] = t;
+  }
+}
+
+// LayerNorm forward streamed through the ring: the producer lane keeps the CTA's next rows in flight while
+// teams of TW consumer warps normalise.  A team copies its row from the slot into registers (thread j of
+// the team owns the 16-byte vectors j + k·32·TW, k < VT; d = 256 TW VT), frees the slot and only then
+// reduces and stores, so the CTA's loads never wait on its arithmetic.  The kernel is bound by its
+// instruction latencies rather than by DRAM (its time follows the SM clock), so it keeps the work per
+// element small and many rows in flight: γ and β are converted to fp32 once per CTA into shared memory
+// (each vector's first four values in one array, its last four in another, so that a warp's 16-byte reads
+// are consecutive), statistics come from shifted sums in one reduction round (K = the row's first
+// element), and the output is (x·rstd − mean·rstd)·γ + β, two fused multiply-adds per float pair, rounded
+// once to bf16 and stored from registers into the row's slot of the gathered tensor.
+template <int VT, int TW, int CONS = kStreamConsumers>
+__global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_fwd_stream(const RowParams p) {
+  constexpr int kTeams = CONS / TW;
+  if (!ring_config_ok(p, kTeams)) return;  // uniform over the CTA: no barrier is left waiting
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = align128(smem_raw);
+  const uint32_t row_bytes = static_cast<uint32_t>(p.d) * 2u;
+  const int nv = p.d / 8;                  // 16-byte vectors per row
+  float4* gb = reinterpret_cast<float4*>(ring + p.slots * row_bytes);  // [4][nv]: γ lo, γ hi, β lo, β hi
+  uint64_t* full = reinterpret_cast<uint64_t*>(gb + 4 * nv);
+  uint64_t* empty = full + p.slots;
+  int* abort_flag = reinterpret_cast<int*>(empty + p.slots);
+  __shared__ float2 red2[2][CONS];
+  __shared__ int vote[2][CONS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.slots; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, TW);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(p.gamma) + v), f);
+    gb[v] = make_float4(f[0], f[1], f[2], f[3]);
+    gb[nv + v] = make_float4(f[4], f[5], f[6], f[7]);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(p.beta) + v), f);
+    gb[2 * nv + v] = make_float4(f[0], f[1], f[2], f[3]);
+    gb[3 * nv + v] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+  __syncthreads();
+  const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
+  const int n_rows = p.rows > static_cast<int>(blockIdx.x)
+                         ? (p.rows - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / gridDim.x
+                         : 0;
+  if (warp == 0) {
+    // the producer drains its copies in flight before it leaves; no CTA-wide barrier follows
+    if (lane == 0) stream_producer(p, ring, row_bytes, row_bytes, full, empty, n_rows, wc, false);
+    return;
+  }
+  const int cw = warp - 1;        // consumer warp index
+  const int team = cw / TW;
+  const int tw = cw % TW;         // warp within the team
+  const int j = tw * 32 + lane;   // thread within the team
+  const float inv_d = 1.f / static_cast<float>(p.d);
+  int par = 0;
+  for (int i = team; i < n_rows; i += kTeams, par ^= 1) {
+    const int slot = i % p.slots;
+    // every warp of the team waits (bounded) on its own; the outcomes are voted at the team barrier
+    const bool ok = stream_wait(full + slot, static_cast<uint32_t>(i / p.slots) & 1u, wc);
+    const uint4* xs = reinterpret_cast<const uint4*>(ring + slot * row_bytes);
+    uint4 xv[VT];
+#pragma unroll
+    for (int k = 0; k < VT; ++k) xv[k] = ok ? xs[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
+    const float shift = ok ? __uint_as_float(xs[0].x << 16) : 0.f;  // the row's first element
+    __syncwarp();
+    if (lane == 0 && ok) mbar_arrive(empty + slot);
+    const float2 nk = make_float2(-shift, -shift);
+    float2 s1 = make_float2(0.f, 0.f), s2 = s1;
+#pragma unroll
+    for (int k = 0; k < VT; ++k)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 c = __fadd2_rn(bf2(word(xv[k], w)), nk);
+        s1 = __fadd2_rn(s1, c);
+        s2 = __ffma2_rn(c, c, s2);
+      }
+    float2 t = warp_sum2(s1.x + s1.y, s2.x + s2.y);
+    bool team_ok = ok;
+    if constexpr (TW > 1) {
+      if (lane == 0) {
+        red2[par][cw] = t;
+        vote[par][cw] = ok ? 1 : 0;
+      }
+      team_sync(team, TW);
+      t = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < TW; ++w) {
+        const float2 r = red2[par][team * TW + w];
+        t.x += r.x;
+        t.y += r.y;
+        team_ok = team_ok && vote[par][team * TW + w] != 0;
+      }
+    }
+    if (!team_ok) break;
+    const float m = t.x * inv_d;  // mean - K
+    const float rstd = rsqrtf(fmaxf(t.y * inv_d - m * m, 0.f) + p.eps);
+    const float nmr = -(shift + m) * rstd;  // -mean rstd
+    const float2 a2 = make_float2(rstd, rstd), b2 = make_float2(nmr, nmr);
+    const int row = blockIdx.x + i * gridDim.x;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dst) + static_cast<long long>(row) * p.d);
+#pragma unroll
+    for (int k = 0; k < VT; ++k) {
+      const int idx = j + k * 32 * TW;
+      const float4 gl = gb[idx], gh = gb[nv + idx], bl = gb[2 * nv + idx], bh = gb[3 * nv + idx];
+      const float2 g2[4] = {make_float2(gl.x, gl.y), make_float2(gl.z, gl.w), make_float2(gh.x, gh.y),
+                            make_float2(gh.z, gh.w)};
+      const float2 be2[4] = {make_float2(bl.x, bl.y), make_float2(bl.z, bl.w), make_float2(bh.x, bh.y),
+                             make_float2(bh.z, bh.w)};
+      uint32_t o[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 y = __ffma2_rn(__ffma2_rn(bf2(word(xv[k], w)), a2, b2), g2[w], be2[w]);
+        o[w] = pack_bf16x2(y.x, y.y);
+      }
+      dst[idx] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -1118,10 +1255,8 @@ static int stream_slots(size_t slot_bytes) {
   return static_cast<int>(n < 2 ? 2 : (n > 32 ? 32 : n));
 }
 
-// LayerNorm forward: one warp per row (two for d = 8192) with the row in
-// registers.  (A shared-memory-streamed variant was measured slower on GB300 in
-// the SP step: between GEMMs this kernel's bandwidth is held by the write-back
-// of the dirty L2 lines the previous kernels leave, not by its load latency.)
+// LayerNorm forward for widths the streamed kernel does not cover: one warp per row (two for d = 8192)
+// with the row in registers.
 // Persistent launch of a pipelined LayerNorm kernel, or cudaErrorNotReady when the grid would give each
 // warp (pair) fewer than kLnPipeMinRows rows: below that the exposed first load and the tail outweigh the
 // overlap (measured on GB300: at T = 8192, d = 4096 the launch-per-group kernel is 7% faster; at T = 65536
@@ -1158,9 +1293,61 @@ static cudaError_t launch_ln_pipe2(const RowParams& r, const DeviceCtx& ctx, cud
   return launch_ln_persistent(k_layernorm_fwd_pipe2<V>, 2, r, ctx, s, per_sm);
 }
 
+// The streamed LayerNorm forward, VT vectors per thread and TW warps per row (d = 256 TW VT), CONS consumer
+// warps: `per_sm` CTAs per SM (fewer for short inputs), each with a ring of about `ring_bytes` of row
+// slots, the slot count a multiple of the teams (see ring_config_ok).
+template <int VT, int TW, int CONS>
+static cudaError_t launch_ln_stream_cfg(const RowParams& r0, const DeviceCtx& ctx, cudaStream_t s,
+                                        size_t ring_bytes, int per_sm) {
+  constexpr int kTeams = CONS / TW;
+  constexpr size_t kMaxSmem = 227u * 1024u;
+  RowParams r = r0;
+  r.err = ctx.err;
+  r.timeout_ns = ctx.timeout_ns;
+  const size_t row_bytes = static_cast<size_t>(r.d) * 2;
+  const size_t fixed = 128 + 4 * row_bytes + 16;  // alignment, fp32 γ/β (8 d bytes), abort flag
+  size_t slots = ring_bytes / row_bytes / kTeams * kTeams;
+  if (slots < static_cast<size_t>(kTeams)) slots = kTeams;
+  while (slots > 32 || (slots > static_cast<size_t>(kTeams) && fixed + slots * (row_bytes + 16) > kMaxSmem))
+    slots -= kTeams;
+  if (fixed + slots * (row_bytes + 16) > kMaxSmem) return cudaErrorNotSupported;
+  r.slots = static_cast<int>(slots);
+  const size_t smem = fixed + slots * (row_bytes + 16);  // + the ring and its two barriers per slot
+  const long long cap = static_cast<long long>(per_sm) * ctx.sm_count;
+  const int grid = static_cast<int>(r.rows < cap ? r.rows : cap);
+  return launch_stream(k_layernorm_fwd_stream<VT, TW, CONS>, r, smem, grid, s, 32 * (CONS + 1));
+}
+
+// Ring bytes per CTA of the streamed forward.  Measured on GB300 (CUDA graphs of back-to-back launches,
+// fraction of the measured HBM bandwidth at T = 8192, d = 4096 / T = 4096, d = 8192): teams of two warps
+// on a 64 KB ring 0.80 / 0.79; one-warp teams 0.74 / 0.78; a 190 KB ring 0.74 / 0.66 (every SM's first
+// rows wait behind the whole start-up burst); two CTAs per SM with 48 KB rings 0.65 / 0.60; the
+// register kernels 0.69 / 0.65.
+constexpr size_t kLnFwdRingBytes = 64u * 1024u;
+constexpr int kLnFwdCtasPerSm = 1;
+
+// cudaErrorNotSupported for widths it does not cover.
+static cudaError_t launch_ln_stream(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
+  constexpr size_t kRing = kLnFwdRingBytes;
+  constexpr int kPer = kLnFwdCtasPerSm;
+  // four teams of VT = 8 vectors per thread where the width allows (measured best at d = 4096 and 8192:
+  // fewer teams leave the SM idle between rows, more run out of registers or issue slots)
+  switch (r.d) {
+    case 256: return launch_ln_stream_cfg<1, 1, 8>(r, ctx, s, kRing, kPer);
+    case 512: return launch_ln_stream_cfg<2, 1, 8>(r, ctx, s, kRing, kPer);
+    case 1024: return launch_ln_stream_cfg<4, 1, 8>(r, ctx, s, kRing, kPer);
+    case 2048: return launch_ln_stream_cfg<8, 1, 8>(r, ctx, s, kRing, kPer);
+    case 4096: return launch_ln_stream_cfg<8, 2, 8>(r, ctx, s, kRing, kPer);
+    case 8192: return launch_ln_stream_cfg<8, 4, 16>(r, ctx, s, kRing, kPer);
+    default: return cudaErrorNotSupported;
+  }
+}
+
 cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
   if (r.rows <= 0) return cudaSuccess;
   {
+    // long inputs: the persistent register-pipelined kernels (T = 65536, d = 4096: 0.95 of HBM, the
+    // streamed kernel 0.92)
     cudaError_t e = cudaErrorNotReady;
     switch (r.d) {
       case 1024: e = launch_ln_pipe<4>(r, ctx, s); break;
@@ -1169,6 +1356,10 @@ cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaS
       default: break;
     }
     if (e != cudaErrorNotReady) return e;  // launched (or failed); otherwise too few rows per warp
+  }
+  {
+    const cudaError_t e = launch_ln_stream(r, ctx, s);
+    if (e != cudaErrorNotSupported) return e;  // launched (or failed); otherwise a width it does not cover
   }
   const int grid4 = (r.rows + 3) / 4;
   const int grid2 = (r.rows + 1) / 2;
@@ -1270,7 +1461,10 @@ cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap
     if (static_cast<size_t>(grid) * per_block > cap_floats) grid = static_cast<int>(cap_floats / per_block);
     if (grid >= 1) {
       const size_t row_bytes = static_cast<size_t>(r.d) * 2;
-      r.slots = stream_slots(2 * row_bytes);
+      // a multiple of the consumer teams (see ring_config_ok)
+      const int teams = kStreamConsumers / ts.tw;
+      r.slots = stream_slots(2 * row_bytes) / teams * teams;
+      if (r.slots < teams) r.slots = teams;
       size_t smem = 128 + r.slots * 2 * row_bytes + row_bytes + 16 * static_cast<size_t>(r.slots) + 16;
       const size_t team_sums = static_cast<size_t>(kStreamConsumers / ts.tw) * per_block * 4 + 128;
       if (smem < team_sums) smem = team_sums;

@@ -167,6 +167,21 @@ def test_layernorm_wide_rows():
         assert_bf16_close(f"Xg d={d}", f64(Xg), ref)
 
 
+@pytest.mark.parametrize("T,d,N", [(8200, 4096, 8), (2056, 8192, 8), (4104, 2048, 4), (3000, 1024, 8),
+                                   (1216, 512, 8), (1000, 256, 8), (152, 4096, 8), (153, 8192, 9)])
+def test_layernorm_gather_streamed(T, d, N):
+    """The streamed forward: many passes around each CTA's slot ring (rows well above the SM count, ragged
+    against it), one row per CTA and more CTAs than rows, every width it covers; checked in full."""
+    w = inputs.small_workload(T, d, N, sp=True, name=f"lnstream_{T}_{d}")
+    X, g, b = _draw(w, "X", "gamma", "beta")
+    Xg = Guarded((T, d))
+    binding.tpmlp_layernorm_gather(list(dev(X[0]).split(T // N)), dev(g[0]), dev(b[0]), N, Xg.t)
+    torch.cuda.synchronize()
+    ref = oracle.all_gather([oracle.layer_norm(c, g[1], b[1], 1e-5) for c in _chunks(X[1], N)])
+    assert_bf16_close("Xg", f64(Xg.t), ref)
+    assert Xg.intact()
+
+
 @pytest.mark.parametrize("N", [2, 4, 8])
 def test_reduce_scatter_random(N):
     T, d = 64 * N, 200
@@ -363,6 +378,44 @@ def test_layernorm_backward_step(T, d, N):
     assert_bf16_close("dgamma", f64(dga.t), sum(r[1] for r in refs))
     assert_bf16_close("dbeta", f64(dbe.t), sum(r[2] for r in refs))
     assert all(x.intact() for x in dX + [dga, dbe])
+
+
+@pytest.mark.parametrize("T,d,N,max_blocks", [(1024, 8192, 8, 1), (1024, 8192, 8, 37), (600, 4096, 4, 5),
+                                                (300, 136, 4, 2), (256, 2048, 8, 300)])
+def test_layernorm_backward_capped_blocks(T, d, N, max_blocks):
+    """The LayerNorm backward with its dgamma/dbeta partials capped below the SM count (the grid a small
+    scratch gives), down to one CTA, in the fused kernels (d = 2048, 4096, 8192) and the generic one
+    (d = 136); a cap above the rows changes nothing."""
+    w = inputs.small_workload(T, d, N, sp=True, backward=True, name=f"lnbwd_cap_{T}_{d}_{max_blocks}")
+    X, g = inputs.draw(w, "X"), inputs.draw(w, "gamma")
+    dXg = inputs.draw(w, "dY")
+    rows = T // N
+    dX = [Guarded((rows, d)) for _ in range(N)]
+    dga, dbe = Guarded((d,), torch.float32), Guarded((d,), torch.float32)
+    ws = Guarded((max_blocks * 2 * d,), torch.float32)
+    binding.tpmlp_layernorm_backward_blocks(list(dev(X[0]).split(rows)), dev(g[0]), dev(dXg[0]), N,
+                                            [x.t for x in dX], dga.t, dbe.t, max_blocks, ws=ws.t.view(torch.uint8))
+    torch.cuda.synchronize()
+    refs = [oracle.layer_norm_backward(X[1][lo:hi], g[1], 1e-5, dXg[1][lo:hi]) for lo, hi in oracle.chunk_ranges(T, N)]
+    assert_bf16_close("dX", np.concatenate([f64(x.t) for x in dX]), np.concatenate([r[0] for r in refs]))
+    assert_bf16_close("dgamma", f64(dga.t), sum(r[1] for r in refs))
+    assert_bf16_close("dbeta", f64(dbe.t), sum(r[2] for r in refs))
+    assert all(x.intact() for x in dX + [dga, dbe, ws])
+
+
+def test_layernorm_backward_blocks_rejects_a_short_workspace():
+    N, rows, d = 2, 8, 1024
+    xs = [torch.zeros(rows, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    args = (xs, torch.ones(d, dtype=torch.bfloat16, device="cuda"),
+            torch.zeros(N * rows, d, dtype=torch.bfloat16, device="cuda"), N, [torch.empty_like(x) for x in xs],
+            torch.empty(d, device="cuda"), torch.empty(d, device="cuda"))
+    with pytest.raises(binding.TpMlpError) as e:
+        binding.tpmlp_layernorm_backward_blocks(*args, 4, ws=torch.empty(4 * 2 * d * 4 - 16, dtype=torch.uint8,
+                                                                         device="cuda"))
+    assert e.value.status == binding.ERR_WORKSPACE
+    with pytest.raises(binding.TpMlpError) as e:
+        binding.tpmlp_layernorm_backward_blocks(*args, 0, ws=torch.empty(1024, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == binding.ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("T,d,N", [(256, 4096, 8), (96, 8192, 4), (200, 1024, 8), (24, 136, 3)])

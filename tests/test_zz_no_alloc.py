@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_util import assert_bf16_close, dev, f64
 from tensor_transformer_mlp_tp_gb300 import binding, inputs
 
@@ -31,6 +32,11 @@ def test_noalloc_matches_workspace_entry_point_twice(T, d, N):
     ref_dg = torch.empty(d, dtype=torch.float32, device="cuda")
     ref_db = torch.empty(d, dtype=torch.float32, device="cuda")
     binding.tpmlp_layernorm_backward(xs, g, dXg, N, list(ref_dx.split(rows)), ref_dg, ref_db)
+    # the oracle's LayerNorm backward on the same chunks, the ground truth for both entry points
+    Xo, go, dXo = inputs.draw(w, "X")[1], inputs.draw(w, "gamma")[1], inputs.draw(w, "dY")[1]
+    refs = [oracle.layer_norm_backward(Xo[lo:hi], go, 1e-5, dXo[lo:hi]) for lo, hi in oracle.chunk_ranges(T, N)]
+    o_dx = np.concatenate([r[0] for r in refs])
+    o_dg, o_db = sum(r[1] for r in refs), sum(r[2] for r in refs)
     for call in range(2):  # the shared scratch keeps the previous call's contents
         dx = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
         dg = torch.full((d,), float("nan"), dtype=torch.float32, device="cuda")
@@ -40,6 +46,9 @@ def test_noalloc_matches_workspace_entry_point_twice(T, d, N):
         assert_bf16_close(f"dX (call {call})", f64(dx), f64(ref_dx))
         assert_bf16_close(f"dgamma (call {call})", f64(dg), f64(ref_dg))
         assert_bf16_close(f"dbeta (call {call})", f64(db), f64(ref_db))
+        assert_bf16_close(f"dX vs oracle (call {call})", f64(dx), o_dx)
+        assert_bf16_close(f"dgamma vs oracle (call {call})", f64(dg), o_dg)
+        assert_bf16_close(f"dbeta vs oracle (call {call})", f64(db), o_db)
     st, site = binding.tpmlp_get_device_status()
     assert st == binding.OK, (st, site)
 
