@@ -9,9 +9,15 @@ the row-parallel GEMM with the in-kernel shard reduction and fused
 reduce-scatter store, then the backward on the forward's saved activations
 (Xg, H, Hpre): dY B^T * GeLU', dB = H^T dY, dA = Xg^T dHpre, dXg = dHpre A^T
 and the LayerNorm backward.
-Every kernel is timed with CUDA events on the stream it is launched on.
+Every kernel is timed with CUDA events on the stream it is launched on; a GEMM
+timed over less than a second is compared with the measured burst bf16 peak,
+a longer one with the sustained peak, and also with the peak at the SM clock
+the run held.  ``step_ms`` gives the p10 / median / p90 of the timed steps.
 ``e2e`` repeats the step through the block calls of the C ABI with the
 activations copied from / to pinned host memory inside the timed region.
+After the step, ``other_rows`` times the rest of the hot path on the same
+shapes and the two forward-only workloads that carry the d = 4096 and d = 8192
+forward GEMM rates (``mlp7b_fwd``, ``sp_large_fwd``).
 The ``reference`` implementation is the CPU fp64 oracle on a bounded sample
 of the same workload.
 """
@@ -47,6 +53,40 @@ def peaks():
             d = json.load(fh)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+# A timed region shorter than this is compared with the burst peak (a cuBLAS GEMM timed alone), a longer
+# one with the sustained peak (the same GEMM back to back for seconds, under the power cap).
+SUSTAINED_AFTER_S = 1.0
+# Dense bf16 tcgen05 rate per SM and clock: one 128 x 128 x 16 UMMA (524288 flops) per 64 cycles on an SM
+# (a probe of the MMA alone on resident operands), i.e. 8192 flop/clk/SM.
+BF16_FLOP_PER_CLK_SM = 8192.0
+
+
+def tensor_peak(pk, region_s, dtype_factor=1.0):
+    """(peak TFLOP/s, description) for a kernel timed over a region of `region_s` seconds: the measured burst
+    peak below SUSTAINED_AFTER_S, the sustained one above; `dtype_factor` scales it (2 for FP8: the nominal
+    dense FP8 : BF16 ratio)."""
+    sustained = region_s >= SUSTAINED_AFTER_S and "bf16_tflops_sustained" in pk
+    base = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+    kind = "sustained" if sustained else "burst"
+    if dtype_factor != 1.0:
+        kind = f"{dtype_factor:g} x bf16 {kind}"
+    return base * dtype_factor, kind
+
+
+def clock_peak(sm_count, sm_mhz, dtype_factor=1.0):
+    """Dense tensor peak (TFLOP/s) at the SM clock the run actually held: flop/clk/SM x SMs x clock."""
+    if not sm_mhz or not sm_count:
+        return None
+    return BF16_FLOP_PER_CLK_SM * dtype_factor * sm_count * sm_mhz * 1e6 / 1e12
+
+
+def percentiles(ms):
+    """p10 / median / p90 of per-step times (ms)."""
+    a = np.sort(np.asarray(ms, dtype=np.float64))
+    return {"p10": round(float(np.percentile(a, 10)), 4), "median": round(float(np.median(a)), 4),
+            "p90": round(float(np.percentile(a, 90)), 4)}
 
 
 _GEMM_SOURCES = ("common.h", "ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_tc.cu")
@@ -148,17 +188,24 @@ class ClockSampler:
         except (ValueError, IndexError):
             return None
 
+    def _rows(self):
+        if getattr(self, "_cache", None) is None:
+            rows = []
+            if self.proc is not None and os.path.exists(self.path):
+                with open(self.path) as fh:
+                    for line in fh:
+                        parts = [x.strip() for x in line.split(",")]
+                        if len(parts) >= 9:
+                            rows.append(parts)
+                os.unlink(self.path)
+            self._cache = rows
+        return self._cache
+
     def summary(self, t0=None, t1=None):
         """Median SM clock and the throttle reasons seen in samples taken between t0 and t1 (epoch seconds)."""
-        if self.proc is None or not os.path.exists(self.path):
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
+        rows = self._rows()
         if t0 is not None:
             inside = [r for r in rows if (lambda e: e is not None and t0 - 0.1 <= e <= t1 + 0.1)(self._epoch(r[0]))]
             rows = inside or rows[-3:]
@@ -257,12 +304,27 @@ def run_reference(args, w):
 class Step:
     """Device buffers of one workload and the sequence of ABI step calls of one step."""
 
-    def __init__(self, w, torch, binding, seed=0):
+    def __init__(self, w, torch, binding, seed=0, on_device=False):
+        """Inputs from the seeded host generator of `inputs` (the parity tests' recipe), or with `on_device`
+        from torch's seeded device generator with the same distributions (fast for the largest weights)."""
         self.w, self.torch, self.b = w, torch, binding
         dev = "cuda"
         T, d, F, N = w.T, w.d, w.F, w.N
+        gen = None
+        if on_device:
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(seed)
 
         def up(name):
+            if on_device:
+                dist = w.dists.get(name)
+                if dist is None:
+                    return None
+                shape = inputs.tensor_shape(w, name)
+                if dist == "zero":
+                    return torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+                t = torch.empty(shape, dtype=torch.float32, device=dev).normal_(dist[0], dist[1], generator=gen)
+                return t.to(torch.bfloat16)  # round to nearest even, as the host recipe
             r = inputs.draw(w, name, seed)
             if r is None:
                 return None
@@ -297,7 +359,10 @@ class Step:
 
     def kernels(self):
         """(name, launches, algorithmic work per launch, unit) of each timed segment of a step."""
-        w = self.w
+        return Step.kernels_of(self.w)
+
+    @staticmethod
+    def kernels_of(w):
         g = 2.0 * w.T * w.d * w.F
         ln = 2.0 * w.T * w.d * 2          # read x, write y (bf16)
         segs = []
@@ -412,7 +477,8 @@ def run_e2e(step, args, torch, binding):
         if w.sp:
             binding.tpmlp_sp_forward(list(Xd[b].split(step.rows)), step.gamma, step.beta, step.A, step.B, N,
                                      Ycd[b], bias=step.bias, Hpre_out=step.Hpre if w.backward else None,
-                                     H_out=step.H if w.backward else None, ws=ws_f)
+                                     H_out=step.H if w.backward else None, Xg_out=step.Xg if w.backward else None,
+                                     ws=ws_f)
         else:
             binding.tpmlp_forward(Xd[b], step.A, step.B, step.bias, N, Yd[b], ws=ws_f)
         fwd_done.record(comp)
@@ -467,12 +533,49 @@ def time_calls(torch, fn, reps, warmup=3):
     return e0.elapsed_time(e1) / reps
 
 
+def time_graph(torch, fn, reps, warmup=3):
+    """Average ms of `fn` over `reps` back-to-back calls captured in one CUDA graph and replayed: the kernels'
+    own time without the host's launch cost between them (a Python call through the C ABI takes about
+    15 us of host time, more than half of a 25 us row kernel)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    del g
+    return ms
+
+
+def hbm_row(nb, ms_graph, ms_eager, pk, **extra):
+    """A row kernel's rates: algorithmic bytes per launch over the graph-timed and the eager time."""
+    gbs = lambda ms: nb / (ms * 1e-3) / 1e9
+    out = {"ms": round(ms_graph, 4), "GB/s": round(gbs(ms_graph), 1), "frac": round(gbs(ms_graph) / pk["hbm_gbs"], 3),
+           "timing": "CUDA graph of back-to-back launches", "eager_ms": round(ms_eager, 4),
+           "eager_frac": round(gbs(ms_eager) / pk["hbm_gbs"], 3), "bytes_per_launch": nb}
+    out.update(extra)
+    return out
+
+
 def run_fp8_step(step, torch, binding, pk):
     """The FP8 path on the step's shapes: the E4M3 forward (weight casts, E4M3 LayerNorm, both E4M3 GEMMs),
     the backward with E5M2 gradients (dY casts, weight casts, the E5M2 GeLU' GEMM, three byte transposes,
     three FP8 GEMMs, the bf16 LayerNorm backward) and both delayed-scale updates, timed as a whole and per
-    GEMM.  The FP8 tensor peak is the measured sustained bf16 peak times the nominal dense FP8 : BF16
-    ratio of 2."""
+    GEMM.  The FP8 tensor peak is the measured burst bf16 peak (each GEMM is timed over ten calls) times the
+    nominal dense FP8 : BF16 ratio of 2."""
     w = step.w
     T, d, F, N = w.T, w.d, w.F, w.N
     u8 = dict(dtype=torch.uint8, device="cuda")
@@ -527,7 +630,8 @@ def run_fp8_step(step, torch, binding, pk):
     ms_wb = time_calls(torch, lambda: binding.tpmlp_gemm_fp8(HqT, binding.E4M3, dYqT, binding.E5M2, sc[3:4],
                                                               gsc[0:1], dB), 10)
     g = 2.0 * T * d * F
-    peak8 = 2.0 * pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    # each GEMM is timed over ten calls (well under a second): the burst peak, doubled for FP8
+    peak8, peak8_kind = tensor_peak(pk, 0.0, dtype_factor=2.0)
     tf = lambda ms: round(g / (ms * 1e-3) / 1e12, 1)
     kern = lambda ms: {"ms": round(ms, 4), "TFLOP/s": tf(ms), "frac": round(tf(ms) / peak8, 3)}
     return {"step_ms": round(ms_step, 4), "step_TFLOP/s": round(6 * g / (ms_step * 1e-3) / 1e12, 1),
@@ -539,7 +643,8 @@ def run_fp8_step(step, torch, binding, pk):
             "cast_weights_transposed_ms": round(ms_ca + ms_cb, 4),
             "cast_weights_GB/s": round(3.0 * 2 * d * F / ((ms_ca + ms_cb) * 1e-3) / 1e9, 1),
             "transpose_H_ms": round(ms_tr, 4), "transpose_H_GB/s": round(2.0 * T * F / (ms_tr * 1e-3) / 1e9, 1),
-            "peak_fp8_tflops": round(peak8, 1), "peak_kind": "2 x measured bf16 sustained (nominal FP8:BF16 ratio)"}
+            "peak_fp8_tflops": round(peak8, 1),
+            "peak_kind": f"measured {peak8_kind} (the nominal dense FP8 : BF16 ratio is 2)"}
 
 
 def run_attention(step, torch, binding, pk):
@@ -577,7 +682,7 @@ def run_attention(step, torch, binding, pk):
     core_bwd_flops = 2.5 * core_flops                          # Q K^T, dO V^T, P^T dO, dS K, dS^T Q
     gemm_flops = 2.0 * T * d * 3 * d + 2.0 * T * d * d
     gemm_bwd_flops = 2.0 * gemm_flops                          # data and weight gradients of both projections
-    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    peak = tensor_peak(pk, 0.0)[0]  # ten calls of each: the burst peak
     tf = lambda f, ms: round(f / (ms * 1e-3) / 1e12, 1)
     return {"workload": f"S={S} x B={B}, d={d}, {H} heads of 128 over N={N} shards, causal",
             "block_ms": round(ms_blk, 4), "block_TFLOP/s": tf(core_flops + gemm_flops, ms_blk),
@@ -588,7 +693,8 @@ def run_attention(step, torch, binding, pk):
             "core_bwd_frac": round(core_bwd_flops / (ms_core_b * 1e-3) / 1e12 / peak, 3)}
 
 
-OTHER_ROWS = ("reduce_scatter_explicit", "rmsnorm_gather", "layernorm_gather_isolated", "gemm2_bias_dropout_add",
+OTHER_ROWS = ("reduce_scatter_explicit", "rmsnorm_gather", "layernorm_gather_isolated", "layernorm_backward_isolated",
+              "gemm2_bias_dropout_add",
               "dropout_backward", "layernorm_gather_long_sequence", "fp8", "attention_tp", "fp32_tiny_forward")
 
 
@@ -605,16 +711,15 @@ def run_other_rows(step, torch, binding, pk, only=None):
         Yc = [torch.empty(w.T // w.N, w.d, dtype=torch.bfloat16, device="cuda") for _ in range(w.N)]
         g = 2.0 * w.T * w.d * w.F
         ms_p = time_calls(torch, lambda: binding.tpmlp_gemm2_partials(step.H, step.B, w.N, P), 10)
-        ms_rs = time_calls(torch, lambda: binding.tpmlp_reduce_scatter(P, w.N, Yc), 20)
+        rs = lambda: binding.tpmlp_reduce_scatter(P, w.N, Yc)
+        ms_rs, ms_rs_e = time_graph(torch, rs, 20), time_calls(torch, rs, 20)
         rs_bytes = (w.N + 1) * w.T * w.d * 2.0
         out["gemm2_partials"] = {"ms": round(ms_p, 4), "TFLOP/s": round(g / (ms_p * 1e-3) / 1e12, 1),
-                                 "frac": round(g / (ms_p * 1e-3) / 1e12 / pk.get("bf16_tflops_sustained",
-                                                                                  pk["bf16_tflops"]), 3)}
-        out["reduce_scatter_explicit"] = {"ms": round(ms_rs, 4), "GB/s": round(rs_bytes / (ms_rs * 1e-3) / 1e9, 1),
-                                          "frac": round(rs_bytes / (ms_rs * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
-                                          "bytes_per_launch": rs_bytes}
+                                 "frac": round(g / (ms_p * 1e-3) / 1e12 / tensor_peak(pk, 0.0)[0], 3)}
+        out["reduce_scatter_explicit"] = hbm_row(rs_bytes, ms_rs, ms_rs_e, pk)
         del P, Yc
-    if (want("rmsnorm_gather") or want("layernorm_gather_isolated")) and w.sp and w.backward:
+    if (want("rmsnorm_gather") or want("layernorm_gather_isolated") or want("layernorm_backward_isolated")) and \
+            w.sp and w.backward:
         # the RMS norm variant of the gathered norm, and the LayerNorm beside it timed the same way; the calls
         # alternate between (X -> Xg) and (dY -> dXg) so each reads 2 T d bytes the previous call did not touch
         # (256 MB of inputs and outputs in all, about twice the L2)
@@ -623,18 +728,26 @@ def run_other_rows(step, torch, binding, pk, only=None):
                          ("layernorm_gather_isolated", binding.tpmlp_layernorm_gather)):
             extra = (step.gamma,) if name.startswith("rms") else (step.gamma, step.beta)
             pair = lambda: (fn(step.Xc, *extra, w.N, step.Xg), fn(step.dYc, *extra, w.N, step.dXg))
-            ms = time_calls(torch, pair, 20) / 2.0
-            out[name] = {"ms": round(ms, 4), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
-                         "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes_per_launch": nb}
+            out[name] = hbm_row(nb, time_graph(torch, pair, 20) / 2.0, time_calls(torch, pair, 20) / 2.0, pk)
+        # the LayerNorm backward alone, two sets of operands alternating (402 MB, three times the L2)
+        nbb = 6.0 * w.T * w.d
+        Xg2, dXc2 = torch.empty_like(step.Xg), [torch.empty_like(c) for c in step.dXc]
+        Xg2.copy_(step.dXg)
+        pair_b = lambda: (binding.tpmlp_layernorm_backward(step.Xc, step.gamma, step.dXg, w.N, step.dXc, step.dgamma,
+                                                           step.dbeta, ws=step.lnws),
+                          binding.tpmlp_layernorm_backward(step.dYc, step.gamma, Xg2, w.N, dXc2, step.dgamma,
+                                                           step.dbeta, ws=step.lnws))
+        out["layernorm_backward_isolated"] = hbm_row(nbb, time_graph(torch, pair_b, 10) / 2.0,
+                                                     time_calls(torch, pair_b, 10) / 2.0, pk, launches=2)
+        del Xg2, dXc2
         # the same bytes moved by a plain device copy (torch), timed the same way: what a launch of this size
         # reaches, beside the bandwidth peak measured on a 4 GB copy
         src_a, src_b = torch.empty_like(step.Xg), torch.empty_like(step.dXg)
         src_a.zero_(), src_b.zero_()
-        ms_c = time_calls(torch, lambda: (step.Xg.copy_(src_a), step.dXg.copy_(src_b)), 20) / 2.0
-        out["copy_same_bytes"] = {"ms": round(ms_c, 4), "GB/s": round(nb / (ms_c * 1e-3) / 1e9, 1),
-                                  "frac": round(nb / (ms_c * 1e-3) / 1e9 / pk["hbm_gbs"], 3), "bytes_per_launch": nb,
-                                  "what": "torch copy_ of one [T x d] bf16 tensor into another, alternating two "
-                                          "pairs as the norm rows do"}
+        cp = lambda: (step.Xg.copy_(src_a), step.dXg.copy_(src_b))
+        out["copy_same_bytes"] = hbm_row(nb, time_graph(torch, cp, 20) / 2.0, time_calls(torch, cp, 20) / 2.0, pk,
+                                         what="torch copy_ of one [T x d] bf16 tensor into another, alternating two "
+                                              "pairs as the norm rows do")
         del src_a, src_b
     if (want("gemm2_bias_dropout_add") or want("dropout_backward")) and w.sp:
         # the rest of the sequence-parallel region on the step's shapes: the row-parallel GEMM with row bias,
@@ -644,8 +757,7 @@ def run_other_rows(step, torch, binding, pk, only=None):
         ms_t = time_calls(torch, lambda: binding.tpmlp_gemm2_bias_dropout_add(
             step.H, step.B, w.N, step.Yc, bias2=b2, p=0.1, seed=1, offset=2, R_chunks=step.Xc), 10)
         out["gemm2_bias_dropout_add"] = {"ms": round(ms_t, 4), "TFLOP/s": round(g / (ms_t * 1e-3) / 1e12, 1),
-                                         "frac": round(g / (ms_t * 1e-3) / 1e12 / pk.get("bf16_tflops_sustained",
-                                                                                          pk["bf16_tflops"]), 3)}
+                                         "frac": round(g / (ms_t * 1e-3) / 1e12 / tensor_peak(pk, 0.0)[0], 3)}
         if w.backward:
             db2 = torch.empty(w.d, dtype=torch.bfloat16, device="cuda")
             dws = binding.workspace(binding.make_shape(w.T, w.d, w.F, w.N), binding.OP_DROPOUT_BWD)
@@ -654,7 +766,7 @@ def run_other_rows(step, torch, binding, pk, only=None):
                                                            offset=2, ws=dws),
                             binding.tpmlp_dropout_backward(step.Yc, w.N, step.Xg, dbias2=db2, p=0.1, seed=1,
                                                            offset=3, ws=dws))
-            ms_d = time_calls(torch, pair, 20) / 2.0
+            ms_d = time_graph(torch, pair, 20) / 2.0
             # with the keep mask the forward saved (one bit per element, read instead of regenerated)
             masks = []
             for off in (2, 3):
@@ -666,13 +778,12 @@ def run_other_rows(step, torch, binding, pk, only=None):
                                                              offset=2, ws=dws, keep_mask=masks[0]),
                               binding.tpmlp_dropout_backward(step.Yc, w.N, step.Xg, dbias2=db2, p=0.1, seed=1,
                                                              offset=3, ws=dws, keep_mask=masks[1]))
-            ms_m = time_calls(torch, pair_m, 20) / 2.0
             nbm = nb + w.T * w.d / 8.0
-            out["dropout_backward"] = {"ms": round(ms_m, 4), "GB/s": round(nbm / (ms_m * 1e-3) / 1e9, 1),
-                                       "frac": round(nbm / (ms_m * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
-                                       "bytes_per_launch": nbm, "launches": 2, "keep_mask": "saved by the forward",
-                                       "regenerated_mask_ms": round(ms_d, 4),
-                                       "regenerated_mask_frac": round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
+            out["dropout_backward"] = hbm_row(nbm, time_graph(torch, pair_m, 20) / 2.0,
+                                              time_calls(torch, pair_m, 20) / 2.0, pk, launches=2,
+                                              keep_mask="saved by the forward",
+                                              regenerated_mask_ms=round(ms_d, 4),
+                                              regenerated_mask_frac=round(nb / (ms_d * 1e-3) / 1e9 / pk["hbm_gbs"], 3))
     if want("layernorm_gather_long_sequence") and w.sp and w.d in (1024, 2048, 4096):
         # the LayerNorm forward on a sequence 8x as long (same d): enough rows per warp for the persistent,
         # software-pipelined kernel, whose start-up the step's 8192 rows do not amortise
@@ -682,11 +793,8 @@ def run_other_rows(step, torch, binding, pk, only=None):
         nb = 4.0 * Tl * w.d
         pair = lambda: [binding.tpmlp_layernorm_gather(list(xl[k].split(Tl // w.N)), step.gamma, step.beta, w.N, yl[k])
                         for k in range(2)]
-        ms = time_calls(torch, pair, 10) / 2.0
-        out["layernorm_gather_long_sequence"] = {"tokens": Tl, "ms": round(ms, 4),
-                                                 "GB/s": round(nb / (ms * 1e-3) / 1e9, 1),
-                                                 "frac": round(nb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
-                                                 "bytes_per_launch": nb}
+        out["layernorm_gather_long_sequence"] = hbm_row(nb, time_graph(torch, pair, 10) / 2.0,
+                                                        time_calls(torch, pair, 10) / 2.0, pk, tokens=Tl)
         del xl, yl
     if want("fp8") and (w.sp and w.backward and w.T % 16 == 0 and w.d % 16 == 0 and w.F % 16 == 0 and
             w.d in (256, 512, 1024, 2048, 4096, 8192)):
@@ -703,6 +811,108 @@ def run_other_rows(step, torch, binding, pk, only=None):
     ms = time_calls(torch, lambda: binding.tpmlp_forward(X, A, B, b, t.N, Y, ws=ws), 200)
     out["fp32_tiny_forward"] = {"us": round(ms * 1e3, 2), "GFLOP/s": round(4.0 * t.T * t.d * t.F / (ms * 1e-3) / 1e9, 1),
                                 "workload": t.name, "bound": "launch latency (2 launches of a few CTAs)"}
+    return out
+
+
+def timed_passes(step, torch, steps, gpu_index, barrier=lambda: None):
+    """Time `steps` back-to-back steps with an event at every step boundary (the step's kernels follow one
+    another with nothing between them), then, after a pause, the same number of steps with an event between
+    consecutive kernels for the per-kernel breakdown.  SM clocks are sampled throughout."""
+    nseg = len(step.kernels())
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    step_ev = [ev() for _ in range(steps + 1)]
+    seg_ev = [[ev() for _ in range(nseg + 1)] for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        time.sleep(0.3)
+        t0 = time.perf_counter()
+        e0 = time.time()
+        step_ev[0].record()
+        for k in range(steps):
+            step.run()
+            step_ev[k + 1].record()
+        torch.cuda.synchronize()
+        e1 = time.time()
+        wall = time.perf_counter() - t0
+        time.sleep(1.0)  # the clocks recover from the timed steps' load before the breakdown
+        b0 = time.time()
+        for k in range(steps):
+            step.run(seg_ev[k])
+        torch.cuda.synchronize()
+        b1 = time.time()
+        time.sleep(0.15)
+    barrier()
+    step_ms = [step_ev[k].elapsed_time(step_ev[k + 1]) for k in range(steps)]
+    seg_ms = [sum(seg_ev[k][i].elapsed_time(seg_ev[k][i + 1]) for k in range(steps)) / steps for i in range(nseg)]
+    return {"step_ms": step_ms, "total_ms": step_ev[0].elapsed_time(step_ev[steps]), "seg_ms": seg_ms,
+            "clocks": clk.summary(e0, e1), "clocks_breakdown": clk.summary(b0, b1), "wall": wall}
+
+
+def kernel_table(step, seg_ms, pk, region_s, sm_count, sm_mhz, workload_key):
+    """Per-segment rates: GEMMs in TFLOP/s against the tensor peak that fits the region's length and against
+    the peak at the clock the run held; row kernels in GB/s of algorithmic bytes against measured HBM.  Also
+    the dominant (longest) GEMM: (name, ms, flops, TFLOP/s, peak, peak kind, clock peak)."""
+    peak, kind = tensor_peak(pk, region_s)
+    cpk = clock_peak(sm_count, sm_mhz)
+    kern, dom = {}, None
+    for (name, nl, work, unit), avg in zip(step.kernels(), seg_ms):
+        if unit == "F":
+            ach = work / (avg * 1e-3) / 1e12
+            kern[name] = {"ms": round(avg, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / peak, 3),
+                          "frac_clock": round(ach / cpk, 3) if cpk else None,
+                          "dram_bytes": measured_traffic(name, workload_key)}
+            if dom is None or avg > dom[1]:
+                dom = (name, avg, work, ach, peak, kind, cpk)
+        else:
+            ach = work / (avg * 1e-3) / 1e9
+            kern[name] = {"ms": round(avg, 4), "GB/s": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 3),
+                          "launches": nl, "dram_bytes": measured_traffic(name, workload_key)}
+    return kern, dom
+
+
+FORWARD_ROWS = ("mlp7b_fwd", "sp_large_fwd")
+
+
+def run_forward_row(name, torch, binding, pk, gpu_index, steps=30, warmup=3):
+    """A forward-only workload timed like the step: the 7B-shaped MLP forward (T = 8192, d = 4096,
+    F = 16384) or the d = 8192 sequence-parallel forward (T = 4096 in 512-row chunks, F = 32768).  Inputs are
+    drawn on the device with torch's seeded generator, the workload's distributions."""
+    w = inputs.WORKLOADS[name]
+    step = Step(w, torch, binding, seed=0, on_device=True)
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    r = timed_passes(step, torch, steps, gpu_index)
+    sms = torch.cuda.get_device_properties(gpu_index).multi_processor_count
+    region_s = r["total_ms"] * 1e-3
+    kern, dom = kernel_table(step, r["seg_ms"], pk, region_s, sms, r["clocks_breakdown"].get("sm_mhz"), w.name)
+    flops = useful_flops(w)
+    ms = r["total_ms"] / steps
+    peak, kind = tensor_peak(pk, region_s)
+    cpk = clock_peak(sms, r["clocks"].get("sm_mhz"))
+    ach = flops / (ms * 1e-3) / 1e12
+    ln = None
+    if w.sp:
+        # the gathered LayerNorm alone at this shape, two buffer sets alternating, in a CUDA graph
+        X2, Xg2 = torch.empty_like(step.X).normal_(), torch.empty_like(step.Xg)
+        X2c = list(X2.split(step.rows))
+        pair = lambda: (binding.tpmlp_layernorm_gather(step.Xc, step.gamma, step.beta, w.N, step.Xg),
+                        binding.tpmlp_layernorm_gather(X2c, step.gamma, step.beta, w.N, Xg2))
+        ln = hbm_row(4.0 * w.T * w.d, time_graph(torch, pair, 20) / 2.0, time_calls(torch, pair, 20) / 2.0, pk,
+                     rows_per_chunk=step.rows)
+        del X2, Xg2, X2c
+    out = {"workload": f"{w.name}: T={w.T} ({w.batch} x {w.seq}), d={w.d}, F={w.F}, N={w.N}"
+                       + (f", LayerNorm on {w.T // w.N}-row chunks" if w.sp else ""),
+           "steps": steps, "ms_per_step": round(ms, 4), "step_ms": percentiles(r["step_ms"]),
+           "TFLOP/s": round(ach, 1), "frac": round(ach / peak, 3), "peak_kind": f"measured bf16 {kind}",
+           "frac_clock": round(ach / cpk, 3) if cpk else None, "tokens_per_s": round(w.T / (ms * 1e-3), 1),
+           "kernels": kern, "clocks": r["clocks"], "inputs": "torch seeded device generator, the recipe's "
+                                                            "distributions"}
+    if ln is not None:
+        out["layernorm_gather_isolated"] = ln
+    del step
+    torch.cuda.empty_cache()
     return out
 
 
@@ -728,9 +938,7 @@ def run_ours(args, w):
     binding.lib()
 
     step = Step(w, torch, binding)
-    segs = step.kernels()
-    nseg = len(segs)
-    stream = torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
 
     for _ in range(args.warmup):
         step.run()
@@ -739,37 +947,8 @@ def run_ours(args, w):
     if st != binding.OK:
         raise RuntimeError(f"device status after warm-up: {binding.status_string(st)} (site {site})")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)] for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        time.sleep(0.3)
-        t0 = time.perf_counter()
-        e0 = time.time()
-        # the timed steps: kernels back to back (an event between two kernels would keep the second from
-        # overlapping its launch with the first's tail)
-        t_start.record()
-        for k in range(args.steps):
-            step.run()
-        t_end.record()
-        torch.cuda.synchronize()
-        e1 = time.time()
-        wall = time.perf_counter() - t0
-        time.sleep(1.0)  # the clocks recover from the timed steps' load before the breakdown
-        # the per-kernel breakdown: the same number of steps with an event between consecutive kernels
-        for k in range(args.steps):
-            step.run(events[k])
-        torch.cuda.synchronize()
-        time.sleep(0.15)
-    if dist is not None:
-        dist.barrier()
-    seg_ms = [0.0] * nseg
-    for k in range(args.steps):
-        for i in range(nseg):
-            seg_ms[i] += events[k][i].elapsed_time(events[k][i + 1])
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist)
+    r = timed_passes(step, torch, args.steps, local, barrier=(dist.barrier if dist is not None else lambda: None))
+    total_ms = max_over_ranks(r["total_ms"], dist)
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after timing: {binding.status_string(st)} (site {site})")
@@ -778,32 +957,32 @@ def run_ours(args, w):
     flops = useful_flops(w)
     value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
     tokens_per_s = whole_job_rate(w.T, args.steps, world, total_ms)
+    clocks = r["clocks"]
+    region_s = r["total_ms"] * 1e-3
+    kern, dom = kernel_table(step, r["seg_ms"], pk, region_s, sms, r["clocks_breakdown"].get("sm_mhz"), w.name)
 
-    kern = {}
-    dom = None
-    for (name, nl, work, unit), ms in zip(segs, seg_ms):
-        avg = ms / args.steps
-        if unit == "F":
-            ach = work / (avg * 1e-3) / 1e12
-            peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-            kern[name] = {"ms": round(avg, 4), "TFLOP/s": round(ach, 1), "frac": round(ach / peak, 3),
-                          "dram_bytes": measured_traffic(name, w.name)}
-            if dom is None or avg > dom[1]:
-                dom = (name, avg, work, ach, peak)
-        else:
-            ach = work / (avg * 1e-3) / 1e9
-            kern[name] = {"ms": round(avg, 4), "GB/s": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 3),
-                          "launches": nl, "dram_bytes": measured_traffic(name, w.name)}
     if args.only_row is None:
         e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
         st, site = binding.tpmlp_get_device_status()
         if st != binding.OK:
             raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
         e2e_ms = max_over_ranks(e2e_ms, dist)
-    other = run_other_rows(step, torch, binding, peaks()[0], only=args.only_row)
+    other = run_other_rows(step, torch, binding, pk, only=args.only_row)
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after the other rows: {binding.status_string(st)} (site {site})")
+    if world == 1 and not args.no_forward_rows:
+        # the forward-only workloads that carry the d = 4096 / 8192 forward GEMM rates and the LayerNorm at
+        # 512-row chunks; the step's buffers are released first (the d = 8192 weights take 1 GiB)
+        keep = (w.name, w.T, w.d, w.F)
+        del step
+        torch.cuda.empty_cache()
+        for name in FORWARD_ROWS:
+            if (args.only_row is None or args.only_row == name) and name != keep[0]:
+                other[name] = run_forward_row(name, torch, binding, pk, local)
+        st, site = binding.tpmlp_get_device_status()
+        if st != binding.OK:
+            raise RuntimeError(f"device status after the forward rows: {binding.status_string(st)} (site {site})")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only_row is None:
@@ -813,23 +992,30 @@ def run_ours(args, w):
                "tokens_per_s": tok / dt, "seconds": round(dt, 2),
                "sample": f"{tok} of {w.T} tokens through the fp64 oracle with the full d={w.d}, F={w.F} weights "
                          f"(numpy float64, BLAS matmul on {cores} threads)"}
-    clocks = clk.summary(e0, e1)
     if rank != 0:
         dist.destroy_process_group() if dist is not None else None
         return
+    launches = sum(n for _, n, _, _ in Step.kernels_of(w)) * args.steps
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "tokens_per_s": round(tokens_per_s, 1),
+        "step_ms": percentiles(r["step_ms"]),
         "config": {"workload": w.name, "tokens": w.T, "batch": w.batch, "seq": w.seq, "d": w.d, "ffn": w.F,
                    "n_shards": w.N, "sequence_parallel": w.sp, "backward": w.backward,
                    "parallelism": f"tp{w.N} shards on one GPU" + (f", {world} replicas" if world > 1 else ""),
                    "l2": "inputs larger than L2 (weights alone 2 x d x F x 2 bytes)",
-                   "host_wall_s": round(wall, 3)},
+                   "host_wall_s": round(r["wall"], 3)},
         "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": round(dom[3], 1), "peak": dom[4],
-                     "unit": "TFLOP/s", "frac": round(dom[3] / dom[4], 3), "traffic": measured_traffic(dom[0], w.name),
-                     "peak_kind": f"{pk_kind} bf16 sustained"},
+                     "unit": "TFLOP/s", "frac": round(dom[3] / dom[4], 3),
+                     "traffic": measured_traffic(dom[0], w.name),
+                     "peak_kind": f"{pk_kind} bf16 {dom[5]} (timed region {region_s:.3f} s; the sustained peak "
+                                  f"from {SUSTAINED_AFTER_S:g} s)",
+                     "clock_peak": round(dom[6], 1) if dom[6] else None,
+                     "frac_clock": round(dom[3] / dom[6], 3) if dom[6] else None,
+                     "clock_peak_kind": f"{BF16_FLOP_PER_CLK_SM:g} flop/clk/SM x {sms} SMs x the median SM clock "
+                                        "sampled during the breakdown pass"},
         "kernels": kern,
         "e2e": {"value": round(whole_job_rate(flops, args.steps, world, e2e_ms * args.steps) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
@@ -837,7 +1023,7 @@ def run_ours(args, w):
                 "what": e2e_what(w)}
                if args.only_row is None else {"skipped": "--only-row " + args.only_row},
         "other_rows": other,
-        "gpu_launches": step.launches_per_step() * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     if cpu is not None:
@@ -856,7 +1042,9 @@ def main():
     ap.add_argument("--workload", default="sp_block_fwd_bwd", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--oracle-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only-row", choices=OTHER_ROWS, default=None,
+    ap.add_argument("--no-forward-rows", action="store_true",
+                    help="skip the forward-only 7B and d=8192 rows timed after the step")
+    ap.add_argument("--only-row", choices=OTHER_ROWS + FORWARD_ROWS, default=None,
                     help="after the step, time only this row of other_rows (no e2e, no CPU baseline): for profiling")
     args = ap.parse_args()
     w = inputs.WORKLOADS[args.workload]

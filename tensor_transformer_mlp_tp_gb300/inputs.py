@@ -60,10 +60,14 @@ def uniforms(key: int, start: int, count: int) -> np.ndarray:
 
 
 def normals(key: int, n: int) -> np.ndarray:
-    """``n`` standard normal doubles from the stream ``key`` (Box-Muller, pairs of counters)."""
+    """``n`` standard normal doubles from the stream ``key`` (Box-Muller, pairs of counters).
+
+    Blocks of counters are independent, so large draws run their blocks on a thread pool (numpy's
+    array operations release the interpreter lock); the values do not depend on the block order."""
     out = np.empty(n, dtype=np.float64)
     pairs = (n + 1) // 2
-    for p0 in range(0, pairs, _BLOCK):
+
+    def block(p0):
         p1 = min(pairs, p0 + _BLOCK)
         u = uniforms(key, 2 * p0, 2 * (p1 - p0))
         u1 = 1.0 - u[0::2]                      # (0, 1]: log is finite
@@ -76,6 +80,17 @@ def normals(key: int, n: int) -> np.ndarray:
         lo = 2 * p0
         hi = min(n, 2 * p1)
         out[lo:hi] = z[: hi - lo]
+
+    starts = range(0, pairs, _BLOCK)
+    if len(starts) <= 1:
+        for p0 in starts:
+            block(p0)
+        return out
+    import concurrent.futures as cf
+    import os
+
+    with cf.ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 1, 32)) as ex:
+        list(ex.map(block, starts))
     return out
 
 
