@@ -533,7 +533,12 @@ def time_calls(torch, fn, reps, warmup=3):
     return e0.elapsed_time(e1) / reps
 
 
-def time_graph(torch, fn, reps, warmup=3):
+# Pause before a row kernel is timed alone: after seconds of GEMMs the GPU sits at its power cap and its SM
+# clock needs about 100 ms to recover, and the row kernels' time follows the SM clock.
+SETTLE_S = 0.3
+
+
+def time_graph(torch, fn, reps, warmup=3, settle=SETTLE_S):
     """Average ms of `fn` over `reps` back-to-back calls captured in one CUDA graph and replayed: the kernels'
     own time without the host's launch cost between them (a Python call through the C ABI takes about
     15 us of host time, more than half of a 25 us row kernel)."""
@@ -550,6 +555,7 @@ def time_graph(torch, fn, reps, warmup=3):
             fn()
     g.replay()
     torch.cuda.synchronize()
+    time.sleep(settle)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     g.replay()
@@ -961,13 +967,16 @@ def run_ours(args, w):
     region_s = r["total_ms"] * 1e-3
     kern, dom = kernel_table(step, r["seg_ms"], pk, region_s, sms, r["clocks_breakdown"].get("sm_mhz"), w.name)
 
+    if args.step_only:
+        # profiling runs: the timed step and its breakdown only
+        args.only_row, args.no_forward_rows, args.no_cpu_baseline = "none", True, True
     if args.only_row is None:
         e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
         st, site = binding.tpmlp_get_device_status()
         if st != binding.OK:
             raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
         e2e_ms = max_over_ranks(e2e_ms, dist)
-    other = run_other_rows(step, torch, binding, pk, only=args.only_row)
+    other = run_other_rows(step, torch, binding, pk, only=args.only_row) if args.only_row != "none" else {}
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after the other rows: {binding.status_string(st)} (site {site})")
@@ -1021,7 +1030,7 @@ def run_ours(args, w):
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "what": e2e_what(w)}
-               if args.only_row is None else {"skipped": "--only-row " + args.only_row},
+               if args.only_row is None else {"skipped": "--step-only" if args.step_only else "--only-row " + args.only_row},
         "other_rows": other,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -1042,6 +1051,9 @@ def main():
     ap.add_argument("--workload", default="sp_block_fwd_bwd", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--oracle-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the step and its per-kernel breakdown only (no e2e, other rows or CPU baseline): for "
+                         "profiling")
     ap.add_argument("--no-forward-rows", action="store_true",
                     help="skip the forward-only 7B and d=8192 rows timed after the step")
     ap.add_argument("--only-row", choices=OTHER_ROWS + FORWARD_ROWS, default=None,

@@ -101,35 +101,6 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
   }
 }
 
-// Non-blocking test of a phase (the thread is never suspended).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// wait_bounded by polling with test_wait instead of a suspended try_wait: for waits that usually end
-// within a few hundred cycles, where a suspended thread's wake-up would add its own latency.  Same limit,
-// abort flag and error reporting.
-__device__ __forceinline__ bool wait_bounded_spin(uint64_t* bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if (*w.abort) return false;
-    if (global_timer_ns() - t0 > w.budget_ns) {
-      record_error(w, kErrTimeout, site);
-      return false;
-    }
-  }
-}
-
 // Teardown wait: same limit, but ignores the abort flag (used to drain
 // copies or MMAs still in flight before shared memory or TMEM is released).
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
