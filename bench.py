@@ -820,6 +820,19 @@ def run_other_rows(step, torch, binding, pk, only=None):
     return out
 
 
+class nvtx_range:
+    """An NVTX range around a bench phase (visible to profilers; no effect on the timing)."""
+
+    def __init__(self, torch, name):
+        self.torch, self.name = torch, name
+
+    def __enter__(self):
+        self.torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        self.torch.cuda.nvtx.range_pop()
+
+
 def timed_passes(step, torch, steps, gpu_index, barrier=lambda: None):
     """Time `steps` back-to-back steps with an event at every step boundary (the step's kernels follow one
     another with nothing between them), then, after a pause, the same number of steps with an event between
@@ -834,18 +847,20 @@ def timed_passes(step, torch, steps, gpu_index, barrier=lambda: None):
         time.sleep(0.3)
         t0 = time.perf_counter()
         e0 = time.time()
-        step_ev[0].record()
-        for k in range(steps):
-            step.run()
-            step_ev[k + 1].record()
-        torch.cuda.synchronize()
+        with nvtx_range(torch, f"{step.w.name}: {steps} timed steps"):
+            step_ev[0].record()
+            for k in range(steps):
+                step.run()
+                step_ev[k + 1].record()
+            torch.cuda.synchronize()
         e1 = time.time()
         wall = time.perf_counter() - t0
         time.sleep(1.0)  # the clocks recover from the timed steps' load before the breakdown
         b0 = time.time()
-        for k in range(steps):
-            step.run(seg_ev[k])
-        torch.cuda.synchronize()
+        with nvtx_range(torch, f"{step.w.name}: per-kernel breakdown"):
+            for k in range(steps):
+                step.run(seg_ev[k])
+            torch.cuda.synchronize()
         b1 = time.time()
         time.sleep(0.15)
     barrier()
@@ -971,12 +986,14 @@ def run_ours(args, w):
         # profiling runs: the timed step and its breakdown only
         args.only_row, args.no_forward_rows, args.no_cpu_baseline = "none", True, True
     if args.only_row is None:
-        e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
+        with nvtx_range(torch, "e2e through the block calls"):
+            e2e_ms, h2d, d2h = run_e2e(step, args, torch, binding)
         st, site = binding.tpmlp_get_device_status()
         if st != binding.OK:
             raise RuntimeError(f"device status after e2e: {binding.status_string(st)} (site {site})")
         e2e_ms = max_over_ranks(e2e_ms, dist)
-    other = run_other_rows(step, torch, binding, pk, only=args.only_row) if args.only_row != "none" else {}
+    with nvtx_range(torch, "other rows"):
+        other = run_other_rows(step, torch, binding, pk, only=args.only_row) if args.only_row != "none" else {}
     st, site = binding.tpmlp_get_device_status()
     if st != binding.OK:
         raise RuntimeError(f"device status after the other rows: {binding.status_string(st)} (site {site})")
@@ -988,7 +1005,8 @@ def run_ours(args, w):
         torch.cuda.empty_cache()
         for name in FORWARD_ROWS:
             if (args.only_row is None or args.only_row == name) and name != keep[0]:
-                other[name] = run_forward_row(name, torch, binding, pk, local)
+                with nvtx_range(torch, f"forward row {name}"):
+                    other[name] = run_forward_row(name, torch, binding, pk, local)
         st, site = binding.tpmlp_get_device_status()
         if st != binding.OK:
             raise RuntimeError(f"device status after the forward rows: {binding.status_string(st)} (site {site})")
@@ -1042,6 +1060,10 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+# The five configurations in their listed order.
+CONFIGS = {1: "tiny_fp32_fwd", 2: "gpt2_medium_fwd", 3: "mlp7b_fwd", 4: "sp_block_fwd_bwd", 5: "sp_large_fwd"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1049,6 +1071,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sp_block_fwd_bwd", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--config", type=int, choices=sorted(CONFIGS), default=None,
+                    help="select the workload by its number in the list of configurations (1 tiny fp32, 2 GPT-2-"
+                         "medium, 3 7B, 4 SP block forward+backward, 5 d=8192 SP forward)")
     ap.add_argument("--oracle-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step-only", action="store_true",
@@ -1059,9 +1084,12 @@ def main():
     ap.add_argument("--only-row", choices=OTHER_ROWS + FORWARD_ROWS, default=None,
                     help="after the step, time only this row of other_rows (no e2e, no CPU baseline): for profiling")
     args = ap.parse_args()
+    if args.config is not None:
+        args.workload = CONFIGS[args.config]
     w = inputs.WORKLOADS[args.workload]
     if w.dtype != "bf16":
-        raise SystemExit("bench.py measures the bf16 workloads")
+        raise SystemExit("bench.py times the bf16 workloads; the fp32 configuration (tiny_fp32_fwd) is the "
+                         "other_rows.fp32_tiny_forward row of every run")
     if args.impl == "reference":
         run_reference(args, w)
     else:

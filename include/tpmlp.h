@@ -141,6 +141,18 @@ TPMLP_API tpmlp_status tpmlp_workspace_size(const tpmlp_shape* shape, int op, si
  * TPMLP_ERR_CUDA if the stream reports a CUDA error, else TPMLP_OK. */
 TPMLP_API tpmlp_status tpmlp_get_device_status(tpmlp_stream_t stream, uint32_t* site);
 
+/* Debug builds (compiled with -DTPMLP_DEBUG_BOUNDS; the tests build one
+ * beside the release library) check the hand-computed global indices of the
+ * row kernels and of the GEMM epilogues' direct stores against the extents of
+ * their buffers, count every index found outside, record the site of the
+ * first one, and skip (stores) or redirect to the first row (loads) that
+ * access.  This call synchronises the device, sets *checked to 1 in such a
+ * build and 0 in a release build (which checks nothing), and returns the
+ * violations counted since the previous call and the first site (0 if none);
+ * it clears both.  There is no counterpart on the pages: it is the library's
+ * stand-in for a memory checker. */
+TPMLP_API tpmlp_status tpmlp_debug_bounds_status(int32_t* checked, uint32_t* violations, uint32_t* first_site);
+
 /* ------------------------------------------------------------------ block calls */
 
 /* Tensor-parallel MLP forward ("6D" guide §3.1; deep-dive page, column/row

@@ -14,7 +14,9 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtpmlp.so")
+# The in-tree library; TPMLP_LIBRARY may name another build of it (the tests load the bounds-checked debug
+# build, libtpmlp_debug.so beside this file, that way in a process of their own).
+_LIB_PATH = os.environ.get("TPMLP_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtpmlp.so")
 _lib = None
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
@@ -74,6 +76,8 @@ _SIGS = {
     "tpmlp_layernorm_backward": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P, ctypes.c_size_t, _P],
                                  ctypes.c_int),
     "tpmlp_layernorm_backward_noalloc": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, _P], ctypes.c_int),
+    "tpmlp_debug_bounds_status": ([ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_uint32),
+                                   ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "tpmlp_layernorm_backward_blocks": ([_PP, _P, ctypes.c_float, _P, _SP, _PP, _P, _P, ctypes.c_int32, _P,
                                          ctypes.c_size_t, _P], ctypes.c_int),
     "tpmlp_selftest_wait_timeout": ([ctypes.c_uint32, _P], ctypes.c_int),
@@ -195,6 +199,15 @@ def tpmlp_workspace_size(shape: Shape, op: int) -> int:
 def workspace(shape: Shape, op: int, device=None) -> torch.Tensor:
     """A device buffer large enough for `op` (torch allocation; contents undefined)."""
     return torch.empty(max(tpmlp_workspace_size(shape, op), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def tpmlp_debug_bounds_status():
+    """(checked, violations, first_site): whether this build checks global indices, and what it found since
+    the previous call (cleared)."""
+    c, n, site = ctypes.c_int32(0), ctypes.c_uint32(0), ctypes.c_uint32(0)
+    _check("tpmlp_debug_bounds_status", lib().tpmlp_debug_bounds_status(ctypes.byref(c), ctypes.byref(n),
+                                                                        ctypes.byref(site)))
+    return bool(c.value), n.value, site.value
 
 
 def tpmlp_get_device_status(stream=None):

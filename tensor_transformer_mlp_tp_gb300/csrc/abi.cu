@@ -618,6 +618,22 @@ tpmlp_status tpmlp_get_device_status(tpmlp_stream_t stream, uint32_t* site) {
   return (w[0] & kErrTimeout) ? TPMLP_ERR_TIMEOUT : TPMLP_ERR_CUDA;
 }
 
+tpmlp_status tpmlp_debug_bounds_status(int32_t* checked, uint32_t* violations, uint32_t* first_site) {
+  if (checked == nullptr || violations == nullptr || first_site == nullptr) return TPMLP_ERR_INVALID_ARG;
+  unsigned int c[2] = {0, 0}, site[2] = {0, 0};
+  if (cudaDeviceSynchronize() != cudaSuccess) return TPMLP_ERR_CUDA;
+  if (rowwise_bounds_status(&c[0], &site[0]) != cudaSuccess || gemm_bounds_status(&c[1], &site[1]) != cudaSuccess)
+    return TPMLP_ERR_CUDA;
+#ifdef TPMLP_DEBUG_BOUNDS
+  *checked = 1;
+#else
+  *checked = 0;
+#endif
+  *violations = c[0] + c[1];
+  *first_site = site[0] != 0 ? site[0] : site[1];
+  return TPMLP_OK;
+}
+
 tpmlp_status tpmlp_selftest_wait_timeout(uint32_t budget_us, tpmlp_stream_t stream) {
   if (budget_us < 1 || budget_us > 1000000) return TPMLP_ERR_INVALID_ARG;
   DeviceCtx c;

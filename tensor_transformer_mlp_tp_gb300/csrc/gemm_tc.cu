@@ -201,6 +201,15 @@ static cudaError_t launch_gemm_fp8(const GemmLaunch& g, const DeviceCtx& ctx, cu
   }
 }
 
+cudaError_t gemm_bounds_status(unsigned int* count, unsigned int* site) {
+#ifdef TPMLP_DEBUG_BOUNDS
+  return bounds_read_and_clear(count, site);
+#else
+  *count = *site = 0;
+  return cudaSuccess;
+#endif
+}
+
 cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return cudaSuccess;
   if (g.fp8) return launch_gemm_fp8(g, ctx, s);

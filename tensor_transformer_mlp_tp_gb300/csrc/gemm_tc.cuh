@@ -24,6 +24,7 @@
 // releases its TMEM before exiting.
 #pragma once
 
+#include "debug_bounds.cuh"
 #include "fp8.cuh"
 #include "philox.cuh"
 #include "ptx.cuh"
@@ -266,14 +267,18 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       box_store_bf16_32(&p.tmC0, sbuf, v, lane, col0, row - static_cast<int>(lane), p.M, p.N);
     } else if (row_ok) {
       __nv_bfloat16* dst;
+      bool ok = true;
       if (p.rows_per_chunk > 0) {
         if (p.tail) sp_tail_32(p, v, row, col0);
         const int j = row / p.rows_per_chunk;
-        dst = static_cast<__nv_bfloat16*>(p.chunks.p[j]) + static_cast<long long>(row - j * p.rows_per_chunk) * p.ld0;
+        ok = TPMLP_IN_BOUNDS(j, (p.M + p.rows_per_chunk - 1) / p.rows_per_chunk, kBoundsGemmChunk);
+        dst = static_cast<__nv_bfloat16*>(p.chunks.p[ok ? j : 0]) +
+              static_cast<long long>(row - j * p.rows_per_chunk) * p.ld0;
       } else {
+        ok = TPMLP_IN_BOUNDS(shard, p.shards, kBoundsGemmShard);
         dst = static_cast<__nv_bfloat16*>(p.out0) + shard * p.shard_stride0 + static_cast<long long>(row) * p.ld0;
       }
-      store_row32(dst, col0, p.N, v);
+      if (ok) store_row32(dst, col0, p.N, v);
     }
   } else if constexpr (EPI == kEpiDGeluQ) {
     // v = dH (dequantised); aux = Hpre.  g = dH * GeLU'(Hpre) -> E5M2 with the output scale, amax, column sums.
@@ -297,7 +302,9 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       const int col = col0 + static_cast<int>(lane);
       // a 128-row block that starts at or past row M (the odd CTA of a last, half-empty pair tile) writes
       // nothing: the partial rows stay 4 per 128-row block of M
-      if (col < p.N && mb * kBM < p.M) p.colsum[static_cast<long long>(mb * 4 + quad) * p.N + col] = s;
+      if (col < p.N && mb * kBM < p.M &&
+          TPMLP_IN_BOUNDS(mb * 4 + quad, 4 * ((p.M + kBM - 1) / kBM), kBoundsGemmColsum))
+        p.colsum[static_cast<long long>(mb * 4 + quad) * p.N + col] = s;
     }
   } else if constexpr (EPI == kEpiDGelu) {
     // v = dH = dY B^T; aux = Hpre.  dHpre = dH * (Phi(h) + h phi(h)); with out1 also H = h Phi(h),
@@ -327,7 +334,9 @@ __device__ __forceinline__ void epilogue_32(const GemmParams& p, float (&v)[32],
       const int col = col0 + static_cast<int>(lane);
       // a 128-row block that starts at or past row M (the odd CTA of a last, half-empty pair tile) writes
       // nothing: the partial rows stay 4 per 128-row block of M
-      if (col < p.N && mb * kBM < p.M) p.colsum[static_cast<long long>(mb * 4 + quad) * p.N + col] = s;
+      if (col < p.N && mb * kBM < p.M &&
+          TPMLP_IN_BOUNDS(mb * 4 + quad, 4 * ((p.M + kBM - 1) / kBM), kBoundsGemmColsum))
+        p.colsum[static_cast<long long>(mb * 4 + quad) * p.N + col] = s;
     }
   }
 }

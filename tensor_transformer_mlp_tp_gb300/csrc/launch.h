@@ -60,6 +60,11 @@ struct DeviceCtx {
   int sm_count;
 };
 
+// Bounds-check violations counted by the row kernels' / the GEMMs' translation units since the last call
+// (zero in release builds, which check nothing), and the first site; both cleared.
+cudaError_t rowwise_bounds_status(unsigned int* count, unsigned int* site);
+cudaError_t gemm_bounds_status(unsigned int* count, unsigned int* site);
+
 // Returns cudaErrorNotSupported for operand/epilogue combinations without a kernel.
 cudaError_t launch_gemm(const GemmLaunch& g, const DeviceCtx& ctx, cudaStream_t s);
 

@@ -7,6 +7,7 @@
 // All global traffic is 16-byte vectors; reductions are warp shuffles.
 #include <cuda_bf16.h>
 
+#include "debug_bounds.cuh"
 #include "fp8.cuh"
 #include "launch.h"
 #include "philox.cuh"
@@ -38,16 +39,25 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+// Row `row` of the chunked input (a debug build that finds the row or its chunk out of range counts it and
+// reads the first row instead).
 __device__ __forceinline__ const __nv_bfloat16* chunk_row(const RowParams& p, int row) {
-  const int j = row / p.rows_per_chunk;
+  int j = row / p.rows_per_chunk;
+  if (!(TPMLP_IN_BOUNDS(row, p.rows, kBoundsInChunk) && TPMLP_IN_BOUNDS(j, p.n_chunks, kBoundsInChunk))) j = row = 0;
   return static_cast<const __nv_bfloat16*>(p.in_chunks.p[j]) +
          static_cast<long long>(row - j * p.rows_per_chunk) * p.d;
 }
 
 __device__ __forceinline__ const __nv_bfloat16* add_chunk_row(const RowParams& p, int row) {
-  const int j = row / p.rows_per_chunk;
+  int j = row / p.rows_per_chunk;
+  if (!(TPMLP_IN_BOUNDS(row, p.rows, kBoundsAddChunk) && TPMLP_IN_BOUNDS(j, p.n_chunks, kBoundsAddChunk))) j = row = 0;
   return static_cast<const __nv_bfloat16*>(p.add_chunks.p[j]) +
          static_cast<long long>(row - j * p.rows_per_chunk) * p.d;
+}
+
+// Debug builds: is 16-byte vector `v` of row `row` inside a [rows x d] tensor (a store is skipped if not)?
+__device__ __forceinline__ bool row_vec_ok(const RowParams& p, long long row, long long v, uint32_t site) {
+  return TPMLP_IN_BOUNDS(row, p.rows, site) && TPMLP_IN_BOUNDS(v, p.d / 8, site);
 }
 
 // The sequence-parallel tail on 8 elements of vector q (= element index / 8) of row `row`, column `col`.
@@ -73,8 +83,10 @@ __device__ __forceinline__ void sp_tail_8(const RowParams& p, float (&a)[8], lon
   }
 }
 
+// Row `row` of the chunked output; the stores through it check the row (row_vec_ok), this checks the chunk.
 __device__ __forceinline__ __nv_bfloat16* out_chunk_row(const RowParams& p, int row) {
-  const int j = row / p.rows_per_chunk;
+  int j = row / p.rows_per_chunk;
+  if (!TPMLP_IN_BOUNDS(j, p.n_chunks, kBoundsOutChunk)) j = row = 0;
   return static_cast<__nv_bfloat16*>(p.out_chunks.p[j]) + static_cast<long long>(row - j * p.rows_per_chunk) * p.d;
 }
 
@@ -217,9 +229,9 @@ __global__ void __launch_bounds__(128, V >= 16 ? kLnRegMinBlocks : 1) k_layernor
       if constexpr (Q8) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(o[e]));
-        dst8[idx] = e4m3x8(o, qs);
+        if (row_vec_ok(p, row, idx, kBoundsRowStore)) dst8[idx] = e4m3x8(o, qs);
       } else {
-        dst[idx] = pack8(o);
+        if (row_vec_ok(p, row, idx, kBoundsRowStore)) dst[idx] = pack8(o);
       }
     }
   }
@@ -273,7 +285,7 @@ __device__ __forceinline__ void ln_row_store(const RowParams& p, int row, int la
     unpack8(b4[idx], b);
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
-    dst[idx] = pack8(o);
+    if (row_vec_ok(p, row, idx, kBoundsRowStore)) dst[idx] = pack8(o);
   }
 }
 
@@ -359,7 +371,7 @@ __device__ __forceinline__ void ln_half_store(const RowParams& p, int row, int h
     unpack8(b4[idx], b);
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
-    dst[v * 32 + lane] = pack8(o);
+    if (row_vec_ok(p, row, idx, kBoundsRowStore)) dst[v * 32 + lane] = pack8(o);
   }
 }
 
@@ -442,7 +454,7 @@ __global__ void __launch_bounds__(128) k_layernorm_fwd_any(const RowParams p) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
     }
-    dst[v] = pack8(o);
+    if (row_vec_ok(p, row, v, kBoundsRowStore)) dst[v] = pack8(o);
   }
 }
 
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(256) k_layernorm_bwd(const RowParams p) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] += a[e];
         }
-        dx4[v] = pack8(o);
+        if (row_vec_ok(p, row, v, kBoundsOutChunk)) dx4[v] = pack8(o);
       }
       if (lane == 0) {
         s_mean[warp] = mean;
@@ -581,7 +593,9 @@ __device__ __forceinline__ void stream_producer(const RowParams& p, uint8_t* rin
     bulk_load(ring + slot * slot_bytes, chunk_row(p, row), row_bytes, full + slot);
     if (second)
       bulk_load(ring + slot * slot_bytes + row_bytes,
-                static_cast<const __nv_bfloat16*>(p.src) + static_cast<long long>(row) * p.d, row_bytes, full + slot);
+                static_cast<const __nv_bfloat16*>(p.src) +
+                    static_cast<long long>(TPMLP_IN_BOUNDS(row, p.rows, kBoundsRowLoad) ? row : 0) * p.d,
+                row_bytes, full + slot);
     if (slot < 32) {
       issued_mask |= 1u << slot;
       issued_parity = (issued_parity & ~(1u << slot)) | (ph << slot);
@@ -777,7 +791,7 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
           if constexpr (ADD) dx = __fadd2_rn(dx, bf2(word(av[k], w)));
           o[w] = pack_bf16x2(dx.x, dx.y);
         }
-        dx4[j + k * 32 * TW] = make_uint4(o[0], o[1], o[2], o[3]);
+        if (row_vec_ok(p, row, j + k * 32 * TW, kBoundsOutChunk)) dx4[j + k * 32 * TW] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
@@ -923,7 +937,7 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_fwd_stream(con
         const float2 y = __ffma2_rn(__ffma2_rn(bf2(word(xv[k], w)), a2, b2), g2[w], be2[w]);
         o[w] = pack_bf16x2(y.x, y.y);
       }
-      dst[idx] = make_uint4(o[0], o[1], o[2], o[3]);
+      if (row_vec_ok(p, row, idx, kBoundsRowStore)) dst[idx] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
@@ -942,7 +956,9 @@ __global__ void __launch_bounds__(256) k_reduce_scatter(const RowParams p) {
     for (int e = 0; e < 8; ++e) a[e] = 0.f;
     for (int s = 0; s < p.n_chunks; ++s) {
       float f[8];
-      unpack8(__ldg(src + s * sstride + i), f);
+      // debug builds: shard s's slice of the partials holds exactly rows x d / 8 vectors
+      const long long k = TPMLP_IN_BOUNDS(i, sstride, kBoundsShard) ? s * sstride + i : 0;
+      unpack8(__ldg(src + k), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) a[e] += f[e];
     }
@@ -950,7 +966,7 @@ __global__ void __launch_bounds__(256) k_reduce_scatter(const RowParams p) {
     const int row = static_cast<int>(el / p.d);
     const int col = static_cast<int>(el - static_cast<long long>(row) * p.d);
     if (p.tail) sp_tail_8(p, a, i, row, col);
-    reinterpret_cast<uint4*>(out_chunk_row(p, row) + col)[0] = pack8(a);
+    if (row_vec_ok(p, row, col / 8, kBoundsOutChunk)) reinterpret_cast<uint4*>(out_chunk_row(p, row) + col)[0] = pack8(a);
   }
 }
 
@@ -1018,7 +1034,7 @@ __global__ void __launch_bounds__(32 * kColWarps, KEEP == 2 ? 1 : 5) k_dropout_b
           f[e] = (m >> e) & 1u ? f[e] * p.drop_scale : 0.f;
           acc[e] += f[e];
         }
-        dst[q] = pack8(f);
+        if (row_vec_ok(p, rb + u, v, kBoundsRowStore)) dst[q] = pack8(f);
       }
     }
   }
@@ -1229,6 +1245,19 @@ __global__ void __launch_bounds__(128) k_fp8_update(float* scale, float* amax, f
     }
   }
 }
+
+}  // namespace
+
+cudaError_t rowwise_bounds_status(unsigned int* count, unsigned int* site) {
+#ifdef TPMLP_DEBUG_BOUNDS
+  return bounds_read_and_clear(count, site);
+#else
+  *count = *site = 0;
+  return cudaSuccess;
+#endif
+}
+
+namespace {
 
 int stream_grid(long long work_items, int sm_count) {
   const long long per = 256;

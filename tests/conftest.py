@@ -24,3 +24,17 @@ def read_golden(name):
             if line:
                 rows.append(line.split())
     return rows
+
+
+@pytest.fixture(autouse=True)
+def _debug_bounds_clean(request):
+    """In a run against the bounds-checked debug build (TPMLP_EXPECT_BOUNDS_CHECKED set, as
+    test_gpu_debug_bounds.py sets it for its child pytest), every GPU test must leave the library with no
+    out-of-range global index counted."""
+    yield
+    if os.environ.get("TPMLP_EXPECT_BOUNDS_CHECKED") and request.node.get_closest_marker("gpu") is not None:
+        from tensor_transformer_mlp_tp_gb300 import binding
+
+        checked, violations, site = binding.tpmlp_debug_bounds_status()
+        assert checked, "the loaded library is not the bounds-checked build"
+        assert violations == 0, f"{violations} global indices out of range (first at site {site})"

@@ -5,9 +5,12 @@ rows (for the sequence-parallel block: a sample of rows of every chunk).
 Backward: input-gradient rows are independent too; dA columns and dB rows
 belong to single hidden units, so the oracle recomputes the block restricted
 to a sample of hidden units over all T tokens.  dgamma/dbeta sum over every
-row: they are checked by the oracle's LayerNorm backward applied to the
-GPU's own gathered gradient dXg, whose sampled rows are checked first.
-The smallest workload (GPT-2-medium shape) is checked in full.
+row: at the full size they are checked by the oracle's LayerNorm backward
+applied to the GPU's own gathered gradient dXg, whose sampled rows are
+checked first; independently of the GPU, the same launch sequence at the
+full width (d = 4096, F = 16384) on T = 1024 tokens is checked in full,
+dgamma and dbeta included.  The smallest workload (GPT-2-medium shape) is
+checked in full.
 """
 import numpy as np
 import pytest
@@ -94,3 +97,26 @@ def test_sp_block_forward_backward_sampled():
         dga, dbe = dga + a, dbe + c
     assert_bf16_close("dgamma", step.dgamma.double().cpu().numpy(), dga)
     assert_bf16_close("dbeta", step.dbeta.double().cpu().numpy(), dbe)
+
+
+def test_sp_block_full_width_checked_in_full():
+    """The SP step's launch sequence at d = 4096, F = 16384, N = 8 on 1024 tokens (128-row chunks): every
+    output against the oracle's own forward and backward, so dgamma and dbeta (sums over all rows) rest on
+    the oracle's gathered gradient, not the GPU's."""
+    w = inputs.small_workload(1024, 4096, 8, F=16384, sp=True, backward=True, bias=None, name="sp_full_width_t1024")
+    step = Step(w, torch, binding)
+    step.run()
+    torch.cuda.synchronize()
+    st, site = binding.tpmlp_get_device_status()
+    assert st == binding.OK, f"device status {binding.status_string(st)} (site {site})"
+    X, g, be, A, B, dY = (inputs.draw(w, n)[1] for n in ("X", "gamma", "beta", "A", "B", "dY"))
+    cr = oracle.chunk_ranges(w.T, w.N)
+    Xc, dYc = [X[lo:hi] for lo, hi in cr], [dY[lo:hi] for lo, hi in cr]
+    assert_bf16_close("Y", f64(step.Y), np.concatenate(oracle.sp_forward(Xc, g, be, 1e-5, A, B, None, w.N)))
+    ref = oracle.sp_backward(Xc, g, be, 1e-5, A, B, None, dYc, w.N)
+    assert_bf16_close("dX", f64(step.dX), np.concatenate(ref["dX_chunks"]))
+    assert_bf16_close("dXg", f64(step.dXg), np.concatenate(ref["dXg_chunks"]))
+    assert_bf16_close("dA", f64(step.dA), ref["dA"])
+    assert_bf16_close("dB", f64(step.dB), ref["dB"])
+    assert_bf16_close("dgamma", step.dgamma.double().cpu().numpy(), ref["dgamma"])
+    assert_bf16_close("dbeta", step.dbeta.double().cpu().numpy(), ref["dbeta"])
