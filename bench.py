@@ -672,17 +672,18 @@ def run_attention(step, torch, binding, pk):
     ws = torch.empty(binding.tpmlp_attention_workspace_size(S, B, H), dtype=torch.uint8, device="cuda")
     block = lambda: binding.tpmlp_attention_tp_forward(X, Wqkv, Wo, S, B, H, N, Y, bqkv=bqkv, bo=bo, causal=True,
                                                        QKV_out=QKV, O_out=O, LSE_out=LSE, ws=ws)
-    ms_blk = time_calls(torch, block, 10)
-    ms_core = time_calls(torch, lambda: binding.tpmlp_attention_core(QKV, S, B, H, O, causal=True, LSE=LSE), 10)
+    # each call graph-timed after a settle pause (the rows before it leave the GPU at its power cap)
+    ms_blk = time_graph(torch, block, 10)
+    ms_core = time_graph(torch, lambda: binding.tpmlp_attention_core(QKV, S, B, H, O, causal=True, LSE=LSE), 10)
     # backward: the gradient of Y flows back through the block from the saved QKV, O and statistics
     dY = step.dY[:T] if getattr(step, "dY", None) is not None else torch.empty(T, d, **bf).normal_()
     dX, dWo, dQKV = torch.empty(T, d, **bf), torch.empty(d, d, **bf), torch.empty(T, 3 * d, **bf)
     dWqkv, dbqkv, dbo = torch.empty(d, 3 * d, **bf), torch.empty(3 * d, **bf), torch.empty(d, **bf)
     dO = torch.empty(T, d, **bf).normal_()
     wsb = torch.empty(binding.tpmlp_attention_backward_workspace_size(S, B, H), dtype=torch.uint8, device="cuda")
-    ms_blk_b = time_calls(torch, lambda: binding.tpmlp_attention_tp_backward(
+    ms_blk_b = time_graph(torch, lambda: binding.tpmlp_attention_tp_backward(
         X, Wqkv, Wo, QKV, O, LSE, dY, S, B, H, N, dX, dWqkv, dWo, dbqkv=dbqkv, dbo=dbo, causal=True, ws=wsb), 10)
-    ms_core_b = time_calls(torch, lambda: binding.tpmlp_attention_core_backward(QKV, O, dO, LSE, S, B, H, dQKV,
+    ms_core_b = time_graph(torch, lambda: binding.tpmlp_attention_core_backward(QKV, O, dO, LSE, S, B, H, dQKV,
                                                                                 causal=True, ws=wsb), 10)
     core_flops = 4.0 * 128 * B * H * S * (S + 1) / 2          # Q K^T and P V over the visible (causal) pairs
     core_bwd_flops = 2.5 * core_flops                          # Q K^T, dO V^T, P^T dO, dS K, dS^T Q
@@ -691,6 +692,7 @@ def run_attention(step, torch, binding, pk):
     peak = tensor_peak(pk, 0.0)[0]  # ten calls of each: the burst peak
     tf = lambda f, ms: round(f / (ms * 1e-3) / 1e12, 1)
     return {"workload": f"S={S} x B={B}, d={d}, {H} heads of 128 over N={N} shards, causal",
+            "timing": "CUDA graph of 10 back-to-back calls after a settle pause; fractions of the burst peak",
             "block_ms": round(ms_blk, 4), "block_TFLOP/s": tf(core_flops + gemm_flops, ms_blk),
             "core_ms": round(ms_core, 4), "core_TFLOP/s": tf(core_flops, ms_core),
             "core_frac": round(core_flops / (ms_core * 1e-3) / 1e12 / peak, 3),
