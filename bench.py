@@ -272,6 +272,22 @@ def oracle_sample(w, seed=0, tokens=None):
     return dt, tok, flops
 
 
+def cpu_baseline_configs(tokens=64):
+    """The oracle timed on a bounded sample of every configuration (the full tiny fp32 one; `tokens` rows of
+    the others, with their full weights, drawn by the host generator), on the host cores: seconds, tokens,
+    flops and TFLOP/s per configuration."""
+    out = {}
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    for num, name in CONFIGS.items():
+        w = inputs.WORKLOADS[name]
+        t0 = time.perf_counter()
+        dt, tok, fl = oracle_sample(w, tokens=w.T if w.dtype == "fp32" else tokens)
+        out[name] = {"config": num, "oracle_s": round(dt, 3), "tokens": tok, "TFLOP/s": round(fl / dt / 1e12, 4),
+                     "draw_s": round(time.perf_counter() - t0 - dt, 1), "cores": cores,
+                     "work": "forward + backward" if w.backward else "forward"}
+    return out
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -1057,6 +1073,8 @@ def run_ours(args, w):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if args.cpu_baseline_configs and rank == 0 and world == 1:
+        line["cpu_baseline_configs"] = cpu_baseline_configs()
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -1078,6 +1096,9 @@ def main():
                          "medium, 3 7B, 4 SP block forward+backward, 5 d=8192 SP forward)")
     ap.add_argument("--oracle-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-configs", action="store_true",
+                    help="also time the oracle on a 64-token sample of every configuration (the full tiny one) on "
+                         "the host cores; minutes of host work for the weight draws")
     ap.add_argument("--step-only", action="store_true",
                     help="time the step and its per-kernel breakdown only (no e2e, other rows or CPU baseline): for "
                          "profiling")
