@@ -270,6 +270,40 @@ def test_sp_backward(T, d, N, save_xg):
     assert all(x.intact() for x in dX + [dA, dB, dgam, dbet])
 
 
+@pytest.mark.parametrize("d,N,rows", [(8, 1, 1), (8, 4, 3), (8, 2, 17), (16, 8, 2), (16, 4, 5)])
+def test_degenerate_small_shapes(d, N, rows):
+    """The smallest widths the ABI takes (d = 8, shards of 8 columns of F = 4 d, down to one row per chunk):
+    K below one 64-deep k-block everywhere, a single partial tile; forward, SP forward and SP backward."""
+    T, F = N * rows, 4 * d
+    w = inputs.small_workload(T, d, N, sp=True, backward=True, bias=(0.0, 0.02), name=f"tiny_{d}_{N}_{rows}")
+    X, g, be, A, B, b, dY = _draw(w, "X", "gamma", "beta", "A", "B", "bias", "dY")
+    Y = Guarded((T, d))
+    binding.tpmlp_forward(dev(X[0]), dev(A[0]), dev(B[0]), dev(b[0]), N, Y.t)
+    torch.cuda.synchronize()
+    assert_bf16_close("Y", f64(Y.t), oracle.mlp_tp(X[1], A[1], B[1], b[1], N))
+    xs = list(dev(X[0]).split(rows))
+    Yc = [Guarded((rows, d)) for _ in range(N)]
+    Hpre = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    Hs = torch.empty(T, F, dtype=torch.bfloat16, device="cuda")
+    binding.tpmlp_sp_forward(xs, dev(g[0]), dev(be[0]), dev(A[0]), dev(B[0]), N, [y.t for y in Yc], bias=dev(b[0]),
+                             Hpre_out=Hpre, H_out=Hs)
+    dX = [Guarded((rows, d)) for _ in range(N)]
+    dA, dB, db = Guarded((d, F)), Guarded((F, d)), Guarded((F,))
+    dgam, dbet = Guarded((d,), torch.float32), Guarded((d,), torch.float32)
+    binding.tpmlp_sp_backward(xs, dev(g[0]), dev(be[0]), dev(A[0]), dev(B[0]), Hpre, list(dev(dY[0]).split(rows)), N,
+                              [x.t for x in dX], dA.t, dB.t, dgam.t, dbet.t, bias=dev(b[0]), dbias=db.t, H=Hs)
+    torch.cuda.synchronize()
+    Xc, dYc = _chunks(X[1], N), _chunks(dY[1], N)
+    assert_bf16_close("Y chunks", np.concatenate([f64(y.t) for y in Yc]),
+                      np.concatenate(oracle.sp_forward(Xc, g[1], be[1], 1e-5, A[1], B[1], b[1], N)))
+    ref = oracle.sp_backward(Xc, g[1], be[1], 1e-5, A[1], B[1], b[1], dYc, N)
+    assert_bf16_close("dX", np.concatenate([f64(x.t) for x in dX]), np.concatenate(ref["dX_chunks"]))
+    for name, t, r in (("dA", dA, ref["dA"]), ("dB", dB, ref["dB"]), ("db", db, ref["db"]),
+                       ("dgamma", dgam, ref["dgamma"]), ("dbeta", dbet, ref["dbeta"])):
+        assert_bf16_close(name, f64(t.t), r)
+    assert all(t.intact() for t in [Y, dA, dB, db, dgam, dbet] + Yc + dX)
+
+
 def test_fp32_tiny_config_full():
     """The tiny fp32 workload (T=128, d=64, F=256, N=2) in full, to 1e-5 relative."""
     w = inputs.WORKLOADS["tiny_fp32_fwd"]
