@@ -1284,8 +1284,6 @@ static int stream_slots(size_t slot_bytes) {
   return static_cast<int>(n < 2 ? 2 : (n > 32 ? 32 : n));
 }
 
-// LayerNorm forward for widths the streamed kernel does not cover: one warp per row (two for d = 8192)
-// with the row in registers.
 // Persistent launch of a pipelined LayerNorm kernel, or cudaErrorNotReady when the grid would give each
 // warp (pair) fewer than kLnPipeMinRows rows: below that the exposed first load and the tail outweigh the
 // overlap (measured on GB300: at T = 8192, d = 4096 the launch-per-group kernel is 7% faster; at T = 65536
@@ -1390,19 +1388,8 @@ cudaError_t launch_layernorm_fwd(const RowParams& r, const DeviceCtx& ctx, cudaS
     const cudaError_t e = launch_ln_stream(r, ctx, s);
     if (e != cudaErrorNotSupported) return e;  // launched (or failed); otherwise a width it does not cover
   }
-  const int grid4 = (r.rows + 3) / 4;
-  const int grid2 = (r.rows + 1) / 2;
-  switch (r.d) {
-    case 256: k_layernorm_fwd_reg<1, 1><<<grid4, 128, 0, s>>>(r); break;
-    case 512: k_layernorm_fwd_reg<2, 1><<<grid4, 128, 0, s>>>(r); break;
-    case 1024: k_layernorm_fwd_reg<4, 1><<<grid4, 128, 0, s>>>(r); break;
-    case 2048: k_layernorm_fwd_reg<8, 1><<<grid4, 128, 0, s>>>(r); break;
-    // one-warp blocks: a row's block leaves as soon as its row is stored, so the SM takes the next row
-    // without waiting for three other warps, and the last rows spread over all SMs
-    case 4096: k_layernorm_fwd_reg<16, 1><<<r.rows, 32, 0, s>>>(r); break;
-    case 8192: k_layernorm_fwd_reg<16, 2><<<grid2, 128, 0, s>>>(r); break;
-    default: k_layernorm_fwd_any<false><<<grid4, 128, 0, s>>>(r); break;
-  }
+  // any other multiple of 8
+  k_layernorm_fwd_any<false><<<(r.rows + 3) / 4, 128, 0, s>>>(r);
   return cudaGetLastError();
 }
 
