@@ -89,8 +89,9 @@ def percentiles(ms):
             "p90": round(float(np.percentile(a, 90)), 4)}
 
 
-_GEMM_SOURCES = ("common.h", "ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_tc.cu")
-_ROW_SOURCES = ("common.h", "ptx.cuh", "launch.h", "rowwise.cu")
+_GEMM_SOURCES = ("common.h", "ptx.cuh", "debug_bounds.cuh", "fp8.cuh", "philox.cuh", "launch.h", "gemm_tc.cuh",
+                 "gemm_tc2.cuh", "gemm_tc.cu")
+_ROW_SOURCES = ("common.h", "ptx.cuh", "debug_bounds.cuh", "fp8.cuh", "philox.cuh", "launch.h", "rowwise.cu")
 
 
 def kernel_source_digest(segment=None):
