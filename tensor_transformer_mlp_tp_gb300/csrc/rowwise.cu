@@ -634,7 +634,8 @@ __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, cons
 // Σ g·(x - mean) = Sgc - (S1/d)·Sg; the shift by a sample of the row keeps the
 // variance free of the cancellation that E[x²] - mean² suffers when the mean
 // is large against the spread.  Arithmetic on float pairs (the packed fp32
-// instructions); c stays in registers for the output pass.  dx goes to the
+// instructions); c stays in registers for the output pass, or (RR) is formed
+// again from the slot's x, which the team then reads twice.  dx goes to the
 // row's chunk; dγ and dβ for the thread's columns accumulate in registers over
 // all rows the team processes, and at the end the teams' sums are added in
 // team order into the CTA's partial row [2 d], which a fixed-order column sum
@@ -663,8 +664,10 @@ __device__ __forceinline__ float warp_sum4(float a, float b, float c, float d) {
 }
 
 // ADD: dx += the rows of p.add_chunks (the residual's gradient), loaded while the row statistics reduce.
-// CONS consumer warps (one more warp produces).
-template <int VT, int TW, bool ADD = false, int CONS = kStreamConsumers>
+// CONS consumer warps (one more warp produces).  RR: the output pass reads x and dy from the row's slot a
+// second time instead of keeping them (and x - K) in registers, and the slot is freed after that pass; the
+// registers saved let more consumer warps share an SM.
+template <int VT, int TW, bool ADD = false, int CONS = kStreamConsumers, bool RR = false>
 __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(const RowParams p) {
   constexpr int kTeams = CONS / TW;
   if (!ring_config_ok(p, kTeams)) return;  // uniform over the CTA: no barrier is left waiting
@@ -714,15 +717,19 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
       const bool ok = stream_wait(full + slot, static_cast<uint32_t>(i / p.slots) & 1u, wc);
       const uint4* xs = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes);
       const uint4* ds = reinterpret_cast<const uint4*>(ring + slot * 2 * row_bytes + row_bytes);
-      uint4 xv[VT], dv[VT];
+      uint4 xv[RR ? 1 : VT], dv[RR ? 1 : VT];
+      if constexpr (!RR) {
 #pragma unroll
-      for (int k = 0; k < VT; ++k) {
-        xv[k] = ok ? xs[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
-        dv[k] = ok ? ds[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < VT; ++k) {
+          xv[k] = ok ? xs[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
+          dv[k] = ok ? ds[j + k * 32 * TW] : make_uint4(0, 0, 0, 0);
+        }
       }
       const float shift = ok ? __uint_as_float(xs[0].x << 16) : 0.f;  // the row's first element
-      __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(empty + slot);
+      if constexpr (!RR) {
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(empty + slot);
+      }
       uint4 av[VT];
       if constexpr (ADD) {
         const uint4* a4 = reinterpret_cast<const uint4*>(add_chunk_row(p, blockIdx.x + i * gridDim.x));
@@ -731,18 +738,21 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
       }
       const float2 nk = make_float2(-shift, -shift);
       float2 s1 = make_float2(0.f, 0.f), s2 = s1, sg = s1, sgc = s1;
-      float2 c[VT][4];
+      float2 c[RR ? 1 : VT][4];
 #pragma unroll
       for (int k = 0; k < VT; ++k) {
         const uint4 gk = gam[j + k * 32 * TW];
+        const uint4 xk = RR ? (ok ? xs[j + k * 32 * TW] : make_uint4(0, 0, 0, 0)) : xv[RR ? 0 : k];
+        const uint4 dk = RR ? (ok ? ds[j + k * 32 * TW] : make_uint4(0, 0, 0, 0)) : dv[RR ? 0 : k];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          c[k][w] = __fadd2_rn(bf2(word(xv[k], w)), nk);
-          const float2 g = __fmul2_rn(bf2(word(dv[k], w)), bf2(word(gk, w)));
-          s1 = __fadd2_rn(s1, c[k][w]);
-          s2 = __ffma2_rn(c[k][w], c[k][w], s2);
+          const float2 ck = __fadd2_rn(bf2(word(xk, w)), nk);
+          if constexpr (!RR) c[k][w] = ck;
+          const float2 g = __fmul2_rn(bf2(word(dk, w)), bf2(word(gk, w)));
+          s1 = __fadd2_rn(s1, ck);
+          s2 = __ffma2_rn(ck, ck, s2);
           sg = __fadd2_rn(sg, g);
-          sgc = __ffma2_rn(g, c[k][w], sgc);
+          sgc = __ffma2_rn(g, ck, sgc);
         }
       }
       const float v = warp_sum4(s1.x + s1.y, s2.x + s2.y, sg.x + sg.y, sgc.x + sgc.y);
@@ -780,11 +790,14 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
 #pragma unroll
       for (int k = 0; k < VT; ++k) {
         const uint4 gk = gam[j + k * 32 * TW];
+        const uint4 xk = RR ? (ok ? xs[j + k * 32 * TW] : make_uint4(0, 0, 0, 0)) : xv[RR ? 0 : k];
+        const uint4 dk = RR ? (ok ? ds[j + k * 32 * TW] : make_uint4(0, 0, 0, 0)) : dv[RR ? 0 : k];
         uint32_t o[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const float2 xhat = __ffma2_rn(c[k][w], r2, nmr);
-          const float2 dy = bf2(word(dv[k], w));
+          const float2 ck = RR ? __fadd2_rn(bf2(word(xk, w)), nk) : c[RR ? 0 : k][w];
+          const float2 xhat = __ffma2_rn(ck, r2, nmr);
+          const float2 dy = bf2(word(dk, w));
           float2 dx = __ffma2_rn(xhat, nm2r, __ffma2_rn(__fmul2_rn(dy, bf2(word(gk, w))), r2, nm1r));
           dg[k][w] = __ffma2_rn(dy, xhat, dg[k][w]);
           db[k][w] = __fadd2_rn(db[k][w], dy);
@@ -792,6 +805,10 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
           o[w] = pack_bf16x2(dx.x, dx.y);
         }
         if (row_vec_ok(p, row, j + k * 32 * TW, kBoundsOutChunk)) dx4[j + k * 32 * TW] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if constexpr (RR) {  // this warp's reads of the slot are done
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(empty + slot);
       }
     }
   }
@@ -1440,6 +1457,27 @@ constexpr int kLnBwdMaxBlocksFused = 256; // upper bound on the fused backward's
 struct TeamShape {
   int tw, vt;
 };
+// The fused backward with CONS consumer warps in teams of TW: a ring of x/dy row-pair slots (a multiple of
+// the teams, at most ring_max bytes; 192 KB when the slots are held through the output pass), the γ row
+// and the barriers, or the teams' dγ/dβ sums if those need more.
+template <int VT, int TW, int CONS, bool RR>
+static cudaError_t launch_ln_bwd_cfg(RowParams r, int grid, bool add, cudaStream_t s) {
+  constexpr int kTeams = CONS / TW;
+  const size_t row_bytes = static_cast<size_t>(r.d) * 2;
+  const size_t ring_max = RR ? 192u * 1024u : 128u * 1024u;
+  int slots = static_cast<int>(ring_max / (2 * row_bytes)) / kTeams * kTeams;
+  if (slots > 32) slots = 32 / kTeams * kTeams;
+  if (slots < kTeams) slots = kTeams;
+  size_t smem = 128 + static_cast<size_t>(slots) * (2 * row_bytes + 16) + row_bytes + 16;
+  const size_t team_sums = static_cast<size_t>(kTeams) * 2 * r.d * 4 + 128;
+  if (smem < team_sums) smem = team_sums;
+  if (smem > 227u * 1024u) return cudaErrorInvalidValue;
+  r.slots = slots;
+  return add ? launch_stream(k_layernorm_bwd_fused<VT, TW, true, CONS, RR>, r, smem, grid, s, 32 * (CONS + 1))
+             : launch_stream(k_layernorm_bwd_fused<VT, TW, false, CONS, RR>, r, smem, grid, s, 32 * (CONS + 1));
+}
+
+
 TeamShape fused_shape(int d) {
   switch (d) {
     case 256: return {1, 1};
@@ -1485,13 +1523,18 @@ cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap
       const size_t team_sums = static_cast<size_t>(kStreamConsumers / ts.tw) * per_block * 4 + 128;
       if (smem < team_sums) smem = team_sums;
       cudaError_t e;
-      if (r.add_chunks.p[0] == nullptr) {
+      if (r.d == 4096) {
+        // three teams of four warps that read x and dy from the slot twice fit 13 warps' 128 registers a
+        // thread (measured on GB300 at T = 8192: 0.638 of HBM against 0.632 for two teams holding them in
+        // registers; at T = 32768 0.82 against 0.78); at d = 8192 neither one team (0.535) nor two
+        // (spilling at 96 registers, 0.433) beat the register kernel (0.565)
+        e = launch_ln_bwd_cfg<4, 4, 12, true>(r, grid, r.add_chunks.p[0] != nullptr, s);
+      } else if (r.add_chunks.p[0] == nullptr) {
         switch (r.d) {
           case 256: e = launch_stream(k_layernorm_bwd_fused<1, 1>, r, smem, grid, s); break;
           case 512: e = launch_stream(k_layernorm_bwd_fused<1, 2>, r, smem, grid, s); break;
           case 1024: e = launch_stream(k_layernorm_bwd_fused<1, 4>, r, smem, grid, s); break;
           case 2048: e = launch_stream(k_layernorm_bwd_fused<2, 4>, r, smem, grid, s); break;
-          case 4096: e = launch_stream(k_layernorm_bwd_fused<4, 4>, r, smem, grid, s); break;
           default: e = launch_stream(k_layernorm_bwd_fused<4, 8>, r, smem, grid, s); break;
         }
       } else {
@@ -1500,7 +1543,6 @@ cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap
           case 512: e = launch_stream(k_layernorm_bwd_fused<1, 2, true>, r, smem, grid, s); break;
           case 1024: e = launch_stream(k_layernorm_bwd_fused<1, 4, true>, r, smem, grid, s); break;
           case 2048: e = launch_stream(k_layernorm_bwd_fused<2, 4, true>, r, smem, grid, s); break;
-          case 4096: e = launch_stream(k_layernorm_bwd_fused<4, 4, true>, r, smem, grid, s); break;
           default: e = launch_stream(k_layernorm_bwd_fused<4, 8, true>, r, smem, grid, s); break;
         }
       }
