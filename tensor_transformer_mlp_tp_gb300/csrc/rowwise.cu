@@ -1514,6 +1514,17 @@ cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap
     if (grid > kLnBwdMaxBlocksFused) grid = kLnBwdMaxBlocksFused;
     if (static_cast<size_t>(grid) * per_block > cap_floats) grid = static_cast<int>(cap_floats / per_block);
     if (grid >= 1) {
+      cudaError_t e;
+      if (r.d == 4096) {
+        // three teams of four warps that read x and dy from the slot twice fit 13 warps' 128 registers a
+        // thread (measured on GB300 at T = 8192: 0.638 of HBM against 0.632 for two teams holding them in
+        // registers; at T = 32768 0.82 against 0.78); at d = 8192 neither one team (0.535) nor two
+        // (spilling at 96 registers, 0.433) beat the register kernel (0.565)
+        e = launch_ln_bwd_cfg<4, 4, 12, true>(r, grid, r.add_chunks.p[0] != nullptr, s);
+        if (e != cudaSuccess) return e;
+        k_column_sum<<<(2 * r.d + 31) / 32, 256, 0, s>>>(r.partial, grid, 2 * r.d, 2LL * r.d, dgamma, dbeta, r.d, 0);
+        return cudaGetLastError();
+      }
       const size_t row_bytes = static_cast<size_t>(r.d) * 2;
       // a multiple of the consumer teams (see ring_config_ok)
       const int teams = kStreamConsumers / ts.tw;
@@ -1522,14 +1533,7 @@ cudaError_t launch_layernorm_bwd(const RowParams& r0, float* scratch, size_t cap
       size_t smem = 128 + r.slots * 2 * row_bytes + row_bytes + 16 * static_cast<size_t>(r.slots) + 16;
       const size_t team_sums = static_cast<size_t>(kStreamConsumers / ts.tw) * per_block * 4 + 128;
       if (smem < team_sums) smem = team_sums;
-      cudaError_t e;
-      if (r.d == 4096) {
-        // three teams of four warps that read x and dy from the slot twice fit 13 warps' 128 registers a
-        // thread (measured on GB300 at T = 8192: 0.638 of HBM against 0.632 for two teams holding them in
-        // registers; at T = 32768 0.82 against 0.78); at d = 8192 neither one team (0.535) nor two
-        // (spilling at 96 registers, 0.433) beat the register kernel (0.565)
-        e = launch_ln_bwd_cfg<4, 4, 12, true>(r, grid, r.add_chunks.p[0] != nullptr, s);
-      } else if (r.add_chunks.p[0] == nullptr) {
+      if (r.add_chunks.p[0] == nullptr) {
         switch (r.d) {
           case 256: e = launch_stream(k_layernorm_bwd_fused<1, 1>, r, smem, grid, s); break;
           case 512: e = launch_stream(k_layernorm_bwd_fused<1, 2>, r, smem, grid, s); break;
