@@ -118,7 +118,8 @@ def test_dropout_backward(T, d, N, p):
     assert dZ.intact() and db2.intact()
 
 
-@pytest.mark.parametrize("T,d,N", [(1000, 1024, 8), (96, 2048, 4), (200, 4096, 8), (24, 136, 3), (64, 8192, 2)])
+@pytest.mark.parametrize("T,d,N", [(1000, 1024, 8), (96, 2048, 4), (200, 4096, 8), (2400, 4096, 8), (24, 136, 3),
+                                   (64, 8192, 2)])
 def test_layernorm_backward_add(T, d, N):
     """The streamed and the generic LayerNorm backward with the residual's gradient added to dx."""
     w = inputs.small_workload(T, d, N, sp=True, backward=True, name=f"lnadd_{T}_{d}_{N}")
