@@ -120,3 +120,20 @@ def test_sp_block_full_width_checked_in_full():
     assert_bf16_close("dB", f64(step.dB), ref["dB"])
     assert_bf16_close("dgamma", step.dgamma.double().cpu().numpy(), ref["dgamma"])
     assert_bf16_close("dbeta", step.dbeta.double().cpu().numpy(), ref["dbeta"])
+
+
+def test_sp_step_is_deterministic():
+    """Two runs of the SP step's launch sequence at the full width (d = 4096, F = 16384, N = 8, 1024 tokens) on
+    the same inputs agree bit for bit: the shard sums run in K order inside one accumulator, and the
+    dgamma/dbeta column sums and every other reduction have a fixed order."""
+    w = inputs.small_workload(1024, 4096, 8, F=16384, sp=True, backward=True, bias=None, name="sp_full_width_t1024")
+    step = Step(w, torch, binding)
+    outs = []
+    for _ in range(2):
+        step.run()
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (step.Y, step.dX, step.dXg, step.dA, step.dB, step.dgamma, step.dbeta)])
+    st, site = binding.tpmlp_get_device_status()
+    assert st == binding.OK, f"device status {binding.status_string(st)} (site {site})"
+    for name, a, b in zip(("Y", "dX", "dXg", "dA", "dB", "dgamma", "dbeta"), *outs):
+        assert torch.equal(a, b), name
