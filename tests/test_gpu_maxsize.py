@@ -105,3 +105,22 @@ def test_mlp_backward_past_2_31_elements():
     Ct = torch.from_numpy(C).cuda()
     assert_bf16_close("dA[:, C]", f64(dA[:, Ct]), gu["dA"])
     assert_bf16_close("dB[C, :]", f64(dB[Ct, :]), gu["dB"])
+
+
+def test_reduce_scatter_past_2_31_elements():
+    """The explicit reduce-scatter of N = 8 partials of T = 65600 rows x d = 4096 (offsets into the partials
+    past 2^31): chunk j's rows are the fixed-order sum of the partials' rows, on sampled rows of every chunk."""
+    T, d, N = 65600, 4096, 8
+    P = torch.empty(N, T, d, dtype=torch.bfloat16, device="cuda")
+    for i in range(N):
+        P[i] = _pattern_device(T, d, 2654435761 + 7 * i, 40503 + 11 * i)
+    Yc = [torch.empty(T // N, d, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    binding.tpmlp_reduce_scatter(P, N, Yc)
+    torch.cuda.synchronize()
+    st, site = binding.tpmlp_get_device_status()
+    assert st == binding.OK, f"device status {binding.status_string(st)} (site {site})"
+    rows = _sample(T, N, 48, 5)
+    per = T // N
+    got = np.stack([f64(Yc[r // per][r % per]) for r in rows])
+    ref = oracle.all_reduce([_pattern_rows(rows, d, 2654435761 + 7 * i, 40503 + 11 * i) for i in range(N)])
+    assert_bf16_close("Y[rows]", got, ref)
