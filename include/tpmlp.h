@@ -74,7 +74,8 @@ typedef enum { TPMLP_BF16 = 0, TPMLP_FP32 = 1 } tpmlp_dtype;
 
 /* Problem shape.  ffn is the FFN width F (4d on the pages); n_shards is N,
  * the tensor-parallel degree and, for the sequence-parallel calls, the number
- * of sequence chunks.  dtype is a tpmlp_dtype. */
+ * of sequence chunks, 1 <= N <= 64 (TPMLP_ERR_INVALID_ARG otherwise).  dtype is
+ * a tpmlp_dtype. */
 typedef struct {
   int64_t tokens;
   int64_t d;

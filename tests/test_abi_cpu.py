@@ -91,6 +91,13 @@ def test_invalid_shapes(lib, bad):
     assert _ws(s, binding.OP_FWD)[0] == binding.ERR_INVALID_ARG
 
 
+def test_largest_shard_count_accepted(lib):
+    """N = 64 (the most shards a call takes) with 8-column shards: every operation sizes its workspace."""
+    s = binding.make_shape(1024, 128, 512, 64)
+    for op in (binding.OP_FWD, binding.OP_SP_FWD, binding.OP_BWD, binding.OP_SP_BWD):
+        assert _ws(s, op)[0] == binding.OK
+
+
 def test_sp_requires_divisible_tokens(lib):
     s = binding.make_shape(100, 64, 256, 8)
     assert _ws(s, binding.OP_SP_FWD)[0] == binding.ERR_INVALID_ARG

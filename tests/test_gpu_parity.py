@@ -197,7 +197,7 @@ def test_reduce_scatter_random(N):
         assert Y[j].intact()
 
 
-@pytest.mark.parametrize("T,d,N", [(256, 128, 4), (384, 192, 8), (128, 256, 2), (384, 128, 8)])
+@pytest.mark.parametrize("T,d,N", [(256, 128, 4), (384, 192, 8), (128, 256, 2), (384, 128, 8), (1024, 128, 64)])
 @pytest.mark.parametrize("rs_mode", [binding.RS_FUSED, binding.RS_PARTIALS])
 def test_sp_forward(T, d, N, rs_mode):
     w = inputs.small_workload(T, d, N, sp=True, bias=(0.0, 0.02))
@@ -217,7 +217,7 @@ def test_sp_forward(T, d, N, rs_mode):
     assert all(y.intact() for y in Yc)
 
 
-@pytest.mark.parametrize("T,d,N", [(300, 192, 4), (256, 128, 8), (130, 64, 2)])
+@pytest.mark.parametrize("T,d,N", [(300, 192, 4), (256, 128, 8), (130, 64, 2), (200, 128, 64)])
 @pytest.mark.parametrize("saved", ["none", "hpre", "hpre_h"])
 def test_backward(T, d, N, saved):
     w = inputs.small_workload(T, d, N, backward=True, bias=(0.0, 0.2))
@@ -239,7 +239,7 @@ def test_backward(T, d, N, saved):
         assert got.intact()
 
 
-@pytest.mark.parametrize("T,d,N", [(256, 128, 4), (384, 192, 8), (64, 256, 2)])
+@pytest.mark.parametrize("T,d,N", [(256, 128, 4), (384, 192, 8), (64, 256, 2), (1024, 128, 64)])
 @pytest.mark.parametrize("save_xg", [False, True])
 def test_sp_backward(T, d, N, save_xg):
     w = inputs.small_workload(T, d, N, sp=True, backward=True, bias=None)
