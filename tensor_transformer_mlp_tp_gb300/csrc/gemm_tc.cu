@@ -4,6 +4,7 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "gemm_tc2.cuh"
@@ -66,8 +67,9 @@ cudaError_t run(const GemmParams& p, int grid, cudaStream_t s) {
 
 // Largest number of co-resident CTA pairs of `kern` on the current device (cached per device).
 template <typename K>
-int max_pairs(K kern, int smem, int threads, int dev_cache_slot, int* cache) {
-  if (cache[dev_cache_slot] > 0) return cache[dev_cache_slot];
+int max_pairs(K kern, int smem, int threads, int dev_cache_slot, std::atomic<int>* cache) {
+  const int known = cache[dev_cache_slot].load(std::memory_order_relaxed);
+  if (known > 0) return known;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
   cfg.blockDim = dim3(threads);
@@ -81,7 +83,7 @@ int max_pairs(K kern, int smem, int threads, int dev_cache_slot, int* cache) {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) n = 1;
-  cache[dev_cache_slot] = n;
+  cache[dev_cache_slot].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -98,7 +100,7 @@ cudaError_t run_pair(GemmParams p, cudaStream_t s) {
   using S = PairShape<BN, kPairStages, kEpiWarps, BAL>;
   auto kern = k_gemm_tc2<BN, AMN, BMN, EPI, kPairStages, kEpiWarps, FP8, BAL>;
   constexpr int kThreads = S::kThreads;
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64] = {};  // co-resident pairs per device (concurrent callers store the same value)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

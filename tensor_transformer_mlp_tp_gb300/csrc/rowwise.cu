@@ -7,6 +7,8 @@
 // All global traffic is 16-byte vectors; reductions are warp shuffles.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "debug_bounds.cuh"
 #include "fp8.cuh"
 #include "launch.h"
@@ -1309,17 +1311,19 @@ constexpr int kLnPipeMinRows = 24;
 
 template <typename K>
 static cudaError_t launch_ln_persistent(K kern, int rows_per_block, const RowParams& r, const DeviceCtx& ctx,
-                                        cudaStream_t s, int* per_sm_cache) {
+                                        cudaStream_t s, std::atomic<int>* per_sm_cache) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (per_sm_cache[dev & 63] == 0) {
+  int per_sm = per_sm_cache[dev & 63].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 128, 0);
     if (e != cudaSuccess) return e;
-    per_sm_cache[dev & 63] = n < 1 ? 1 : n;
+    per_sm = n < 1 ? 1 : n;
+    per_sm_cache[dev & 63].store(per_sm, std::memory_order_relaxed);  // concurrent callers store the same value
   }
-  const long long grid = static_cast<long long>(per_sm_cache[dev & 63]) * ctx.sm_count;
+  const long long grid = static_cast<long long>(per_sm) * ctx.sm_count;
   if (static_cast<long long>(r.rows) < grid * rows_per_block * kLnPipeMinRows) return cudaErrorNotReady;
   kern<<<static_cast<int>(grid), 128, 0, s>>>(r);
   return cudaGetLastError();
@@ -1327,13 +1331,13 @@ static cudaError_t launch_ln_persistent(K kern, int rows_per_block, const RowPar
 
 template <int V>
 static cudaError_t launch_ln_pipe(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
-  static int per_sm[64] = {0};
+  static std::atomic<int> per_sm[64] = {};
   return launch_ln_persistent(k_layernorm_fwd_pipe<V>, 4, r, ctx, s, per_sm);
 }
 
 template <int V>
 static cudaError_t launch_ln_pipe2(const RowParams& r, const DeviceCtx& ctx, cudaStream_t s) {
-  static int per_sm[64] = {0};
+  static std::atomic<int> per_sm[64] = {};
   return launch_ln_persistent(k_layernorm_fwd_pipe2<V>, 2, r, ctx, s, per_sm);
 }
 
