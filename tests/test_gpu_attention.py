@@ -259,3 +259,32 @@ def test_attention_core_forward_backward_bench_shape():
         for name, got, ref in (("dQ", dQKVg[rows, c[0]], dq), ("dK", dQKVg[rows, c[1]], dk),
                                ("dV", dQKVg[rows, c[2]], dv)):
             assert_bf16_close(f"{name} (b={b}, h={h})", got, ref)
+
+
+def _random_attention_shapes(seed, n):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 600)), int(rng.integers(1, 4)), int(rng.integers(1, 4)), bool(rng.integers(0, 2)))
+            for _ in range(n)]
+
+
+@pytest.mark.parametrize("S,B,H,causal", _random_attention_shapes(20261204, 10))
+def test_attention_core_random_shape(S, B, H, causal):
+    """A seeded sweep of sequence lengths (ragged against the 128-row tiles, down to one position), batch
+    sizes and head counts: the forward output, then dQ, dK, dV from its saved statistics."""
+    w = inputs.small_workload(64, 64, 2, name=f"attnrand_{S}_{B}_{H}")
+    qkv = inputs.draw(w, "QKV", shape=(S * B, 3 * H * HD), dist=(0.0, 1.0))
+    dO = inputs.draw(w, "dO", shape=(S * B, H * HD), dist=(0.0, 1.0))
+    QKV = dev(qkv[0])
+    O = torch.empty(S * B, H * HD, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(binding.attention_lse_shape(S, B, H), dtype=torch.float32, device="cuda")
+    binding.tpmlp_attention_core(QKV, S, B, H, O, causal=causal, LSE=lse)
+    dQKV = Guarded((S * B, 3 * H * HD))
+    binding.tpmlp_attention_core_backward(QKV, O, dev(dO[0]), lse, S, B, H, dQKV.t, causal=causal)
+    torch.cuda.synchronize()
+    assert_bf16_close("O", f64(O), _core_reference(qkv[1], S, B, H, causal))
+    ref = _core_backward_reference(qkv[1], dO[1], S, B, H, causal)
+    got = f64(dQKV.t)
+    d = H * HD
+    for part, name in enumerate(("dQ", "dK", "dV")):
+        assert_bf16_close(name, got[:, part * d:(part + 1) * d], ref[:, part * d:(part + 1) * d])
+    assert dQKV.intact()
