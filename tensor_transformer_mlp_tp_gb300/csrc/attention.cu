@@ -2,8 +2,9 @@
 // backward, and the block (QKV projection, attention, output projection with the
 // shard sum, and its backward).
 //
-// Forward core (one CTA per 128-query tile of one batch element and head, head
-// dim 128): softmax(Q K^T / sqrt(hd)) V with an online softmax over 128-key tiles.
+// Forward core (persistent CTAs walking 128-query tiles of one batch element and
+// head each, head dim 128): softmax(Q K^T / sqrt(hd)) V with an online softmax over
+// 128-key tiles.
 //   warp 0   TMA producer: Q once, then K and V tiles into 3-stage rings; Q, K,
 //            V come straight out of the QKV projection's [S, B, 3, H, hd] layout
 //            through 4-D tensor maps (two 64-element boxes per row).
@@ -46,7 +47,7 @@ constexpr int kAtom = 128 * 128;    // one 64-element-wide swizzled column of a 
 constexpr int kTileBytes = 2 * kAtom;  // a 128 x 128 bf16 tile: two atom columns
 constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
 constexpr uint32_t kSiteAttnQ = 32, kSiteAttnKv = 33, kSiteAttnS = 34, kSiteAttnP = 35, kSiteAttnSEmpty = 36,
-                   kSiteAttnKvEmpty = 37, kSiteAttnPv = 38;
+                   kSiteAttnKvEmpty = 37, kSiteAttnPv = 38, kSiteAttnQEmpty = 39, kSiteAttnOEmpty = 40;
 
 struct AttnParams {
   CUtensorMap tmQ, tmK, tmV;
@@ -154,6 +155,12 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
   tma_load_4d(dst + kAtom, map, bar, 64, h, b, s0);
 }
 
+// Persistent: one CTA per SM walks the work items (query tile, batch element, head), longest query tiles
+// first, items blockIdx.x, blockIdx.x + gridDim.x, ...  The K/V rings, the S and P buffers and their
+// barriers run on over the items (phases from a running key-tile count), so the next item's Q load, K/V
+// loads and first score MMA overlap the previous item's epilogue: Q is reloaded once the previous
+// item's score MMAs have read it (q_empty), and the next item's first P V overwrites O only once the
+// softmax warps have read it (o_empty).
 __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -162,8 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   uint8_t* sV = sK + kFwdKvStages * kTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kFwdKvStages * kTileBytes);
   uint64_t* q_full = bars;
+  uint64_t* q_empty = q_full + 1;   // every score MMA of the item has read Q
   // K and V have their own barriers: K_j is released as soon as S_j is done, V_j after P_j V_j
-  uint64_t* k_full = q_full + 1;
+  uint64_t* k_full = q_empty + 1;
   uint64_t* k_empty = k_full + kFwdKvStages;
   uint64_t* v_full = k_empty + kFwdKvStages;
   uint64_t* v_empty = v_full + kFwdKvStages;
@@ -171,21 +179,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   uint64_t* s_empty = s_full + 2;
   uint64_t* p_full = s_empty + 2;   // [P buffer]
   uint64_t* pv_done = p_full + 2;   // [P buffer]: P V of the tiles that used that buffer
-  uint64_t* drain = pv_done + 2;
+  uint64_t* o_empty = pv_done + 2;  // the softmax warps have read the item's O
+  uint64_t* drain = o_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
-  // longest causal tiles first: the last query tiles have the most key tiles
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x % p.n_qtiles);
-  const int bh = static_cast<int>(blockIdx.x / p.n_qtiles);
-  const int b = bh % p.B, h = bh / p.B;
+  const int bh_count = p.B * p.H;
+  const int n_items = p.n_qtiles * bh_count;
   const int n_kt_all = (p.S + kKTile - 1) / kKTile;
-  const int nk = p.causal ? min(n_kt_all, qt + 1) : n_kt_all;
+  // item w: query tile n_qtiles - 1 - w / (B H) (the longest causal tiles first), batch-head w % (B H)
+  auto item_of = [&](int w, int& qt, int& b, int& h, int& nk) {
+    qt = p.n_qtiles - 1 - w / bh_count;
+    const int bh = w % bh_count;
+    b = bh % p.B;
+    h = bh / p.B;
+    nk = p.causal ? min(n_kt_all, qt + 1) : n_kt_all;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kFwdKvStages; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -198,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       mbar_init(p_full + s, 8);
       mbar_init(pv_done + s, 1);
     }
+    mbar_init(o_empty, 8);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -216,25 +232,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ producer
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
-      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
-      for (int j = 0; j < nk; ++j) {
-        const int st = j % kFwdKvStages;
-        const uint32_t ph = static_cast<uint32_t>(j / kFwdKvStages) & 1u;
-        if (!wait_spin(k_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(k_full + st, kTileBytes);
-        load_tile(sK + st * kTileBytes, &p.tmK, k_full + st, h, b, j * kKTile);
-        k_issued |= 1u << st;
-        k_par = (k_par & ~(1u << st)) | (ph << st);
-        if (!wait_spin(v_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(v_full + st, kTileBytes);
-        load_tile(sV + st * kTileBytes, &p.tmV, v_full + st, h, b, j * kKTile);
-        v_issued |= 1u << st;
-        v_par = (v_par & ~(1u << st)) | (ph << st);
+      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0, q_par = 0;
+      bool q_issued = false, ok = true;
+      int g = 0;  // key tiles issued so far, over all items
+      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+        int qt, b, h, nk;
+        item_of(w, qt, b, h, nk);
+        if (it >= 1 && !wait_spin(q_empty, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnQEmpty)) break;
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
+        q_issued = true;
+        q_par = static_cast<uint32_t>(it) & 1u;
+        for (int j = 0; j < nk; ++j, ++g) {
+          const int st = g % kFwdKvStages;
+          const uint32_t ph = static_cast<uint32_t>(g / kFwdKvStages) & 1u;
+          if (!wait_spin(k_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full + st, kTileBytes);
+          load_tile(sK + st * kTileBytes, &p.tmK, k_full + st, h, b, j * kKTile);
+          k_issued |= 1u << st;
+          k_par = (k_par & ~(1u << st)) | (ph << st);
+          if (!wait_spin(v_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full + st, kTileBytes);
+          load_tile(sV + st * kTileBytes, &p.tmV, v_full + st, h, b, j * kKTile);
+          v_issued |= 1u << st;
+          v_par = (v_par & ~(1u << st)) | (ph << st);
+        }
       }
       // copies in flight land before shared memory is released
-      wait_drain(q_full, 0, p.timeout_ns);
+      if (q_issued) wait_drain(q_full, q_par, p.timeout_ns);
       for (int s = 0; s < kFwdKvStages; ++s) {
         if (k_issued & (1u << s)) wait_drain(k_full + s, (k_par >> s) & 1u, p.timeout_ns);
         if (v_issued & (1u << s)) wait_drain(v_full + s, (v_par >> s) & 1u, p.timeout_ns);
@@ -243,46 +274,66 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------------ MMA issuer
-      // step j: S_j = Q K_j^T (j < nk) into S buffer j % 2, then O += P_{j-1} V_{j-1} (j >= 1): O stays
-      // in TMEM across the key tiles
+      // step j of an item: S_j = Q K_j^T (j < nk) into S buffer g % 2, then O += P_{j-1} V_{j-1} (j >= 1):
+      // O stays in TMEM across the item's key tiles (g = the running key-tile count)
       constexpr uint32_t idesc_s = idesc_bf16_f32(kQTile, kKTile, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kQTile, kHd, false, true);
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t o_tmem = tmem_base + 256;
-      bool ok = wait_spin(q_full, 0, wc, kSiteAttnQ);
-      if (ok) tc_fence_after_sync();
-      for (int j = 0; ok && j <= nk; ++j) {
-        if (j < nk) {
-          const int sb = j & 1;
-          const int st = j % kFwdKvStages;
-          if (!wait_spin(s_empty + sb, (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
-          if (!wait_spin(k_full + st, static_cast<uint32_t>(j / kFwdKvStages) & 1u, wc, kSiteAttnKv)) break;
-          tc_fence_after_sync();
-          const uint32_t k_base = smem_u32(sK + st * kTileBytes);
+      bool ok = true;
+      int g0 = 0;
+      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+        int qt, b, h, nk;
+        item_of(w, qt, b, h, nk);
+        if (!wait_spin(q_full, static_cast<uint32_t>(it) & 1u, wc, kSiteAttnQ)) break;
+        tc_fence_after_sync();
+        for (int j = 0; ok && j <= nk; ++j) {
+          if (j < nk) {
+            const int gj = g0 + j;
+            const int sb = gj & 1;
+            const int st = gj % kFwdKvStages;
+            if (!wait_spin(s_empty + sb, (static_cast<uint32_t>(gj >> 1) & 1u) ^ 1u, wc, kSiteAttnSEmpty) ||
+                !wait_spin(k_full + st, static_cast<uint32_t>(gj / kFwdKvStages) & 1u, wc, kSiteAttnKv)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t k_base = smem_u32(sK + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kHd / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base + sb * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
-                      idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kHd / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+              umma_bf16(tmem_base + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
+                        sdesc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(s_full + sb);
+            umma_commit(k_empty + st);
+            if (j == nk - 1) umma_commit(q_empty);  // the item's last score MMA: Q may be reloaded
           }
-          umma_commit(s_full + sb);
-          umma_commit(k_empty + st);
-        }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int pb = jj & 1;
-          const int st = jj % kFwdKvStages;
-          if (!wait_spin(p_full + pb, static_cast<uint32_t>(jj >> 1) & 1u, wc, kSiteAttnP)) break;
-          if (!wait_spin(v_full + st, static_cast<uint32_t>(jj / kFwdKvStages) & 1u, wc, kSiteAttnKv)) break;
-          tc_fence_after_sync();
-          const uint32_t v_base = smem_u32(sV + st * kTileBytes);
+          if (j >= 1) {
+            const int gj = g0 + j - 1;
+            const int pb = gj & 1;
+            const int st = gj % kFwdKvStages;
+            // the item's first P V overwrites O: the previous item's epilogue must have read it
+            if (j == 1 && it >= 1 && !wait_spin(o_empty, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnOEmpty)) {
+              ok = false;
+              break;
+            }
+            if (!wait_spin(p_full + pb, static_cast<uint32_t>(gj >> 1) & 1u, wc, kSiteAttnP) ||
+                !wait_spin(v_full + st, static_cast<uint32_t>(gj / kFwdKvStages) & 1u, wc, kSiteAttnKv)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t v_base = smem_u32(sV + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kKTile / 16; ++kk)
-            umma_bf16_tmem_a(o_tmem, tmem_base + 384 + 64 * pb + 8 * kk, sdesc_sw128(v_base + kk * 2048, kAtom, 1024),
-                             idesc_pv, (jj | kk) != 0 ? 1u : 0u);
-          umma_commit(pv_done + pb);
-          umma_commit(v_empty + st);
+            for (int kk = 0; kk < kKTile / 16; ++kk)
+              umma_bf16_tmem_a(o_tmem, tmem_base + 384 + 64 * pb + 8 * kk,
+                               sdesc_sw128(v_base + kk * 2048, kAtom, 1024), idesc_pv, (j > 1 || kk > 0) ? 1u : 0u);
+            umma_commit(pv_done + pb);
+            umma_commit(v_empty + st);
+          }
         }
+        g0 += nk;
       }
       umma_commit(drain);
       wait_drain(drain, 0, p.timeout_ns);
@@ -301,145 +352,163 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
     const int half = (warp - 2) >> 2;
     const int pair_bar = 1 + quad;        // named barrier of the two warps of this quadrant
     const int r = quad * 32 + static_cast<int>(lane);  // row within the tile = TMEM lane
-    const int q = qt * kQTile + r;                      // query position
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nk; ++j) {
-      const int sb = j & 1, pb = j & 1;
-      int w_ok = 1;
-      if (lane == 0) w_ok = wait_spin(s_full + sb, static_cast<uint32_t>(j >> 1) & 1u, wc, kSiteAttnS) ? 1 : 0;
-      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-      // both warps of the pair learn each other's outcome at the barrier below, so they leave together
-      tc_fence_after_sync();
-      float sc[2][32];  // this half's 64 raw scores
-      if (w_ok) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(sb * 128 + 64 * half + 32 * c), sc[c]);
-        tmem_wait_ld();
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0 && w_ok) mbar_arrive(s_empty + sb);
-      const int key0 = j * kKTile + 64 * half;
-      const int key_end = p.causal ? min(p.S, q + 1) : p.S;  // visible keys: [0, key_end)
-      // raw scores; invisible keys become -inf (only tiles that reach past some row's last key need it)
-      if (!__all_sync(0xffffffffu, key0 + 64 <= key_end)) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (key0 + 32 * c + i >= key_end) sc[c][i] = -INFINITY;
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sc[c][i]);
-      mx *= p.scale_log2;  // the scale is positive: the maximum of the scaled scores
-      // Both warps of the pair pass the same named barriers: a failed wait anywhere in a tile travels to
-      // the partner as NaN through the next exchange, and the pair leaves the loop there together.
-      xchg[half][r] = ok && w_ok ? mx : NAN;
-      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-      const float other = xchg[half ^ 1][r];
-      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");  // both read before the next write
-      if (!(ok && w_ok) || __any_sync(0xffffffffu, isnan(other))) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, other);
-      const bool move = mx > m + kRescaleLog2;
-      const float m_new = move ? mx : m;
-      const float alpha = move ? (m == -INFINITY ? 0.f : ex2_approx(m - m_new)) : 1.f;
-      l *= alpha;
-      // O (the tiles before j, once their P V is done) rescaled in TMEM where a row of the warp moved;
-      // each half rescales its 64 columns
-      if (j >= 1 && __any_sync(0xffffffffu, move)) {
-        const int pj = j - 1;
-        if (lane == 0)
-          w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-          ok = false;  // finish the tile without touching TMEM or P; the next exchange ends the pair
-          continue;
-        }
+    int g0 = 0;
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      int qt, b, h, nk;
+      item_of(w, qt, b, h, nk);
+      const int q = qt * kQTile + r;  // query position
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nk; ++j) {
+        const int gj = g0 + j;
+        const int sb = gj & 1, pb = gj & 1;
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_spin(s_full + sb, static_cast<uint32_t>(gj >> 1) & 1u, wc, kSiteAttnS) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        // both warps of the pair learn each other's outcome at the barrier below, so they leave together
         tc_fence_after_sync();
+        float sc[2][32];  // this half's 64 raw scores
+        if (w_ok) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t addr = lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c);
-          uint32_t o[32];
-          tmem_ld32_nowait(addr, o);
+          for (int c = 0; c < 2; ++c)
+            tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(sb * 128 + 64 * half + 32 * c), sc[c]);
           tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(addr, o);
         }
-        tmem_wait_st();
-      }
-      m = m_new;
-      const float m_use = m == -INFINITY ? 0.f : m;  // a row with nothing visible yet keeps p = 0
-      // P_j into buffer j % 2, once the P V that last read that buffer (tile j - 2) is done
-      if (j >= 2) {
-        const int pj = j - 2;
-        if (lane == 0)
-          w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-          ok = false;  // as above
-          continue;
-        }
-      }
-      // P_j in bf16 pairs into TMEM buffer j % 2 (this half's 64 keys: 32 columns), the A operand of P V
-      float psum = 0.f;
-      uint32_t pw[32];
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0 && w_ok) mbar_arrive(s_empty + sb);
+        const int key0 = j * kKTile + 64 * half;
+        const int key_end = p.causal ? min(p.S, q + 1) : p.S;  // visible keys: [0, key_end)
+        // raw scores; invisible keys become -inf (only tiles that reach past some row's last key need it)
+        if (!__all_sync(0xffffffffu, key0 + 64 <= key_end)) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float e0 = ex2_approx(fmaf(sc[i >> 4][2 * (i & 15)], p.scale_log2, -m_use));
-        const float e1 = ex2_approx(fmaf(sc[i >> 4][2 * (i & 15) + 1], p.scale_log2, -m_use));
-        psum += e0 + e1;
-        pw[i] = pack_bf16x2(e0, e1);
-      }
-      l += psum;
-      tmem_st32(lane_base + 384u + static_cast<uint32_t>(64 * pb + 32 * half), pw);
-      // P_j (and any rescaled O) handed to the MMA
-      tmem_wait_st();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + pb);
-    }
-    // the row sum of both halves (the pair left the loop at the same tile: the exchange buffer is free)
-    xchg[half][r] = ok ? l : NAN;
-    asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-    const float l_all = xchg[0][r] + xchg[1][r];
-    if (ok && !isnan(l_all) && nk > 0) {
-      const int pj = nk - 1;
-      int w_ok = 1;
-      if (lane == 0)
-        w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, w_ok, 0)) {
-        tc_fence_after_sync();
-        uint32_t o[2][32];
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (key0 + 32 * c + i >= key_end) sc[c][i] = -INFINITY;
+        }
+        float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 2; ++c)
-          tmem_ld32_nowait(lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
-        tmem_wait_ld();
-        if (p.lse != nullptr && half == 0 && q < p.S)
-          p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + q] = m + log2f(l_all);
-        if (q < p.S) {
-          const float inv_l = l_all > 0.f ? 1.f / l_all : 0.f;
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                (static_cast<long long>(q) * p.B + b) *
-                                                    (static_cast<long long>(p.H) * kHd) +
-                                                static_cast<long long>(h) * kHd + 64 * half);
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint32_t* y = o[g / 4] + 8 * (g % 4);
-            dst[g] = make_uint4(pack_bf16x2(__uint_as_float(y[0]) * inv_l, __uint_as_float(y[1]) * inv_l),
-                                pack_bf16x2(__uint_as_float(y[2]) * inv_l, __uint_as_float(y[3]) * inv_l),
-                                pack_bf16x2(__uint_as_float(y[4]) * inv_l, __uint_as_float(y[5]) * inv_l),
-                                pack_bf16x2(__uint_as_float(y[6]) * inv_l, __uint_as_float(y[7]) * inv_l));
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, sc[c][i]);
+        mx *= p.scale_log2;  // the scale is positive: the maximum of the scaled scores
+        // Both warps of the pair pass the same named barriers: a failed wait anywhere in a tile travels to
+        // the partner as NaN through the next exchange, and the pair leaves the loop there together.
+        xchg[half][r] = ok && w_ok ? mx : NAN;
+        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+        const float other = xchg[half ^ 1][r];
+        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");  // both read before the next write
+        if (!(ok && w_ok) || __any_sync(0xffffffffu, isnan(other))) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, other);
+        const bool move = mx > m + kRescaleLog2;
+        const float m_new = move ? mx : m;
+        const float alpha = move ? (m == -INFINITY ? 0.f : ex2_approx(m - m_new)) : 1.f;
+        l *= alpha;
+        // O (the item's tiles before j, once their P V is done) rescaled in TMEM where a row of the warp
+        // moved; each half rescales its 64 columns
+        if (j >= 1 && __any_sync(0xffffffffu, move)) {
+          const int pj = gj - 1;
+          if (lane == 0)
+            w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+            ok = false;  // finish the tile without touching TMEM or P; the next exchange ends the pair
+            continue;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t addr = lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c);
+            uint32_t o[32];
+            tmem_ld32_nowait(addr, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(addr, o);
+          }
+          tmem_wait_st();
+        }
+        m = m_new;
+        const float m_use = m == -INFINITY ? 0.f : m;  // a row with nothing visible yet keeps p = 0
+        // P into buffer g % 2, once the P V that last read that buffer (two key tiles earlier, possibly
+        // in the previous item) is done
+        if (gj >= 2) {
+          const int pj = gj - 2;
+          if (lane == 0)
+            w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+            ok = false;  // as above
+            continue;
           }
         }
+        // P in bf16 pairs into TMEM buffer g % 2 (this half's 64 keys: 32 columns), the A operand of P V
+        float psum = 0.f;
+        uint32_t pw[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float e0 = ex2_approx(fmaf(sc[i >> 4][2 * (i & 15)], p.scale_log2, -m_use));
+          const float e1 = ex2_approx(fmaf(sc[i >> 4][2 * (i & 15) + 1], p.scale_log2, -m_use));
+          psum += e0 + e1;
+          pw[i] = pack_bf16x2(e0, e1);
+        }
+        l += psum;
+        tmem_st32(lane_base + 384u + static_cast<uint32_t>(64 * pb + 32 * half), pw);
+        // P (and any rescaled O) handed to the MMA
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + pb);
       }
+      // the row sum of both halves (the pair left the loop at the same tile: the exchange buffer is free);
+      // the second barrier keeps the next item's first exchange from overwriting it before both have read
+      xchg[half][r] = ok ? l : NAN;
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+      const float l_all = xchg[0][r] + xchg[1][r];
+      asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+      if (ok && isnan(l_all)) ok = false;
+      if (ok && nk > 0) {
+        const int pj = g0 + nk - 1;
+        int w_ok = 1;
+        if (lane == 0)
+          w_ok = wait_spin(pv_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, w_ok, 0)) {
+          tc_fence_after_sync();
+          uint32_t o[2][32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tmem_ld32_nowait(lane_base + 256u + static_cast<uint32_t>(64 * half + 32 * c), o[c]);
+          tmem_wait_ld();
+          if (p.lse != nullptr && half == 0 && q < p.S)
+            p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + q] = m + log2f(l_all);
+          if (q < p.S) {
+            const float inv_l = l_all > 0.f ? 1.f / l_all : 0.f;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                  (static_cast<long long>(q) * p.B + b) *
+                                                      (static_cast<long long>(p.H) * kHd) +
+                                                  static_cast<long long>(h) * kHd + 64 * half);
+#pragma unroll
+            for (int gg = 0; gg < 8; ++gg) {
+              const uint32_t* y = o[gg / 4] + 8 * (gg % 4);
+              dst[gg] = make_uint4(pack_bf16x2(__uint_as_float(y[0]) * inv_l, __uint_as_float(y[1]) * inv_l),
+                                   pack_bf16x2(__uint_as_float(y[2]) * inv_l, __uint_as_float(y[3]) * inv_l),
+                                   pack_bf16x2(__uint_as_float(y[4]) * inv_l, __uint_as_float(y[5]) * inv_l),
+                                   pack_bf16x2(__uint_as_float(y[6]) * inv_l, __uint_as_float(y[7]) * inv_l));
+            }
+          }
+        }
+        // a failed wait here leaves `ok` as it is: `ok` changes only where both warps of the pair see the
+        // same values (the exchanges), so they leave the item loop together; the wait raised the CTA's
+        // abort flag, so the next item's first wait fails in both and the exchange ends them
+      }
+      // this warp has read the item's O: the next item's first P V may overwrite it
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+      g0 += nk;
     }
   }
 
@@ -1035,12 +1104,14 @@ cudaError_t launch_attention(const void* qkv, int S, int B, int H, bool causal, 
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHd)));
   p.err = ctx.err;
   p.timeout_ns = ctx.timeout_ns;
-  const long long grid = static_cast<long long>(p.n_qtiles) * B * H;
-  if (grid > INT_MAX) return cudaErrorInvalidValue;
+  const long long items = static_cast<long long>(p.n_qtiles) * B * H;
+  if (items > INT_MAX) return cudaErrorInvalidValue;
+  // persistent: one CTA per SM (the shared memory allows no second), each walking its share of the items
+  const int grid = static_cast<int>(items < ctx.sm_count ? items : ctx.sm_count);
   cudaError_t e = cudaFuncSetAttribute(k_attention_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kAttnSmem));
   if (e != cudaSuccess) return e;
-  k_attention_fwd<<<static_cast<int>(grid), kThreads, kAttnSmem, s>>>(p);
+  k_attention_fwd<<<grid, kThreads, kAttnSmem, s>>>(p);
   return cudaGetLastError();
 }
 
