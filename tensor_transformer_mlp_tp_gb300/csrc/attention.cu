@@ -17,9 +17,9 @@
 //            memory, a reference maximum moves (rescaling O in TMEM) only when a
 //            tile's maximum exceeds it by 2^8, and P = exp2(S - m) goes to TMEM
 //            in bf16 pairs; the row's denominator and log-sum-exp come at the end.
-// Backward core: D = rowsum(dO O); a dQ kernel per query tile and a dK/dV kernel
-// per key tile recompute S and dP in TMEM and write P, dS in bf16 to TMEM for the
-// gradient MMAs (described at each kernel).  Causal attention masks inside the
+// Backward core: D = rowsum(dO O); a dQ kernel over query tiles and a dK/dV kernel
+// over key tiles (persistent, like the forward) recompute S and dP in TMEM and write
+// P, dS in bf16 to TMEM for the gradient MMAs (described at each kernel).  Causal attention masks inside the
 // tiles that reach past a row's last key; positions at or past S are masked.
 // Every wait is bounded (error word + abort flag), and each CTA drains its copies
 // and MMAs before it releases TMEM.
@@ -611,7 +611,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
   uint8_t* sV = sK + kDqKStages * kTileBytes;      // 2 stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kKvStages * kTileBytes);
   uint64_t* q_full = bars;                          // Q and dO
-  uint64_t* k_full = q_full + 1;
+  uint64_t* q_empty = q_full + 1;                   // the item's last S and dP MMAs have read Q and dO
+  uint64_t* k_full = q_empty + 1;
   uint64_t* k_empty = k_full + kDqKStages;
   uint64_t* v_full = k_empty + kDqKStages;
   uint64_t* v_empty = v_full + kKvStages;
@@ -619,18 +620,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
   uint64_t* s_empty = s_full + 1;                   // both read by every compute warp
   uint64_t* ds_full = s_empty + 1;                  // [buffer]: dS_j written
   uint64_t* dq_done = ds_full + 2;                  // [buffer]: dQ += dS_j K_j done (buffer free)
-  uint64_t* drain = dq_done + 2;
+  uint64_t* dq_read = dq_done + 2;                  // the compute warps have read the item's dQ
+  uint64_t* drain = dq_read + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
-  const int qt = p.n_tiles - 1 - static_cast<int>(blockIdx.x % p.n_tiles);
-  const int bh = static_cast<int>(blockIdx.x / p.n_tiles);
-  const int b = bh % p.B, h = bh / p.B;
-  const int nk = p.causal ? min(p.n_tiles, qt + 1) : p.n_tiles;
+  const int bh_count = p.B * p.H;
+  const int n_items = p.n_tiles * bh_count;
+  // item w: query tile n_tiles - 1 - w / (B H) (the longest causal tiles first), batch-head w % (B H)
+  auto item_of = [&](int w, int& qt, int& b, int& h, int& nk) {
+    qt = p.n_tiles - 1 - w / bh_count;
+    const int bh = w % bh_count;
+    b = bh % p.B;
+    h = bh / p.B;
+    nk = p.causal ? min(p.n_tiles, qt + 1) : p.n_tiles;
+  };
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kDqKStages; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -645,6 +654,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
       mbar_init(ds_full + x, kBwdComputeWarps);
       mbar_init(dq_done + x, 1);
     }
+    mbar_init(dq_read, kBwdComputeWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -662,25 +672,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-      load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
-      load_tile(sdO, &p.tmdO, q_full, h, b, qt * kQTile);
-      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
-      for (int j = 0; j < nk; ++j) {
-        const int sk = j % kDqKStages, sv = j % kKvStages;
-        const uint32_t pk = static_cast<uint32_t>(j / kDqKStages) & 1u, pv = static_cast<uint32_t>(j / kKvStages) & 1u;
-        if (!wait_spin(k_empty + sk, pk ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(k_full + sk, kTileBytes);
-        load_tile(sK + sk * kTileBytes, &p.tmK, k_full + sk, h, b, j * kKTile);
-        k_issued |= 1u << sk;
-        k_par = (k_par & ~(1u << sk)) | (pk << sk);
-        if (!wait_spin(v_empty + sv, pv ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(v_full + sv, kTileBytes);
-        load_tile(sV + sv * kTileBytes, &p.tmV, v_full + sv, h, b, j * kKTile);
-        v_issued |= 1u << sv;
-        v_par = (v_par & ~(1u << sv)) | (pv << sv);
+      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0, q_par = 0;
+      bool q_issued = false, ok = true;
+      int g = 0;  // key tiles issued so far, over all items
+      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+        int qt, b, h, nk;
+        item_of(w, qt, b, h, nk);
+        if (it >= 1 && !wait_spin(q_empty, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnQEmpty)) break;
+        mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+        load_tile(sQ, &p.tmQ, q_full, h, b, qt * kQTile);
+        load_tile(sdO, &p.tmdO, q_full, h, b, qt * kQTile);
+        q_issued = true;
+        q_par = static_cast<uint32_t>(it) & 1u;
+        for (int j = 0; j < nk; ++j, ++g) {
+          const int sk = g % kDqKStages, sv = g % kKvStages;
+          const uint32_t pk = static_cast<uint32_t>(g / kDqKStages) & 1u, pv = static_cast<uint32_t>(g / kKvStages) & 1u;
+          if (!wait_spin(k_empty + sk, pk ^ 1u, wc, kSiteAttnKvEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full + sk, kTileBytes);
+          load_tile(sK + sk * kTileBytes, &p.tmK, k_full + sk, h, b, j * kKTile);
+          k_issued |= 1u << sk;
+          k_par = (k_par & ~(1u << sk)) | (pk << sk);
+          if (!wait_spin(v_empty + sv, pv ^ 1u, wc, kSiteAttnKvEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full + sv, kTileBytes);
+          load_tile(sV + sv * kTileBytes, &p.tmV, v_full + sv, h, b, j * kKTile);
+          v_issued |= 1u << sv;
+          v_par = (v_par & ~(1u << sv)) | (pv << sv);
+        }
       }
-      wait_drain(q_full, 0, p.timeout_ns);
+      if (q_issued) wait_drain(q_full, q_par, p.timeout_ns);
       for (int s = 0; s < kDqKStages; ++s)
         if (k_issued & (1u << s)) wait_drain(k_full + s, (k_par >> s) & 1u, p.timeout_ns);
       for (int s = 0; s < kKvStages; ++s)
@@ -691,46 +716,66 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
       constexpr uint32_t idesc_kk = idesc_bf16_f32(kQTile, kKTile, false, false);  // both K-major
       constexpr uint32_t idesc_mn = idesc_bf16_f32(kQTile, kHd, false, true);       // B MN-major
       const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sdO);
-      bool ok = wait_spin(q_full, 0, wc, kSiteAttnQ);
-      if (ok) tc_fence_after_sync();
-      // step j: S_j and dP_j (j < nk), then dQ += dS_{j-1} K_{j-1} (j >= 1)
-      for (int j = 0; ok && j <= nk; ++j) {
-        if (j < nk) {
-          const int sk = j % kDqKStages, sv = j % kKvStages;
-          if (!wait_spin(s_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, wc, kSiteAttnSEmpty)) break;
-          if (!wait_spin(k_full + sk, static_cast<uint32_t>(j / kDqKStages) & 1u, wc, kSiteAttnKv)) break;
-          if (!wait_spin(v_full + sv, static_cast<uint32_t>(j / kKvStages) & 1u, wc, kSiteAttnKv)) break;
-          tc_fence_after_sync();
-          const uint32_t k_base = smem_u32(sK + sk * kTileBytes), v_base = smem_u32(sV + sv * kTileBytes);
+      bool ok = true;
+      int g0 = 0;
+      // step j of an item: S_j and dP_j (j < nk), then dQ += dS_{j-1} K_{j-1} (j >= 1); g = running tile count
+      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+        int qt, b, h, nk;
+        item_of(w, qt, b, h, nk);
+        if (!wait_spin(q_full, static_cast<uint32_t>(it) & 1u, wc, kSiteAttnQ)) break;
+        tc_fence_after_sync();
+        for (int j = 0; ok && j <= nk; ++j) {
+          if (j < nk) {
+            const int gj = g0 + j;
+            const int sk = gj % kDqKStages, sv = gj % kKvStages;
+            if (!wait_spin(s_empty, (static_cast<uint32_t>(gj) & 1u) ^ 1u, wc, kSiteAttnSEmpty) ||
+                !wait_spin(k_full + sk, static_cast<uint32_t>(gj / kDqKStages) & 1u, wc, kSiteAttnKv) ||
+                !wait_spin(v_full + sv, static_cast<uint32_t>(gj / kKvStages) & 1u, wc, kSiteAttnKv)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t k_base = smem_u32(sK + sk * kTileBytes), v_base = smem_u32(sV + sv * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kHd / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idesc_kk,
-                      kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kHd / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+              umma_bf16(tmem_base, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idesc_kk,
+                        kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kHd / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+              umma_bf16(tmem_base + 128, sdesc_sw128(do_base + off, 16, 1024), sdesc_sw128(v_base + off, 16, 1024),
+                        idesc_kk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(s_full);
+            umma_commit(v_empty + sv);
+            if (j == nk - 1) umma_commit(q_empty);  // the item's last S and dP: Q and dO may be reloaded
           }
+          if (j >= 1) {
+            const int gj = g0 + j - 1;
+            const int st = gj % kDqKStages;
+            const int buf = gj & 1;
+            // the item's first dQ MMA overwrites dQ: the previous item's epilogue must have read it
+            if (j == 1 && it >= 1 && !wait_spin(dq_read, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnOEmpty)) {
+              ok = false;
+              break;
+            }
+            if (!wait_spin(ds_full + buf, static_cast<uint32_t>(gj >> 1) & 1u, wc, kSiteAttnP)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t k_base = smem_u32(sK + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kHd / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base + 128, sdesc_sw128(do_base + off, 16, 1024), sdesc_sw128(v_base + off, 16, 1024),
-                      idesc_kk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kKTile / 16; ++kk)
+              umma_bf16_tmem_a(tmem_base + 256, tmem_base + 384 + 64 * buf + 8 * kk,
+                               sdesc_sw128(k_base + kk * 2048, kAtom, 1024), idesc_mn, (j > 1 || kk > 0) ? 1u : 0u);
+            umma_commit(dq_done + buf);
+            umma_commit(k_empty + st);
           }
-          umma_commit(s_full);
-          umma_commit(v_empty + sv);
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int st = jj % kDqKStages;
-          const int buf = jj & 1;
-          if (!wait_spin(ds_full + buf, static_cast<uint32_t>(jj >> 1) & 1u, wc, kSiteAttnP)) break;
-          tc_fence_after_sync();
-          const uint32_t k_base = smem_u32(sK + st * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kKTile / 16; ++kk)
-            umma_bf16_tmem_a(tmem_base + 256, tmem_base + 384 + 64 * buf + 8 * kk,
-                             sdesc_sw128(k_base + kk * 2048, kAtom, 1024), idesc_mn, (jj | kk) != 0 ? 1u : 0u);
-          umma_commit(dq_done + buf);
-          umma_commit(k_empty + st);
-        }
+        g0 += nk;
       }
       umma_commit(drain);
       wait_drain(drain, 0, p.timeout_ns);
@@ -739,73 +784,89 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
     const int quad = warp & 3;
     const int quarter = (warp - 2) >> 2;  // keys 32 quarter .. 32 quarter + 31 of every tile
     const int r = quad * 32 + static_cast<int>(lane);
-    const int q = qt * kQTile + r;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    const long long stat = (static_cast<long long>(b) * p.H + h) * p.s_pad + q;
-    const float neg_lse = q < p.S ? -__ldg(p.lse + stat) : 0.f;
-    const float dd = q < p.S ? __ldg(p.delta + stat) : 0.f;
-    const int key_end = q < p.S ? (p.causal ? min(p.S, q + 1) : p.S) : 0;  // padding rows: nothing
     bool ok = true;
-    for (int j = 0; ok && j < nk; ++j) {
-      int w_ok = 1;
-      if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(j) & 1u, wc, kSiteAttnS) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      float sc[32], dp[32];
-      tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(32 * quarter), sc);
-      tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(32 * quarter), dp);
-      tmem_wait_ld();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
-      const int key0 = j * kKTile + 32 * quarter;
-      if (__all_sync(0xffffffffu, key0 + 32 <= key_end)) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = fmaf(sc[i], p.scale_log2, neg_lse);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = key0 + i < key_end ? ex2_approx(fmaf(sc[i], p.scale_log2, neg_lse)) : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) dp[i] = sc[i] * (dp[i] - dd);  // dS
-      uint32_t w[16];
-      pack_pairs(dp, w);
-      const int buf = j & 1;
-      // the buffer is free once the dQ MMA of tile j - 2 has read it
-      if (j >= 2) {
-        if (lane == 0) w_ok = wait_spin(dq_done + buf, static_cast<uint32_t>((j - 2) >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+    int g0 = 0;
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      int qt, b, h, nk;
+      item_of(w, qt, b, h, nk);
+      const int q = qt * kQTile + r;
+      const long long stat = (static_cast<long long>(b) * p.H + h) * p.s_pad + q;
+      const float neg_lse = q < p.S ? -__ldg(p.lse + stat) : 0.f;
+      const float dd = q < p.S ? __ldg(p.delta + stat) : 0.f;
+      const int key_end = q < p.S ? (p.causal ? min(p.S, q + 1) : p.S) : 0;  // padding rows: nothing
+      for (int j = 0; ok && j < nk; ++j) {
+        const int gj = g0 + j;
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(gj) & 1u, wc, kSiteAttnS) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
+        float sc[32], dp[32];
+        tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(32 * quarter), sc);
+        tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(32 * quarter), dp);
+        tmem_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty);
+        const int key0 = j * kKTile + 32 * quarter;
+        if (__all_sync(0xffffffffu, key0 + 32 <= key_end)) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sc[i] = fmaf(sc[i], p.scale_log2, neg_lse);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sc[i] = key0 + i < key_end ? ex2_approx(fmaf(sc[i], p.scale_log2, neg_lse)) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dp[i] = sc[i] * (dp[i] - dd);  // dS
+        uint32_t wds[16];
+        pack_pairs(dp, wds);
+        const int buf = gj & 1;
+        // the buffer is free once the dQ MMA of the key tile two before (possibly the previous item's) read it
+        if (gj >= 2) {
+          if (lane == 0)
+            w_ok = wait_spin(dq_done + buf, static_cast<uint32_t>((gj - 2) >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        tmem_st16(lane_base + 384u + static_cast<uint32_t>(64 * buf + 16 * quarter), wds);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full + buf);
       }
-      tmem_st16(lane_base + 384u + static_cast<uint32_t>(64 * buf + 16 * quarter), w);
-      tmem_wait_st();
+      if (ok && nk > 0) {
+        // the item's last dQ commit covers every earlier MMA
+        const int pj = g0 + nk - 1;
+        int w_ok = 1;
+        if (lane == 0)
+          w_ok = wait_spin(dq_done + (pj & 1), static_cast<uint32_t>(pj >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, w_ok, 0)) {
+          tc_fence_after_sync();
+          float o[32];
+          tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(32 * quarter), o);
+          tmem_wait_ld();
+          if (q < p.S)
+            store_row32_scaled(static_cast<__nv_bfloat16*>(p.dqkv) +
+                                   (static_cast<long long>(q) * p.B + b) * (3LL * p.H * kHd) +
+                                   static_cast<long long>(h) * kHd + 32 * quarter,
+                               o, p.scale);
+        } else {
+          ok = false;
+        }
+      }
+      // this warp has read the item's dQ: the next item's first dQ MMA may overwrite it
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full + buf);
-    }
-    if (ok && nk > 0) {
-      // the last dQ commit covers every earlier MMA
-      int w_ok = 1;
-      if (lane == 0)
-        w_ok = wait_spin(dq_done + ((nk - 1) & 1), static_cast<uint32_t>((nk - 1) >> 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, w_ok, 0)) {
-        tc_fence_after_sync();
-        float o[32];
-        tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(32 * quarter), o);
-        tmem_wait_ld();
-        if (q < p.S)
-          store_row32_scaled(static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<long long>(q) * p.B + b) * (3LL * p.H * kHd) +
-                                 static_cast<long long>(h) * kHd + 32 * quarter,
-                             o, p.scale);
-      }
+      if (lane == 0) mbar_arrive(dq_read);
+      g0 += nk;
     }
   }
   tc_fence_before_sync();
@@ -832,24 +893,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
   float* sStat = reinterpret_cast<float*>(sdO + kKvStages * kTileBytes);  // [stage][lse, D][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kKvStages * 2 * kQTile);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = kv_full + 1;                  // [stage]: Q_i and dO_i
+  uint64_t* kv_empty = kv_full + 1;                // the item's last S^T and dP^T MMAs have read K and V
+  uint64_t* q_full = kv_empty + 1;                 // [stage]: Q_i and dO_i
   uint64_t* q_empty = q_full + kKvStages;
   uint64_t* s_full = q_empty + kKvStages;          // S^T_i and dP^T_i in TMEM
   uint64_t* p_full = s_full + 1;                   // P^T_i and dS^T_i written by every compute warp
   uint64_t* pd_done = p_full + 1;                  // dV and dK MMAs of tile i done (score columns free)
-  uint64_t* drain = pd_done + 1;
+  uint64_t* dkdv_read = pd_done + 1;               // the compute warps have read the item's dK and dV
+  uint64_t* drain = dkdv_read + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
-  const int kt = static_cast<int>(blockIdx.x % p.n_tiles);  // causal: the first key tiles have the most work
-  const int bh = static_cast<int>(blockIdx.x / p.n_tiles);
-  const int b = bh % p.B, h = bh / p.B;
-  const int i0 = p.causal ? kt : 0;
-  const int nq = p.n_tiles - i0;
+  const int bh_count = p.B * p.H;
+  const int n_items = p.n_tiles * bh_count;
+  // item w: key tile w / (B H) (causal: the first key tiles have the most query tiles), batch-head w % (B H);
+  // its query tiles i0 .. n_tiles - 1
+  auto item_of = [&](int w, int& kt, int& b, int& h, int& i0, int& nq) {
+    kt = w / bh_count;
+    const int bh = w % bh_count;
+    b = bh % p.B;
+    h = bh / p.B;
+    i0 = p.causal ? kt : 0;
+    nq = p.n_tiles - i0;
+  };
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
     for (int s = 0; s < kKvStages; ++s) {
       mbar_init(q_full + s, 1);
       mbar_init(q_empty + s, 1);
@@ -857,6 +928,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
     mbar_init(s_full, 1);
     mbar_init(p_full, kBwdComputeWarps);
     mbar_init(pd_done, 1);
+    mbar_init(dkdv_read, kBwdComputeWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -874,25 +946,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * kTileBytes);
-      load_tile(sK, &p.tmK, kv_full, h, b, kt * kKTile);
-      load_tile(sV, &p.tmV, kv_full, h, b, kt * kKTile);
-      uint32_t issued = 0, par = 0;
-      for (int t = 0; t < nq; ++t) {
-        const int st = t % kKvStages;
-        const uint32_t ph = static_cast<uint32_t>(t / kKvStages) & 1u;
-        if (!wait_spin(q_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) break;
-        mbar_arrive_expect_tx(q_full + st, 2 * kTileBytes + 2 * kQTile * 4);
-        load_tile(sQ + st * kTileBytes, &p.tmQ, q_full + st, h, b, (i0 + t) * kQTile);
-        load_tile(sdO + st * kTileBytes, &p.tmdO, q_full + st, h, b, (i0 + t) * kQTile);
-        // the tile's statistics (512 bytes each, 16-byte aligned: rows of s_pad floats, tiles of 128)
-        const long long st0 = (static_cast<long long>(b) * p.H + h) * p.s_pad + (i0 + t) * kQTile;
-        bulk_load(sStat + st * 2 * kQTile, p.lse + st0, kQTile * 4, q_full + st);
-        bulk_load(sStat + st * 2 * kQTile + kQTile, p.delta + st0, kQTile * 4, q_full + st);
-        issued |= 1u << st;
-        par = (par & ~(1u << st)) | (ph << st);
+      uint32_t issued = 0, par = 0, kv_par = 0;
+      bool kv_issued = false, ok = true;
+      int g = 0;  // query tiles issued so far, over all items
+      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+        int kt, b, h, i0, nq;
+        item_of(w, kt, b, h, i0, nq);
+        if (it >= 1 && !wait_spin(kv_empty, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnQEmpty)) break;
+        mbar_arrive_expect_tx(kv_full, 2 * kTileBytes);
+        load_tile(sK, &p.tmK, kv_full, h, b, kt * kKTile);
+        load_tile(sV, &p.tmV, kv_full, h, b, kt * kKTile);
+        kv_issued = true;
+        kv_par = static_cast<uint32_t>(it) & 1u;
+        for (int t = 0; t < nq; ++t, ++g) {
+          const int st = g % kKvStages;
+          const uint32_t ph = static_cast<uint32_t>(g / kKvStages) & 1u;
+          if (!wait_spin(q_empty + st, ph ^ 1u, wc, kSiteAttnKvEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(q_full + st, 2 * kTileBytes + 2 * kQTile * 4);
+          load_tile(sQ + st * kTileBytes, &p.tmQ, q_full + st, h, b, (i0 + t) * kQTile);
+          load_tile(sdO + st * kTileBytes, &p.tmdO, q_full + st, h, b, (i0 + t) * kQTile);
+          // the tile's statistics (512 bytes each, 16-byte aligned: rows of s_pad floats, tiles of 128)
+          const long long st0 = (static_cast<long long>(b) * p.H + h) * p.s_pad + (i0 + t) * kQTile;
+          bulk_load(sStat + st * 2 * kQTile, p.lse + st0, kQTile * 4, q_full + st);
+          bulk_load(sStat + st * 2 * kQTile + kQTile, p.delta + st0, kQTile * 4, q_full + st);
+          issued |= 1u << st;
+          par = (par & ~(1u << st)) | (ph << st);
+        }
       }
-      wait_drain(kv_full, 0, p.timeout_ns);
+      if (kv_issued) wait_drain(kv_full, kv_par, p.timeout_ns);
       for (int s = 0; s < kKvStages; ++s)
         if (issued & (1u << s)) wait_drain(q_full + s, (par >> s) & 1u, p.timeout_ns);
     }
@@ -901,39 +985,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
       constexpr uint32_t idesc_kk = idesc_bf16_f32(kKTile, kQTile, false, false);
       constexpr uint32_t idesc_mn = idesc_bf16_f32(kKTile, kHd, false, true);
       const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-      bool ok = wait_spin(kv_full, 0, wc, kSiteAttnQ);
-      if (ok) tc_fence_after_sync();
-      for (int t = 0; ok && t < nq; ++t) {
-        const int st = t % kKvStages;
-        if (!wait_spin(q_full + st, static_cast<uint32_t>(t / kKvStages) & 1u, wc, kSiteAttnKv)) break;
-        if (t >= 1 && !wait_spin(pd_done, static_cast<uint32_t>(t - 1) & 1u, wc, kSiteAttnSEmpty)) break;
+      bool ok = true;
+      int g0 = 0;
+      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+        int kt, b, h, i0, nq;
+        item_of(w, kt, b, h, i0, nq);
+        if (!wait_spin(kv_full, static_cast<uint32_t>(it) & 1u, wc, kSiteAttnQ)) break;
         tc_fence_after_sync();
-        const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
+        for (int t = 0; ok && t < nq; ++t) {
+          const int gt = g0 + t;  // running query-tile count: stages, score columns and barrier phases
+          const int st = gt % kKvStages;
+          if (!wait_spin(q_full + st, static_cast<uint32_t>(gt / kKvStages) & 1u, wc, kSiteAttnKv) ||
+              (gt >= 1 && !wait_spin(pd_done, static_cast<uint32_t>(gt - 1) & 1u, wc, kSiteAttnSEmpty))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kHd / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-          umma_bf16(tmem_base, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), idesc_kk,
-                    kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), idesc_kk,
+                      kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16(tmem_base + 128, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
+                      idesc_kk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
+          if (t == nq - 1) umma_commit(kv_empty);  // the item's last reads of K and V
+          // the item's first dV and dK MMAs overwrite them: the previous item's epilogue must have read them
+          if ((t == 0 && it >= 1 && !wait_spin(dkdv_read, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnOEmpty)) ||
+              !wait_spin(p_full, static_cast<uint32_t>(gt) & 1u, wc, kSiteAttnP)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < kQTile / 16; ++kk)
+            umma_bf16_tmem_a(tmem_base + 256, tmem_base + packed_col(kk), sdesc_sw128(do_base + kk * 2048, kAtom, 1024),
+                             idesc_mn, (t | kk) != 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kQTile / 16; ++kk)
+            umma_bf16_tmem_a(tmem_base + 384, tmem_base + 128 + packed_col(kk),
+                             sdesc_sw128(q_base + kk * 2048, kAtom, 1024), idesc_mn, (t | kk) != 0 ? 1u : 0u);
+          umma_commit(pd_done);
+          umma_commit(q_empty + st);
         }
-#pragma unroll
-        for (int kk = 0; kk < kHd / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-          umma_bf16(tmem_base + 128, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
-                    idesc_kk, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(s_full);
-        if (!wait_spin(p_full, static_cast<uint32_t>(t) & 1u, wc, kSiteAttnP)) break;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < kQTile / 16; ++kk)
-          umma_bf16_tmem_a(tmem_base + 256, tmem_base + packed_col(kk), sdesc_sw128(do_base + kk * 2048, kAtom, 1024),
-                           idesc_mn, (t | kk) != 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kQTile / 16; ++kk)
-          umma_bf16_tmem_a(tmem_base + 384, tmem_base + 128 + packed_col(kk),
-                           sdesc_sw128(q_base + kk * 2048, kAtom, 1024), idesc_mn, (t | kk) != 0 ? 1u : 0u);
-        umma_commit(pd_done);
-        umma_commit(q_empty + st);
+        g0 += nq;
       }
       umma_commit(drain);
       wait_drain(drain, 0, p.timeout_ns);
@@ -942,98 +1043,112 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
     const int quad = warp & 3;
     const int quarter = (warp - 2) >> 2;  // queries 32 quarter .. 32 quarter + 31 of every tile
     const int r = quad * 32 + static_cast<int>(lane);
-    const int k = kt * kKTile + r;  // key position
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
-    for (int t = 0; t < nq; ++t) {
-      const int q0 = (i0 + t) * kQTile + 32 * quarter;  // this warp's first query
-      int w_ok = 1;
-      if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(t) & 1u, wc, kSiteAttnS) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      float sc[32], dp[32];
-      tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(32 * quarter), sc);
-      tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(32 * quarter), dp);
-      tmem_wait_ld();
-      // the statistics of this warp's 32 queries, staged with Q and dO (all lanes read the same words)
-      const float4* l4 = reinterpret_cast<const float4*>(sStat + (t % kKvStages) * 2 * kQTile + 32 * quarter);
-      const float4* d4 = l4 + kQTile / 4;
-      // query q sees key k when q < S and (not causal or k <= q); only the diagonal and the ragged last
-      // tile need the test (the condition is the same for the whole warp)
-      if (q0 + 32 <= p.S && (!p.causal || q0 >= kt * kKTile + kKTile - 1)) {
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float4 l = l4[g];
-          sc[4 * g] = fmaf(sc[4 * g], p.scale_log2, -l.x);
-          sc[4 * g + 1] = fmaf(sc[4 * g + 1], p.scale_log2, -l.y);
-          sc[4 * g + 2] = fmaf(sc[4 * g + 2], p.scale_log2, -l.z);
-          sc[4 * g + 3] = fmaf(sc[4 * g + 3], p.scale_log2, -l.w);
+    int g0 = 0;
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      int kt, b, h, i0, nq;
+      item_of(w, kt, b, h, i0, nq);
+      const int k = kt * kKTile + r;  // key position
+      for (int t = 0; t < nq; ++t) {
+        const int gt = g0 + t;
+        const int q0 = (i0 + t) * kQTile + 32 * quarter;  // this warp's first query
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(gt) & 1u, wc, kSiteAttnS) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
         }
+        tc_fence_after_sync();
+        float sc[32], dp[32];
+        tmem_ld32f_nowait(lane_base + static_cast<uint32_t>(32 * quarter), sc);
+        tmem_ld32f_nowait(lane_base + 128u + static_cast<uint32_t>(32 * quarter), dp);
+        tmem_wait_ld();
+        // the statistics of this warp's 32 queries, staged with Q and dO (all lanes read the same words)
+        const float4* l4 = reinterpret_cast<const float4*>(sStat + (gt % kKvStages) * 2 * kQTile + 32 * quarter);
+        const float4* d4 = l4 + kQTile / 4;
+        // query q sees key k when q < S and (not causal or k <= q); only the diagonal and the ragged last
+        // tile need the test (the condition is the same for the whole warp)
+        if (q0 + 32 <= p.S && (!p.causal || q0 >= kt * kKTile + kKTile - 1)) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
+          for (int g = 0; g < 8; ++g) {
+            const float4 l = l4[g];
+            sc[4 * g] = fmaf(sc[4 * g], p.scale_log2, -l.x);
+            sc[4 * g + 1] = fmaf(sc[4 * g + 1], p.scale_log2, -l.y);
+            sc[4 * g + 2] = fmaf(sc[4 * g + 2], p.scale_log2, -l.z);
+            sc[4 * g + 3] = fmaf(sc[4 * g + 3], p.scale_log2, -l.w);
+          }
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float4 dd = d4[g];
-          dp[4 * g] = sc[4 * g] * (dp[4 * g] - dd.x);
-          dp[4 * g + 1] = sc[4 * g + 1] * (dp[4 * g + 1] - dd.y);
-          dp[4 * g + 2] = sc[4 * g + 2] * (dp[4 * g + 2] - dd.z);
-          dp[4 * g + 3] = sc[4 * g + 3] * (dp[4 * g + 3] - dd.w);
-        }
-      } else {
-        // a query past S reads unwritten statistics: the selects keep them out
-        const int q_end = p.causal ? min(p.S, q0 + 32) : p.S;
-        const int q_first = p.causal ? k : 0;  // visible: q_first <= q < q_end
+          for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float4 l = l4[g];
-          const float lv[4] = {l.x, l.y, l.z, l.w};
+          for (int g = 0; g < 8; ++g) {
+            const float4 dd = d4[g];
+            dp[4 * g] = sc[4 * g] * (dp[4 * g] - dd.x);
+            dp[4 * g + 1] = sc[4 * g + 1] * (dp[4 * g + 1] - dd.y);
+            dp[4 * g + 2] = sc[4 * g + 2] * (dp[4 * g + 2] - dd.z);
+            dp[4 * g + 3] = sc[4 * g + 3] * (dp[4 * g + 3] - dd.w);
+          }
+        } else {
+          // a query past S reads unwritten statistics: the selects keep them out
+          const int q_end = p.causal ? min(p.S, q0 + 32) : p.S;
+          const int q_first = p.causal ? k : 0;  // visible: q_first <= q < q_end
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = q0 + 4 * g + u;
-            const float pv = ex2_approx(fmaf(sc[4 * g + u], p.scale_log2, -lv[u]));
-            sc[4 * g + u] = q >= q_first && q < q_end ? pv : 0.f;
+          for (int g = 0; g < 8; ++g) {
+            const float4 l = l4[g];
+            const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int q = q0 + 4 * g + u;
+              const float pv = ex2_approx(fmaf(sc[4 * g + u], p.scale_log2, -lv[u]));
+              sc[4 * g + u] = q >= q_first && q < q_end ? pv : 0.f;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const float4 dd = d4[g];
+            const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int q = q0 + 4 * g + u;
+              dp[4 * g + u] = q >= q_first && q < q_end ? sc[4 * g + u] * (dp[4 * g + u] - dv[u]) : 0.f;
+            }
           }
         }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float4 dd = d4[g];
-          const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = q0 + 4 * g + u;
-            dp[4 * g + u] = q >= q_first && q < q_end ? sc[4 * g + u] * (dp[4 * g + u] - dv[u]) : 0.f;
-          }
+        // P^T and dS^T in bf16 over this quarter's own score columns
+        uint32_t w[16];
+        pack_pairs(sc, w);
+        tmem_st16(lane_base + static_cast<uint32_t>(32 * quarter), w);
+        pack_pairs(dp, w);
+        tmem_st16(lane_base + 128u + static_cast<uint32_t>(32 * quarter), w);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      if (ok && nq > 0) {
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_spin(pd_done, static_cast<uint32_t>(g0 + nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, w_ok, 0)) {
+          tc_fence_after_sync();
+          __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dqkv) +
+                               (static_cast<long long>(k) * p.B + b) * (3LL * p.H * kHd) +
+                               static_cast<long long>(h) * kHd + 32 * quarter;
+          float o[32];
+          tmem_ld32f_nowait(lane_base + 384u + static_cast<uint32_t>(32 * quarter), o);  // dK
+          tmem_wait_ld();
+          if (k < p.S) store_row32_scaled(row + static_cast<long long>(p.H) * kHd, o, p.scale);
+          tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(32 * quarter), o);  // dV
+          tmem_wait_ld();
+          if (k < p.S) store_row32_scaled(row + 2LL * p.H * kHd, o, 1.f);
+        } else {
+          ok = false;
         }
       }
-      // P^T and dS^T in bf16 over this quarter's own score columns
-      uint32_t w[16];
-      pack_pairs(sc, w);
-      tmem_st16(lane_base + static_cast<uint32_t>(32 * quarter), w);
-      pack_pairs(dp, w);
-      tmem_st16(lane_base + 128u + static_cast<uint32_t>(32 * quarter), w);
-      tmem_wait_st();
+      // this warp has read the item's dK and dV: the next item's first dV and dK MMAs may overwrite them
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok && nq > 0) {
-      int w_ok = 1;
-      if (lane == 0) w_ok = wait_spin(pd_done, static_cast<uint32_t>(nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, w_ok, 0)) {
-        tc_fence_after_sync();
-        __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dqkv) + (static_cast<long long>(k) * p.B + b) * (3LL * p.H * kHd) +
-                             static_cast<long long>(h) * kHd + 32 * quarter;
-        float o[32];
-        tmem_ld32f_nowait(lane_base + 384u + static_cast<uint32_t>(32 * quarter), o);  // dK
-        tmem_wait_ld();
-        if (k < p.S) store_row32_scaled(row + static_cast<long long>(p.H) * kHd, o, p.scale);
-        tmem_ld32f_nowait(lane_base + 256u + static_cast<uint32_t>(32 * quarter), o);  // dV
-        tmem_wait_ld();
-        if (k < p.S) store_row32_scaled(row + 2LL * p.H * kHd, o, 1.f);
-      }
+      if (lane == 0) mbar_arrive(dkdv_read);
+      g0 += nq;
     }
   }
   tc_fence_before_sync();
@@ -1150,13 +1265,15 @@ cudaError_t launch_attention_bwd(const void* qkv, const void* o, const void* dO,
   e = cudaFuncSetAttribute(k_attention_bwd_dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kAttnDqSmem));
   if (e != cudaSuccess) return e;
-  k_attention_bwd_dq<<<static_cast<int>(grid), kBwdThreads, kAttnDqSmem, s>>>(p);
+  // persistent: one CTA per SM, each walking its share of the (query tile, batch, head) items
+  k_attention_bwd_dq<<<static_cast<int>(grid < ctx.sm_count ? grid : ctx.sm_count), kBwdThreads, kAttnDqSmem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_attention_bwd_dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kAttnDkdvSmem));
   if (e != cudaSuccess) return e;
-  k_attention_bwd_dkdv<<<static_cast<int>(grid), kBwdThreads, kAttnDkdvSmem, s>>>(p);
+  k_attention_bwd_dkdv<<<static_cast<int>(grid < ctx.sm_count ? grid : ctx.sm_count), kBwdThreads, kAttnDkdvSmem,
+                         s>>>(p);
   return cudaGetLastError();
 }
 
