@@ -596,7 +596,8 @@ __device__ __forceinline__ void pack_pairs(const float (&v)[32], uint32_t (&w)[1
 // 32 elements sit as 16 packed columns at 32 q.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint32_t>(32 * (kk >> 1) + 8 * (kk & 1)); }
 
-// dQ for one 128-query tile of one (batch, head): per key tile j, S_j = Q K_j^T into TMEM columns 0..127 and
+// dQ, per work item (one 128-query tile of one (batch, head); persistent CTAs walk the items as the
+// forward does): per key tile j, S_j = Q K_j^T into TMEM columns 0..127 and
 // dP_j = dO V_j^T into 128..255; the 16 compute warps (four per lane quadrant = query rows, 32 keys each)
 // release S and dP as soon as they hold them in registers (so S_{j+1}, dP_{j+1} run during their math),
 // form P = exp2(S scale - lse) and dS = P (dP - D), and write dS in bf16 into one of two TMEM buffers
@@ -877,7 +878,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
   }
 }
 
-// dK and dV for one 128-key tile of one (batch, head): per query tile i, S^T_i = K Q_i^T into TMEM columns
+// dK and dV, per work item (one 128-key tile of one (batch, head); persistent CTAs walk the items, the first
+// key tiles first): per query tile i, S^T_i = K Q_i^T into TMEM columns
 // 0..127 and dP^T_i = V dO_i^T into 128..255; the 16 compute warps (four per lane quadrant = key rows, 32
 // queries each) form P^T = exp2(S^T scale - lse[q]) and dS^T = P^T (dP^T - D[q]) and write both in bf16
 // over their own score columns; dV += P^T dO_i and dK += dS^T Q_i take them from TMEM as the A operand (dO,
