@@ -149,6 +149,17 @@ __device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// The persistent CTAs' items, sorted longest first, dealt in rounds of gridDim.x.  Causal items shrink
+// along the order, so the direction is reversed every other round (CTA c takes item r G + c in even rounds r
+// and r G + G - 1 - c in odd ones) and no CTA takes the longest item of every round (measured at S = 4096 x
+// 2, 32 heads: forward 0.309 -> 0.298 ms, backward 1.185 -> 1.113 ms); items of equal length keep the
+// plain order (the reversal measured 1.7% slower on the non-causal forward).  A CTA's first index at or
+// past the item count ends its walk (every later round starts beyond it).
+__device__ __forceinline__ int item_of_round(int round, bool snake) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return round * g + ((snake && (round & 1)) ? g - 1 - c : c);
+}
+
 // Rows s0 .. s0 + 127 of one part (Q, K or V) of head h, batch b: two boxes of 64 elements.
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int h, int b, int s0) {
   tma_load_4d(dst, map, bar, 0, h, b, s0);
@@ -188,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
   const uint32_t lane = threadIdx.x & 31u;
   const int bh_count = p.B * p.H;
   const int n_items = p.n_qtiles * bh_count;
+  const bool snake = p.causal != 0;  // item order: see item_of_round
   const int n_kt_all = (p.S + kKTile - 1) / kKTile;
   // item w: query tile n_qtiles - 1 - w / (B H) (the longest causal tiles first), batch-head w % (B H)
   auto item_of = [&](int w, int& qt, int& b, int& h, int& nk) {
@@ -235,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0, q_par = 0;
       bool q_issued = false, ok = true;
       int g = 0;  // key tiles issued so far, over all items
-      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+      for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
         int qt, b, h, nk;
         item_of(w, qt, b, h, nk);
         if (it >= 1 && !wait_spin(q_empty, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnQEmpty)) break;
@@ -282,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
       const uint32_t o_tmem = tmem_base + 256;
       bool ok = true;
       int g0 = 0;
-      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+      for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
         int qt, b, h, nk;
         item_of(w, qt, b, h, nk);
         if (!wait_spin(q_full, static_cast<uint32_t>(it) & 1u, wc, kSiteAttnQ)) break;
@@ -355,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
     int g0 = 0;
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+    for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
       int qt, b, h, nk;
       item_of(w, qt, b, h, nk);
       const int q = qt * kQTile + r;  // query position
@@ -523,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attention_fwd(const __grid_cons
 // ----------------------------------------------------------------------------- attention backward
 
 constexpr int kBwdComputeWarps = 16;
-constexpr int kDqKStages = 3;                             // K ring of the dQ kernel                      // four per TMEM lane quadrant, 32 columns each
+constexpr int kDqKStages = 3;                             // K ring of the dQ kernel
 constexpr int kBwdThreads = 32 * (2 + kBwdComputeWarps);  // producer, MMA issuer, compute warps
 
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& c) {
@@ -630,6 +642,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
   const uint32_t lane = threadIdx.x & 31u;
   const int bh_count = p.B * p.H;
   const int n_items = p.n_tiles * bh_count;
+  const bool snake = p.causal != 0;  // item order: see item_of_round
   // item w: query tile n_tiles - 1 - w / (B H) (the longest causal tiles first), batch-head w % (B H)
   auto item_of = [&](int w, int& qt, int& b, int& h, int& nk) {
     qt = p.n_tiles - 1 - w / bh_count;
@@ -676,7 +689,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
       uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0, q_par = 0;
       bool q_issued = false, ok = true;
       int g = 0;  // key tiles issued so far, over all items
-      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+      for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
         int qt, b, h, nk;
         item_of(w, qt, b, h, nk);
         if (it >= 1 && !wait_spin(q_empty, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnQEmpty)) break;
@@ -687,7 +700,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
         q_par = static_cast<uint32_t>(it) & 1u;
         for (int j = 0; j < nk; ++j, ++g) {
           const int sk = g % kDqKStages, sv = g % kKvStages;
-          const uint32_t pk = static_cast<uint32_t>(g / kDqKStages) & 1u, pv = static_cast<uint32_t>(g / kKvStages) & 1u;
+          const uint32_t pk = static_cast<uint32_t>(g / kDqKStages) & 1u;
+          const uint32_t pv = static_cast<uint32_t>(g / kKvStages) & 1u;
           if (!wait_spin(k_empty + sk, pk ^ 1u, wc, kSiteAttnKvEmpty)) {
             ok = false;
             break;
@@ -720,7 +734,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
       bool ok = true;
       int g0 = 0;
       // step j of an item: S_j and dP_j (j < nk), then dQ += dS_{j-1} K_{j-1} (j >= 1); g = running tile count
-      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+      for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
         int qt, b, h, nk;
         item_of(w, qt, b, h, nk);
         if (!wait_spin(q_full, static_cast<uint32_t>(it) & 1u, wc, kSiteAttnQ)) break;
@@ -788,7 +802,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
     int g0 = 0;
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+    for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
       int qt, b, h, nk;
       item_of(w, qt, b, h, nk);
       const int q = qt * kQTile + r;
@@ -820,7 +834,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
           for (int i = 0; i < 32; ++i) sc[i] = ex2_approx(sc[i]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sc[i] = key0 + i < key_end ? ex2_approx(fmaf(sc[i], p.scale_log2, neg_lse)) : 0.f;
+          for (int i = 0; i < 32; ++i)
+            sc[i] = key0 + i < key_end ? ex2_approx(fmaf(sc[i], p.scale_log2, neg_lse)) : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) dp[i] = sc[i] * (dp[i] - dd);  // dS
@@ -910,6 +925,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
   const uint32_t lane = threadIdx.x & 31u;
   const int bh_count = p.B * p.H;
   const int n_items = p.n_tiles * bh_count;
+  const bool snake = p.causal != 0;  // item order: see item_of_round
   // item w: key tile w / (B H) (causal: the first key tiles have the most query tiles), batch-head w % (B H);
   // its query tiles i0 .. n_tiles - 1
   auto item_of = [&](int w, int& kt, int& b, int& h, int& i0, int& nq) {
@@ -951,7 +967,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
       uint32_t issued = 0, par = 0, kv_par = 0;
       bool kv_issued = false, ok = true;
       int g = 0;  // query tiles issued so far, over all items
-      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+      for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
         int kt, b, h, i0, nq;
         item_of(w, kt, b, h, i0, nq);
         if (it >= 1 && !wait_spin(kv_empty, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnQEmpty)) break;
@@ -989,7 +1005,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
       const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
       bool ok = true;
       int g0 = 0;
-      for (int w = blockIdx.x, it = 0; ok && w < n_items; w += gridDim.x, ++it) {
+      for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
         int kt, b, h, i0, nq;
         item_of(w, kt, b, h, i0, nq);
         if (!wait_spin(kv_full, static_cast<uint32_t>(it) & 1u, wc, kSiteAttnQ)) break;
@@ -1048,7 +1064,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
     int g0 = 0;
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+    for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
       int kt, b, h, i0, nq;
       item_of(w, kt, b, h, i0, nq);
       const int k = kt * kKTile + r;  // key position
