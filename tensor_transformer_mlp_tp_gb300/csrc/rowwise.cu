@@ -1163,28 +1163,34 @@ __global__ void __launch_bounds__(256) k_cast_fp8(const __nv_bfloat16* __restric
   amax_combine_warp(amax, m);
 }
 
-// Transposing cast: src [rows x cols] -> dst [cols x rows], 64 x 64 tiles through shared memory
-// (rows, cols multiples of 16).  Loads: 16-byte vectors along the source row; stores: 16 bytes of one
-// destination row (16 consecutive source rows of one column).
-constexpr int kCastTile = 64;
+// Transposing cast: src [rows x cols] -> dst [cols x rows], tiles of 128 source rows x 64 columns through
+// shared memory (rows, cols multiples of 16).  Loads: 16-byte vectors along the source row, all four of a
+// thread issued before any is used; stores: 16 bytes of one destination row (16 consecutive source rows of
+// one column), so each destination row of the tile is one 128-byte line.  Measured on GB300 against 64 x 64
+// tiles: the weight casts at d = 4096, F = 16384 54 -> 52 µs.
+constexpr int kCastTile = 64;   // columns per tile
+constexpr int kCastRows = 128;  // rows per tile
 template <int FMT>
 __global__ void __launch_bounds__(256) k_cast_fp8_t(const __nv_bfloat16* __restrict__ src, int rows, int cols,
                                                     const float* scale, uint8_t* __restrict__ dst, float* amax) {
-  __shared__ float tile[kCastTile][kCastTile + 1];
+  __shared__ float tile[kCastRows][kCastTile + 1];
   const float s = __ldg(scale);
-  const int r0 = blockIdx.y * kCastTile, c0 = blockIdx.x * kCastTile;
+  const int r0 = blockIdx.y * kCastRows, c0 = blockIdx.x * kCastTile;
   const int t = threadIdx.x;
   float m = 0.f;
+  uint4 raw[kCastRows / 32];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < kCastRows / 32; ++h) {
+    const int r = t / 8 + 32 * h, cv = (t % 8) * 8;
+    raw[h] = (r0 + r < rows && c0 + cv < cols)
+                 ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * cols + c0 + cv))
+                 : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int h = 0; h < kCastRows / 32; ++h) {
     const int r = t / 8 + 32 * h, cv = (t % 8) * 8;
     float f[8];
-    if (r0 + r < rows && c0 + cv < cols) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * cols + c0 + cv)), f);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = 0.f;
-    }
+    unpack8(raw[h], f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       m = fmaxf(m, fabsf(f[e]));
@@ -1192,17 +1198,21 @@ __global__ void __launch_bounds__(256) k_cast_fp8_t(const __nv_bfloat16* __restr
     }
   }
   __syncthreads();
-  const int oc = t / 4, rb = (t % 4) * 16;  // destination row c0 + oc, bytes [r0 + rb, r0 + rb + 16)
-  if (c0 + oc < cols && r0 + rb < rows) {
-    float f[16];
+  const int oc = t / 4;  // destination row c0 + oc, bytes [r0 + rb, r0 + rb + 16)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = tile[rb + i][oc];
-    uint4 o;
-    o.x = fp8x4<FMT>(f[0], f[1], f[2], f[3], s);
-    o.y = fp8x4<FMT>(f[4], f[5], f[6], f[7], s);
-    o.z = fp8x4<FMT>(f[8], f[9], f[10], f[11], s);
-    o.w = fp8x4<FMT>(f[12], f[13], f[14], f[15], s);
-    *reinterpret_cast<uint4*>(dst + static_cast<long long>(c0 + oc) * rows + r0 + rb) = o;
+  for (int q = 0; q < kCastRows / 64; ++q) {
+    const int rb = (t % 4) * 16 + 64 * q;
+    if (c0 + oc < cols && r0 + rb < rows) {
+      float f[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f[i] = tile[rb + i][oc];
+      uint4 o;
+      o.x = fp8x4<FMT>(f[0], f[1], f[2], f[3], s);
+      o.y = fp8x4<FMT>(f[4], f[5], f[6], f[7], s);
+      o.z = fp8x4<FMT>(f[8], f[9], f[10], f[11], s);
+      o.w = fp8x4<FMT>(f[12], f[13], f[14], f[15], s);
+      *reinterpret_cast<uint4*>(dst + static_cast<long long>(c0 + oc) * rows + r0 + rb) = o;
+    }
   }
   amax_combine_warp(amax, m);
 }
@@ -1667,7 +1677,7 @@ cudaError_t launch_cast_fp8(const void* src, int rows, int cols, bool transpose,
   const auto* in = static_cast<const __nv_bfloat16*>(src);
   auto* out = static_cast<uint8_t*>(dst);
   if (transpose) {
-    const dim3 grid((cols + kCastTile - 1) / kCastTile, (rows + kCastTile - 1) / kCastTile);
+    const dim3 grid((cols + kCastTile - 1) / kCastTile, (rows + kCastRows - 1) / kCastRows);
     if (grid.y > 65535) return cudaErrorInvalidValue;
     if (fmt == 0) {
       k_cast_fp8_t<0><<<grid, 256, 0, s>>>(in, rows, cols, scale, out, amax);
