@@ -895,11 +895,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dq(const __gri
 
 // dK and dV, per work item (one 128-key tile of one (batch, head); persistent CTAs walk the items, the first
 // key tiles first): per query tile i, S^T_i = K Q_i^T into TMEM columns
-// 0..127 and dP^T_i = V dO_i^T into 128..255; the 16 compute warps (four per lane quadrant = key rows, 32
-// queries each) form P^T = exp2(S^T scale - lse[q]) and dS^T = P^T (dP^T - D[q]) and write both in bf16
+// 0..127 and dP^T_i = V dO_i^T into 128..255, each issued as two halves of 64 queries with a barrier of
+// their own; the 16 compute warps (four per lane quadrant = key rows, 32 queries each, the first eight on
+// the lower half) form P^T = exp2(S^T scale - lse[q]) and dS^T = P^T (dP^T - D[q]) and write both in bf16
 // over their own score columns; dV += P^T dO_i and dK += dS^T Q_i take them from TMEM as the A operand (dO,
-// Q as the MN-major B), accumulating in columns 256..383 and 384..511.  The columns of S^T and dP^T take the
-// next tile's scores once both of those MMAs are done.  Causal attention visits query tiles i >= the key tile.
+// Q as the MN-major B), accumulating in columns 256..383 and 384..511, again per half.  The issue order
+// (lower-half scores of tile i, upper-half gradients of tile i - 1, upper-half scores of tile i, lower-half
+// gradients of tile i) lets one half's math run while the tensor pipe works on the other; a half's score
+// columns take new scores once the MMAs that read its P^T and dS^T are done.  Causal attention visits
+// query tiles i >= the key tile.
 __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __grid_constant__ AttnBwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -913,10 +917,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
   uint64_t* kv_empty = kv_full + 1;                // the item's last S^T and dP^T MMAs have read K and V
   uint64_t* q_full = kv_empty + 1;                 // [stage]: Q_i and dO_i
   uint64_t* q_empty = q_full + kKvStages;
-  uint64_t* s_full = q_empty + kKvStages;          // S^T_i and dP^T_i in TMEM
-  uint64_t* p_full = s_full + 1;                   // P^T_i and dS^T_i written by every compute warp
-  uint64_t* pd_done = p_full + 1;                  // dV and dK MMAs of tile i done (score columns free)
-  uint64_t* dkdv_read = pd_done + 1;               // the compute warps have read the item's dK and dV
+  uint64_t* s_half = q_empty + kKvStages;          // [half]: S^T_i and dP^T_i of one half of the queries in TMEM
+  uint64_t* p_half = s_half + 2;                   // [half]: P^T_i and dS^T_i written by the half's compute warps
+  uint64_t* pd_half = p_half + 2;                  // [half]: dV and dK MMAs of the half done (its columns free)
+  uint64_t* dkdv_read = pd_half + 2;               // the compute warps have read the item's dK and dV
   uint64_t* drain = dkdv_read + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -943,9 +947,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
       mbar_init(q_full + s, 1);
       mbar_init(q_empty + s, 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, kBwdComputeWarps);
-    mbar_init(pd_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_half + x, 1);
+      mbar_init(p_half + x, kBwdComputeWarps / 2);
+      mbar_init(pd_half + x, 1);
+    }
     mbar_init(dkdv_read, kBwdComputeWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -1000,9 +1006,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_kk = idesc_bf16_f32(kKTile, kQTile, false, false);
+      constexpr uint32_t idesc_half = idesc_bf16_f32(kKTile, kQTile / 2, false, false);  // 128 keys x 64 queries
       constexpr uint32_t idesc_mn = idesc_bf16_f32(kKTile, kHd, false, true);
       const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
+      // S^T and dP^T of half x (queries 64 x .. 64 x + 63) of the tile in stage st: the half's Q and dO rows
+      // start 64 rows (8 KB) into each atom column
+      auto issue_scores = [&](int st, int x) {
+        const uint32_t q_base = smem_u32(sQ + st * kTileBytes) + static_cast<uint32_t>(x) * 8192u;
+        const uint32_t do_base = smem_u32(sdO + st * kTileBytes) + static_cast<uint32_t>(x) * 8192u;
+#pragma unroll
+        for (int kk = 0; kk < kHd / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+          umma_bf16(tmem_base + 64u * x, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024),
+                    idesc_half, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kHd / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+          umma_bf16(tmem_base + 128u + 64u * x, sdesc_sw128(v_base + off, 16, 1024),
+                    sdesc_sw128(do_base + off, 16, 1024), idesc_half, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_half + x);
+      };
+      // dV += P^T dO and dK += dS^T Q over the queries of half x of the item's tile t (stage st); the item's
+      // first of them (t = 0, lower half) starts the accumulators
+      auto issue_grads = [&](int st, int t, int x) {
+        const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
+#pragma unroll
+        for (int j = 0; j < kQTile / 32; ++j) {
+          const int kk = 4 * x + j;
+          umma_bf16_tmem_a(tmem_base + 256, tmem_base + packed_col(kk), sdesc_sw128(do_base + kk * 2048, kAtom, 1024),
+                           idesc_mn, (t | kk) != 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kQTile / 32; ++j) {
+          const int kk = 4 * x + j;
+          umma_bf16_tmem_a(tmem_base + 384, tmem_base + 128 + packed_col(kk),
+                           sdesc_sw128(q_base + kk * 2048, kAtom, 1024), idesc_mn, (t | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit(pd_half + x);
+        if (x == 1) umma_commit(q_empty + st);  // the tile's last reads of Q and dO
+      };
       bool ok = true;
       int g0 = 0;
       for (int it = 0, w = item_of_round(0, snake); ok && w < n_items; ++it, w = item_of_round(it, snake)) {
@@ -1010,47 +1054,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
         item_of(w, kt, b, h, i0, nq);
         if (!wait_spin(kv_full, static_cast<uint32_t>(it) & 1u, wc, kSiteAttnQ)) break;
         tc_fence_after_sync();
+        // Per tile: the lower half's scores, the previous tile's upper-half gradients, this tile's upper-half
+        // scores, then its lower-half gradients, so that each half's softmax math runs while the tensor pipe
+        // works on the other half.  A half's score columns take new scores only after the MMAs that read
+        // its P^T and dS^T have completed.
         for (int t = 0; ok && t < nq; ++t) {
           const int gt = g0 + t;  // running query-tile count: stages, score columns and barrier phases
           const int st = gt % kKvStages;
+          const uint32_t prev = static_cast<uint32_t>(gt - 1) & 1u;
           if (!wait_spin(q_full + st, static_cast<uint32_t>(gt / kKvStages) & 1u, wc, kSiteAttnKv) ||
-              (gt >= 1 && !wait_spin(pd_done, static_cast<uint32_t>(gt - 1) & 1u, wc, kSiteAttnSEmpty))) {
+              (gt >= 1 && !wait_spin(pd_half, prev, wc, kSiteAttnSEmpty))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t q_base = smem_u32(sQ + st * kTileBytes), do_base = smem_u32(sdO + st * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kHd / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(q_base + off, 16, 1024), idesc_kk,
-                      kk > 0 ? 1u : 0u);
+          issue_scores(st, 0);
+          if (t >= 1) {
+            if (!wait_spin(p_half + 1, prev, wc, kSiteAttnP)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_grads((gt - 1) % kKvStages, t - 1, 1);
           }
-#pragma unroll
-          for (int kk = 0; kk < kHd / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-            umma_bf16(tmem_base + 128, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(do_base + off, 16, 1024),
-                      idesc_kk, kk > 0 ? 1u : 0u);
+          if (gt >= 1 && !wait_spin(pd_half + 1, prev, wc, kSiteAttnSEmpty)) {
+            ok = false;
+            break;
           }
-          umma_commit(s_full);
+          tc_fence_after_sync();
+          issue_scores(st, 1);
           if (t == nq - 1) umma_commit(kv_empty);  // the item's last reads of K and V
           // the item's first dV and dK MMAs overwrite them: the previous item's epilogue must have read them
           if ((t == 0 && it >= 1 && !wait_spin(dkdv_read, static_cast<uint32_t>(it - 1) & 1u, wc, kSiteAttnOEmpty)) ||
-              !wait_spin(p_full, static_cast<uint32_t>(gt) & 1u, wc, kSiteAttnP)) {
+              !wait_spin(p_half, static_cast<uint32_t>(gt) & 1u, wc, kSiteAttnP)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < kQTile / 16; ++kk)
-            umma_bf16_tmem_a(tmem_base + 256, tmem_base + packed_col(kk), sdesc_sw128(do_base + kk * 2048, kAtom, 1024),
-                             idesc_mn, (t | kk) != 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < kQTile / 16; ++kk)
-            umma_bf16_tmem_a(tmem_base + 384, tmem_base + 128 + packed_col(kk),
-                             sdesc_sw128(q_base + kk * 2048, kAtom, 1024), idesc_mn, (t | kk) != 0 ? 1u : 0u);
-          umma_commit(pd_done);
-          umma_commit(q_empty + st);
+          issue_grads(st, t, 0);
+        }
+        if (ok && nq > 0) {  // the item's last tile: its upper half's gradients
+          const int gl = g0 + nq - 1;
+          if (!wait_spin(p_half + 1, static_cast<uint32_t>(gl) & 1u, wc, kSiteAttnP)) break;
+          tc_fence_after_sync();
+          issue_grads(gl % kKvStages, nq - 1, 1);
         }
         g0 += nq;
       }
@@ -1060,6 +1107,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
   } else {
     const int quad = warp & 3;
     const int quarter = (warp - 2) >> 2;  // queries 32 quarter .. 32 quarter + 31 of every tile
+    const int half = quarter >> 1;        // the half of the tile's queries (and score barriers) it works on
     const int r = quad * 32 + static_cast<int>(lane);
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
@@ -1072,7 +1120,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
         const int gt = g0 + t;
         const int q0 = (i0 + t) * kQTile + 32 * quarter;  // this warp's first query
         int w_ok = 1;
-        if (lane == 0) w_ok = wait_spin(s_full, static_cast<uint32_t>(gt) & 1u, wc, kSiteAttnS) ? 1 : 0;
+        if (lane == 0) w_ok = wait_spin(s_half + half, static_cast<uint32_t>(gt) & 1u, wc, kSiteAttnS) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
           ok = false;
           break;
@@ -1141,11 +1189,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_attention_bwd_dkdv(const __g
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(p_half + half);
       }
       if (ok && nq > 0) {
+        // the upper half's gradients of the item's last tile are its last MMAs: their commit covers them all
         int w_ok = 1;
-        if (lane == 0) w_ok = wait_spin(pd_done, static_cast<uint32_t>(g0 + nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
+        if (lane == 0) w_ok = wait_spin(pd_half + 1, static_cast<uint32_t>(g0 + nq - 1) & 1u, wc, kSiteAttnPv) ? 1 : 0;
         if (__shfl_sync(0xffffffffu, w_ok, 0)) {
           tc_fence_after_sync();
           __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dqkv) +
