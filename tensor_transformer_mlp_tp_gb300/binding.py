@@ -202,7 +202,7 @@ def workspace(shape: Shape, op: int, device=None) -> torch.Tensor:
 
 
 def tpmlp_debug_bounds_status():
-    """(checked, violations, first_site): whether this build checks global indices, and what it found since
+    """(checked, violations, first_site): whether the loaded library checks global indices, and what it found since
     the previous call (cleared)."""
     c, n, site = ctypes.c_int32(0), ctypes.c_uint32(0), ctypes.c_uint32(0)
     _check("tpmlp_debug_bounds_status", lib().tpmlp_debug_bounds_status(ctypes.byref(c), ctypes.byref(n),
