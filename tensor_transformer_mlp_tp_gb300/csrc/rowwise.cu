@@ -692,7 +692,6 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  for (int i = threadIdx.x; i < p.d / 8; i += blockDim.x) gam[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma) + i);
   __syncthreads();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int n_rows = p.rows > static_cast<int>(blockIdx.x)
@@ -710,6 +709,11 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
   if (warp == 0) {
     if (lane == 0) stream_producer(p, ring, 2 * row_bytes, row_bytes, full, empty, n_rows, wc, true);
   } else {
+    // γ is staged by the consumer warps while the producer's first copies are in flight (measured on GB300 at
+    // T = 8192, d = 4096: 0.0472 -> 0.0459 ms); named barrier 1 + kTeams (the teams use 1 .. kTeams)
+    for (int i = threadIdx.x - 32; i < p.d / 8; i += 32 * CONS)
+      gam[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma) + i);
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + kTeams), "r"(32 * CONS) : "memory");
     const float inv_d = 1.f / static_cast<float>(p.d);
     int parity_buf = 0;
     for (int i = team; i < n_rows; i += kTeams, parity_buf ^= 1) {
@@ -872,15 +876,6 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_fwd_stream(con
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    float f[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(p.gamma) + v), f);
-    gb[v] = make_float4(f[0], f[1], f[2], f[3]);
-    gb[nv + v] = make_float4(f[4], f[5], f[6], f[7]);
-    unpack8(__ldg(reinterpret_cast<const uint4*>(p.beta) + v), f);
-    gb[2 * nv + v] = make_float4(f[0], f[1], f[2], f[3]);
-    gb[3 * nv + v] = make_float4(f[4], f[5], f[6], f[7]);
-  }
   __syncthreads();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int n_rows = p.rows > static_cast<int>(blockIdx.x)
@@ -891,6 +886,18 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_fwd_stream(con
     if (lane == 0) stream_producer(p, ring, row_bytes, row_bytes, full, empty, n_rows, wc, false);
     return;
   }
+  // γ and β are staged by the consumer warps while the producer's first copies are in flight (measured on
+  // GB300 at T = 8192, d = 4096: 0.0252 -> 0.0245 ms); named barrier 1 + kTeams (the teams use 1 .. kTeams)
+  for (int v = threadIdx.x - 32; v < nv; v += 32 * CONS) {
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(p.gamma) + v), f);
+    gb[v] = make_float4(f[0], f[1], f[2], f[3]);
+    gb[nv + v] = make_float4(f[4], f[5], f[6], f[7]);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(p.beta) + v), f);
+    gb[2 * nv + v] = make_float4(f[0], f[1], f[2], f[3]);
+    gb[3 * nv + v] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + kTeams), "r"(32 * CONS) : "memory");
   const int cw = warp - 1;        // consumer warp index
   const int team = cw / TW;
   const int tw = cw % TW;         // warp within the team
