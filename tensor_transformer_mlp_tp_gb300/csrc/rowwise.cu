@@ -693,6 +693,8 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_bwd_fused(cons
     fence_proxy_async_smem();
   }
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int n_rows = p.rows > static_cast<int>(blockIdx.x)
                          ? (p.rows - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / gridDim.x
@@ -877,6 +879,8 @@ __global__ void __launch_bounds__(32 * (CONS + 1), 1) k_layernorm_fwd_stream(con
     fence_proxy_async_smem();
   }
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   const int n_rows = p.rows > static_cast<int>(blockIdx.x)
                          ? (p.rows - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / gridDim.x
@@ -1310,8 +1314,20 @@ static cudaError_t launch_stream(K kern, const RowParams& r, size_t smem, int gr
                                  int threads = kStreamThreads) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, threads, smem, s>>>(r);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  // programmatic dependent launch: the kernel's set-up overlaps the previous kernel's tail; it waits for that
+  // kernel (griddepcontrol.wait) before its first global access (measured on GB300, T = 8192, d = 4096: the
+  // forward 0.0243 -> 0.0235 ms graph-timed, 0.0271 -> 0.0244 ms eager)
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, r);
 }
 
 // Shared-memory row slots for rows of `slot_bytes`: about 128 KB of rows in flight per SM.
