@@ -63,3 +63,27 @@ def test_traffic_lookup_follows_the_source_digest():
             assert got is None  # a kernel changed since its capture reads as unmeasured
         assert bench.measured_traffic(name, workload + "_other") is None
     assert bench.measured_traffic("no_such_segment", workload) is None
+
+
+def test_step_work_per_segment():
+    from tensor_transformer_mlp_tp_gb300 import inputs
+    w = inputs.WORKLOADS["sp_block_fwd_bwd"]  # T = 8192, d = 4096, F = 16384, N = 8
+    segs = {name: (n, work, unit) for name, n, work, unit in bench.Step.kernels_of(w)}
+    gemm = 2.0 * 8192 * 4096 * 16384  # 1.1 TFLOP
+    assert [s for s in segs if s.startswith("gemm")] == [
+        "gemm1_bias_gelu", "gemm2_shard_accum_rs_store", "gemm_dh_geluprime", "gemm_wgrad_b", "gemm_wgrad_a",
+        "gemm_dx_shard_accum"]
+    assert all(segs[s] == (1, gemm, "F") for s in segs if s.startswith("gemm"))
+    assert segs["layernorm_gather"] == (1, 4.0 * 8192 * 4096, "B")      # read x, write the gathered row (bf16)
+    assert segs["layernorm_backward"] == (2, 6.0 * 8192 * 4096, "B")    # read x, dy, write dx; two launches
+    assert bench.useful_flops(w) == 6 * gemm
+
+
+def test_forward_workloads_count_two_gemms():
+    from tensor_transformer_mlp_tp_gb300 import inputs
+    for name in ("gpt2_medium_fwd", "mlp7b_fwd", "sp_large_fwd"):
+        w = inputs.WORKLOADS[name]
+        names = [s[0] for s in bench.Step.kernels_of(w)]
+        assert sum(n.startswith("gemm") for n in names) == 2
+        assert ("layernorm_gather" in names) == w.sp
+        assert bench.useful_flops(w) == 2 * 2.0 * w.T * w.d * w.F
